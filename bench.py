@@ -1,0 +1,481 @@
+#!/usr/bin/env python3
+"""Benchmark of libkda on one GB300 (or N replicas, one per GPU).
+
+One step = one ``kda_chunk_fwd`` over the single-head-group prefill workload
+(B=1, H=16, T=4096, d_k=d_v=128, chunk 64, bf16 q/k/v, fp32 gates and state,
+seeded synthetic inputs), i.e. every prefill stage of the hot path.  The
+decode row (``kda_recurrent_step``, 256 sequences x 32 heads, 512 MiB fp32
+state, 64 steps) is measured in the same run and reported under "decode".
+
+Timing: CUDA events on the launch stream, W untimed warm-up steps, K timed
+steps with an L2 flush (256 MiB write) before each timed step (the prefill
+inputs, ~100 MB, would otherwise stay in the 129 MB L2), barrier and
+synchronize on both sides, max over ranks.  libkda itself records events
+between its kernels (kda_chunk_fwd_ws_timed), which gives the per-kernel
+device times behind the roofline figures.
+
+``--impl reference`` times the fp64 CPU oracle (the reference arm of this
+repository) on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s & % bf16 tensor peak; decode state GB/s % of HBM peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--engine", choices=["auto", "tensor", "simt"], default="auto")
+    ap.add_argument("--decode-steps", type=int, default=64)
+    ap.add_argument("--skip-decode", action="store_true")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained",
+                                                     p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; no data-path collective)
+# ---------------------------------------------------------------------------
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local_rank)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if self.pg is None:
+            return x
+        import torch
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int = 0):
+        self.proc = None
+        self.dev = device_index
+        self.out_path = None
+
+    def start(self):
+        import tempfile
+        try:
+            fd, self.out_path = tempfile.mkstemp(prefix="kda_clocks_", suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "200"]
+            uuid = self._uuid()
+            if uuid:
+                cmd += ["-i", uuid]
+            self.fh = open(self.out_path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def _uuid(self):
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(self.dev).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            return None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.out_path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.out_path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work per (token, head): the figures behind the roofline
+# ---------------------------------------------------------------------------
+
+def prefill_flops_per_tok_head(d: int, C: int) -> int:
+    """Dense chunk contractions: K K^T, Q K^T, A^kk (beta V), A^kk (beta Gamma K),
+    A^qk E (5 x 2Cd) plus W S, K_end^T E, Q_hat S (3 x 2d^2)."""
+    return 10 * C * d + 6 * d * d
+
+
+def stage_work(d: int, C: int):
+    """Per (token, head) compulsory bytes and dense flops of each kernel of the
+    tensor-core engine (its own inputs read once, outputs written once)."""
+    prep_bytes = (2 * 2 * d          # q, k (bf16)
+                  + 4 * d + 4        # log_alpha, beta (fp32)
+                  + 3 * 2 * d        # -W, Q_hat, K_end^T (bf16)
+                  + 2 * 2 * C        # A^kk, A^qk rows (bf16)
+                  + 4 * d / C + 4)   # Gamma_last per chunk, beta copy (fp32)
+    scan_bytes = (3 * 2 * d + 2 * 2 * C + 4 * d / C + 4   # the prep products
+                  + 2 * d                                  # v (bf16)
+                  + 2 * d)                                 # out (bf16)
+    prep_flops = 3 * 2 * C * d        # [K;Q] K^T (two C x C x d) and W
+    scan_flops = 2 * 2 * C * d + 3 * 2 * d * d
+    return {"prep": (prep_bytes, prep_flops), "scan": (scan_bytes, scan_flops)}
+
+
+def path_bytes_per_tok_head(d: int) -> int:
+    """Whole-path minimum: q, k, v, out (bf16) and log_alpha (fp32) once, beta."""
+    return 4 * 2 * d + 4 * d + 4
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 oracle on host cores
+# ---------------------------------------------------------------------------
+
+def oracle_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, dist: Dist):
+    if dist.rank != 0:
+        return
+    import oracle
+    from kimi_delta_attention_chunkwise_gb300 import inputs
+    w = inputs.head_group_prefill()
+    Ts = 512  # bounded sample: the first 512 tokens of the workload, all 16 heads
+    sl = slice(0, Ts)
+    arrs = [w.q[sl], w.k[sl], w.v[sl], w.log_alpha[sl], w.beta[sl]]
+    oracle.build()
+    thr = oracle_threads()
+    for _ in range(args.warmup):
+        oracle.recurrent(*arrs, w.scale, None, [0, Ts], threads=thr)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.recurrent(*arrs, w.scale, None, [0, Ts], threads=thr)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = Ts * args.steps / total
+    sample = (f"first {Ts} of {w.T} tokens x {w.H} heads of the prefill workload per step, "
+              f"fp64 token recurrence")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name + " (B=1, chunk 64, seed 1)", "sample_tokens": Ts},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(w):
+    """The oracle as it stands on the whole prefill workload, repeated to at
+    least ~5 s of wall time (bounded: at most 4 runs)."""
+    import oracle
+    oracle.build()
+    thr = oracle_threads()
+    runs, t_total = 0, 0.0
+    while runs < 4 and (t_total < 5.0 or runs == 0):
+        t0 = time.perf_counter()
+        oracle.recurrent(w.q, w.k, w.v, w.log_alpha, w.beta, w.scale, None, w.cu_seqlens,
+                         threads=thr)
+        t_total += time.perf_counter() - t0
+        runs += 1
+    return {"value": w.T * runs / t_total, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+            "sample": f"the whole workload ({w.T} tokens x {w.H} heads) x {runs} run(s), "
+                      f"fp64 token recurrence, {t_total:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, dist: Dist):
+    import numpy as np
+    import torch
+    import kimi_delta_attention_chunkwise_gb300 as kda
+    from kimi_delta_attention_chunkwise_gb300 import build, inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(dist.local_rank)
+    build.build()
+    peaks = load_peaks()
+    dev = torch.device("cuda", dist.local_rank)
+    stream = torch.cuda.current_stream()
+
+    # ---------------- prefill workload ----------------
+    w = inputs.head_group_prefill()
+    T, H, d, C = w.T, w.H, w.d_k, w.chunk_size
+    q = torch.from_numpy(w.q).to(dev, torch.bfloat16)
+    k = torch.from_numpy(w.k).to(dev, torch.bfloat16)
+    v = torch.from_numpy(w.v).to(dev, torch.bfloat16)
+    la = torch.from_numpy(w.log_alpha).to(dev)
+    beta = torch.from_numpy(w.beta).to(dev)
+    cu = torch.from_numpy(w.cu_seqlens).to(dev)
+    out = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+    fin = torch.empty((1, H, d, d), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def new_events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record(stream)  # creates the underlying CUDA event
+        return evs
+
+    MAXEV = 8
+    warm_evs = new_events(MAXEV)
+    n_rec = 0
+    for _ in range(args.warmup):
+        _, _, n_rec = kda.kda_chunk_fwd_ws_timed(q, k, v, la, beta, w.scale, None, cu, out, fin,
+                                                 warm_evs, engine=args.engine)
+    torch.cuda.synchronize()
+    n_stages = max(1, n_rec - 1)
+    step_evs = [new_events(MAXEV) for _ in range(args.steps)]
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(dist.local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        kda.kda_chunk_fwd_ws_timed(q, k, v, la, beta, w.scale, None, cu, out, fin, step_evs[i],
+                                   engine=args.engine)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clocks = sampler.stop()
+
+    step_ms = [starts[i].elapsed_time(ends[i]) for i in range(args.steps)]
+    stage_ms = [[step_evs[i][s].elapsed_time(step_evs[i][s + 1]) for s in range(n_stages)]
+                for i in range(args.steps)]
+    total_ms = dist.max(sum(step_ms))
+    ms_per_step = total_ms / args.steps
+    tokens = T * args.steps * dist.world
+    value = tokens / (total_ms / 1e3)
+    flops_step = prefill_flops_per_tok_head(d, C) * T * H
+    tflops = flops_step * args.steps * dist.world / (total_ms / 1e3) / 1e12
+
+    stage_avg = [statistics.mean(s[j] for s in stage_ms) for j in range(n_stages)]
+    if n_stages == 3:
+        names = ["chunk_table", "prep", "scan"]
+    else:
+        names = [f"stage{j}" for j in range(n_stages)]
+        names[-1] = "chunk_simt" if n_stages == 1 else names[-1]
+    dom = max(range(n_stages), key=lambda j: stage_avg[j])
+    work = stage_work(d, C)
+    if names[dom] in work:
+        bpt, fpt = work[names[dom]]
+    else:
+        bpt, fpt = path_bytes_per_tok_head(d), prefill_flops_per_tok_head(d, C)
+    dom_s = stage_avg[dom] / 1e3
+    achieved_gbs = bpt * T * H / dom_s / 1e9
+    roofline = {"kernel": names[dom], "bound": "hbm", "achieved": achieved_gbs,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": None,
+                "peak_source": peaks["source"],
+                "bytes_per_launch": bpt * T * H, "launch_ms": stage_avg[dom],
+                "tensor_tflops": fpt * T * H / dom_s / 1e12,
+                "tensor_frac": fpt * T * H / dom_s / 1e12 / peaks["bf16_tflops"]}
+
+    # ---------------- end to end through the public API, host buffers ----------------
+    pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    hq, hk, hv = (pin(a).to(torch.bfloat16).pin_memory() for a in (w.q, w.k, w.v))
+    hla, hb, hcu = pin(w.log_alpha), pin(w.beta), pin(w.cu_seqlens)
+    hout = torch.empty((T, H, d), dtype=torch.bfloat16).pin_memory()
+    hfin = torch.empty((1, H, d, d), dtype=torch.float32).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hla, hb, hcu))
+    d2h = hout.numel() * 2 + hfin.numel() * 4
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True); k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True); la.copy_(hla, non_blocking=True)
+        beta.copy_(hb, non_blocking=True); cu.copy_(hcu, non_blocking=True)
+        kda.kda_chunk_fwd(q, k, v, la, beta, w.scale, None, cu, out, fin, engine=args.engine)
+        hout.copy_(out, non_blocking=True); hfin.copy_(fin, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        e_start[i].record(stream)
+        e2e_step()
+        e_end[i].record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    e2e_ms = dist.max(sum(e_start[i].elapsed_time(e_end[i]) for i in range(args.steps)))
+    e2e = {"value": T * args.steps * dist.world / (e2e_ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "ms_per_step": e2e_ms / args.steps}
+
+    # ---------------- decode row ----------------
+    decode = None
+    if not args.skip_decode:
+        decode = run_decode(args, dist, peaks, dev, stream)
+
+    del flush
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{w.name}: B=1, H={H}, T={T}, d_k=d_v={d}, chunk {C}, "
+                               "bf16 q/k/v, fp32 gates/state, zero initial state, seed 1",
+                   "engine": args.engine, "l2": "flushed (256 MiB write) before each timed step",
+                   "parallelism": "replicas" if dist.world > 1 else "single GPU"},
+        "tflops": tflops, "tensor_frac_of_bf16_peak": tflops / peaks["bf16_tflops"],
+        "path_gbs": path_bytes_per_tok_head(d) * T * H * args.steps * dist.world
+                    / (total_ms / 1e3) / 1e9,
+        "stages_ms": dict(zip(names, stage_avg)),
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": n_stages * args.steps,
+        "clocks": clocks,
+        "decode": decode,
+    }
+    if not args.skip_cpu_baseline and dist.rank == 0 and dist.world == 1:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_decode(args, dist, peaks, dev, stream):
+    import torch
+    import kimi_delta_attention_chunkwise_gb300 as kda
+    from kimi_delta_attention_chunkwise_gb300 import inputs
+    S = args.decode_steps
+    dw = inputs.batched_decode(steps=S)
+    N, H, d = dw.q.shape[1], dw.q.shape[2], dw.q.shape[3]
+    q = torch.from_numpy(dw.q).to(dev, torch.bfloat16)
+    k = torch.from_numpy(dw.k).to(dev, torch.bfloat16)
+    v = torch.from_numpy(dw.v).to(dev, torch.bfloat16)
+    la = torch.from_numpy(dw.log_alpha).to(dev)
+    b = torch.from_numpy(dw.beta).to(dev)
+    state = torch.from_numpy(dw.initial_state).to(dev)
+    out = torch.empty((N, H, d), dtype=torch.bfloat16, device=dev)
+    for t in range(min(args.warmup, S)):
+        kda.kda_recurrent_step(q[t], k[t], v[t], la[t], b[t], dw.scale, state, out)
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(S + 1)]
+    dist.barrier()
+    torch.cuda.synchronize()
+    evs[0].record(stream)
+    for t in range(S):
+        kda.kda_recurrent_step(q[t], k[t], v[t], la[t], b[t], dw.scale, state, out)
+        evs[t + 1].record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    per = [evs[t].elapsed_time(evs[t + 1]) for t in range(S)]
+    total_ms = dist.max(sum(per))
+    bytes_step = (2 * d * d * 4 + 3 * 2 * d + 2 * d + 4 * d + 4) * N * H
+    gbs = bytes_step * S * dist.world / (total_ms / 1e3) / 1e9
+    return {"workload": f"{N} sequences x {H} heads, d={d}, fp32 state "
+                        f"{N * H * d * d * 4 / 2**20:.0f} MiB, {S} steps (state > L2)",
+            "value": gbs, "unit": "GB/s", "us_per_step": 1e3 * total_ms / S,
+            "median_us_per_step": 1e3 * statistics.median(per),
+            "gpu_launches": S,
+            "roofline": {"kernel": "recurrent_step", "bound": "hbm", "achieved": gbs,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                         "bytes_per_launch": bytes_step, "peak_source": peaks["source"]}}
+
+
+def main():
+    args = parse_args()
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            run_reference(args, dist)
+        else:
+            run_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

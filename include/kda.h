@@ -1,0 +1,193 @@
+/*
+ * kda.h -- C ABI of libkda, a GB300 (sm_103a) implementation of the
+ * Kimi Delta Attention (KDA) token mixer.
+ *
+ * What the library computes (per sequence n and head h, tokens in order):
+ *
+ *     S_bar_t = Diag(alpha_t) S_{t-1}                 forget each key channel
+ *     e_t     = beta_t (v_t - S_bar_t^T k_t)          correct the prediction
+ *     S_t     = S_bar_t + k_t e_t^T                   rank-one delta write
+ *     o_t     = S_t^T (scale * q_t)                   read after the write
+ *
+ * with S a d_k x d_v fp32 matrix (row i = key channel i) and
+ * alpha_t = exp(log_alpha_t).  Sources: "Kimi Unveils Delta Attention and K3
+ * Architecture Updates", sec. 4 (KDA) and sec. 4.1 (the d_k x d_v five-line
+ * form); "Kimi Delta Attention: Channel-Wise Memory Control", "Change one
+ * piece of Gated DeltaNet" (key-by-value orientation, o_t = S_t^T q_t).
+ *
+ * Memory contract shared by every entry point:
+ *   - All tensor arguments are DEVICE pointers, contiguous, row-major, in the
+ *     layouts given below, and 16-byte aligned.  The caller owns every buffer.
+ *   - Calls are asynchronous with respect to the host; all work is enqueued
+ *     on `stream` (0 = the legacy default stream).
+ *   - Host-detectable errors are returned before anything is launched, and
+ *     then no output is written.  A launch failure returns KDA_ERR_CUDA.
+ *   - Outputs must not overlap inputs, except where stated.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_SUCCESS = 0,
+    KDA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size or flag   */
+    KDA_ERR_UNSUPPORTED = 2,   /* valid request outside the support matrix     */
+    KDA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed         */
+    KDA_ERR_TIMEOUT = 4        /* a bounded device-side wait gave up           */
+} kdaStatus_t;
+
+typedef enum {
+    KDA_DTYPE_BF16 = 0,        /* q, k, v and out are bfloat16 */
+    KDA_DTYPE_F32 = 1          /* q, k, v and out are float32  */
+} kdaDtype_t;
+
+typedef enum {
+    KDA_ENGINE_AUTO = 0,       /* tensor-core engine where supported, else SIMT */
+    KDA_ENGINE_TENSOR = 1,     /* tcgen05/TMEM chunk engine (bf16, d = 128, C = 64) */
+    KDA_ENGINE_SIMT = 2        /* fp32 CUDA-core chunk engine (any supported shape) */
+} kdaEngine_t;
+
+/* Problem description.  All fields are plain int32 so the struct has the
+   same layout from C, C++ and ctypes. */
+typedef struct {
+    int32_t num_seqs;      /* N >= 1: packed sequences (chunk_fwd) / batch (step) */
+    int32_t total_tokens;  /* T >= 0: packed tokens (chunk_fwd); must equal N (step) */
+    int32_t num_heads;     /* H >= 1 */
+    int32_t d_k;           /* key width; d_k == d_v in {16, 32, 64, 128} */
+    int32_t d_v;           /* value width */
+    int32_t dtype;         /* kdaDtype_t of q, k, v, out */
+    int32_t chunk_size;    /* chunk_fwd: 0 = default (64 for d >= 64, else 16),
+                              or 16 / 32 / 64; ignored by the step */
+    int32_t engine;        /* chunk_fwd: kdaEngine_t; ignored by the step */
+    int32_t out_f32;       /* 0: out has the dtype of q; 1: out is float32
+                              (bf16 inputs, fp32 results: no output rounding) */
+} kdaShape_t;
+
+/*
+ * kda_chunk_fwd -- chunkwise prefill over packed variable-length sequences.
+ *
+ * Defines: the recurrence above, evaluated chunk by chunk as in "Kimi Unveils
+ * Delta Attention and K3 Architecture Updates", sec. 6 (chunk-local cumulative
+ * log decay, the causal key-key system and its triangular solve, the WY form
+ * of the corrected writes, the single inter-chunk state scan, and the causal
+ * outputs).  Chunks restart at every sequence start ("Linear Attention, From
+ * Scratch to Kimi 3", sec. 9, cu_seqlens); the last chunk of a sequence may be
+ * shorter.  Results do not depend on the chunk size beyond rounding.
+ *
+ *   q, k          [T, H, d_k]  dtype        (q and k are used as given; the
+ *                                            caller normalises them)
+ *   v             [T, H, d_v]  dtype
+ *   log_alpha     [T, H, d_k]  float32      finite and <= 0 (log retention)
+ *   beta          [T, H]       float32      finite write strength
+ *   scale                      host float   applied to q (pass d_k^-1/2 for
+ *                                            the usual 1/sqrt(d_k) read)
+ *   initial_state [N, H, d_k, d_v] float32  or NULL for zero states
+ *   cu_seqlens    [N + 1]      int32        device; cu[0] = 0, non-decreasing,
+ *                                            cu[N] = T.  NULL means one
+ *                                            sequence (then N must be 1).
+ *   out           [T, H, d_v]  dtype (float32 if shape->out_f32)
+ *                                            written for every token
+ *   final_state   [N, H, d_k, d_v] float32  or NULL (not written).  May be
+ *                                            the same buffer as initial_state
+ *                                            (in-place resume).
+ *
+ * cu_seqlens contents are not validated on the host (they live on the
+ * device); the kernels clamp every sequence to [0, T], so out-of-range
+ * offsets give wrong results but never an out-of-bounds access.
+ * Scratch: up to kda_chunk_fwd_workspace_size() bytes, taken with
+ * cudaMallocAsync/cudaFreeAsync on `stream` (stream-ordered, pooled by the
+ * driver).  Use kda_chunk_fwd_ws to pass caller-owned scratch instead.
+ */
+kdaStatus_t kda_chunk_fwd(const void *q, const void *k, const void *v,
+                          const float *log_alpha, const float *beta, float scale,
+                          const float *initial_state, const int32_t *cu_seqlens,
+                          void *out, float *final_state, const kdaShape_t *shape,
+                          cudaStream_t stream);
+
+/*
+ * kda_chunk_fwd_workspace_size -- bytes of device scratch kda_chunk_fwd_ws
+ * needs for `shape` (0 for the SIMT engine).  *bytes is written on success.
+ */
+kdaStatus_t kda_chunk_fwd_workspace_size(const kdaShape_t *shape, size_t *bytes);
+
+/*
+ * kda_chunk_fwd_ws -- kda_chunk_fwd with caller-owned scratch: `workspace` is
+ * a device buffer of at least kda_chunk_fwd_workspace_size() bytes, 256-byte
+ * aligned, not used by anything else until the work on `stream` is done.
+ * Allocates nothing.
+ */
+kdaStatus_t kda_chunk_fwd_ws(const void *q, const void *k, const void *v,
+                             const float *log_alpha, const float *beta, float scale,
+                             const float *initial_state, const int32_t *cu_seqlens,
+                             void *out, float *final_state, const kdaShape_t *shape,
+                             void *workspace, size_t workspace_bytes,
+                             cudaStream_t stream);
+
+/*
+ * kda_chunk_fwd_ws_timed -- kda_chunk_fwd_ws that also records CUDA events
+ * on `stream` around its kernels, for measuring each stage on the device:
+ * events[0] just before the first launch and events[i] right after launch i,
+ * while i < max_events.  *n_recorded (if not NULL) receives the number of
+ * events recorded, i.e. launches + 1; stage i spans events[i] -> events[i+1].
+ * The events must have been created by the caller (cudaEventCreate or an
+ * already-recorded framework event).  Stage order: tensor-core engine =
+ * chunk table, intra-chunk prep, state scan + output; SIMT engine = one
+ * fused kernel.
+ */
+kdaStatus_t kda_chunk_fwd_ws_timed(const void *q, const void *k, const void *v,
+                                   const float *log_alpha, const float *beta, float scale,
+                                   const float *initial_state, const int32_t *cu_seqlens,
+                                   void *out, float *final_state, const kdaShape_t *shape,
+                                   void *workspace, size_t workspace_bytes,
+                                   cudaStream_t stream, cudaEvent_t *events,
+                                   int32_t max_events, int32_t *n_recorded);
+
+/*
+ * kda_recurrent_step -- one decode token for each of N independent sequences.
+ *
+ * Defines: one step of the recurrence above ("Kimi Unveils Delta Attention
+ * and K3 Architecture Updates", sec. 4.1 five-line form and sec. 5, the fused
+ * recurrent schedule for decode; "Kimi Delta Attention: Channel-Wise Memory
+ * Control", "The core update in a few lines").  The state streams through
+ * once: it is read, decayed, corrected and written back in place.
+ *
+ *   q, k       [N, H, d_k]  dtype
+ *   v          [N, H, d_v]  dtype
+ *   log_alpha  [N, H, d_k]  float32, finite and <= 0
+ *   beta       [N, H]       float32
+ *   scale                   host float applied to q
+ *   state      [N, H, d_k, d_v] float32, read and updated in place
+ *   out        [N, H, d_v]  dtype (float32 if shape->out_f32)
+ *
+ * shape->total_tokens must equal shape->num_seqs (one token per sequence);
+ * chunk_size and engine are ignored.  Allocates nothing.
+ */
+kdaStatus_t kda_recurrent_step(const void *q, const void *k, const void *v,
+                               const float *log_alpha, const float *beta, float scale,
+                               float *state, void *out, const kdaShape_t *shape,
+                               cudaStream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *kda_status_string(kdaStatus_t status);
+
+/*
+ * kda_device_status -- synchronises `stream`, then reads and clears the
+ * library's device-side status word on the current device: KDA_SUCCESS, or
+ * KDA_ERR_TIMEOUT if a bounded wait inside a kernel gave up since the last
+ * call (that kernel's outputs are then invalid).  Returns KDA_ERR_CUDA if the
+ * synchronisation itself fails.
+ */
+kdaStatus_t kda_device_status(cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

@@ -1,0 +1,331 @@
+"""Thin Python binding of libkda's C ABI (include/kda.h).
+
+Argument marshalling only: every step of the computation runs in libkda's
+CUDA kernels.  Torch supplies device memory and streams.  The shared library
+is built in-tree (``build.build()``); if it is missing this module raises --
+there is no CPU or PyTorch fallback.
+
+The functions carry the C names:
+
+* ``kda_chunk_fwd``      -- chunkwise prefill over packed sequences;
+* ``kda_recurrent_step`` -- one decode token per sequence, state in place;
+* ``kda_chunk_fwd_workspace_size`` / ``kda_chunk_fwd_ws`` -- caller-owned scratch;
+* ``kda_status_string``, ``kda_device_status``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional, Tuple
+
+from . import build as _build
+
+KDA_SUCCESS = 0
+KDA_ERR_INVALID_ARG = 1
+KDA_ERR_UNSUPPORTED = 2
+KDA_ERR_CUDA = 3
+KDA_ERR_TIMEOUT = 4
+
+KDA_DTYPE_BF16 = 0
+KDA_DTYPE_F32 = 1
+
+KDA_ENGINE_AUTO = 0
+KDA_ENGINE_TENSOR = 1
+KDA_ENGINE_SIMT = 2
+_ENGINES = {"auto": KDA_ENGINE_AUTO, "tensor": KDA_ENGINE_TENSOR, "simt": KDA_ENGINE_SIMT}
+
+
+class kdaShape_t(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
+                ("num_heads", ctypes.c_int32), ("d_k", ctypes.c_int32),
+                ("d_v", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("chunk_size", ctypes.c_int32), ("engine", ctypes.c_int32),
+                ("out_f32", ctypes.c_int32)]
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {kda_status_string(status)}")
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libkda.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _build.LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"libkda.so not found at {p}; build it with "
+            "kimi_delta_attention_chunkwise_gb300.build.build()")
+    lib = ctypes.CDLL(p)
+    vp, fp, ip = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+    shp = ctypes.POINTER(kdaShape_t)
+    lib.kda_chunk_fwd.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, fp, ip, vp, fp, shp, vp]
+    lib.kda_chunk_fwd.restype = ctypes.c_int
+    lib.kda_chunk_fwd_ws.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, fp, ip, vp, fp, shp,
+                                     vp, ctypes.c_size_t, vp]
+    lib.kda_chunk_fwd_ws.restype = ctypes.c_int
+    lib.kda_chunk_fwd_ws_timed.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, fp, ip, vp, fp,
+                                           shp, vp, ctypes.c_size_t, vp,
+                                           ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32,
+                                           ctypes.POINTER(ctypes.c_int32)]
+    lib.kda_chunk_fwd_ws_timed.restype = ctypes.c_int
+    lib.kda_chunk_fwd_workspace_size.argtypes = [shp, ctypes.POINTER(ctypes.c_size_t)]
+    lib.kda_chunk_fwd_workspace_size.restype = ctypes.c_int
+    lib.kda_recurrent_step.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, fp, vp, shp, vp]
+    lib.kda_recurrent_step.restype = ctypes.c_int
+    lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_device_status.argtypes = [vp]
+    lib.kda_device_status.restype = ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def header_functions() -> list:
+    """Names of every function include/kda.h declares."""
+    hdr = os.path.join(_build.INCLUDE, "kda.h")
+    with open(hdr) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_\w+)\s*\(", text)))
+
+
+def kda_status_string(status: int) -> str:
+    return load().kda_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != KDA_SUCCESS:
+        raise KdaError(status, where)
+
+
+# ---------------------------------------------------------------------------
+# torch marshalling
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return KDA_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return KDA_DTYPE_F32
+    raise TypeError(f"q/k/v must be bfloat16 or float32, got {t.dtype}")
+
+
+def _require(t, name, dtype=None, shape=None):
+    torch = _torch()
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def make_shape(N, T, H, dk, dv, dtype_code, chunk_size=0, engine=KDA_ENGINE_AUTO,
+               out_f32=0) -> kdaShape_t:
+    return kdaShape_t(int(N), int(T), int(H), int(dk), int(dv), int(dtype_code),
+                      int(chunk_size), int(engine), int(out_f32))
+
+
+def _out_dtype(q, out, out_f32):
+    torch = _torch()
+    if out is not None:
+        return out.dtype
+    return torch.float32 if out_f32 else q.dtype
+
+
+_ws_cache = {}
+
+
+def kda_chunk_fwd_workspace_size(shape: kdaShape_t) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().kda_chunk_fwd_workspace_size(ctypes.byref(shape), ctypes.byref(n)),
+           "kda_chunk_fwd_workspace_size")
+    return int(n.value)
+
+
+def _workspace(nbytes: int, device):
+    torch = _torch()
+    if nbytes == 0:
+        return None
+    key = (device.index if device.index is not None else torch.cuda.current_device())
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+def _prefill_args(q, k, v, log_alpha, beta, initial_state, cu_seqlens, out, final_state,
+                  chunk_size, engine, out_f32=False):
+    torch = _torch()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, name)
+    if q.dim() != 3:
+        raise ValueError("q must be [T, H, d_k]")
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    _require(k, "k", q.dtype, (T, H, dk))
+    _require(v, "v", q.dtype, (T, H, dv))
+    _require(log_alpha, "log_alpha", torch.float32, (T, H, dk))
+    _require(beta, "beta", torch.float32, (T, H))
+    if cu_seqlens is not None:
+        _require(cu_seqlens, "cu_seqlens", torch.int32)
+        N = cu_seqlens.numel() - 1
+    else:
+        N = 1
+    _require(initial_state, "initial_state", torch.float32, (N, H, dk, dv))
+    odt = _out_dtype(q, out, out_f32)
+    if odt not in (q.dtype, torch.float32):
+        raise TypeError("out must have the dtype of q, or float32")
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=odt, device=q.device)
+    _require(out, "out", odt, (T, H, dv))
+    _require(final_state, "final_state", torch.float32, (N, H, dk, dv))
+    eng = _ENGINES[engine] if isinstance(engine, str) else int(engine)
+    shape = make_shape(N, T, H, dk, dv, _dtype_code(q), chunk_size, eng,
+                       int(odt == torch.float32 and q.dtype != torch.float32))
+    return shape, out
+
+
+def kda_chunk_fwd(q, k, v, log_alpha, beta, scale: float, initial_state=None,
+                  cu_seqlens=None, out=None, final_state=None, *, chunk_size: int = 0,
+                  engine="auto", stream=None, use_library_scratch: bool = False,
+                  out_f32: bool = False) -> Tuple[object, object]:
+    """Chunkwise KDA prefill (C: kda_chunk_fwd).  Returns ``(out, final_state)``.
+
+    q, k: [T, H, d_k] bf16/fp32; v: [T, H, d_v]; log_alpha: [T, H, d_k] fp32;
+    beta: [T, H] fp32; initial_state / final_state: [N, H, d_k, d_v] fp32;
+    cu_seqlens: int32 [N + 1] on the device.  ``final_state`` may be the same
+    tensor as ``initial_state``.  Scratch comes from torch (kda_chunk_fwd_ws)
+    unless ``use_library_scratch`` asks libkda to take it with cudaMallocAsync.
+    ``out_f32`` (or a float32 ``out``) returns fp32 results for bf16 inputs.
+    """
+    shape, out = _prefill_args(q, k, v, log_alpha, beta, initial_state, cu_seqlens, out,
+                               final_state, chunk_size, engine, out_f32)
+    lib = load()
+    s = _stream_handle(stream)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), float(scale),
+            _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+            ctypes.byref(shape))
+    if use_library_scratch:
+        _check(lib.kda_chunk_fwd(*args, s), "kda_chunk_fwd")
+    else:
+        nbytes = kda_chunk_fwd_workspace_size(shape)
+        ws = _workspace(nbytes, q.device)
+        wp = None
+        if ws is not None:
+            wp = (ws.data_ptr() + 255) // 256 * 256
+        _check(lib.kda_chunk_fwd_ws(*args, wp, nbytes, s), "kda_chunk_fwd_ws")
+    return out, final_state
+
+
+def kda_chunk_fwd_ws_timed(q, k, v, log_alpha, beta, scale: float, initial_state, cu_seqlens,
+                           out, final_state, events, *, chunk_size: int = 0, engine="auto",
+                           stream=None, out_f32: bool = False):
+    """kda_chunk_fwd with library-owned stage events: ``events`` is a list of
+    already-recorded ``torch.cuda.Event(enable_timing=True)``; libkda records
+    events[0] before its first kernel and events[i] after kernel i on the
+    launch stream.  Returns ``(out, final_state, n_recorded)``."""
+    shape, out = _prefill_args(q, k, v, log_alpha, beta, initial_state, cu_seqlens, out,
+                               final_state, chunk_size, engine, out_f32)
+    nbytes = kda_chunk_fwd_workspace_size(shape)
+    ws = _workspace(nbytes, q.device)
+    wp = None if ws is None else (ws.data_ptr() + 255) // 256 * 256
+    handles = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    n = ctypes.c_int32(0)
+    _check(load().kda_chunk_fwd_ws_timed(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), float(scale),
+        _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+        ctypes.byref(shape), wp, nbytes, _stream_handle(stream), handles, len(events),
+        ctypes.byref(n)), "kda_chunk_fwd_ws_timed")
+    return out, final_state, int(n.value)
+
+
+def kda_chunk_fwd_ws(q, k, v, log_alpha, beta, scale: float, initial_state, cu_seqlens,
+                     out, final_state, workspace, *, chunk_size: int = 0, engine="auto",
+                     stream=None):
+    """kda_chunk_fwd with an explicit workspace tensor (uint8, >= the size query)."""
+    shape, out = _prefill_args(q, k, v, log_alpha, beta, initial_state, cu_seqlens, out,
+                               final_state, chunk_size, engine)
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().kda_chunk_fwd_ws(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), float(scale),
+        _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+        ctypes.byref(shape), _ptr(workspace), nbytes, _stream_handle(stream)),
+        "kda_chunk_fwd_ws")
+    return out, final_state
+
+
+def kda_recurrent_step(q, k, v, log_alpha, beta, scale: float, state, out=None, *,
+                       stream=None, out_f32: bool = False):
+    """One KDA decode step (C: kda_recurrent_step).  ``state`` is updated in place.
+
+    q, k: [N, H, d_k] bf16/fp32; v: [N, H, d_v]; log_alpha: [N, H, d_k] fp32;
+    beta: [N, H] fp32; state: [N, H, d_k, d_v] fp32.  Returns ``out`` [N, H, d_v].
+    """
+    torch = _torch()
+    _require(q, "q")
+    if q.dim() != 3:
+        raise ValueError("q must be [N, H, d_k]")
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    _require(k, "k", q.dtype, (N, H, dk))
+    _require(v, "v", q.dtype, (N, H, dv))
+    _require(log_alpha, "log_alpha", torch.float32, (N, H, dk))
+    _require(beta, "beta", torch.float32, (N, H))
+    _require(state, "state", torch.float32, (N, H, dk, dv))
+    odt = _out_dtype(q, out, out_f32)
+    if odt not in (q.dtype, torch.float32):
+        raise TypeError("out must have the dtype of q, or float32")
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=odt, device=q.device)
+    _require(out, "out", odt, (N, H, dv))
+    shape = make_shape(N, N, H, dk, dv, _dtype_code(q),
+                       out_f32=int(odt == torch.float32 and q.dtype != torch.float32))
+    _check(load().kda_recurrent_step(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), float(scale), _ptr(state),
+        _ptr(out), ctypes.byref(shape), _stream_handle(stream)), "kda_recurrent_step")
+    return out
+
+
+def kda_device_status(stream=None) -> int:
+    """Synchronise the stream; return and clear the device-side status word."""
+    return int(load().kda_device_status(_stream_handle(stream)))

@@ -1,0 +1,252 @@
+// kda_api.cu -- the C ABI of libkda: host validation, engine selection,
+// scratch handling and launch.  See include/kda.h for the contract.
+#include <cmath>
+#include <cstdint>
+
+#include "kda_internal.cuh"
+
+namespace kda {
+
+namespace {
+
+// Device-side status word, one per device that loaded the library.  Kernels
+// with a bounded wait store KDA_ERR_TIMEOUT into it when the wait gives up;
+// kda_device_status() reads and clears it.
+__device__ int g_device_status = 0;
+
+constexpr int kMaxDevices = 64;
+int *g_status_ptr[kMaxDevices] = {};
+
+// Device address of g_device_status on the current device (looked up once
+// per device; the host-side symbol itself is not a device address).
+int *device_status_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int *>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_dim(int32_t d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+int32_t default_chunk(int32_t d) { return d >= 64 ? 64 : 16; }
+
+// Shared shape checks.  Returns KDA_SUCCESS or the first error found.
+kdaStatus_t check_shape(const kdaShape_t *s, bool step) {
+    if (!s) return KDA_ERR_INVALID_ARG;
+    if (s->num_seqs < 1 || s->total_tokens < 0 || s->num_heads < 1)
+        return KDA_ERR_INVALID_ARG;
+    if (s->d_k < 1 || s->d_v < 1) return KDA_ERR_INVALID_ARG;
+    if (s->dtype != KDA_DTYPE_BF16 && s->dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
+    if (s->out_f32 != 0 && s->out_f32 != 1) return KDA_ERR_INVALID_ARG;
+    if (step && s->total_tokens != s->num_seqs) return KDA_ERR_INVALID_ARG;
+    if (!step) {
+        if (s->chunk_size != 0 && s->chunk_size != 16 && s->chunk_size != 32 &&
+            s->chunk_size != 64)
+            return KDA_ERR_INVALID_ARG;
+        if (s->engine < KDA_ENGINE_AUTO || s->engine > KDA_ENGINE_SIMT)
+            return KDA_ERR_INVALID_ARG;
+    }
+    if (s->d_k != s->d_v || !supported_dim(s->d_k)) return KDA_ERR_UNSUPPORTED;
+    // Index arithmetic inside the kernels is 64-bit, but token and
+    // (token, head) counts travel as int32.
+    if ((int64_t)s->total_tokens * s->num_heads > INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    if ((int64_t)s->num_seqs * s->num_heads > INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    return KDA_SUCCESS;
+}
+
+bool tc_eligible(const kdaShape_t *s, int32_t C) {
+    return s->dtype == KDA_DTYPE_BF16 && s->d_k == 128 && s->d_v == 128 && C == 64;
+}
+
+struct Plan {
+    ChunkArgs args;
+    bool use_tc;
+    size_t workspace;
+};
+
+kdaStatus_t plan_chunk(const void *q, const void *k, const void *v, const float *log_alpha,
+                       const float *beta, float scale, const float *initial_state,
+                       const int32_t *cu_seqlens, void *out, float *final_state,
+                       const kdaShape_t *shape, Plan *plan) {
+    kdaStatus_t st = check_shape(shape, false);
+    if (st != KDA_SUCCESS) return st;
+    if (!std::isfinite(scale)) return KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens && shape->num_seqs != 1) return KDA_ERR_INVALID_ARG;
+    if (shape->total_tokens > 0) {
+        const void *ptrs[] = {q, k, v, log_alpha, beta, out};
+        for (const void *p : ptrs)
+            if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    }
+    const void *opt[] = {initial_state, final_state, cu_seqlens};
+    for (const void *p : opt)
+        if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    const int32_t C = shape->chunk_size ? shape->chunk_size : default_chunk(shape->d_k);
+    bool use_tc;
+    switch (shape->engine) {
+        case KDA_ENGINE_TENSOR:
+            if (!tc_eligible(shape, C)) return KDA_ERR_UNSUPPORTED;
+            use_tc = true;
+            break;
+        case KDA_ENGINE_SIMT: use_tc = false; break;
+        default: use_tc = tc_eligible(shape, C); break;
+    }
+    ChunkArgs &a = plan->args;
+    a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.scale = scale;
+    a.initial_state = initial_state; a.cu_seqlens = cu_seqlens; a.out = out;
+    a.final_state = final_state;
+    a.N = shape->num_seqs; a.T = shape->total_tokens; a.H = shape->num_heads;
+    a.D = shape->d_k; a.C = C; a.dtype = shape->dtype;
+    a.out_f32 = (shape->dtype == KDA_DTYPE_F32) ? 1 : shape->out_f32;
+    plan->use_tc = use_tc;
+    plan->workspace = use_tc ? chunk_tc_workspace_bytes(a.N, a.T, a.H) : 0;
+    return KDA_SUCCESS;
+}
+
+kdaStatus_t cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return KDA_SUCCESS;
+    (void)cudaGetLastError();  // clear a non-sticky error so later calls start clean
+    return KDA_ERR_CUDA;
+}
+
+kdaStatus_t run_plan(Plan p, void *workspace, cudaStream_t stream, StageClock *clock) {
+    StageClock local;
+    p.args.clock = clock ? clock : &local;
+    p.args.status = device_status_ptr();
+    if (!p.args.status) {
+        (void)cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    p.args.clock->mark(stream);
+    if (p.use_tc) return cuda_status(launch_chunk_tc(p.args, workspace, p.workspace, stream));
+    return cuda_status(launch_chunk_simt(p.args, stream));
+}
+
+}  // namespace
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" {
+
+const char *kda_status_string(kdaStatus_t status) {
+    switch (status) {
+        case KDA_SUCCESS: return "KDA_SUCCESS";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: outside the support matrix";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA: a CUDA call or launch failed";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded device wait gave up";
+    }
+    return "KDA_ERR_UNKNOWN";
+}
+
+kdaStatus_t kda_chunk_fwd_workspace_size(const kdaShape_t *shape, size_t *bytes) {
+    if (!bytes) return KDA_ERR_INVALID_ARG;
+    kdaStatus_t st = check_shape(shape, false);
+    if (st != KDA_SUCCESS) return st;
+    const int32_t C = shape->chunk_size ? shape->chunk_size : default_chunk(shape->d_k);
+    bool use_tc = shape->engine == KDA_ENGINE_SIMT ? false : tc_eligible(shape, C);
+    if (shape->engine == KDA_ENGINE_TENSOR && !use_tc) return KDA_ERR_UNSUPPORTED;
+    *bytes = use_tc ? chunk_tc_workspace_bytes(shape->num_seqs, shape->total_tokens,
+                                               shape->num_heads)
+                    : 0;
+    return KDA_SUCCESS;
+}
+
+kdaStatus_t kda_chunk_fwd_ws_timed(const void *q, const void *k, const void *v,
+                                   const float *log_alpha, const float *beta, float scale,
+                                   const float *initial_state, const int32_t *cu_seqlens,
+                                   void *out, float *final_state, const kdaShape_t *shape,
+                                   void *workspace, size_t workspace_bytes,
+                                   cudaStream_t stream, cudaEvent_t *events,
+                                   int32_t max_events, int32_t *n_recorded) {
+    if (n_recorded) *n_recorded = 0;
+    if (max_events < 0 || (max_events > 0 && !events)) return KDA_ERR_INVALID_ARG;
+    Plan p;
+    kdaStatus_t st = plan_chunk(q, k, v, log_alpha, beta, scale, initial_state, cu_seqlens,
+                                out, final_state, shape, &p);
+    if (st != KDA_SUCCESS) return st;
+    if (p.workspace > 0) {
+        if (!workspace || workspace_bytes < p.workspace) return KDA_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KDA_ERR_INVALID_ARG;
+    }
+    StageClock clock;
+    clock.events = events;
+    clock.max_events = max_events;
+    st = run_plan(p, workspace, stream, &clock);
+    if (n_recorded) *n_recorded = clock.n < max_events ? clock.n : max_events;
+    return st;
+}
+
+kdaStatus_t kda_chunk_fwd_ws(const void *q, const void *k, const void *v,
+                             const float *log_alpha, const float *beta, float scale,
+                             const float *initial_state, const int32_t *cu_seqlens,
+                             void *out, float *final_state, const kdaShape_t *shape,
+                             void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return kda_chunk_fwd_ws_timed(q, k, v, log_alpha, beta, scale, initial_state, cu_seqlens,
+                                  out, final_state, shape, workspace, workspace_bytes, stream,
+                                  nullptr, 0, nullptr);
+}
+
+kdaStatus_t kda_chunk_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                          const float *beta, float scale, const float *initial_state,
+                          const int32_t *cu_seqlens, void *out, float *final_state,
+                          const kdaShape_t *shape, cudaStream_t stream) {
+    Plan p;
+    kdaStatus_t st = plan_chunk(q, k, v, log_alpha, beta, scale, initial_state, cu_seqlens,
+                                out, final_state, shape, &p);
+    if (st != KDA_SUCCESS) return st;
+    void *ws = nullptr;
+    if (p.workspace > 0) {
+        if (cudaMallocAsync(&ws, p.workspace, stream) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return KDA_ERR_CUDA;
+        }
+    }
+    st = run_plan(p, ws, stream, nullptr);
+    if (ws && cudaFreeAsync(ws, stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        if (st == KDA_SUCCESS) st = KDA_ERR_CUDA;
+    }
+    return st;
+}
+
+kdaStatus_t kda_recurrent_step(const void *q, const void *k, const void *v,
+                               const float *log_alpha, const float *beta, float scale,
+                               float *state, void *out, const kdaShape_t *shape,
+                               cudaStream_t stream) {
+    kdaStatus_t st = check_shape(shape, true);
+    if (st != KDA_SUCCESS) return st;
+    if (!std::isfinite(scale)) return KDA_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, log_alpha, beta, state, out};
+    for (const void *p : ptrs)
+        if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    StepArgs a;
+    a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.scale = scale;
+    a.state = state; a.out = out; a.N = shape->num_seqs; a.H = shape->num_heads;
+    a.D = shape->d_k; a.dtype = shape->dtype;
+    a.out_f32 = (shape->dtype == KDA_DTYPE_F32) ? 1 : shape->out_f32;
+    return cuda_status(launch_recurrent_step(a, stream));
+}
+
+kdaStatus_t kda_device_status(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    int value = 0;
+    const int zero = 0;
+    if (cudaMemcpyFromSymbol(&value, g_device_status, sizeof(int)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    return value == 0 ? KDA_SUCCESS : static_cast<kdaStatus_t>(value);
+}
+
+}  // extern "C"

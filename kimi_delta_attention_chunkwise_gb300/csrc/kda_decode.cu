@@ -1,0 +1,170 @@
+// kda_decode.cu -- one KDA decode step for a batch of independent sequences.
+//
+// The step is the recurrence of "Kimi Unveils Delta Attention and K3
+// Architecture Updates", sec. 4.1 (five-line d_k x d_v form) and sec. 5
+// (fused recurrent schedule): decay the rows of the state, predict S_bar^T k,
+// correct, write k e^T, read S_t^T (scale q).  Using
+//     S_t^T q = S_bar^T q + (k . q) e,
+// both reductions (S_bar^T k and S_bar^T q) come out of ONE pass over the
+// decayed state held in registers, and the write goes back in place, so every
+// state byte crosses HBM exactly once in each direction.
+//
+// Work decomposition (d = d_k = d_v): one CTA per (sequence, head).  A thread
+// owns a 4-column group of the state (one float4 per row) and ROWS rows
+// strided by RG, so a warp's load of one row is fully coalesced (D = 128:
+// 32 lanes x 16 B = one 512 B row).  Column sums over rows go through warp
+// registers, then one shared-memory exchange across row groups.
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+    return __bfloat162float(x);
+}
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+template <int D>
+struct StepCfg {
+    static constexpr int CG = D / 4;                                  // column groups
+    static constexpr int THREADS = (CG * D < 256) ? CG * D : 256;
+    static constexpr int RG = THREADS / CG;                           // row groups
+    static constexpr int ROWS = D / RG;                               // rows per thread
+    static_assert(RG * ROWS == D, "row split");
+};
+
+template <typename TIn, typename TOut, int D>
+__global__ void __launch_bounds__(StepCfg<D>::THREADS)
+recurrent_step_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
+                      const TIn *__restrict__ v, const float *__restrict__ log_alpha,
+                      const float *__restrict__ beta, float scale, float *state,
+                      TOut *__restrict__ out, int32_t NH) {
+    using Cfg = StepCfg<D>;
+    constexpr int CG = Cfg::CG, RG = Cfg::RG, ROWS = Cfg::ROWS, THREADS = Cfg::THREADS;
+    __shared__ float s_k[D], s_q[D], s_alpha[D], s_e[D];
+    __shared__ float s_red[2][RG][D];
+    __shared__ float s_kq;
+
+    const int64_t nh = blockIdx.x;  // (sequence, head) pair; vectors are [N*H, D]
+    if (nh >= NH) return;
+    const int tid = threadIdx.x;
+    const int cg = tid % CG, rg = tid / CG;
+
+    float4 *S = reinterpret_cast<float4 *>(state + nh * D * D);
+    // Issue the state loads first: they are the bulk of the traffic.
+    float4 s[ROWS];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) s[r] = __ldcs(S + (size_t)(rg + r * RG) * CG + cg);
+
+    for (int i = tid; i < D; i += THREADS) {
+        s_k[i] = to_f32(k[nh * D + i]);
+        s_q[i] = to_f32(q[nh * D + i]);
+        s_alpha[i] = __expf(log_alpha[nh * D + i]);
+    }
+    __syncthreads();
+    if (tid < 32) {
+        float acc = 0.f;
+        for (int i = tid; i < D; i += 32) acc += s_k[i] * s_q[i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (tid == 0) s_kq = acc;
+    }
+
+    // Decay the rows, then both column reductions in one pass.
+    float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+        const int row = rg + r * RG;
+        const float a = s_alpha[row], kr = s_k[row], qr = s_q[row];
+        s[r].x *= a; s[r].y *= a; s[r].z *= a; s[r].w *= a;
+        pk.x += s[r].x * kr; pk.y += s[r].y * kr; pk.z += s[r].z * kr; pk.w += s[r].w * kr;
+        pq.x += s[r].x * qr; pq.y += s[r].y * qr; pq.z += s[r].z * qr; pq.w += s[r].w * qr;
+    }
+    // Lanes of a warp that share a column group hold different row groups
+    // when CG < 32: fold them with shuffles first.
+#pragma unroll
+    for (int o = CG; o < 32; o <<= 1) {
+        pk.x += __shfl_xor_sync(0xffffffffu, pk.x, o); pk.y += __shfl_xor_sync(0xffffffffu, pk.y, o);
+        pk.z += __shfl_xor_sync(0xffffffffu, pk.z, o); pk.w += __shfl_xor_sync(0xffffffffu, pk.w, o);
+        pq.x += __shfl_xor_sync(0xffffffffu, pq.x, o); pq.y += __shfl_xor_sync(0xffffffffu, pq.y, o);
+        pq.z += __shfl_xor_sync(0xffffffffu, pq.z, o); pq.w += __shfl_xor_sync(0xffffffffu, pq.w, o);
+    }
+    constexpr int RG_PER_WARP = (CG < 32) ? 32 / CG : 1;
+    if ((tid % 32) < CG || CG >= 32) {
+        const int slot = rg / RG_PER_WARP;
+        reinterpret_cast<float4 *>(s_red[0][slot])[cg] = pk;
+        reinterpret_cast<float4 *>(s_red[1][slot])[cg] = pq;
+    }
+    __syncthreads();
+    constexpr int SLOTS = RG / RG_PER_WARP;
+    if (tid < D) {
+        float p = 0.f, rq = 0.f;
+#pragma unroll
+        for (int w = 0; w < SLOTS; ++w) { p += s_red[0][w][tid]; rq += s_red[1][w][tid]; }
+        const float e = beta[nh] * (to_f32(v[nh * D + tid]) - p);
+        s_e[tid] = e;
+        out[nh * D + tid] = from_f32<TOut>(scale * (rq + s_kq * e));
+    }
+    __syncthreads();
+
+    // Write S_t = S_bar + k e^T back in place.
+    const float4 e4 = reinterpret_cast<const float4 *>(s_e)[cg];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+        const int row = rg + r * RG;
+        const float kr = s_k[row];
+        float4 x = s[r];
+        x.x += kr * e4.x; x.y += kr * e4.y; x.z += kr * e4.z; x.w += kr * e4.w;
+        __stcs(S + (size_t)row * CG + cg, x);
+    }
+}
+
+template <typename TIn, typename TOut, int D>
+cudaError_t launch_step_t(const StepArgs &a, cudaStream_t stream) {
+    const int64_t NH = (int64_t)a.N * a.H;
+    if (NH == 0) return cudaSuccess;
+    recurrent_step_kernel<TIn, TOut, D><<<(unsigned)NH, StepCfg<D>::THREADS, 0, stream>>>(
+        static_cast<const TIn *>(a.q), static_cast<const TIn *>(a.k),
+        static_cast<const TIn *>(a.v), a.log_alpha, a.beta, a.scale, a.state,
+        static_cast<TOut *>(a.out), (int32_t)NH);
+    return cudaGetLastError();
+}
+
+template <typename TIn, typename TOut>
+cudaError_t launch_step_dtype(const StepArgs &a, cudaStream_t stream) {
+    switch (a.D) {
+        case 16: return launch_step_t<TIn, TOut, 16>(a, stream);
+        case 32: return launch_step_t<TIn, TOut, 32>(a, stream);
+        case 64: return launch_step_t<TIn, TOut, 64>(a, stream);
+        case 128: return launch_step_t<TIn, TOut, 128>(a, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_recurrent_step(const StepArgs &a, cudaStream_t stream) {
+    if (a.dtype == KDA_DTYPE_BF16) {
+        if (a.out_f32) return launch_step_dtype<__nv_bfloat16, float>(a, stream);
+        return launch_step_dtype<__nv_bfloat16, __nv_bfloat16>(a, stream);
+    }
+    return launch_step_dtype<float, float>(a, stream);
+}
+
+}  // namespace kda

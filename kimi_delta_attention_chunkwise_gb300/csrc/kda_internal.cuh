@@ -1,0 +1,64 @@
+// kda_internal.cuh -- declarations shared by the libkda translation units.
+// Not part of the public ABI (that is include/kda.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kda.h"
+
+namespace kda {
+
+// Optional device-side stage timing: records caller-created events on the
+// launch stream before the first kernel and after each kernel.
+struct StageClock {
+    cudaEvent_t *events = nullptr;
+    int32_t max_events = 0;
+    int32_t n = 0;
+    void mark(cudaStream_t s) {
+        if (events && n < max_events) cudaEventRecord(events[n], s);
+        ++n;
+    }
+};
+
+// Everything a chunk launch needs, after host validation.
+struct ChunkArgs {
+    const void *q, *k, *v;
+    const float *log_alpha, *beta;
+    float scale;
+    const float *initial_state;
+    const int32_t *cu_seqlens;   // device, N + 1 entries, or nullptr (one sequence)
+    void *out;
+    float *final_state;
+    int32_t N, T, H, D, C;
+    int32_t dtype;               // kdaDtype_t of q, k, v
+    int32_t out_f32;             // 1: out is float32, 0: out has dtype
+    int *status;                 // device status word (kernels with bounded waits
+                                 // store KDA_ERR_TIMEOUT here when one gives up)
+    StageClock *clock;           // never null inside the launchers
+};
+
+struct StepArgs {
+    const void *q, *k, *v;
+    const float *log_alpha, *beta;
+    float scale;
+    float *state;
+    void *out;
+    int32_t N, H, D;
+    int32_t dtype;
+    int32_t out_f32;
+};
+
+// fp32 CUDA-core chunk engine (kda_chunk_simt.cu).  Needs no scratch.
+cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t stream);
+
+// Decode step (kda_decode.cu).
+cudaError_t launch_recurrent_step(const StepArgs &a, cudaStream_t stream);
+
+// Tensor-core chunk engine (kda_chunk_tc.cu): bf16, D = 128, C = 64.
+size_t chunk_tc_workspace_bytes(int32_t N, int32_t T, int32_t H);
+cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
+
+}  // namespace kda

@@ -1,0 +1,119 @@
+"""The C ABI without a GPU: the library builds, loads, exports every function
+include/kda.h declares, and rejects bad arguments on the host before any CUDA
+call.  No kernel runs here."""
+import ctypes
+
+import pytest
+
+import kimi_delta_attention_chunkwise_gb300 as kda
+from kimi_delta_attention_chunkwise_gb300 import binding, build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def test_header_declares_the_boundary():
+    names = binding.header_functions()
+    for required in ("kda_chunk_fwd", "kda_recurrent_step", "kda_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_header_symbol(lib):
+    for name in binding.header_functions():
+        assert hasattr(lib, name), f"libkda.so does not export {name}"
+
+
+def test_library_is_the_in_tree_build(lib):
+    assert binding.lib_path().startswith(build.PKG)
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        s = kda.kda_status_string(code)
+        assert s.startswith("KDA_")
+    assert "UNKNOWN" in kda.kda_status_string(99)
+
+
+def _shape(**kw):
+    base = dict(N=1, T=64, H=2, dk=128, dv=128, dtype_code=kda.KDA_DTYPE_BF16)
+    base.update(kw)
+    return kda.make_shape(base["N"], base["T"], base["H"], base["dk"], base["dv"],
+                          base["dtype_code"], base.get("chunk_size", 0),
+                          base.get("engine", kda.KDA_ENGINE_AUTO))
+
+
+FAKE = 0x10000  # 16-byte-aligned fake address: never dereferenced by these calls
+
+
+def _chunk(lib, shape, ptrs=None, scale=1.0, cu=None):
+    p = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, b=FAKE, out=FAKE)
+    p.update(ptrs or {})
+    return lib.kda_chunk_fwd(p["q"], p["k"], p["v"], p["g"], p["b"], ctypes.c_float(scale),
+                             None, cu, p["out"], None,
+                             ctypes.byref(shape) if shape is not None else None, None)
+
+
+def test_chunk_rejects_bad_arguments(lib):
+    assert _chunk(lib, None) == kda.KDA_ERR_INVALID_ARG
+    assert _chunk(lib, _shape(N=0)) == kda.KDA_ERR_INVALID_ARG
+    assert _chunk(lib, _shape(T=-1)) == kda.KDA_ERR_INVALID_ARG
+    assert _chunk(lib, _shape(H=0)) == kda.KDA_ERR_INVALID_ARG
+    assert _chunk(lib, _shape(dtype_code=7)) == kda.KDA_ERR_INVALID_ARG
+    assert _chunk(lib, _shape(chunk_size=48)) == kda.KDA_ERR_INVALID_ARG
+    assert _chunk(lib, _shape(engine=9)) == kda.KDA_ERR_INVALID_ARG
+    assert _chunk(lib, _shape(N=3)) == kda.KDA_ERR_INVALID_ARG       # N > 1 needs cu_seqlens
+    assert _chunk(lib, _shape(), scale=float("nan")) == kda.KDA_ERR_INVALID_ARG
+    assert _chunk(lib, _shape(), ptrs={"v": FAKE + 2}) == kda.KDA_ERR_INVALID_ARG  # misaligned
+    assert _chunk(lib, _shape(), ptrs={"out": None}) == kda.KDA_ERR_INVALID_ARG
+    assert _chunk(lib, _shape(), ptrs={"g": None}) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_chunk_support_matrix(lib):
+    assert _chunk(lib, _shape(dk=96, dv=96)) == kda.KDA_ERR_UNSUPPORTED
+    assert _chunk(lib, _shape(dk=128, dv=64)) == kda.KDA_ERR_UNSUPPORTED
+    # the tensor-core engine is bf16, d = 128, C = 64 only
+    assert _chunk(lib, _shape(dtype_code=kda.KDA_DTYPE_F32,
+                              engine=kda.KDA_ENGINE_TENSOR)) == kda.KDA_ERR_UNSUPPORTED
+    assert _chunk(lib, _shape(dk=64, dv=64, engine=kda.KDA_ENGINE_TENSOR)) == kda.KDA_ERR_UNSUPPORTED
+    assert _chunk(lib, _shape(chunk_size=32, engine=kda.KDA_ENGINE_TENSOR)) == kda.KDA_ERR_UNSUPPORTED
+
+
+def test_workspace_query(lib):
+    n = ctypes.c_size_t(123)
+    assert lib.kda_chunk_fwd_workspace_size(None, ctypes.byref(n)) == kda.KDA_ERR_INVALID_ARG
+    s = _shape(engine=kda.KDA_ENGINE_SIMT)
+    assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(s), ctypes.byref(n)) == kda.KDA_SUCCESS
+    assert n.value == 0
+    s = _shape(T=1 << 20, H=32)
+    assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(s), ctypes.byref(n)) == kda.KDA_SUCCESS
+    assert n.value % 256 == 0
+
+
+def test_workspace_variant_rejects_missing_scratch(lib):
+    s = _shape(T=4096, H=16)
+    need = ctypes.c_size_t(0)
+    assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(s), ctypes.byref(need)) == 0
+    if need.value == 0:
+        pytest.skip("engine needs no scratch")
+    rc = lib.kda_chunk_fwd_ws(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(1.0), None, None,
+                              FAKE, None, ctypes.byref(s), None, 0, None)
+    assert rc == kda.KDA_ERR_INVALID_ARG
+    rc = lib.kda_chunk_fwd_ws(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(1.0), None, None,
+                              FAKE, None, ctypes.byref(s), FAKE + 16, need.value, None)
+    assert rc == kda.KDA_ERR_INVALID_ARG  # not 256-byte aligned
+
+
+def test_step_rejects_bad_arguments(lib):
+    def step(shape, **kw):
+        p = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, b=FAKE, s=FAKE, out=FAKE)
+        p.update(kw)
+        return lib.kda_recurrent_step(p["q"], p["k"], p["v"], p["g"], p["b"],
+                                      ctypes.c_float(1.0), p["s"], p["out"],
+                                      ctypes.byref(shape), None)
+    assert step(_shape(N=4, T=5)) == kda.KDA_ERR_INVALID_ARG     # one token per sequence
+    assert step(_shape(N=4, T=4), s=None) == kda.KDA_ERR_INVALID_ARG
+    assert step(_shape(N=4, T=4), q=FAKE + 8) == kda.KDA_ERR_INVALID_ARG
+    assert step(_shape(N=4, T=4, dk=48, dv=48)) == kda.KDA_ERR_UNSUPPORTED
