@@ -16,8 +16,10 @@
  * piece of Gated DeltaNet" (key-by-value orientation, o_t = S_t^T q_t).
  *
  * Memory contract shared by every entry point:
- *   - All tensor arguments are DEVICE pointers, contiguous, row-major, in the
- *     layouts given below, and 16-byte aligned.  The caller owns every buffer.
+ *   - All tensor arguments are DEVICE pointers, contiguous and row-major in
+ *     the layouts given below.  q, k, v, out and the states must be 16-byte
+ *     aligned; log_alpha, beta and cu_seqlens 4-byte aligned.  The caller
+ *     owns every buffer.
  *   - Calls are asynchronous with respect to the host; all work is enqueued
  *     on `stream` (0 = the legacy default stream).
  *   - Host-detectable errors are returned before anything is launched, and

@@ -31,6 +31,7 @@ int *device_status_ptr() {
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 bool supported_dim(int32_t d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 
@@ -79,13 +80,17 @@ kdaStatus_t plan_chunk(const void *q, const void *k, const void *v, const float 
     if (!std::isfinite(scale)) return KDA_ERR_INVALID_ARG;
     if (!cu_seqlens && shape->num_seqs != 1) return KDA_ERR_INVALID_ARG;
     if (shape->total_tokens > 0) {
-        const void *ptrs[] = {q, k, v, log_alpha, beta, out};
-        for (const void *p : ptrs)
+        const void *vec[] = {q, k, v, out};
+        for (const void *p : vec)
             if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+        const void *sc[] = {log_alpha, beta};
+        for (const void *p : sc)
+            if (!p || !aligned4(p)) return KDA_ERR_INVALID_ARG;
     }
-    const void *opt[] = {initial_state, final_state, cu_seqlens};
+    const void *opt[] = {initial_state, final_state};
     for (const void *p : opt)
         if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens && !aligned4(cu_seqlens)) return KDA_ERR_INVALID_ARG;
     const int32_t C = shape->chunk_size ? shape->chunk_size : default_chunk(shape->d_k);
     bool use_tc;
     switch (shape->engine) {
@@ -223,9 +228,12 @@ kdaStatus_t kda_recurrent_step(const void *q, const void *k, const void *v,
     kdaStatus_t st = check_shape(shape, true);
     if (st != KDA_SUCCESS) return st;
     if (!std::isfinite(scale)) return KDA_ERR_INVALID_ARG;
-    const void *ptrs[] = {q, k, v, log_alpha, beta, state, out};
-    for (const void *p : ptrs)
+    const void *vec[] = {q, k, v, state, out};
+    for (const void *p : vec)
         if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    const void *sc[] = {log_alpha, beta};
+    for (const void *p : sc)
+        if (!p || !aligned4(p)) return KDA_ERR_INVALID_ARG;
     StepArgs a;
     a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.scale = scale;
     a.state = state; a.out = out; a.N = shape->num_seqs; a.H = shape->num_heads;

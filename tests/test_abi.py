@@ -67,6 +67,7 @@ def test_chunk_rejects_bad_arguments(lib):
     assert _chunk(lib, _shape(N=3)) == kda.KDA_ERR_INVALID_ARG       # N > 1 needs cu_seqlens
     assert _chunk(lib, _shape(), scale=float("nan")) == kda.KDA_ERR_INVALID_ARG
     assert _chunk(lib, _shape(), ptrs={"v": FAKE + 2}) == kda.KDA_ERR_INVALID_ARG  # misaligned
+    assert _chunk(lib, _shape(), ptrs={"b": FAKE + 2}) == kda.KDA_ERR_INVALID_ARG
     assert _chunk(lib, _shape(), ptrs={"out": None}) == kda.KDA_ERR_INVALID_ARG
     assert _chunk(lib, _shape(), ptrs={"g": None}) == kda.KDA_ERR_INVALID_ARG
 
@@ -116,4 +117,5 @@ def test_step_rejects_bad_arguments(lib):
     assert step(_shape(N=4, T=5)) == kda.KDA_ERR_INVALID_ARG     # one token per sequence
     assert step(_shape(N=4, T=4), s=None) == kda.KDA_ERR_INVALID_ARG
     assert step(_shape(N=4, T=4), q=FAKE + 8) == kda.KDA_ERR_INVALID_ARG
+    assert step(_shape(N=4, T=4), b=FAKE + 2) == kda.KDA_ERR_INVALID_ARG
     assert step(_shape(N=4, T=4, dk=48, dv=48)) == kda.KDA_ERR_UNSUPPORTED
