@@ -54,6 +54,7 @@ kdaStatus_t check_shape(const kdaShape_t *s, bool step) {
             return KDA_ERR_INVALID_ARG;
     }
     if (s->d_k != s->d_v || !supported_dim(s->d_k)) return KDA_ERR_UNSUPPORTED;
+    if (s->num_heads > 65535) return KDA_ERR_UNSUPPORTED;  // heads index grid.y
     // Index arithmetic inside the kernels is 64-bit, but token and
     // (token, head) counts travel as int32.
     if ((int64_t)s->total_tokens * s->num_heads > INT32_MAX) return KDA_ERR_UNSUPPORTED;

@@ -1,13 +1,767 @@
-// kda_chunk_tc.cu -- tensor-core chunk engine (placeholder until the
-// tcgen05 kernels land).
+// kda_chunk_tc.cu -- tensor-core (tcgen05 / TMEM) chunk engine for bf16
+// inputs, d_k = d_v = 128, chunk C = 64.
+//
+// The chunkwise form of "Kimi Unveils Delta Attention and K3 Architecture
+// Updates", sec. 6, in the d_k x d_v layout, written with the WY
+// factorisation that the page's pipeline (sec. 6.6) names: for a chunk with
+// incoming state S_c and local cumulative log decay G (sec. 6.1),
+//
+//   R_ij   = beta_i <k_j, exp(G_i - G_j) k_i>   (j < i)        sec. 6.3
+//   A^kk   = (I + R)^-1                                          sec. 6.3
+//   A^qk_ij= s <k_j, exp(G_i - G_j) q_i>        (j <= i)       sec. 6.5
+//   W      = A^kk Diag(beta) (exp(G) * K),  U = A^kk Diag(beta) V
+//   E      = U - W S_c                (resolved errors; sec. 6.2 + 6.3)
+//   O      = (s exp(G) * Q) S_c + A^qk E                         sec. 6.5
+//   S_c+1  = Diag(exp(G_last)) S_c + K_end^T E,
+//            K_end_i = exp(G_last - G_i) * k_i                   sec. 6.4
+//
+// Three launches on the caller's stream:
+//   1. chunk_table  -- cu_seqlens -> first chunk index of every sequence
+//                      (chunks restart at each sequence start).
+//   2. chunk_prep   -- one CTA per (chunk, head), fully parallel: G, the
+//                      decayed [K;Q] K^T products on the tensor core, the
+//                      triangular solve, W on the tensor core, and the
+//                      boundary-facing factors.  Writes bf16 operand images
+//                      (already in the 128-byte-swizzled shared-memory
+//                      layout) to scratch.
+//   3. chunk_scan   -- one CTA per (sequence, head, 32-wide value tile):
+//                      the only serial loop, over the chunks of a sequence.
+//                      The fp32 state tile lives in registers; per chunk four
+//                      tcgen05 MMAs ([A^kk;0](beta V), [-W;Q_hat] S_c,
+//                      K_end^T E, [0;A^qk] E) and the next chunks' operands
+//                      stream in with bulk async copies (double buffered).
+//
+// Precision: every tensor-core product accumulates in fp32 (TMEM).  The
+// decayed [K;Q] K^T product takes tf32 operands (the exp factors need fp32
+// range); every other operand (A^kk, A^qk, W, Q_hat, K_end, beta V, E and
+// the state S_c) is fp16, whose 11-bit significand keeps the result within
+// the parity bound where bf16 operands (8 bits) do not.  The state itself
+// stays fp32 in registers across the whole sequence.
+//
+// Overflow of the factorised decay (hard part of any tensor-core form): the
+// products exp(G_i - G_j) are formed as exp(G_i - G_m) * exp(G_m - G_j) with
+// the mid-chunk reference m, which is exact in fp32/bf16 range as long as
+// |G_i - G_m| <= 80 for every channel and row.  A chunk that breaks this
+// (decays stronger than ~exp(-80) across half a chunk) takes a CUDA-core path
+// that evaluates every exp(G_i - G_j) directly, so any finite gates <= 0 work.
+#include <cstdint>
+#include <cuda_bf16.h>
+
 #include "kda_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace kda {
+namespace {
 
-size_t chunk_tc_workspace_bytes(int32_t, int32_t, int32_t) { return 0; }
+using namespace tc;
 
-cudaError_t launch_chunk_tc(const ChunkArgs &a, void *, size_t, cudaStream_t stream) {
-    return launch_chunk_simt(a, stream);
+constexpr int D = 128;        // d_k = d_v
+constexpr int C = 64;         // chunk
+constexpr int BV = 32;        // value columns per scan CTA
+constexpr int NT = D / BV;    // value tiles per head
+constexpr int MID = 32;       // reference row of the factorised decay
+constexpr float kSpanLimit = 80.f;
+constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
+
+// Per-(chunk, head) scratch images (f16 operands in the swizzled layout,
+// fp32 gates).
+constexpr uint32_t WQ_BYTES = 2 * 16384;  // [-W ; Q_hat] : 128 rows x 128 K, 2 panels
+constexpr uint32_t KE_BYTES = 16384;      // K_end^T     : 128 rows x 64 K
+constexpr uint32_t AK_BYTES = 8192;       // A^kk        : 64 rows x 64 K
+constexpr uint32_t AQ_BYTES = 8192;       // A^qk        : 64 rows x 64 K
+constexpr uint32_t GB_BYTES = 768;        // Gamma_last [128] f32, beta [64] f32
+
+struct Scratch {
+    uint8_t *wq, *ke, *ak, *aq, *gb;
+    int32_t *chunk_off;  // [N + 1]
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t max_chunks(int32_t N, int32_t T) { return (size_t)T / C + (size_t)N + 1; }
+
+Scratch carve(void *ws, int32_t N, int32_t T, int32_t H) {
+    const size_t nch = max_chunks(N, T) * (size_t)H;
+    uint8_t *p = static_cast<uint8_t *>(ws);
+    Scratch s;
+    s.wq = p; p += align256(nch * WQ_BYTES);
+    s.ke = p; p += align256(nch * KE_BYTES);
+    s.ak = p; p += align256(nch * AK_BYTES);
+    s.aq = p; p += align256(nch * AQ_BYTES);
+    s.gb = p; p += align256(nch * GB_BYTES);
+    s.chunk_off = reinterpret_cast<int32_t *>(p);
+    return s;
+}
+
+__device__ __forceinline__ void seq_bounds(const int32_t *cu, int32_t s, int32_t T, int32_t &a,
+                                           int32_t &b) {
+    if (cu) {
+        a = min(max(cu[s], 0), T);
+        b = min(max(cu[s + 1], a), T);
+    } else {
+        a = 0;
+        b = T;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 1. chunk table: chunk_off[s] = number of chunks before sequence s
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t *cu, int32_t N,
+                                                           int32_t T, int32_t *chunk_off) {
+    __shared__ int32_t warp_sum[32];
+    __shared__ int32_t carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (int32_t base = 0; base < N; base += 1024) {
+        const int32_t s = base + tid;
+        int32_t n = 0;
+        if (s < N) {
+            int32_t a, b;
+            seq_bounds(cu, s, T, a, b);
+            n = (b - a + C - 1) / C;
+        }
+        int32_t x = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_sum[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int32_t w = warp_sum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            warp_sum[lane] = w;  // inclusive over warps
+        }
+        __syncthreads();
+        const int32_t before = carry + (warp ? warp_sum[warp - 1] : 0) + x - n;
+        if (s < N) chunk_off[s] = before;
+        __syncthreads();
+        if (tid == 1023) carry = before + n;
+        __syncthreads();
+    }
+    if (tid == 0) chunk_off[N] = carry;
+}
+
+// Largest s with chunk_off[s] <= c (chunk_off is non-decreasing).
+__device__ __forceinline__ int32_t find_seq(const int32_t *off, int32_t N, int32_t c) {
+    int32_t lo = 0, hi = N - 1;
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (off[mid] <= c) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// ---------------------------------------------------------------------------
+// 2. per-(chunk, head) preparation
+// ---------------------------------------------------------------------------
+// Shared memory, with regions reused once their first tenant is done:
+//   a1: tf32 [K_tilde ; Q_tilde], 128 rows x 128 K in 4 panels (64 KB);
+//       after that MMA: R, X (= A^kk) and the solve's block products (fp32).
+//   b1: tf32 K_hat, 64 rows x 128 K in 4 panels (32 KB) (slow path: G fp32
+//       [64][128]); after that: A^kk f16 panel (8 KB) and
+//       (beta Gamma K)^T f16 panel, 128 rows x 64 K (16 KB).
+struct PrepSmem {
+    uint8_t a1[4 * 16384];
+    uint8_t b1[4 * 8192];
+    float beta[C];
+    uint64_t bar;
+    uint32_t tmem;
+};
+constexpr uint32_t kOffX = C * (C + 1) * 4;        // X after R inside a1
+constexpr uint32_t kOffTb = 2 * C * (C + 1) * 4;   // block products after X
+constexpr uint32_t kOffA2 = 8192;                  // (beta Gamma K)^T after A^kk inside b1
+static_assert(kOffTb + 3 * 16 * 17 * 4 <= 4 * 16384, "a1 reuse");
+
+__device__ __forceinline__ void store_row_f16_image(uint8_t *img, uint32_t row,
+                                                    const float (&v)[64]) {
+    // one 128-byte swizzled row of a 64-wide f16 panel, 8 chunks of 16 bytes
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+        uint4 u;
+        u.x = pack_f16x2(v[ch * 8 + 0], v[ch * 8 + 1]);
+        u.y = pack_f16x2(v[ch * 8 + 2], v[ch * 8 + 3]);
+        u.z = pack_f16x2(v[ch * 8 + 4], v[ch * 8 + 5]);
+        u.w = pack_f16x2(v[ch * 8 + 6], v[ch * 8 + 7]);
+        *reinterpret_cast<uint4 *>(img + sw128_chunk(row, ch)) = u;
+    }
+}
+
+__global__ void __launch_bounds__(128)
+chunk_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                  const float *__restrict__ log_alpha, const float *__restrict__ beta,
+                  float scale, const int32_t *__restrict__ cu, int32_t N, int32_t T, int32_t H,
+                  Scratch sc, int *status) {
+    extern __shared__ uint8_t smem_raw[];
+    PrepSmem &sm = *reinterpret_cast<PrepSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float(*R)[C + 1] = reinterpret_cast<float(*)[C + 1]>(sm.a1);
+    float(*X)[C + 1] = reinterpret_cast<float(*)[C + 1]>(sm.a1 + kOffX);
+    float(*Tb)[16][17] = reinterpret_cast<float(*)[16][17]>(sm.a1 + kOffTb);
+    uint8_t *b2 = sm.b1;            // A^kk, f16 panel
+    uint8_t *a2 = sm.b1 + kOffA2;   // (beta Gamma K)^T, f16 panel
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t c = blockIdx.x, h = blockIdx.y;
+    const int32_t total = sc.chunk_off[N];
+    if (c >= total) return;
+    const int32_t s = find_seq(sc.chunk_off, N, c);
+    int32_t ta, tb;
+    seq_bounds(cu, s, T, ta, tb);
+    const int32_t t0 = ta + (c - sc.chunk_off[s]) * C;
+    const int32_t L = min(C, tb - t0);
+    const size_t ch = (size_t)c * H + h;
+    uint8_t *wq = sc.wq + ch * WQ_BYTES;
+    uint8_t *ke = sc.ke + ch * KE_BYTES;
+    uint8_t *ak = sc.ak + ch * AK_BYTES;
+    uint8_t *aq = sc.aq + ch * AQ_BYTES;
+    float *gb = reinterpret_cast<float *>(sc.gb + ch * GB_BYTES);
+    const __nv_bfloat16 *kc = k + ((size_t)t0 * H + h) * D;  // row i at kc + i*H*D
+    const __nv_bfloat16 *qc = q + ((size_t)t0 * H + h) * D;
+    const size_t rs = (size_t)H * D;
+
+    if (tid == 0) {
+        mbar_init(&sm.bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&sm.tmem, 128);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    if (tid < C) {
+        const float b = tid < L ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
+        sm.beta[tid] = b;
+        gb[128 + tid] = b;
+    }
+
+    // sec. 6.1: chunk-local cumulative log decay of key channel d = tid.
+    const int d = tid;
+    float G[C];
+    {
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < C; ++i) {
+            acc += (i < L) ? log_alpha[(size_t)i * rs + ((size_t)t0 * H + h) * D + d] : 0.f;
+            G[i] = acc;
+        }
+    }
+    const float Gm = G[MID], Gl = G[C - 1];
+    float span = 0.f;
+#pragma unroll
+    for (int i = 0; i < C; ++i) span = fmaxf(span, fabsf(G[i] - Gm));
+    const int slow = __syncthreads_or(!(span <= kSpanLimit));
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem;
+    uint32_t mma_phase = 0;
+    bool ok = true;
+
+    if (slow) {
+        // CUDA-core path: every exp(G_i - G_j) taken directly (exponent <= 0).
+        float *Gs = reinterpret_cast<float *>(sm.b1);  // [64][128]
+#pragma unroll
+        for (int i = 0; i < C; ++i) Gs[i * D + d] = G[i];
+        __syncthreads();
+        for (int i = warp; i < C; i += 4) {
+            for (int j = 0; j <= i; ++j) {
+                float r = 0.f, a = 0.f;
+                if (i < L) {
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const int dd = lane + 32 * m;
+                        const float w = __expf(Gs[i * D + dd] - Gs[j * D + dd]) *
+                                        __bfloat162float(kc[j * rs + dd]);
+                        r += w * __bfloat162float(kc[i * rs + dd]);
+                        a += w * __bfloat162float(qc[i * rs + dd]);
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    r += __shfl_xor_sync(0xffffffffu, r, o);
+                    a += __shfl_xor_sync(0xffffffffu, a, o);
+                }
+                if (lane == 0) {
+                    R[i][j] = (j < i) ? sm.beta[i] * r : 0.f;
+                    X[i][j] = scale * a;
+                }
+            }
+            for (int j = i + 1 + lane; j < C; j += 32) {
+                R[i][j] = 0.f;
+                X[i][j] = 0.f;
+            }
+        }
+        __syncthreads();
+        if (tid < C) {
+            float row[64];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) row[j] = X[tid][j];
+            store_row_f16_image(aq, tid, row);
+        }
+        __syncthreads();
+    }
+
+    // Boundary-facing factors and the tf32 operands, token by token.
+    {
+        const float e_m = __expf(Gm), e_lm = __expf(Gl - Gm);
+        const uint32_t pa = (d >> 5) * 16384u, pb = (d >> 5) * 8192u;
+        uint8_t *qrow = wq + (d >> 6) * 16384u;
+        float kend[8];
+#pragma unroll
+        for (int i = 0; i < C; ++i) {
+            const bool in = i < L;
+            const float kv = in ? __bfloat162float(kc[i * rs + d]) : 0.f;
+            const float qv = in ? __bfloat162float(qc[i * rs + d]) : 0.f;
+            float gam, eend;
+            if (!slow) {
+                const float ep = __expf(G[i] - Gm), en = __expf(Gm - G[i]);
+                gam = ep * e_m;
+                eend = e_lm * en;
+                *reinterpret_cast<float *>(sm.a1 + pa + sw128_offset_f32(i, d & 31)) =
+                    to_tf32(kv * ep);
+                *reinterpret_cast<float *>(sm.a1 + pa + sw128_offset_f32(64 + i, d & 31)) =
+                    to_tf32(qv * ep);
+                *reinterpret_cast<float *>(sm.b1 + pb + sw128_offset_f32(i, d & 31)) =
+                    to_tf32(kv * en);
+            } else {
+                gam = __expf(G[i]);
+                eend = __expf(Gl - G[i]);
+            }
+            // Q_hat = s Gamma q -> rows 64..127 of the [-W ; Q_hat] image
+            *reinterpret_cast<__half *>(qrow + sw128_offset(64 + i, d & 63)) =
+                __float2half_rn(scale * gam * qv);
+            kend[i & 7] = eend * kv;
+            if ((i & 7) == 7) {
+                uint4 u;
+                u.x = pack_f16x2(kend[0], kend[1]); u.y = pack_f16x2(kend[2], kend[3]);
+                u.z = pack_f16x2(kend[4], kend[5]); u.w = pack_f16x2(kend[6], kend[7]);
+                *reinterpret_cast<uint4 *>(ke + sw128_chunk(d, i >> 3)) = u;
+            }
+        }
+        gb[d] = slow ? __expf(Gl) : e_lm * e_m;
+    }
+
+    if (!slow) {
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        // [K_tilde ; Q_tilde] K_hat^T on the tensor core (tf32): TMEM cols 0..63.
+        if (tid == 0) {
+            tc_fence_after();
+            mma_panels<true>(tmem, smem_u32(sm.a1), 16384, smem_u32(sm.b1), 8192, 16,
+                             idesc_tf32_f32(128, 64), false);
+            mma_commit(&sm.bar);
+        }
+        ok = mbar_wait_bounded(&sm.bar, mma_phase, kWaitCycles);
+        mma_phase ^= 1;
+        tc_fence_after();
+        float v[64];
+        if (ok) {
+            tmem_ld32(tmem_addr(tmem, warp * 32, 0), *reinterpret_cast<float(*)[32]>(&v[0]));
+            tmem_ld32(tmem_addr(tmem, warp * 32, 32), *reinterpret_cast<float(*)[32]>(&v[32]));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) v[j] = 0.f;
+        }
+        __syncthreads();  // a1 is free: the operands were consumed by the MMA
+        if (warp < 2) {
+            const int i = tid;  // key-key row
+            const float b = sm.beta[i];
+#pragma unroll
+            for (int j = 0; j < C; ++j) R[i][j] = (j < i && i < L) ? b * v[j] : 0.f;
+        } else {
+            const int i = tid - 64;  // query-key row
+            float row[64];
+#pragma unroll
+            for (int j = 0; j < C; ++j) row[j] = (j <= i && i < L) ? scale * v[j] : 0.f;
+            store_row_f16_image(aq, i, row);
+        }
+    }
+    for (int idx = tid; idx < C * (C + 1); idx += 128) (&X[0][0])[idx] = 0.f;
+    __syncthreads();
+
+    // sec. 6.3: A^kk = (I + R)^-1, unit lower triangular, fp32, 16 x 16 blocks.
+    if (tid < C) {
+        const int b = tid >> 4, cc = tid & 15, o = b * 16;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float acc2 = 0.f;
+#pragma unroll
+            for (int m = 0; m < 15; ++m)
+                if (m < r && m >= cc) acc2 += R[o + r][o + m] * x[m];
+            x[r] = (r < cc) ? 0.f : (r == cc ? 1.f : -acc2);
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) X[o + r][o + cc] = x[r];
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int dist = 1; dist < 4; ++dist) {
+        const int nblk = 4 - dist;
+        // T_IJ = sum_{K=J}^{I-1} R_IK X_KJ
+        for (int e = tid; e < nblk * 256; e += 128) {
+            const int bi = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+            const int I = bi + dist, J = bi;
+            float acc2 = 0.f;
+            for (int K = J; K < I; ++K) {
+#pragma unroll
+                for (int m = 0; m < 16; ++m)
+                    acc2 += R[I * 16 + r][K * 16 + m] * X[K * 16 + m][J * 16 + cc];
+            }
+            Tb[bi][r][cc] = acc2;
+        }
+        __syncthreads();
+        // X_IJ = -X_II T_IJ
+        for (int e = tid; e < nblk * 256; e += 128) {
+            const int bi = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+            const int I = bi + dist, J = bi;
+            float acc2 = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) acc2 += X[I * 16 + r][I * 16 + m] * Tb[bi][m][cc];
+            X[I * 16 + r][J * 16 + cc] = -acc2;
+        }
+        __syncthreads();
+    }
+    if (tid < C) {
+        float row[64];
+#pragma unroll
+        for (int j = 0; j < 64; ++j) row[j] = X[tid][j];
+        store_row_f16_image(b2, tid, row);
+        store_row_f16_image(ak, tid, row);
+    }
+    // (beta Gamma K)^T, row d, f16
+    {
+        float bgk[8];
+#pragma unroll
+        for (int i = 0; i < C; ++i) {
+            const float kv = (i < L) ? __bfloat162float(kc[i * rs + d]) : 0.f;
+            bgk[i & 7] = sm.beta[i] * __expf(G[i]) * kv;
+            if ((i & 7) == 7) {
+                uint4 u;
+                u.x = pack_f16x2(bgk[0], bgk[1]); u.y = pack_f16x2(bgk[2], bgk[3]);
+                u.z = pack_f16x2(bgk[4], bgk[5]); u.w = pack_f16x2(bgk[6], bgk[7]);
+                *reinterpret_cast<uint4 *>(a2 + sw128_chunk(d, i >> 3)) = u;
+            }
+        }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+
+    // W^T = (beta Gamma K)^T A^kk^T on the tensor core (f16): TMEM cols 64..127.
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        mma_panels(tmem + 64, smem_u32(a2), 0, smem_u32(b2), 0, 4, idesc_f16_f32(128, 64),
+                   false);
+        mma_commit(&sm.bar);
+    }
+    if (ok) ok = mbar_wait_bounded(&sm.bar, mma_phase, kWaitCycles);
+    tc_fence_after();
+    if (ok) {
+        float v[64];
+        tmem_ld32(tmem_addr(tmem, warp * 32, 64), *reinterpret_cast<float(*)[32]>(&v[0]));
+        tmem_ld32(tmem_addr(tmem, warp * 32, 96), *reinterpret_cast<float(*)[32]>(&v[32]));
+        // thread = key channel d, v[i] = W[i][d]; store -W into rows 0..63.
+        uint8_t *pnl = wq + (d >> 6) * 16384u;
+#pragma unroll
+        for (int i = 0; i < C; ++i)
+            *reinterpret_cast<__half *>(pnl + sw128_offset(i, d & 63)) = __float2half_rn(-v[i]);
+    } else if (tid == 0) {
+        atomicExch(status, (int)KDA_ERR_TIMEOUT);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+// ---------------------------------------------------------------------------
+// 3. the inter-chunk scan with fused outputs
+// ---------------------------------------------------------------------------
+struct ScanStage {
+    uint8_t wq[WQ_BYTES];        // [-W ; Q_hat]
+    uint8_t ke[KE_BYTES];        // K_end^T
+    uint8_t aa[3 * 8192];        // [A^kk | zeros | A^qk]
+    uint8_t v[C * BV * 2];       // value tile rows, bf16 [64][32]
+    float gb[GB_BYTES / 4];      // Gamma_last [128], beta [64]
+    uint8_t pad[1024 - (GB_BYTES % 1024) - (C * BV * 2) % 1024];
+};
+
+struct ScanSmem {
+    ScanStage st[2];
+    uint8_t sbt[2 * 4096];       // S_c^T f16: 32 rows x 128 K, 2 panels
+    uint8_t ebt[4096];           // E^T f16: 32 rows x 64 K
+    uint8_t bvt[4096];           // (beta V)^T f16: 32 rows x 64 K
+    uint64_t full[2];
+    uint64_t mma;
+    uint32_t tmem;
+    int32_t abort_flag;
+};
+
+template <typename TOut>
+__global__ void __launch_bounds__(128, 1)
+chunk_scan_kernel(const __nv_bfloat16 *__restrict__ v, const float *__restrict__ initial_state,
+                  const int32_t *__restrict__ cu, TOut *__restrict__ out,
+                  float *__restrict__ final_state, int32_t N, int32_t T, int32_t H, Scratch sc,
+                  int *status) {
+    extern __shared__ uint8_t smem_raw[];
+    ScanSmem &sm = *reinterpret_cast<ScanSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t seq = blockIdx.x / NT, vt = blockIdx.x % NT, h = blockIdx.y;
+    int32_t ta, tb;
+    seq_bounds(cu, seq, T, ta, tb);
+    const int32_t c_begin = sc.chunk_off[seq];
+    const int32_t n_chunks = (tb - ta + C - 1) / C;
+    const size_t state_off = (((size_t)seq * H + h) * D + tid) * D + (size_t)vt * BV;
+
+    // state row of key channel tid, 32 value columns, fp32
+    float S[BV];
+    if (initial_state) {
+#pragma unroll
+        for (int j = 0; j < BV; j += 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(initial_state + state_off + j);
+            S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < BV; ++j) S[j] = 0.f;
+    }
+
+    if (n_chunks > 0) {
+        // zero the constant zero blocks and the value tiles (rows past a
+        // partial chunk are never loaded and must stay finite)
+        for (int st = 0; st < 2; ++st) {
+            uint4 *z = reinterpret_cast<uint4 *>(sm.st[st].aa + 8192);
+            for (int idx = tid; idx < 8192 / 16; idx += 128) z[idx] = make_uint4(0, 0, 0, 0);
+            uint4 *zv = reinterpret_cast<uint4 *>(sm.st[st].v);
+            for (int idx = tid; idx < (C * BV * 2) / 16; idx += 128) zv[idx] = make_uint4(0, 0, 0, 0);
+        }
+        if (tid == 0) {
+            mbar_init(&sm.full[0], 1);
+            mbar_init(&sm.full[1], 1);
+            mbar_init(&sm.mma, 1);
+            sm.abort_flag = 0;
+            fence_mbar_init();
+        }
+        if (warp == 0) {
+            tmem_alloc(&sm.tmem, 64);
+            tmem_relinquish();
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        const uint32_t tmem = sm.tmem;
+        const uint32_t d1 = tmem, d2 = tmem + 32;
+        constexpr uint32_t IDESC = idesc_f16_f32(128, BV);
+
+        auto issue = [&](int32_t n, int stg) {
+            // warp 0: expect the bytes, then the copies of chunk n into stage stg
+            const int32_t t0 = ta + n * C;
+            const int32_t L = min(C, tb - t0);
+            const size_t ch = (size_t)(c_begin + n) * H + h;
+            ScanStage &S_ = sm.st[stg];
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&sm.full[stg],
+                                      WQ_BYTES + KE_BYTES + AK_BYTES + AQ_BYTES + GB_BYTES +
+                                          (uint32_t)L * BV * 2);
+                bulk_g2s(S_.wq, sc.wq + ch * WQ_BYTES, WQ_BYTES, &sm.full[stg]);
+                bulk_g2s(S_.ke, sc.ke + ch * KE_BYTES, KE_BYTES, &sm.full[stg]);
+                bulk_g2s(S_.aa, sc.ak + ch * AK_BYTES, AK_BYTES, &sm.full[stg]);
+                bulk_g2s(S_.aa + 16384, sc.aq + ch * AQ_BYTES, AQ_BYTES, &sm.full[stg]);
+                bulk_g2s(S_.gb, sc.gb + ch * GB_BYTES, GB_BYTES, &sm.full[stg]);
+            }
+            __syncwarp();
+            for (int i = lane; i < L; i += 32)
+                bulk_g2s(S_.v + i * BV * 2, v + ((size_t)(t0 + i) * H + h) * D + vt * BV,
+                         BV * 2, &sm.full[stg]);
+        };
+
+        if (warp == 0) {
+            issue(0, 0);
+            if (n_chunks > 1) issue(1, 1);
+        }
+        uint32_t mma_phase = 0;
+        bool ok = true;
+
+        for (int32_t n = 0; n < n_chunks; ++n) {
+            const int stg = n & 1;
+            ScanStage &st = sm.st[stg];
+            const int32_t t0 = ta + n * C;
+            const int32_t L = min(C, tb - t0);
+
+            ok = mbar_wait_bounded(&sm.full[stg], (n >> 1) & 1, kWaitCycles);
+            if (__syncthreads_or(!ok)) break;
+
+            // (beta V)^T operand: thread -> token row i = tid/2, 16 value columns
+            {
+                const int i = tid >> 1, j0 = (tid & 1) * 16;
+                const float b = st.gb[128 + i];
+                const __nv_bfloat16 *vr = reinterpret_cast<const __nv_bfloat16 *>(st.v) + i * BV + j0;
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    *reinterpret_cast<__half *>(sm.bvt + sw128_offset(j0 + j, i)) =
+                        __float2half_rn(b * __bfloat162float(vr[j]));
+            }
+            // S_c^T operand (f16): thread = key row tid
+            {
+                uint8_t *pnl = sm.sbt + (tid >> 6) * 4096;
+#pragma unroll
+                for (int j = 0; j < BV; ++j)
+                    *reinterpret_cast<__half *>(pnl + sw128_offset(j, tid & 63)) =
+                        __float2half_rn(S[j]);
+            }
+            fence_proxy_async();
+            tc_fence_before();
+            __syncthreads();
+            if (tid == 0) {
+                tc_fence_after();
+                // D1 = [A^kk ; 0] (beta V)      -> rows 0..63: U, rows 64..127: 0
+                mma_panels(d1, smem_u32(st.aa), 0, smem_u32(sm.bvt), 0, 4, IDESC, false);
+                // D1 += [-W ; Q_hat] S_c       -> rows 0..63: E, rows 64..127: Q_hat S_c
+                mma_panels(d1, smem_u32(st.wq), 16384, smem_u32(sm.sbt), 4096, 8, IDESC, true);
+                mma_commit(&sm.mma);
+            }
+            ok = mbar_wait_bounded(&sm.mma, mma_phase, kWaitCycles);
+            mma_phase ^= 1;
+            if (__syncthreads_or(!ok)) break;
+            tc_fence_after();
+            if (warp < 2) {
+                float e[32];
+                tmem_ld32(tmem_addr(d1, warp * 32, 0), e);
+                const int i = tid;  // token row
+#pragma unroll
+                for (int j = 0; j < BV; ++j)
+                    *reinterpret_cast<__half *>(sm.ebt + sw128_offset(j, i)) =
+                        __float2half_rn(e[j]);
+            }
+            fence_proxy_async();
+            tc_fence_before();
+            __syncthreads();
+            if (tid == 0) {
+                tc_fence_after();
+                // D2 = K_end^T E  (state increment)
+                mma_panels(d2, smem_u32(st.ke), 0, smem_u32(sm.ebt), 0, 4, IDESC, false);
+                // D1 += [0 ; A^qk] E  -> rows 64..127: outputs
+                mma_panels(d1, smem_u32(st.aa) + 8192, 0, smem_u32(sm.ebt), 0, 4, IDESC, true);
+                mma_commit(&sm.mma);
+            }
+            ok = mbar_wait_bounded(&sm.mma, mma_phase, kWaitCycles);
+            mma_phase ^= 1;
+            if (__syncthreads_or(!ok)) break;
+            tc_fence_after();
+            {
+                float ds[32];
+                tmem_ld32(tmem_addr(d2, warp * 32, 0), ds);
+                const float g = st.gb[tid];
+#pragma unroll
+                for (int j = 0; j < BV; ++j) S[j] = fmaf(g, S[j], ds[j]);
+            }
+            if (warp >= 2) {
+                float o[32];
+                tmem_ld32(tmem_addr(d1, warp * 32, 0), o);
+                const int i = tid - 64;
+                if (i < L) {
+                    TOut *dst = out + ((size_t)(t0 + i) * H + h) * D + vt * BV;
+                    if constexpr (sizeof(TOut) == 2) {
+#pragma unroll
+                        for (int j = 0; j < BV; j += 8) {
+                            uint4 u;
+                            u.x = pack_bf16x2(o[j], o[j + 1]); u.y = pack_bf16x2(o[j + 2], o[j + 3]);
+                            u.z = pack_bf16x2(o[j + 4], o[j + 5]); u.w = pack_bf16x2(o[j + 6], o[j + 7]);
+                            *reinterpret_cast<uint4 *>(dst + j) = u;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BV; j += 4)
+                            *reinterpret_cast<float4 *>(dst + j) =
+                                make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncthreads();
+            if (warp == 0 && n + 2 < n_chunks) issue(n + 2, stg);
+        }
+        if (!ok) {
+            if (tid == 0) atomicExch(status, (int)KDA_ERR_TIMEOUT);
+            // let copies already in flight land before the shared memory goes away
+            for (int stg = 0; stg < 2; ++stg)
+                (void)mbar_wait_bounded(&sm.full[stg], 0, kWaitCycles / 8);
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tmem, 64);
+        if (!ok) return;
+    }
+    if (final_state) {
+#pragma unroll
+        for (int j = 0; j < BV; j += 4)
+            *reinterpret_cast<float4 *>(final_state + state_off + j) =
+                make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    }
+}
+
+constexpr size_t kPrepSmem = sizeof(PrepSmem) + 1024;
+constexpr size_t kScanSmem = sizeof(ScanSmem) + 1024;
+
+}  // namespace
+
+size_t chunk_tc_workspace_bytes(int32_t N, int32_t T, int32_t H) {
+    const size_t nch = max_chunks(N, T) * (size_t)H;
+    return align256(nch * WQ_BYTES) + align256(nch * KE_BYTES) + align256(nch * AK_BYTES) +
+           align256(nch * AQ_BYTES) + align256(nch * GB_BYTES) +
+           align256(((size_t)N + 1) * sizeof(int32_t));
+}
+
+cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+    if (workspace_bytes < chunk_tc_workspace_bytes(a.N, a.T, a.H) || !workspace)
+        return cudaErrorInvalidValue;
+    const Scratch sc = carve(workspace, a.N, a.T, a.H);
+    chunk_table_kernel<<<1, 1024, 0, stream>>>(a.cu_seqlens, a.N, a.T, sc.chunk_off);
+    a.clock->mark(stream);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kPrepSmem);
+    if (e != cudaSuccess) return e;
+    const dim3 pgrid((unsigned)max_chunks(a.N, a.T), (unsigned)a.H);
+    chunk_prep_kernel<<<pgrid, 128, kPrepSmem, stream>>>(
+        static_cast<const __nv_bfloat16 *>(a.q), static_cast<const __nv_bfloat16 *>(a.k),
+        a.log_alpha, a.beta, a.scale, a.cu_seqlens, a.N, a.T, a.H, sc, a.status);
+    a.clock->mark(stream);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    const dim3 sgrid((unsigned)(a.N * NT), (unsigned)a.H);
+    if (a.out_f32) {
+        auto kern = chunk_scan_kernel<float>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
+        if (e != cudaSuccess) return e;
+        kern<<<sgrid, 128, kScanSmem, stream>>>(static_cast<const __nv_bfloat16 *>(a.v),
+                                                a.initial_state, a.cu_seqlens,
+                                                static_cast<float *>(a.out), a.final_state, a.N,
+                                                a.T, a.H, sc, a.status);
+    } else {
+        auto kern = chunk_scan_kernel<__nv_bfloat16>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
+        if (e != cudaSuccess) return e;
+        kern<<<sgrid, 128, kScanSmem, stream>>>(static_cast<const __nv_bfloat16 *>(a.v),
+                                                a.initial_state, a.cu_seqlens,
+                                                static_cast<__nv_bfloat16 *>(a.out),
+                                                a.final_state, a.N, a.T, a.H, sc, a.status);
+    }
+    a.clock->mark(stream);
+    return cudaGetLastError();
 }
 
 }  // namespace kda

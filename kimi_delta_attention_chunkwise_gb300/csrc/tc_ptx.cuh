@@ -1,0 +1,273 @@
+// tc_ptx.cuh -- hand-written inline PTX for the sm_103a tensor-core engine:
+// mbarriers, bulk async copies (TMA engine, non-tensor form), TMEM
+// allocation, tcgen05.mma (kind::f16, one CTA) and TMEM loads.
+//
+// Operand layout used everywhere: K-major, 128-byte swizzle.  A tile of R
+// rows (R a multiple of 8) and 128 bytes of K (64 half-precision or 32 tf32
+// elements) is a "panel": row r lives at byte r*128 of the panel, and its
+// 16-byte chunk c sits at chunk position (c ^ (r % 8)).  Panels are
+// 1024-byte aligned, so the swizzle the tensor core applies (address bits
+// [4,7) xor bits [7,10)) matches.  The MMA walks K in 32-byte steps by
+// advancing the descriptor start address inside the panel.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace kda {
+namespace tc {
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Byte offset of element (row, col) in a K-major SW128 panel of bf16.
+__device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col) {
+    return row * 128u + ((((col >> 3) ^ row) & 7u) << 4) + ((col & 7u) << 1);
+}
+
+// Byte offset of the 16-byte chunk `chunk` (0..7) of row `row`.
+__device__ __forceinline__ uint32_t sw128_chunk(uint32_t row, uint32_t chunk) {
+    return row * 128u + (((chunk ^ row) & 7u) << 4);
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete, for at most
+// `max_cycles` SM clocks.  Returns false when the limit is reached.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  long long max_cycles) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (clock64() - t0 > max_cycles) return false;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// bulk async copy global -> shared, completion counted on an mbarrier
+// (addresses 16-byte aligned, size a multiple of 16)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Make generic-proxy writes to shared memory visible to the async proxy
+// (tensor core operand reads, bulk copies).
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// TMEM
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// descriptors
+// ---------------------------------------------------------------------------
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address, 16 B units
+    d |= static_cast<uint64_t>(1u) << 16;                   // leading byte offset (unused)
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;           // stride byte offset
+    d |= static_cast<uint64_t>(1u) << 46;                   // version
+    d |= static_cast<uint64_t>(2u) << 61;                   // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: fp32 D, A and B K-major of one element format
+// (0 = f16 or 1 = bf16 under kind::f16, 2 = tf32 under kind::tf32).
+enum : uint32_t { kFmtF16 = 0, kFmtBF16 = 1, kFmtTF32 = 2 };
+__host__ __device__ constexpr uint32_t idesc_f32acc(uint32_t fmt, int M, int N) {
+    return (1u << 4)                                   // D: f32
+           | (fmt << 7)                                // A format
+           | (fmt << 10)                               // B format
+           | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return idesc_f32acc(kFmtBF16, M, N);
+}
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+    return idesc_f32acc(kFmtF16, M, N);
+}
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
+    return idesc_f32acc(kFmtTF32, M, N);
+}
+
+// ---------------------------------------------------------------------------
+// MMA and commit (issued by one thread)
+// ---------------------------------------------------------------------------
+// Half-precision operands (f16 or bf16, chosen by the instruction descriptor).
+__device__ __forceinline__ void mma_half(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// tf32 operands (fp32 storage, 8 elements = 32 bytes per K step).
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+// D[128 x N] (+)= A[128 x K] * B[N x K]^T over SW128 panels, K walked in
+// 32-byte steps (16 half-precision or 8 tf32 elements), 4 steps per panel.
+// a_base/b_base: shared addresses of the first panel; panel strides in bytes.
+template <bool TF32 = false>
+__device__ __forceinline__ void mma_panels(uint32_t d_tmem, uint32_t a_base, uint32_t a_panel,
+                                           uint32_t b_base, uint32_t b_panel, int ksteps,
+                                           uint32_t idesc, bool accumulate_first) {
+#pragma unroll 1
+    for (int ks = 0; ks < ksteps; ++ks) {
+        const uint32_t a = a_base + (ks >> 2) * a_panel + (ks & 3) * 32;
+        const uint32_t b = b_base + (ks >> 2) * b_panel + (ks & 3) * 32;
+        const uint32_t acc = (ks > 0 || accumulate_first) ? 1u : 0u;
+        if (TF32)
+            mma_tf32(d_tmem, sdesc_sw128(a), sdesc_sw128(b), idesc, acc);
+        else
+            mma_half(d_tmem, sdesc_sw128(a), sdesc_sw128(b), idesc, acc);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// TMEM -> registers: 32 lanes x 32-bit, N consecutive columns per thread
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// TMEM address of (lane, column): lane in bits [16, 32), column in [0, 16).
+__device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint32_t col) {
+    return base + (lane << 16) + col;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// fp32 -> tf32 rounded to nearest (ties away from zero), kept in fp32 storage,
+// so the tensor core's own reduction of the operand is exact.
+__device__ __forceinline__ float to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// Byte offset of fp32 element (row, col) in a K-major SW128 panel (32 per row).
+__device__ __forceinline__ uint32_t sw128_offset_f32(uint32_t row, uint32_t col) {
+    return row * 128u + ((((col >> 2) ^ row) & 7u) << 4) + ((col & 3u) << 2);
+}
+
+}  // namespace tc
+}  // namespace kda
