@@ -86,7 +86,9 @@ typedef struct {
  *   q, k          [T, H, d_k]  dtype        (q and k are used as given; the
  *                                            caller normalises them)
  *   v             [T, H, d_v]  dtype
- *   log_alpha     [T, H, d_k]  float32      finite and <= 0 (log retention)
+ *   log_alpha     [T, H, d_k]  float32      finite and <= 0 (log retention);
+ *                                            16-byte aligned for the tensor-core
+ *                                            engine
  *   beta          [T, H]       float32      finite write strength
  *   scale                      host float   applied to q (pass d_k^-1/2 for
  *                                            the usual 1/sqrt(d_k) read)

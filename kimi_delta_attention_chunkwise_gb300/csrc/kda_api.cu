@@ -102,6 +102,9 @@ kdaStatus_t plan_chunk(const void *q, const void *k, const void *v, const float 
         case KDA_ENGINE_SIMT: use_tc = false; break;
         default: use_tc = tc_eligible(shape, C); break;
     }
+    // The tensor-core engine reads log_alpha through a TMA tensor map, whose
+    // base must be 16-byte aligned.
+    if (use_tc && shape->total_tokens > 0 && !aligned16(log_alpha)) return KDA_ERR_INVALID_ARG;
     ChunkArgs &a = plan->args;
     a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.scale = scale;
     a.initial_state = initial_state; a.cu_seqlens = cu_seqlens; a.out = out;

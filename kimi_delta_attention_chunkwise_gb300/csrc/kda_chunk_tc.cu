@@ -45,6 +45,8 @@
 // (decays stronger than ~exp(-80) across half a chunk) takes a CUDA-core path
 // that evaluates every exp(G_i - G_j) directly, so any finite gates <= 0 work.
 #include <cstdint>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
 #include "kda_internal.cuh"
@@ -162,23 +164,34 @@ __device__ __forceinline__ int32_t find_seq(const int32_t *off, int32_t N, int32
 // ---------------------------------------------------------------------------
 // 2. per-(chunk, head) preparation
 // ---------------------------------------------------------------------------
-// Shared memory, with regions reused once their first tenant is done:
-//   a1: tf32 [K_tilde ; Q_tilde], 128 rows x 128 K in 4 panels (64 KB);
-//       after that MMA: R, X (= A^kk) and the solve's block products (fp32).
-//   b1: tf32 K_hat, 64 rows x 128 K in 4 panels (32 KB) (slow path: G fp32
-//       [64][128]); after that: A^kk f16 panel (8 KB) and
-//       (beta Gamma K)^T f16 panel, 128 rows x 64 K (16 KB).
+// 256 threads: thread t owns key channel d = t % 128 for the tokens of one
+// half chunk (t / 128).  Shared memory, with regions reused once their
+// first tenant is done:
+//   a1: g tile (TMA, f32 [64][128]) -> tf32 [K_tilde ; Q_tilde], 128 rows x
+//       128 K in 4 panels (64 KB) -> R, X (= A^kk) and the solve's block
+//       products (fp32);
+//   b1: k and q tiles (TMA, bf16 [64][128] each) -> tf32 K_hat, 64 rows x
+//       128 K in 4 panels (32 KB) (slow path: G f32 [64][128]) -> A^kk f16
+//       panel (8 KB) and (beta Gamma K)^T f16 panel, 128 rows x 64 K (16 KB).
+constexpr int kPrepThreads = 256;
+constexpr int HALF = C / 2;
+
 struct PrepSmem {
     uint8_t a1[4 * 16384];
     uint8_t b1[4 * 8192];
     float beta[C];
-    uint64_t bar;
+    float gcarry[D];   // G at token 31 of each channel
+    float gmid[D];     // G at the reference token MID
+    float glast[D];    // G at the chunk's last token
+    uint64_t bar_in, bar_mma;
     uint32_t tmem;
 };
 constexpr uint32_t kOffX = C * (C + 1) * 4;        // X after R inside a1
 constexpr uint32_t kOffTb = 2 * C * (C + 1) * 4;   // block products after X
 constexpr uint32_t kOffA2 = 8192;                  // (beta Gamma K)^T after A^kk inside b1
+constexpr uint32_t kInBytes = 2 * C * D * 2 + C * D * 4;  // k, q bf16 + g f32 tiles
 static_assert(kOffTb + 3 * 16 * 17 * 4 <= 4 * 16384, "a1 reuse");
+static_assert(MID == HALF, "the reference token opens the second half");
 
 __device__ __forceinline__ void store_row_f16_image(uint8_t *img, uint32_t row,
                                                     const float (&v)[64]) {
@@ -194,9 +207,27 @@ __device__ __forceinline__ void store_row_f16_image(uint8_t *img, uint32_t row,
     }
 }
 
-__global__ void __launch_bounds__(128)
-chunk_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-                  const float *__restrict__ log_alpha, const float *__restrict__ beta,
+// Four 16-byte chunks (32 consecutive f16 values) of one swizzled row.
+__device__ __forceinline__ void store_quarter_f16_image(uint8_t *img, uint32_t row,
+                                                       uint32_t chunk0, const float (&v)[32]) {
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+        uint4 u;
+        u.x = pack_f16x2(v[c4 * 8 + 0], v[c4 * 8 + 1]);
+        u.y = pack_f16x2(v[c4 * 8 + 2], v[c4 * 8 + 3]);
+        u.z = pack_f16x2(v[c4 * 8 + 4], v[c4 * 8 + 5]);
+        u.w = pack_f16x2(v[c4 * 8 + 6], v[c4 * 8 + 7]);
+        *reinterpret_cast<uint4 *>(img + sw128_chunk(row, chunk0 + c4)) = u;
+    }
+}
+
+struct PrepMaps {
+    CUtensorMap q, k, g;  // [T, H, D] viewed as {D, H, T}, box {128, 1, 64}
+};
+
+__global__ void __launch_bounds__(kPrepThreads, 2)
+chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__restrict__ q,
+                  const __nv_bfloat16 *__restrict__ k, const float *__restrict__ beta,
                   float scale, const int32_t *__restrict__ cu, int32_t N, int32_t T, int32_t H,
                   Scratch sc, int *status) {
     extern __shared__ uint8_t smem_raw[];
@@ -223,13 +254,17 @@ chunk_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__re
     uint8_t *ak = sc.ak + ch * AK_BYTES;
     uint8_t *aq = sc.aq + ch * AQ_BYTES;
     float *gb = reinterpret_cast<float *>(sc.gb + ch * GB_BYTES);
-    const __nv_bfloat16 *kc = k + ((size_t)t0 * H + h) * D;  // row i at kc + i*H*D
-    const __nv_bfloat16 *qc = q + ((size_t)t0 * H + h) * D;
     const size_t rs = (size_t)H * D;
 
+    // Stream the chunk's k, q and log-decay tiles in (one tensor load each).
     if (tid == 0) {
-        mbar_init(&sm.bar, 1);
+        mbar_init(&sm.bar_in, 1);
+        mbar_init(&sm.bar_mma, 1);
         fence_mbar_init();
+        mbar_arrive_expect_tx(&sm.bar_in, kInBytes);
+        tma_load_3d(sm.b1, &maps.k, 0, h, t0, &sm.bar_in);
+        tma_load_3d(sm.b1 + C * D * 2, &maps.q, 0, h, t0, &sm.bar_in);
+        tma_load_3d(sm.a1, &maps.g, 0, h, t0, &sm.bar_in);
     }
     if (warp == 0) {
         tmem_alloc(&sm.tmem, 128);
@@ -241,35 +276,65 @@ chunk_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__re
         sm.beta[tid] = b;
         gb[128 + tid] = b;
     }
-
-    // sec. 6.1: chunk-local cumulative log decay of key channel d = tid.
-    const int d = tid;
-    float G[C];
-    {
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < C; ++i) {
-            acc += (i < L) ? log_alpha[(size_t)i * rs + ((size_t)t0 * H + h) * D + d] : 0.f;
-            G[i] = acc;
-        }
-    }
-    const float Gm = G[MID], Gl = G[C - 1];
-    float span = 0.f;
-#pragma unroll
-    for (int i = 0; i < C; ++i) span = fmaxf(span, fabsf(G[i] - Gm));
-    const int slow = __syncthreads_or(!(span <= kSpanLimit));
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem;
+    bool ok = mbar_wait_bounded(&sm.bar_in, 0, kWaitCycles);
+
+    const int d = tid & (D - 1), hf = tid >> 7, i0 = hf * HALF;
+    uint32_t kp[HALF / 2], qp[HALF / 2];
+    float G[HALF];
+    {
+        const float *gs = reinterpret_cast<const float *>(sm.a1);
+        const unsigned short *ks = reinterpret_cast<const unsigned short *>(sm.b1);
+        const unsigned short *qs = ks + C * D;
+#pragma unroll
+        for (int jj = 0; jj < HALF / 2; ++jj) {
+            const int ia = i0 + 2 * jj, ib = ia + 1;
+            const uint32_t k0 = ia < L ? ks[ia * D + d] : 0u, k1 = ib < L ? ks[ib * D + d] : 0u;
+            const uint32_t q0 = ia < L ? qs[ia * D + d] : 0u, q1 = ib < L ? qs[ib * D + d] : 0u;
+            kp[jj] = k0 | (k1 << 16);
+            qp[jj] = q0 | (q1 << 16);
+        }
+        float acc = 0.f;
+#pragma unroll
+        for (int ii = 0; ii < HALF; ++ii) {
+            acc += (i0 + ii < L) ? gs[(i0 + ii) * D + d] : 0.f;
+            G[ii] = acc;
+        }
+    }
+    if (hf == 0) sm.gcarry[d] = G[HALF - 1];
+    __syncthreads();  // staging consumed; carries published
+    if (hf == 1) {
+        const float carry = sm.gcarry[d];
+#pragma unroll
+        for (int ii = 0; ii < HALF; ++ii) G[ii] += carry;
+        sm.gmid[d] = G[0];
+        sm.glast[d] = G[HALF - 1];
+    }
+    __syncthreads();
+    const float Gm = sm.gmid[d], Gl = sm.glast[d];
+    float span = 0.f;
+#pragma unroll
+    for (int ii = 0; ii < HALF; ++ii) span = fmaxf(span, fabsf(G[ii] - Gm));
+    const int slow = __syncthreads_or(!(span <= kSpanLimit));
+    auto kval = [&](int ii) {
+        return __uint_as_float((ii & 1) ? (kp[ii >> 1] & 0xFFFF0000u) : (kp[ii >> 1] << 16));
+    };
+    auto qval = [&](int ii) {
+        return __uint_as_float((ii & 1) ? (qp[ii >> 1] & 0xFFFF0000u) : (qp[ii >> 1] << 16));
+    };
     uint32_t mma_phase = 0;
-    bool ok = true;
 
     if (slow) {
         // CUDA-core path: every exp(G_i - G_j) taken directly (exponent <= 0).
         float *Gs = reinterpret_cast<float *>(sm.b1);  // [64][128]
 #pragma unroll
-        for (int i = 0; i < C; ++i) Gs[i * D + d] = G[i];
+        for (int ii = 0; ii < HALF; ++ii) Gs[(i0 + ii) * D + d] = G[ii];
         __syncthreads();
-        for (int i = warp; i < C; i += 4) {
+        const __nv_bfloat16 *kc = k + ((size_t)t0 * H + h) * D;
+        const __nv_bfloat16 *qc = q + ((size_t)t0 * H + h) * D;
+        for (int i = warp; i < C; i += kPrepThreads / 32) {
             for (int j = 0; j <= i; ++j) {
                 float r = 0.f, a = 0.f;
                 if (i < L) {
@@ -314,13 +379,12 @@ chunk_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__re
         uint8_t *qrow = wq + (d >> 6) * 16384u;
         float kend[8];
 #pragma unroll
-        for (int i = 0; i < C; ++i) {
-            const bool in = i < L;
-            const float kv = in ? __bfloat162float(kc[i * rs + d]) : 0.f;
-            const float qv = in ? __bfloat162float(qc[i * rs + d]) : 0.f;
+        for (int ii = 0; ii < HALF; ++ii) {
+            const int i = i0 + ii;
+            const float kv = kval(ii), qv = qval(ii);
             float gam, eend;
             if (!slow) {
-                const float ep = __expf(G[i] - Gm), en = __expf(Gm - G[i]);
+                const float ep = __expf(G[ii] - Gm), en = __expf(Gm - G[ii]);
                 gam = ep * e_m;
                 eend = e_lm * en;
                 *reinterpret_cast<float *>(sm.a1 + pa + sw128_offset_f32(i, d & 31)) =
@@ -330,21 +394,21 @@ chunk_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__re
                 *reinterpret_cast<float *>(sm.b1 + pb + sw128_offset_f32(i, d & 31)) =
                     to_tf32(kv * en);
             } else {
-                gam = __expf(G[i]);
-                eend = __expf(Gl - G[i]);
+                gam = __expf(G[ii]);
+                eend = __expf(Gl - G[ii]);
             }
             // Q_hat = s Gamma q -> rows 64..127 of the [-W ; Q_hat] image
             *reinterpret_cast<__half *>(qrow + sw128_offset(64 + i, d & 63)) =
                 __float2half_rn(scale * gam * qv);
-            kend[i & 7] = eend * kv;
-            if ((i & 7) == 7) {
+            kend[ii & 7] = eend * kv;
+            if ((ii & 7) == 7) {
                 uint4 u;
                 u.x = pack_f16x2(kend[0], kend[1]); u.y = pack_f16x2(kend[2], kend[3]);
                 u.z = pack_f16x2(kend[4], kend[5]); u.w = pack_f16x2(kend[6], kend[7]);
                 *reinterpret_cast<uint4 *>(ke + sw128_chunk(d, i >> 3)) = u;
             }
         }
-        gb[d] = slow ? __expf(Gl) : e_lm * e_m;
+        if (hf == 0) gb[d] = slow ? __expf(Gl) : e_lm * e_m;
     }
 
     if (!slow) {
@@ -352,38 +416,45 @@ chunk_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__re
         tc_fence_before();
         __syncthreads();
         // [K_tilde ; Q_tilde] K_hat^T on the tensor core (tf32): TMEM cols 0..63.
-        if (tid == 0) {
+        if (tid == 0 && ok) {
             tc_fence_after();
             mma_panels<true>(tmem, smem_u32(sm.a1), 16384, smem_u32(sm.b1), 8192, 16,
                              idesc_tf32_f32(128, 64), false);
-            mma_commit(&sm.bar);
+            mma_commit(&sm.bar_mma);
         }
-        ok = mbar_wait_bounded(&sm.bar, mma_phase, kWaitCycles);
+        if (ok) ok = mbar_wait_bounded(&sm.bar_mma, mma_phase, kWaitCycles);
         mma_phase ^= 1;
         tc_fence_after();
-        float v[64];
+        // warp w reads TMEM lanes 32*(w%4).., columns 32*(w/4)..
+        const int quad = warp & 3, chalf = warp >> 2, r = quad * 32 + lane;
+        float v[32];
         if (ok) {
-            tmem_ld32(tmem_addr(tmem, warp * 32, 0), *reinterpret_cast<float(*)[32]>(&v[0]));
-            tmem_ld32(tmem_addr(tmem, warp * 32, 32), *reinterpret_cast<float(*)[32]>(&v[32]));
+            tmem_ld32(tmem_addr(tmem, quad * 32, chalf * 32), v);
         } else {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) v[j] = 0.f;
+            for (int j = 0; j < 32; ++j) v[j] = 0.f;
         }
-        __syncthreads();  // a1 is free: the operands were consumed by the MMA
-        if (warp < 2) {
-            const int i = tid;  // key-key row
+        __syncthreads();  // a1 is free: the MMA consumed its operands
+        if (r < C) {
+            const int i = r;  // key-key row
             const float b = sm.beta[i];
 #pragma unroll
-            for (int j = 0; j < C; ++j) R[i][j] = (j < i && i < L) ? b * v[j] : 0.f;
+            for (int jj = 0; jj < 32; ++jj) {
+                const int j = chalf * 32 + jj;
+                R[i][j] = (j < i && i < L) ? b * v[jj] : 0.f;
+            }
         } else {
-            const int i = tid - 64;  // query-key row
-            float row[64];
+            const int i = r - C;  // query-key row
+            float row[32];
 #pragma unroll
-            for (int j = 0; j < C; ++j) row[j] = (j <= i && i < L) ? scale * v[j] : 0.f;
-            store_row_f16_image(aq, i, row);
+            for (int jj = 0; jj < 32; ++jj) {
+                const int j = chalf * 32 + jj;
+                row[jj] = (j <= i && i < L) ? scale * v[jj] : 0.f;
+            }
+            store_quarter_f16_image(aq, i, chalf * 4, row);
         }
     }
-    for (int idx = tid; idx < C * (C + 1); idx += 128) (&X[0][0])[idx] = 0.f;
+    for (int idx = tid; idx < C * (C + 1); idx += kPrepThreads) (&X[0][0])[idx] = 0.f;
     __syncthreads();
 
     // sec. 6.3: A^kk = (I + R)^-1, unit lower triangular, fp32, 16 x 16 blocks.
@@ -406,7 +477,7 @@ chunk_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__re
     for (int dist = 1; dist < 4; ++dist) {
         const int nblk = 4 - dist;
         // T_IJ = sum_{K=J}^{I-1} R_IK X_KJ
-        for (int e = tid; e < nblk * 256; e += 128) {
+        for (int e = tid; e < nblk * 256; e += kPrepThreads) {
             const int bi = e >> 8, r = (e >> 4) & 15, cc = e & 15;
             const int I = bi + dist, J = bi;
             float acc2 = 0.f;
@@ -419,7 +490,7 @@ chunk_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__re
         }
         __syncthreads();
         // X_IJ = -X_II T_IJ
-        for (int e = tid; e < nblk * 256; e += 128) {
+        for (int e = tid; e < nblk * 256; e += kPrepThreads) {
             const int bi = e >> 8, r = (e >> 4) & 15, cc = e & 15;
             const int I = bi + dist, J = bi;
             float acc2 = 0.f;
@@ -429,27 +500,20 @@ chunk_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__re
         }
         __syncthreads();
     }
-    if (tid < C) {
-        float row[64];
+    if (tid < 2 * C) {
+        const int row = tid >> 1, q4 = tid & 1;
+        float v32[32];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) row[j] = X[tid][j];
-        store_row_f16_image(b2, tid, row);
-        store_row_f16_image(ak, tid, row);
+        for (int j = 0; j < 32; ++j) v32[j] = X[row][q4 * 32 + j];
+        store_quarter_f16_image(b2, row, q4 * 4, v32);
+        store_quarter_f16_image(ak, row, q4 * 4, v32);
     }
-    // (beta Gamma K)^T, row d, f16
+    // (beta Gamma K)^T, row d, this thread's half of the tokens, f16
     {
-        float bgk[8];
+        float bgk[32];
 #pragma unroll
-        for (int i = 0; i < C; ++i) {
-            const float kv = (i < L) ? __bfloat162float(kc[i * rs + d]) : 0.f;
-            bgk[i & 7] = sm.beta[i] * __expf(G[i]) * kv;
-            if ((i & 7) == 7) {
-                uint4 u;
-                u.x = pack_f16x2(bgk[0], bgk[1]); u.y = pack_f16x2(bgk[2], bgk[3]);
-                u.z = pack_f16x2(bgk[4], bgk[5]); u.w = pack_f16x2(bgk[6], bgk[7]);
-                *reinterpret_cast<uint4 *>(a2 + sw128_chunk(d, i >> 3)) = u;
-            }
-        }
+        for (int ii = 0; ii < HALF; ++ii) bgk[ii] = sm.beta[i0 + ii] * __expf(G[ii]) * kval(ii);
+        store_quarter_f16_image(a2, d, hf * 4, bgk);
     }
     fence_proxy_async();
     tc_fence_before();
@@ -460,19 +524,20 @@ chunk_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__re
         tc_fence_after();
         mma_panels(tmem + 64, smem_u32(a2), 0, smem_u32(b2), 0, 4, idesc_f16_f32(128, 64),
                    false);
-        mma_commit(&sm.bar);
+        mma_commit(&sm.bar_mma);
     }
-    if (ok) ok = mbar_wait_bounded(&sm.bar, mma_phase, kWaitCycles);
+    if (ok) ok = mbar_wait_bounded(&sm.bar_mma, mma_phase, kWaitCycles);
     tc_fence_after();
     if (ok) {
-        float v[64];
-        tmem_ld32(tmem_addr(tmem, warp * 32, 64), *reinterpret_cast<float(*)[32]>(&v[0]));
-        tmem_ld32(tmem_addr(tmem, warp * 32, 96), *reinterpret_cast<float(*)[32]>(&v[32]));
-        // thread = key channel d, v[i] = W[i][d]; store -W into rows 0..63.
-        uint8_t *pnl = wq + (d >> 6) * 16384u;
+        const int quad = warp & 3, chalf = warp >> 2, dd = quad * 32 + lane;
+        float v[32];
+        tmem_ld32(tmem_addr(tmem, quad * 32, 64 + chalf * 32), v);
+        // thread = key channel dd, v[jj] = W[i][dd] for i = 32*chalf + jj; store -W.
+        uint8_t *pnl = wq + (dd >> 6) * 16384u;
 #pragma unroll
-        for (int i = 0; i < C; ++i)
-            *reinterpret_cast<__half *>(pnl + sw128_offset(i, d & 63)) = __float2half_rn(-v[i]);
+        for (int jj = 0; jj < 32; ++jj)
+            *reinterpret_cast<__half *>(pnl + sw128_offset(chalf * 32 + jj, dd & 63)) =
+                __float2half_rn(-v[jj]);
     } else if (tid == 0) {
         atomicExch(status, (int)KDA_ERR_TIMEOUT);
     }
@@ -488,9 +553,8 @@ struct ScanStage {
     uint8_t wq[WQ_BYTES];        // [-W ; Q_hat]
     uint8_t ke[KE_BYTES];        // K_end^T
     uint8_t aa[3 * 8192];        // [A^kk | zeros | A^qk]
-    uint8_t v[C * BV * 2];       // value tile rows, bf16 [64][32]
     float gb[GB_BYTES / 4];      // Gamma_last [128], beta [64]
-    uint8_t pad[1024 - (GB_BYTES % 1024) - (C * BV * 2) % 1024];
+    uint8_t pad[1024 - GB_BYTES % 1024];
 };
 
 struct ScanSmem {
@@ -498,14 +562,21 @@ struct ScanSmem {
     uint8_t sbt[2 * 4096];       // S_c^T f16: 32 rows x 128 K, 2 panels
     uint8_t ebt[4096];           // E^T f16: 32 rows x 64 K
     uint8_t bvt[4096];           // (beta V)^T f16: 32 rows x 64 K
-    uint64_t full[2];
-    uint64_t mma;
+    uint64_t full[2];            // stage loaded (producer -> compute)
+    uint64_t empty[2];           // stage released (compute -> producer)
+    uint64_t mma_e, mma_s, mma_o;  // MMA groups done: E, state increment, outputs
     uint32_t tmem;
-    int32_t abort_flag;
+    volatile int32_t abort_flag;
 };
 
+constexpr int kScanThreads = 160;  // warps 0-3 compute, warp 4 streams operands in
+
+__device__ __forceinline__ void compute_barrier() {
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
 template <typename TOut>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kScanThreads, 1)
 chunk_scan_kernel(const __nv_bfloat16 *__restrict__ v, const float *__restrict__ initial_state,
                   const int32_t *__restrict__ cu, TOut *__restrict__ out,
                   float *__restrict__ final_state, int32_t N, int32_t T, int32_t H, Scratch sc,
@@ -519,11 +590,11 @@ chunk_scan_kernel(const __nv_bfloat16 *__restrict__ v, const float *__restrict__
     seq_bounds(cu, seq, T, ta, tb);
     const int32_t c_begin = sc.chunk_off[seq];
     const int32_t n_chunks = (tb - ta + C - 1) / C;
-    const size_t state_off = (((size_t)seq * H + h) * D + tid) * D + (size_t)vt * BV;
+    const size_t state_off = (((size_t)seq * H + h) * D + (tid & 127)) * D + (size_t)vt * BV;
 
-    // state row of key channel tid, 32 value columns, fp32
+    // state row of key channel tid (compute threads), 32 value columns, fp32
     float S[BV];
-    if (initial_state) {
+    if (tid < 128 && initial_state) {
 #pragma unroll
         for (int j = 0; j < BV; j += 4) {
             const float4 x = *reinterpret_cast<const float4 *>(initial_state + state_off + j);
@@ -534,19 +605,21 @@ chunk_scan_kernel(const __nv_bfloat16 *__restrict__ v, const float *__restrict__
         for (int j = 0; j < BV; ++j) S[j] = 0.f;
     }
 
+    bool ok = true;
     if (n_chunks > 0) {
-        // zero the constant zero blocks and the value tiles (rows past a
-        // partial chunk are never loaded and must stay finite)
-        for (int st = 0; st < 2; ++st) {
-            uint4 *z = reinterpret_cast<uint4 *>(sm.st[st].aa + 8192);
-            for (int idx = tid; idx < 8192 / 16; idx += 128) z[idx] = make_uint4(0, 0, 0, 0);
-            uint4 *zv = reinterpret_cast<uint4 *>(sm.st[st].v);
-            for (int idx = tid; idx < (C * BV * 2) / 16; idx += 128) zv[idx] = make_uint4(0, 0, 0, 0);
+        // zero the constant zero blocks
+        for (int stg = 0; stg < 2; ++stg) {
+            uint4 *z = reinterpret_cast<uint4 *>(sm.st[stg].aa + 8192);
+            for (int idx = tid; idx < 8192 / 16; idx += kScanThreads) z[idx] = make_uint4(0, 0, 0, 0);
         }
         if (tid == 0) {
-            mbar_init(&sm.full[0], 1);
-            mbar_init(&sm.full[1], 1);
-            mbar_init(&sm.mma, 1);
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&sm.full[i], 1);
+                mbar_init(&sm.empty[i], 1);
+            }
+            mbar_init(&sm.mma_e, 1);
+            mbar_init(&sm.mma_s, 1);
+            mbar_init(&sm.mma_o, 1);
             sm.abort_flag = 0;
             fence_mbar_init();
         }
@@ -562,146 +635,176 @@ chunk_scan_kernel(const __nv_bfloat16 *__restrict__ v, const float *__restrict__
         const uint32_t d1 = tmem, d2 = tmem + 32;
         constexpr uint32_t IDESC = idesc_f16_f32(128, BV);
 
-        auto issue = [&](int32_t n, int stg) {
-            // warp 0: expect the bytes, then the copies of chunk n into stage stg
-            const int32_t t0 = ta + n * C;
-            const int32_t L = min(C, tb - t0);
-            const size_t ch = (size_t)(c_begin + n) * H + h;
-            ScanStage &S_ = sm.st[stg];
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&sm.full[stg],
-                                      WQ_BYTES + KE_BYTES + AK_BYTES + AQ_BYTES + GB_BYTES +
-                                          (uint32_t)L * BV * 2);
-                bulk_g2s(S_.wq, sc.wq + ch * WQ_BYTES, WQ_BYTES, &sm.full[stg]);
-                bulk_g2s(S_.ke, sc.ke + ch * KE_BYTES, KE_BYTES, &sm.full[stg]);
-                bulk_g2s(S_.aa, sc.ak + ch * AK_BYTES, AK_BYTES, &sm.full[stg]);
-                bulk_g2s(S_.aa + 16384, sc.aq + ch * AQ_BYTES, AQ_BYTES, &sm.full[stg]);
-                bulk_g2s(S_.gb, sc.gb + ch * GB_BYTES, GB_BYTES, &sm.full[stg]);
-            }
-            __syncwarp();
-            for (int i = lane; i < L; i += 32)
-                bulk_g2s(S_.v + i * BV * 2, v + ((size_t)(t0 + i) * H + h) * D + vt * BV,
-                         BV * 2, &sm.full[stg]);
-        };
-
-        if (warp == 0) {
-            issue(0, 0);
-            if (n_chunks > 1) issue(1, 1);
-        }
-        uint32_t mma_phase = 0;
-        bool ok = true;
-
-        for (int32_t n = 0; n < n_chunks; ++n) {
-            const int stg = n & 1;
-            ScanStage &st = sm.st[stg];
-            const int32_t t0 = ta + n * C;
-            const int32_t L = min(C, tb - t0);
-
-            ok = mbar_wait_bounded(&sm.full[stg], (n >> 1) & 1, kWaitCycles);
-            if (__syncthreads_or(!ok)) break;
-
-            // (beta V)^T operand: thread -> token row i = tid/2, 16 value columns
-            {
-                const int i = tid >> 1, j0 = (tid & 1) * 16;
-                const float b = st.gb[128 + i];
-                const __nv_bfloat16 *vr = reinterpret_cast<const __nv_bfloat16 *>(st.v) + i * BV + j0;
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    *reinterpret_cast<__half *>(sm.bvt + sw128_offset(j0 + j, i)) =
-                        __float2half_rn(b * __bfloat162float(vr[j]));
-            }
-            // S_c^T operand (f16): thread = key row tid
-            {
-                uint8_t *pnl = sm.sbt + (tid >> 6) * 4096;
-#pragma unroll
-                for (int j = 0; j < BV; ++j)
-                    *reinterpret_cast<__half *>(pnl + sw128_offset(j, tid & 63)) =
-                        __float2half_rn(S[j]);
-            }
-            fence_proxy_async();
-            tc_fence_before();
-            __syncthreads();
-            if (tid == 0) {
-                tc_fence_after();
-                // D1 = [A^kk ; 0] (beta V)      -> rows 0..63: U, rows 64..127: 0
-                mma_panels(d1, smem_u32(st.aa), 0, smem_u32(sm.bvt), 0, 4, IDESC, false);
-                // D1 += [-W ; Q_hat] S_c       -> rows 0..63: E, rows 64..127: Q_hat S_c
-                mma_panels(d1, smem_u32(st.wq), 16384, smem_u32(sm.sbt), 4096, 8, IDESC, true);
-                mma_commit(&sm.mma);
-            }
-            ok = mbar_wait_bounded(&sm.mma, mma_phase, kWaitCycles);
-            mma_phase ^= 1;
-            if (__syncthreads_or(!ok)) break;
-            tc_fence_after();
-            if (warp < 2) {
-                float e[32];
-                tmem_ld32(tmem_addr(d1, warp * 32, 0), e);
-                const int i = tid;  // token row
-#pragma unroll
-                for (int j = 0; j < BV; ++j)
-                    *reinterpret_cast<__half *>(sm.ebt + sw128_offset(j, i)) =
-                        __float2half_rn(e[j]);
-            }
-            fence_proxy_async();
-            tc_fence_before();
-            __syncthreads();
-            if (tid == 0) {
-                tc_fence_after();
-                // D2 = K_end^T E  (state increment)
-                mma_panels(d2, smem_u32(st.ke), 0, smem_u32(sm.ebt), 0, 4, IDESC, false);
-                // D1 += [0 ; A^qk] E  -> rows 64..127: outputs
-                mma_panels(d1, smem_u32(st.aa) + 8192, 0, smem_u32(sm.ebt), 0, 4, IDESC, true);
-                mma_commit(&sm.mma);
-            }
-            ok = mbar_wait_bounded(&sm.mma, mma_phase, kWaitCycles);
-            mma_phase ^= 1;
-            if (__syncthreads_or(!ok)) break;
-            tc_fence_after();
-            {
-                float ds[32];
-                tmem_ld32(tmem_addr(d2, warp * 32, 0), ds);
-                const float g = st.gb[tid];
-#pragma unroll
-                for (int j = 0; j < BV; ++j) S[j] = fmaf(g, S[j], ds[j]);
-            }
-            if (warp >= 2) {
-                float o[32];
-                tmem_ld32(tmem_addr(d1, warp * 32, 0), o);
-                const int i = tid - 64;
-                if (i < L) {
-                    TOut *dst = out + ((size_t)(t0 + i) * H + h) * D + vt * BV;
-                    if constexpr (sizeof(TOut) == 2) {
-#pragma unroll
-                        for (int j = 0; j < BV; j += 8) {
-                            uint4 u;
-                            u.x = pack_bf16x2(o[j], o[j + 1]); u.y = pack_bf16x2(o[j + 2], o[j + 3]);
-                            u.z = pack_bf16x2(o[j + 4], o[j + 5]); u.w = pack_bf16x2(o[j + 6], o[j + 7]);
-                            *reinterpret_cast<uint4 *>(dst + j) = u;
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < BV; j += 4)
-                            *reinterpret_cast<float4 *>(dst + j) =
-                                make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+        if (warp == 4) {
+            // ---------------- producer: stream each chunk's operands in ----------------
+            for (int32_t n = 0; n < n_chunks; ++n) {
+                const int stg = n & 1;
+                if (n >= 2) {
+                    const bool got = mbar_wait_bounded(&sm.empty[stg], ((n >> 1) - 1) & 1,
+                                                       kWaitCycles);
+                    if (!got || sm.abort_flag) {
+                        sm.abort_flag = 1;
+                        break;
                     }
                 }
+                const size_t ch = (size_t)(c_begin + n) * H + h;
+                ScanStage &S_ = sm.st[stg];
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&sm.full[stg],
+                                          WQ_BYTES + KE_BYTES + AK_BYTES + AQ_BYTES + GB_BYTES);
+                    bulk_g2s(S_.wq, sc.wq + ch * WQ_BYTES, WQ_BYTES, &sm.full[stg]);
+                    bulk_g2s(S_.ke, sc.ke + ch * KE_BYTES, KE_BYTES, &sm.full[stg]);
+                    bulk_g2s(S_.aa, sc.ak + ch * AK_BYTES, AK_BYTES, &sm.full[stg]);
+                    bulk_g2s(S_.aa + 16384, sc.aq + ch * AQ_BYTES, AQ_BYTES, &sm.full[stg]);
+                    bulk_g2s(S_.gb, sc.gb + ch * GB_BYTES, GB_BYTES, &sm.full[stg]);
+                }
+                __syncwarp();
             }
-            tc_fence_before();
-            __syncthreads();
-            if (warp == 0 && n + 2 < n_chunks) issue(n + 2, stg);
+        } else {
+            // ---------------- compute warps ----------------
+            // value tile of a chunk: thread -> token row tid/2, 16 columns (32 B),
+            // prefetched into registers one chunk ahead
+            const int vi = tid >> 1, vj0 = (tid & 1) * 16;
+            auto load_v = [&](int32_t n, uint4 &p0, uint4 &p1) {
+                const int32_t t0n = ta + n * C;
+                if (n < n_chunks && vi < min(C, tb - t0n)) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(
+                        v + ((size_t)(t0n + vi) * H + h) * D + vt * BV + vj0);
+                    p0 = __ldg(src);
+                    p1 = __ldg(src + 1);
+                } else {
+                    p0 = make_uint4(0, 0, 0, 0);
+                    p1 = p0;
+                }
+            };
+            uint4 vnext0, vnext1;
+            load_v(0, vnext0, vnext1);
+            for (int32_t n = 0; n < n_chunks; ++n) {
+                const int stg = n & 1;
+                ScanStage &st = sm.st[stg];
+                const int32_t t0 = ta + n * C;
+                const int32_t L = min(C, tb - t0);
+                const uint32_t par = n & 1;
+
+                if (!mbar_wait_bounded(&sm.full[stg], (n >> 1) & 1, kWaitCycles))
+                    sm.abort_flag = 1;
+
+                // (beta V)^T operand: thread -> token row i = tid/2, 16 value columns
+                {
+                    const int i = vi, j0 = vj0;
+                    const float b = st.gb[128 + i];
+                    const uint4 p0 = vnext0, p1 = vnext1;
+                    load_v(n + 1, vnext0, vnext1);
+                    const uint32_t w[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        const float lo = __uint_as_float(w[jj] << 16);
+                        const float hi = __uint_as_float(w[jj] & 0xFFFF0000u);
+                        *reinterpret_cast<__half *>(sm.bvt + sw128_offset(j0 + 2 * jj, i)) =
+                            __float2half_rn(b * lo);
+                        *reinterpret_cast<__half *>(sm.bvt + sw128_offset(j0 + 2 * jj + 1, i)) =
+                            __float2half_rn(b * hi);
+                    }
+                }
+                // S_c^T operand (f16): thread = key row tid
+                {
+                    uint8_t *pnl = sm.sbt + (tid >> 6) * 4096;
+#pragma unroll
+                    for (int j = 0; j < BV; ++j)
+                        *reinterpret_cast<__half *>(pnl + sw128_offset(j, tid & 63)) =
+                            __float2half_rn(S[j]);
+                }
+                fence_proxy_async();
+                tc_fence_before();
+                compute_barrier();
+                if (sm.abort_flag) break;
+                if (tid == 0) {
+                    tc_fence_after();
+                    if (n > 0) mbar_arrive(&sm.empty[(n - 1) & 1]);  // chunk n-1 fully consumed
+                    // D1 = [A^kk ; 0] (beta V)      -> rows 0..63: U, rows 64..127: 0
+                    mma_panels(d1, smem_u32(st.aa), 0, smem_u32(sm.bvt), 0, 4, IDESC, false);
+                    // D1 += [-W ; Q_hat] S_c       -> rows 0..63: E, rows 64..127: Q_hat S_c
+                    mma_panels(d1, smem_u32(st.wq), 16384, smem_u32(sm.sbt), 4096, 8, IDESC, true);
+                    mma_commit(&sm.mma_e);
+                }
+                if (!mbar_wait_bounded(&sm.mma_e, par, kWaitCycles)) sm.abort_flag = 1;
+                tc_fence_after();
+                if (warp < 2) {
+                    float e[32];
+                    tmem_ld32(tmem_addr(d1, warp * 32, 0), e);
+                    const int i = tid;  // token row
+#pragma unroll
+                    for (int j = 0; j < BV; ++j)
+                        *reinterpret_cast<__half *>(sm.ebt + sw128_offset(j, i)) =
+                            __float2half_rn(e[j]);
+                }
+                fence_proxy_async();
+                tc_fence_before();
+                compute_barrier();
+                if (sm.abort_flag) break;
+                if (tid == 0) {
+                    tc_fence_after();
+                    // D2 = K_end^T E  (state increment)
+                    mma_panels(d2, smem_u32(st.ke), 0, smem_u32(sm.ebt), 0, 4, IDESC, false);
+                    mma_commit(&sm.mma_s);
+                    // D1 += [0 ; A^qk] E  -> rows 64..127: outputs
+                    mma_panels(d1, smem_u32(st.aa) + 8192, 0, smem_u32(sm.ebt), 0, 4, IDESC, true);
+                    mma_commit(&sm.mma_o);
+                }
+                if (!mbar_wait_bounded(&sm.mma_s, par, kWaitCycles)) sm.abort_flag = 1;
+                tc_fence_after();
+                {
+                    float ds[32];
+                    tmem_ld32(tmem_addr(d2, warp * 32, 0), ds);
+                    const float g = st.gb[tid];
+#pragma unroll
+                    for (int j = 0; j < BV; ++j) S[j] = fmaf(g, S[j], ds[j]);
+                }
+                if (warp >= 2) {
+                    if (!mbar_wait_bounded(&sm.mma_o, par, kWaitCycles)) sm.abort_flag = 1;
+                    tc_fence_after();
+                    float o[32];
+                    tmem_ld32(tmem_addr(d1, warp * 32, 0), o);
+                    const int i = tid - 64;
+                    if (i < L) {
+                        TOut *dst = out + ((size_t)(t0 + i) * H + h) * D + vt * BV;
+                        if constexpr (sizeof(TOut) == 2) {
+#pragma unroll
+                            for (int j = 0; j < BV; j += 8) {
+                                uint4 u;
+                                u.x = pack_bf16x2(o[j], o[j + 1]);
+                                u.y = pack_bf16x2(o[j + 2], o[j + 3]);
+                                u.z = pack_bf16x2(o[j + 4], o[j + 5]);
+                                u.w = pack_bf16x2(o[j + 6], o[j + 7]);
+                                *reinterpret_cast<uint4 *>(dst + j) = u;
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < BV; j += 4)
+                                *reinterpret_cast<float4 *>(dst + j) =
+                                    make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+                        }
+                    }
+                }
+                tc_fence_before();
+            }
+            if (sm.abort_flag) ok = false;
         }
-        if (!ok) {
+        __syncthreads();
+        if (sm.abort_flag) {
+            ok = false;
             if (tid == 0) atomicExch(status, (int)KDA_ERR_TIMEOUT);
             // let copies already in flight land before the shared memory goes away
-            for (int stg = 0; stg < 2; ++stg)
-                (void)mbar_wait_bounded(&sm.full[stg], 0, kWaitCycles / 8);
+            if (tid == 0)
+                for (int stg = 0; stg < 2; ++stg)
+                    (void)mbar_wait_bounded(&sm.full[stg], 0, kWaitCycles / 8);
         }
         tc_fence_before();
         __syncthreads();
         if (warp == 0) tmem_dealloc(tmem, 64);
         if (!ok) return;
     }
-    if (final_state) {
+    if (final_state && tid < 128) {
 #pragma unroll
         for (int j = 0; j < BV; j += 4)
             *reinterpret_cast<float4 *>(final_state + state_off + j) =
@@ -721,6 +824,36 @@ size_t chunk_tc_workspace_bytes(int32_t N, int32_t T, int32_t H) {
            align256(((size_t)N + 1) * sizeof(int32_t));
 }
 
+// cuTensorMapEncodeTiled, fetched from the driver once (no libcuda link).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// [T, H, D] row-major tensor as a 3-D map {D, H, T}; box = one head's
+// [64 tokens x 128 channels] tile.  Rows past T read as zero.
+bool encode_tile_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, size_t esize,
+                     int32_t T, int32_t H) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * esize, (cuuint64_t)H * D * esize};
+    const cuuint32_t box[3] = {(cuuint32_t)D, 1u, (cuuint32_t)C};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspace_bytes,
                             cudaStream_t stream) {
     if (workspace_bytes < chunk_tc_workspace_bytes(a.N, a.T, a.H) || !workspace)
@@ -731,34 +864,40 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
-    e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kPrepSmem);
-    if (e != cudaSuccess) return e;
-    const dim3 pgrid((unsigned)max_chunks(a.N, a.T), (unsigned)a.H);
-    chunk_prep_kernel<<<pgrid, 128, kPrepSmem, stream>>>(
-        static_cast<const __nv_bfloat16 *>(a.q), static_cast<const __nv_bfloat16 *>(a.k),
-        a.log_alpha, a.beta, a.scale, a.cu_seqlens, a.N, a.T, a.H, sc, a.status);
+    if (a.T > 0) {
+        PrepMaps maps;
+        if (!encode_tile_map(&maps.q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H) ||
+            !encode_tile_map(&maps.k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H) ||
+            !encode_tile_map(&maps.g, a.log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.T, a.H))
+            return cudaErrorInvalidValue;
+        e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kPrepSmem);
+        if (e != cudaSuccess) return e;
+        const dim3 pgrid((unsigned)max_chunks(a.N, a.T), (unsigned)a.H);
+        chunk_prep_kernel<<<pgrid, kPrepThreads, kPrepSmem, stream>>>(
+            maps, static_cast<const __nv_bfloat16 *>(a.q),
+            static_cast<const __nv_bfloat16 *>(a.k), a.beta, a.scale, a.cu_seqlens, a.N, a.T,
+            a.H, sc, a.status);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     a.clock->mark(stream);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
 
     const dim3 sgrid((unsigned)(a.N * NT), (unsigned)a.H);
     if (a.out_f32) {
         auto kern = chunk_scan_kernel<float>;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
         if (e != cudaSuccess) return e;
-        kern<<<sgrid, 128, kScanSmem, stream>>>(static_cast<const __nv_bfloat16 *>(a.v),
-                                                a.initial_state, a.cu_seqlens,
-                                                static_cast<float *>(a.out), a.final_state, a.N,
-                                                a.T, a.H, sc, a.status);
+        kern<<<sgrid, kScanThreads, kScanSmem, stream>>>(
+            static_cast<const __nv_bfloat16 *>(a.v), a.initial_state, a.cu_seqlens,
+            static_cast<float *>(a.out), a.final_state, a.N, a.T, a.H, sc, a.status);
     } else {
         auto kern = chunk_scan_kernel<__nv_bfloat16>;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
         if (e != cudaSuccess) return e;
-        kern<<<sgrid, 128, kScanSmem, stream>>>(static_cast<const __nv_bfloat16 *>(a.v),
-                                                a.initial_state, a.cu_seqlens,
-                                                static_cast<__nv_bfloat16 *>(a.out),
-                                                a.final_state, a.N, a.T, a.H, sc, a.status);
+        kern<<<sgrid, kScanThreads, kScanSmem, stream>>>(
+            static_cast<const __nv_bfloat16 *>(a.v), a.initial_state, a.cu_seqlens,
+            static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.N, a.T, a.H, sc, a.status);
     }
     a.clock->mark(stream);
     return cudaGetLastError();

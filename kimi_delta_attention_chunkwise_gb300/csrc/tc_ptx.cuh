@@ -50,6 +50,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -84,6 +88,17 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
             "r"(smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Tiled tensor load (TMA), 3-D coordinates {x innermost, y, z}; the tensor
+// map lives in kernel parameter space (__grid_constant__).
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int32_t x, int32_t y,
+                                            int32_t z, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
 }
 
@@ -194,7 +209,7 @@ template <bool TF32 = false>
 __device__ __forceinline__ void mma_panels(uint32_t d_tmem, uint32_t a_base, uint32_t a_panel,
                                            uint32_t b_base, uint32_t b_panel, int ksteps,
                                            uint32_t idesc, bool accumulate_first) {
-#pragma unroll 1
+#pragma unroll
     for (int ks = 0; ks < ksteps; ++ks) {
         const uint32_t a = a_base + (ks >> 2) * a_panel + (ks & 3) * 32;
         const uint32_t b = b_base + (ks >> 2) * b_panel + (ks & 3) * 32;
