@@ -154,6 +154,39 @@ kdaStatus_t kda_chunk_fwd_ws_timed(const void *q, const void *k, const void *v,
                                    int32_t max_events, int32_t *n_recorded);
 
 /*
+ * kda_chunk_fwd_static -- kda_chunk_fwd for callers that cannot allocate
+ * device memory.  No page describes it; it exists for users of this library.
+ *
+ * Some callers are not allowed to allocate device memory when they run
+ * prefill: code inside a host framework that owns every allocation, code on a
+ * latency-critical path where an allocation could synchronise the device, or
+ * services that must keep a fixed footprint after start-up.  This entry point
+ * allocates nothing.  It takes the same arguments as kda_chunk_fwd and runs
+ * the same kernels, with scratch taken from a fixed device array of
+ * KDA_STATIC_SCRATCH_BYTES that the library reserves when it is loaded.
+ *
+ *   - The array is held on every GPU that loads the library, until exit.
+ *   - Problems whose scratch (kda_chunk_fwd_workspace_size) exceeds
+ *     KDA_STATIC_SCRATCH_BYTES are rejected with KDA_ERR_UNSUPPORTED before
+ *     anything runs.  With H heads that is about (T/64 + N + 1) * H > 1000
+ *     (chunk, head) pairs, e.g. more than ~3,900 tokens of one 16-head
+ *     sequence.
+ *   - All calls share the one array: calls whose GPU work overlaps (other
+ *     streams, other host threads) race on it and give wrong results, so
+ *     serialise them.  The array keeps the previous call's contents; nothing
+ *     in it needs clearing, because the kernels write every byte they read.
+ *   - The first call on each device looks up the array's device address
+ *     (with that device current).  Make that first call before any stream
+ *     capture begins.
+ */
+#define KDA_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+kdaStatus_t kda_chunk_fwd_static(const void *q, const void *k, const void *v,
+                                 const float *log_alpha, const float *beta, float scale,
+                                 const float *initial_state, const int32_t *cu_seqlens,
+                                 void *out, float *final_state, const kdaShape_t *shape,
+                                 cudaStream_t stream);
+
+/*
  * kda_recurrent_step -- one decode token for each of N independent sequences.
  *
  * Defines: one step of the recurrence above ("Kimi Unveils Delta Attention
