@@ -45,6 +45,7 @@
 // (decays stronger than ~exp(-80) across half a chunk) takes a CUDA-core path
 // that evaluates every exp(G_i - G_j) directly, so any finite gates <= 0 work.
 #include <cstdint>
+#include <cstring>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -59,7 +60,7 @@ using namespace tc;
 
 constexpr int D = 128;        // d_k = d_v
 constexpr int C = 64;         // chunk
-constexpr int BV = 32;        // value columns per scan CTA
+constexpr int BV = 64;        // value columns per scan CTA
 constexpr int NT = D / BV;    // value tiles per head
 constexpr int MID = 32;       // reference row of the factorised decay
 constexpr float kSpanLimit = 80.f;
@@ -559,25 +560,57 @@ struct ScanStage {
 
 struct ScanSmem {
     ScanStage st[2];
-    uint8_t sbt[2 * 4096];       // S_c^T f16: 32 rows x 128 K, 2 panels
-    uint8_t ebt[4096];           // E^T f16: 32 rows x 64 K
-    uint8_t bvt[4096];           // (beta V)^T f16: 32 rows x 64 K
+    // B operands in MN-major (value columns contiguous) 128-byte-swizzled
+    // layout: one row of 64 f16 values per K index.
+    uint8_t sb[D * 128];         // S_c:    K = 128 key rows
+    uint8_t eb[C * 128];         // E:      K = 64 token rows
+    uint8_t bv[C * 128];         // beta V: K = 64 token rows
+    uint8_t ob[C * BV * 4];      // output tile staging for the TMA store (swizzled panels)
     uint64_t full[2];            // stage loaded (producer -> compute)
     uint64_t empty[2];           // stage released (compute -> producer)
-    uint64_t mma_e, mma_s, mma_o;  // MMA groups done: E, state increment, outputs
+    uint64_t mma_e, mma_s;       // MMA groups done: E; state increment and outputs
     uint32_t tmem;
     volatile int32_t abort_flag;
 };
 
 constexpr int kScanThreads = 160;  // warps 0-3 compute, warp 4 streams operands in
+constexpr uint32_t kScanTmemCols = 128;  // D1 (BV columns) + D2 (BV columns)
 
 __device__ __forceinline__ void compute_barrier() {
     asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
+// B operand (MN-major, SW128, N = 64): K walks 16 rows = 2048 bytes per step.
+__device__ __forceinline__ void mma_kmajor_a_mn_b(uint32_t d_tmem, uint32_t a_base,
+                                                  uint32_t a_panel, uint32_t b_base, int ksteps,
+                                                  uint32_t idesc, bool accumulate_first) {
+#pragma unroll
+    for (int ks = 0; ks < ksteps; ++ks) {
+        const uint32_t a = a_base + (ks >> 2) * a_panel + (ks & 3) * 32;
+        const uint32_t b = b_base + ks * 2048;
+        mma_half(d_tmem, sdesc_sw128(a), sdesc_sw128(b), idesc,
+                 (ks > 0 || accumulate_first) ? 1u : 0u);
+    }
+}
+
+// 32 consecutive f16 values (4 swizzled 16-byte chunks) of one MN-major row.
+__device__ __forceinline__ void store_row32_f16(uint8_t *img, uint32_t row, uint32_t chunk0,
+                                                const float *v) {
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+        uint4 u;
+        u.x = pack_f16x2(v[c4 * 8 + 0], v[c4 * 8 + 1]);
+        u.y = pack_f16x2(v[c4 * 8 + 2], v[c4 * 8 + 3]);
+        u.z = pack_f16x2(v[c4 * 8 + 4], v[c4 * 8 + 5]);
+        u.w = pack_f16x2(v[c4 * 8 + 6], v[c4 * 8 + 7]);
+        *reinterpret_cast<uint4 *>(img + sw128_chunk(row, chunk0 + c4)) = u;
+    }
+}
+
 template <typename TOut>
 __global__ void __launch_bounds__(kScanThreads, 1)
-chunk_scan_kernel(const __nv_bfloat16 *__restrict__ v, const float *__restrict__ initial_state,
+chunk_scan_kernel(const __grid_constant__ CUtensorMap out_map,
+                  const __nv_bfloat16 *__restrict__ v, const float *__restrict__ initial_state,
                   const int32_t *__restrict__ cu, TOut *__restrict__ out,
                   float *__restrict__ final_state, int32_t N, int32_t T, int32_t H, Scratch sc,
                   int *status) {
@@ -592,7 +625,7 @@ chunk_scan_kernel(const __nv_bfloat16 *__restrict__ v, const float *__restrict__
     const int32_t n_chunks = (tb - ta + C - 1) / C;
     const size_t state_off = (((size_t)seq * H + h) * D + (tid & 127)) * D + (size_t)vt * BV;
 
-    // state row of key channel tid (compute threads), 32 value columns, fp32
+    // state row of key channel tid (compute threads), BV value columns, fp32
     float S[BV];
     if (tid < 128 && initial_state) {
 #pragma unroll
@@ -607,24 +640,22 @@ chunk_scan_kernel(const __nv_bfloat16 *__restrict__ v, const float *__restrict__
 
     bool ok = true;
     if (n_chunks > 0) {
-        // zero the constant zero blocks
-        for (int stg = 0; stg < 2; ++stg) {
+        for (int stg = 0; stg < 2; ++stg) {  // the constant zero blocks
             uint4 *z = reinterpret_cast<uint4 *>(sm.st[stg].aa + 8192);
             for (int idx = tid; idx < 8192 / 16; idx += kScanThreads) z[idx] = make_uint4(0, 0, 0, 0);
         }
         if (tid == 0) {
             for (int i = 0; i < 2; ++i) {
                 mbar_init(&sm.full[i], 1);
-                mbar_init(&sm.empty[i], 1);
+                mbar_init(&sm.empty[i], 128);  // every compute thread releases
             }
             mbar_init(&sm.mma_e, 1);
             mbar_init(&sm.mma_s, 1);
-            mbar_init(&sm.mma_o, 1);
             sm.abort_flag = 0;
             fence_mbar_init();
         }
         if (warp == 0) {
-            tmem_alloc(&sm.tmem, 64);
+            tmem_alloc(&sm.tmem, kScanTmemCols);
             tmem_relinquish();
         }
         fence_proxy_async();
@@ -632,8 +663,7 @@ chunk_scan_kernel(const __nv_bfloat16 *__restrict__ v, const float *__restrict__
         __syncthreads();
         tc_fence_after();
         const uint32_t tmem = sm.tmem;
-        const uint32_t d1 = tmem, d2 = tmem + 32;
-        constexpr uint32_t IDESC = idesc_f16_f32(128, BV);
+        constexpr uint32_t IDESC = idesc_f16_f32(128, BV) | (1u << 16);  // B MN-major
 
         if (warp == 4) {
             // ---------------- producer: stream each chunk's operands in ----------------
@@ -662,81 +692,150 @@ chunk_scan_kernel(const __nv_bfloat16 *__restrict__ v, const float *__restrict__
             }
         } else {
             // ---------------- compute warps ----------------
-            // value tile of a chunk: thread -> token row tid/2, 16 columns (32 B),
+            // value tile of a chunk: thread -> token row tid/2, 32 columns (64 B),
             // prefetched into registers one chunk ahead
-            const int vi = tid >> 1, vj0 = (tid & 1) * 16;
-            auto load_v = [&](int32_t n, uint4 &p0, uint4 &p1) {
+            const int vi = tid >> 1, vh = tid & 1;
+            uint4 vreg[4];
+            auto load_v = [&](int32_t n) {
                 const int32_t t0n = ta + n * C;
                 if (n < n_chunks && vi < min(C, tb - t0n)) {
                     const uint4 *src = reinterpret_cast<const uint4 *>(
-                        v + ((size_t)(t0n + vi) * H + h) * D + vt * BV + vj0);
-                    p0 = __ldg(src);
-                    p1 = __ldg(src + 1);
+                        v + ((size_t)(t0n + vi) * H + h) * D + vt * BV + vh * 32);
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) vreg[x] = __ldg(src + x);
                 } else {
-                    p0 = make_uint4(0, 0, 0, 0);
-                    p1 = p0;
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) vreg[x] = make_uint4(0, 0, 0, 0);
                 }
             };
-            uint4 vnext0, vnext1;
-            load_v(0, vnext0, vnext1);
+            // beta V of chunk n into the MN-major operand; then prefetch chunk n+1
+            auto build_bv = [&](int32_t n) {
+                const float b = sm.st[n & 1].gb[128 + vi];
+                float f[32];
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const uint32_t w[4] = {vreg[x].x, vreg[x].y, vreg[x].z, vreg[x].w};
+#pragma unroll
+                    for (int y = 0; y < 4; ++y) {
+                        f[x * 8 + 2 * y] = b * __uint_as_float(w[y] << 16);
+                        f[x * 8 + 2 * y + 1] = b * __uint_as_float(w[y] & 0xFFFF0000u);
+                    }
+                }
+                store_row32_f16(sm.bv, vi, vh * 4, f);
+                load_v(n + 1);
+            };
+
+            // outputs of chunk n from D1 rows 64..127 (warps 2 and 3: token = tid - 64).
+            // A full chunk goes out as one TMA tensor store from a staging tile; a
+            // partial chunk (the end of a sequence) writes its valid rows directly,
+            // so nothing past the sequence is touched.
+            auto store_outputs = [&](uint32_t d1n, int32_t n) {
+                const int32_t t0n = ta + n * C;
+                const int32_t Ln = min(C, tb - t0n);
+                const int i = tid - 64;
+                float o0[32], o1[32];
+                tmem_ld32x2(tmem_addr(d1n, warp * 32, 0), tmem_addr(d1n, warp * 32, 32), o0, o1);
+                if (Ln == C) {
+                    // staging: 128-byte column panels (1 for bf16, 2 for fp32), each
+                    // [64 rows x 128 B] in the 128-byte swizzle the TMA store expects
+                    if (tid == 64) bulk_wait_group_read<0>();  // staging free again
+                    asm volatile("bar.sync 2, 64;" ::: "memory");
+                    if constexpr (sizeof(TOut) == 2) {
+#pragma unroll
+                        for (int c8 = 0; c8 < 8; ++c8) {
+                            const float *src = c8 < 4 ? &o0[c8 * 8] : &o1[(c8 - 4) * 8];
+                            uint4 u;
+                            u.x = pack_bf16x2(src[0], src[1]);
+                            u.y = pack_bf16x2(src[2], src[3]);
+                            u.z = pack_bf16x2(src[4], src[5]);
+                            u.w = pack_bf16x2(src[6], src[7]);
+                            *reinterpret_cast<uint4 *>(sm.ob + sw128_chunk(i, c8)) = u;
+                        }
+                    } else {
+#pragma unroll
+                        for (int c16 = 0; c16 < 16; ++c16) {
+                            const float *src = c16 < 8 ? &o0[c16 * 4] : &o1[(c16 - 8) * 4];
+                            *reinterpret_cast<float4 *>(sm.ob + (c16 >> 3) * (C * 128) +
+                                                        sw128_chunk(i, c16 & 7)) =
+                                make_float4(src[0], src[1], src[2], src[3]);
+                        }
+                    }
+                    fence_proxy_async();
+                    asm volatile("bar.sync 2, 64;" ::: "memory");
+                    if (tid == 64) {
+                        constexpr int per_panel = 128 / (int)sizeof(TOut);
+#pragma unroll
+                        for (int pnl = 0; pnl < (int)sizeof(TOut) / 2; ++pnl)
+                            tma_store_3d(&out_map, sm.ob + pnl * (C * 128),
+                                         vt * BV + pnl * per_panel, h, t0n);
+                        bulk_commit_group();
+                    }
+                } else if (i < Ln) {
+                    TOut *dst = out + ((size_t)(t0n + i) * H + h) * D + vt * BV;
+                    if constexpr (sizeof(TOut) == 2) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 8) {
+                            uint4 u;
+                            u.x = pack_bf16x2(o0[j], o0[j + 1]);
+                            u.y = pack_bf16x2(o0[j + 2], o0[j + 3]);
+                            u.z = pack_bf16x2(o0[j + 4], o0[j + 5]);
+                            u.w = pack_bf16x2(o0[j + 6], o0[j + 7]);
+                            *reinterpret_cast<uint4 *>(dst + j) = u;
+                            u.x = pack_bf16x2(o1[j], o1[j + 1]);
+                            u.y = pack_bf16x2(o1[j + 2], o1[j + 3]);
+                            u.z = pack_bf16x2(o1[j + 4], o1[j + 5]);
+                            u.w = pack_bf16x2(o1[j + 6], o1[j + 7]);
+                            *reinterpret_cast<uint4 *>(dst + 32 + j) = u;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4) {
+                            *reinterpret_cast<float4 *>(dst + j) =
+                                make_float4(o0[j], o0[j + 1], o0[j + 2], o0[j + 3]);
+                            *reinterpret_cast<float4 *>(dst + 32 + j) =
+                                make_float4(o1[j], o1[j + 1], o1[j + 2], o1[j + 3]);
+                        }
+                    }
+                }
+            };
+
+            load_v(0);
+            if (!mbar_wait_bounded(&sm.full[0], 0, kWaitCycles)) sm.abort_flag = 1;
+            build_bv(0);
+            const uint32_t d1 = tmem, d2 = tmem + BV;
+            fence_proxy_async();
+            compute_barrier();
+            if (tid == 0 && !sm.abort_flag) {
+                tc_fence_after();
+                // D1 = [A^kk ; 0] (beta V) of chunk 0
+                mma_kmajor_a_mn_b(d1, smem_u32(sm.st[0].aa), 0, smem_u32(sm.bv), 4, IDESC, false);
+            }
             for (int32_t n = 0; n < n_chunks; ++n) {
                 const int stg = n & 1;
                 ScanStage &st = sm.st[stg];
-                const int32_t t0 = ta + n * C;
-                const int32_t L = min(C, tb - t0);
                 const uint32_t par = n & 1;
 
-                if (!mbar_wait_bounded(&sm.full[stg], (n >> 1) & 1, kWaitCycles))
-                    sm.abort_flag = 1;
-
-                // (beta V)^T operand: thread -> token row i = tid/2, 16 value columns
-                {
-                    const int i = vi, j0 = vj0;
-                    const float b = st.gb[128 + i];
-                    const uint4 p0 = vnext0, p1 = vnext1;
-                    load_v(n + 1, vnext0, vnext1);
-                    const uint32_t w[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-#pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) {
-                        const float lo = __uint_as_float(w[jj] << 16);
-                        const float hi = __uint_as_float(w[jj] & 0xFFFF0000u);
-                        *reinterpret_cast<__half *>(sm.bvt + sw128_offset(j0 + 2 * jj, i)) =
-                            __float2half_rn(b * lo);
-                        *reinterpret_cast<__half *>(sm.bvt + sw128_offset(j0 + 2 * jj + 1, i)) =
-                            __float2half_rn(b * hi);
-                    }
-                }
-                // S_c^T operand (f16): thread = key row tid
-                {
-                    uint8_t *pnl = sm.sbt + (tid >> 6) * 4096;
-#pragma unroll
-                    for (int j = 0; j < BV; ++j)
-                        *reinterpret_cast<__half *>(pnl + sw128_offset(j, tid & 63)) =
-                            __float2half_rn(S[j]);
-                }
+                // S_c operand (f16): thread = key row tid, 64 values
+                store_row32_f16(sm.sb, tid, 0, &S[0]);
+                store_row32_f16(sm.sb, tid, 4, &S[32]);
                 fence_proxy_async();
                 tc_fence_before();
                 compute_barrier();
                 if (sm.abort_flag) break;
                 if (tid == 0) {
                     tc_fence_after();
-                    if (n > 0) mbar_arrive(&sm.empty[(n - 1) & 1]);  // chunk n-1 fully consumed
-                    // D1 = [A^kk ; 0] (beta V)      -> rows 0..63: U, rows 64..127: 0
-                    mma_panels(d1, smem_u32(st.aa), 0, smem_u32(sm.bvt), 0, 4, IDESC, false);
-                    // D1 += [-W ; Q_hat] S_c       -> rows 0..63: E, rows 64..127: Q_hat S_c
-                    mma_panels(d1, smem_u32(st.wq), 16384, smem_u32(sm.sbt), 4096, 8, IDESC, true);
+                    // D1 += [-W ; Q_hat] S_c  -> rows 0..63: E = U - W S_c, rows 64..127: Q_hat S_c
+                    mma_kmajor_a_mn_b(d1, smem_u32(st.wq), 16384, smem_u32(sm.sb), 8, IDESC,
+                                      true);
                     mma_commit(&sm.mma_e);
                 }
-                if (!mbar_wait_bounded(&sm.mma_e, par, kWaitCycles)) sm.abort_flag = 1;
-                tc_fence_after();
                 if (warp < 2) {
-                    float e[32];
-                    tmem_ld32(tmem_addr(d1, warp * 32, 0), e);
-                    const int i = tid;  // token row
-#pragma unroll
-                    for (int j = 0; j < BV; ++j)
-                        *reinterpret_cast<__half *>(sm.ebt + sw128_offset(j, i)) =
-                            __float2half_rn(e[j]);
+                    if (!mbar_wait_bounded(&sm.mma_e, par, kWaitCycles)) sm.abort_flag = 1;
+                    tc_fence_after();
+                    float e0[32], e1[32];
+                    tmem_ld32x2(tmem_addr(d1, warp * 32, 0), tmem_addr(d1, warp * 32, 32), e0, e1);
+                    store_row32_f16(sm.eb, tid, 0, e0);
+                    store_row32_f16(sm.eb, tid, 4, e1);
                 }
                 fence_proxy_async();
                 tc_fence_before();
@@ -744,50 +843,46 @@ chunk_scan_kernel(const __nv_bfloat16 *__restrict__ v, const float *__restrict__
                 if (sm.abort_flag) break;
                 if (tid == 0) {
                     tc_fence_after();
-                    // D2 = K_end^T E  (state increment)
-                    mma_panels(d2, smem_u32(st.ke), 0, smem_u32(sm.ebt), 0, 4, IDESC, false);
+                    // D2 = K_end^T E (state increment); D1 += [0 ; A^qk] E (outputs)
+                    mma_kmajor_a_mn_b(d2, smem_u32(st.ke), 0, smem_u32(sm.eb), 4, IDESC, false);
+                    mma_kmajor_a_mn_b(d1, smem_u32(st.aa) + 8192, 0, smem_u32(sm.eb), 4, IDESC,
+                                      true);
                     mma_commit(&sm.mma_s);
-                    // D1 += [0 ; A^qk] E  -> rows 64..127: outputs
-                    mma_panels(d1, smem_u32(st.aa) + 8192, 0, smem_u32(sm.ebt), 0, 4, IDESC, true);
-                    mma_commit(&sm.mma_o);
                 }
                 if (!mbar_wait_bounded(&sm.mma_s, par, kWaitCycles)) sm.abort_flag = 1;
                 tc_fence_after();
                 {
-                    float ds[32];
-                    tmem_ld32(tmem_addr(d2, warp * 32, 0), ds);
                     const float g = st.gb[tid];
+                    // this thread's reads of chunk n's stage are done (MMAs completed)
+                    mbar_arrive(&sm.empty[stg]);
+                    float ds0[32], ds1[32];
+                    tmem_ld32x2(tmem_addr(d2, warp * 32, 0), tmem_addr(d2, warp * 32, 32), ds0,
+                                ds1);
 #pragma unroll
-                    for (int j = 0; j < BV; ++j) S[j] = fmaf(g, S[j], ds[j]);
-                }
-                if (warp >= 2) {
-                    if (!mbar_wait_bounded(&sm.mma_o, par, kWaitCycles)) sm.abort_flag = 1;
-                    tc_fence_after();
-                    float o[32];
-                    tmem_ld32(tmem_addr(d1, warp * 32, 0), o);
-                    const int i = tid - 64;
-                    if (i < L) {
-                        TOut *dst = out + ((size_t)(t0 + i) * H + h) * D + vt * BV;
-                        if constexpr (sizeof(TOut) == 2) {
-#pragma unroll
-                            for (int j = 0; j < BV; j += 8) {
-                                uint4 u;
-                                u.x = pack_bf16x2(o[j], o[j + 1]);
-                                u.y = pack_bf16x2(o[j + 2], o[j + 3]);
-                                u.z = pack_bf16x2(o[j + 4], o[j + 5]);
-                                u.w = pack_bf16x2(o[j + 6], o[j + 7]);
-                                *reinterpret_cast<uint4 *>(dst + j) = u;
-                            }
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < BV; j += 4)
-                                *reinterpret_cast<float4 *>(dst + j) =
-                                    make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
-                        }
+                    for (int j = 0; j < 32; ++j) {
+                        S[j] = fmaf(g, S[j], ds0[j]);
+                        S[32 + j] = fmaf(g, S[32 + j], ds1[j]);
                     }
                 }
+                if (warp >= 2) store_outputs(d1, n);
+                // next chunk's beta V, and its U on the tensor core ahead of time
+                const bool more = n + 1 < n_chunks;
+                if (more) {
+                    if (!mbar_wait_bounded(&sm.full[(n + 1) & 1], ((n + 1) >> 1) & 1, kWaitCycles))
+                        sm.abort_flag = 1;
+                    build_bv(n + 1);
+                    fence_proxy_async();
+                }
                 tc_fence_before();
+                compute_barrier();
+                if (sm.abort_flag) break;
+                if (tid == 0 && more) {
+                    tc_fence_after();
+                    mma_kmajor_a_mn_b(d1, smem_u32(sm.st[(n + 1) & 1].aa), 0, smem_u32(sm.bv), 4,
+                                      IDESC, false);
+                }
             }
+            if (tid == 64) bulk_wait_group_all();  // output tiles written
             if (sm.abort_flag) ok = false;
         }
         __syncthreads();
@@ -801,7 +896,7 @@ chunk_scan_kernel(const __nv_bfloat16 *__restrict__ v, const float *__restrict__
         }
         tc_fence_before();
         __syncthreads();
-        if (warp == 0) tmem_dealloc(tmem, 64);
+        if (warp == 0) tmem_dealloc(tmem, kScanTmemCols);
         if (!ok) return;
     }
     if (final_state && tid < 128) {
@@ -884,19 +979,37 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
     a.clock->mark(stream);
 
     const dim3 sgrid((unsigned)(a.N * NT), (unsigned)a.H);
+    // output tiles [64 tokens x 64 columns] of one head; unused when T == 0
+    CUtensorMap out_map;
+    memset(&out_map, 0, sizeof(out_map));
+    if (a.T > 0) {
+        auto enc = tensor_map_encoder();
+        const size_t es = a.out_f32 ? 4 : 2;
+        const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.H, (cuuint64_t)a.T};
+        const cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)a.H * D * es};
+        // one 128-byte column panel per box, 128-byte swizzle
+        const cuuint32_t box[3] = {(cuuint32_t)(128 / es), 1u, (cuuint32_t)C};
+        const cuuint32_t estr[3] = {1u, 1u, 1u};
+        if (!enc ||
+            enc(&out_map, a.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                3, a.out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
     if (a.out_f32) {
         auto kern = chunk_scan_kernel<float>;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
         if (e != cudaSuccess) return e;
         kern<<<sgrid, kScanThreads, kScanSmem, stream>>>(
-            static_cast<const __nv_bfloat16 *>(a.v), a.initial_state, a.cu_seqlens,
+            out_map, static_cast<const __nv_bfloat16 *>(a.v), a.initial_state, a.cu_seqlens,
             static_cast<float *>(a.out), a.final_state, a.N, a.T, a.H, sc, a.status);
     } else {
         auto kern = chunk_scan_kernel<__nv_bfloat16>;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
         if (e != cudaSuccess) return e;
         kern<<<sgrid, kScanThreads, kScanSmem, stream>>>(
-            static_cast<const __nv_bfloat16 *>(a.v), a.initial_state, a.cu_seqlens,
+            out_map, static_cast<const __nv_bfloat16 *>(a.v), a.initial_state, a.cu_seqlens,
             static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.N, a.T, a.H, sc, a.status);
     }
     a.clock->mark(stream);
