@@ -176,19 +176,25 @@ def prefill_flops_per_tok_head(d: int, C: int) -> int:
 
 
 def stage_work(d: int, C: int):
-    """Per (token, head) compulsory bytes and dense flops of each kernel of the
-    tensor-core engine (its own inputs read once, outputs written once)."""
-    prep_bytes = (2 * 2 * d          # q, k (bf16)
-                  + 4 * d + 4        # log_alpha, beta (fp32)
-                  + 3 * 2 * d        # -W, Q_hat, K_end^T (f16 images)
-                  + 2 * 2 * C        # A^kk, A^qk rows (f16 images)
-                  + 4 * d / C + 4)   # Gamma_last per chunk, beta copy (fp32)
-    scan_bytes = (3 * 2 * d + 2 * 2 * C + 4 * d / C + 4   # the prep products
-                  + 2 * d                                  # v (bf16)
-                  + 2 * d)                                 # out (bf16)
-    prep_flops = 3 * 2 * C * d        # [K;Q] K^T (two C x C x d) and W
-    scan_flops = 2 * 2 * C * d + 3 * 2 * d * d
-    return {"prep": (prep_bytes, prep_flops), "scan": (scan_bytes, scan_flops)}
+    """Per (token, head) compulsory bytes and issued tensor-core flops of each
+    kernel of the tensor-core engine (its own inputs read once, its outputs
+    written once).  The per-(chunk, head) image holds -M' (d x d), P' (d x C),
+    Q' (C x d), Z (C x C) in f16 plus Gamma_last and beta in fp32; the scan
+    reads its -M'/P' part once per value tile and writes S_c (d x d, f16) per
+    chunk; the output pass reads Q'/Z (with 8 KB of filler rows), S_c and v."""
+    nt = 2                                            # value tiles per head
+    img = (2 * d * d + 2 * d * C + 2 * C * d + 2 * C * C + 4 * d + 4 * C) / C
+    prep_bytes = 2 * 2 * d + 4 * d + 4 + img          # q, k, log_alpha, beta -> image
+    scan_bytes = (nt * (2 * d * d + 2 * d * C) / C    # -M', P' per value tile
+                  + 2 * d + 4 * d / C * nt + 4 * nt   # v, Gamma_last, beta
+                  + 2 * d * d / C)                    # S_c out (f16)
+    out_bytes = ((2 * C * d + 2 * C * C + 2 * 64 * 64 + 2 * d * d) / C  # Q', Z, filler, S_c
+                 + 2 * d + 4 + 2 * d)                 # v, beta in; out (bf16)
+    prep_flops = 10 * C * d + 2 * d * d + 2 * C * C   # [K;Q]K^T, W, M', P', A^qk W, Z
+    scan_flops = 2 * d * d + 2 * d * d * d / C        # P' (beta V), M' S_c
+    out_flops = 2 * d * d + 2 * C * d                 # Q' S_c, Z (beta V)
+    return {"prep": (prep_bytes, prep_flops), "scan": (scan_bytes, scan_flops),
+            "out": (out_bytes, out_flops)}
 
 
 PROFILE_FILES = {
@@ -373,8 +379,8 @@ def run_ours(args, dist: Dist):
     tflops = flops_step * args.steps * dist.world / (total_ms / 1e3) / 1e12
 
     stage_avg = [statistics.mean(s[j] for s in stage_ms) for j in range(n_stages)]
-    if n_stages == 3:
-        names = ["chunk_table", "prep", "scan"]
+    if n_stages == 4:
+        names = ["chunk_table", "prep", "scan", "out"]
     else:
         names = [f"stage{j}" for j in range(n_stages)]
         names[-1] = "chunk_simt" if n_stages == 1 else names[-1]

@@ -66,16 +66,32 @@ constexpr int MID = 32;       // reference row of the factorised decay
 constexpr float kSpanLimit = 80.f;
 constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
 
-// Per-(chunk, head) scratch images (f16 operands in the swizzled layout,
-// fp32 gates).
-constexpr uint32_t WQ_BYTES = 2 * 16384;  // [-W ; Q_hat] : 128 rows x 128 K, 2 panels
-constexpr uint32_t KE_BYTES = 16384;      // K_end^T     : 128 rows x 64 K
-constexpr uint32_t AK_BYTES = 8192;       // A^kk        : 64 rows x 64 K
-constexpr uint32_t AQ_BYTES = 8192;       // A^qk        : 64 rows x 64 K
-constexpr uint32_t GB_BYTES = 768;        // Gamma_last [128] f32, beta [64] f32
+// Per-(chunk, head) scratch image: the scan's operands for one chunk, already
+// in its shared-memory layout (f16, K-major, 128-byte swizzle), so the scan
+// brings a chunk in with one bulk copy.  With
+//   M' = K_end^T W        (128 x 128)   P' = K_end^T A^kk  (128 x 64)
+//   Q' = Q_hat - A^qk W   (64 x 128)    Z  = A^qk A^kk     (64 x 64)
+// the chunk's recurrence and outputs are
+//   S_c+1 = Diag(Gamma_last) S_c + P' (beta V) - M' S_c
+//   O     = Q' S_c + Z (beta V)
+// (K_end^T E and A^qk E with E = U - W S_c, U = A^kk beta V, expanded).
+constexpr uint32_t IMG_MN = 0;          // -M': 2 panels of 128 rows
+constexpr uint32_t IMG_P = 32768;       // P' : 128 rows
+constexpr uint32_t IMG_Q0 = 49152;      // Q' keys 0..63  : 64 rows
+constexpr uint32_t IMG_Z = 57344;       // Z  : 64 rows
+constexpr uint32_t IMG_Q1 = 65536;      // Q' keys 64..127: 64 rows
+constexpr uint32_t IMG_GB = 73728;      // Gamma_last [128] f32, beta [64] f32
+constexpr uint32_t IMG_BYTES = IMG_GB + 768;   // bytes written per chunk (the scan
+                                               // copies the operands, IMG_GB bytes)
+constexpr uint32_t IMG_STRIDE = 74752;         // 73 KB slot, 1024-aligned
+static_assert(IMG_BYTES <= IMG_STRIDE && IMG_STRIDE % 1024 == 0, "image slot");
+// As 128-row MMA A operands the 64-row tiles are read with the 8 KB that
+// precedes them: rows 64..127 of [filler ; Q'] and [filler ; Z] hold them, and
+// the filler rows produce accumulator rows that are never read.
 
 struct Scratch {
-    uint8_t *wq, *ke, *ak, *aq, *gb;
+    uint8_t *img;        // [n_chunks x H] x IMG_STRIDE
+    uint8_t *sst;        // [n_chunks x H x value tiles] S_c images (f16, 16 KB each)
     int32_t *chunk_off;  // [N + 1]
 };
 
@@ -87,11 +103,8 @@ Scratch carve(void *ws, int32_t N, int32_t T, int32_t H) {
     const size_t nch = max_chunks(N, T) * (size_t)H;
     uint8_t *p = static_cast<uint8_t *>(ws);
     Scratch s;
-    s.wq = p; p += align256(nch * WQ_BYTES);
-    s.ke = p; p += align256(nch * KE_BYTES);
-    s.ak = p; p += align256(nch * AK_BYTES);
-    s.aq = p; p += align256(nch * AQ_BYTES);
-    s.gb = p; p += align256(nch * GB_BYTES);
+    s.img = p; p += align256(nch * IMG_STRIDE);
+    s.sst = p; p += align256(nch * NT * (size_t)(D * 128));
     s.chunk_off = reinterpret_cast<int32_t *>(p);
     return s;
 }
@@ -170,10 +183,12 @@ __device__ __forceinline__ int32_t find_seq(const int32_t *off, int32_t N, int32
 // first tenant is done:
 //   a1: g tile (TMA, f32 [64][128]) -> tf32 [K_tilde ; Q_tilde], 128 rows x
 //       128 K in 4 panels (64 KB) -> R, X (= A^kk) and the solve's block
-//       products (fp32);
+//       products (fp32), with A^qk (f16, at kOffAqk) kept beside them ->
+//       W^T (f16, at 0), Q' staging (f16, at kOffQs), A^qk, K_end^T (f16, at
+//       kOffKe);
 //   b1: k and q tiles (TMA, bf16 [64][128] each) -> tf32 K_hat, 64 rows x
-//       128 K in 4 panels (32 KB) (slow path: G f32 [64][128]) -> A^kk f16
-//       panel (8 KB) and (beta Gamma K)^T f16 panel, 128 rows x 64 K (16 KB).
+//       128 K in 4 panels (32 KB) (slow path: G f32 [64][128]) -> A^kk and
+//       A^kk^T (f16, 8 KB each) and (beta Gamma K)^T (f16, 128 x 64, 16 KB).
 constexpr int kPrepThreads = 256;
 constexpr int HALF = C / 2;
 
@@ -189,7 +204,12 @@ struct PrepSmem {
 };
 constexpr uint32_t kOffX = C * (C + 1) * 4;        // X after R inside a1
 constexpr uint32_t kOffTb = 2 * C * (C + 1) * 4;   // block products after X
-constexpr uint32_t kOffA2 = 8192;                  // (beta Gamma K)^T after A^kk inside b1
+constexpr uint32_t kOffQs = 16384;                 // Q' staging (2 x 8 KB) inside a1
+constexpr uint32_t kOffAqk = 40960;                // A^qk (f16) inside a1
+constexpr uint32_t kOffKe = 49152;                 // K_end^T (f16) inside a1
+constexpr uint32_t kOffAkT = 8192;                 // A^kk^T after A^kk inside b1
+constexpr uint32_t kOffA2 = 16384;                 // (beta Gamma K)^T inside b1
+static_assert(kOffTb + 3 * 16 * 17 * 4 <= kOffAqk, "solve scratch below A^qk");
 constexpr uint32_t kInBytes = 2 * C * D * 2 + C * D * 4;  // k, q bf16 + g f32 tiles
 static_assert(kOffTb + 3 * 16 * 17 * 4 <= 4 * 16384, "a1 reuse");
 static_assert(MID == HALF, "the reference token opens the second half");
@@ -237,8 +257,12 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
     float(*R)[C + 1] = reinterpret_cast<float(*)[C + 1]>(sm.a1);
     float(*X)[C + 1] = reinterpret_cast<float(*)[C + 1]>(sm.a1 + kOffX);
     float(*Tb)[16][17] = reinterpret_cast<float(*)[16][17]>(sm.a1 + kOffTb);
-    uint8_t *b2 = sm.b1;            // A^kk, f16 panel
-    uint8_t *a2 = sm.b1 + kOffA2;   // (beta Gamma K)^T, f16 panel
+    uint8_t *b2 = sm.b1;              // A^kk, f16 panel
+    uint8_t *akt = sm.b1 + kOffAkT;   // A^kk^T, f16 panel
+    uint8_t *a2 = sm.b1 + kOffA2;     // (beta Gamma K)^T, f16 panel
+    uint8_t *aqk = sm.a1 + kOffAqk;   // A^qk, f16 panel
+    uint8_t *ket = sm.a1 + kOffKe;    // K_end^T, f16 panel
+    uint8_t *wt = sm.a1;              // W^T, f16 panel (after the solve)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t c = blockIdx.x, h = blockIdx.y;
@@ -250,11 +274,8 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
     const int32_t t0 = ta + (c - sc.chunk_off[s]) * C;
     const int32_t L = min(C, tb - t0);
     const size_t ch = (size_t)c * H + h;
-    uint8_t *wq = sc.wq + ch * WQ_BYTES;
-    uint8_t *ke = sc.ke + ch * KE_BYTES;
-    uint8_t *ak = sc.ak + ch * AK_BYTES;
-    uint8_t *aq = sc.aq + ch * AQ_BYTES;
-    float *gb = reinterpret_cast<float *>(sc.gb + ch * GB_BYTES);
+    uint8_t *img = sc.img + ch * IMG_STRIDE;
+    float *gb = reinterpret_cast<float *>(img + IMG_GB);
     const size_t rs = (size_t)H * D;
 
     // Stream the chunk's k, q and log-decay tiles in (one tensor load each).
@@ -268,7 +289,7 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
         tma_load_3d(sm.a1, &maps.g, 0, h, t0, &sm.bar_in);
     }
     if (warp == 0) {
-        tmem_alloc(&sm.tmem, 128);
+        tmem_alloc(&sm.tmem, 256);
         tmem_relinquish();
         tc_fence_before();
     }
@@ -368,45 +389,27 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
             float row[64];
 #pragma unroll
             for (int j = 0; j < 64; ++j) row[j] = X[tid][j];
-            store_row_f16_image(aq, tid, row);
+            store_row_f16_image(aqk, tid, row);
         }
         __syncthreads();
     }
 
-    // Boundary-facing factors and the tf32 operands, token by token.
+    // The decay-factorised tf32 operands, token by token.
     {
         const float e_m = __expf(Gm), e_lm = __expf(Gl - Gm);
-        const uint32_t pa = (d >> 5) * 16384u, pb = (d >> 5) * 8192u;
-        uint8_t *qrow = wq + (d >> 6) * 16384u;
-        float kend[8];
+        if (!slow) {
+            const uint32_t pa = (d >> 5) * 16384u, pb = (d >> 5) * 8192u;
 #pragma unroll
-        for (int ii = 0; ii < HALF; ++ii) {
-            const int i = i0 + ii;
-            const float kv = kval(ii), qv = qval(ii);
-            float gam, eend;
-            if (!slow) {
+            for (int ii = 0; ii < HALF; ++ii) {
+                const int i = i0 + ii;
+                const float kv = kval(ii), qv = qval(ii);
                 const float ep = __expf(G[ii] - Gm), en = __expf(Gm - G[ii]);
-                gam = ep * e_m;
-                eend = e_lm * en;
                 *reinterpret_cast<float *>(sm.a1 + pa + sw128_offset_f32(i, d & 31)) =
                     to_tf32(kv * ep);
                 *reinterpret_cast<float *>(sm.a1 + pa + sw128_offset_f32(64 + i, d & 31)) =
                     to_tf32(qv * ep);
                 *reinterpret_cast<float *>(sm.b1 + pb + sw128_offset_f32(i, d & 31)) =
                     to_tf32(kv * en);
-            } else {
-                gam = __expf(G[ii]);
-                eend = __expf(Gl - G[ii]);
-            }
-            // Q_hat = s Gamma q -> rows 64..127 of the [-W ; Q_hat] image
-            *reinterpret_cast<__half *>(qrow + sw128_offset(64 + i, d & 63)) =
-                __float2half_rn(scale * gam * qv);
-            kend[ii & 7] = eend * kv;
-            if ((ii & 7) == 7) {
-                uint4 u;
-                u.x = pack_f16x2(kend[0], kend[1]); u.y = pack_f16x2(kend[2], kend[3]);
-                u.z = pack_f16x2(kend[4], kend[5]); u.w = pack_f16x2(kend[6], kend[7]);
-                *reinterpret_cast<uint4 *>(ke + sw128_chunk(d, i >> 3)) = u;
             }
         }
         if (hf == 0) gb[d] = slow ? __expf(Gl) : e_lm * e_m;
@@ -424,6 +427,7 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
             mma_commit(&sm.bar_mma);
         }
         if (ok) ok = mbar_wait_bounded(&sm.bar_mma, mma_phase, kWaitCycles);
+        ok = __all_sync(0xffffffffu, ok);  // TMEM loads below are warp-collective
         mma_phase ^= 1;
         tc_fence_after();
         // warp w reads TMEM lanes 32*(w%4).., columns 32*(w/4)..
@@ -452,7 +456,7 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
                 const int j = chalf * 32 + jj;
                 row[jj] = (j <= i && i < L) ? scale * v[jj] : 0.f;
             }
-            store_quarter_f16_image(aq, i, chalf * 4, row);
+            store_quarter_f16_image(aqk, i, chalf * 4, row);
         }
     }
     for (int idx = tid; idx < C * (C + 1); idx += kPrepThreads) (&X[0][0])[idx] = 0.f;
@@ -501,25 +505,35 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
         }
         __syncthreads();
     }
+    // A^kk (rows i) and A^kk^T (rows j), f16
     if (tid < 2 * C) {
         const int row = tid >> 1, q4 = tid & 1;
-        float v32[32];
+        float v32[32], t32[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v32[j] = X[row][q4 * 32 + j];
+        for (int j = 0; j < 32; ++j) {
+            v32[j] = X[row][q4 * 32 + j];
+            t32[j] = X[q4 * 32 + j][row];
+        }
         store_quarter_f16_image(b2, row, q4 * 4, v32);
-        store_quarter_f16_image(ak, row, q4 * 4, v32);
+        store_quarter_f16_image(akt, row, q4 * 4, t32);
     }
-    // (beta Gamma K)^T, row d, this thread's half of the tokens, f16
+    // (beta Gamma K)^T and K_end^T: row d, this thread's half of the tokens, f16
     {
-        float bgk[32];
+        float bgk[32], kend[32];
 #pragma unroll
-        for (int ii = 0; ii < HALF; ++ii) bgk[ii] = sm.beta[i0 + ii] * __expf(G[ii]) * kval(ii);
+        for (int ii = 0; ii < HALF; ++ii) {
+            const float kv = kval(ii);
+            bgk[ii] = sm.beta[i0 + ii] * __expf(G[ii]) * kv;
+            kend[ii] = __expf(Gl - G[ii]) * kv;
+        }
         store_quarter_f16_image(a2, d, hf * 4, bgk);
+        store_quarter_f16_image(ket, d, hf * 4, kend);
     }
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
 
+    const int quad = warp & 3, chalf = warp >> 2;  // TMEM lanes 32*quad.., column half
     // W^T = (beta Gamma K)^T A^kk^T on the tensor core (f16): TMEM cols 64..127.
     if (tid == 0 && ok) {
         tc_fence_after();
@@ -528,59 +542,148 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
         mma_commit(&sm.bar_mma);
     }
     if (ok) ok = mbar_wait_bounded(&sm.bar_mma, mma_phase, kWaitCycles);
+    ok = __all_sync(0xffffffffu, ok);  // TMEM loads below are warp-collective
+    mma_phase ^= 1;
+    tc_fence_after();
+    {
+        // thread = key channel d, token half chalf: W^T row d
+        float v[32];
+        if (ok) tmem_ld32(tmem_addr(tmem, quad * 32, 64 + chalf * 32), v);
+        else
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0.f;
+        store_quarter_f16_image(wt, d, chalf * 4, v);
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+
+    // M' = K_end^T W (cols 0..127), P' = K_end^T A^kk (cols 128..191),
+    // (A^qk W)^T = W^T A^qk^T (cols 192..255).
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        mma_panels(tmem, smem_u32(ket), 0, smem_u32(wt), 0, 4, idesc_f16_f32(128, 128), false);
+        mma_panels(tmem + 128, smem_u32(ket), 0, smem_u32(akt), 0, 4, idesc_f16_f32(128, 64),
+                   false);
+        mma_panels(tmem + 192, smem_u32(wt), 0, smem_u32(aqk), 0, 4, idesc_f16_f32(128, 64),
+                   false);
+        mma_commit(&sm.bar_mma);
+    }
+    if (ok) ok = mbar_wait_bounded(&sm.bar_mma, mma_phase, kWaitCycles);
+    ok = __all_sync(0xffffffffu, ok);  // TMEM loads below are warp-collective
+    mma_phase ^= 1;
     tc_fence_after();
     if (ok) {
-        const int quad = warp & 3, chalf = warp >> 2, dd = quad * 32 + lane;
-        float v[32];
-        tmem_ld32(tmem_addr(tmem, quad * 32, 64 + chalf * 32), v);
-        // thread = key channel dd, v[jj] = W[i][dd] for i = 32*chalf + jj; store -W.
-        uint8_t *pnl = wq + (dd >> 6) * 16384u;
+        float v0[32], v1[32];
+        // -M' row d (key), columns (keys) 64*chalf.. -> image panel chalf
+        tmem_ld32x2(tmem_addr(tmem, quad * 32, chalf * 64), tmem_addr(tmem, quad * 32, chalf * 64 + 32),
+                    v0, v1);
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj)
-            *reinterpret_cast<__half *>(pnl + sw128_offset(chalf * 32 + jj, dd & 63)) =
-                __float2half_rn(-v[jj]);
+        for (int j = 0; j < 32; ++j) {
+            v0[j] = -v0[j];
+            v1[j] = -v1[j];
+        }
+        store_quarter_f16_image(img + IMG_MN + chalf * 16384, d, 0, v0);
+        store_quarter_f16_image(img + IMG_MN + chalf * 16384, d, 4, v1);
+        // P' row d, tokens 32*chalf..
+        tmem_ld32(tmem_addr(tmem, quad * 32, 128 + chalf * 32), v0);
+        store_quarter_f16_image(img + IMG_P, d, chalf * 4, v0);
+        // Q'[i][d] = s Gamma_i q_i[d] - (A^qk W)[i][d], tokens i = 32*chalf + jj (this
+        // thread's own tokens), staged as two 64-row panels
+        tmem_ld32(tmem_addr(tmem, quad * 32, 192 + chalf * 32), v0);
+        uint8_t *qs = sm.a1 + kOffQs + (d >> 6) * 8192u;
+#pragma unroll
+        for (int jj = 0; jj < HALF; ++jj)
+            *reinterpret_cast<__half *>(qs + sw128_offset(chalf * 32 + jj, d & 63)) =
+                __float2half_rn(scale * __expf(G[jj]) * qval(jj) - v0[jj]);
+    }
+    tc_fence_before();
+    __syncthreads();
+
+    // Z = A^qk A^kk (rows 0..63 of a 128-row operand; rows 64..127 are filler):
+    // TMEM cols 0..63.
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        mma_panels(tmem, smem_u32(aqk), 0, smem_u32(akt), 0, 4, idesc_f16_f32(128, 64), false);
+        mma_commit(&sm.bar_mma);
+    }
+    // Q' out to the image while the tensor core works: 1024 chunks of 16 bytes
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int kk = tid + r * kPrepThreads, pnl = kk >> 9;
+        const uint4 u = *reinterpret_cast<const uint4 *>(sm.a1 + kOffQs + (kk << 4));
+        *reinterpret_cast<uint4 *>(img + (pnl ? IMG_Q1 : IMG_Q0) + ((kk & 511) << 4)) = u;
+    }
+    if (ok) ok = mbar_wait_bounded(&sm.bar_mma, mma_phase, kWaitCycles);
+    ok = __all_sync(0xffffffffu, ok);  // TMEM loads below are warp-collective
+    tc_fence_after();
+    if (ok) {
+        if (quad < 2) {
+            float v[32];
+            tmem_ld32(tmem_addr(tmem, quad * 32, chalf * 32), v);
+            store_quarter_f16_image(img + IMG_Z, quad * 32 + lane, chalf * 4, v);
+        }
     } else if (tid == 0) {
         atomicExch(status, (int)KDA_ERR_TIMEOUT);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 128);
+    if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 // ---------------------------------------------------------------------------
-// 3. the inter-chunk scan with fused outputs
+// 3. the inter-chunk scan: state only
 // ---------------------------------------------------------------------------
-struct ScanStage {
-    uint8_t wq[WQ_BYTES];        // [-W ; Q_hat]
-    uint8_t ke[KE_BYTES];        // K_end^T
-    uint8_t aa[3 * 8192];        // [A^kk | zeros | A^qk]
-    float gb[GB_BYTES / 4];      // Gamma_last [128], beta [64]
-    uint8_t pad[1024 - GB_BYTES % 1024];
-};
+// One CTA per (sequence, head, 64-wide value tile).  Per chunk n:
+//   D2[n & 1]  = P' (beta V)            (issued one chunk ahead: no S_c in it)
+//   D2[n & 1] += (-M') S_c              (the only dependency chain)
+//   S_c+1      = Diag(Gamma_last) S_c + D2[n & 1]
+// and the state entering each chunk goes out (f16, the output kernel's B
+// operand image) for the fully parallel output pass.
+constexpr int NSTAGE = 3;                   // image ring depth
+constexpr uint32_t SCAN_IMG = IMG_P + 16384;  // -M' and P': the scan's part of an image
+static_assert(SCAN_IMG == IMG_Q0, "the scan's operands lead the image");
 
 struct ScanSmem {
-    ScanStage st[2];
+    uint8_t st[NSTAGE][SCAN_IMG];  // -M' (32 KB) and P' (16 KB) of three chunks
     // B operands in MN-major (value columns contiguous) 128-byte-swizzled
-    // layout: one row of 64 f16 values per K index.
-    uint8_t sb[D * 128];         // S_c:    K = 128 key rows
-    uint8_t eb[C * 128];         // E:      K = 64 token rows
-    uint8_t bv[C * 128];         // beta V: K = 64 token rows
-    uint8_t ob[C * BV * 4];      // output tile staging for the TMA store (swizzled panels)
-    uint64_t full[2];            // stage loaded (producer -> compute)
-    uint64_t empty[2];           // stage released (compute -> producer)
-    uint64_t mma_e, mma_s;       // MMA groups done: E; state increment and outputs
+    // layout: one row of 64 f16 values per K index
+    uint8_t vs[NSTAGE][C * 128];   // the chunk's value tile, bf16 [64 tokens][64], 128 B swizzle
+    uint8_t sb[2][D * 128];      // S_c:    K = 128 key rows (also the source of its
+                                 // bulk copy out)
+    uint8_t bv[2][C * 128];      // beta V: K = 64 token rows
+    float gbs[NSTAGE][D + C];    // the chunk's Gamma_last [128] and beta [64]
+    uint64_t full[NSTAGE];       // stage loaded (bulk copy -> MMA issuer)
+    uint64_t empty[NSTAGE];      // stage consumed (tcgen05.commit -> producer)
+    uint64_t ready_s;            // S_c operand written (compute -> issuer)
+    uint64_t ready_bv[2];        // beta V operand written, per buffer
+    uint64_t mma_s;              // chunk's state increment complete
     uint32_t tmem;
+    volatile int32_t issued;     // bulk copies issued (error path drains them)
     volatile int32_t abort_flag;
 };
 
-constexpr int kScanThreads = 160;  // warps 0-3 compute, warp 4 streams operands in
-constexpr uint32_t kScanTmemCols = 128;  // D1 (BV columns) + D2 (BV columns)
+constexpr int kScanThreads = 192;  // warps 0-3 compute, 4 streams operands in, 5 issues MMAs
+constexpr uint32_t kScanTmemCols = 128;  // D2 ping-pong (2 x BV)
+constexpr uint32_t kStateImg = D * 128;  // one value tile of S_c, f16 image
 
-__device__ __forceinline__ void compute_barrier() {
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+// Barrier over the 128 compute threads that also ORs a predicate over them,
+// so that every one of them takes the same branch on the result.
+__device__ __forceinline__ bool compute_barrier_or(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, 1, 128, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
 }
 
-// B operand (MN-major, SW128, N = 64): K walks 16 rows = 2048 bytes per step.
+// A K-major (panels of 128-byte rows), B MN-major (N = 64, SW128): K walks
+// 32 bytes of A and 16 rows = 2048 bytes of B per step.
 __device__ __forceinline__ void mma_kmajor_a_mn_b(uint32_t d_tmem, uint32_t a_base,
                                                   uint32_t a_panel, uint32_t b_base, int ksteps,
                                                   uint32_t idesc, bool accumulate_first) {
@@ -593,27 +696,40 @@ __device__ __forceinline__ void mma_kmajor_a_mn_b(uint32_t d_tmem, uint32_t a_ba
     }
 }
 
-// 32 consecutive f16 values (4 swizzled 16-byte chunks) of one MN-major row.
+// 32 consecutive f16 values as 4 swizzled 16-byte chunks of one MN-major row.
+__device__ __forceinline__ uint4 pack8_f16(const float *v) {
+    uint4 u;
+    u.x = pack_f16x2(v[0], v[1]);
+    u.y = pack_f16x2(v[2], v[3]);
+    u.z = pack_f16x2(v[4], v[5]);
+    u.w = pack_f16x2(v[6], v[7]);
+    return u;
+}
 __device__ __forceinline__ void store_row32_f16(uint8_t *img, uint32_t row, uint32_t chunk0,
                                                 const float *v) {
 #pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
-        uint4 u;
-        u.x = pack_f16x2(v[c4 * 8 + 0], v[c4 * 8 + 1]);
-        u.y = pack_f16x2(v[c4 * 8 + 2], v[c4 * 8 + 3]);
-        u.z = pack_f16x2(v[c4 * 8 + 4], v[c4 * 8 + 5]);
-        u.w = pack_f16x2(v[c4 * 8 + 6], v[c4 * 8 + 7]);
-        *reinterpret_cast<uint4 *>(img + sw128_chunk(row, chunk0 + c4)) = u;
+    for (int c4 = 0; c4 < 4; ++c4)
+        *reinterpret_cast<uint4 *>(img + sw128_chunk(row, chunk0 + c4)) = pack8_f16(v + c4 * 8);
+}
+
+// beta V of one token row, 32 value columns (64 bytes of bf16 in x), as f16
+__device__ __forceinline__ void scale_row32(const uint4 (&x)[4], float b, float (&f)[32]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t w[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+            f[i * 8 + 2 * y] = b * __uint_as_float(w[y] << 16);
+            f[i * 8 + 2 * y + 1] = b * __uint_as_float(w[y] & 0xFFFF0000u);
+        }
     }
 }
 
-template <typename TOut>
 __global__ void __launch_bounds__(kScanThreads, 1)
-chunk_scan_kernel(const __grid_constant__ CUtensorMap out_map,
-                  const __nv_bfloat16 *__restrict__ v, const float *__restrict__ initial_state,
-                  const int32_t *__restrict__ cu, TOut *__restrict__ out,
-                  float *__restrict__ final_state, int32_t N, int32_t T, int32_t H, Scratch sc,
-                  int *status) {
+chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
+                  const float *__restrict__ initial_state,
+                  const int32_t *__restrict__ cu, float *__restrict__ final_state, int32_t N,
+                  int32_t T, int32_t H, Scratch sc, int *status) {
     extern __shared__ uint8_t smem_raw[];
     ScanSmem &sm = *reinterpret_cast<ScanSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -640,17 +756,16 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap out_map,
 
     bool ok = true;
     if (n_chunks > 0) {
-        for (int stg = 0; stg < 2; ++stg) {  // the constant zero blocks
-            uint4 *z = reinterpret_cast<uint4 *>(sm.st[stg].aa + 8192);
-            for (int idx = tid; idx < 8192 / 16; idx += kScanThreads) z[idx] = make_uint4(0, 0, 0, 0);
-        }
         if (tid == 0) {
-            for (int i = 0; i < 2; ++i) {
+            for (int i = 0; i < NSTAGE; ++i) {
                 mbar_init(&sm.full[i], 1);
-                mbar_init(&sm.empty[i], 128);  // every compute thread releases
+                mbar_init(&sm.empty[i], 1);
             }
-            mbar_init(&sm.mma_e, 1);
+            mbar_init(&sm.ready_s, 128);
+            mbar_init(&sm.ready_bv[0], 128);
+            mbar_init(&sm.ready_bv[1], 128);
             mbar_init(&sm.mma_s, 1);
+            sm.issued = 0;
             sm.abort_flag = 0;
             fence_mbar_init();
         }
@@ -658,203 +773,148 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap out_map,
             tmem_alloc(&sm.tmem, kScanTmemCols);
             tmem_relinquish();
         }
-        fence_proxy_async();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
         const uint32_t tmem = sm.tmem;
         constexpr uint32_t IDESC = idesc_f16_f32(128, BV) | (1u << 16);  // B MN-major
+        auto chunk_img = [&](int32_t n) {
+            return sc.img + ((size_t)(c_begin + n) * H + h) * IMG_STRIDE;
+        };
 
         if (warp == 4) {
-            // ---------------- producer: stream each chunk's operands in ----------------
-            for (int32_t n = 0; n < n_chunks; ++n) {
-                const int stg = n & 1;
-                if (n >= 2) {
-                    const bool got = mbar_wait_bounded(&sm.empty[stg], ((n >> 1) - 1) & 1,
-                                                       kWaitCycles);
+            // -------- producer: -M' and P' of a chunk, once its stage is free --------
+            if (lane == 0) {
+                for (int32_t n = 0; n < n_chunks; ++n) {
+                    const int stg = n % NSTAGE;
+                    if (n >= NSTAGE) {
+                        const bool got = mbar_wait_bounded(
+                            &sm.empty[stg], (uint32_t)(n / NSTAGE - 1) & 1u, kWaitCycles);
+                        if (!got || sm.abort_flag) {
+                            sm.abort_flag = 1;
+                            break;
+                        }
+                    }
+                    mbar_arrive_expect_tx(&sm.full[stg],
+                                          SCAN_IMG + C * 128 + (D + C) * (uint32_t)sizeof(float));
+                    bulk_g2s(sm.st[stg], chunk_img(n), SCAN_IMG, &sm.full[stg]);
+                    bulk_g2s(sm.gbs[stg], chunk_img(n) + IMG_GB, (D + C) * sizeof(float),
+                             &sm.full[stg]);
+                    tma_load_3d(sm.vs[stg], &v_map, vt * BV, h, ta + n * C, &sm.full[stg]);
+                    sm.issued = n + 1;
+                }
+            }
+            __syncwarp();
+        } else if (warp == 5) {
+            // -------- MMA issuer --------
+            if (lane == 0) {
+                int32_t done = 0;  // chunks whose state group was issued
+                for (int32_t n = 0; n < n_chunks; ++n) {
+                    const int stg = n % NSTAGE;
+                    const uint8_t *img = sm.st[stg];
+                    const uint32_t d2 = tmem + (uint32_t)(n & 1) * BV;
+                    // P' (beta V): needs only the chunk's own operands
+                    bool got = mbar_wait_bounded(&sm.full[stg], (uint32_t)(n / NSTAGE) & 1u,
+                                                 kWaitCycles) &&
+                               mbar_wait_bounded(&sm.ready_bv[n & 1], (uint32_t)(n >> 1) & 1u,
+                                                 kWaitCycles);
                     if (!got || sm.abort_flag) {
                         sm.abort_flag = 1;
                         break;
                     }
+                    tc_fence_after();
+                    mma_kmajor_a_mn_b(d2, smem_u32(img + IMG_P), 0, smem_u32(sm.bv[n & 1]), 4,
+                                      IDESC, false);
+                    // (-M') S_c once the state is in
+                    got = mbar_wait_bounded(&sm.ready_s, (uint32_t)n & 1u, kWaitCycles);
+                    if (!got || sm.abort_flag) {
+                        sm.abort_flag = 1;
+                        mma_commit(&sm.empty[stg]);  // keeps the drain below exact
+                        done = n + 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    mma_kmajor_a_mn_b(d2, smem_u32(img + IMG_MN), 16384,
+                                      smem_u32(sm.sb[n & 1]), 8, IDESC, true);
+                    mma_commit(&sm.mma_s);
+                    mma_commit(&sm.empty[stg]);  // the stage may be refilled after these
+                    done = n + 1;
                 }
-                const size_t ch = (size_t)(c_begin + n) * H + h;
-                ScanStage &S_ = sm.st[stg];
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&sm.full[stg],
-                                          WQ_BYTES + KE_BYTES + AK_BYTES + AQ_BYTES + GB_BYTES);
-                    bulk_g2s(S_.wq, sc.wq + ch * WQ_BYTES, WQ_BYTES, &sm.full[stg]);
-                    bulk_g2s(S_.ke, sc.ke + ch * KE_BYTES, KE_BYTES, &sm.full[stg]);
-                    bulk_g2s(S_.aa, sc.ak + ch * AK_BYTES, AK_BYTES, &sm.full[stg]);
-                    bulk_g2s(S_.aa + 16384, sc.aq + ch * AQ_BYTES, AQ_BYTES, &sm.full[stg]);
-                    bulk_g2s(S_.gb, sc.gb + ch * GB_BYTES, GB_BYTES, &sm.full[stg]);
-                }
-                __syncwarp();
+                // the stage-release arrivals of the last chunks (no one else waits
+                // for them) land before the shared memory goes away; the last one
+                // also means every MMA issued is done
+                for (int32_t j = max(done - NSTAGE, 0); j < done; ++j)
+                    if (!mbar_wait_bounded(&sm.empty[j % NSTAGE], (uint32_t)(j / NSTAGE) & 1u,
+                                           kWaitCycles))
+                        sm.abort_flag = 1;
             }
+            __syncwarp();
         } else {
             // ---------------- compute warps ----------------
-            // value tile of a chunk: thread -> token row tid/2, 32 columns (64 B),
-            // prefetched into registers one chunk ahead
+            // Everything a chunk needs arrives with its stage (no global loads in
+            // the loop: a barrier would wait for them).  beta V: thread -> token
+            // row tid/2, 32 value columns.
             const int vi = tid >> 1, vh = tid & 1;
-            uint4 vreg[4];
-            auto load_v = [&](int32_t n) {
-                const int32_t t0n = ta + n * C;
-                if (n < n_chunks && vi < min(C, tb - t0n)) {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(
-                        v + ((size_t)(t0n + vi) * H + h) * D + vt * BV + vh * 32);
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) vreg[x] = __ldg(src + x);
-                } else {
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) vreg[x] = make_uint4(0, 0, 0, 0);
-                }
-            };
-            // beta V of chunk n into the MN-major operand; then prefetch chunk n+1
             auto build_bv = [&](int32_t n) {
-                const float b = sm.st[n & 1].gb[128 + vi];
+                const int stg = n % NSTAGE;
+                const bool valid = vi < tb - (ta + n * C);  // rows past the sequence are zero
+                const float b = valid ? sm.gbs[stg][D + vi] : 0.f;
+                uint4 x[4];
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4)
+                    x[c4] = *reinterpret_cast<const uint4 *>(sm.vs[stg] +
+                                                             sw128_chunk(vi, vh * 4 + c4));
                 float f[32];
+                scale_row32(x, b, f);
+                store_row32_f16(sm.bv[n & 1], vi, vh * 4, f);
+                fence_proxy_async();
+                mbar_arrive(&sm.ready_bv[n & 1]);
+            };
+            auto wait_full = [&](int32_t n) {
+                if (!mbar_wait_bounded(&sm.full[n % NSTAGE], (uint32_t)(n / NSTAGE) & 1u,
+                                       kWaitCycles))
+                    sm.abort_flag = 1;
+            };
+            // S_c of chunk n as the MMA's B operand (f16); the same image goes out
+            // to global memory for the output pass as one bulk copy (below)
+            auto put_state = [&](int32_t n) {
 #pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                    const uint32_t w[4] = {vreg[x].x, vreg[x].y, vreg[x].z, vreg[x].w};
-#pragma unroll
-                    for (int y = 0; y < 4; ++y) {
-                        f[x * 8 + 2 * y] = b * __uint_as_float(w[y] << 16);
-                        f[x * 8 + 2 * y + 1] = b * __uint_as_float(w[y] & 0xFFFF0000u);
-                    }
-                }
-                store_row32_f16(sm.bv, vi, vh * 4, f);
-                load_v(n + 1);
+                for (int c8 = 0; c8 < 8; ++c8)
+                    *reinterpret_cast<uint4 *>(sm.sb[n & 1] + sw128_chunk(tid, c8)) =
+                        pack8_f16(&S[c8 * 8]);
+                fence_proxy_async();
+            };
+            auto state_img = [&](int32_t n) {
+                return sc.sst + (((size_t)(c_begin + n) * H + h) * NT + vt) * kStateImg;
             };
 
-            // outputs of chunk n from D1 rows 64..127 (warps 2 and 3: token = tid - 64).
-            // A full chunk goes out as one TMA tensor store from a staging tile; a
-            // partial chunk (the end of a sequence) writes its valid rows directly,
-            // so nothing past the sequence is touched.
-            auto store_outputs = [&](uint32_t d1n, int32_t n) {
-                const int32_t t0n = ta + n * C;
-                const int32_t Ln = min(C, tb - t0n);
-                const int i = tid - 64;
-                float o0[32], o1[32];
-                tmem_ld32x2(tmem_addr(d1n, warp * 32, 0), tmem_addr(d1n, warp * 32, 32), o0, o1);
-                if (Ln == C) {
-                    // staging: 128-byte column panels (1 for bf16, 2 for fp32), each
-                    // [64 rows x 128 B] in the 128-byte swizzle the TMA store expects
-                    if (tid == 64) bulk_wait_group_read<0>();  // staging free again
-                    asm volatile("bar.sync 2, 64;" ::: "memory");
-                    if constexpr (sizeof(TOut) == 2) {
-#pragma unroll
-                        for (int c8 = 0; c8 < 8; ++c8) {
-                            const float *src = c8 < 4 ? &o0[c8 * 8] : &o1[(c8 - 4) * 8];
-                            uint4 u;
-                            u.x = pack_bf16x2(src[0], src[1]);
-                            u.y = pack_bf16x2(src[2], src[3]);
-                            u.z = pack_bf16x2(src[4], src[5]);
-                            u.w = pack_bf16x2(src[6], src[7]);
-                            *reinterpret_cast<uint4 *>(sm.ob + sw128_chunk(i, c8)) = u;
-                        }
-                    } else {
-#pragma unroll
-                        for (int c16 = 0; c16 < 16; ++c16) {
-                            const float *src = c16 < 8 ? &o0[c16 * 4] : &o1[(c16 - 8) * 4];
-                            *reinterpret_cast<float4 *>(sm.ob + (c16 >> 3) * (C * 128) +
-                                                        sw128_chunk(i, c16 & 7)) =
-                                make_float4(src[0], src[1], src[2], src[3]);
-                        }
-                    }
-                    fence_proxy_async();
-                    asm volatile("bar.sync 2, 64;" ::: "memory");
-                    if (tid == 64) {
-                        constexpr int per_panel = 128 / (int)sizeof(TOut);
-#pragma unroll
-                        for (int pnl = 0; pnl < (int)sizeof(TOut) / 2; ++pnl)
-                            tma_store_3d(&out_map, sm.ob + pnl * (C * 128),
-                                         vt * BV + pnl * per_panel, h, t0n);
-                        bulk_commit_group();
-                    }
-                } else if (i < Ln) {
-                    TOut *dst = out + ((size_t)(t0n + i) * H + h) * D + vt * BV;
-                    if constexpr (sizeof(TOut) == 2) {
-#pragma unroll
-                        for (int j = 0; j < 32; j += 8) {
-                            uint4 u;
-                            u.x = pack_bf16x2(o0[j], o0[j + 1]);
-                            u.y = pack_bf16x2(o0[j + 2], o0[j + 3]);
-                            u.z = pack_bf16x2(o0[j + 4], o0[j + 5]);
-                            u.w = pack_bf16x2(o0[j + 6], o0[j + 7]);
-                            *reinterpret_cast<uint4 *>(dst + j) = u;
-                            u.x = pack_bf16x2(o1[j], o1[j + 1]);
-                            u.y = pack_bf16x2(o1[j + 2], o1[j + 3]);
-                            u.z = pack_bf16x2(o1[j + 4], o1[j + 5]);
-                            u.w = pack_bf16x2(o1[j + 6], o1[j + 7]);
-                            *reinterpret_cast<uint4 *>(dst + 32 + j) = u;
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            *reinterpret_cast<float4 *>(dst + j) =
-                                make_float4(o0[j], o0[j + 1], o0[j + 2], o0[j + 3]);
-                            *reinterpret_cast<float4 *>(dst + 32 + j) =
-                                make_float4(o1[j], o1[j + 1], o1[j + 2], o1[j + 3]);
-                        }
-                    }
-                }
-            };
-
-            load_v(0);
-            if (!mbar_wait_bounded(&sm.full[0], 0, kWaitCycles)) sm.abort_flag = 1;
+            wait_full(0);
+            float g = sm.gbs[0][tid];  // Gamma_last of chunk n (read before its stage is freed)
             build_bv(0);
-            const uint32_t d1 = tmem, d2 = tmem + BV;
-            fence_proxy_async();
-            compute_barrier();
-            if (tid == 0 && !sm.abort_flag) {
-                tc_fence_after();
-                // D1 = [A^kk ; 0] (beta V) of chunk 0
-                mma_kmajor_a_mn_b(d1, smem_u32(sm.st[0].aa), 0, smem_u32(sm.bv), 4, IDESC, false);
-            }
+            put_state(0);
             for (int32_t n = 0; n < n_chunks; ++n) {
-                const int stg = n & 1;
-                ScanStage &st = sm.st[stg];
-                const uint32_t par = n & 1;
-
-                // S_c operand (f16): thread = key row tid, 64 values
-                store_row32_f16(sm.sb, tid, 0, &S[0]);
-                store_row32_f16(sm.sb, tid, 4, &S[32]);
-                fence_proxy_async();
+                // the previous chunk's state copy has read sb[(n + 1) & 1]
+                if (tid == 0) bulk_wait_group_read<0>();
+                if (compute_barrier_or(sm.abort_flag != 0)) break;
                 tc_fence_before();
-                compute_barrier();
-                if (sm.abort_flag) break;
+                mbar_arrive(&sm.ready_s);
                 if (tid == 0) {
-                    tc_fence_after();
-                    // D1 += [-W ; Q_hat] S_c  -> rows 0..63: E = U - W S_c, rows 64..127: Q_hat S_c
-                    mma_kmajor_a_mn_b(d1, smem_u32(st.wq), 16384, smem_u32(sm.sb), 8, IDESC,
-                                      true);
-                    mma_commit(&sm.mma_e);
+                    bulk_s2g(state_img(n), sm.sb[n & 1], kStateImg);
+                    bulk_commit_group();
                 }
-                if (warp < 2) {
-                    if (!mbar_wait_bounded(&sm.mma_e, par, kWaitCycles)) sm.abort_flag = 1;
-                    tc_fence_after();
-                    float e0[32], e1[32];
-                    tmem_ld32x2(tmem_addr(d1, warp * 32, 0), tmem_addr(d1, warp * 32, 32), e0, e1);
-                    store_row32_f16(sm.eb, tid, 0, e0);
-                    store_row32_f16(sm.eb, tid, 4, e1);
+                const bool more = n + 1 < n_chunks;
+                float g_next = 0.f;
+                if (more) {
+                    // beta V of the next chunk (its buffer was last read two chunks ago)
+                    wait_full(n + 1);
+                    g_next = sm.gbs[(n + 1) % NSTAGE][tid];
+                    build_bv(n + 1);
                 }
-                fence_proxy_async();
-                tc_fence_before();
-                compute_barrier();
-                if (sm.abort_flag) break;
-                if (tid == 0) {
-                    tc_fence_after();
-                    // D2 = K_end^T E (state increment); D1 += [0 ; A^qk] E (outputs)
-                    mma_kmajor_a_mn_b(d2, smem_u32(st.ke), 0, smem_u32(sm.eb), 4, IDESC, false);
-                    mma_kmajor_a_mn_b(d1, smem_u32(st.aa) + 8192, 0, smem_u32(sm.eb), 4, IDESC,
-                                      true);
-                    mma_commit(&sm.mma_s);
-                }
-                if (!mbar_wait_bounded(&sm.mma_s, par, kWaitCycles)) sm.abort_flag = 1;
+                if (!mbar_wait_bounded(&sm.mma_s, (uint32_t)n & 1u, kWaitCycles))
+                    sm.abort_flag = 1;
                 tc_fence_after();
                 {
-                    const float g = st.gb[tid];
-                    // this thread's reads of chunk n's stage are done (MMAs completed)
-                    mbar_arrive(&sm.empty[stg]);
+                    const uint32_t d2 = tmem + (uint32_t)(n & 1) * BV;
                     float ds0[32], ds1[32];
                     tmem_ld32x2(tmem_addr(d2, warp * 32, 0), tmem_addr(d2, warp * 32, 32), ds0,
                                 ds1);
@@ -864,35 +924,22 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap out_map,
                         S[32 + j] = fmaf(g, S[32 + j], ds1[j]);
                     }
                 }
-                if (warp >= 2) store_outputs(d1, n);
-                // next chunk's beta V, and its U on the tensor core ahead of time
-                const bool more = n + 1 < n_chunks;
-                if (more) {
-                    if (!mbar_wait_bounded(&sm.full[(n + 1) & 1], ((n + 1) >> 1) & 1, kWaitCycles))
-                        sm.abort_flag = 1;
-                    build_bv(n + 1);
-                    fence_proxy_async();
-                }
-                tc_fence_before();
-                compute_barrier();
-                if (sm.abort_flag) break;
-                if (tid == 0 && more) {
-                    tc_fence_after();
-                    mma_kmajor_a_mn_b(d1, smem_u32(sm.st[(n + 1) & 1].aa), 0, smem_u32(sm.bv), 4,
-                                      IDESC, false);
-                }
+                g = g_next;
+                if (more) put_state(n + 1);
             }
-            if (tid == 64) bulk_wait_group_all();  // output tiles written
-            if (sm.abort_flag) ok = false;
+            if (tid == 0) bulk_wait_group_all();  // state images written
         }
         __syncthreads();
         if (sm.abort_flag) {
             ok = false;
-            if (tid == 0) atomicExch(status, (int)KDA_ERR_TIMEOUT);
-            // let copies already in flight land before the shared memory goes away
-            if (tid == 0)
-                for (int stg = 0; stg < 2; ++stg)
-                    (void)mbar_wait_bounded(&sm.full[stg], 0, kWaitCycles / 8);
+            if (tid == 0) {
+                atomicExch(status, (int)KDA_ERR_TIMEOUT);
+                // copies already in flight land before the shared memory goes away
+                const int32_t iss = sm.issued;
+                for (int32_t j = max(iss - NSTAGE, 0); j < iss; ++j)
+                    (void)mbar_wait_bounded(&sm.full[j % NSTAGE], (uint32_t)(j / NSTAGE) & 1u,
+                                            kWaitCycles);
+            }
         }
         tc_fence_before();
         __syncthreads();
@@ -907,15 +954,188 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap out_map,
     }
 }
 
+// ---------------------------------------------------------------------------
+// 4. outputs: O = Q' S_c + Z (beta V), one CTA per (chunk, head)
+// ---------------------------------------------------------------------------
+// Fully parallel once the scan has written every S_c.  128 threads; the
+// A operands are 128-row tiles whose first 64 rows are filler (see IMG_*),
+// so the outputs sit in TMEM lanes 64..127 (warps 2 and 3).
+constexpr uint32_t OUT_IMG_OFF = IMG_Q0 - 8192;      // filler, Q' keys 0..63, Z, Q' keys 64..
+constexpr uint32_t OUT_IMG_BYTES = IMG_GB - OUT_IMG_OFF;
+static_assert(OUT_IMG_OFF % 1024 == 0 && OUT_IMG_BYTES == 32768, "output operand region");
+
+struct OutSmem {
+    uint8_t qz[OUT_IMG_BYTES];   // [filler ; Q'] panels and [filler ; Z]
+    uint8_t sS[NT][kStateImg];   // S_c, one MN-major image per value tile
+    uint8_t bv[NT][C * 128];     // beta V, per value tile
+    uint64_t bar_in, bar_mma;
+    uint32_t tmem;
+};
+constexpr int kOutThreads = 128;
+
+template <typename TOut>
+__global__ void __launch_bounds__(kOutThreads)
+chunk_out_kernel(const __grid_constant__ CUtensorMap out_map, const __nv_bfloat16 *__restrict__ v,
+                 const int32_t *__restrict__ cu, TOut *__restrict__ out, int32_t N, int32_t T,
+                 int32_t H, Scratch sc, int *status) {
+    extern __shared__ uint8_t smem_raw[];
+    OutSmem &sm = *reinterpret_cast<OutSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int32_t c = blockIdx.x, h = blockIdx.y;
+    const int32_t total = sc.chunk_off[N];
+    if (c >= total) return;
+    const int32_t s = find_seq(sc.chunk_off, N, c);
+    int32_t ta, tb;
+    seq_bounds(cu, s, T, ta, tb);
+    const int32_t t0 = ta + (c - sc.chunk_off[s]) * C;
+    const int32_t L = min(C, tb - t0);
+    const uint8_t *img = sc.img + ((size_t)c * H + h) * IMG_STRIDE;
+
+    if (tid == 0) {
+        mbar_init(&sm.bar_in, 1);
+        mbar_init(&sm.bar_mma, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&sm.bar_in, OUT_IMG_BYTES + NT * kStateImg);
+        bulk_g2s(sm.qz, img + OUT_IMG_OFF, OUT_IMG_BYTES, &sm.bar_in);
+        bulk_g2s(sm.sS, sc.sst + ((size_t)c * H + h) * NT * kStateImg, NT * kStateImg,
+                 &sm.bar_in);
+    }
+    if (warp == 0) {
+        tmem_alloc(&sm.tmem, 128);
+        tmem_relinquish();
+    }
+    // beta V: thread -> token tid / 2, value half tid % 2 (= value tile)
+    {
+        const int i = tid >> 1, half = tid & 1;
+        uint4 x[2][4];
+        float b = 0.f;
+        if (i < L) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                v + ((size_t)(t0 + i) * H + h) * D + half * BV);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[j >> 2][j & 3] = __ldg(src + j);
+            b = reinterpret_cast<const float *>(img + IMG_GB)[128 + i];
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[j >> 2][j & 3] = make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 2; ++q4) {
+            float f[32];
+            scale_row32(x[q4], b, f);
+            store_row32_f16(sm.bv[half], i, q4 * 4, f);
+        }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem;
+    bool ok = mbar_wait_bounded(&sm.bar_in, 0, kWaitCycles);
+    if (tid == 0 && ok) {
+        constexpr uint32_t IDESC = idesc_f16_f32(128, BV) | (1u << 16);  // B MN-major
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const uint32_t d = tmem + t * BV;
+            mma_kmajor_a_mn_b(d, smem_u32(sm.qz), 16384, smem_u32(sm.sS[t]), 8, IDESC, false);
+            mma_kmajor_a_mn_b(d, smem_u32(sm.qz) + (IMG_Z - 8192 - OUT_IMG_OFF), 0,
+                              smem_u32(sm.bv[t]), 4, IDESC, true);
+        }
+        mma_commit(&sm.bar_mma);
+    }
+    if (ok) ok = mbar_wait_bounded(&sm.bar_mma, 0, kWaitCycles);
+    tc_fence_after();
+    ok = !__syncthreads_or(!ok);  // one verdict for all (warps 2-3 share a barrier below)
+    if (ok && warp >= 2) {
+        const int i = tid - 64;  // token
+        if (L == C) {
+            // swizzled 128-byte column panels (over the consumed operands), then
+            // TMA tensor stores
+            uint8_t *ob = sm.qz;
+            static_assert(C * D * 4 <= OUT_IMG_BYTES + NT * kStateImg, "staging fits");
+            constexpr int kPanelCols = 128 / (int)sizeof(TOut);
+#pragma unroll
+            for (int cb = 0; cb < D; cb += 32) {
+                float o[32];
+                tmem_ld32(tmem_addr(tmem, warp * 32, cb), o);
+#pragma unroll
+                for (int j = 0; j < 32; j += 16 / (int)sizeof(TOut)) {
+                    const int col = cb + j, pnl = col / kPanelCols;
+                    const int chunk = (col % kPanelCols) * (int)sizeof(TOut) / 16;
+                    uint4 u;
+                    if constexpr (sizeof(TOut) == 2) {
+                        u.x = pack_bf16x2(o[j], o[j + 1]);
+                        u.y = pack_bf16x2(o[j + 2], o[j + 3]);
+                        u.z = pack_bf16x2(o[j + 4], o[j + 5]);
+                        u.w = pack_bf16x2(o[j + 6], o[j + 7]);
+                    } else {
+                        u = make_uint4(__float_as_uint(o[j]), __float_as_uint(o[j + 1]),
+                                       __float_as_uint(o[j + 2]), __float_as_uint(o[j + 3]));
+                    }
+                    *reinterpret_cast<uint4 *>(ob + pnl * (C * 128) + sw128_chunk(i, chunk)) = u;
+                }
+            }
+            fence_proxy_async();
+            asm volatile("bar.sync 2, 64;" ::: "memory");
+            if (tid == 64) {
+#pragma unroll
+                for (int pnl = 0; pnl < D / kPanelCols; ++pnl)
+                    tma_store_3d(&out_map, ob + pnl * (C * 128), pnl * kPanelCols, h, t0);
+                bulk_commit_group();
+                bulk_wait_group_all();
+            }
+        } else {
+            // a sequence's last, partial chunk: valid rows only, plain stores
+            // (the TMEM loads are warp-collective: every lane takes part)
+            TOut *dst = out + ((size_t)(t0 + min(i, L - 1)) * H + h) * D;
+#pragma unroll
+            for (int cb = 0; cb < D; cb += 32) {
+                float o[32];
+                tmem_ld32(tmem_addr(tmem, warp * 32, cb), o);
+                if (i >= L) continue;
+                if constexpr (sizeof(TOut) == 2) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 8) {
+                        uint4 u;
+                        u.x = pack_bf16x2(o[j], o[j + 1]);
+                        u.y = pack_bf16x2(o[j + 2], o[j + 3]);
+                        u.z = pack_bf16x2(o[j + 4], o[j + 5]);
+                        u.w = pack_bf16x2(o[j + 6], o[j + 7]);
+                        *reinterpret_cast<uint4 *>(dst + cb + j) = u;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4 *>(dst + cb + j) =
+                            make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+                }
+            }
+        }
+    }
+    if (!ok && tid == 0) atomicExch(status, (int)KDA_ERR_TIMEOUT);
+    if (!ok && tid == 0) {
+        // let the loads land before the shared memory goes away
+        (void)mbar_wait_bounded(&sm.bar_in, 0, kWaitCycles);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
 constexpr size_t kPrepSmem = sizeof(PrepSmem) + 1024;
 constexpr size_t kScanSmem = sizeof(ScanSmem) + 1024;
+constexpr size_t kOutSmem = sizeof(OutSmem) + 1024;
+static_assert(kScanSmem <= 227 * 1024, "scan shared memory");
+static_assert(2 * kOutSmem <= 228 * 1024 - 2 * 1024, "two output CTAs per SM");
+static_assert(2 * kPrepSmem <= 228 * 1024 - 2 * 1024, "two prep CTAs per SM");
 
 }  // namespace
 
 size_t chunk_tc_workspace_bytes(int32_t N, int32_t T, int32_t H) {
     const size_t nch = max_chunks(N, T) * (size_t)H;
-    return align256(nch * WQ_BYTES) + align256(nch * KE_BYTES) + align256(nch * AK_BYTES) +
-           align256(nch * AQ_BYTES) + align256(nch * GB_BYTES) +
+    return align256(nch * IMG_STRIDE) + align256(nch * NT * (size_t)(D * 128)) +
            align256(((size_t)N + 1) * sizeof(int32_t));
 }
 
@@ -936,17 +1156,17 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // [T, H, D] row-major tensor as a 3-D map {D, H, T}; box = one head's
 // [64 tokens x 128 channels] tile.  Rows past T read as zero.
 bool encode_tile_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, size_t esize,
-                     int32_t T, int32_t H) {
+                     int32_t T, int32_t H, uint32_t box_x = D,
+                     CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
     const cuuint64_t strides[2] = {(cuuint64_t)D * esize, (cuuint64_t)H * D * esize};
-    const cuuint32_t box[3] = {(cuuint32_t)D, 1u, (cuuint32_t)C};
+    const cuuint32_t box[3] = {box_x, 1u, (cuuint32_t)C};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     return enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspace_bytes,
@@ -979,15 +1199,29 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
     a.clock->mark(stream);
 
     const dim3 sgrid((unsigned)(a.N * NT), (unsigned)a.H);
-    // output tiles [64 tokens x 64 columns] of one head; unused when T == 0
-    CUtensorMap out_map;
-    memset(&out_map, 0, sizeof(out_map));
+    // value tiles [64 tokens x 64 columns] of one head, 128-byte swizzle; unused when T == 0
+    CUtensorMap v_map;
+    memset(&v_map, 0, sizeof(v_map));
+    if (a.T > 0 && !encode_tile_map(&v_map, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H,
+                                    BV, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kScanSmem);
+    if (e != cudaSuccess) return e;
+    chunk_scan_kernel<<<sgrid, kScanThreads, kScanSmem, stream>>>(
+        v_map, a.initial_state, a.cu_seqlens, a.final_state, a.N, a.T, a.H, sc, a.status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    a.clock->mark(stream);
+
     if (a.T > 0) {
+        // output tiles [64 tokens x 128-byte column panel] of one head
+        CUtensorMap out_map;
+        memset(&out_map, 0, sizeof(out_map));
         auto enc = tensor_map_encoder();
         const size_t es = a.out_f32 ? 4 : 2;
         const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.H, (cuuint64_t)a.T};
         const cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)a.H * D * es};
-        // one 128-byte column panel per box, 128-byte swizzle
         const cuuint32_t box[3] = {(cuuint32_t)(128 / es), 1u, (cuuint32_t)C};
         const cuuint32_t estr[3] = {1u, 1u, 1u};
         if (!enc ||
@@ -996,21 +1230,26 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-    }
-    if (a.out_f32) {
-        auto kern = chunk_scan_kernel<float>;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
+        const dim3 ogrid((unsigned)max_chunks(a.N, a.T), (unsigned)a.H);
+        if (a.out_f32) {
+            auto kern = chunk_out_kernel<float>;
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kOutSmem);
+            if (e != cudaSuccess) return e;
+            kern<<<ogrid, kOutThreads, kOutSmem, stream>>>(
+                out_map, static_cast<const __nv_bfloat16 *>(a.v), a.cu_seqlens,
+                static_cast<float *>(a.out), a.N, a.T, a.H, sc, a.status);
+        } else {
+            auto kern = chunk_out_kernel<__nv_bfloat16>;
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kOutSmem);
+            if (e != cudaSuccess) return e;
+            kern<<<ogrid, kOutThreads, kOutSmem, stream>>>(
+                out_map, static_cast<const __nv_bfloat16 *>(a.v), a.cu_seqlens,
+                static_cast<__nv_bfloat16 *>(a.out), a.N, a.T, a.H, sc, a.status);
+        }
+        e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        kern<<<sgrid, kScanThreads, kScanSmem, stream>>>(
-            out_map, static_cast<const __nv_bfloat16 *>(a.v), a.initial_state, a.cu_seqlens,
-            static_cast<float *>(a.out), a.final_state, a.N, a.T, a.H, sc, a.status);
-    } else {
-        auto kern = chunk_scan_kernel<__nv_bfloat16>;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
-        if (e != cudaSuccess) return e;
-        kern<<<sgrid, kScanThreads, kScanSmem, stream>>>(
-            out_map, static_cast<const __nv_bfloat16 *>(a.v), a.initial_state, a.cu_seqlens,
-            static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.N, a.T, a.H, sc, a.status);
     }
     a.clock->mark(stream);
     return cudaGetLastError();

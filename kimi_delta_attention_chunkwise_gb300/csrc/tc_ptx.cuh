@@ -91,6 +91,14 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// bulk async copy shared -> global, bulk-group completion (addresses 16-byte
+// aligned, size a multiple of 16)
+__device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+
 // Tiled tensor load (TMA), 3-D coordinates {x innermost, y, z}; the tensor
 // map lives in kernel parameter space (__grid_constant__).
 __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int32_t x, int32_t y,
