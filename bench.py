@@ -200,6 +200,7 @@ def stage_work(d: int, C: int):
 PROFILE_FILES = {
     "prep": "chunk_prep_prefill_T4096_H16.md",
     "scan": "chunk_scan_prefill_T4096_H16.md",
+    "out": "chunk_out_prefill_T4096_H16.md",
     "recurrent_step": "recurrent_step_decode_256x32_d128.md",
 }
 

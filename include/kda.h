@@ -168,8 +168,8 @@ kdaStatus_t kda_chunk_fwd_ws_timed(const void *q, const void *k, const void *v,
  *   - The array is held on every GPU that loads the library, until exit.
  *   - Problems whose scratch (kda_chunk_fwd_workspace_size) exceeds
  *     KDA_STATIC_SCRATCH_BYTES are rejected with KDA_ERR_UNSUPPORTED before
- *     anything runs.  With H heads that is about (T/64 + N + 1) * H > 1000
- *     (chunk, head) pairs, e.g. more than ~3,900 tokens of one 16-head
+ *     anything runs.  With H heads that is about (T/64 + N + 1) * H > 620
+ *     (chunk, head) pairs, e.g. more than ~2,300 tokens of one 16-head
  *     sequence.
  *   - All calls share the one array: calls whose GPU work overlaps (other
  *     streams, other host threads) race on it and give wrong results, so

@@ -15,26 +15,35 @@
 //   S_c+1  = Diag(exp(G_last)) S_c + K_end^T E,
 //            K_end_i = exp(G_last - G_i) * k_i                   sec. 6.4
 //
-// Three launches on the caller's stream:
+// The engine regroups the last two lines (associativity only) so that the
+// serial scan holds one matrix product per chunk:
+//
+//   M' = K_end^T W,  P' = K_end^T A^kk,  Q' = Q_hat - A^qk W,  Z = A^qk A^kk
+//   S_c+1 = Diag(exp(G_last)) S_c + P' (beta V) - M' S_c
+//   O     = Q' S_c + Z (beta V)
+//
+// Four launches on the caller's stream:
 //   1. chunk_table  -- cu_seqlens -> first chunk index of every sequence
 //                      (chunks restart at each sequence start).
 //   2. chunk_prep   -- one CTA per (chunk, head), fully parallel: G, the
 //                      decayed [K;Q] K^T products on the tensor core, the
-//                      triangular solve, W on the tensor core, and the
-//                      boundary-facing factors.  Writes bf16 operand images
-//                      (already in the 128-byte-swizzled shared-memory
-//                      layout) to scratch.
-//   3. chunk_scan   -- one CTA per (sequence, head, 32-wide value tile):
+//                      triangular solve, and W, M', P', Q', Z on the tensor
+//                      core.  Writes f16 operand images (already in the
+//                      128-byte-swizzled shared-memory layout) to scratch.
+//   3. chunk_scan   -- one CTA per (sequence, head, 64-wide value tile):
 //                      the only serial loop, over the chunks of a sequence.
-//                      The fp32 state tile lives in registers; per chunk four
-//                      tcgen05 MMAs ([A^kk;0](beta V), [-W;Q_hat] S_c,
-//                      K_end^T E, [0;A^qk] E) and the next chunks' operands
-//                      stream in with bulk async copies (double buffered).
+//                      The fp32 state tile lives in registers; per chunk one
+//                      dependent group of tcgen05 MMAs (-M' S_c, with
+//                      P' (beta V) issued a chunk ahead), operands streamed
+//                      in by a producer warp, and the state entering each
+//                      chunk written out (f16) for the output pass.
+//   4. chunk_out    -- one CTA per (chunk, head), fully parallel: the
+//                      outputs from Q', Z, v and the stored states.
 //
 // Precision: every tensor-core product accumulates in fp32 (TMEM).  The
 // decayed [K;Q] K^T product takes tf32 operands (the exp factors need fp32
-// range); every other operand (A^kk, A^qk, W, Q_hat, K_end, beta V, E and
-// the state S_c) is fp16, whose 11-bit significand keeps the result within
+// range); every other operand (A^kk, A^qk, W, K_end, M', P', Q', Z, beta V
+// and the state S_c) is fp16, whose 11-bit significand keeps the result within
 // the parity bound where bf16 operands (8 bits) do not.  The state itself
 // stays fp32 in registers across the whole sequence.
 //
@@ -183,12 +192,13 @@ __device__ __forceinline__ int32_t find_seq(const int32_t *off, int32_t N, int32
 // first tenant is done:
 //   a1: g tile (TMA, f32 [64][128]) -> tf32 [K_tilde ; Q_tilde], 128 rows x
 //       128 K in 4 panels (64 KB) -> R, X (= A^kk) and the solve's block
-//       products (fp32), with A^qk (f16, at kOffAqk) kept beside them ->
-//       W^T (f16, at 0), Q' staging (f16, at kOffQs), A^qk, K_end^T (f16, at
-//       kOffKe);
+//       products (fp32), with A^qk and K_end^T (f16, at kOffAqk, kOffKe) kept
+//       beside them -> W^T (f16, at 0) -> the staging of the image's -M', P'
+//       and Q' panels, in image order;
 //   b1: k and q tiles (TMA, bf16 [64][128] each) -> tf32 K_hat, 64 rows x
 //       128 K in 4 panels (32 KB) (slow path: G f32 [64][128]) -> A^kk and
-//       A^kk^T (f16, 8 KB each) and (beta Gamma K)^T (f16, 128 x 64, 16 KB).
+//       A^kk^T (f16, 8 KB each) and (beta Gamma K)^T (f16, 128 x 64, 16 KB)
+//       -> Z staging (at 0).
 constexpr int kPrepThreads = 256;
 constexpr int HALF = C / 2;
 
@@ -204,7 +214,6 @@ struct PrepSmem {
 };
 constexpr uint32_t kOffX = C * (C + 1) * 4;        // X after R inside a1
 constexpr uint32_t kOffTb = 2 * C * (C + 1) * 4;   // block products after X
-constexpr uint32_t kOffQs = 16384;                 // Q' staging (2 x 8 KB) inside a1
 constexpr uint32_t kOffAqk = 40960;                // A^qk (f16) inside a1
 constexpr uint32_t kOffKe = 49152;                 // K_end^T (f16) inside a1
 constexpr uint32_t kOffAkT = 8192;                 // A^kk^T after A^kk inside b1
@@ -242,6 +251,51 @@ __device__ __forceinline__ void store_quarter_f16_image(uint8_t *img, uint32_t r
     }
 }
 
+// One level of the blocked triangular inverse: for the block pairs (I, J)
+// with I - J = DIST, T_IJ = sum_{K=J}^{I-1} R_IK X_KJ, then X_IJ = -X_II T_IJ.
+// 2 x 2 output tiles per thread, NBLK x 64 tiles.
+template <int DIST>
+__device__ __forceinline__ void solve_blocks_below(float (*R)[C + 1], float (*X)[C + 1],
+                                                   float (*Tb)[16][17], int tid) {
+    constexpr int NBLK = 4 - DIST;
+    const int bi = tid >> 6, t = tid & 63, r0 = (t >> 3) * 2, c0 = (t & 7) * 2;
+    const int I = bi + DIST, J = bi;
+    if (tid < NBLK * 64) {
+        float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < 16 * DIST; ++kk) {
+            const float ra = R[I * 16 + r0][J * 16 + kk], rb = R[I * 16 + r0 + 1][J * 16 + kk];
+            const float xa = X[J * 16 + kk][J * 16 + c0], xb = X[J * 16 + kk][J * 16 + c0 + 1];
+            a00 = fmaf(ra, xa, a00);
+            a01 = fmaf(ra, xb, a01);
+            a10 = fmaf(rb, xa, a10);
+            a11 = fmaf(rb, xb, a11);
+        }
+        Tb[bi][r0][c0] = a00;
+        Tb[bi][r0][c0 + 1] = a01;
+        Tb[bi][r0 + 1][c0] = a10;
+        Tb[bi][r0 + 1][c0 + 1] = a11;
+    }
+    __syncthreads();
+    if (tid < NBLK * 64) {
+        float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const float xa = X[I * 16 + r0][I * 16 + m], xb = X[I * 16 + r0 + 1][I * 16 + m];
+            const float ta = Tb[bi][m][c0], tb = Tb[bi][m][c0 + 1];
+            a00 = fmaf(xa, ta, a00);
+            a01 = fmaf(xa, tb, a01);
+            a10 = fmaf(xb, ta, a10);
+            a11 = fmaf(xb, tb, a11);
+        }
+        X[I * 16 + r0][J * 16 + c0] = -a00;
+        X[I * 16 + r0][J * 16 + c0 + 1] = -a01;
+        X[I * 16 + r0 + 1][J * 16 + c0] = -a10;
+        X[I * 16 + r0 + 1][J * 16 + c0 + 1] = -a11;
+    }
+    __syncthreads();
+}
+
 struct PrepMaps {
     CUtensorMap q, k, g;  // [T, H, D] viewed as {D, H, T}, box {128, 1, 64}
 };
@@ -263,6 +317,7 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
     uint8_t *aqk = sm.a1 + kOffAqk;   // A^qk, f16 panel
     uint8_t *ket = sm.a1 + kOffKe;    // K_end^T, f16 panel
     uint8_t *wt = sm.a1;              // W^T, f16 panel (after the solve)
+    uint8_t *zst = sm.b1;             // Z staging (after the MMAs that read A^kk)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t c = blockIdx.x, h = blockIdx.y;
@@ -462,49 +517,28 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
     for (int idx = tid; idx < C * (C + 1); idx += kPrepThreads) (&X[0][0])[idx] = 0.f;
     __syncthreads();
 
-    // sec. 6.3: A^kk = (I + R)^-1, unit lower triangular, fp32, 16 x 16 blocks.
+    // sec. 6.3: A^kk = (I + R)^-1, unit lower triangular, fp32.  The 16 x 16
+    // diagonal blocks by right-looking substitution (one column per thread),
+    // then the blocks below them, nearest first:
+    //   X_IJ = -X_II sum_{K=J}^{I-1} R_IK X_KJ
     if (tid < C) {
-        const int b = tid >> 4, cc = tid & 15, o = b * 16;
-        float x[16];
+        const int o = (tid >> 4) * 16, cc = tid & 15;
+        float x[16], acc[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float acc2 = 0.f;
+        for (int r = 0; r < 16; ++r) acc[r] = 0.f;
 #pragma unroll
-            for (int m = 0; m < 15; ++m)
-                if (m < r && m >= cc) acc2 += R[o + r][o + m] * x[m];
-            x[r] = (r < cc) ? 0.f : (r == cc ? 1.f : -acc2);
+        for (int m = 0; m < 16; ++m) {
+            x[m] = m < cc ? 0.f : (m == cc ? 1.f : -acc[m]);
+#pragma unroll
+            for (int r = m + 1; r < 16; ++r) acc[r] = fmaf(R[o + r][o + m], x[m], acc[r]);
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) X[o + r][o + cc] = x[r];
     }
     __syncthreads();
-#pragma unroll 1
-    for (int dist = 1; dist < 4; ++dist) {
-        const int nblk = 4 - dist;
-        // T_IJ = sum_{K=J}^{I-1} R_IK X_KJ
-        for (int e = tid; e < nblk * 256; e += kPrepThreads) {
-            const int bi = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-            const int I = bi + dist, J = bi;
-            float acc2 = 0.f;
-            for (int K = J; K < I; ++K) {
-#pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    acc2 += R[I * 16 + r][K * 16 + m] * X[K * 16 + m][J * 16 + cc];
-            }
-            Tb[bi][r][cc] = acc2;
-        }
-        __syncthreads();
-        // X_IJ = -X_II T_IJ
-        for (int e = tid; e < nblk * 256; e += kPrepThreads) {
-            const int bi = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-            const int I = bi + dist, J = bi;
-            float acc2 = 0.f;
-#pragma unroll
-            for (int m = 0; m < 16; ++m) acc2 += X[I * 16 + r][I * 16 + m] * Tb[bi][m][cc];
-            X[I * 16 + r][J * 16 + cc] = -acc2;
-        }
-        __syncthreads();
-    }
+    solve_blocks_below<1>(R, X, Tb, tid);
+    solve_blocks_below<2>(R, X, Tb, tid);
+    solve_blocks_below<3>(R, X, Tb, tid);
     // A^kk (rows i) and A^kk^T (rows j), f16
     if (tid < 2 * C) {
         const int row = tid >> 1, q4 = tid & 1;
@@ -534,11 +568,13 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
     __syncthreads();
 
     const int quad = warp & 3, chalf = warp >> 2;  // TMEM lanes 32*quad.., column half
-    // W^T = (beta Gamma K)^T A^kk^T on the tensor core (f16): TMEM cols 64..127.
+    // W^T = (beta Gamma K)^T A^kk^T (TMEM cols 64..127) and Z = A^qk A^kk (cols
+    // 0..63; rows 0..63 of a 128-row operand whose rows 64..127 are filler).
     if (tid == 0 && ok) {
         tc_fence_after();
         mma_panels(tmem + 64, smem_u32(a2), 0, smem_u32(b2), 0, 4, idesc_f16_f32(128, 64),
                    false);
+        mma_panels(tmem, smem_u32(aqk), 0, smem_u32(akt), 0, 4, idesc_f16_f32(128, 64), false);
         mma_commit(&sm.bar_mma);
     }
     if (ok) ok = mbar_wait_bounded(&sm.bar_mma, mma_phase, kWaitCycles);
@@ -553,6 +589,11 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = 0.f;
         store_quarter_f16_image(wt, d, chalf * 4, v);
+        // Z rows 0..63 -> staging in the A^kk slot (read by the MMAs just done)
+        if (quad < 2) {
+            if (ok) tmem_ld32(tmem_addr(tmem, quad * 32, chalf * 32), v);
+            store_quarter_f16_image(zst, quad * 32 + lane, chalf * 4, v);
+        }
     }
     fence_proxy_async();
     tc_fence_before();
@@ -571,62 +612,46 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
     }
     if (ok) ok = mbar_wait_bounded(&sm.bar_mma, mma_phase, kWaitCycles);
     ok = __all_sync(0xffffffffu, ok);  // TMEM loads below are warp-collective
-    mma_phase ^= 1;
     tc_fence_after();
+    // Every operand is consumed: a1 becomes the staging of the image's first
+    // 72 KB (-M' | P' | Q' keys 0..63 | . | Q' keys 64..127), Z waits in b1.
     if (ok) {
         float v0[32], v1[32];
         // -M' row d (key), columns (keys) 64*chalf.. -> image panel chalf
-        tmem_ld32x2(tmem_addr(tmem, quad * 32, chalf * 64), tmem_addr(tmem, quad * 32, chalf * 64 + 32),
-                    v0, v1);
+        tmem_ld32x2(tmem_addr(tmem, quad * 32, chalf * 64),
+                    tmem_addr(tmem, quad * 32, chalf * 64 + 32), v0, v1);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             v0[j] = -v0[j];
             v1[j] = -v1[j];
         }
-        store_quarter_f16_image(img + IMG_MN + chalf * 16384, d, 0, v0);
-        store_quarter_f16_image(img + IMG_MN + chalf * 16384, d, 4, v1);
+        store_quarter_f16_image(sm.a1 + IMG_MN + chalf * 16384, d, 0, v0);
+        store_quarter_f16_image(sm.a1 + IMG_MN + chalf * 16384, d, 4, v1);
         // P' row d, tokens 32*chalf..
         tmem_ld32(tmem_addr(tmem, quad * 32, 128 + chalf * 32), v0);
-        store_quarter_f16_image(img + IMG_P, d, chalf * 4, v0);
+        store_quarter_f16_image(sm.a1 + IMG_P, d, chalf * 4, v0);
         // Q'[i][d] = s Gamma_i q_i[d] - (A^qk W)[i][d], tokens i = 32*chalf + jj (this
-        // thread's own tokens), staged as two 64-row panels
+        // thread's own tokens), as two 64-row panels
         tmem_ld32(tmem_addr(tmem, quad * 32, 192 + chalf * 32), v0);
-        uint8_t *qs = sm.a1 + kOffQs + (d >> 6) * 8192u;
+        uint8_t *qs = sm.a1 + IMG_Q0 + (d >> 6) * 8192u;  // staged at IMG_Q0 and IMG_Z
 #pragma unroll
         for (int jj = 0; jj < HALF; ++jj)
             *reinterpret_cast<__half *>(qs + sw128_offset(chalf * 32 + jj, d & 63)) =
                 __float2half_rn(scale * __expf(G[jj]) * qval(jj) - v0[jj]);
-    }
-    tc_fence_before();
-    __syncthreads();
-
-    // Z = A^qk A^kk (rows 0..63 of a 128-row operand; rows 64..127 are filler):
-    // TMEM cols 0..63.
-    if (tid == 0 && ok) {
-        tc_fence_after();
-        mma_panels(tmem, smem_u32(aqk), 0, smem_u32(akt), 0, 4, idesc_f16_f32(128, 64), false);
-        mma_commit(&sm.bar_mma);
-    }
-    // Q' out to the image while the tensor core works: 1024 chunks of 16 bytes
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int kk = tid + r * kPrepThreads, pnl = kk >> 9;
-        const uint4 u = *reinterpret_cast<const uint4 *>(sm.a1 + kOffQs + (kk << 4));
-        *reinterpret_cast<uint4 *>(img + (pnl ? IMG_Q1 : IMG_Q0) + ((kk & 511) << 4)) = u;
-    }
-    if (ok) ok = mbar_wait_bounded(&sm.bar_mma, mma_phase, kWaitCycles);
-    ok = __all_sync(0xffffffffu, ok);  // TMEM loads below are warp-collective
-    tc_fence_after();
-    if (ok) {
-        if (quad < 2) {
-            float v[32];
-            tmem_ld32(tmem_addr(tmem, quad * 32, chalf * 32), v);
-            store_quarter_f16_image(img + IMG_Z, quad * 32 + lane, chalf * 4, v);
-        }
     } else if (tid == 0) {
         atomicExch(status, (int)KDA_ERR_TIMEOUT);
     }
+    fence_proxy_async();
     tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+        // image out: [-M' | P' | Q' 0..63] in one piece, then Z and Q' 64..127
+        bulk_s2g(img, sm.a1, IMG_Z);
+        bulk_s2g(img + IMG_Z, zst, IMG_Q1 - IMG_Z);
+        bulk_s2g(img + IMG_Q1, sm.a1 + IMG_Z, IMG_GB - IMG_Q1);
+        bulk_commit_group();
+        bulk_wait_group_read<0>();  // the shared memory may go; the writes land on their own
+    }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
@@ -1084,7 +1109,7 @@ chunk_out_kernel(const __grid_constant__ CUtensorMap out_map, const __nv_bfloat1
                 for (int pnl = 0; pnl < D / kPanelCols; ++pnl)
                     tma_store_3d(&out_map, ob + pnl * (C * 128), pnl * kPanelCols, h, t0);
                 bulk_commit_group();
-                bulk_wait_group_all();
+                bulk_wait_group_read<0>();
             }
         } else {
             // a sequence's last, partial chunk: valid rows only, plain stores
