@@ -288,12 +288,12 @@ def run_reference(args, dist: Dist):
 
 def cpu_baseline(w):
     """The oracle as it stands on the whole prefill workload, repeated to at
-    least ~5 s of wall time (bounded: at most 4 runs)."""
+    least ~10 s of wall time (bounded: at most 40 runs)."""
     import oracle
     oracle.build()
     thr = oracle_threads()
     runs, t_total = 0, 0.0
-    while runs < 4 and (t_total < 5.0 or runs == 0):
+    while runs < 40 and (t_total < 10.0 or runs == 0):
         t0 = time.perf_counter()
         oracle.recurrent(w.q, w.k, w.v, w.log_alpha, w.beta, w.scale, None, w.cu_seqlens,
                          threads=thr)
@@ -345,6 +345,7 @@ def run_ours(args, dist: Dist):
     warm_evs = new_events(MAXEV)
     n_rec = 0
     for _ in range(args.warmup):
+        kda.kda_chunk_fwd(q, k, v, la, beta, w.scale, None, cu, out, fin, engine=args.engine)
         _, _, n_rec = kda.kda_chunk_fwd_ws_timed(q, k, v, la, beta, w.scale, None, cu, out, fin,
                                                  warm_evs, engine=args.engine)
     torch.cuda.synchronize()
@@ -354,6 +355,7 @@ def run_ours(args, dist: Dist):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     torch.cuda.synchronize()
 
+    # the headline: the public call, as a user makes it (no events between its kernels)
     sampler = ClockSampler(dist.local_rank)
     sampler.start()
     time.sleep(0.3)
@@ -362,12 +364,19 @@ def run_ours(args, dist: Dist):
     for i in range(args.steps):
         flush.zero_()
         starts[i].record(stream)
-        kda.kda_chunk_fwd_ws_timed(q, k, v, la, beta, w.scale, None, cu, out, fin, step_evs[i],
-                                   engine=args.engine)
+        kda.kda_chunk_fwd(q, k, v, la, beta, w.scale, None, cu, out, fin, engine=args.engine)
         ends[i].record(stream)
     torch.cuda.synchronize()
     dist.barrier()
     clocks = sampler.stop()
+
+    # per-kernel device times (the roofline inputs): the same call with
+    # library-recorded events between its kernels; not part of the headline
+    for i in range(args.steps):
+        flush.zero_()
+        kda.kda_chunk_fwd_ws_timed(q, k, v, la, beta, w.scale, None, cu, out, fin, step_evs[i],
+                                   engine=args.engine)
+    torch.cuda.synchronize()
 
     step_ms = [starts[i].elapsed_time(ends[i]) for i in range(args.steps)]
     stage_ms = [[step_evs[i][s].elapsed_time(step_evs[i][s + 1]) for s in range(n_stages)]
@@ -455,6 +464,8 @@ def run_ours(args, dist: Dist):
         "path_gbs": path_bytes_per_tok_head(d) * T * H * args.steps * dist.world
                     / (total_ms / 1e3) / 1e9,
         "stages_ms": dict(zip(names, stage_avg)),
+        "stages_note": "per-kernel device times from a separate run with library-recorded events "
+                       "between the kernels; the headline times the plain public call",
         "roofline": roofline,
         "e2e": e2e,
         "gpu_launches": n_stages * args.steps,
