@@ -445,10 +445,11 @@ def run_ours(args, dist: Dist):
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "ms_per_step": e2e_ms / args.steps}
 
-    # ---------------- decode row ----------------
-    decode = None
+    # ---------------- decode rows ----------------
+    decode = recurrent = None
     if not args.skip_decode:
         decode = run_decode(args, dist, peaks, dev, stream)
+        recurrent = run_recurrent_fwd(args, dist, peaks, dev, stream)
 
     del flush
     line = {
@@ -471,6 +472,7 @@ def run_ours(args, dist: Dist):
         "gpu_launches": n_stages * args.steps,
         "clocks": clocks,
         "decode": decode,
+        "recurrent_fwd": recurrent,
     }
     if not args.skip_cpu_baseline and dist.rank == 0 and dist.world == 1:
         line["cpu_baseline"] = cpu_baseline(w)
@@ -518,6 +520,52 @@ def run_decode(args, dist, peaks, dev, stream):
                          "frac": gbs / peaks["hbm_gbs"],
                          "traffic": profiled_traffic("recurrent_step"),
                          "bytes_per_launch": bytes_step, "peak_source": peaks["source"]}}
+
+
+def run_recurrent_fwd(args, dist, peaks, dev, stream):
+    """Multi-token recurrent pass: every sequence of the decode batch takes 8
+    new tokens in one call (a speculative-verification step), states in a
+    slot pool; the state crosses HBM once in each direction per call."""
+    import torch
+    import kimi_delta_attention_chunkwise_gb300 as kda
+    from kimi_delta_attention_chunkwise_gb300 import inputs
+    N, H, d, L = 256, 32, 128, 8
+    w = inputs.prefill(5, [L] * N, H=H, d=d, dtype="bf16", init_std=0.02,
+                       name="multi_token_decode")
+    to = lambda x, dt=None: torch.from_numpy(x).to(dev, dt)
+    q, k, v = to(w.q, torch.bfloat16), to(w.k, torch.bfloat16), to(w.v, torch.bfloat16)
+    la, b, cu = to(w.log_alpha), to(w.beta), to(w.cu_seqlens)
+    pool = to(w.initial_state)
+    slots = torch.arange(N, dtype=torch.int32, device=dev).flip(0).contiguous()
+    out = torch.empty((w.T, H, d), dtype=torch.bfloat16, device=dev)
+    call = lambda: kda.kda_recurrent_fwd(q, k, v, la, b, w.scale, pool, cu, slots, out)
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    reps = 20
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    dist.barrier()
+    torch.cuda.synchronize()
+    evs[0].record(stream)
+    for i in range(reps):
+        call()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(reps)]
+    total_ms = dist.max(sum(per))
+    # state read + written once per (sequence, head); per token q, k, v, out
+    # (bf16), log_alpha (fp32), beta
+    bytes_call = (2 * d * d * 4 + L * (4 * 2 * d + 4 * d + 4)) * N * H
+    gbs = bytes_call * reps * dist.world / (total_ms / 1e3) / 1e9
+    return {"workload": f"{N} sequences x {H} heads x {L} new tokens, d={d}, bf16, fp32 state "
+                        f"pool {N * H * d * d * 4 / 2**20:.0f} MiB (reversed slot order)",
+            "value": N * L * reps * dist.world / (total_ms / 1e3), "unit": "tokens/s",
+            "us_per_call": 1e3 * total_ms / reps, "gbs": gbs, "gpu_launches": reps,
+            "roofline": {"kernel": "recurrent_fwd", "bound": "hbm", "achieved": gbs,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                         "traffic": profiled_traffic("recurrent_fwd"),
+                         "bytes_per_launch": bytes_call, "peak_source": peaks["source"]}}
 
 
 def main():

@@ -211,15 +211,56 @@ kdaStatus_t kda_recurrent_step(const void *q, const void *k, const void *v,
                                float *state, void *out, const kdaShape_t *shape,
                                cudaStream_t stream);
 
+/*
+ * kda_recurrent_fwd -- the token-by-token recurrence over packed sequences of
+ * any length, each against its own slot of a state pool (short prefills,
+ * multi-token decode and speculative verification, serving batches whose
+ * states live in a cache).
+ *
+ * Defines: the recurrence above applied to every token of every sequence in
+ * order ("Kimi Unveils Delta Attention and K3 Architecture Updates", sec. 4.1
+ * and sec. 5, the fused recurrent kernel; "Linear Attention, From Scratch to
+ * Kimi 3", sec. 9, whose fused kernel loops over the tokens of each
+ * cu_seqlens sequence).  Each (sequence, head) state is read from its slot
+ * once, carried through the sequence's tokens on chip and written back once,
+ * in place.
+ *
+ *   q, k, v, log_alpha, beta, scale, out   as for kda_chunk_fwd ([T, H, d])
+ *   cu_seqlens     int32 [N + 1] device, non-decreasing, 0 .. T; NULL when
+ *                  N == 1 (one sequence of T tokens)
+ *   state_pool     float32 [num_slots, H, d_k, d_v], read and updated in place
+ *   state_indices  int32 [N] device: the pool slot of each sequence; a
+ *                  negative index skips the sequence (its outputs are not
+ *                  written, no slot is touched).  NULL: sequence s uses slot s
+ *                  (num_slots >= N).  Two sequences must not share a slot.
+ *   num_slots      number of slots in the pool; an index >= num_slots makes
+ *                  the kernel skip that sequence and set the device status
+ *                  word to KDA_ERR_INVALID_ARG (see kda_device_status)
+ *
+ * shape: num_seqs N, total_tokens T, num_heads H, d_k == d_v in {16, 32, 64,
+ * 128}, dtype, out_f32; chunk_size and engine are ignored.  Alignment as for
+ * kda_chunk_fwd (state_pool 16 bytes, state_indices 4).  Allocates nothing.
+ * Errors detectable on the host return before any launch.
+ *
+ * This entry has no counterpart on the pages beyond the fused kernel itself:
+ * the slot indirection is the serving-side state indexing of a state cache.
+ */
+kdaStatus_t kda_recurrent_fwd(const void *q, const void *k, const void *v,
+                              const float *log_alpha, const float *beta, float scale,
+                              const int32_t *cu_seqlens, float *state_pool,
+                              const int32_t *state_indices, int32_t num_slots, void *out,
+                              const kdaShape_t *shape, cudaStream_t stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *kda_status_string(kdaStatus_t status);
 
 /*
  * kda_device_status -- synchronises `stream`, then reads and clears the
- * library's device-side status word on the current device: KDA_SUCCESS, or
+ * library's device-side status word on the current device: KDA_SUCCESS,
  * KDA_ERR_TIMEOUT if a bounded wait inside a kernel gave up since the last
- * call (that kernel's outputs are then invalid).  Returns KDA_ERR_CUDA if the
- * synchronisation itself fails.
+ * call (that kernel's outputs are then invalid), or KDA_ERR_INVALID_ARG if
+ * kda_recurrent_fwd met a state index >= num_slots (that sequence was
+ * skipped).  Returns KDA_ERR_CUDA if the synchronisation itself fails.
  */
 kdaStatus_t kda_device_status(cudaStream_t stream);
 

@@ -9,6 +9,7 @@ The functions carry the C names:
 
 * ``kda_chunk_fwd``      -- chunkwise prefill over packed sequences;
 * ``kda_recurrent_step`` -- one decode token per sequence, state in place;
+* ``kda_recurrent_fwd``  -- token-by-token over packed sequences, slot-indexed state pool;
 * ``kda_chunk_fwd_workspace_size`` / ``kda_chunk_fwd_ws`` -- caller-owned scratch;
 * ``kda_status_string``, ``kda_device_status``.
 """
@@ -84,6 +85,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.kda_chunk_fwd_workspace_size.restype = ctypes.c_int
     lib.kda_recurrent_step.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, fp, vp, shp, vp]
     lib.kda_recurrent_step.restype = ctypes.c_int
+    lib.kda_recurrent_fwd.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, ip, fp, ip,
+                                      ctypes.c_int32, vp, shp, vp]
+    lib.kda_recurrent_fwd.restype = ctypes.c_int
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_device_status.argtypes = [vp]
@@ -323,6 +327,53 @@ def kda_recurrent_step(q, k, v, log_alpha, beta, scale: float, state, out=None, 
     _check(load().kda_recurrent_step(
         _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), float(scale), _ptr(state),
         _ptr(out), ctypes.byref(shape), _stream_handle(stream)), "kda_recurrent_step")
+    return out
+
+
+def kda_recurrent_fwd(q, k, v, log_alpha, beta, scale: float, state_pool, cu_seqlens=None,
+                      state_indices=None, out=None, *, stream=None, out_f32: bool = False):
+    """Token-by-token recurrence over packed sequences against a slot-indexed
+    state pool (C: kda_recurrent_fwd).  ``state_pool`` is updated in place.
+
+    q, k: [T, H, d_k] bf16/fp32; v: [T, H, d_v]; log_alpha: [T, H, d_k] fp32;
+    beta: [T, H] fp32; state_pool: [S, H, d_k, d_v] fp32; cu_seqlens: int32
+    [N + 1] on the device (None: one sequence); state_indices: int32 [N] on the
+    device (None: sequence s uses slot s; negative: skip the sequence).
+    Returns ``out`` [T, H, d_v].
+    """
+    torch = _torch()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, name)
+    if q.dim() != 3:
+        raise ValueError("q must be [T, H, d_k]")
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    _require(k, "k", q.dtype, (T, H, dk))
+    _require(v, "v", q.dtype, (T, H, dv))
+    _require(log_alpha, "log_alpha", torch.float32, (T, H, dk))
+    _require(beta, "beta", torch.float32, (T, H))
+    if cu_seqlens is not None:
+        _require(cu_seqlens, "cu_seqlens", torch.int32)
+        N = cu_seqlens.numel() - 1
+    else:
+        N = 1
+    _require(state_pool, "state_pool", torch.float32)
+    if state_pool is None or state_pool.dim() != 4 or tuple(state_pool.shape[1:]) != (H, dk, dv):
+        raise ValueError("state_pool must be [S, H, d_k, d_v]")
+    if state_indices is not None:
+        _require(state_indices, "state_indices", torch.int32, (N,))
+    odt = _out_dtype(q, out, out_f32)
+    if odt not in (q.dtype, torch.float32):
+        raise TypeError("out must have the dtype of q, or float32")
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=odt, device=q.device)
+    _require(out, "out", odt, (T, H, dv))
+    shape = make_shape(N, T, H, dk, dv, _dtype_code(q),
+                       out_f32=int(odt == torch.float32 and q.dtype != torch.float32))
+    _check(load().kda_recurrent_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), float(scale), _ptr(cu_seqlens),
+        _ptr(state_pool), _ptr(state_indices), int(state_pool.shape[0]), _ptr(out),
+        ctypes.byref(shape), _stream_handle(stream)), "kda_recurrent_fwd")
     return out
 
 

@@ -246,6 +246,42 @@ kdaStatus_t kda_recurrent_step(const void *q, const void *k, const void *v,
     return cuda_status(launch_recurrent_step(a, stream));
 }
 
+kdaStatus_t kda_recurrent_fwd(const void *q, const void *k, const void *v,
+                              const float *log_alpha, const float *beta, float scale,
+                              const int32_t *cu_seqlens, float *state_pool,
+                              const int32_t *state_indices, int32_t num_slots, void *out,
+                              const kdaShape_t *shape, cudaStream_t stream) {
+    kdaStatus_t st = check_shape(shape, false);
+    if (st != KDA_SUCCESS) return st;
+    if (!std::isfinite(scale)) return KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens && shape->num_seqs != 1) return KDA_ERR_INVALID_ARG;
+    if (num_slots < 0 || (!state_indices && num_slots < shape->num_seqs))
+        return KDA_ERR_INVALID_ARG;
+    if ((int64_t)num_slots * shape->num_heads > INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    if (shape->total_tokens > 0) {
+        const void *vec[] = {q, k, v, out, state_pool};
+        for (const void *p : vec)
+            if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+        const void *sc[] = {log_alpha, beta};
+        for (const void *p : sc)
+            if (!p || !aligned4(p)) return KDA_ERR_INVALID_ARG;
+    }
+    const void *idx[] = {cu_seqlens, state_indices};
+    for (const void *p : idx)
+        if (p && !aligned4(p)) return KDA_ERR_INVALID_ARG;
+    int *status = device_status_ptr();
+    if (!status) return cuda_status(cudaErrorUnknown);
+    RecurArgs a;
+    a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.scale = scale;
+    a.cu_seqlens = cu_seqlens; a.state_indices = state_indices; a.num_slots = num_slots;
+    a.pool = state_pool; a.out = out;
+    a.N = shape->num_seqs; a.T = shape->total_tokens; a.H = shape->num_heads;
+    a.D = shape->d_k; a.dtype = shape->dtype;
+    a.out_f32 = (shape->dtype == KDA_DTYPE_F32) ? 1 : shape->out_f32;
+    a.status = status;
+    return cuda_status(launch_recurrent_fwd(a, stream));
+}
+
 kdaStatus_t kda_device_status(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) {
         (void)cudaGetLastError();

@@ -157,6 +157,182 @@ cudaError_t launch_step_dtype(const StepArgs &a, cudaStream_t stream) {
     return cudaErrorInvalidValue;
 }
 
+// ---------------------------------------------------------------------------
+// Multi-token fused recurrent pass (the fused kernel "looping over multiple
+// tokens" of "Linear Attention, From Scratch to Kimi 3", sec. 9, and the
+// low-latency regime of "Kimi Unveils Delta Attention and K3 Architecture
+// Updates", sec. 5): one CTA per (sequence, head) holds the state in
+// registers across all of the sequence's tokens, so the state crosses HBM
+// once in each direction however many tokens the sequence has.  Each token
+// is the step above; its vectors are double-buffered in shared memory (three
+// barriers a token) and the next token's are loaded while this one runs.
+// The state lives in a pool of slots; state_indices picks each sequence's
+// slot (negative: the sequence is skipped).
+// ---------------------------------------------------------------------------
+// Thread layout of the multi-token pass: a thread owns a 4-column group and
+// ROWS consecutive rows (its per-row coefficients load as vectors).
+template <int D, int MAXT>
+struct FwdCfg {
+    static constexpr int CG = D / 4;
+    static constexpr int THREADS = (CG * D < MAXT) ? CG * D : MAXT;
+    static constexpr int RG = THREADS / CG;
+    static constexpr int ROWS = D / RG;
+    static constexpr int RG_PER_WARP = (CG < 32) ? 32 / CG : 1;
+    static constexpr int SLOTS = RG / RG_PER_WARP;
+    static constexpr int TB = 8;  // tokens staged in shared memory at a time
+    static_assert(RG * ROWS == D, "row split");
+};
+constexpr int kFwdThreads = 256;
+
+// ROWS consecutive floats of a shared-memory vector (16-byte aligned when ROWS % 4 == 0)
+template <int ROWS>
+__device__ __forceinline__ void load_rows(const float *src, float (&dst)[ROWS]) {
+    if constexpr (ROWS % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < ROWS; i += 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(src + i);
+            dst[i] = x.x; dst[i + 1] = x.y; dst[i + 2] = x.z; dst[i + 3] = x.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < ROWS; ++i) dst[i] = src[i];
+    }
+}
+
+template <typename TIn, typename TOut, int D>
+__global__ void __launch_bounds__(FwdCfg<D, kFwdThreads>::THREADS)
+recurrent_fwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
+                     const TIn *__restrict__ v, const float *__restrict__ log_alpha,
+                     const float *__restrict__ beta, float scale, const int32_t *__restrict__ cu,
+                     const int32_t *__restrict__ slots, int32_t num_slots, float *pool,
+                     TOut *__restrict__ out, int32_t T, int32_t H, int *status) {
+    using Cfg = FwdCfg<D, kFwdThreads>;
+    constexpr int CG = Cfg::CG, RG = Cfg::RG, ROWS = Cfg::ROWS, THREADS = Cfg::THREADS;
+    constexpr int RG_PER_WARP = Cfg::RG_PER_WARP, SLOTS = Cfg::SLOTS, TB = Cfg::TB;
+    // a block of TB tokens' vectors, fp32 (alpha = exp(log_alpha) already taken)
+    __shared__ __align__(16) float s_k[TB][D];
+    __shared__ __align__(16) float s_q[TB][D];
+    __shared__ __align__(16) float s_v[TB][D];
+    __shared__ __align__(16) float s_alpha[TB][D];
+    __shared__ float s_beta[TB];
+    __shared__ __align__(16) float s_e[2][D];
+    __shared__ __align__(16) float s_red[2][2][SLOTS][D];
+    __shared__ float s_kq[2];
+
+    const int tid = threadIdx.x;
+    const int cg = tid % CG, rg = tid / CG, row0 = rg * ROWS;
+    const int32_t seq = blockIdx.x / H, h = blockIdx.x % H;
+    int32_t ta = 0, tb = T;
+    if (cu) {
+        ta = min(max(cu[seq], 0), T);
+        tb = min(max(cu[seq + 1], ta), T);
+    }
+    const int32_t slot = slots ? slots[seq] : seq;
+    if (slot < 0 || ta >= tb) return;  // skipped, or nothing to do: state untouched
+    if (slot >= num_slots) {
+        if (tid == 0) atomicExch(status, (int)KDA_ERR_INVALID_ARG);
+        return;
+    }
+    float4 *S = reinterpret_cast<float4 *>(pool + ((size_t)slot * H + h) * D * D);
+    float4 s[ROWS];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) s[r] = __ldcs(S + (size_t)(row0 + r) * CG + cg);
+
+    int32_t n = 0;  // tokens done
+    for (int32_t t0 = ta; t0 < tb; t0 += TB) {
+        const int nt = min(TB, tb - t0);
+        __syncthreads();  // the previous block's vectors are no longer read
+        for (int idx = tid; idx < nt * D; idx += THREADS) {
+            const int i = idx / D, c = idx % D;
+            const size_t o = ((size_t)(t0 + i) * H + h) * D + c;
+            s_k[i][c] = to_f32(k[o]);
+            s_q[i][c] = to_f32(q[o]);
+            s_v[i][c] = to_f32(v[o]);
+            s_alpha[i][c] = __expf(log_alpha[o]);
+        }
+        if (tid < nt) s_beta[tid] = beta[(size_t)(t0 + tid) * H + h];
+        __syncthreads();
+        for (int i = 0; i < nt; ++i, ++n) {
+            const int b = n & 1;
+            if (tid < 32) {
+                float acc = 0.f;
+                for (int j = tid; j < D; j += 32) acc += s_k[i][j] * s_q[i][j];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                if (tid == 0) s_kq[b] = acc;
+            }
+            // decay the rows; both column reductions in one pass
+            float ra[ROWS], rk[ROWS], rq[ROWS];
+            load_rows<ROWS>(&s_alpha[i][row0], ra);
+            load_rows<ROWS>(&s_k[i][row0], rk);
+            load_rows<ROWS>(&s_q[i][row0], rq);
+            float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                const float a = ra[r], kr = rk[r], qr = rq[r];
+                s[r].x *= a; s[r].y *= a; s[r].z *= a; s[r].w *= a;
+                pk.x += s[r].x * kr; pk.y += s[r].y * kr; pk.z += s[r].z * kr; pk.w += s[r].w * kr;
+                pq.x += s[r].x * qr; pq.y += s[r].y * qr; pq.z += s[r].z * qr; pq.w += s[r].w * qr;
+            }
+#pragma unroll
+            for (int o = CG; o < 32; o <<= 1) {
+                pk.x += __shfl_xor_sync(0xffffffffu, pk.x, o); pk.y += __shfl_xor_sync(0xffffffffu, pk.y, o);
+                pk.z += __shfl_xor_sync(0xffffffffu, pk.z, o); pk.w += __shfl_xor_sync(0xffffffffu, pk.w, o);
+                pq.x += __shfl_xor_sync(0xffffffffu, pq.x, o); pq.y += __shfl_xor_sync(0xffffffffu, pq.y, o);
+                pq.z += __shfl_xor_sync(0xffffffffu, pq.z, o); pq.w += __shfl_xor_sync(0xffffffffu, pq.w, o);
+            }
+            if ((tid % 32) < CG || CG >= 32) {
+                const int sl = rg / RG_PER_WARP;
+                reinterpret_cast<float4 *>(s_red[b][0][sl])[cg] = pk;
+                reinterpret_cast<float4 *>(s_red[b][1][sl])[cg] = pq;
+            }
+            __syncthreads();
+            if (tid < D) {
+                float p = 0.f, rqs = 0.f;
+#pragma unroll
+                for (int w = 0; w < SLOTS; ++w) { p += s_red[b][0][w][tid]; rqs += s_red[b][1][w][tid]; }
+                const float e = s_beta[i] * (s_v[i][tid] - p);
+                s_e[b][tid] = e;
+                out[((size_t)(t0 + i) * H + h) * D + tid] =
+                    from_f32<TOut>(scale * (rqs + s_kq[b] * e));
+            }
+            __syncthreads();
+            // S_t = S_bar + k e^T
+            const float4 e4 = reinterpret_cast<const float4 *>(s_e[b])[cg];
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                const float kr = rk[r];
+                s[r].x += kr * e4.x; s[r].y += kr * e4.y; s[r].z += kr * e4.z; s[r].w += kr * e4.w;
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) __stcs(S + (size_t)(row0 + r) * CG + cg, s[r]);
+}
+
+template <typename TIn, typename TOut, int D>
+cudaError_t launch_fwd_t(const RecurArgs &a, cudaStream_t stream) {
+    const int64_t NH = (int64_t)a.N * a.H;
+    if (NH == 0 || a.T == 0) return cudaSuccess;
+    recurrent_fwd_kernel<TIn, TOut, D><<<(unsigned)NH, FwdCfg<D, kFwdThreads>::THREADS, 0,
+                                         stream>>>(
+        static_cast<const TIn *>(a.q), static_cast<const TIn *>(a.k),
+        static_cast<const TIn *>(a.v), a.log_alpha, a.beta, a.scale, a.cu_seqlens,
+        a.state_indices, a.num_slots, a.pool, static_cast<TOut *>(a.out), a.T, a.H, a.status);
+    return cudaGetLastError();
+}
+
+template <typename TIn, typename TOut>
+cudaError_t launch_fwd_dtype(const RecurArgs &a, cudaStream_t stream) {
+    switch (a.D) {
+        case 16: return launch_fwd_t<TIn, TOut, 16>(a, stream);
+        case 32: return launch_fwd_t<TIn, TOut, 32>(a, stream);
+        case 64: return launch_fwd_t<TIn, TOut, 64>(a, stream);
+        case 128: return launch_fwd_t<TIn, TOut, 128>(a, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 cudaError_t launch_recurrent_step(const StepArgs &a, cudaStream_t stream) {
@@ -165,6 +341,14 @@ cudaError_t launch_recurrent_step(const StepArgs &a, cudaStream_t stream) {
         return launch_step_dtype<__nv_bfloat16, __nv_bfloat16>(a, stream);
     }
     return launch_step_dtype<float, float>(a, stream);
+}
+
+cudaError_t launch_recurrent_fwd(const RecurArgs &a, cudaStream_t stream) {
+    if (a.dtype == KDA_DTYPE_BF16) {
+        if (a.out_f32) return launch_fwd_dtype<__nv_bfloat16, float>(a, stream);
+        return launch_fwd_dtype<__nv_bfloat16, __nv_bfloat16>(a, stream);
+    }
+    return launch_fwd_dtype<float, float>(a, stream);
 }
 
 }  // namespace kda

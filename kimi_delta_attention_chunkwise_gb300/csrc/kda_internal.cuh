@@ -50,11 +50,29 @@ struct StepArgs {
     int32_t out_f32;
 };
 
+// Multi-token fused recurrent pass over packed sequences with a slot-indexed
+// state pool (kda_decode.cu).
+struct RecurArgs {
+    const void *q, *k, *v;
+    const float *log_alpha, *beta;
+    float scale;
+    const int32_t *cu_seqlens;     // device [N + 1] or nullptr (one sequence)
+    const int32_t *state_indices;  // device [N] or nullptr (slot = sequence)
+    int32_t num_slots;
+    float *pool;                   // [num_slots, H, D, D]
+    void *out;
+    int32_t N, T, H, D;
+    int32_t dtype;
+    int32_t out_f32;
+    int *status;                   // device status word
+};
+
 // fp32 CUDA-core chunk engine (kda_chunk_simt.cu).  Needs no scratch.
 cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t stream);
 
-// Decode step (kda_decode.cu).
+// Decode step and the multi-token recurrent pass (kda_decode.cu).
 cudaError_t launch_recurrent_step(const StepArgs &a, cudaStream_t stream);
+cudaError_t launch_recurrent_fwd(const RecurArgs &a, cudaStream_t stream);
 
 // Tensor-core chunk engine (kda_chunk_tc.cu): bf16, D = 128, C = 64.
 size_t chunk_tc_workspace_bytes(int32_t N, int32_t T, int32_t H);

@@ -119,3 +119,24 @@ def test_step_rejects_bad_arguments(lib):
     assert step(_shape(N=4, T=4), q=FAKE + 8) == kda.KDA_ERR_INVALID_ARG
     assert step(_shape(N=4, T=4), b=FAKE + 2) == kda.KDA_ERR_INVALID_ARG
     assert step(_shape(N=4, T=4, dk=48, dv=48)) == kda.KDA_ERR_UNSUPPORTED
+
+
+def _recur(lib, shape, ptrs=None, cu=None, idx=None, num_slots=4, scale=1.0):
+    p = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, b=FAKE, pool=FAKE, out=FAKE)
+    p.update(ptrs or {})
+    return lib.kda_recurrent_fwd(p["q"], p["k"], p["v"], p["g"], p["b"], ctypes.c_float(scale),
+                                 cu, p["pool"], idx, num_slots, p["out"],
+                                 ctypes.byref(shape) if shape is not None else None, None)
+
+
+def test_recurrent_fwd_rejects_bad_arguments(lib):
+    assert _recur(lib, None) == kda.KDA_ERR_INVALID_ARG
+    assert _recur(lib, _shape(N=0)) == kda.KDA_ERR_INVALID_ARG
+    assert _recur(lib, _shape(N=3)) == kda.KDA_ERR_INVALID_ARG            # N > 1 needs cu_seqlens
+    assert _recur(lib, _shape(), num_slots=0) == kda.KDA_ERR_INVALID_ARG  # slot s for sequence s
+    assert _recur(lib, _shape(), num_slots=-1, idx=FAKE) == kda.KDA_ERR_INVALID_ARG
+    assert _recur(lib, _shape(), scale=float("inf")) == kda.KDA_ERR_INVALID_ARG
+    assert _recur(lib, _shape(), ptrs={"pool": FAKE + 4}) == kda.KDA_ERR_INVALID_ARG
+    assert _recur(lib, _shape(), ptrs={"pool": None}) == kda.KDA_ERR_INVALID_ARG
+    assert _recur(lib, _shape(), idx=FAKE + 2) == kda.KDA_ERR_INVALID_ARG   # misaligned indices
+    assert _recur(lib, _shape(dk=96, dv=96)) == kda.KDA_ERR_UNSUPPORTED
