@@ -202,6 +202,7 @@ PROFILE_FILES = {
     "scan": "chunk_scan_prefill_T4096_H16.md",
     "out": "chunk_out_prefill_T4096_H16.md",
     "recurrent_step": "recurrent_step_decode_256x32_d128.md",
+    "recurrent_fwd": "recurrent_fwd_decode_256x32x8_d128.md",
 }
 
 
