@@ -70,6 +70,11 @@ typedef struct {
     int32_t engine;        /* chunk_fwd: kdaEngine_t; ignored by the step */
     int32_t out_f32;       /* 0: out has the dtype of q; 1: out is float32
                               (bf16 inputs, fp32 results: no output rounding) */
+    int32_t num_v_heads;   /* HV: 0 = H.  Otherwise a multiple of H: value
+                              heads in groups of HV / H sharing one q/k head
+                              (value head j reads q/k head j / (HV / H));
+                              v, log_alpha, beta, out and the states carry HV
+                              heads, q and k carry H */
 } kdaShape_t;
 
 /*
@@ -85,22 +90,27 @@ typedef struct {
  *
  *   q, k          [T, H, d_k]  dtype        (q and k are used as given; the
  *                                            caller normalises them)
- *   v             [T, H, d_v]  dtype
- *   log_alpha     [T, H, d_k]  float32      finite and <= 0 (log retention);
+ *   v             [T, HV, d_v] dtype        HV = shape->num_v_heads, or H
+ *   log_alpha     [T, HV, d_k] float32      finite and <= 0 (log retention);
  *                                            16-byte aligned for the tensor-core
  *                                            engine
- *   beta          [T, H]       float32      finite write strength
+ *   beta          [T, HV]      float32      finite write strength
  *   scale                      host float   applied to q (pass d_k^-1/2 for
  *                                            the usual 1/sqrt(d_k) read)
- *   initial_state [N, H, d_k, d_v] float32  or NULL for zero states
+ *   initial_state [N, HV, d_k, d_v] float32 or NULL for zero states
  *   cu_seqlens    [N + 1]      int32        device; cu[0] = 0, non-decreasing,
  *                                            cu[N] = T.  NULL means one
  *                                            sequence (then N must be 1).
- *   out           [T, H, d_v]  dtype (float32 if shape->out_f32)
+ *   out           [T, HV, d_v] dtype (float32 if shape->out_f32)
  *                                            written for every token
- *   final_state   [N, H, d_k, d_v] float32  or NULL (not written).  May be
+ *   final_state   [N, HV, d_k, d_v] float32 or NULL (not written).  May be
  *                                            the same buffer as initial_state
  *                                            (in-place resume).
+ *
+ * Value-head groups (shape->num_v_heads = HV, a multiple of H): value head j
+ * runs the recurrence with its own v, log_alpha, beta and state and with q/k
+ * head j / (HV / H), as the pages' recurrent launch grid over value heads
+ * ("Kimi Unveils Delta Attention and K3 Architecture Updates", sec. 5).
  *
  * cu_seqlens contents are not validated on the host (they live on the
  * device); the kernels clamp every sequence to [0, T], so out-of-range
@@ -196,12 +206,13 @@ kdaStatus_t kda_chunk_fwd_static(const void *q, const void *k, const void *v,
  * once: it is read, decayed, corrected and written back in place.
  *
  *   q, k       [N, H, d_k]  dtype
- *   v          [N, H, d_v]  dtype
- *   log_alpha  [N, H, d_k]  float32, finite and <= 0
- *   beta       [N, H]       float32
+ *   v          [N, HV, d_v] dtype (HV = shape->num_v_heads, or H; groups as
+ *                           for kda_chunk_fwd)
+ *   log_alpha  [N, HV, d_k] float32, finite and <= 0
+ *   beta       [N, HV]      float32
  *   scale                   host float applied to q
- *   state      [N, H, d_k, d_v] float32, read and updated in place
- *   out        [N, H, d_v]  dtype (float32 if shape->out_f32)
+ *   state      [N, HV, d_k, d_v] float32, read and updated in place
+ *   out        [N, HV, d_v] dtype (float32 if shape->out_f32)
  *
  * shape->total_tokens must equal shape->num_seqs (one token per sequence);
  * chunk_size and engine are ignored.  Allocates nothing.
@@ -225,10 +236,10 @@ kdaStatus_t kda_recurrent_step(const void *q, const void *k, const void *v,
  * once, carried through the sequence's tokens on chip and written back once,
  * in place.
  *
- *   q, k, v, log_alpha, beta, scale, out   as for kda_chunk_fwd ([T, H, d])
+ *   q, k, v, log_alpha, beta, scale, out   as for kda_chunk_fwd ([T, H or HV, d])
  *   cu_seqlens     int32 [N + 1] device, non-decreasing, 0 .. T; NULL when
  *                  N == 1 (one sequence of T tokens)
- *   state_pool     float32 [num_slots, H, d_k, d_v], read and updated in place
+ *   state_pool     float32 [num_slots, HV, d_k, d_v], read and updated in place
  *   state_indices  int32 [N] device: the pool slot of each sequence; a
  *                  negative index skips the sequence (its outputs are not
  *                  written, no slot is touched).  NULL: sequence s uses slot s

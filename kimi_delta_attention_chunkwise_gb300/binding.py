@@ -42,7 +42,7 @@ class kdaShape_t(ctypes.Structure):
                 ("num_heads", ctypes.c_int32), ("d_k", ctypes.c_int32),
                 ("d_v", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("chunk_size", ctypes.c_int32), ("engine", ctypes.c_int32),
-                ("out_f32", ctypes.c_int32)]
+                ("out_f32", ctypes.c_int32), ("num_v_heads", ctypes.c_int32)]
 
 
 class KdaError(RuntimeError):
@@ -163,9 +163,18 @@ def _require(t, name, dtype=None, shape=None):
 
 
 def make_shape(N, T, H, dk, dv, dtype_code, chunk_size=0, engine=KDA_ENGINE_AUTO,
-               out_f32=0) -> kdaShape_t:
+               out_f32=0, num_v_heads=0) -> kdaShape_t:
+    """H: q/k heads; num_v_heads: value heads (0 = H), a multiple of H."""
     return kdaShape_t(int(N), int(T), int(H), int(dk), int(dv), int(dtype_code),
-                      int(chunk_size), int(engine), int(out_f32))
+                      int(chunk_size), int(engine), int(out_f32), int(num_v_heads))
+
+
+def _value_heads(q, v):
+    """Value heads from the tensors: v carries HV heads, q carries H (HV % H == 0)."""
+    H, HV = q.shape[-2], v.shape[-2]
+    if HV % H:
+        raise ValueError(f"v has {HV} heads, not a multiple of q's {H}")
+    return HV, (0 if HV == H else HV)
 
 
 def _out_dtype(q, out, out_f32):
@@ -206,26 +215,29 @@ def _prefill_args(q, k, v, log_alpha, beta, initial_state, cu_seqlens, out, fina
         raise ValueError("q must be [T, H, d_k]")
     T, H, dk = q.shape
     dv = v.shape[-1]
+    if v.dim() != 3:
+        raise ValueError("v must be [T, HV, d_v]")
+    HV, nvh = _value_heads(q, v)
     _require(k, "k", q.dtype, (T, H, dk))
-    _require(v, "v", q.dtype, (T, H, dv))
-    _require(log_alpha, "log_alpha", torch.float32, (T, H, dk))
-    _require(beta, "beta", torch.float32, (T, H))
+    _require(v, "v", q.dtype, (T, HV, dv))
+    _require(log_alpha, "log_alpha", torch.float32, (T, HV, dk))
+    _require(beta, "beta", torch.float32, (T, HV))
     if cu_seqlens is not None:
         _require(cu_seqlens, "cu_seqlens", torch.int32)
         N = cu_seqlens.numel() - 1
     else:
         N = 1
-    _require(initial_state, "initial_state", torch.float32, (N, H, dk, dv))
+    _require(initial_state, "initial_state", torch.float32, (N, HV, dk, dv))
     odt = _out_dtype(q, out, out_f32)
     if odt not in (q.dtype, torch.float32):
         raise TypeError("out must have the dtype of q, or float32")
     if out is None:
-        out = torch.empty((T, H, dv), dtype=odt, device=q.device)
-    _require(out, "out", odt, (T, H, dv))
-    _require(final_state, "final_state", torch.float32, (N, H, dk, dv))
+        out = torch.empty((T, HV, dv), dtype=odt, device=q.device)
+    _require(out, "out", odt, (T, HV, dv))
+    _require(final_state, "final_state", torch.float32, (N, HV, dk, dv))
     eng = _ENGINES[engine] if isinstance(engine, str) else int(engine)
     shape = make_shape(N, T, H, dk, dv, _dtype_code(q), chunk_size, eng,
-                       int(odt == torch.float32 and q.dtype != torch.float32))
+                       int(odt == torch.float32 and q.dtype != torch.float32), nvh)
     return shape, out
 
 
@@ -311,19 +323,23 @@ def kda_recurrent_step(q, k, v, log_alpha, beta, scale: float, state, out=None, 
         raise ValueError("q must be [N, H, d_k]")
     N, H, dk = q.shape
     dv = v.shape[-1]
+    if v.dim() != 3:
+        raise ValueError("v must be [N, HV, d_v]")
+    HV, nvh = _value_heads(q, v)
     _require(k, "k", q.dtype, (N, H, dk))
-    _require(v, "v", q.dtype, (N, H, dv))
-    _require(log_alpha, "log_alpha", torch.float32, (N, H, dk))
-    _require(beta, "beta", torch.float32, (N, H))
-    _require(state, "state", torch.float32, (N, H, dk, dv))
+    _require(v, "v", q.dtype, (N, HV, dv))
+    _require(log_alpha, "log_alpha", torch.float32, (N, HV, dk))
+    _require(beta, "beta", torch.float32, (N, HV))
+    _require(state, "state", torch.float32, (N, HV, dk, dv))
     odt = _out_dtype(q, out, out_f32)
     if odt not in (q.dtype, torch.float32):
         raise TypeError("out must have the dtype of q, or float32")
     if out is None:
-        out = torch.empty((N, H, dv), dtype=odt, device=q.device)
-    _require(out, "out", odt, (N, H, dv))
+        out = torch.empty((N, HV, dv), dtype=odt, device=q.device)
+    _require(out, "out", odt, (N, HV, dv))
     shape = make_shape(N, N, H, dk, dv, _dtype_code(q),
-                       out_f32=int(odt == torch.float32 and q.dtype != torch.float32))
+                       out_f32=int(odt == torch.float32 and q.dtype != torch.float32),
+                       num_v_heads=nvh)
     _check(load().kda_recurrent_step(
         _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), float(scale), _ptr(state),
         _ptr(out), ctypes.byref(shape), _stream_handle(stream)), "kda_recurrent_step")
@@ -348,28 +364,32 @@ def kda_recurrent_fwd(q, k, v, log_alpha, beta, scale: float, state_pool, cu_seq
         raise ValueError("q must be [T, H, d_k]")
     T, H, dk = q.shape
     dv = v.shape[-1]
+    if v.dim() != 3:
+        raise ValueError("v must be [T, HV, d_v]")
+    HV, nvh = _value_heads(q, v)
     _require(k, "k", q.dtype, (T, H, dk))
-    _require(v, "v", q.dtype, (T, H, dv))
-    _require(log_alpha, "log_alpha", torch.float32, (T, H, dk))
-    _require(beta, "beta", torch.float32, (T, H))
+    _require(v, "v", q.dtype, (T, HV, dv))
+    _require(log_alpha, "log_alpha", torch.float32, (T, HV, dk))
+    _require(beta, "beta", torch.float32, (T, HV))
     if cu_seqlens is not None:
         _require(cu_seqlens, "cu_seqlens", torch.int32)
         N = cu_seqlens.numel() - 1
     else:
         N = 1
     _require(state_pool, "state_pool", torch.float32)
-    if state_pool is None or state_pool.dim() != 4 or tuple(state_pool.shape[1:]) != (H, dk, dv):
-        raise ValueError("state_pool must be [S, H, d_k, d_v]")
+    if state_pool is None or state_pool.dim() != 4 or tuple(state_pool.shape[1:]) != (HV, dk, dv):
+        raise ValueError("state_pool must be [S, HV, d_k, d_v]")
     if state_indices is not None:
         _require(state_indices, "state_indices", torch.int32, (N,))
     odt = _out_dtype(q, out, out_f32)
     if odt not in (q.dtype, torch.float32):
         raise TypeError("out must have the dtype of q, or float32")
     if out is None:
-        out = torch.empty((T, H, dv), dtype=odt, device=q.device)
-    _require(out, "out", odt, (T, H, dv))
+        out = torch.empty((T, HV, dv), dtype=odt, device=q.device)
+    _require(out, "out", odt, (T, HV, dv))
     shape = make_shape(N, T, H, dk, dv, _dtype_code(q),
-                       out_f32=int(odt == torch.float32 and q.dtype != torch.float32))
+                       out_f32=int(odt == torch.float32 and q.dtype != torch.float32),
+                       num_v_heads=nvh)
     _check(load().kda_recurrent_fwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), float(scale), _ptr(cu_seqlens),
         _ptr(state_pool), _ptr(state_indices), int(state_pool.shape[0]), _ptr(out),

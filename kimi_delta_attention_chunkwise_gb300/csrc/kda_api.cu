@@ -37,11 +37,16 @@ bool supported_dim(int32_t d) { return d == 16 || d == 32 || d == 64 || d == 128
 
 int32_t default_chunk(int32_t d) { return d >= 64 ? 64 : 16; }
 
+// Value heads (HV) and the group size HV / H.
+int32_t value_heads(const kdaShape_t *s) { return s->num_v_heads ? s->num_v_heads : s->num_heads; }
+int32_t group_size(const kdaShape_t *s) { return value_heads(s) / s->num_heads; }
+
 // Shared shape checks.  Returns KDA_SUCCESS or the first error found.
 kdaStatus_t check_shape(const kdaShape_t *s, bool step) {
     if (!s) return KDA_ERR_INVALID_ARG;
     if (s->num_seqs < 1 || s->total_tokens < 0 || s->num_heads < 1)
         return KDA_ERR_INVALID_ARG;
+    if (s->num_v_heads < 0 || (s->num_v_heads % s->num_heads) != 0) return KDA_ERR_INVALID_ARG;
     if (s->d_k < 1 || s->d_v < 1) return KDA_ERR_INVALID_ARG;
     if (s->dtype != KDA_DTYPE_BF16 && s->dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
     if (s->out_f32 != 0 && s->out_f32 != 1) return KDA_ERR_INVALID_ARG;
@@ -54,11 +59,11 @@ kdaStatus_t check_shape(const kdaShape_t *s, bool step) {
             return KDA_ERR_INVALID_ARG;
     }
     if (s->d_k != s->d_v || !supported_dim(s->d_k)) return KDA_ERR_UNSUPPORTED;
-    if (s->num_heads > 65535) return KDA_ERR_UNSUPPORTED;  // heads index grid.y
+    if (value_heads(s) > 65535) return KDA_ERR_UNSUPPORTED;  // heads index grid.y
     // Index arithmetic inside the kernels is 64-bit, but token and
     // (token, head) counts travel as int32.
-    if ((int64_t)s->total_tokens * s->num_heads > INT32_MAX) return KDA_ERR_UNSUPPORTED;
-    if ((int64_t)s->num_seqs * s->num_heads > INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    if ((int64_t)s->total_tokens * value_heads(s) > INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    if ((int64_t)s->num_seqs * value_heads(s) > INT32_MAX) return KDA_ERR_UNSUPPORTED;
     return KDA_SUCCESS;
 }
 
@@ -109,8 +114,8 @@ kdaStatus_t plan_chunk(const void *q, const void *k, const void *v, const float 
     a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.scale = scale;
     a.initial_state = initial_state; a.cu_seqlens = cu_seqlens; a.out = out;
     a.final_state = final_state;
-    a.N = shape->num_seqs; a.T = shape->total_tokens; a.H = shape->num_heads;
-    a.D = shape->d_k; a.C = C; a.dtype = shape->dtype;
+    a.N = shape->num_seqs; a.T = shape->total_tokens; a.H = value_heads(shape);
+    a.G = group_size(shape); a.D = shape->d_k; a.C = C; a.dtype = shape->dtype;
     a.out_f32 = (shape->dtype == KDA_DTYPE_F32) ? 1 : shape->out_f32;
     plan->use_tc = use_tc;
     plan->workspace = use_tc ? chunk_tc_workspace_bytes(a.N, a.T, a.H) : 0;
@@ -162,7 +167,7 @@ kdaStatus_t kda_chunk_fwd_workspace_size(const kdaShape_t *shape, size_t *bytes)
     bool use_tc = shape->engine == KDA_ENGINE_SIMT ? false : tc_eligible(shape, C);
     if (shape->engine == KDA_ENGINE_TENSOR && !use_tc) return KDA_ERR_UNSUPPORTED;
     *bytes = use_tc ? chunk_tc_workspace_bytes(shape->num_seqs, shape->total_tokens,
-                                               shape->num_heads)
+                                               value_heads(shape))
                     : 0;
     return KDA_SUCCESS;
 }
@@ -240,7 +245,8 @@ kdaStatus_t kda_recurrent_step(const void *q, const void *k, const void *v,
         if (!p || !aligned4(p)) return KDA_ERR_INVALID_ARG;
     StepArgs a;
     a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.scale = scale;
-    a.state = state; a.out = out; a.N = shape->num_seqs; a.H = shape->num_heads;
+    a.state = state; a.out = out; a.N = shape->num_seqs; a.H = value_heads(shape);
+    a.G = group_size(shape);
     a.D = shape->d_k; a.dtype = shape->dtype;
     a.out_f32 = (shape->dtype == KDA_DTYPE_F32) ? 1 : shape->out_f32;
     return cuda_status(launch_recurrent_step(a, stream));
@@ -257,7 +263,7 @@ kdaStatus_t kda_recurrent_fwd(const void *q, const void *k, const void *v,
     if (!cu_seqlens && shape->num_seqs != 1) return KDA_ERR_INVALID_ARG;
     if (num_slots < 0 || (!state_indices && num_slots < shape->num_seqs))
         return KDA_ERR_INVALID_ARG;
-    if ((int64_t)num_slots * shape->num_heads > INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    if ((int64_t)num_slots * value_heads(shape) > INT32_MAX) return KDA_ERR_UNSUPPORTED;
     if (shape->total_tokens > 0) {
         const void *vec[] = {q, k, v, out, state_pool};
         for (const void *p : vec)
@@ -275,8 +281,8 @@ kdaStatus_t kda_recurrent_fwd(const void *q, const void *k, const void *v,
     a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.scale = scale;
     a.cu_seqlens = cu_seqlens; a.state_indices = state_indices; a.num_slots = num_slots;
     a.pool = state_pool; a.out = out;
-    a.N = shape->num_seqs; a.T = shape->total_tokens; a.H = shape->num_heads;
-    a.D = shape->d_k; a.dtype = shape->dtype;
+    a.N = shape->num_seqs; a.T = shape->total_tokens; a.H = value_heads(shape);
+    a.G = group_size(shape); a.D = shape->d_k; a.dtype = shape->dtype;
     a.out_f32 = (shape->dtype == KDA_DTYPE_F32) ? 1 : shape->out_f32;
     a.status = status;
     return cuda_status(launch_recurrent_fwd(a, stream));

@@ -72,7 +72,7 @@ chunk_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
                   const float *__restrict__ beta, float scale,
                   const float *__restrict__ initial_state, const int32_t *__restrict__ cu,
                   TOut *__restrict__ out, float *__restrict__ final_state, int32_t T,
-                  int32_t H) {
+                  int32_t H, int32_t G) {
     using Cfg = SimtCfg<D, C>;
     constexpr int BV = Cfg::BV, DP = Cfg::DP, CP = Cfg::CP, PARTS = Cfg::PARTS;
     extern __shared__ float sm[];
@@ -110,8 +110,9 @@ chunk_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
             float kv = 0.f, qv = 0.f, gv = 0.f;
             if (i < L) {
                 const size_t off = ((size_t)(c0 + i) * H + h) * D + d;
-                kv = ld_f32(k + off);
-                qv = ld_f32(q + off);
+                const size_t offq = ((size_t)(c0 + i) * (H / G) + h / G) * D + d;  // group's q/k
+                kv = ld_f32(k + offq);
+                qv = ld_f32(q + offq);
                 gv = log_alpha[off];
             }
             Kc[i * DP + d] = kv;
@@ -225,7 +226,7 @@ cudaError_t launch_simt_t(const ChunkArgs &a, cudaStream_t stream) {
     kern<<<grid, kThreads, Cfg::BYTES, stream>>>(
         static_cast<const TIn *>(a.q), static_cast<const TIn *>(a.k),
         static_cast<const TIn *>(a.v), a.log_alpha, a.beta, a.scale, a.initial_state,
-        a.cu_seqlens, static_cast<TOut *>(a.out), a.final_state, a.T, a.H);
+        a.cu_seqlens, static_cast<TOut *>(a.out), a.final_state, a.T, a.H, a.G);
     a.clock->mark(stream);
     return cudaGetLastError();
 }

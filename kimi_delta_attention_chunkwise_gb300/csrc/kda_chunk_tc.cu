@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__restrict__ q,
                   const __nv_bfloat16 *__restrict__ k, const float *__restrict__ beta,
                   float scale, const int32_t *__restrict__ cu, int32_t N, int32_t T, int32_t H,
-                  Scratch sc, int *status) {
+                  int32_t grp, Scratch sc, int *status) {
     extern __shared__ uint8_t smem_raw[];
     PrepSmem &sm = *reinterpret_cast<PrepSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -331,7 +331,8 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
     const size_t ch = (size_t)c * H + h;
     uint8_t *img = sc.img + ch * IMG_STRIDE;
     float *gb = reinterpret_cast<float *>(img + IMG_GB);
-    const size_t rs = (size_t)H * D;
+    const int32_t hq = h / grp;                 // the q/k head of this value head's group
+    const size_t rs = (size_t)(H / grp) * D;    // q/k token stride
 
     // Stream the chunk's k, q and log-decay tiles in (one tensor load each).
     if (tid == 0) {
@@ -339,8 +340,8 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
         mbar_init(&sm.bar_mma, 1);
         fence_mbar_init();
         mbar_arrive_expect_tx(&sm.bar_in, kInBytes);
-        tma_load_3d(sm.b1, &maps.k, 0, h, t0, &sm.bar_in);
-        tma_load_3d(sm.b1 + C * D * 2, &maps.q, 0, h, t0, &sm.bar_in);
+        tma_load_3d(sm.b1, &maps.k, 0, hq, t0, &sm.bar_in);
+        tma_load_3d(sm.b1 + C * D * 2, &maps.q, 0, hq, t0, &sm.bar_in);
         tma_load_3d(sm.a1, &maps.g, 0, h, t0, &sm.bar_in);
     }
     if (warp == 0) {
@@ -409,8 +410,8 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
 #pragma unroll
         for (int ii = 0; ii < HALF; ++ii) Gs[(i0 + ii) * D + d] = G[ii];
         __syncthreads();
-        const __nv_bfloat16 *kc = k + ((size_t)t0 * H + h) * D;
-        const __nv_bfloat16 *qc = q + ((size_t)t0 * H + h) * D;
+        const __nv_bfloat16 *kc = k + ((size_t)t0 * (H / grp) + hq) * D;
+        const __nv_bfloat16 *qc = q + ((size_t)t0 * (H / grp) + hq) * D;
         for (int i = warp; i < C; i += kPrepThreads / 32) {
             for (int j = 0; j <= i; ++j) {
                 float r = 0.f, a = 0.f;
@@ -1206,8 +1207,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
 
     if (a.T > 0) {
         PrepMaps maps;
-        if (!encode_tile_map(&maps.q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H) ||
-            !encode_tile_map(&maps.k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H) ||
+        if (!encode_tile_map(&maps.q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H / a.G) ||
+            !encode_tile_map(&maps.k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H / a.G) ||
             !encode_tile_map(&maps.g, a.log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.T, a.H))
             return cudaErrorInvalidValue;
         e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1217,7 +1218,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
         chunk_prep_kernel<<<pgrid, kPrepThreads, kPrepSmem, stream>>>(
             maps, static_cast<const __nv_bfloat16 *>(a.q),
             static_cast<const __nv_bfloat16 *>(a.k), a.beta, a.scale, a.cu_seqlens, a.N, a.T,
-            a.H, sc, a.status);
+            a.H, a.G, sc, a.status);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -54,15 +54,17 @@ __global__ void __launch_bounds__(StepCfg<D>::THREADS)
 recurrent_step_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
                       const TIn *__restrict__ v, const float *__restrict__ log_alpha,
                       const float *__restrict__ beta, float scale, float *state,
-                      TOut *__restrict__ out, int32_t NH) {
+                      TOut *__restrict__ out, int32_t NH, int32_t H, int32_t G) {
     using Cfg = StepCfg<D>;
     constexpr int CG = Cfg::CG, RG = Cfg::RG, ROWS = Cfg::ROWS, THREADS = Cfg::THREADS;
     __shared__ float s_k[D], s_q[D], s_alpha[D], s_e[D];
     __shared__ float s_red[2][RG][D];
     __shared__ float s_kq;
 
-    const int64_t nh = blockIdx.x;  // (sequence, head) pair; vectors are [N*H, D]
+    const int64_t nh = blockIdx.x;  // (sequence, value head) pair; vectors are [N*H, D]
     if (nh >= NH) return;
+    // q and k of this value head's group: [N * H / G, D]
+    const int64_t qk = (nh / H) * (H / G) + (nh % H) / G;
     const int tid = threadIdx.x;
     const int cg = tid % CG, rg = tid / CG;
 
@@ -73,8 +75,8 @@ recurrent_step_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
     for (int r = 0; r < ROWS; ++r) s[r] = __ldcs(S + (size_t)(rg + r * RG) * CG + cg);
 
     for (int i = tid; i < D; i += THREADS) {
-        s_k[i] = to_f32(k[nh * D + i]);
-        s_q[i] = to_f32(q[nh * D + i]);
+        s_k[i] = to_f32(k[qk * D + i]);
+        s_q[i] = to_f32(q[qk * D + i]);
         s_alpha[i] = __expf(log_alpha[nh * D + i]);
     }
     __syncthreads();
@@ -142,7 +144,7 @@ cudaError_t launch_step_t(const StepArgs &a, cudaStream_t stream) {
     recurrent_step_kernel<TIn, TOut, D><<<(unsigned)NH, StepCfg<D>::THREADS, 0, stream>>>(
         static_cast<const TIn *>(a.q), static_cast<const TIn *>(a.k),
         static_cast<const TIn *>(a.v), a.log_alpha, a.beta, a.scale, a.state,
-        static_cast<TOut *>(a.out), (int32_t)NH);
+        static_cast<TOut *>(a.out), (int32_t)NH, a.H, a.G);
     return cudaGetLastError();
 }
 
@@ -205,9 +207,9 @@ recurrent_fwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
                      const TIn *__restrict__ v, const float *__restrict__ log_alpha,
                      const float *__restrict__ beta, float scale, const int32_t *__restrict__ cu,
                      const int32_t *__restrict__ slots, int32_t num_slots, float *pool,
-                     TOut *__restrict__ out, int32_t T, int32_t H, int *status) {
+                     TOut *__restrict__ out, int32_t T, int32_t H, int32_t G, int *status) {
     using Cfg = FwdCfg<D, kFwdThreads>;
-    constexpr int CG = Cfg::CG, RG = Cfg::RG, ROWS = Cfg::ROWS, THREADS = Cfg::THREADS;
+    constexpr int CG = Cfg::CG, ROWS = Cfg::ROWS, THREADS = Cfg::THREADS;
     constexpr int RG_PER_WARP = Cfg::RG_PER_WARP, SLOTS = Cfg::SLOTS, TB = Cfg::TB;
     // a block of TB tokens' vectors, fp32 (alpha = exp(log_alpha) already taken)
     __shared__ __align__(16) float s_k[TB][D];
@@ -245,8 +247,9 @@ recurrent_fwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
         for (int idx = tid; idx < nt * D; idx += THREADS) {
             const int i = idx / D, c = idx % D;
             const size_t o = ((size_t)(t0 + i) * H + h) * D + c;
-            s_k[i][c] = to_f32(k[o]);
-            s_q[i][c] = to_f32(q[o]);
+            const size_t oq = ((size_t)(t0 + i) * (H / G) + h / G) * D + c;  // the group's q/k
+            s_k[i][c] = to_f32(k[oq]);
+            s_q[i][c] = to_f32(q[oq]);
             s_v[i][c] = to_f32(v[o]);
             s_alpha[i][c] = __expf(log_alpha[o]);
         }
@@ -318,7 +321,8 @@ cudaError_t launch_fwd_t(const RecurArgs &a, cudaStream_t stream) {
                                          stream>>>(
         static_cast<const TIn *>(a.q), static_cast<const TIn *>(a.k),
         static_cast<const TIn *>(a.v), a.log_alpha, a.beta, a.scale, a.cu_seqlens,
-        a.state_indices, a.num_slots, a.pool, static_cast<TOut *>(a.out), a.T, a.H, a.status);
+        a.state_indices, a.num_slots, a.pool, static_cast<TOut *>(a.out), a.T, a.H, a.G,
+        a.status);
     return cudaGetLastError();
 }
 

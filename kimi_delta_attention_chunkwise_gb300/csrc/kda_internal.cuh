@@ -31,7 +31,8 @@ struct ChunkArgs {
     const int32_t *cu_seqlens;   // device, N + 1 entries, or nullptr (one sequence)
     void *out;
     float *final_state;
-    int32_t N, T, H, D, C;
+    int32_t N, T, H, D, C;      // H: value heads (v, log_alpha, beta, out, states)
+    int32_t G;                   // value heads per q/k head (q, k have H / G heads)
     int32_t dtype;               // kdaDtype_t of q, k, v
     int32_t out_f32;             // 1: out is float32, 0: out has dtype
     int *status;                 // device status word (kernels with bounded waits
@@ -45,7 +46,8 @@ struct StepArgs {
     float scale;
     float *state;
     void *out;
-    int32_t N, H, D;
+    int32_t N, H, D;            // H: value heads
+    int32_t G;                  // value heads per q/k head
     int32_t dtype;
     int32_t out_f32;
 };
@@ -61,7 +63,8 @@ struct RecurArgs {
     int32_t num_slots;
     float *pool;                   // [num_slots, H, D, D]
     void *out;
-    int32_t N, T, H, D;
+    int32_t N, T, H, D;            // H: value heads
+    int32_t G;                     // value heads per q/k head
     int32_t dtype;
     int32_t out_f32;
     int *status;                   // device status word

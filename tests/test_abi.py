@@ -140,3 +140,16 @@ def test_recurrent_fwd_rejects_bad_arguments(lib):
     assert _recur(lib, _shape(), ptrs={"pool": None}) == kda.KDA_ERR_INVALID_ARG
     assert _recur(lib, _shape(), idx=FAKE + 2) == kda.KDA_ERR_INVALID_ARG   # misaligned indices
     assert _recur(lib, _shape(dk=96, dv=96)) == kda.KDA_ERR_UNSUPPORTED
+
+
+def test_value_head_groups_are_checked(lib):
+    def shp(H, HV):
+        return kda.make_shape(1, 64, H, 128, 128, kda.KDA_DTYPE_BF16, 0, kda.KDA_ENGINE_AUTO, 0, HV)
+    assert _chunk(lib, shp(2, 3)) == kda.KDA_ERR_INVALID_ARG     # HV not a multiple of H
+    assert _chunk(lib, shp(2, -2)) == kda.KDA_ERR_INVALID_ARG
+    assert _recur(lib, shp(4, 6)) == kda.KDA_ERR_INVALID_ARG
+    size = ctypes.c_size_t(0)
+    assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(shp(2, 8)), ctypes.byref(size)) == 0
+    grouped = size.value
+    assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(shp(2, 0)), ctypes.byref(size)) == 0
+    assert grouped == 4 * size.value or grouped > size.value   # scratch follows the value heads
