@@ -447,10 +447,11 @@ def run_ours(args, dist: Dist):
            "ms_per_step": e2e_ms / args.steps}
 
     # ---------------- decode rows ----------------
-    decode = recurrent = None
+    decode = recurrent = conv = None
     if not args.skip_decode:
         decode = run_decode(args, dist, peaks, dev, stream)
         recurrent = run_recurrent_fwd(args, dist, peaks, dev, stream)
+        conv = run_short_conv(args, dist, peaks, dev, stream)
 
     del flush
     line = {
@@ -474,6 +475,7 @@ def run_ours(args, dist: Dist):
         "clocks": clocks,
         "decode": decode,
         "recurrent_fwd": recurrent,
+        "short_conv": conv,
     }
     if not args.skip_cpu_baseline and dist.rank == 0 and dist.world == 1:
         line["cpu_baseline"] = cpu_baseline(w)
@@ -567,6 +569,67 @@ def run_recurrent_fwd(args, dist, peaks, dev, stream):
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
                          "traffic": profiled_traffic("recurrent_fwd"),
                          "bytes_per_launch": bytes_call, "peak_source": peaks["source"]}}
+
+
+def run_short_conv(args, dist, peaks, dev, stream):
+    """The layer's short convolution at K3 width (96 heads x 128 = 12,288
+    channels, 4 taps, SiLU, bf16) over 4 packed sequences totalling 4,096
+    tokens, caches in and out; then one decode step for 256 sequences."""
+    import numpy as np
+    import torch
+    import kimi_delta_attention_chunkwise_gb300 as kda
+    C, W, N = 12288, 4, 4
+    rng = np.random.default_rng(6)
+    lengths = [1000, 17, 2048, 1031]
+    T = sum(lengths)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32), device=dev)
+    x = torch.from_numpy(rng.standard_normal((T, C)).astype(np.float32)).to(dev, torch.bfloat16)
+    w = torch.from_numpy((rng.standard_normal((C, W)) * 0.5).astype(np.float32)).to(dev)
+    b = torch.from_numpy(rng.standard_normal(C).astype(np.float32)).to(dev)
+    cin = torch.zeros((N, C, W), dtype=torch.bfloat16, device=dev)
+    cout = torch.empty_like(cin)
+    y = torch.empty_like(x)
+    call = lambda: kda.kda_short_conv_fwd(x, w, b, cu, cin, cout, y, silu=True)
+    ND = 256
+    xd = torch.from_numpy(rng.standard_normal((ND, C)).astype(np.float32)).to(dev, torch.bfloat16)
+    cache = torch.zeros((ND, C, W), dtype=torch.bfloat16, device=dev)
+    yd = torch.empty_like(xd)
+    step = lambda: kda.kda_short_conv_step(xd, w, cache, b, yd, silu=True)
+    for _ in range(max(3, args.warmup)):
+        call(); step()
+    torch.cuda.synchronize()
+    # the calls are short next to a Python launch: capture each in a CUDA graph
+    # and time replays, so the device time is what is measured
+    reps = 20
+    res = {}
+    for name, fn in (("prefill", call), ("step", step)):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn()
+        graph.replay()
+        torch.cuda.synchronize()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        dist.barrier()
+        torch.cuda.synchronize()
+        evs[0].record(stream)
+        for _ in range(reps):
+            graph.replay()
+        evs[1].record(stream)
+        torch.cuda.synchronize()
+        res[name] = dist.max(evs[0].elapsed_time(evs[1])) / reps
+    # bytes: x read once, y written once, weights and bias, caches in and out
+    b_pre = 2 * T * C * 2 + C * (W + 1) * 4 + 2 * N * C * W * 2
+    b_step = 2 * ND * C * 2 + C * (W + 1) * 4 + 2 * ND * C * W * 2
+    gbs = b_pre / (res["prefill"] / 1e3) / 1e9
+    return {"workload": f"C={C} channels, {W} taps, SiLU, bf16; prefill {T} tokens in {N} "
+                        f"sequences; decode step for {ND} sequences",
+            "value": gbs, "unit": "GB/s", "us_per_call": 1e3 * res["prefill"],
+            "step_us": 1e3 * res["step"],
+            "step_gbs": b_step / (res["step"] / 1e3) / 1e9, "gpu_launches": 2 * reps,
+            "roofline": {"kernel": "short_conv_fwd", "bound": "hbm", "achieved": gbs,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                         "traffic": None, "bytes_per_launch": b_pre,
+                         "peak_source": peaks["source"]}}
 
 
 def main():

@@ -262,6 +262,57 @@ kdaStatus_t kda_recurrent_fwd(const void *q, const void *k, const void *v,
                               const int32_t *state_indices, int32_t num_slots, void *out,
                               const kdaShape_t *shape, cudaStream_t stream);
 
+/*
+ * The short causal convolution that precedes the mixer in each KDA layer
+ * ("Linear Attention, From Scratch to Kimi 3", sec. 7, "The short
+ * convolution is temporal, not channel mixing"): every channel c owns a
+ * W-tap filter over time, nothing mixes channels, and each sequence keeps a
+ * cache of its W most recent pre-convolution inputs for decode.  q, k and v
+ * each take their own call (own weights, own cache).  The tap formula is not
+ * in the page text; this library computes, for token t of a sequence,
+ *
+ *     y[t, c] = act( sum_{i<W} weight[c, i] * x[t - W + 1 + i, c] + bias[c] )
+ *
+ * act = identity or SiLU (z * sigmoid(z)); inputs before a sequence's first
+ * token come from its cache (slot W - 1 the most recent) or are zero.
+ */
+typedef struct {
+    int32_t num_seqs;      /* N >= 1 */
+    int32_t total_tokens;  /* T >= 0 packed tokens (prefill; ignored by the step) */
+    int32_t channels;      /* C >= 1, a multiple of 8 */
+    int32_t width;         /* W: taps, 2 .. 8 (4 in the K3 layer) */
+    int32_t dtype;         /* kdaDtype_t of x, y and the caches */
+    int32_t activation;    /* 0: none, 1: SiLU */
+} kdaConvShape_t;
+
+/*
+ * kda_short_conv_fwd -- prefill over packed sequences.
+ *
+ *   x          [T, C] dtype, 16-byte aligned
+ *   weight     [C, W] float32;  bias [C] float32 or NULL (both 16-byte aligned)
+ *   cu_seqlens [N + 1] int32 device (NULL when N == 1); sequences never see
+ *              each other's tokens
+ *   cache_in   [N, C, W] dtype or NULL (zeros): each sequence's inputs before
+ *              its first token, oldest first
+ *   cache_out  [N, C, W] dtype or NULL: each sequence's W most recent inputs
+ *              after the call (may be the same buffer as cache_in)
+ *   y          [T, C] dtype, 16-byte aligned, not x
+ *
+ * Allocates nothing; errors detectable on the host return before any launch.
+ */
+kdaStatus_t kda_short_conv_fwd(const void *x, const float *weight, const float *bias,
+                               const int32_t *cu_seqlens, const void *cache_in, void *cache_out,
+                               void *y, const kdaConvShape_t *shape, cudaStream_t stream);
+
+/*
+ * kda_short_conv_step -- one decode token per sequence: each cache [N, C, W]
+ * shifts by one, takes x [N, C] as its newest slot (in place), and y [N, C]
+ * is the filter over it.  shape->total_tokens is ignored.
+ */
+kdaStatus_t kda_short_conv_step(const void *x, const float *weight, const float *bias,
+                                void *cache, void *y, const kdaConvShape_t *shape,
+                                cudaStream_t stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *kda_status_string(kdaStatus_t status);
 

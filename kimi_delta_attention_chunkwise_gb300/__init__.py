@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     KDA_ERR_CUDA, KDA_ERR_INVALID_ARG, KDA_ERR_TIMEOUT, KDA_ERR_UNSUPPORTED, KDA_SUCCESS,
     KdaError, kda_chunk_fwd, kda_chunk_fwd_workspace_size, kda_chunk_fwd_ws,
     kda_chunk_fwd_ws_timed,
-    kda_device_status, kda_recurrent_fwd, kda_recurrent_step, kda_status_string, kdaShape_t, lib_path, load,
+    kda_device_status, kda_recurrent_fwd, kda_recurrent_step, kda_short_conv_fwd,
+    kda_short_conv_step, kda_status_string, kdaConvShape_t, kdaShape_t, lib_path, load,
     make_shape,
 )

@@ -10,6 +10,7 @@ The functions carry the C names:
 * ``kda_chunk_fwd``      -- chunkwise prefill over packed sequences;
 * ``kda_recurrent_step`` -- one decode token per sequence, state in place;
 * ``kda_recurrent_fwd``  -- token-by-token over packed sequences, slot-indexed state pool;
+* ``kda_short_conv_fwd`` / ``kda_short_conv_step`` -- the layer's short causal convolution;
 * ``kda_chunk_fwd_workspace_size`` / ``kda_chunk_fwd_ws`` -- caller-owned scratch;
 * ``kda_status_string``, ``kda_device_status``.
 """
@@ -43,6 +44,12 @@ class kdaShape_t(ctypes.Structure):
                 ("d_v", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("chunk_size", ctypes.c_int32), ("engine", ctypes.c_int32),
                 ("out_f32", ctypes.c_int32), ("num_v_heads", ctypes.c_int32)]
+
+
+class kdaConvShape_t(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
+                ("channels", ctypes.c_int32), ("width", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("activation", ctypes.c_int32)]
 
 
 class KdaError(RuntimeError):
@@ -88,6 +95,11 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.kda_recurrent_fwd.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, ip, fp, ip,
                                       ctypes.c_int32, vp, shp, vp]
     lib.kda_recurrent_fwd.restype = ctypes.c_int
+    cshp = ctypes.POINTER(kdaConvShape_t)
+    lib.kda_short_conv_fwd.argtypes = [vp, fp, fp, ip, vp, vp, vp, cshp, vp]
+    lib.kda_short_conv_fwd.restype = ctypes.c_int
+    lib.kda_short_conv_step.argtypes = [vp, fp, fp, vp, vp, cshp, vp]
+    lib.kda_short_conv_step.restype = ctypes.c_int
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_device_status.argtypes = [vp]
@@ -395,6 +407,68 @@ def kda_recurrent_fwd(q, k, v, log_alpha, beta, scale: float, state_pool, cu_seq
         _ptr(state_pool), _ptr(state_indices), int(state_pool.shape[0]), _ptr(out),
         ctypes.byref(shape), _stream_handle(stream)), "kda_recurrent_fwd")
     return out
+
+
+def kda_short_conv_fwd(x, weight, bias=None, cu_seqlens=None, cache_in=None, cache_out=None,
+                       y=None, *, silu: bool = False, stream=None):
+    """Short causal convolution over packed sequences (C: kda_short_conv_fwd).
+
+    x: [T, C] bf16/fp32; weight: [C, W] fp32; bias: [C] fp32 or None;
+    cu_seqlens: int32 [N + 1] on the device (None: one sequence); cache_in /
+    cache_out: [N, C, W] of x's dtype or None (cache_out may be cache_in).
+    Returns ``y`` [T, C].
+    """
+    torch = _torch()
+    _require(x, "x")
+    if x.dim() != 2:
+        raise ValueError("x must be [T, C]")
+    T, C = x.shape
+    _require(weight, "weight", torch.float32)
+    if weight is None or weight.dim() != 2 or weight.shape[0] != C:
+        raise ValueError("weight must be [C, W]")
+    W = weight.shape[1]
+    _require(bias, "bias", torch.float32, (C,))
+    if cu_seqlens is not None:
+        _require(cu_seqlens, "cu_seqlens", torch.int32)
+        N = cu_seqlens.numel() - 1
+    else:
+        N = 1
+    _require(cache_in, "cache_in", x.dtype, (N, C, W))
+    _require(cache_out, "cache_out", x.dtype, (N, C, W))
+    if y is None:
+        y = torch.empty_like(x)
+    _require(y, "y", x.dtype, (T, C))
+    shape = kdaConvShape_t(N, T, C, W, _dtype_code(x), int(bool(silu)))
+    _check(load().kda_short_conv_fwd(_ptr(x), _ptr(weight), _ptr(bias), _ptr(cu_seqlens),
+                                     _ptr(cache_in), _ptr(cache_out), _ptr(y),
+                                     ctypes.byref(shape), _stream_handle(stream)),
+           "kda_short_conv_fwd")
+    return y
+
+
+def kda_short_conv_step(x, weight, cache, bias=None, y=None, *, silu: bool = False,
+                        stream=None):
+    """One decode token per sequence (C: kda_short_conv_step): x [N, C];
+    cache [N, C, W] updated in place.  Returns ``y`` [N, C]."""
+    torch = _torch()
+    _require(x, "x")
+    if x.dim() != 2:
+        raise ValueError("x must be [N, C]")
+    N, C = x.shape
+    _require(weight, "weight", torch.float32)
+    if weight is None or weight.dim() != 2 or weight.shape[0] != C:
+        raise ValueError("weight must be [C, W]")
+    W = weight.shape[1]
+    _require(bias, "bias", torch.float32, (C,))
+    _require(cache, "cache", x.dtype, (N, C, W))
+    if y is None:
+        y = torch.empty_like(x)
+    _require(y, "y", x.dtype, (N, C))
+    shape = kdaConvShape_t(N, N, C, W, _dtype_code(x), int(bool(silu)))
+    _check(load().kda_short_conv_step(_ptr(x), _ptr(weight), _ptr(bias), _ptr(cache), _ptr(y),
+                                      ctypes.byref(shape), _stream_handle(stream)),
+           "kda_short_conv_step")
+    return y
 
 
 def kda_device_status(stream=None) -> int:

@@ -288,6 +288,61 @@ kdaStatus_t kda_recurrent_fwd(const void *q, const void *k, const void *v,
     return cuda_status(launch_recurrent_fwd(a, stream));
 }
 
+namespace {
+kdaStatus_t check_conv(const kdaConvShape_t *s, bool step) {
+    if (!s) return KDA_ERR_INVALID_ARG;
+    if (s->num_seqs < 1 || s->channels < 1 || (!step && s->total_tokens < 0))
+        return KDA_ERR_INVALID_ARG;
+    if (s->dtype != KDA_DTYPE_BF16 && s->dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
+    if (s->activation != 0 && s->activation != 1) return KDA_ERR_INVALID_ARG;
+    if (s->width < 2 || s->width > 8 || s->channels % 8 != 0) return KDA_ERR_UNSUPPORTED;
+    if (s->num_seqs > 65535) return KDA_ERR_UNSUPPORTED;  // sequences index grid.y
+    if ((int64_t)s->num_seqs * s->channels * s->width > INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    if (!step && (int64_t)s->total_tokens * s->channels > INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    return KDA_SUCCESS;
+}
+}  // namespace
+
+kdaStatus_t kda_short_conv_fwd(const void *x, const float *weight, const float *bias,
+                               const int32_t *cu_seqlens, const void *cache_in, void *cache_out,
+                               void *y, const kdaConvShape_t *shape, cudaStream_t stream) {
+    kdaStatus_t st = check_conv(shape, false);
+    if (st != KDA_SUCCESS) return st;
+    if (!cu_seqlens && shape->num_seqs != 1) return KDA_ERR_INVALID_ARG;
+    if (!weight || !aligned16(weight) || (bias && !aligned16(bias))) return KDA_ERR_INVALID_ARG;
+    if (shape->total_tokens > 0) {
+        if (!x || !y || !aligned16(x) || !aligned16(y) || x == y) return KDA_ERR_INVALID_ARG;
+    }
+    const void *opt[] = {cache_in, cache_out, cu_seqlens};
+    for (const void *p : opt)
+        if (p && !aligned4(p)) return KDA_ERR_INVALID_ARG;
+    ConvArgs a;
+    a.x = x; a.weight = weight; a.bias = bias; a.cu_seqlens = cu_seqlens;
+    a.cache_in = cache_in; a.cache_out = cache_out; a.y = y;
+    a.N = shape->num_seqs; a.T = shape->total_tokens; a.C = shape->channels;
+    a.W = shape->width; a.dtype = shape->dtype; a.activation = shape->activation;
+    a.step = false;
+    return cuda_status(launch_short_conv(a, stream));
+}
+
+kdaStatus_t kda_short_conv_step(const void *x, const float *weight, const float *bias,
+                                void *cache, void *y, const kdaConvShape_t *shape,
+                                cudaStream_t stream) {
+    kdaStatus_t st = check_conv(shape, true);
+    if (st != KDA_SUCCESS) return st;
+    const void *need[] = {x, weight, cache, y};
+    for (const void *p : need)
+        if (!p || !aligned4(p)) return KDA_ERR_INVALID_ARG;
+    if (bias && !aligned4(bias)) return KDA_ERR_INVALID_ARG;
+    ConvArgs a;
+    a.x = x; a.weight = weight; a.bias = bias; a.cu_seqlens = nullptr;
+    a.cache_in = cache; a.cache_out = cache; a.y = y;
+    a.N = shape->num_seqs; a.T = shape->num_seqs; a.C = shape->channels;
+    a.W = shape->width; a.dtype = shape->dtype; a.activation = shape->activation;
+    a.step = true;
+    return cuda_status(launch_short_conv(a, stream));
+}
+
 kdaStatus_t kda_device_status(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) {
         (void)cudaGetLastError();

@@ -70,6 +70,19 @@ struct RecurArgs {
     int *status;                   // device status word
 };
 
+// Short causal convolution (kda_conv.cu).
+struct ConvArgs {
+    const void *x;                 // [T, C] (prefill) or [N, C] (step)
+    const float *weight, *bias;    // [C, W], [C] or nullptr
+    const int32_t *cu_seqlens;     // prefill: [N + 1] or nullptr (one sequence)
+    const void *cache_in;          // prefill: [N, C, W] or nullptr (zeros)
+    void *cache_out;               // prefill: [N, C, W] or nullptr; step: the cache, in place
+    void *y;
+    int32_t N, T, C, W, dtype, activation;
+    bool step;
+};
+cudaError_t launch_short_conv(const ConvArgs &a, cudaStream_t stream);
+
 // fp32 CUDA-core chunk engine (kda_chunk_simt.cu).  Needs no scratch.
 cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t stream);
 

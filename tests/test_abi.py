@@ -153,3 +153,22 @@ def test_value_head_groups_are_checked(lib):
     grouped = size.value
     assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(shp(2, 0)), ctypes.byref(size)) == 0
     assert grouped == 4 * size.value or grouped > size.value   # scratch follows the value heads
+
+
+def test_short_conv_rejects_bad_arguments(lib):
+    def cs(N=1, T=16, C=64, W=4, dtype=kda.KDA_DTYPE_BF16, act=0):
+        return kda.kdaConvShape_t(N, T, C, W, dtype, act)
+    def fwd(shape, x=FAKE, w=FAKE, y=FAKE + 4096, cu=None):
+        return lib.kda_short_conv_fwd(x, w, None, cu, None, None, y,
+                                      ctypes.byref(shape) if shape is not None else None, None)
+    assert fwd(None) == kda.KDA_ERR_INVALID_ARG
+    assert fwd(cs(N=0)) == kda.KDA_ERR_INVALID_ARG
+    assert fwd(cs(N=2)) == kda.KDA_ERR_INVALID_ARG          # N > 1 needs cu_seqlens
+    assert fwd(cs(act=2)) == kda.KDA_ERR_INVALID_ARG
+    assert fwd(cs(), y=FAKE) == kda.KDA_ERR_INVALID_ARG     # y must not be x
+    assert fwd(cs(), x=FAKE + 8) == kda.KDA_ERR_INVALID_ARG  # 16-byte alignment
+    assert fwd(cs(), w=None) == kda.KDA_ERR_INVALID_ARG
+    assert fwd(cs(W=9)) == kda.KDA_ERR_UNSUPPORTED
+    assert fwd(cs(C=60)) == kda.KDA_ERR_UNSUPPORTED
+    assert lib.kda_short_conv_step(FAKE, FAKE, None, None, FAKE, ctypes.byref(cs()),
+                                   None) == kda.KDA_ERR_INVALID_ARG   # no cache
