@@ -75,7 +75,32 @@ typedef struct {
                               (value head j reads q/k head j / (HV / H));
                               v, log_alpha, beta, out and the states carry HV
                               heads, q and k carry H */
+    int32_t prologue;      /* kdaPrologue_t bits applied in-kernel to the
+                              inputs; 0: q, k, beta, log_alpha used as given */
+    const float *gate_bias;   /* [HV, d_k] float32, with KDA_PROLOGUE_GATE */
+    const float *gate_A_log;  /* [HV] float32, with KDA_PROLOGUE_GATE */
 } kdaShape_t;
+
+/*
+ * The fused input prologue ("Linear Attention, From Scratch to Kimi 3",
+ * sec. 6 "Exactly how K3 computes the forget values" and sec. 7 "Q/K
+ * normalization and query scaling"), applied by every kernel as it loads its
+ * inputs, so the raw projections cross HBM once:
+ *   KDA_PROLOGUE_L2NORM_QK   q and k are L2-normalised per head,
+ *                            x / sqrt(sum x^2 + 1e-6)
+ *   KDA_PROLOGUE_BETA_LOGITS beta holds logits: beta = sigmoid(beta)
+ *   KDA_PROLOGUE_GATE        log_alpha holds the gate projection g:
+ *                            log_alpha = -5 sigmoid(exp(A_log[h]) (g + b[h, j]))
+ *                            with b = gate_bias, A_log = gate_A_log (the
+ *                            page strips this formula; this is the reading
+ *                            its stated range, ingredients and sigmoid leave)
+ * The scale argument still applies to q after normalisation.
+ */
+typedef enum {
+    KDA_PROLOGUE_L2NORM_QK = 1,
+    KDA_PROLOGUE_BETA_LOGITS = 2,
+    KDA_PROLOGUE_GATE = 4
+} kdaPrologue_t;
 
 /*
  * kda_chunk_fwd -- chunkwise prefill over packed variable-length sequences.
@@ -91,7 +116,8 @@ typedef struct {
  *   q, k          [T, H, d_k]  dtype        (q and k are used as given; the
  *                                            caller normalises them)
  *   v             [T, HV, d_v] dtype        HV = shape->num_v_heads, or H
- *   log_alpha     [T, HV, d_k] float32      finite and <= 0 (log retention);
+ *   log_alpha     [T, HV, d_k] float32      finite and <= 0 (log retention;
+ *                                            gate logits with KDA_PROLOGUE_GATE);
  *                                            16-byte aligned for the tensor-core
  *                                            engine
  *   beta          [T, HV]      float32      finite write strength

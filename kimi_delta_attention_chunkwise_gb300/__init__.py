@@ -8,6 +8,7 @@ synthetic workloads (``inputs.py``).
 from .binding import (  # noqa: F401
     KDA_DTYPE_BF16, KDA_DTYPE_F32, KDA_ENGINE_AUTO, KDA_ENGINE_SIMT, KDA_ENGINE_TENSOR,
     KDA_ERR_CUDA, KDA_ERR_INVALID_ARG, KDA_ERR_TIMEOUT, KDA_ERR_UNSUPPORTED, KDA_SUCCESS,
+    KDA_PROLOGUE_BETA_LOGITS, KDA_PROLOGUE_GATE, KDA_PROLOGUE_L2NORM_QK,
     KdaError, kda_chunk_fwd, kda_chunk_fwd_workspace_size, kda_chunk_fwd_ws,
     kda_chunk_fwd_ws_timed,
     kda_device_status, kda_recurrent_fwd, kda_recurrent_step, kda_short_conv_fwd,

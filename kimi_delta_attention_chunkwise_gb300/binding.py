@@ -32,6 +32,10 @@ KDA_ERR_TIMEOUT = 4
 KDA_DTYPE_BF16 = 0
 KDA_DTYPE_F32 = 1
 
+KDA_PROLOGUE_L2NORM_QK = 1
+KDA_PROLOGUE_BETA_LOGITS = 2
+KDA_PROLOGUE_GATE = 4
+
 KDA_ENGINE_AUTO = 0
 KDA_ENGINE_TENSOR = 1
 KDA_ENGINE_SIMT = 2
@@ -43,7 +47,9 @@ class kdaShape_t(ctypes.Structure):
                 ("num_heads", ctypes.c_int32), ("d_k", ctypes.c_int32),
                 ("d_v", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("chunk_size", ctypes.c_int32), ("engine", ctypes.c_int32),
-                ("out_f32", ctypes.c_int32), ("num_v_heads", ctypes.c_int32)]
+                ("out_f32", ctypes.c_int32), ("num_v_heads", ctypes.c_int32),
+                ("prologue", ctypes.c_int32), ("gate_bias", ctypes.c_void_p),
+                ("gate_A_log", ctypes.c_void_p)]
 
 
 class kdaConvShape_t(ctypes.Structure):
@@ -175,10 +181,27 @@ def _require(t, name, dtype=None, shape=None):
 
 
 def make_shape(N, T, H, dk, dv, dtype_code, chunk_size=0, engine=KDA_ENGINE_AUTO,
-               out_f32=0, num_v_heads=0) -> kdaShape_t:
-    """H: q/k heads; num_v_heads: value heads (0 = H), a multiple of H."""
+               out_f32=0, num_v_heads=0, prologue=0, gate_bias=None,
+               gate_A_log=None) -> kdaShape_t:
+    """H: q/k heads; num_v_heads: value heads (0 = H), a multiple of H;
+    prologue: KDA_PROLOGUE_* bits; gate_bias / gate_A_log: device addresses."""
     return kdaShape_t(int(N), int(T), int(H), int(dk), int(dv), int(dtype_code),
-                      int(chunk_size), int(engine), int(out_f32), int(num_v_heads))
+                      int(chunk_size), int(engine), int(out_f32), int(num_v_heads),
+                      int(prologue), gate_bias, gate_A_log)
+
+
+def _prologue(l2norm_qk, beta_logits, gate, HV, dk):
+    """(bits, bias pointer, A_log pointer) of the in-kernel input prologue;
+    gate = (bias [HV, d_k] fp32, A_log [HV] fp32) tensors on the device."""
+    torch = _torch()
+    bits = (KDA_PROLOGUE_L2NORM_QK if l2norm_qk else 0) | (
+        KDA_PROLOGUE_BETA_LOGITS if beta_logits else 0)
+    if gate is None:
+        return bits, None, None
+    bias, a_log = gate
+    _require(bias, "gate bias", torch.float32, (HV, dk))
+    _require(a_log, "gate A_log", torch.float32, (HV,))
+    return bits | KDA_PROLOGUE_GATE, bias.data_ptr(), a_log.data_ptr()
 
 
 def _value_heads(q, v):
@@ -219,7 +242,7 @@ def _workspace(nbytes: int, device):
 
 
 def _prefill_args(q, k, v, log_alpha, beta, initial_state, cu_seqlens, out, final_state,
-                  chunk_size, engine, out_f32=False):
+                  chunk_size, engine, out_f32=False, prologue=None):
     torch = _torch()
     for name, t in (("q", q), ("k", k), ("v", v)):
         _require(t, name)
@@ -248,15 +271,17 @@ def _prefill_args(q, k, v, log_alpha, beta, initial_state, cu_seqlens, out, fina
     _require(out, "out", odt, (T, HV, dv))
     _require(final_state, "final_state", torch.float32, (N, HV, dk, dv))
     eng = _ENGINES[engine] if isinstance(engine, str) else int(engine)
+    bits, gb, ga = _prologue(*(prologue or (False, False, None)), HV, dk)
     shape = make_shape(N, T, H, dk, dv, _dtype_code(q), chunk_size, eng,
-                       int(odt == torch.float32 and q.dtype != torch.float32), nvh)
+                       int(odt == torch.float32 and q.dtype != torch.float32), nvh, bits, gb, ga)
     return shape, out
 
 
 def kda_chunk_fwd(q, k, v, log_alpha, beta, scale: float, initial_state=None,
                   cu_seqlens=None, out=None, final_state=None, *, chunk_size: int = 0,
                   engine="auto", stream=None, use_library_scratch: bool = False,
-                  out_f32: bool = False) -> Tuple[object, object]:
+                  out_f32: bool = False, l2norm_qk: bool = False, beta_logits: bool = False,
+                  gate=None) -> Tuple[object, object]:
     """Chunkwise KDA prefill (C: kda_chunk_fwd).  Returns ``(out, final_state)``.
 
     q, k: [T, H, d_k] bf16/fp32; v: [T, H, d_v]; log_alpha: [T, H, d_k] fp32;
@@ -265,9 +290,14 @@ def kda_chunk_fwd(q, k, v, log_alpha, beta, scale: float, initial_state=None,
     tensor as ``initial_state``.  Scratch comes from torch (kda_chunk_fwd_ws)
     unless ``use_library_scratch`` asks libkda to take it with cudaMallocAsync.
     ``out_f32`` (or a float32 ``out``) returns fp32 results for bf16 inputs.
+    Prologue (applied in-kernel as the inputs load; kdaPrologue_t):
+    ``l2norm_qk`` L2-normalises q and k per head, ``beta_logits`` takes beta as
+    logits (sigmoid), ``gate = (bias [HV, d_k], A_log [HV])`` takes log_alpha
+    as the K3 gate projection.
     """
     shape, out = _prefill_args(q, k, v, log_alpha, beta, initial_state, cu_seqlens, out,
-                               final_state, chunk_size, engine, out_f32)
+                               final_state, chunk_size, engine, out_f32,
+                               (l2norm_qk, beta_logits, gate))
     lib = load()
     s = _stream_handle(stream)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), float(scale),
@@ -287,13 +317,15 @@ def kda_chunk_fwd(q, k, v, log_alpha, beta, scale: float, initial_state=None,
 
 def kda_chunk_fwd_ws_timed(q, k, v, log_alpha, beta, scale: float, initial_state, cu_seqlens,
                            out, final_state, events, *, chunk_size: int = 0, engine="auto",
-                           stream=None, out_f32: bool = False):
+                           stream=None, out_f32: bool = False, l2norm_qk: bool = False,
+                           beta_logits: bool = False, gate=None):
     """kda_chunk_fwd with library-owned stage events: ``events`` is a list of
     already-recorded ``torch.cuda.Event(enable_timing=True)``; libkda records
     events[0] before its first kernel and events[i] after kernel i on the
     launch stream.  Returns ``(out, final_state, n_recorded)``."""
     shape, out = _prefill_args(q, k, v, log_alpha, beta, initial_state, cu_seqlens, out,
-                               final_state, chunk_size, engine, out_f32)
+                               final_state, chunk_size, engine, out_f32,
+                               (l2norm_qk, beta_logits, gate))
     nbytes = kda_chunk_fwd_workspace_size(shape)
     ws = _workspace(nbytes, q.device)
     wp = None if ws is None else (ws.data_ptr() + 255) // 256 * 256
@@ -323,7 +355,8 @@ def kda_chunk_fwd_ws(q, k, v, log_alpha, beta, scale: float, initial_state, cu_s
 
 
 def kda_recurrent_step(q, k, v, log_alpha, beta, scale: float, state, out=None, *,
-                       stream=None, out_f32: bool = False):
+                       stream=None, out_f32: bool = False, l2norm_qk: bool = False,
+                       beta_logits: bool = False, gate=None):
     """One KDA decode step (C: kda_recurrent_step).  ``state`` is updated in place.
 
     q, k: [N, H, d_k] bf16/fp32; v: [N, H, d_v]; log_alpha: [N, H, d_k] fp32;
@@ -349,9 +382,10 @@ def kda_recurrent_step(q, k, v, log_alpha, beta, scale: float, state, out=None, 
     if out is None:
         out = torch.empty((N, HV, dv), dtype=odt, device=q.device)
     _require(out, "out", odt, (N, HV, dv))
+    bits, gb, ga = _prologue(l2norm_qk, beta_logits, gate, HV, dk)
     shape = make_shape(N, N, H, dk, dv, _dtype_code(q),
                        out_f32=int(odt == torch.float32 and q.dtype != torch.float32),
-                       num_v_heads=nvh)
+                       num_v_heads=nvh, prologue=bits, gate_bias=gb, gate_A_log=ga)
     _check(load().kda_recurrent_step(
         _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), float(scale), _ptr(state),
         _ptr(out), ctypes.byref(shape), _stream_handle(stream)), "kda_recurrent_step")
@@ -359,7 +393,8 @@ def kda_recurrent_step(q, k, v, log_alpha, beta, scale: float, state, out=None, 
 
 
 def kda_recurrent_fwd(q, k, v, log_alpha, beta, scale: float, state_pool, cu_seqlens=None,
-                      state_indices=None, out=None, *, stream=None, out_f32: bool = False):
+                      state_indices=None, out=None, *, stream=None, out_f32: bool = False,
+                      l2norm_qk: bool = False, beta_logits: bool = False, gate=None):
     """Token-by-token recurrence over packed sequences against a slot-indexed
     state pool (C: kda_recurrent_fwd).  ``state_pool`` is updated in place.
 
@@ -399,9 +434,10 @@ def kda_recurrent_fwd(q, k, v, log_alpha, beta, scale: float, state_pool, cu_seq
     if out is None:
         out = torch.empty((T, HV, dv), dtype=odt, device=q.device)
     _require(out, "out", odt, (T, HV, dv))
+    bits, gb, ga = _prologue(l2norm_qk, beta_logits, gate, HV, dk)
     shape = make_shape(N, T, H, dk, dv, _dtype_code(q),
                        out_f32=int(odt == torch.float32 and q.dtype != torch.float32),
-                       num_v_heads=nvh)
+                       num_v_heads=nvh, prologue=bits, gate_bias=gb, gate_A_log=ga)
     _check(load().kda_recurrent_fwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), float(scale), _ptr(cu_seqlens),
         _ptr(state_pool), _ptr(state_indices), int(state_pool.shape[0]), _ptr(out),

@@ -47,6 +47,11 @@ kdaStatus_t check_shape(const kdaShape_t *s, bool step) {
     if (s->num_seqs < 1 || s->total_tokens < 0 || s->num_heads < 1)
         return KDA_ERR_INVALID_ARG;
     if (s->num_v_heads < 0 || (s->num_v_heads % s->num_heads) != 0) return KDA_ERR_INVALID_ARG;
+    if (s->prologue & ~(KDA_PROLOGUE_L2NORM_QK | KDA_PROLOGUE_BETA_LOGITS | KDA_PROLOGUE_GATE))
+        return KDA_ERR_INVALID_ARG;
+    if ((s->prologue & KDA_PROLOGUE_GATE) &&
+        (!s->gate_bias || !s->gate_A_log || !aligned4(s->gate_bias) || !aligned4(s->gate_A_log)))
+        return KDA_ERR_INVALID_ARG;
     if (s->d_k < 1 || s->d_v < 1) return KDA_ERR_INVALID_ARG;
     if (s->dtype != KDA_DTYPE_BF16 && s->dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
     if (s->out_f32 != 0 && s->out_f32 != 1) return KDA_ERR_INVALID_ARG;
@@ -116,6 +121,7 @@ kdaStatus_t plan_chunk(const void *q, const void *k, const void *v, const float 
     a.final_state = final_state;
     a.N = shape->num_seqs; a.T = shape->total_tokens; a.H = value_heads(shape);
     a.G = group_size(shape); a.D = shape->d_k; a.C = C; a.dtype = shape->dtype;
+    a.pro = shape->prologue; a.gbias = shape->gate_bias; a.galog = shape->gate_A_log;
     a.out_f32 = (shape->dtype == KDA_DTYPE_F32) ? 1 : shape->out_f32;
     plan->use_tc = use_tc;
     plan->workspace = use_tc ? chunk_tc_workspace_bytes(a.N, a.T, a.H) : 0;
@@ -247,6 +253,7 @@ kdaStatus_t kda_recurrent_step(const void *q, const void *k, const void *v,
     a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.scale = scale;
     a.state = state; a.out = out; a.N = shape->num_seqs; a.H = value_heads(shape);
     a.G = group_size(shape);
+    a.pro = shape->prologue; a.gbias = shape->gate_bias; a.galog = shape->gate_A_log;
     a.D = shape->d_k; a.dtype = shape->dtype;
     a.out_f32 = (shape->dtype == KDA_DTYPE_F32) ? 1 : shape->out_f32;
     return cuda_status(launch_recurrent_step(a, stream));
@@ -284,6 +291,7 @@ kdaStatus_t kda_recurrent_fwd(const void *q, const void *k, const void *v,
     a.N = shape->num_seqs; a.T = shape->total_tokens; a.H = value_heads(shape);
     a.G = group_size(shape); a.D = shape->d_k; a.dtype = shape->dtype;
     a.out_f32 = (shape->dtype == KDA_DTYPE_F32) ? 1 : shape->out_f32;
+    a.pro = shape->prologue; a.gbias = shape->gate_bias; a.galog = shape->gate_A_log;
     a.status = status;
     return cuda_status(launch_recurrent_fwd(a, stream));
 }

@@ -72,7 +72,8 @@ chunk_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
                   const float *__restrict__ beta, float scale,
                   const float *__restrict__ initial_state, const int32_t *__restrict__ cu,
                   TOut *__restrict__ out, float *__restrict__ final_state, int32_t T,
-                  int32_t H, int32_t G) {
+                  int32_t H, int32_t G, int32_t pro, const float *__restrict__ gbias,
+                  const float *__restrict__ galog) {
     using Cfg = SimtCfg<D, C>;
     constexpr int BV = Cfg::BV, DP = Cfg::DP, CP = Cfg::CP, PARTS = Cfg::PARTS;
     extern __shared__ float sm[];
@@ -102,6 +103,7 @@ chunk_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
         S[idx] = initial_state ? initial_state[state_off + (size_t)d * D + j] : 0.f;
     }
 
+    const float sens = (pro & KDA_PROLOGUE_GATE) ? __expf(galog[h]) : 0.f;
     for (int32_t c0 = t_begin; c0 < t_end; c0 += C) {
         const int L = min(C, t_end - c0);
         __syncthreads();  // previous chunk's readers of Kc/Qc/Gc/E are done
@@ -114,14 +116,39 @@ chunk_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
                 kv = ld_f32(k + offq);
                 qv = ld_f32(q + offq);
                 gv = log_alpha[off];
+                if (pro & KDA_PROLOGUE_GATE) gv = pro_gate(gv, sens, gbias[(size_t)h * D + d]);
             }
             Kc[i * DP + d] = kv;
             Qc[i * DP + d] = qv;
             Gc[i * DP + d] = gv;
         }
-        for (int i = tid; i < C; i += kThreads)
-            Bs[i] = i < L ? beta[(size_t)(c0 + i) * H + h] : 0.f;
+        for (int i = tid; i < C; i += kThreads) {
+            float bv = i < L ? beta[(size_t)(c0 + i) * H + h] : 0.f;
+            if ((pro & KDA_PROLOGUE_BETA_LOGITS) && i < L) bv = pro_sigmoid(bv);
+            Bs[i] = bv;
+        }
         __syncthreads();
+        // the L2 prologue: each warp normalises whole token rows of k and q
+        if (pro & KDA_PROLOGUE_L2NORM_QK) {
+            const int lane = tid & 31;
+            for (int i = tid >> 5; i < C; i += kThreads / 32) {
+                float kk = 0.f, qq = 0.f;
+                for (int d = lane; d < D; d += 32) {
+                    kk += Kc[i * DP + d] * Kc[i * DP + d];
+                    qq += Qc[i * DP + d] * Qc[i * DP + d];
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    kk += __shfl_xor_sync(0xffffffffu, kk, o);
+                    qq += __shfl_xor_sync(0xffffffffu, qq, o);
+                }
+                const float rk = rsqrtf(kk + kL2Eps), rq = rsqrtf(qq + kL2Eps);
+                for (int d = lane; d < D; d += 32) {
+                    Kc[i * DP + d] *= rk;
+                    Qc[i * DP + d] *= rq;
+                }
+            }
+        }
         // 6.1: cumulative log decay along the chunk (rows past L add 0).
         for (int d = tid; d < D; d += kThreads) {
             float acc = 0.f;
@@ -226,7 +253,8 @@ cudaError_t launch_simt_t(const ChunkArgs &a, cudaStream_t stream) {
     kern<<<grid, kThreads, Cfg::BYTES, stream>>>(
         static_cast<const TIn *>(a.q), static_cast<const TIn *>(a.k),
         static_cast<const TIn *>(a.v), a.log_alpha, a.beta, a.scale, a.initial_state,
-        a.cu_seqlens, static_cast<TOut *>(a.out), a.final_state, a.T, a.H, a.G);
+        a.cu_seqlens, static_cast<TOut *>(a.out), a.final_state, a.T, a.H, a.G, a.pro, a.gbias,
+        a.galog);
     a.clock->mark(stream);
     return cudaGetLastError();
 }

@@ -209,6 +209,8 @@ struct PrepSmem {
     float gcarry[D];   // G at token 31 of each channel
     float gmid[D];     // G at the reference token MID
     float glast[D];    // G at the chunk's last token
+    float knorm[C];    // 1 / |k_i|, 1 / |q_i| (L2 prologue; else 1)
+    float qnorm[C];
     uint64_t bar_in, bar_mma;
     uint32_t tmem;
 };
@@ -300,11 +302,14 @@ struct PrepMaps {
     CUtensorMap q, k, g;  // [T, H, D] viewed as {D, H, T}, box {128, 1, 64}
 };
 
+// PRO: the kernel applies an input prologue (compiled out when false)
+template <bool PRO>
 __global__ void __launch_bounds__(kPrepThreads, 2)
 chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__restrict__ q,
                   const __nv_bfloat16 *__restrict__ k, const float *__restrict__ beta,
                   float scale, const int32_t *__restrict__ cu, int32_t N, int32_t T, int32_t H,
-                  int32_t grp, Scratch sc, int *status) {
+                  int32_t grp, int32_t pro, const float *__restrict__ gbias,
+                  const float *__restrict__ galog, Scratch sc, int *status) {
     extern __shared__ uint8_t smem_raw[];
     PrepSmem &sm = *reinterpret_cast<PrepSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -350,7 +355,8 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
         tc_fence_before();
     }
     if (tid < C) {
-        const float b = tid < L ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
+        float b = tid < L ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
+        if (PRO && (pro & KDA_PROLOGUE_BETA_LOGITS) && tid < L) b = pro_sigmoid(b);
         sm.beta[tid] = b;
         gb[128 + tid] = b;
     }
@@ -360,6 +366,10 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
     bool ok = mbar_wait_bounded(&sm.bar_in, 0, kWaitCycles);
 
     const int d = tid & (D - 1), hf = tid >> 7, i0 = hf * HALF;
+    const bool l2 = PRO && (pro & KDA_PROLOGUE_L2NORM_QK);
+    const bool gate = PRO && (pro & KDA_PROLOGUE_GATE);
+    const float sens = gate ? __expf(galog[h]) : 0.f;
+    const float gbias_d = gate ? gbias[(size_t)h * D + d] : 0.f;
     uint32_t kp[HALF / 2], qp[HALF / 2];
     float G[HALF];
     {
@@ -377,8 +387,36 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
         float acc = 0.f;
 #pragma unroll
         for (int ii = 0; ii < HALF; ++ii) {
-            acc += (i0 + ii < L) ? gs[(i0 + ii) * D + d] : 0.f;
+            float lg = (i0 + ii < L) ? gs[(i0 + ii) * D + d] : 0.f;
+            if (gate && i0 + ii < L) lg = pro_gate(lg, sens, gbias_d);
+            acc += lg;
             G[ii] = acc;
+        }
+        // the L2 prologue: warp w finds 1/|k_i| and 1/|q_i| of tokens 8w .. 8w + 7
+        if (l2) {
+#pragma unroll 1
+            for (int i = warp * 8; i < warp * 8 + 8; ++i) {
+                const uint2 kw = *reinterpret_cast<const uint2 *>(ks + i * D + lane * 4);
+                const uint2 qw = *reinterpret_cast<const uint2 *>(qs + i * D + lane * 4);
+                const uint32_t kv4[2] = {kw.x, kw.y}, qv4[2] = {qw.x, qw.y};
+                float kk = 0.f, qq = 0.f;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float k0 = __uint_as_float(kv4[e] << 16), k1 = __uint_as_float(kv4[e] & 0xFFFF0000u);
+                    const float q0 = __uint_as_float(qv4[e] << 16), q1 = __uint_as_float(qv4[e] & 0xFFFF0000u);
+                    kk += k0 * k0 + k1 * k1;
+                    qq += q0 * q0 + q1 * q1;
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    kk += __shfl_xor_sync(0xffffffffu, kk, o);
+                    qq += __shfl_xor_sync(0xffffffffu, qq, o);
+                }
+                if (lane == 0) {
+                    sm.knorm[i] = rsqrtf(kk + kL2Eps);
+                    sm.qnorm[i] = rsqrtf(qq + kL2Eps);
+                }
+            }
         }
     }
     if (hf == 0) sm.gcarry[d] = G[HALF - 1];
@@ -397,10 +435,14 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
     for (int ii = 0; ii < HALF; ++ii) span = fmaxf(span, fabsf(G[ii] - Gm));
     const int slow = __syncthreads_or(!(span <= kSpanLimit));
     auto kval = [&](int ii) {
-        return __uint_as_float((ii & 1) ? (kp[ii >> 1] & 0xFFFF0000u) : (kp[ii >> 1] << 16));
+        const float x =
+            __uint_as_float((ii & 1) ? (kp[ii >> 1] & 0xFFFF0000u) : (kp[ii >> 1] << 16));
+        return l2 ? x * sm.knorm[i0 + ii] : x;
     };
     auto qval = [&](int ii) {
-        return __uint_as_float((ii & 1) ? (qp[ii >> 1] & 0xFFFF0000u) : (qp[ii >> 1] << 16));
+        const float x =
+            __uint_as_float((ii & 1) ? (qp[ii >> 1] & 0xFFFF0000u) : (qp[ii >> 1] << 16));
+        return l2 ? x * sm.qnorm[i0 + ii] : x;
     };
     uint32_t mma_phase = 0;
 
@@ -431,8 +473,11 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
                     a += __shfl_xor_sync(0xffffffffu, a, o);
                 }
                 if (lane == 0) {
-                    R[i][j] = (j < i) ? sm.beta[i] * r : 0.f;
-                    X[i][j] = scale * a;
+                    // the L2 prologue rescales the raw dot products
+                    const float nk = l2 ? sm.knorm[i] * sm.knorm[j] : 1.f;
+                    const float nq = l2 ? sm.qnorm[i] * sm.knorm[j] : 1.f;
+                    R[i][j] = (j < i) ? sm.beta[i] * r * nk : 0.f;
+                    X[i][j] = scale * a * nq;
                 }
             }
             for (int j = i + 1 + lane; j < C; j += 32) {
@@ -1211,14 +1256,15 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
             !encode_tile_map(&maps.k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H / a.G) ||
             !encode_tile_map(&maps.g, a.log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.T, a.H))
             return cudaErrorInvalidValue;
-        e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        auto prep = a.pro ? chunk_prep_kernel<true> : chunk_prep_kernel<false>;
+        e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kPrepSmem);
         if (e != cudaSuccess) return e;
         const dim3 pgrid((unsigned)max_chunks(a.N, a.T), (unsigned)a.H);
-        chunk_prep_kernel<<<pgrid, kPrepThreads, kPrepSmem, stream>>>(
+        prep<<<pgrid, kPrepThreads, kPrepSmem, stream>>>(
             maps, static_cast<const __nv_bfloat16 *>(a.q),
             static_cast<const __nv_bfloat16 *>(a.k), a.beta, a.scale, a.cu_seqlens, a.N, a.T,
-            a.H, a.G, sc, a.status);
+            a.H, a.G, a.pro, a.gbias, a.galog, sc, a.status);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

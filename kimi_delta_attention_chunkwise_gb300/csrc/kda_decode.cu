@@ -49,17 +49,19 @@ struct StepCfg {
     static_assert(RG * ROWS == D, "row split");
 };
 
-template <typename TIn, typename TOut, int D>
+// PRO: the kernel applies an input prologue (compiled out when false)
+template <typename TIn, typename TOut, int D, bool PRO>
 __global__ void __launch_bounds__(StepCfg<D>::THREADS)
 recurrent_step_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
                       const TIn *__restrict__ v, const float *__restrict__ log_alpha,
                       const float *__restrict__ beta, float scale, float *state,
-                      TOut *__restrict__ out, int32_t NH, int32_t H, int32_t G) {
+                      TOut *__restrict__ out, int32_t NH, int32_t H, int32_t G, int32_t pro,
+                      const float *__restrict__ gbias, const float *__restrict__ galog) {
     using Cfg = StepCfg<D>;
     constexpr int CG = Cfg::CG, RG = Cfg::RG, ROWS = Cfg::ROWS, THREADS = Cfg::THREADS;
     __shared__ float s_k[D], s_q[D], s_alpha[D], s_e[D];
     __shared__ float s_red[2][RG][D];
-    __shared__ float s_kq;
+    __shared__ float s_kq, s_rk, s_rq;
 
     const int64_t nh = blockIdx.x;  // (sequence, value head) pair; vectors are [N*H, D]
     if (nh >= NH) return;
@@ -74,18 +76,38 @@ recurrent_step_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) s[r] = __ldcs(S + (size_t)(rg + r * RG) * CG + cg);
 
+    const int hh = (int)(nh % H);
+    if (!PRO) pro = 0;
+    const float sens = (pro & KDA_PROLOGUE_GATE) ? __expf(galog[hh]) : 0.f;
     for (int i = tid; i < D; i += THREADS) {
         s_k[i] = to_f32(k[qk * D + i]);
         s_q[i] = to_f32(q[qk * D + i]);
-        s_alpha[i] = __expf(log_alpha[nh * D + i]);
+        float lg = log_alpha[nh * D + i];
+        if (pro & KDA_PROLOGUE_GATE) lg = pro_gate(lg, sens, gbias[(size_t)hh * D + i]);
+        s_alpha[i] = __expf(lg);
     }
     __syncthreads();
+    // k.q, and with the L2 prologue the two inverse norms: the row pass below
+    // uses raw k and q, its sums are rescaled afterwards
     if (tid < 32) {
-        float acc = 0.f;
-        for (int i = tid; i < D; i += 32) acc += s_k[i] * s_q[i];
+        float acc = 0.f, kk = 0.f, qq = 0.f;
+        for (int i = tid; i < D; i += 32) {
+            acc += s_k[i] * s_q[i];
+            kk += s_k[i] * s_k[i];
+            qq += s_q[i] * s_q[i];
+        }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (tid == 0) s_kq = acc;
+        for (int o = 16; o > 0; o >>= 1) {
+            acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            kk += __shfl_xor_sync(0xffffffffu, kk, o);
+            qq += __shfl_xor_sync(0xffffffffu, qq, o);
+        }
+        if (tid == 0) {
+            const bool l2 = pro & KDA_PROLOGUE_L2NORM_QK;
+            s_rk = l2 ? rsqrtf(kk + kL2Eps) : 1.f;
+            s_rq = l2 ? rsqrtf(qq + kL2Eps) : 1.f;
+            s_kq = acc * s_rk * s_rq;
+        }
     }
 
     // Decay the rows, then both column reductions in one pass.
@@ -119,9 +141,10 @@ recurrent_step_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
         float p = 0.f, rq = 0.f;
 #pragma unroll
         for (int w = 0; w < SLOTS; ++w) { p += s_red[0][w][tid]; rq += s_red[1][w][tid]; }
-        const float e = beta[nh] * (to_f32(v[nh * D + tid]) - p);
-        s_e[tid] = e;
-        out[nh * D + tid] = from_f32<TOut>(scale * (rq + s_kq * e));
+        const float bt = (pro & KDA_PROLOGUE_BETA_LOGITS) ? pro_sigmoid(beta[nh]) : beta[nh];
+        const float e = bt * (to_f32(v[nh * D + tid]) - s_rk * p);
+        s_e[tid] = s_rk * e;  // the write k_hat e^T, with k_hat = k / |k|
+        out[nh * D + tid] = from_f32<TOut>(scale * (s_rq * rq + s_kq * e));
     }
     __syncthreads();
 
@@ -141,10 +164,12 @@ template <typename TIn, typename TOut, int D>
 cudaError_t launch_step_t(const StepArgs &a, cudaStream_t stream) {
     const int64_t NH = (int64_t)a.N * a.H;
     if (NH == 0) return cudaSuccess;
-    recurrent_step_kernel<TIn, TOut, D><<<(unsigned)NH, StepCfg<D>::THREADS, 0, stream>>>(
+    auto kern = a.pro ? recurrent_step_kernel<TIn, TOut, D, true>
+                      : recurrent_step_kernel<TIn, TOut, D, false>;
+    kern<<<(unsigned)NH, StepCfg<D>::THREADS, 0, stream>>>(
         static_cast<const TIn *>(a.q), static_cast<const TIn *>(a.k),
         static_cast<const TIn *>(a.v), a.log_alpha, a.beta, a.scale, a.state,
-        static_cast<TOut *>(a.out), (int32_t)NH, a.H, a.G);
+        static_cast<TOut *>(a.out), (int32_t)NH, a.H, a.G, a.pro, a.gbias, a.galog);
     return cudaGetLastError();
 }
 
@@ -201,13 +226,15 @@ __device__ __forceinline__ void load_rows(const float *src, float (&dst)[ROWS]) 
     }
 }
 
-template <typename TIn, typename TOut, int D>
+template <typename TIn, typename TOut, int D, bool PRO>
 __global__ void __launch_bounds__(FwdCfg<D, kFwdThreads>::THREADS)
 recurrent_fwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
                      const TIn *__restrict__ v, const float *__restrict__ log_alpha,
                      const float *__restrict__ beta, float scale, const int32_t *__restrict__ cu,
                      const int32_t *__restrict__ slots, int32_t num_slots, float *pool,
-                     TOut *__restrict__ out, int32_t T, int32_t H, int32_t G, int *status) {
+                     TOut *__restrict__ out, int32_t T, int32_t H, int32_t G, int32_t pro,
+                     const float *__restrict__ gbias, const float *__restrict__ galog,
+                     int *status) {
     using Cfg = FwdCfg<D, kFwdThreads>;
     constexpr int CG = Cfg::CG, ROWS = Cfg::ROWS, THREADS = Cfg::THREADS;
     constexpr int RG_PER_WARP = Cfg::RG_PER_WARP, SLOTS = Cfg::SLOTS, TB = Cfg::TB;
@@ -219,7 +246,7 @@ recurrent_fwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
     __shared__ float s_beta[TB];
     __shared__ __align__(16) float s_e[2][D];
     __shared__ __align__(16) float s_red[2][2][SLOTS][D];
-    __shared__ float s_kq[2];
+    __shared__ float s_kq[2], s_rk[2], s_rq[2];
 
     const int tid = threadIdx.x;
     const int cg = tid % CG, rg = tid / CG, row0 = rg * ROWS;
@@ -240,6 +267,9 @@ recurrent_fwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) s[r] = __ldcs(S + (size_t)(row0 + r) * CG + cg);
 
+    if (!PRO) pro = 0;
+    const float sens = (pro & KDA_PROLOGUE_GATE) ? __expf(galog[h]) : 0.f;
+    const bool l2 = pro & KDA_PROLOGUE_L2NORM_QK;
     int32_t n = 0;  // tokens done
     for (int32_t t0 = ta; t0 < tb; t0 += TB) {
         const int nt = min(TB, tb - t0);
@@ -251,18 +281,39 @@ recurrent_fwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
             s_k[i][c] = to_f32(k[oq]);
             s_q[i][c] = to_f32(q[oq]);
             s_v[i][c] = to_f32(v[o]);
-            s_alpha[i][c] = __expf(log_alpha[o]);
+            float lg = log_alpha[o];
+            if (pro & KDA_PROLOGUE_GATE) lg = pro_gate(lg, sens, gbias[(size_t)h * D + c]);
+            s_alpha[i][c] = __expf(lg);
         }
-        if (tid < nt) s_beta[tid] = beta[(size_t)(t0 + tid) * H + h];
+        if (tid < nt) {
+            const float bt = beta[(size_t)(t0 + tid) * H + h];
+            s_beta[tid] = (pro & KDA_PROLOGUE_BETA_LOGITS) ? pro_sigmoid(bt) : bt;
+        }
         __syncthreads();
         for (int i = 0; i < nt; ++i, ++n) {
             const int b = n & 1;
+            // k.q and, with the L2 prologue, the inverse norms (the row pass
+            // uses raw k and q; its sums are rescaled below)
             if (tid < 32) {
-                float acc = 0.f;
-                for (int j = tid; j < D; j += 32) acc += s_k[i][j] * s_q[i][j];
+                float acc = 0.f, kk = 0.f, qq = 0.f;
+                for (int j = tid; j < D; j += 32) {
+                    acc += s_k[i][j] * s_q[i][j];
+                    kk += s_k[i][j] * s_k[i][j];
+                    qq += s_q[i][j] * s_q[i][j];
+                }
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                if (tid == 0) s_kq[b] = acc;
+                for (int o = 16; o > 0; o >>= 1) {
+                    acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                    kk += __shfl_xor_sync(0xffffffffu, kk, o);
+                    qq += __shfl_xor_sync(0xffffffffu, qq, o);
+                }
+                if (tid == 0) {
+                    const float rk = l2 ? rsqrtf(kk + kL2Eps) : 1.f;
+                    const float rq = l2 ? rsqrtf(qq + kL2Eps) : 1.f;
+                    s_rk[b] = rk;
+                    s_rq[b] = rq;
+                    s_kq[b] = acc * rk * rq;
+                }
             }
             // decay the rows; both column reductions in one pass
             float ra[ROWS], rk[ROWS], rq[ROWS];
@@ -294,10 +345,10 @@ recurrent_fwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
                 float p = 0.f, rqs = 0.f;
 #pragma unroll
                 for (int w = 0; w < SLOTS; ++w) { p += s_red[b][0][w][tid]; rqs += s_red[b][1][w][tid]; }
-                const float e = s_beta[i] * (s_v[i][tid] - p);
-                s_e[b][tid] = e;
+                const float e = s_beta[i] * (s_v[i][tid] - s_rk[b] * p);
+                s_e[b][tid] = s_rk[b] * e;  // the write k_hat e^T, k_hat = k / |k|
                 out[((size_t)(t0 + i) * H + h) * D + tid] =
-                    from_f32<TOut>(scale * (rqs + s_kq[b] * e));
+                    from_f32<TOut>(scale * (s_rq[b] * rqs + s_kq[b] * e));
             }
             __syncthreads();
             // S_t = S_bar + k e^T
@@ -317,12 +368,13 @@ template <typename TIn, typename TOut, int D>
 cudaError_t launch_fwd_t(const RecurArgs &a, cudaStream_t stream) {
     const int64_t NH = (int64_t)a.N * a.H;
     if (NH == 0 || a.T == 0) return cudaSuccess;
-    recurrent_fwd_kernel<TIn, TOut, D><<<(unsigned)NH, FwdCfg<D, kFwdThreads>::THREADS, 0,
-                                         stream>>>(
+    auto kern = a.pro ? recurrent_fwd_kernel<TIn, TOut, D, true>
+                      : recurrent_fwd_kernel<TIn, TOut, D, false>;
+    kern<<<(unsigned)NH, FwdCfg<D, kFwdThreads>::THREADS, 0, stream>>>(
         static_cast<const TIn *>(a.q), static_cast<const TIn *>(a.k),
         static_cast<const TIn *>(a.v), a.log_alpha, a.beta, a.scale, a.cu_seqlens,
-        a.state_indices, a.num_slots, a.pool, static_cast<TOut *>(a.out), a.T, a.H, a.G,
-        a.status);
+        a.state_indices, a.num_slots, a.pool, static_cast<TOut *>(a.out), a.T, a.H, a.G, a.pro,
+        a.gbias, a.galog, a.status);
     return cudaGetLastError();
 }
 

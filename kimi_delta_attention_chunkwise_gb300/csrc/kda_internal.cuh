@@ -33,6 +33,8 @@ struct ChunkArgs {
     float *final_state;
     int32_t N, T, H, D, C;      // H: value heads (v, log_alpha, beta, out, states)
     int32_t G;                   // value heads per q/k head (q, k have H / G heads)
+    int32_t pro;                 // kdaPrologue_t bits
+    const float *gbias, *galog;  // gate bias [H, D], sensitivity [H] (KDA_PROLOGUE_GATE)
     int32_t dtype;               // kdaDtype_t of q, k, v
     int32_t out_f32;             // 1: out is float32, 0: out has dtype
     int *status;                 // device status word (kernels with bounded waits
@@ -48,6 +50,8 @@ struct StepArgs {
     void *out;
     int32_t N, H, D;            // H: value heads
     int32_t G;                  // value heads per q/k head
+    int32_t pro;                // kdaPrologue_t bits
+    const float *gbias, *galog;
     int32_t dtype;
     int32_t out_f32;
 };
@@ -65,10 +69,21 @@ struct RecurArgs {
     void *out;
     int32_t N, T, H, D;            // H: value heads
     int32_t G;                     // value heads per q/k head
+    int32_t pro;                   // kdaPrologue_t bits
+    const float *gbias, *galog;
     int32_t dtype;
     int32_t out_f32;
     int *status;                   // device status word
 };
+
+// The fused input prologue, as each kernel applies it to one element.
+constexpr float kL2Eps = 1e-6f;
+__device__ __forceinline__ float pro_sigmoid(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
+// gate logit g of channel j of a head with sensitivity exp(A_log) = sens and
+// bias b[j] -> log retention -5 sigmoid(sens (g + b[j]))
+__device__ __forceinline__ float pro_gate(float g, float sens, float bias) {
+    return -5.f * pro_sigmoid(sens * (g + bias));
+}
 
 // Short causal convolution (kda_conv.cu).
 struct ConvArgs {

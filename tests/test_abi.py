@@ -172,3 +172,13 @@ def test_short_conv_rejects_bad_arguments(lib):
     assert fwd(cs(C=60)) == kda.KDA_ERR_UNSUPPORTED
     assert lib.kda_short_conv_step(FAKE, FAKE, None, None, FAKE, ctypes.byref(cs()),
                                    None) == kda.KDA_ERR_INVALID_ARG   # no cache
+
+
+def test_prologue_flags_are_checked(lib):
+    def shp(pro, gb=None, ga=None):
+        return kda.make_shape(1, 64, 2, 128, 128, kda.KDA_DTYPE_BF16, prologue=pro,
+                              gate_bias=gb, gate_A_log=ga)
+    assert _chunk(lib, shp(8)) == kda.KDA_ERR_INVALID_ARG                  # unknown bit
+    assert _chunk(lib, shp(kda.KDA_PROLOGUE_GATE)) == kda.KDA_ERR_INVALID_ARG   # gate needs params
+    assert _chunk(lib, shp(kda.KDA_PROLOGUE_GATE, FAKE, FAKE + 2)) == kda.KDA_ERR_INVALID_ARG
+    assert _recur(lib, shp(kda.KDA_PROLOGUE_GATE, FAKE, None)) == kda.KDA_ERR_INVALID_ARG
