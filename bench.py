@@ -447,6 +447,7 @@ def run_ours(args, dist: Dist):
            "ms_per_step": e2e_ms / args.steps}
 
     # ---------------- decode rows ----------------
+    variants = run_prefill_variants(args, dist, dev, stream, w, (q, k, v, la, beta, cu))
     decode = recurrent = conv = None
     if not args.skip_decode:
         decode = run_decode(args, dist, peaks, dev, stream)
@@ -476,6 +477,7 @@ def run_ours(args, dist: Dist):
         "decode": decode,
         "recurrent_fwd": recurrent,
         "short_conv": conv,
+        "prefill_variants": variants,
     }
     if not args.skip_cpu_baseline and dist.rank == 0 and dist.world == 1:
         line["cpu_baseline"] = cpu_baseline(w)
@@ -569,6 +571,58 @@ def run_recurrent_fwd(args, dist, peaks, dev, stream):
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
                          "traffic": profiled_traffic("recurrent_fwd"),
                          "bytes_per_launch": bytes_call, "peak_source": peaks["source"]}}
+
+
+def run_prefill_variants(args, dist, dev, stream, w, dev_inputs):
+    """The head-group prefill workload again, (a) with the whole fused input
+    prologue on (raw q/k, beta logits, K3 gate projections) and (b) with
+    value-head groups (8 q/k heads shared by the 16 value heads).  Timed
+    like the headline (L2 flushed before every step)."""
+    import numpy as np
+    import torch
+    import kimi_delta_attention_chunkwise_gb300 as kda
+    q, k, v, la, beta, cu = dev_inputs
+    T, H, d = q.shape
+    rng = np.random.default_rng(7)
+    gate = (torch.from_numpy((rng.standard_normal((H, d)) * 0.5 - 3.0).astype(np.float32)).to(dev),
+            torch.from_numpy(rng.uniform(-1, 1, H).astype(np.float32)).to(dev))
+    g_raw = torch.from_numpy(rng.standard_normal((T, H, d)).astype(np.float32)).to(dev)
+    beta_raw = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(dev)
+    q_raw, k_raw = q * 3, k * 3
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    fin = torch.empty((1, H, d, d), device=dev)
+    qg, kg = q[:, : H // 2].contiguous(), k[:, : H // 2].contiguous()
+    cases = {
+        "prologue": lambda: kda.kda_chunk_fwd(q_raw, k_raw, v, g_raw, beta_raw, w.scale, None, cu,
+                                             out, fin, l2norm_qk=True, beta_logits=True,
+                                             gate=gate),
+        "value_groups": lambda: kda.kda_chunk_fwd(qg, kg, v, la, beta, w.scale, None, cu, out,
+                                                 fin),
+    }
+    res = {}
+    for name, fn in cases.items():
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        dist.barrier()
+        torch.cuda.synchronize()
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        ms = dist.max(sum(a.elapsed_time(b) for a, b in evs)) / args.steps
+        res[name] = {"value": T * dist.world / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms}
+    res["prologue"]["workload"] = ("the headline workload with raw q/k (L2-normalised in-kernel), "
+                                   "beta logits and K3 gate projections (bias, A_log)")
+    res["value_groups"]["workload"] = (f"the headline workload with {H // 2} q/k heads shared by "
+                                       f"{H} value heads")
+    del flush
+    return res
 
 
 def run_short_conv(args, dist, peaks, dev, stream):
