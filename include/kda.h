@@ -339,6 +339,39 @@ kdaStatus_t kda_short_conv_step(const void *x, const float *weight, const float 
                                 void *cache, void *y, const kdaConvShape_t *shape,
                                 cudaStream_t stream);
 
+/*
+ * kda_recurrent_bwd -- gradients of kda_chunk_fwd / kda_recurrent_fwd's
+ * outputs and final states with respect to every input (training).
+ *
+ * Defines: reverse-mode differentiation of the recurrence above ("Kimi
+ * Unveils Delta Attention and K3 Architecture Updates", sec. 4.1; the pages
+ * say the chunkwise form serves training but derive no gradients, so this
+ * library derives them from the token recurrence, step by step).  Inputs as
+ * for kda_chunk_fwd, plus
+ *
+ *   d_out            [T, H, d_v] dtype of q, or NULL (zero)
+ *   d_final_state    [N, H, d_k, d_v] float32, or NULL (zero)
+ *
+ * and outputs, all float32 whatever the input dtype:
+ *
+ *   dq, dk [T, H, d_k];  dv [T, H, d_v];  dlog_alpha [T, H, d_k];
+ *   dbeta [T, H];  d_initial_state [N, H, d_k, d_v] or NULL (not written)
+ *
+ * One CTA per (sequence, head) carries the state and its gradient through the
+ * sequence: a forward sweep checkpoints the state every 8 tokens, and the
+ * reverse sweep recomputes each 8-token chunk from its checkpoint.  Scratch
+ * (checkpoints and one chunk of states per (sequence, head), about
+ * (T / 8 + N) * H * d_k * d_v * 4 + N * H * 8 * d_k * d_v * 4 bytes) is taken
+ * with cudaMallocAsync / cudaFreeAsync on `stream`.  Value-head groups and
+ * the input prologue are not supported here (KDA_ERR_UNSUPPORTED).
+ */
+kdaStatus_t kda_recurrent_bwd(const void *q, const void *k, const void *v,
+                              const float *log_alpha, const float *beta, float scale,
+                              const float *initial_state, const int32_t *cu_seqlens,
+                              const void *d_out, const float *d_final_state, float *dq, float *dk,
+                              float *dv, float *dlog_alpha, float *dbeta, float *d_initial_state,
+                              const kdaShape_t *shape, cudaStream_t stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *kda_status_string(kdaStatus_t status);
 

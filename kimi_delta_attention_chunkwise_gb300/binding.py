@@ -106,6 +106,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.kda_short_conv_fwd.restype = ctypes.c_int
     lib.kda_short_conv_step.argtypes = [vp, fp, fp, vp, vp, cshp, vp]
     lib.kda_short_conv_step.restype = ctypes.c_int
+    lib.kda_recurrent_bwd.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, fp, ip, vp, fp,
+                                      fp, fp, fp, fp, fp, fp, shp, vp]
+    lib.kda_recurrent_bwd.restype = ctypes.c_int
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_device_status.argtypes = [vp]
@@ -505,6 +508,45 @@ def kda_short_conv_step(x, weight, cache, bias=None, y=None, *, silu: bool = Fal
                                       ctypes.byref(shape), _stream_handle(stream)),
            "kda_short_conv_step")
     return y
+
+
+def kda_recurrent_bwd(q, k, v, log_alpha, beta, scale: float, initial_state=None,
+                      cu_seqlens=None, d_out=None, d_final_state=None, *, stream=None,
+                      want_initial: bool = True):
+    """Gradients of the recurrence (C: kda_recurrent_bwd).  Returns ``(dq, dk,
+    dv, dlog_alpha, dbeta, d_initial_state)``, float32 (d_initial_state None
+    unless ``want_initial``)."""
+    torch = _torch()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, name)
+    if q.dim() != 3:
+        raise ValueError("q must be [T, H, d_k]")
+    T, H, dk_ = q.shape
+    dv_ = v.shape[-1]
+    _require(k, "k", q.dtype, (T, H, dk_))
+    _require(v, "v", q.dtype, (T, H, dv_))
+    _require(log_alpha, "log_alpha", torch.float32, (T, H, dk_))
+    _require(beta, "beta", torch.float32, (T, H))
+    if cu_seqlens is not None:
+        _require(cu_seqlens, "cu_seqlens", torch.int32)
+        N = cu_seqlens.numel() - 1
+    else:
+        N = 1
+    _require(initial_state, "initial_state", torch.float32, (N, H, dk_, dv_))
+    _require(d_out, "d_out", q.dtype, (T, H, dv_))
+    _require(d_final_state, "d_final_state", torch.float32, (N, H, dk_, dv_))
+    f32 = dict(dtype=torch.float32, device=q.device)
+    dq, dk, dlog = (torch.empty((T, H, dk_), **f32) for _ in range(3))
+    dv = torch.empty((T, H, dv_), **f32)
+    db = torch.empty((T, H), **f32)
+    dS0 = torch.empty((N, H, dk_, dv_), **f32) if want_initial else None
+    shape = make_shape(N, T, H, dk_, dv_, _dtype_code(q))
+    _check(load().kda_recurrent_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), float(scale),
+        _ptr(initial_state), _ptr(cu_seqlens), _ptr(d_out), _ptr(d_final_state), _ptr(dq),
+        _ptr(dk), _ptr(dv), _ptr(dlog), _ptr(db), _ptr(dS0), ctypes.byref(shape),
+        _stream_handle(stream)), "kda_recurrent_bwd")
+    return dq, dk, dv, dlog, db, dS0
 
 
 def kda_device_status(stream=None) -> int:

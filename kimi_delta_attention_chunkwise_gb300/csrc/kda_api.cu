@@ -351,6 +351,46 @@ kdaStatus_t kda_short_conv_step(const void *x, const float *weight, const float 
     return cuda_status(launch_short_conv(a, stream));
 }
 
+kdaStatus_t kda_recurrent_bwd(const void *q, const void *k, const void *v,
+                              const float *log_alpha, const float *beta, float scale,
+                              const float *initial_state, const int32_t *cu_seqlens,
+                              const void *d_out, const float *d_final_state, float *dq, float *dk,
+                              float *dv, float *dlog_alpha, float *dbeta, float *d_initial_state,
+                              const kdaShape_t *shape, cudaStream_t stream) {
+    kdaStatus_t st = check_shape(shape, false);
+    if (st != KDA_SUCCESS) return st;
+    if (group_size(shape) != 1 || shape->prologue != 0) return KDA_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale)) return KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens && shape->num_seqs != 1) return KDA_ERR_INVALID_ARG;
+    if (shape->total_tokens > 0) {
+        const void *need[] = {q, k, v, log_alpha, beta, dq, dk, dv, dlog_alpha, dbeta};
+        for (const void *p : need)
+            if (!p || !aligned4(p)) return KDA_ERR_INVALID_ARG;
+        if (d_out && !aligned4(d_out)) return KDA_ERR_INVALID_ARG;
+    }
+    const void *states[] = {initial_state, d_final_state, d_initial_state};
+    for (const void *p : states)
+        if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens && !aligned4(cu_seqlens)) return KDA_ERR_INVALID_ARG;
+    BwdArgs a;
+    a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.scale = scale;
+    a.initial_state = initial_state; a.cu_seqlens = cu_seqlens; a.d_out = d_out;
+    a.d_final_state = d_final_state; a.dq = dq; a.dk = dk; a.dv = dv; a.dlog_alpha = dlog_alpha;
+    a.dbeta = dbeta; a.d_initial_state = d_initial_state;
+    a.N = shape->num_seqs; a.T = shape->total_tokens; a.H = shape->num_heads;
+    a.D = shape->d_k; a.dtype = shape->dtype;
+    const size_t bytes = recurrent_bwd_workspace_bytes(a.N, a.T, a.H, a.D);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes, stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    a.workspace = ws;
+    const cudaError_t e = launch_recurrent_bwd(a, stream);
+    const cudaError_t f = cudaFreeAsync(ws, stream);
+    return cuda_status(e != cudaSuccess ? e : f);
+}
+
 kdaStatus_t kda_device_status(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) {
         (void)cudaGetLastError();

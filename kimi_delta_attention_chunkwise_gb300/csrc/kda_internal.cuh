@@ -76,6 +76,22 @@ struct RecurArgs {
     int *status;                   // device status word
 };
 
+// Gradients of the recurrence (kda_backward.cu).
+struct BwdArgs {
+    const void *q, *k, *v;
+    const float *log_alpha, *beta;
+    float scale;
+    const float *initial_state;    // [N, H, D, D] or nullptr
+    const int32_t *cu_seqlens;
+    const void *d_out;             // [T, H, D] dtype of q, or nullptr (zero)
+    const float *d_final_state;    // [N, H, D, D] or nullptr (zero)
+    float *dq, *dk, *dv, *dlog_alpha, *dbeta, *d_initial_state;
+    void *workspace;               // recurrent_bwd_workspace_bytes, 256-byte aligned
+    int32_t N, T, H, D, dtype;
+};
+size_t recurrent_bwd_workspace_bytes(int32_t N, int32_t T, int32_t H, int32_t D);
+cudaError_t launch_recurrent_bwd(const BwdArgs &a, cudaStream_t stream);
+
 // The fused input prologue, as each kernel applies it to one element.
 constexpr float kL2Eps = 1e-6f;
 __device__ __forceinline__ float pro_sigmoid(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }

@@ -182,3 +182,16 @@ def test_prologue_flags_are_checked(lib):
     assert _chunk(lib, shp(kda.KDA_PROLOGUE_GATE)) == kda.KDA_ERR_INVALID_ARG   # gate needs params
     assert _chunk(lib, shp(kda.KDA_PROLOGUE_GATE, FAKE, FAKE + 2)) == kda.KDA_ERR_INVALID_ARG
     assert _recur(lib, shp(kda.KDA_PROLOGUE_GATE, FAKE, None)) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_recurrent_bwd_support(lib):
+    def bwd(shape):
+        p = [FAKE] * 5
+        return lib.kda_recurrent_bwd(p[0], p[1], p[2], p[3], p[4], ctypes.c_float(1.0), None, None,
+                                     None, None, FAKE, FAKE, FAKE, FAKE, FAKE, None,
+                                     ctypes.byref(shape), None)
+    grouped = kda.make_shape(1, 64, 2, 128, 128, kda.KDA_DTYPE_BF16, num_v_heads=4)
+    assert bwd(grouped) == kda.KDA_ERR_UNSUPPORTED
+    pro = kda.make_shape(1, 64, 2, 128, 128, kda.KDA_DTYPE_BF16, prologue=kda.KDA_PROLOGUE_BETA_LOGITS)
+    assert bwd(pro) == kda.KDA_ERR_UNSUPPORTED
+    assert bwd(kda.make_shape(2, 64, 2, 128, 128, kda.KDA_DTYPE_BF16)) == kda.KDA_ERR_INVALID_ARG
