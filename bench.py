@@ -448,6 +448,7 @@ def run_ours(args, dist: Dist):
 
     # ---------------- decode rows ----------------
     variants = run_prefill_variants(args, dist, dev, stream, w, (q, k, v, la, beta, cu))
+    backward = run_backward(args, dist, dev, stream, w, (q, k, v, la, beta, cu))
     decode = recurrent = conv = None
     if not args.skip_decode:
         decode = run_decode(args, dist, peaks, dev, stream)
@@ -478,6 +479,7 @@ def run_ours(args, dist: Dist):
         "recurrent_fwd": recurrent,
         "short_conv": conv,
         "prefill_variants": variants,
+        "backward": backward,
     }
     if not args.skip_cpu_baseline and dist.rank == 0 and dist.world == 1:
         line["cpu_baseline"] = cpu_baseline(w)
@@ -623,6 +625,37 @@ def run_prefill_variants(args, dist, dev, stream, w, dev_inputs):
                                        f"{H} value heads")
     del flush
     return res
+
+
+def run_backward(args, dist, dev, stream, w, dev_inputs):
+    """Gradients of the head-group prefill workload (1 sequence x 16 heads x
+    4,096 tokens): the recurrent backward with output and final-state
+    gradients, timed like the headline."""
+    import numpy as np
+    import torch
+    import kimi_delta_attention_chunkwise_gb300 as kda
+    q, k, v, la, beta, cu = dev_inputs
+    T, H, d = q.shape
+    rng = np.random.default_rng(8)
+    do = torch.from_numpy(rng.standard_normal((T, H, d)).astype(np.float32)).to(dev, torch.bfloat16)
+    dsf = torch.from_numpy(rng.standard_normal((1, H, d, d)).astype(np.float32)).to(dev)
+    call = lambda: kda.kda_recurrent_bwd(q, k, v, la, beta, w.scale, None, cu, do, dsf)
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    reps = max(3, min(args.steps, 5))
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    dist.barrier()
+    torch.cuda.synchronize()
+    evs[0].record(stream)
+    for _ in range(reps):
+        call()
+    evs[1].record(stream)
+    torch.cuda.synchronize()
+    ms = dist.max(evs[0].elapsed_time(evs[1])) / reps
+    return {"workload": f"gradients of the headline workload (1 x {H} heads x {T} tokens, d={d}, "
+                        "bf16 in, fp32 gradients), recurrent form with 8-token checkpoints",
+            "value": T * dist.world / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms}
 
 
 def run_short_conv(args, dist, peaks, dev, stream):
