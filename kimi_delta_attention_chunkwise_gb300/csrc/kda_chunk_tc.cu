@@ -325,6 +325,8 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
     uint8_t *zst = sm.b1;             // Z staging (after the MMAs that read A^kk)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_wait_primaries();      // the chunk table
+    pdl_launch_dependents();   // the scan may start setting up once every prep CTA runs
     const int32_t c = blockIdx.x, h = blockIdx.y;
     const int32_t total = sc.chunk_off[N];
     if (c >= total) return;
@@ -805,6 +807,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
     ScanSmem &sm = *reinterpret_cast<ScanSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_launch_dependents();  // the output pass may start setting up
     const int32_t seq = blockIdx.x / NT, vt = blockIdx.x % NT, h = blockIdx.y;
     int32_t ta, tb;
     seq_bounds(cu, seq, T, ta, tb);
@@ -856,6 +859,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
         if (warp == 4) {
             // -------- producer: -M' and P' of a chunk, once its stage is free --------
             if (lane == 0) {
+                pdl_wait_primaries();  // the prep kernel has written every image
                 for (int32_t n = 0; n < n_chunks; ++n) {
                     const int stg = n % NSTAGE;
                     if (n >= NSTAGE) {
@@ -1063,6 +1067,7 @@ chunk_out_kernel(const __grid_constant__ CUtensorMap out_map, const __nv_bfloat1
     const int32_t L = min(C, tb - t0);
     const uint8_t *img = sc.img + ((size_t)c * H + h) * IMG_STRIDE;
 
+    pdl_wait_primaries();  // the scan (and before it the prep) has finished
     if (tid == 0) {
         mbar_init(&sm.bar_in, 1);
         mbar_init(&sm.bar_mma, 1);
@@ -1245,6 +1250,24 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
     if (workspace_bytes < chunk_tc_workspace_bytes(a.N, a.T, a.H) || !workspace)
         return cudaErrorInvalidValue;
     const Scratch sc = carve(workspace, a.N, a.T, a.H);
+    // The later kernels go out as programmatic dependents: each one's CTAs can
+    // be resident and set up while the kernel ahead drains, and wait
+    // (griddepcontrol.wait) before reading its results.  With per-kernel
+    // events between them (clock) they are plain launches.
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    const unsigned n_pdl = (a.clock && a.clock->max_events > 0) ? 0u : 1u;
+    auto config = [&](dim3 grid, int threads, size_t smem) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3((unsigned)threads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cfg.attrs = pdl;
+        cfg.numAttrs = n_pdl;
+        return cfg;
+    };
     chunk_table_kernel<<<1, 1024, 0, stream>>>(a.cu_seqlens, a.N, a.T, sc.chunk_off);
     a.clock->mark(stream);
     cudaError_t e = cudaGetLastError();
@@ -1260,12 +1283,12 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
         e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kPrepSmem);
         if (e != cudaSuccess) return e;
-        const dim3 pgrid((unsigned)max_chunks(a.N, a.T), (unsigned)a.H);
-        prep<<<pgrid, kPrepThreads, kPrepSmem, stream>>>(
-            maps, static_cast<const __nv_bfloat16 *>(a.q),
-            static_cast<const __nv_bfloat16 *>(a.k), a.beta, a.scale, a.cu_seqlens, a.N, a.T,
-            a.H, a.G, a.pro, a.gbias, a.galog, sc, a.status);
-        e = cudaGetLastError();
+        const cudaLaunchConfig_t cfg =
+            config(dim3((unsigned)max_chunks(a.N, a.T), (unsigned)a.H), kPrepThreads, kPrepSmem);
+        e = cudaLaunchKernelEx(&cfg, prep, maps, static_cast<const __nv_bfloat16 *>(a.q),
+                               static_cast<const __nv_bfloat16 *>(a.k), a.beta, a.scale,
+                               static_cast<const int32_t *>(a.cu_seqlens), a.N, a.T, a.H, a.G,
+                               a.pro, a.gbias, a.galog, sc, a.status);
         if (e != cudaSuccess) return e;
     }
     a.clock->mark(stream);
@@ -1280,10 +1303,14 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
     e = cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kScanSmem);
     if (e != cudaSuccess) return e;
-    chunk_scan_kernel<<<sgrid, kScanThreads, kScanSmem, stream>>>(
-        v_map, a.initial_state, a.cu_seqlens, a.final_state, a.N, a.T, a.H, sc, a.status);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    {
+        cudaLaunchConfig_t cfg = config(sgrid, kScanThreads, kScanSmem);
+        if (a.T == 0) cfg.numAttrs = 0;  // no prep ahead of it
+        e = cudaLaunchKernelEx(&cfg, chunk_scan_kernel, v_map, a.initial_state,
+                               static_cast<const int32_t *>(a.cu_seqlens), a.final_state, a.N,
+                               a.T, a.H, sc, a.status);
+        if (e != cudaSuccess) return e;
+    }
     a.clock->mark(stream);
 
     if (a.T > 0) {
@@ -1302,25 +1329,24 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        const dim3 ogrid((unsigned)max_chunks(a.N, a.T), (unsigned)a.H);
+        const cudaLaunchConfig_t cfg =
+            config(dim3((unsigned)max_chunks(a.N, a.T), (unsigned)a.H), kOutThreads, kOutSmem);
+        const __nv_bfloat16 *vb = static_cast<const __nv_bfloat16 *>(a.v);
+        const int32_t *cu = static_cast<const int32_t *>(a.cu_seqlens);
         if (a.out_f32) {
-            auto kern = chunk_out_kernel<float>;
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kOutSmem);
+            e = cudaFuncSetAttribute(chunk_out_kernel<float>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOutSmem);
             if (e != cudaSuccess) return e;
-            kern<<<ogrid, kOutThreads, kOutSmem, stream>>>(
-                out_map, static_cast<const __nv_bfloat16 *>(a.v), a.cu_seqlens,
-                static_cast<float *>(a.out), a.N, a.T, a.H, sc, a.status);
+            e = cudaLaunchKernelEx(&cfg, chunk_out_kernel<float>, out_map, vb, cu,
+                                   static_cast<float *>(a.out), a.N, a.T, a.H, sc, a.status);
         } else {
-            auto kern = chunk_out_kernel<__nv_bfloat16>;
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kOutSmem);
+            e = cudaFuncSetAttribute(chunk_out_kernel<__nv_bfloat16>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOutSmem);
             if (e != cudaSuccess) return e;
-            kern<<<ogrid, kOutThreads, kOutSmem, stream>>>(
-                out_map, static_cast<const __nv_bfloat16 *>(a.v), a.cu_seqlens,
-                static_cast<__nv_bfloat16 *>(a.out), a.N, a.T, a.H, sc, a.status);
+            e = cudaLaunchKernelEx(&cfg, chunk_out_kernel<__nv_bfloat16>, out_map, vb, cu,
+                                   static_cast<__nv_bfloat16 *>(a.out), a.N, a.T, a.H, sc,
+                                   a.status);
         }
-        e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     a.clock->mark(stream);

@@ -79,6 +79,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched as a programmatic dependent
+// may start before the kernel ahead of it in the stream has finished; it
+// waits with pdl_wait_primaries() before touching that kernel's results
+// (both are no-ops for an ordinary launch).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primaries() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // bulk async copy global -> shared, completion counted on an mbarrier
 // (addresses 16-byte aligned, size a multiple of 16)
 // ---------------------------------------------------------------------------
