@@ -53,6 +53,7 @@
 // |G_i - G_m| <= 80 for every channel and row.  A chunk that breaks this
 // (decays stronger than ~exp(-80) across half a chunk) takes a CUDA-core path
 // that evaluates every exp(G_i - G_j) directly, so any finite gates <= 0 work.
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <cuda.h>
@@ -101,6 +102,7 @@ static_assert(IMG_BYTES <= IMG_STRIDE && IMG_STRIDE % 1024 == 0, "image slot");
 struct Scratch {
     uint8_t *img;        // [n_chunks x H] x IMG_STRIDE
     uint8_t *sst;        // [n_chunks x H x value tiles] S_c images (f16, 16 KB each)
+    uint32_t *ready;     // [n_chunks x H] image written (prep and scan run concurrently)
     int32_t *chunk_off;  // [N + 1]
 };
 
@@ -114,6 +116,7 @@ Scratch carve(void *ws, int32_t N, int32_t T, int32_t H) {
     Scratch s;
     s.img = p; p += align256(nch * IMG_STRIDE);
     s.sst = p; p += align256(nch * NT * (size_t)(D * 128));
+    s.ready = reinterpret_cast<uint32_t *>(p); p += align256(nch * sizeof(uint32_t));
     s.chunk_off = reinterpret_cast<int32_t *>(p);
     return s;
 }
@@ -130,13 +133,18 @@ __device__ __forceinline__ void seq_bounds(const int32_t *cu, int32_t s, int32_t
 }
 
 // ---------------------------------------------------------------------------
-// 1. chunk table: chunk_off[s] = number of chunks before sequence s
+// 1. chunk table: chunk_off[s] = number of chunks before sequence s (CTA 0);
+//    every CTA also clears a share of the n_ready image flags.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t *cu, int32_t N,
-                                                           int32_t T, int32_t *chunk_off) {
+                                                           int32_t T, int32_t *chunk_off,
+                                                           uint32_t *ready, size_t n_ready) {
     __shared__ int32_t warp_sum[32];
     __shared__ int32_t carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (size_t i = (size_t)blockIdx.x * 1024 + tid; i < n_ready; i += (size_t)gridDim.x * 1024)
+        ready[i] = 0u;
+    if (blockIdx.x != 0) return;
     if (tid == 0) carry = 0;
     __syncthreads();
     for (int32_t base = 0; base < N; base += 1024) {
@@ -309,7 +317,7 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
                   const __nv_bfloat16 *__restrict__ k, const float *__restrict__ beta,
                   float scale, const int32_t *__restrict__ cu, int32_t N, int32_t T, int32_t H,
                   int32_t grp, int32_t pro, const float *__restrict__ gbias,
-                  const float *__restrict__ galog, Scratch sc, int *status) {
+                  const float *__restrict__ galog, Scratch sc, int32_t streamed, int *status) {
     extern __shared__ uint8_t smem_raw[];
     PrepSmem &sm = *reinterpret_cast<PrepSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -325,9 +333,15 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
     uint8_t *zst = sm.b1;             // Z staging (after the MMAs that read A^kk)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    pdl_wait_primaries();      // the chunk table
-    pdl_launch_dependents();   // the scan may start setting up once every prep CTA runs
-    const int32_t c = blockIdx.x, h = blockIdx.y;
+    // After the chunk table as a programmatic dependent: wait for the table.
+    // Streamed (launched behind the scan, which waits on the image flags):
+    // the table is complete before the scan starts, and waiting here for the
+    // scan would never end.
+    if (!streamed) pdl_wait_primaries();
+    pdl_launch_dependents();   // the next kernel may start setting up once every prep CTA runs
+    // heads fastest: the images of chunk 0 of every head come first, in the
+    // order the scan consumes them
+    const int32_t c = (int32_t)(blockIdx.x / (unsigned)H), h = (int32_t)(blockIdx.x % (unsigned)H);
     const int32_t total = sc.chunk_off[N];
     if (c >= total) return;
     const int32_t s = find_seq(sc.chunk_off, N, c);
@@ -698,7 +712,14 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
         bulk_s2g(img + IMG_Z, zst, IMG_Q1 - IMG_Z);
         bulk_s2g(img + IMG_Q1, sm.a1 + IMG_Z, IMG_GB - IMG_Q1);
         bulk_commit_group();
-        bulk_wait_group_read<0>();  // the shared memory may go; the writes land on their own
+        if (streamed) {
+            // publish the image to the scan, which is already running
+            bulk_wait_group_all();
+            fence_proxy_async_global();
+            flag_release(sc.ready + ch, 1u);
+        } else {
+            bulk_wait_group_read<0>();  // the shared memory may go; the writes land on their own
+        }
     }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
@@ -802,12 +823,14 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                   const float *__restrict__ initial_state,
                   const int32_t *__restrict__ cu, float *__restrict__ final_state, int32_t N,
-                  int32_t T, int32_t H, Scratch sc, int *status) {
+                  int32_t T, int32_t H, Scratch sc, int32_t streamed, int *status) {
     extern __shared__ uint8_t smem_raw[];
     ScanSmem &sm = *reinterpret_cast<ScanSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    pdl_launch_dependents();  // the output pass may start setting up
+    // the next kernel (the output pass; streamed: the prep) may start once
+    // every scan CTA runs
+    pdl_launch_dependents();
     const int32_t seq = blockIdx.x / NT, vt = blockIdx.x % NT, h = blockIdx.y;
     int32_t ta, tb;
     seq_bounds(cu, seq, T, ta, tb);
@@ -859,7 +882,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
         if (warp == 4) {
             // -------- producer: -M' and P' of a chunk, once its stage is free --------
             if (lane == 0) {
-                pdl_wait_primaries();  // the prep kernel has written every image
+                pdl_wait_primaries();  // not streamed: the prep has written every image
                 for (int32_t n = 0; n < n_chunks; ++n) {
                     const int stg = n % NSTAGE;
                     if (n >= NSTAGE) {
@@ -869,6 +892,15 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                             sm.abort_flag = 1;
                             break;
                         }
+                    }
+                    if (streamed) {
+                        // the prep CTA of this chunk publishes its image
+                        if (!flag_wait_bounded(sc.ready + (size_t)(c_begin + n) * H + h,
+                                               kWaitCycles)) {
+                            sm.abort_flag = 1;
+                            break;
+                        }
+                        fence_proxy_async_global();
                     }
                     mbar_arrive_expect_tx(&sm.full[stg],
                                           SCAN_IMG + C * 128 + (D + C) * (uint32_t)sizeof(float));
@@ -1206,13 +1238,16 @@ constexpr size_t kOutSmem = sizeof(OutSmem) + 1024;
 static_assert(kScanSmem <= 227 * 1024, "scan shared memory");
 static_assert(2 * kOutSmem <= 228 * 1024 - 2 * 1024, "two output CTAs per SM");
 static_assert(2 * kPrepSmem <= 228 * 1024 - 2 * 1024, "two prep CTAs per SM");
+// Largest prep grid run concurrently with the scan: the scan's wait for an
+// image is bounded (~1 s), and a prep of this many items ends well within it.
+constexpr size_t kStreamMaxItems = 1u << 16;
 
 }  // namespace
 
 size_t chunk_tc_workspace_bytes(int32_t N, int32_t T, int32_t H) {
     const size_t nch = max_chunks(N, T) * (size_t)H;
     return align256(nch * IMG_STRIDE) + align256(nch * NT * (size_t)(D * 128)) +
-           align256(((size_t)N + 1) * sizeof(int32_t));
+           align256(nch * sizeof(uint32_t)) + align256(((size_t)N + 1) * sizeof(int32_t));
 }
 
 // cuTensorMapEncodeTiled, fetched from the driver once (no libcuda link).
@@ -1250,65 +1285,109 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
     if (workspace_bytes < chunk_tc_workspace_bytes(a.N, a.T, a.H) || !workspace)
         return cudaErrorInvalidValue;
     const Scratch sc = carve(workspace, a.N, a.T, a.H);
-    // The later kernels go out as programmatic dependents: each one's CTAs can
-    // be resident and set up while the kernel ahead drains, and wait
-    // (griddepcontrol.wait) before reading its results.  With per-kernel
-    // events between them (clock) they are plain launches.
+    // Sequential order: table -> prep -> scan -> output, each after the first
+    // a programmatic dependent (its CTAs become resident and set up while the
+    // kernel ahead drains, then wait on griddepcontrol before reading its
+    // results).  With per-kernel events between them (clock) the launches are
+    // plain.
+    //
+    // Streamed order, when the scan's CTAs take at most half of the SMs:
+    // table -> scan -> prep (programmatic dependent of the scan, so it starts
+    // once every scan CTA is resident) -> output.  The scan follows the prep
+    // chunk by chunk through the image flags, so its serial chain runs under
+    // the prep's parallel work instead of after it.  The output pass is a
+    // plain launch: it waits for both.
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
-    const unsigned n_pdl = (a.clock && a.clock->max_events > 0) ? 0u : 1u;
-    auto config = [&](dim3 grid, int threads, size_t smem) {
+    const bool timed = a.clock && a.clock->max_events > 0;
+    const size_t n_items = max_chunks(a.N, a.T) * (size_t)a.H;  // prep CTAs
+    const size_t scan_ctas = (size_t)a.N * NT * (size_t)a.H;
+    bool streamed = false;
+    if (!timed && a.T > 0 && n_items <= kStreamMaxItems) {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+            streamed = 2 * scan_ctas <= (size_t)sms;
+    }
+    auto config = [&](dim3 grid, int threads, size_t smem, bool dependent) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
         cfg.blockDim = dim3((unsigned)threads);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
         cfg.attrs = pdl;
-        cfg.numAttrs = n_pdl;
+        cfg.numAttrs = (dependent && !timed) ? 1u : 0u;
         return cfg;
     };
-    chunk_table_kernel<<<1, 1024, 0, stream>>>(a.cu_seqlens, a.N, a.T, sc.chunk_off);
-    a.clock->mark(stream);
-    cudaError_t e = cudaGetLastError();
+    // Every kernel is set up (and so loaded, under lazy module loading) before
+    // the first launch: loading the prep while the scan already waits for it
+    // would wait for the scan.
+    auto prep = a.pro ? chunk_prep_kernel<true> : chunk_prep_kernel<false>;
+    auto out_kernel_f32 = chunk_out_kernel<float>;
+    auto out_kernel_bf16 = chunk_out_kernel<__nv_bfloat16>;
+    cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kPrepSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kScanSmem);
+    if (e == cudaSuccess)
+        e = a.out_f32 ? cudaFuncSetAttribute(out_kernel_f32,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kOutSmem)
+                      : cudaFuncSetAttribute(out_kernel_bf16,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kOutSmem);
     if (e != cudaSuccess) return e;
 
+    // the tensor maps too, so that the prep follows the scan without delay
+    PrepMaps maps;
+    CUtensorMap v_map;
+    memset(&maps, 0, sizeof(maps));
+    memset(&v_map, 0, sizeof(v_map));
     if (a.T > 0) {
-        PrepMaps maps;
         if (!encode_tile_map(&maps.q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H / a.G) ||
             !encode_tile_map(&maps.k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H / a.G) ||
             !encode_tile_map(&maps.g, a.log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.T, a.H))
             return cudaErrorInvalidValue;
-        auto prep = a.pro ? chunk_prep_kernel<true> : chunk_prep_kernel<false>;
-        e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kPrepSmem);
-        if (e != cudaSuccess) return e;
+        // value tiles [64 tokens x 64 columns] of one head, 128-byte swizzle
+        if (!encode_tile_map(&v_map, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, BV,
+                             CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+
+    const size_t n_ready = streamed ? n_items : 0;
+    const unsigned table_ctas = 1u + (unsigned)std::min<size_t>(n_ready / 16384, 63);
+    chunk_table_kernel<<<table_ctas, 1024, 0, stream>>>(a.cu_seqlens, a.N, a.T, sc.chunk_off,
+                                                        sc.ready, n_ready);
+    a.clock->mark(stream);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    auto launch_scan = [&](bool dependent) {
         const cudaLaunchConfig_t cfg =
-            config(dim3((unsigned)max_chunks(a.N, a.T), (unsigned)a.H), kPrepThreads, kPrepSmem);
+            config(dim3((unsigned)(a.N * NT), (unsigned)a.H), kScanThreads, kScanSmem, dependent);
+        return cudaLaunchKernelEx(&cfg, chunk_scan_kernel, v_map, a.initial_state,
+                                  static_cast<const int32_t *>(a.cu_seqlens), a.final_state, a.N,
+                                  a.T, a.H, sc, (int32_t)streamed, a.status);
+    };
+    if (streamed) {
+        e = launch_scan(false);
+        if (e != cudaSuccess) return e;
+    }
+
+    if (a.T > 0) {
+        const cudaLaunchConfig_t cfg = config(dim3((unsigned)n_items), kPrepThreads, kPrepSmem, true);
         e = cudaLaunchKernelEx(&cfg, prep, maps, static_cast<const __nv_bfloat16 *>(a.q),
                                static_cast<const __nv_bfloat16 *>(a.k), a.beta, a.scale,
                                static_cast<const int32_t *>(a.cu_seqlens), a.N, a.T, a.H, a.G,
-                               a.pro, a.gbias, a.galog, sc, a.status);
+                               a.pro, a.gbias, a.galog, sc, (int32_t)streamed, a.status);
         if (e != cudaSuccess) return e;
     }
     a.clock->mark(stream);
 
-    const dim3 sgrid((unsigned)(a.N * NT), (unsigned)a.H);
-    // value tiles [64 tokens x 64 columns] of one head, 128-byte swizzle; unused when T == 0
-    CUtensorMap v_map;
-    memset(&v_map, 0, sizeof(v_map));
-    if (a.T > 0 && !encode_tile_map(&v_map, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H,
-                                    BV, CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-    e = cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kScanSmem);
-    if (e != cudaSuccess) return e;
-    {
-        cudaLaunchConfig_t cfg = config(sgrid, kScanThreads, kScanSmem);
-        if (a.T == 0) cfg.numAttrs = 0;  // no prep ahead of it
-        e = cudaLaunchKernelEx(&cfg, chunk_scan_kernel, v_map, a.initial_state,
-                               static_cast<const int32_t *>(a.cu_seqlens), a.final_state, a.N,
-                               a.T, a.H, sc, a.status);
+    if (!streamed) {
+        e = launch_scan(a.T > 0);  // with T == 0 no prep runs ahead of it
         if (e != cudaSuccess) return e;
     }
     a.clock->mark(stream);
@@ -1329,21 +1408,15 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        const cudaLaunchConfig_t cfg =
-            config(dim3((unsigned)max_chunks(a.N, a.T), (unsigned)a.H), kOutThreads, kOutSmem);
+        const cudaLaunchConfig_t cfg = config(dim3((unsigned)max_chunks(a.N, a.T), (unsigned)a.H),
+                                              kOutThreads, kOutSmem, !streamed);
         const __nv_bfloat16 *vb = static_cast<const __nv_bfloat16 *>(a.v);
         const int32_t *cu = static_cast<const int32_t *>(a.cu_seqlens);
         if (a.out_f32) {
-            e = cudaFuncSetAttribute(chunk_out_kernel<float>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOutSmem);
-            if (e != cudaSuccess) return e;
-            e = cudaLaunchKernelEx(&cfg, chunk_out_kernel<float>, out_map, vb, cu,
+            e = cudaLaunchKernelEx(&cfg, out_kernel_f32, out_map, vb, cu,
                                    static_cast<float *>(a.out), a.N, a.T, a.H, sc, a.status);
         } else {
-            e = cudaFuncSetAttribute(chunk_out_kernel<__nv_bfloat16>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOutSmem);
-            if (e != cudaSuccess) return e;
-            e = cudaLaunchKernelEx(&cfg, chunk_out_kernel<__nv_bfloat16>, out_map, vb, cu,
+            e = cudaLaunchKernelEx(&cfg, out_kernel_bf16, out_map, vb, cu,
                                    static_cast<__nv_bfloat16 *>(a.out), a.N, a.T, a.H, sc,
                                    a.status);
         }

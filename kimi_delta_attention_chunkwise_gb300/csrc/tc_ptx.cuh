@@ -92,6 +92,35 @@ __device__ __forceinline__ void pdl_wait_primaries() {
 }
 
 // ---------------------------------------------------------------------------
+// hand-off between CTAs of concurrently running kernels: the producer writes
+// with bulk copies, waits for them, and publishes a flag with release
+// semantics; the consumer acquires the flag before it reads with bulk copies.
+// The proxy fences order the bulk-copy (async proxy) accesses against the
+// flag's ordinary (generic proxy) access on each side.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ void flag_release(uint32_t *f, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t flag_acquire(const uint32_t *f) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+}
+// Spins (with a short sleep) until *f is non-zero or max_cycles have passed.
+__device__ __forceinline__ bool flag_wait_bounded(const uint32_t *f, long long max_cycles) {
+    if (flag_acquire(f)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        __nanosleep(100);
+        if (flag_acquire(f)) return true;
+        if (clock64() - t0 > max_cycles) return false;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // bulk async copy global -> shared, completion counted on an mbarrier
 // (addresses 16-byte aligned, size a multiple of 16)
 // ---------------------------------------------------------------------------
