@@ -103,12 +103,15 @@ struct Scratch {
     uint8_t *img;        // [n_chunks x H] x IMG_STRIDE
     uint8_t *sst;        // [n_chunks x H x value tiles] S_c images (f16, 16 KB each)
     uint32_t *ready;     // [n_chunks x H] image written (prep and scan run concurrently)
+    int2 *chunk_tok;     // [max chunks] first token and length of each chunk (0: none)
     int32_t *chunk_off;  // [N + 1]
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-size_t max_chunks(int32_t N, int32_t T) { return (size_t)T / C + (size_t)N + 1; }
+__host__ __device__ inline size_t max_chunks(int32_t N, int32_t T) {
+    return (size_t)T / C + (size_t)N + 1;
+}
 
 Scratch carve(void *ws, int32_t N, int32_t T, int32_t H) {
     const size_t nch = max_chunks(N, T) * (size_t)H;
@@ -117,6 +120,7 @@ Scratch carve(void *ws, int32_t N, int32_t T, int32_t H) {
     s.img = p; p += align256(nch * IMG_STRIDE);
     s.sst = p; p += align256(nch * NT * (size_t)(D * 128));
     s.ready = reinterpret_cast<uint32_t *>(p); p += align256(nch * sizeof(uint32_t));
+    s.chunk_tok = reinterpret_cast<int2 *>(p); p += align256(max_chunks(N, T) * sizeof(int2));
     s.chunk_off = reinterpret_cast<int32_t *>(p);
     return s;
 }
@@ -132,13 +136,25 @@ __device__ __forceinline__ void seq_bounds(const int32_t *cu, int32_t s, int32_t
     }
 }
 
+// Largest s with chunk_off[s] <= c (chunk_off is non-decreasing).
+__device__ __forceinline__ int32_t find_seq(const int32_t *off, int32_t N, int32_t c) {
+    int32_t lo = 0, hi = N - 1;
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (off[mid] <= c) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
 // ---------------------------------------------------------------------------
-// 1. chunk table: chunk_off[s] = number of chunks before sequence s (CTA 0);
-//    every CTA also clears a share of the n_ready image flags.
+// 1. chunk table (CTA 0): chunk_off[s] = number of chunks before sequence s,
+//    and chunk_tok[c] = {first token, length} of chunk c ({0, 0} past the
+//    last chunk); every CTA also clears a share of the n_ready image flags.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t *cu, int32_t N,
                                                            int32_t T, int32_t *chunk_off,
-                                                           uint32_t *ready, size_t n_ready) {
+                                                           int2 *chunk_tok, uint32_t *ready,
+                                                           size_t n_ready) {
     __shared__ int32_t warp_sum[32];
     __shared__ int32_t carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -180,17 +196,21 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t *cu, in
         __syncthreads();
     }
     if (tid == 0) chunk_off[N] = carry;
+    __syncthreads();  // chunk_off is visible to the whole CTA
+    const int32_t total = chunk_off[N], n_max = (int32_t)max_chunks(N, T);
+    for (int32_t c = tid; c < n_max; c += 1024) {
+        int2 tok = make_int2(0, 0);
+        if (c < total) {
+            const int32_t s = find_seq(chunk_off, N, c);
+            int32_t a, b;
+            seq_bounds(cu, s, T, a, b);
+            tok.x = a + (c - chunk_off[s]) * C;
+            tok.y = min(C, b - tok.x);
+        }
+        chunk_tok[c] = tok;
+    }
 }
 
-// Largest s with chunk_off[s] <= c (chunk_off is non-decreasing).
-__device__ __forceinline__ int32_t find_seq(const int32_t *off, int32_t N, int32_t c) {
-    int32_t lo = 0, hi = N - 1;
-    while (lo < hi) {
-        const int32_t mid = (lo + hi + 1) >> 1;
-        if (off[mid] <= c) lo = mid; else hi = mid - 1;
-    }
-    return lo;
-}
 
 // ---------------------------------------------------------------------------
 // 2. per-(chunk, head) preparation
@@ -317,7 +337,8 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
                   const __nv_bfloat16 *__restrict__ k, const float *__restrict__ beta,
                   float scale, const int32_t *__restrict__ cu, int32_t N, int32_t T, int32_t H,
                   int32_t grp, int32_t pro, const float *__restrict__ gbias,
-                  const float *__restrict__ galog, Scratch sc, int32_t streamed, int *status) {
+                  const float *__restrict__ galog, Scratch sc, int32_t streamed,
+                  int32_t prefetch_dist, int *status) {
     extern __shared__ uint8_t smem_raw[];
     PrepSmem &sm = *reinterpret_cast<PrepSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -342,13 +363,9 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
     // heads fastest: the images of chunk 0 of every head come first, in the
     // order the scan consumes them
     const int32_t c = (int32_t)(blockIdx.x / (unsigned)H), h = (int32_t)(blockIdx.x % (unsigned)H);
-    const int32_t total = sc.chunk_off[N];
-    if (c >= total) return;
-    const int32_t s = find_seq(sc.chunk_off, N, c);
-    int32_t ta, tb;
-    seq_bounds(cu, s, T, ta, tb);
-    const int32_t t0 = ta + (c - sc.chunk_off[s]) * C;
-    const int32_t L = min(C, tb - t0);
+    const int2 tok = sc.chunk_tok[c];
+    const int32_t t0 = tok.x, L = tok.y;
+    if (L <= 0) return;
     const size_t ch = (size_t)c * H + h;
     uint8_t *img = sc.img + ch * IMG_STRIDE;
     float *gb = reinterpret_cast<float *>(img + IMG_GB);
@@ -364,6 +381,18 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
         tma_load_3d(sm.b1, &maps.k, 0, hq, t0, &sm.bar_in);
         tma_load_3d(sm.b1 + C * D * 2, &maps.q, 0, hq, t0, &sm.bar_in);
         tma_load_3d(sm.a1, &maps.g, 0, h, t0, &sm.bar_in);
+        // The item that will take this CTA's place about one full wave of
+        // resident CTAs later: its tiles go to L2 now.
+        const unsigned ahead = blockIdx.x + (unsigned)prefetch_dist;
+        if (prefetch_dist > 0 && ahead < gridDim.x) {
+            const int32_t ca = (int32_t)(ahead / (unsigned)H), ha = (int32_t)(ahead % (unsigned)H);
+            const int2 ta = sc.chunk_tok[ca];
+            if (ta.y > 0) {
+                tma_prefetch_l2_3d(&maps.k, 0, ha / grp, ta.x);
+                tma_prefetch_l2_3d(&maps.q, 0, ha / grp, ta.x);
+                tma_prefetch_l2_3d(&maps.g, 0, ha, ta.x);
+            }
+        }
     }
     if (warp == 0) {
         tmem_alloc(&sm.tmem, 256);
@@ -1090,13 +1119,9 @@ chunk_out_kernel(const __grid_constant__ CUtensorMap out_map, const __nv_bfloat1
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5;
     const int32_t c = blockIdx.x, h = blockIdx.y;
-    const int32_t total = sc.chunk_off[N];
-    if (c >= total) return;
-    const int32_t s = find_seq(sc.chunk_off, N, c);
-    int32_t ta, tb;
-    seq_bounds(cu, s, T, ta, tb);
-    const int32_t t0 = ta + (c - sc.chunk_off[s]) * C;
-    const int32_t L = min(C, tb - t0);
+    const int2 tok = sc.chunk_tok[c];
+    const int32_t t0 = tok.x, L = tok.y;
+    if (L <= 0) return;
     const uint8_t *img = sc.img + ((size_t)c * H + h) * IMG_STRIDE;
 
     pdl_wait_primaries();  // the scan (and before it the prep) has finished
@@ -1247,7 +1272,8 @@ constexpr size_t kStreamMaxItems = 1u << 16;
 size_t chunk_tc_workspace_bytes(int32_t N, int32_t T, int32_t H) {
     const size_t nch = max_chunks(N, T) * (size_t)H;
     return align256(nch * IMG_STRIDE) + align256(nch * NT * (size_t)(D * 128)) +
-           align256(nch * sizeof(uint32_t)) + align256(((size_t)N + 1) * sizeof(int32_t));
+           align256(nch * sizeof(uint32_t)) + align256(max_chunks(N, T) * sizeof(int2)) +
+           align256(((size_t)N + 1) * sizeof(int32_t));
 }
 
 // cuTensorMapEncodeTiled, fetched from the driver once (no libcuda link).
@@ -1303,13 +1329,14 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
     const bool timed = a.clock && a.clock->max_events > 0;
     const size_t n_items = max_chunks(a.N, a.T) * (size_t)a.H;  // prep CTAs
     const size_t scan_ctas = (size_t)a.N * NT * (size_t)a.H;
-    bool streamed = false;
-    if (!timed && a.T > 0 && n_items <= kStreamMaxItems) {
-        int dev = 0, sms = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess &&
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
-            streamed = 2 * scan_ctas <= (size_t)sms;
-    }
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 0;
+    const bool streamed =
+        !timed && a.T > 0 && n_items <= kStreamMaxItems && sms > 0 && 2 * scan_ctas <= (size_t)sms;
+    // prep CTAs resident at once (two per SM on the SMs the scan leaves)
+    const int32_t prefetch_dist = 2 * (sms - (streamed ? (int32_t)scan_ctas : 0));
     auto config = [&](dim3 grid, int threads, size_t smem, bool dependent) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
@@ -1359,7 +1386,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
     const size_t n_ready = streamed ? n_items : 0;
     const unsigned table_ctas = 1u + (unsigned)std::min<size_t>(n_ready / 16384, 63);
     chunk_table_kernel<<<table_ctas, 1024, 0, stream>>>(a.cu_seqlens, a.N, a.T, sc.chunk_off,
-                                                        sc.ready, n_ready);
+                                                        sc.chunk_tok, sc.ready, n_ready);
     a.clock->mark(stream);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -1381,7 +1408,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
         e = cudaLaunchKernelEx(&cfg, prep, maps, static_cast<const __nv_bfloat16 *>(a.q),
                                static_cast<const __nv_bfloat16 *>(a.k), a.beta, a.scale,
                                static_cast<const int32_t *>(a.cu_seqlens), a.N, a.T, a.H, a.G,
-                               a.pro, a.gbias, a.galog, sc, (int32_t)streamed, a.status);
+                               a.pro, a.gbias, a.galog, sc, (int32_t)streamed, prefetch_dist,
+                               a.status);
         if (e != cudaSuccess) return e;
     }
     a.clock->mark(stream);

@@ -151,6 +151,14 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int32_t
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
 }
+// Brings a 3-D tile into L2 only (a hint: no completion, no shared memory).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int32_t x, int32_t y,
+                                                   int32_t z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
 
 // Tiled tensor store (TMA) from shared memory, bulk-group completion.
 __device__ __forceinline__ void tma_store_3d(const void *tmap, const void *src, int32_t x,
