@@ -102,7 +102,8 @@ static_assert(IMG_BYTES <= IMG_STRIDE && IMG_STRIDE % 1024 == 0, "image slot");
 struct Scratch {
     uint8_t *img;        // [n_chunks x H] x IMG_STRIDE
     uint8_t *sst;        // [n_chunks x H x value tiles] S_c images (f16, 16 KB each)
-    uint32_t *ready;     // [n_chunks x H] image written (prep and scan run concurrently)
+    uint32_t *ready;     // image written [n_chunks x H], then state images written
+                         // [n_chunks x H x value tiles] (kernels run concurrently)
     int2 *chunk_tok;     // [max chunks] first token and length of each chunk (0: none)
     int32_t *chunk_off;  // [N + 1]
 };
@@ -119,7 +120,7 @@ Scratch carve(void *ws, int32_t N, int32_t T, int32_t H) {
     Scratch s;
     s.img = p; p += align256(nch * IMG_STRIDE);
     s.sst = p; p += align256(nch * NT * (size_t)(D * 128));
-    s.ready = reinterpret_cast<uint32_t *>(p); p += align256(nch * sizeof(uint32_t));
+    s.ready = reinterpret_cast<uint32_t *>(p); p += align256(nch * (1 + NT) * sizeof(uint32_t));
     s.chunk_tok = reinterpret_cast<int2 *>(p); p += align256(max_chunks(N, T) * sizeof(int2));
     s.chunk_off = reinterpret_cast<int32_t *>(p);
     return s;
@@ -781,12 +782,14 @@ struct ScanSmem {
     uint64_t ready_s;            // S_c operand written (compute -> issuer)
     uint64_t ready_bv[2];        // beta V operand written, per buffer
     uint64_t mma_s;              // chunk's state increment complete
+    uint64_t sb_read;            // S_c copied out of sb (state writer -> compute)
     uint32_t tmem;
     volatile int32_t issued;     // bulk copies issued (error path drains them)
     volatile int32_t abort_flag;
 };
 
-constexpr int kScanThreads = 192;  // warps 0-3 compute, 4 streams operands in, 5 issues MMAs
+// warps 0-3 compute, 4 streams operands in, 5 issues MMAs, 6 writes the S_c images out
+constexpr int kScanThreads = 224;
 constexpr uint32_t kScanTmemCols = 128;  // D2 ping-pong (2 x BV)
 constexpr uint32_t kStateImg = D * 128;  // one value tile of S_c, f16 image
 
@@ -852,7 +855,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                   const float *__restrict__ initial_state,
                   const int32_t *__restrict__ cu, float *__restrict__ final_state, int32_t N,
-                  int32_t T, int32_t H, Scratch sc, int32_t streamed, int *status) {
+                  int32_t T, int32_t H, Scratch sc, int32_t streamed, int64_t sc_items,
+                  int *status) {
     extern __shared__ uint8_t smem_raw[];
     ScanSmem &sm = *reinterpret_cast<ScanSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -891,6 +895,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
             mbar_init(&sm.ready_bv[0], 128);
             mbar_init(&sm.ready_bv[1], 128);
             mbar_init(&sm.mma_s, 1);
+            mbar_init(&sm.sb_read, 1);
             sm.issued = 0;
             sm.abort_flag = 0;
             fence_mbar_init();
@@ -906,6 +911,9 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
         constexpr uint32_t IDESC = idesc_f16_f32(128, BV) | (1u << 16);  // B MN-major
         auto chunk_img = [&](int32_t n) {
             return sc.img + ((size_t)(c_begin + n) * H + h) * IMG_STRIDE;
+        };
+        auto state_img = [&](int32_t n) {
+            return sc.sst + (((size_t)(c_begin + n) * H + h) * NT + vt) * kStateImg;
         };
 
         if (warp == 4) {
@@ -985,6 +993,38 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                         sm.abort_flag = 1;
             }
             __syncwarp();
+        } else if (warp == 6) {
+            // -------- state writer: the S_c images out (streamed: and their flags,
+            // for the output pass), off the compute warps' chain --------
+            if (lane == 0) {
+                auto publish = [&](int32_t n) {
+                    fence_proxy_async_global();
+                    flag_release(sc.ready + (size_t)sc_items +
+                                     ((size_t)(c_begin + n) * H + h) * NT + vt,
+                                 1u);
+                };
+                int32_t copied = 0;
+                for (int32_t n = 0; n < n_chunks; ++n) {
+                    // S_c in sb[n & 1], written and fenced by the compute warps
+                    if (!mbar_wait_bounded(&sm.ready_s, (uint32_t)n & 1u, kWaitCycles) ||
+                        sm.abort_flag) {
+                        sm.abort_flag = 1;
+                        break;
+                    }
+                    bulk_s2g(state_img(n), sm.sb[n & 1], kStateImg);
+                    bulk_commit_group();
+                    bulk_wait_group_read<0>();
+                    mbar_arrive(&sm.sb_read);
+                    copied = n + 1;
+                    if (streamed && n >= 1) {
+                        bulk_wait_group<1>();  // the copy of chunk n - 1 has landed
+                        publish(n - 1);
+                    }
+                }
+                bulk_wait_group_all();  // state images written
+                if (streamed && copied > 0 && !sm.abort_flag) publish(copied - 1);
+            }
+            __syncwarp();
         } else {
             // ---------------- compute warps ----------------
             // Everything a chunk needs arrives with its stage (no global loads in
@@ -1012,7 +1052,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                     sm.abort_flag = 1;
             };
             // S_c of chunk n as the MMA's B operand (f16); the same image goes out
-            // to global memory for the output pass as one bulk copy (below)
+            // to global memory for the output pass (the writer warp copies it)
             auto put_state = [&](int32_t n) {
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8)
@@ -1020,24 +1060,15 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                         pack8_f16(&S[c8 * 8]);
                 fence_proxy_async();
             };
-            auto state_img = [&](int32_t n) {
-                return sc.sst + (((size_t)(c_begin + n) * H + h) * NT + vt) * kStateImg;
-            };
 
             wait_full(0);
             float g = sm.gbs[0][tid];  // Gamma_last of chunk n (read before its stage is freed)
             build_bv(0);
             put_state(0);
             for (int32_t n = 0; n < n_chunks; ++n) {
-                // the previous chunk's state copy has read sb[(n + 1) & 1]
-                if (tid == 0) bulk_wait_group_read<0>();
                 if (compute_barrier_or(sm.abort_flag != 0)) break;
                 tc_fence_before();
                 mbar_arrive(&sm.ready_s);
-                if (tid == 0) {
-                    bulk_s2g(state_img(n), sm.sb[n & 1], kStateImg);
-                    bulk_commit_group();
-                }
                 const bool more = n + 1 < n_chunks;
                 float g_next = 0.f;
                 if (more) {
@@ -1061,9 +1092,15 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                     }
                 }
                 g = g_next;
-                if (more) put_state(n + 1);
+                if (more) {
+                    // sb[(n + 1) & 1] holds S_n-1; once the writer has copied S_n
+                    // out, it is long done with S_n-1 (waiting for the later copy
+                    // keeps the barrier's phases unambiguous)
+                    if (!mbar_wait_bounded(&sm.sb_read, (uint32_t)n & 1u, kWaitCycles))
+                        sm.abort_flag = 1;
+                    put_state(n + 1);
+                }
             }
-            if (tid == 0) bulk_wait_group_all();  // state images written
         }
         __syncthreads();
         if (sm.abort_flag) {
@@ -1113,19 +1150,32 @@ template <typename TOut>
 __global__ void __launch_bounds__(kOutThreads)
 chunk_out_kernel(const __grid_constant__ CUtensorMap out_map, const __nv_bfloat16 *__restrict__ v,
                  const int32_t *__restrict__ cu, TOut *__restrict__ out, int32_t N, int32_t T,
-                 int32_t H, Scratch sc, int *status) {
+                 int32_t H, Scratch sc, int32_t streamed, int64_t sc_items, int *status) {
     extern __shared__ uint8_t smem_raw[];
     OutSmem &sm = *reinterpret_cast<OutSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int32_t c = blockIdx.x, h = blockIdx.y;
+    // heads fastest: the order in which the scan finishes the chunks' states
+    const int32_t c = (int32_t)(blockIdx.x / (unsigned)H), h = (int32_t)(blockIdx.x % (unsigned)H);
     const int2 tok = sc.chunk_tok[c];
     const int32_t t0 = tok.x, L = tok.y;
     if (L <= 0) return;
     const uint8_t *img = sc.img + ((size_t)c * H + h) * IMG_STRIDE;
 
-    pdl_wait_primaries();  // the scan (and before it the prep) has finished
+    // Sequential: the scan (and before it the prep) has finished.  Streamed
+    // (running beside the prep's last CTAs and the scan): this chunk's image
+    // and both value tiles of its S_c are up.  A wait that runs out leaves the
+    // status set and garbage outputs, never a hang.
+    if (!streamed) pdl_wait_primaries();
     if (tid == 0) {
+        if (streamed) {
+            bool got = flag_wait_bounded(sc.ready + (size_t)c * H + h, kWaitCycles);
+            for (int t = 0; t < NT && got; ++t)
+                got = flag_wait_bounded(sc.ready + sc_items + ((size_t)c * H + h) * NT + t,
+                                        kWaitCycles);
+            if (!got) atomicExch(status, (int)KDA_ERR_TIMEOUT);
+            fence_proxy_async_global();
+        }
         mbar_init(&sm.bar_in, 1);
         mbar_init(&sm.bar_mma, 1);
         fence_mbar_init();
@@ -1134,6 +1184,7 @@ chunk_out_kernel(const __grid_constant__ CUtensorMap out_map, const __nv_bfloat1
         bulk_g2s(sm.sS, sc.sst + ((size_t)c * H + h) * NT * kStateImg, NT * kStateImg,
                  &sm.bar_in);
     }
+    if (streamed) __syncthreads();  // beta below comes from the image too
     if (warp == 0) {
         tmem_alloc(&sm.tmem, 128);
         tmem_relinquish();
@@ -1148,7 +1199,7 @@ chunk_out_kernel(const __grid_constant__ CUtensorMap out_map, const __nv_bfloat1
                 v + ((size_t)(t0 + i) * H + h) * D + half * BV);
 #pragma unroll
             for (int j = 0; j < 8; ++j) x[j >> 2][j & 3] = __ldg(src + j);
-            b = reinterpret_cast<const float *>(img + IMG_GB)[128 + i];
+            b = __ldcg(reinterpret_cast<const float *>(img + IMG_GB) + 128 + i);
         } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j) x[j >> 2][j & 3] = make_uint4(0, 0, 0, 0);
@@ -1272,7 +1323,7 @@ constexpr size_t kStreamMaxItems = 1u << 16;
 size_t chunk_tc_workspace_bytes(int32_t N, int32_t T, int32_t H) {
     const size_t nch = max_chunks(N, T) * (size_t)H;
     return align256(nch * IMG_STRIDE) + align256(nch * NT * (size_t)(D * 128)) +
-           align256(nch * sizeof(uint32_t)) + align256(max_chunks(N, T) * sizeof(int2)) +
+           align256(nch * (1 + NT) * sizeof(uint32_t)) + align256(max_chunks(N, T) * sizeof(int2)) +
            align256(((size_t)N + 1) * sizeof(int32_t));
 }
 
@@ -1319,10 +1370,12 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
     //
     // Streamed order, when the scan's CTAs take at most half of the SMs:
     // table -> scan -> prep (programmatic dependent of the scan, so it starts
-    // once every scan CTA is resident) -> output.  The scan follows the prep
-    // chunk by chunk through the image flags, so its serial chain runs under
-    // the prep's parallel work instead of after it.  The output pass is a
-    // plain launch: it waits for both.
+    // once every scan CTA is resident) -> output (programmatic dependent of
+    // the prep, so it starts once every prep CTA has started).  The scan
+    // follows the prep chunk by chunk through the image flags, so its serial
+    // chain runs under the prep's parallel work instead of after it; the
+    // output CTAs follow the scan through the state flags and fill the SMs
+    // that the prep's last CTAs leave.
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1383,7 +1436,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
             return cudaErrorInvalidValue;
     }
 
-    const size_t n_ready = streamed ? n_items : 0;
+    const size_t n_ready = streamed ? n_items * (1 + NT) : 0;  // image and state flags
     const unsigned table_ctas = 1u + (unsigned)std::min<size_t>(n_ready / 16384, 63);
     chunk_table_kernel<<<table_ctas, 1024, 0, stream>>>(a.cu_seqlens, a.N, a.T, sc.chunk_off,
                                                         sc.chunk_tok, sc.ready, n_ready);
@@ -1396,7 +1449,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
             config(dim3((unsigned)(a.N * NT), (unsigned)a.H), kScanThreads, kScanSmem, dependent);
         return cudaLaunchKernelEx(&cfg, chunk_scan_kernel, v_map, a.initial_state,
                                   static_cast<const int32_t *>(a.cu_seqlens), a.final_state, a.N,
-                                  a.T, a.H, sc, (int32_t)streamed, a.status);
+                                  a.T, a.H, sc, (int32_t)streamed, (int64_t)n_items,
+                                  a.status);
     };
     if (streamed) {
         e = launch_scan(false);
@@ -1436,17 +1490,19 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        const cudaLaunchConfig_t cfg = config(dim3((unsigned)max_chunks(a.N, a.T), (unsigned)a.H),
-                                              kOutThreads, kOutSmem, !streamed);
+        // a programmatic dependent of the scan (sequential) or of the prep
+        // (streamed: its CTAs fill the SMs that the prep's last CTAs leave)
+        const cudaLaunchConfig_t cfg = config(dim3((unsigned)n_items), kOutThreads, kOutSmem, true);
         const __nv_bfloat16 *vb = static_cast<const __nv_bfloat16 *>(a.v);
         const int32_t *cu = static_cast<const int32_t *>(a.cu_seqlens);
         if (a.out_f32) {
             e = cudaLaunchKernelEx(&cfg, out_kernel_f32, out_map, vb, cu,
-                                   static_cast<float *>(a.out), a.N, a.T, a.H, sc, a.status);
+                                   static_cast<float *>(a.out), a.N, a.T, a.H, sc,
+                                   (int32_t)streamed, (int64_t)n_items, a.status);
         } else {
             e = cudaLaunchKernelEx(&cfg, out_kernel_bf16, out_map, vb, cu,
                                    static_cast<__nv_bfloat16 *>(a.out), a.N, a.T, a.H, sc,
-                                   a.status);
+                                   (int32_t)streamed, (int64_t)n_items, a.status);
         }
         if (e != cudaSuccess) return e;
     }

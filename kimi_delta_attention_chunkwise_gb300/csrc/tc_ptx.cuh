@@ -181,6 +181,12 @@ __device__ __forceinline__ void bulk_wait_group_read() {
 }
 
 // Wait until every committed bulk group has completed (writes visible).
+// Waits until at most N of this thread's most recent bulk groups are still
+// writing (the older ones are complete).
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
 __device__ __forceinline__ void bulk_wait_group_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
@@ -382,10 +388,13 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 
 // fp32 -> tf32 rounded to nearest (ties away from zero), kept in fp32 storage,
 // so the tensor core's own reduction of the operand is exact.
+// fp32 -> tf32 (10-bit significand), round to nearest with ties away from
+// zero, by integer arithmetic on the bit pattern: adding half a unit of the
+// 13 dropped bits carries into the kept ones exactly when the dropped part is
+// at least half.  Finite inputs only (the operands here are finite).  Two
+// integer operations instead of a conversion instruction.
 __device__ __forceinline__ float to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
 }
 
 // Byte offset of fp32 element (row, col) in a K-major SW128 panel (32 per row).
