@@ -782,8 +782,8 @@ struct ScanSmem {
     uint64_t ready_s;            // S_c operand written (compute -> issuer)
     uint64_t ready_bv[2];        // beta V operand written, per buffer
     uint64_t mma_s;              // chunk's state increment complete
-    uint64_t sb_read;            // S_c copied out of sb (state writer -> compute)
     uint32_t tmem;
+    volatile int32_t copied;     // S_c images copied out of sb (state writer -> compute)
     volatile int32_t issued;     // bulk copies issued (error path drains them)
     volatile int32_t abort_flag;
 };
@@ -895,7 +895,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
             mbar_init(&sm.ready_bv[0], 128);
             mbar_init(&sm.ready_bv[1], 128);
             mbar_init(&sm.mma_s, 1);
-            mbar_init(&sm.sb_read, 1);
+            sm.copied = 0;
             sm.issued = 0;
             sm.abort_flag = 0;
             fence_mbar_init();
@@ -1011,15 +1011,18 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                         sm.abort_flag = 1;
                         break;
                     }
+                    if (streamed && n >= 1) {
+                        // the copy of chunk n - 1 (issued a chunk ago) has landed;
+                        // published before the next copy starts, the release has
+                        // no copy in flight to wait for
+                        bulk_wait_group_all();
+                        publish(n - 1);
+                    }
                     bulk_s2g(state_img(n), sm.sb[n & 1], kStateImg);
                     bulk_commit_group();
                     bulk_wait_group_read<0>();
-                    mbar_arrive(&sm.sb_read);
                     copied = n + 1;
-                    if (streamed && n >= 1) {
-                        bulk_wait_group<1>();  // the copy of chunk n - 1 has landed
-                        publish(n - 1);
-                    }
+                    sm.copied = copied;
                 }
                 bulk_wait_group_all();  // state images written
                 if (streamed && copied > 0 && !sm.abort_flag) publish(copied - 1);
@@ -1093,11 +1096,17 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                 }
                 g = g_next;
                 if (more) {
-                    // sb[(n + 1) & 1] holds S_n-1; once the writer has copied S_n
-                    // out, it is long done with S_n-1 (waiting for the later copy
-                    // keeps the barrier's phases unambiguous)
-                    if (!mbar_wait_bounded(&sm.sb_read, (uint32_t)n & 1u, kWaitCycles))
-                        sm.abort_flag = 1;
+                    // sb[(n + 1) & 1] holds S_n-1: wait until the writer has copied
+                    // it out (issued a chunk ago: normally long done)
+                    if (sm.copied < n) {
+                        const long long t0 = clock64();
+                        while (sm.copied < n) {
+                            if (clock64() - t0 > kWaitCycles) {
+                                sm.abort_flag = 1;
+                                break;
+                            }
+                        }
+                    }
                     put_state(n + 1);
                 }
             }
