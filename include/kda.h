@@ -178,8 +178,11 @@ kdaStatus_t kda_chunk_fwd_ws(const void *q, const void *k, const void *v,
  * events recorded, i.e. launches + 1; stage i spans events[i] -> events[i+1].
  * The events must have been created by the caller (cudaEventCreate or an
  * already-recorded framework event).  Stage order: tensor-core engine =
- * chunk table, intra-chunk prep, state scan + output; SIMT engine = one
- * fused kernel.
+ * chunk table, intra-chunk prep, state scan, outputs; SIMT engine = one
+ * fused kernel.  With events recorded the tensor-core engine runs its
+ * kernels one after another (its default order runs the scan and the
+ * outputs beside the prep), so the stage times add up to more than the
+ * plain call takes.
  */
 kdaStatus_t kda_chunk_fwd_ws_timed(const void *q, const void *k, const void *v,
                                    const float *log_alpha, const float *beta, float scale,
@@ -188,6 +191,41 @@ kdaStatus_t kda_chunk_fwd_ws_timed(const void *q, const void *k, const void *v,
                                    void *workspace, size_t workspace_bytes,
                                    cudaStream_t stream, cudaEvent_t *events,
                                    int32_t max_events, int32_t *n_recorded);
+
+/*
+ * kda_chunk_fwd_host_scratch_size -- bytes of device scratch that
+ * kda_chunk_fwd_host needs for `shape`: device copies of every input and
+ * output plus the engine's workspace.  *bytes is written on success.
+ */
+kdaStatus_t kda_chunk_fwd_host_scratch_size(const kdaShape_t *shape, size_t *bytes);
+
+/*
+ * kda_chunk_fwd_host -- kda_chunk_fwd on HOST buffers: the same operation
+ * (chunkwise form, "Kimi Unveils Delta Attention and K3 Architecture
+ * Updates", sec. 6) with q, k, v, log_alpha, beta, initial_state, cu_seqlens,
+ * out and final_state (and, with KDA_PROLOGUE_GATE, shape->gate_bias and
+ * shape->gate_A_log) all in host memory, in the layouts kda_chunk_fwd
+ * documents.  On `stream` the call enqueues the host-to-device copies of the
+ * inputs, the prefill, and the device-to-host copies of out and final_state,
+ * then returns: the results are in the host buffers once the stream's work
+ * up to this point is done (cudaStreamSynchronize).  With page-locked host
+ * buffers (cudaHostAlloc / cudaHostRegister) the copies are asynchronous,
+ * so calls on two streams with two scratch buffers overlap one call's copies
+ * with the other's kernels; with pageable buffers the copies block the host.
+ *
+ * device_scratch: a device buffer of at least
+ * kda_chunk_fwd_host_scratch_size() bytes, 256-byte aligned, owned by this
+ * call until its work on `stream` is done.  The host buffers must stay valid
+ * (and out / final_state untouched) until then too.  Allocates nothing.
+ * Errors: as kda_chunk_fwd, plus KDA_ERR_INVALID_ARG for a missing, short or
+ * misaligned scratch buffer.
+ */
+kdaStatus_t kda_chunk_fwd_host(const void *q, const void *k, const void *v,
+                               const float *log_alpha, const float *beta, float scale,
+                               const float *initial_state, const int32_t *cu_seqlens,
+                               void *out, float *final_state, const kdaShape_t *shape,
+                               void *device_scratch, size_t scratch_bytes,
+                               cudaStream_t stream);
 
 /*
  * kda_chunk_fwd_static -- kda_chunk_fwd for callers that cannot allocate

@@ -12,6 +12,9 @@ The functions carry the C names:
 * ``kda_recurrent_fwd``  -- token-by-token over packed sequences, slot-indexed state pool;
 * ``kda_short_conv_fwd`` / ``kda_short_conv_step`` -- the layer's short causal convolution;
 * ``kda_chunk_fwd_workspace_size`` / ``kda_chunk_fwd_ws`` -- caller-owned scratch;
+* ``kda_chunk_fwd_host`` / ``kda_chunk_fwd_host_scratch_size`` -- prefill on host buffers
+  (copies in, prefill, copies out, all on one stream);
+* ``kda_recurrent_bwd`` -- gradients of the recurrence;
 * ``kda_status_string``, ``kda_device_status``.
 """
 from __future__ import annotations
@@ -94,6 +97,11 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                            ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32,
                                            ctypes.POINTER(ctypes.c_int32)]
     lib.kda_chunk_fwd_ws_timed.restype = ctypes.c_int
+    lib.kda_chunk_fwd_host_scratch_size.argtypes = [shp, ctypes.POINTER(ctypes.c_size_t)]
+    lib.kda_chunk_fwd_host_scratch_size.restype = ctypes.c_int
+    lib.kda_chunk_fwd_host.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, fp, ip, vp, fp, shp,
+                                       vp, ctypes.c_size_t, vp]
+    lib.kda_chunk_fwd_host.restype = ctypes.c_int
     lib.kda_chunk_fwd_workspace_size.argtypes = [shp, ctypes.POINTER(ctypes.c_size_t)]
     lib.kda_chunk_fwd_workspace_size.restype = ctypes.c_int
     lib.kda_recurrent_step.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, fp, vp, shp, vp]
@@ -167,13 +175,15 @@ def _dtype_code(t) -> int:
     raise TypeError(f"q/k/v must be bfloat16 or float32, got {t.dtype}")
 
 
-def _require(t, name, dtype=None, shape=None):
+def _require(t, name, dtype=None, shape=None, on_host=False):
     torch = _torch()
     if t is None:
         return
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if not t.is_cuda:
+    if on_host and t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not on_host and not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
@@ -193,17 +203,18 @@ def make_shape(N, T, H, dk, dv, dtype_code, chunk_size=0, engine=KDA_ENGINE_AUTO
                       int(prologue), gate_bias, gate_A_log)
 
 
-def _prologue(l2norm_qk, beta_logits, gate, HV, dk):
+def _prologue(l2norm_qk, beta_logits, gate, HV, dk, on_host=False):
     """(bits, bias pointer, A_log pointer) of the in-kernel input prologue;
-    gate = (bias [HV, d_k] fp32, A_log [HV] fp32) tensors on the device."""
+    gate = (bias [HV, d_k] fp32, A_log [HV] fp32) tensors on the device (on
+    the host for kda_chunk_fwd_host)."""
     torch = _torch()
     bits = (KDA_PROLOGUE_L2NORM_QK if l2norm_qk else 0) | (
         KDA_PROLOGUE_BETA_LOGITS if beta_logits else 0)
     if gate is None:
         return bits, None, None
     bias, a_log = gate
-    _require(bias, "gate bias", torch.float32, (HV, dk))
-    _require(a_log, "gate A_log", torch.float32, (HV,))
+    _require(bias, "gate bias", torch.float32, (HV, dk), on_host)
+    _require(a_log, "gate A_log", torch.float32, (HV,), on_host)
     return bits | KDA_PROLOGUE_GATE, bias.data_ptr(), a_log.data_ptr()
 
 
@@ -245,10 +256,11 @@ def _workspace(nbytes: int, device):
 
 
 def _prefill_args(q, k, v, log_alpha, beta, initial_state, cu_seqlens, out, final_state,
-                  chunk_size, engine, out_f32=False, prologue=None):
+                  chunk_size, engine, out_f32=False, prologue=None, on_host=False):
     torch = _torch()
+    _req = lambda t, name, dtype=None, shape=None: _require(t, name, dtype, shape, on_host)
     for name, t in (("q", q), ("k", k), ("v", v)):
-        _require(t, name)
+        _req(t, name)
     if q.dim() != 3:
         raise ValueError("q must be [T, H, d_k]")
     T, H, dk = q.shape
@@ -256,25 +268,27 @@ def _prefill_args(q, k, v, log_alpha, beta, initial_state, cu_seqlens, out, fina
     if v.dim() != 3:
         raise ValueError("v must be [T, HV, d_v]")
     HV, nvh = _value_heads(q, v)
-    _require(k, "k", q.dtype, (T, H, dk))
-    _require(v, "v", q.dtype, (T, HV, dv))
-    _require(log_alpha, "log_alpha", torch.float32, (T, HV, dk))
-    _require(beta, "beta", torch.float32, (T, HV))
+    _req(k, "k", q.dtype, (T, H, dk))
+    _req(v, "v", q.dtype, (T, HV, dv))
+    _req(log_alpha, "log_alpha", torch.float32, (T, HV, dk))
+    _req(beta, "beta", torch.float32, (T, HV))
     if cu_seqlens is not None:
-        _require(cu_seqlens, "cu_seqlens", torch.int32)
+        _req(cu_seqlens, "cu_seqlens", torch.int32)
         N = cu_seqlens.numel() - 1
     else:
         N = 1
-    _require(initial_state, "initial_state", torch.float32, (N, HV, dk, dv))
+    _req(initial_state, "initial_state", torch.float32, (N, HV, dk, dv))
     odt = _out_dtype(q, out, out_f32)
     if odt not in (q.dtype, torch.float32):
         raise TypeError("out must have the dtype of q, or float32")
     if out is None:
         out = torch.empty((T, HV, dv), dtype=odt, device=q.device)
-    _require(out, "out", odt, (T, HV, dv))
-    _require(final_state, "final_state", torch.float32, (N, HV, dk, dv))
+        if on_host:
+            out = out.pin_memory()
+    _req(out, "out", odt, (T, HV, dv))
+    _req(final_state, "final_state", torch.float32, (N, HV, dk, dv))
     eng = _ENGINES[engine] if isinstance(engine, str) else int(engine)
-    bits, gb, ga = _prologue(*(prologue or (False, False, None)), HV, dk)
+    bits, gb, ga = _prologue(*(prologue or (False, False, None)), HV, dk, on_host)
     shape = make_shape(N, T, H, dk, dv, _dtype_code(q), chunk_size, eng,
                        int(odt == torch.float32 and q.dtype != torch.float32), nvh, bits, gb, ga)
     return shape, out
@@ -340,6 +354,43 @@ def kda_chunk_fwd_ws_timed(q, k, v, log_alpha, beta, scale: float, initial_state
         ctypes.byref(shape), wp, nbytes, _stream_handle(stream), handles, len(events),
         ctypes.byref(n)), "kda_chunk_fwd_ws_timed")
     return out, final_state, int(n.value)
+
+
+def kda_chunk_fwd_host_scratch_size(shape: kdaShape_t) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().kda_chunk_fwd_host_scratch_size(ctypes.byref(shape), ctypes.byref(n)),
+           "kda_chunk_fwd_host_scratch_size")
+    return int(n.value)
+
+
+def kda_chunk_fwd_host(q, k, v, log_alpha, beta, scale: float, initial_state=None,
+                       cu_seqlens=None, out=None, final_state=None, *, scratch=None,
+                       chunk_size: int = 0, engine="auto", stream=None, out_f32: bool = False,
+                       l2norm_qk: bool = False, beta_logits: bool = False, gate=None):
+    """kda_chunk_fwd on host tensors (C: kda_chunk_fwd_host): every tensor is a
+    CPU tensor (page-locked for asynchronous copies), laid out as for
+    kda_chunk_fwd; ``gate`` tensors too.  The call enqueues the copies in,
+    the prefill and the copies out on ``stream`` and returns
+    ``(out, final_state)``, valid once that stream is synchronised.
+    ``scratch``: a uint8 CUDA tensor of at least
+    kda_chunk_fwd_host_scratch_size() bytes (plus 256 for alignment), owned
+    by the call until its work is done; one per stream for overlapping calls.
+    Without it, a cached per-device buffer serves (calls on one stream)."""
+    shape, out = _prefill_args(q, k, v, log_alpha, beta, initial_state, cu_seqlens, out,
+                               final_state, chunk_size, engine, out_f32,
+                               (l2norm_qk, beta_logits, gate), on_host=True)
+    torch = _torch()
+    nbytes = kda_chunk_fwd_host_scratch_size(shape)
+    if scratch is None:
+        scratch = _workspace(nbytes, torch.device("cuda", torch.cuda.current_device()))
+    if not scratch.is_cuda or scratch.numel() * scratch.element_size() < nbytes + 255:
+        raise ValueError(f"scratch must be a CUDA buffer of at least {nbytes + 256} bytes")
+    sp = (scratch.data_ptr() + 255) // 256 * 256
+    _check(load().kda_chunk_fwd_host(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), float(scale),
+        _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+        ctypes.byref(shape), sp, nbytes, _stream_handle(stream)), "kda_chunk_fwd_host")
+    return out, final_state
 
 
 def kda_chunk_fwd_ws(q, k, v, log_alpha, beta, scale: float, initial_state, cu_seqlens,

@@ -147,6 +147,57 @@ kdaStatus_t run_plan(Plan p, void *workspace, cudaStream_t stream, StageClock *c
     return cuda_status(launch_chunk_simt(p.args, stream));
 }
 
+// Device scratch of kda_chunk_fwd_host: the device copies of every input and
+// output, then the engine's workspace, each region 256-byte aligned.
+struct HostLayout {
+    size_t q, k, v, la, beta, cu, s0, out, sf, gb, ga, ws, total;       // offsets
+    size_t bq, bk, bv, bla, bbeta, bcu, bs, bout, bgb, bga;             // bytes
+};
+
+kdaStatus_t host_layout(const kdaShape_t *s, HostLayout *L) {
+    kdaStatus_t st = check_shape(s, false);
+    if (st != KDA_SUCCESS) return st;
+    size_t ws = 0;
+    st = kda_chunk_fwd_workspace_size(s, &ws);
+    if (st != KDA_SUCCESS) return st;
+    const size_t T = (size_t)s->total_tokens, H = (size_t)s->num_heads,
+                 HV = (size_t)value_heads(s), dk = (size_t)s->d_k, dv = (size_t)s->d_v,
+                 N = (size_t)s->num_seqs;
+    const size_t es = s->dtype == KDA_DTYPE_BF16 ? 2 : 4;
+    const size_t eo = (s->dtype == KDA_DTYPE_F32 || s->out_f32) ? 4 : 2;
+    const bool gate = (s->prologue & KDA_PROLOGUE_GATE) != 0;
+    L->bq = T * H * dk * es;
+    L->bk = L->bq;
+    L->bv = T * HV * dv * es;
+    L->bla = T * HV * dk * 4;
+    L->bbeta = T * HV * 4;
+    L->bcu = (N + 1) * 4;
+    L->bs = N * HV * dk * dv * 4;
+    L->bout = T * HV * dv * eo;
+    L->bgb = gate ? HV * dk * 4 : 0;
+    L->bga = gate ? HV * 4 : 0;
+    size_t off = 0;
+    auto take = [&](size_t n) {
+        const size_t o = off;
+        off += (n + 255) & ~size_t(255);
+        return o;
+    };
+    L->q = take(L->bq);
+    L->k = take(L->bk);
+    L->v = take(L->bv);
+    L->la = take(L->bla);
+    L->beta = take(L->bbeta);
+    L->cu = take(L->bcu);
+    L->s0 = take(L->bs);
+    L->out = take(L->bout);
+    L->sf = take(L->bs);
+    L->gb = take(L->bgb);
+    L->ga = take(L->bga);
+    L->ws = take(ws);
+    L->total = off;
+    return KDA_SUCCESS;
+}
+
 }  // namespace
 }  // namespace kda
 
@@ -234,6 +285,72 @@ kdaStatus_t kda_chunk_fwd(const void *q, const void *k, const void *v, const flo
         if (st == KDA_SUCCESS) st = KDA_ERR_CUDA;
     }
     return st;
+}
+
+kdaStatus_t kda_chunk_fwd_host_scratch_size(const kdaShape_t *shape, size_t *bytes) {
+    if (!bytes) return KDA_ERR_INVALID_ARG;
+    HostLayout L;
+    const kdaStatus_t st = host_layout(shape, &L);
+    if (st != KDA_SUCCESS) return st;
+    *bytes = L.total;
+    return KDA_SUCCESS;
+}
+
+kdaStatus_t kda_chunk_fwd_host(const void *q, const void *k, const void *v,
+                               const float *log_alpha, const float *beta, float scale,
+                               const float *initial_state, const int32_t *cu_seqlens,
+                               void *out, float *final_state, const kdaShape_t *shape,
+                               void *device_scratch, size_t scratch_bytes,
+                               cudaStream_t stream) {
+    HostLayout L;
+    kdaStatus_t st = host_layout(shape, &L);
+    if (st != KDA_SUCCESS) return st;
+    if (!device_scratch || scratch_bytes < L.total ||
+        (reinterpret_cast<uintptr_t>(device_scratch) & 255u) != 0)
+        return KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens && shape->num_seqs != 1) return KDA_ERR_INVALID_ARG;
+    const bool any = shape->total_tokens > 0;
+    if (any && (!q || !k || !v || !log_alpha || !beta || !out)) return KDA_ERR_INVALID_ARG;
+    const bool gate = (shape->prologue & KDA_PROLOGUE_GATE) != 0;
+    uint8_t *d = static_cast<uint8_t *>(device_scratch);
+    cudaError_t e = cudaSuccess;
+    auto h2d = [&](size_t off, const void *src, size_t n) {
+        if (e == cudaSuccess && src && n > 0)
+            e = cudaMemcpyAsync(d + off, src, n, cudaMemcpyHostToDevice, stream);
+    };
+    if (any) {
+        h2d(L.q, q, L.bq);
+        h2d(L.k, k, L.bk);
+        h2d(L.v, v, L.bv);
+        h2d(L.la, log_alpha, L.bla);
+        h2d(L.beta, beta, L.bbeta);
+    }
+    h2d(L.cu, cu_seqlens, L.bcu);
+    h2d(L.s0, initial_state, L.bs);
+    if (gate) {
+        h2d(L.gb, shape->gate_bias, L.bgb);
+        h2d(L.ga, shape->gate_A_log, L.bga);
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+    kdaShape_t ds = *shape;  // the gate parameters, from their device copies
+    if (gate) {
+        ds.gate_bias = reinterpret_cast<const float *>(d + L.gb);
+        ds.gate_A_log = reinterpret_cast<const float *>(d + L.ga);
+    }
+    Plan p;
+    st = plan_chunk(d + L.q, d + L.k, d + L.v, reinterpret_cast<const float *>(d + L.la),
+                    reinterpret_cast<const float *>(d + L.beta), scale,
+                    initial_state ? reinterpret_cast<const float *>(d + L.s0) : nullptr,
+                    cu_seqlens ? reinterpret_cast<const int32_t *>(d + L.cu) : nullptr,
+                    d + L.out, final_state ? reinterpret_cast<float *>(d + L.sf) : nullptr, &ds,
+                    &p);
+    if (st != KDA_SUCCESS) return st;
+    st = run_plan(p, d + L.ws, stream, nullptr);
+    if (st != KDA_SUCCESS) return st;
+    if (any) e = cudaMemcpyAsync(out, d + L.out, L.bout, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess && final_state)
+        e = cudaMemcpyAsync(final_state, d + L.sf, L.bs, cudaMemcpyDeviceToHost, stream);
+    return cuda_status(e);
 }
 
 kdaStatus_t kda_recurrent_step(const void *q, const void *k, const void *v,

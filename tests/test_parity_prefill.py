@@ -222,3 +222,37 @@ def test_launch_orders_agree(lengths, H):
         ref_o, ref_s = run_oracle(w)
         assert nerr(o1.cpu().numpy(), ref_o) < TOL_BF16
         assert nerr(fin[0].cpu().numpy(), ref_s) < TOL_BF16
+
+
+@pytest.mark.parametrize("lengths,H,out_f32", [([4096], 16, False), ([300, 129, 1], 2, True)])
+def test_host_buffers_match_device_entry(lengths, H, out_f32):
+    """kda_chunk_fwd_host (host tensors in and out, copies on the stream) gives
+    bit-identical results to kda_chunk_fwd on device copies of the same
+    inputs; two calls on two streams with two scratch buffers overlap and
+    still agree."""
+    import torch
+    import kimi_delta_attention_chunkwise_gb300 as kda
+    w = inputs.prefill(110, lengths, H=H, d=128, dtype="bf16", init_std=0.02)
+    d = to_device(w)
+    fin = torch.empty((w.N, w.H, 128, 128), dtype=torch.float32, device="cuda")
+    ref, _ = kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], w.scale,
+                               d["initial_state"], d["cu_seqlens"], None, fin, engine="tensor",
+                               out_f32=out_f32)
+    torch.cuda.synchronize()
+    pin = lambda x: x.cpu().pin_memory()
+    h = {key: (pin(val) if val is not None else None) for key, val in d.items()}
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    results = []
+    for s in streams:
+        hfin = torch.empty((w.N, w.H, 128, 128), dtype=torch.float32).pin_memory()
+        scratch = torch.empty(320 << 20, dtype=torch.uint8, device="cuda")
+        o, f = kda.kda_chunk_fwd_host(h["q"], h["k"], h["v"], h["log_alpha"], h["beta"],
+                                      w.scale, h["initial_state"], h["cu_seqlens"], None, hfin,
+                                      scratch=scratch, engine="tensor", stream=s,
+                                      out_f32=out_f32)
+        results.append((o, f, scratch))
+    torch.cuda.synchronize()
+    for o, f, _ in results:
+        assert o.device.type == "cpu" and f.device.type == "cpu"
+        torch.testing.assert_close(o, ref.cpu(), rtol=0, atol=0)
+        torch.testing.assert_close(f, fin.cpu(), rtol=0, atol=0)
