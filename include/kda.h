@@ -143,7 +143,15 @@ typedef enum {
  * offsets give wrong results but never an out-of-bounds access.
  * Scratch: up to kda_chunk_fwd_workspace_size() bytes, taken with
  * cudaMallocAsync/cudaFreeAsync on `stream` (stream-ordered, pooled by the
- * driver).  Use kda_chunk_fwd_ws to pass caller-owned scratch instead.
+ * driver).  Use kda_chunk_fwd_ws to pass caller-owned scratch instead. *
+ * Kernel overlap: when its serial scan needs at most half of the SMs, the
+ * tensor-core engine runs the scan and the output pass beside the
+ * chunk-parallel prep, handing work over through flags in its scratch (the
+ * results are bit-identical to running them one after another).  Tools that
+ * run kernels one at a time would leave the scan waiting out its ~1 s
+ * timeouts, so the engine runs its kernels in sequence when the environment
+ * sets CUDA_INJECTION64_PATH (how Nsight Compute and the compute sanitizer
+ * attach) or KDA_LAUNCH_ORDER=sequential.
  */
 kdaStatus_t kda_chunk_fwd(const void *q, const void *k, const void *v,
                           const float *log_alpha, const float *beta, float scale,

@@ -55,6 +55,7 @@
 // that evaluates every exp(G_i - G_j) directly, so any finite gates <= 0 work.
 #include <algorithm>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -249,9 +250,9 @@ constexpr uint32_t kOffAqk = 40960;                // A^qk (f16) inside a1
 constexpr uint32_t kOffKe = 49152;                 // K_end^T (f16) inside a1
 constexpr uint32_t kOffAkT = 8192;                 // A^kk^T after A^kk inside b1
 constexpr uint32_t kOffA2 = 16384;                 // (beta Gamma K)^T inside b1
-static_assert(kOffTb + 3 * 16 * 17 * 4 <= kOffAqk, "solve scratch below A^qk");
+static_assert(kOffTb + 32 * 33 * 4 <= kOffAqk, "solve scratch below A^qk");
 constexpr uint32_t kInBytes = 2 * C * D * 2 + C * D * 4;  // k, q bf16 + g f32 tiles
-static_assert(kOffTb + 3 * 16 * 17 * 4 <= 4 * 16384, "a1 reuse");
+static_assert(kOffTb + 32 * 33 * 4 <= 4 * 16384, "a1 reuse");
 static_assert(MID == HALF, "the reference token opens the second half");
 
 __device__ __forceinline__ void store_row_f16_image(uint8_t *img, uint32_t row,
@@ -282,48 +283,73 @@ __device__ __forceinline__ void store_quarter_f16_image(uint8_t *img, uint32_t r
     }
 }
 
-// One level of the blocked triangular inverse: for the block pairs (I, J)
-// with I - J = DIST, T_IJ = sum_{K=J}^{I-1} R_IK X_KJ, then X_IJ = -X_II T_IJ.
-// 2 x 2 output tiles per thread, NBLK x 64 tiles.
-template <int DIST>
-__device__ __forceinline__ void solve_blocks_below(float (*R)[C + 1], float (*X)[C + 1],
-                                                   float (*Tb)[16][17], int tid) {
-    constexpr int NBLK = 4 - DIST;
-    const int bi = tid >> 6, t = tid & 63, r0 = (t >> 3) * 2, c0 = (t & 7) * 2;
-    const int I = bi + DIST, J = bi;
-    if (tid < NBLK * 64) {
-        float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+// The inverse of a unit lower-triangular L = I + R, two levels up from its
+// 16 x 16 diagonal-block inverses.  For a split L = [A 0; B D] with A and D
+// square, L^-1 = [A^-1 0; -D^-1 B A^-1  D^-1].  Level 1 applies it inside the
+// two 32 x 32 diagonal blocks (16 x 16 halves), level 2 to the whole 64 x 64
+// (32 x 32 halves); B is the block of R below the diagonal.  The products run
+// over full K ranges: X is zero above its diagonal.  256 threads.
+__device__ __forceinline__ void solve_level16(float (*R)[C + 1], float (*X)[C + 1],
+                                              float (*Tb)[33], int tid) {
+    // thread -> 32 x 32 block p, one row of its lower-left 16 x 16, two columns
+    const int p = tid >> 7, t = tid & 127, o = 32 * p;
+    const int lr = t >> 3, lc = (t & 7) * 2;
+    const int r = o + 16 + lr, c = o + lc;
+    float a0 = 0.f, a1 = 0.f;  // (B A^-1)[r][c]
 #pragma unroll
-        for (int kk = 0; kk < 16 * DIST; ++kk) {
-            const float ra = R[I * 16 + r0][J * 16 + kk], rb = R[I * 16 + r0 + 1][J * 16 + kk];
-            const float xa = X[J * 16 + kk][J * 16 + c0], xb = X[J * 16 + kk][J * 16 + c0 + 1];
-            a00 = fmaf(ra, xa, a00);
-            a01 = fmaf(ra, xb, a01);
-            a10 = fmaf(rb, xa, a10);
-            a11 = fmaf(rb, xb, a11);
-        }
-        Tb[bi][r0][c0] = a00;
-        Tb[bi][r0][c0 + 1] = a01;
-        Tb[bi][r0 + 1][c0] = a10;
-        Tb[bi][r0 + 1][c0 + 1] = a11;
+    for (int k = 0; k < 16; ++k) {
+        const float rv = R[r][o + k];
+        a0 = fmaf(rv, X[o + k][c], a0);
+        a1 = fmaf(rv, X[o + k][c + 1], a1);
     }
+    Tb[16 * p + lr][lc] = a0;
+    Tb[16 * p + lr][lc + 1] = a1;
     __syncthreads();
-    if (tid < NBLK * 64) {
-        float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+    float b0 = 0.f, b1 = 0.f;  // (D^-1 B A^-1)[r][c]
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float xa = X[I * 16 + r0][I * 16 + m], xb = X[I * 16 + r0 + 1][I * 16 + m];
-            const float ta = Tb[bi][m][c0], tb = Tb[bi][m][c0 + 1];
-            a00 = fmaf(xa, ta, a00);
-            a01 = fmaf(xa, tb, a01);
-            a10 = fmaf(xb, ta, a10);
-            a11 = fmaf(xb, tb, a11);
-        }
-        X[I * 16 + r0][J * 16 + c0] = -a00;
-        X[I * 16 + r0][J * 16 + c0 + 1] = -a01;
-        X[I * 16 + r0 + 1][J * 16 + c0] = -a10;
-        X[I * 16 + r0 + 1][J * 16 + c0 + 1] = -a11;
+    for (int m = 0; m < 16; ++m) {
+        const float xv = X[r][o + 16 + m];
+        b0 = fmaf(xv, Tb[16 * p + m][lc], b0);
+        b1 = fmaf(xv, Tb[16 * p + m][lc + 1], b1);
     }
+    X[r][c] = -b0;
+    X[r][c + 1] = -b1;
+    __syncthreads();
+}
+
+__device__ __forceinline__ void solve_level32(float (*R)[C + 1], float (*X)[C + 1],
+                                              float (*Tb)[33], int tid) {
+    // thread -> 2 x 2 tile of the lower-left 32 x 32: rows 32 + rr.., columns cc..
+    const int rr = (tid >> 4) * 2, cc = (tid & 15) * 2, r = 32 + rr;
+    float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;  // B A^-1
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+        const float ra = R[r][k], rb = R[r + 1][k];
+        const float xa = X[k][cc], xb = X[k][cc + 1];
+        a00 = fmaf(ra, xa, a00);
+        a01 = fmaf(ra, xb, a01);
+        a10 = fmaf(rb, xa, a10);
+        a11 = fmaf(rb, xb, a11);
+    }
+    Tb[rr][cc] = a00;
+    Tb[rr][cc + 1] = a01;
+    Tb[rr + 1][cc] = a10;
+    Tb[rr + 1][cc + 1] = a11;
+    __syncthreads();
+    float b00 = 0.f, b01 = 0.f, b10 = 0.f, b11 = 0.f;  // D^-1 B A^-1
+#pragma unroll 8
+    for (int m = 0; m < 32; ++m) {
+        const float xa = X[r][32 + m], xb = X[r + 1][32 + m];
+        const float ta = Tb[m][cc], tb = Tb[m][cc + 1];
+        b00 = fmaf(xa, ta, b00);
+        b01 = fmaf(xa, tb, b01);
+        b10 = fmaf(xb, ta, b10);
+        b11 = fmaf(xb, tb, b11);
+    }
+    X[r][cc] = -b00;
+    X[r][cc + 1] = -b01;
+    X[r + 1][cc] = -b10;
+    X[r + 1][cc + 1] = -b11;
     __syncthreads();
 }
 
@@ -345,7 +371,7 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float(*R)[C + 1] = reinterpret_cast<float(*)[C + 1]>(sm.a1);
     float(*X)[C + 1] = reinterpret_cast<float(*)[C + 1]>(sm.a1 + kOffX);
-    float(*Tb)[16][17] = reinterpret_cast<float(*)[16][17]>(sm.a1 + kOffTb);
+    float(*Tb)[33] = reinterpret_cast<float(*)[33]>(sm.a1 + kOffTb);
     uint8_t *b2 = sm.b1;              // A^kk, f16 panel
     uint8_t *akt = sm.b1 + kOffAkT;   // A^kk^T, f16 panel
     uint8_t *a2 = sm.b1 + kOffA2;     // (beta Gamma K)^T, f16 panel
@@ -611,8 +637,8 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
 
     // sec. 6.3: A^kk = (I + R)^-1, unit lower triangular, fp32.  The 16 x 16
     // diagonal blocks by right-looking substitution (one column per thread),
-    // then the blocks below them, nearest first:
-    //   X_IJ = -X_II sum_{K=J}^{I-1} R_IK X_KJ
+    // then the 32 x 32 diagonal blocks and the whole from block inverses:
+    //   [A 0; B D]^-1 = [A^-1 0; -D^-1 B A^-1  D^-1]
     if (tid < C) {
         const int o = (tid >> 4) * 16, cc = tid & 15;
         float x[16], acc[16];
@@ -628,9 +654,8 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
         for (int r = 0; r < 16; ++r) X[o + r][o + cc] = x[r];
     }
     __syncthreads();
-    solve_blocks_below<1>(R, X, Tb, tid);
-    solve_blocks_below<2>(R, X, Tb, tid);
-    solve_blocks_below<3>(R, X, Tb, tid);
+    solve_level16(R, X, Tb, tid);
+    solve_level32(R, X, Tb, tid);
     // A^kk (rows i) and A^kk^T (rows j), f16
     if (tid < 2 * C) {
         const int row = tid >> 1, q4 = tid & 1;
@@ -1366,6 +1391,21 @@ bool encode_tile_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, s
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The concurrent order needs the scan, prep and output kernels to run side by
+// side.  Tools that run kernels one at a time (Nsight Compute, the compute
+// sanitizer: both inject themselves through CUDA_INJECTION64_PATH) would make
+// the scan wait out its flag timeouts, so under them, or with
+// KDA_LAUNCH_ORDER=sequential, the sequential order is used.
+bool concurrent_order_allowed() {
+    static const bool allowed = [] {
+        const char *order = std::getenv("KDA_LAUNCH_ORDER");
+        if (order && std::strcmp(order, "sequential") == 0) return false;
+        const char *inj = std::getenv("CUDA_INJECTION64_PATH");
+        return !(inj && inj[0] != '\0');
+    }();
+    return allowed;
+}
+
 cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspace_bytes,
                             cudaStream_t stream) {
     if (workspace_bytes < chunk_tc_workspace_bytes(a.N, a.T, a.H) || !workspace)
@@ -1395,8 +1435,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         sms = 0;
-    const bool streamed =
-        !timed && a.T > 0 && n_items <= kStreamMaxItems && sms > 0 && 2 * scan_ctas <= (size_t)sms;
+    const bool streamed = !timed && concurrent_order_allowed() && a.T > 0 &&
+                          n_items <= kStreamMaxItems && sms > 0 && 2 * scan_ctas <= (size_t)sms;
     // prep CTAs resident at once (two per SM on the SMs the scan leaves)
     const int32_t prefetch_dist = 2 * (sms - (streamed ? (int32_t)scan_ctas : 0));
     auto config = [&](dim3 grid, int threads, size_t smem, bool dependent) {
