@@ -408,8 +408,22 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
         tma_load_3d(sm.b1, &maps.k, 0, hq, t0, &sm.bar_in);
         tma_load_3d(sm.b1 + C * D * 2, &maps.q, 0, hq, t0, &sm.bar_in);
         tma_load_3d(sm.a1, &maps.g, 0, h, t0, &sm.bar_in);
+    }
+    if (warp == 0) {
+        tmem_alloc(&sm.tmem, 256);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    // beta: loaded now, stored once the tiles are in (its latency hides under theirs)
+    float beta_i = 0.f;
+    if (tid < C && tid < L) beta_i = beta[(size_t)(t0 + tid) * H + h];
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem;
+    if (tid == 32) {
         // The item that will take this CTA's place about one full wave of
-        // resident CTAs later: its tiles go to L2 now.
+        // resident CTAs later: its tiles go to L2 now (while this CTA waits
+        // for its own; off the path to the barrier above).
         const unsigned ahead = blockIdx.x + (unsigned)prefetch_dist;
         if (prefetch_dist > 0 && ahead < gridDim.x) {
             const int32_t ca = (int32_t)(ahead / (unsigned)H), ha = (int32_t)(ahead % (unsigned)H);
@@ -421,21 +435,12 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
             }
         }
     }
-    if (warp == 0) {
-        tmem_alloc(&sm.tmem, 256);
-        tmem_relinquish();
-        tc_fence_before();
-    }
-    if (tid < C) {
-        float b = tid < L ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
-        if (PRO && (pro & KDA_PROLOGUE_BETA_LOGITS) && tid < L) b = pro_sigmoid(b);
-        sm.beta[tid] = b;
-        gb[128 + tid] = b;
-    }
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = sm.tmem;
     bool ok = mbar_wait_bounded(&sm.bar_in, 0, kWaitCycles);
+    if (tid < C) {
+        if (PRO && (pro & KDA_PROLOGUE_BETA_LOGITS) && tid < L) beta_i = pro_sigmoid(beta_i);
+        sm.beta[tid] = beta_i;  // read after the next block barrier
+        gb[128 + tid] = beta_i;
+    }
 
     const int d = tid & (D - 1), hf = tid >> 7, i0 = hf * HALF;
     const bool l2 = PRO && (pro & KDA_PROLOGUE_L2NORM_QK);
@@ -744,6 +749,17 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
         }
         store_quarter_f16_image(sm.a1 + IMG_MN + chalf * 16384, d, 0, v0);
         store_quarter_f16_image(sm.a1 + IMG_MN + chalf * 16384, d, 4, v1);
+    }
+    // -M' (with Z, staged before) starts out while P' and Q' are staged
+    fence_proxy_async();
+    __syncthreads();
+    if (tid == 0) {
+        bulk_s2g(img, sm.a1, IMG_P - IMG_MN);
+        bulk_s2g(img + IMG_Z, zst, IMG_Q1 - IMG_Z);
+        bulk_commit_group();
+    }
+    if (ok) {
+        float v0[32];
         // P' row d, tokens 32*chalf..
         tmem_ld32(tmem_addr(tmem, quad * 32, 128 + chalf * 32), v0);
         store_quarter_f16_image(sm.a1 + IMG_P, d, chalf * 4, v0);
@@ -762,9 +778,8 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
     tc_fence_before();
     __syncthreads();
     if (tid == 0) {
-        // image out: [-M' | P' | Q' 0..63] in one piece, then Z and Q' 64..127
-        bulk_s2g(img, sm.a1, IMG_Z);
-        bulk_s2g(img + IMG_Z, zst, IMG_Q1 - IMG_Z);
+        // the rest of the image: [P' | Q' 0..63] in one piece, then Q' 64..127
+        bulk_s2g(img + IMG_P, sm.a1 + IMG_P, IMG_Z - IMG_P);
         bulk_s2g(img + IMG_Q1, sm.a1 + IMG_Z, IMG_GB - IMG_Q1);
         bulk_commit_group();
         if (streamed) {
