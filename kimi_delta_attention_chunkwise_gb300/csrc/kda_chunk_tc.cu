@@ -822,14 +822,15 @@ struct ScanSmem {
     uint64_t ready_s;            // S_c operand written (compute -> issuer)
     uint64_t ready_bv[2];        // beta V operand written, per buffer
     uint64_t mma_s;              // chunk's state increment complete
+    uint64_t ready_w[2];         // S_c operand written, for the writer of even / odd chunks
     uint32_t tmem;
-    volatile int32_t copied;     // S_c images copied out of sb (state writer -> compute)
+    volatile int32_t copied[2];  // S_c images copied out of sb, per writer (writer -> compute)
     volatile int32_t issued;     // bulk copies issued (error path drains them)
     volatile int32_t abort_flag;
 };
 
-// warps 0-3 compute, 4 streams operands in, 5 issues MMAs, 6 writes the S_c images out
-constexpr int kScanThreads = 224;
+// warps 0-3 compute, 4 streams operands in, 5 issues MMAs, 6-7 write the S_c images out
+constexpr int kScanThreads = 256;
 constexpr uint32_t kScanTmemCols = 128;  // D2 ping-pong (2 x BV)
 constexpr uint32_t kStateImg = D * 128;  // one value tile of S_c, f16 image
 
@@ -935,7 +936,10 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
             mbar_init(&sm.ready_bv[0], 128);
             mbar_init(&sm.ready_bv[1], 128);
             mbar_init(&sm.mma_s, 1);
-            sm.copied = 0;
+            mbar_init(&sm.ready_w[0], 128);
+            mbar_init(&sm.ready_w[1], 128);
+            sm.copied[0] = 0;
+            sm.copied[1] = 0;
             sm.issued = 0;
             sm.abort_flag = 0;
             fence_mbar_init();
@@ -1033,39 +1037,35 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                         sm.abort_flag = 1;
             }
             __syncwarp();
-        } else if (warp == 6) {
-            // -------- state writer: the S_c images out (streamed: and their flags,
-            // for the output pass), off the compute warps' chain --------
+        } else if (warp >= 6) {
+            // -------- state writers: the S_c images out (streamed: and their
+            // flags, for the output pass), off the compute warps' chain.  Two
+            // of them take the chunks in turn, so that each waits for its copy
+            // to land and publishes it with no other copy of its own in flight
+            // (a release waits for those) while the other copies the next.
+            const int b = warp - 6;
             if (lane == 0) {
-                auto publish = [&](int32_t n) {
-                    fence_proxy_async_global();
-                    flag_release(sc.ready + (size_t)sc_items +
-                                     ((size_t)(c_begin + n) * H + h) * NT + vt,
-                                 1u);
-                };
-                int32_t copied = 0;
-                for (int32_t n = 0; n < n_chunks; ++n) {
+                for (int32_t n = b; n < n_chunks; n += 2) {
                     // S_c in sb[n & 1], written and fenced by the compute warps
-                    if (!mbar_wait_bounded(&sm.ready_s, (uint32_t)n & 1u, kWaitCycles) ||
+                    if (!mbar_wait_bounded(&sm.ready_w[b], (uint32_t)(n >> 1) & 1u,
+                                           kWaitCycles) ||
                         sm.abort_flag) {
                         sm.abort_flag = 1;
                         break;
                     }
-                    if (streamed && n >= 1) {
-                        // the copy of chunk n - 1 (issued a chunk ago) has landed;
-                        // published before the next copy starts, the release has
-                        // no copy in flight to wait for
-                        bulk_wait_group_all();
-                        publish(n - 1);
-                    }
                     bulk_s2g(state_img(n), sm.sb[n & 1], kStateImg);
                     bulk_commit_group();
                     bulk_wait_group_read<0>();
-                    copied = n + 1;
-                    sm.copied = copied;
+                    sm.copied[b] = (n >> 1) + 1;
+                    if (streamed) {
+                        bulk_wait_group_all();
+                        fence_proxy_async_global();
+                        flag_release(sc.ready + (size_t)sc_items +
+                                         ((size_t)(c_begin + n) * H + h) * NT + vt,
+                                     1u);
+                    }
                 }
                 bulk_wait_group_all();  // state images written
-                if (streamed && copied > 0 && !sm.abort_flag) publish(copied - 1);
             }
             __syncwarp();
         } else {
@@ -1112,6 +1112,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                 if (compute_barrier_or(sm.abort_flag != 0)) break;
                 tc_fence_before();
                 mbar_arrive(&sm.ready_s);
+                mbar_arrive(&sm.ready_w[n & 1]);
                 const bool more = n + 1 < n_chunks;
                 float g_next = 0.f;
                 if (more) {
@@ -1136,14 +1137,18 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                 }
                 g = g_next;
                 if (more) {
-                    // sb[(n + 1) & 1] holds S_n-1: wait until the writer has copied
+                    // sb[(n + 1) & 1] holds S_n-1: wait until its writer has copied
                     // it out (issued a chunk ago: normally long done)
-                    if (sm.copied < n) {
-                        const long long t0 = clock64();
-                        while (sm.copied < n) {
-                            if (clock64() - t0 > kWaitCycles) {
-                                sm.abort_flag = 1;
-                                break;
+                    if (n >= 1) {
+                        const int wb = (n - 1) & 1;
+                        const int32_t need = ((n - 1) >> 1) + 1;
+                        if (sm.copied[wb] < need) {
+                            const long long t0 = clock64();
+                            while (sm.copied[wb] < need) {
+                                if (clock64() - t0 > kWaitCycles) {
+                                    sm.abort_flag = 1;
+                                    break;
+                                }
                             }
                         }
                     }
