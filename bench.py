@@ -46,6 +46,9 @@ def parse_args():
     ap.add_argument("--decode-steps", type=int, default=64)
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--preroll", type=float, default=0.3,
+                    help="seconds of back-to-back steps before each timed loop (0: none, "
+                         "for profiler runs)")
     return ap.parse_args()
 
 
@@ -251,11 +254,20 @@ def oracle_threads() -> int:
         return os.cpu_count() or 1
 
 
-def preroll(step, seconds: float = 0.3):
-    """Runs `step` back to back for about `seconds` so that the timed loop that
-    follows starts on a GPU in its loaded state: the first call after an idle
-    gap runs at about half speed while the clocks come back up."""
+PREROLL_SECONDS = 0.3
+
+
+def preroll(step, seconds: float = None):
+    """Runs `step` back to back for about `seconds` (default --preroll) so that
+    the timed loop that follows starts on a GPU in its loaded state: the first
+    call after an idle gap runs at about half speed while the clocks come
+    back up."""
     import torch
+    if seconds is None:
+        seconds = PREROLL_SECONDS
+    seconds = min(seconds, PREROLL_SECONDS)
+    if seconds <= 0:
+        return
     t0 = time.time()
     while time.time() - t0 < seconds:
         for _ in range(16):
@@ -765,7 +777,9 @@ def run_short_conv(args, dist, peaks, dev, stream):
 
 
 def main():
+    global PREROLL_SECONDS
     args = parse_args()
+    PREROLL_SECONDS = max(0.0, args.preroll)
     dist = Dist()
     try:
         if args.impl == "reference":
