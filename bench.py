@@ -206,6 +206,7 @@ PROFILE_FILES = {
     "out": "chunk_out_prefill_T4096_H16.md",
     "recurrent_step": "recurrent_step_decode_256x32_d128.md",
     "recurrent_fwd": "recurrent_fwd_decode_256x32x8_d128.md",
+    "short_conv_fwd": "short_conv_fwd_prefill_C12288_T4096.md",
 }
 
 
@@ -772,7 +773,7 @@ def run_short_conv(args, dist, peaks, dev, stream):
             "step_gbs": b_step / (res["step"] / 1e3) / 1e9, "gpu_launches": 2 * reps,
             "roofline": {"kernel": "short_conv_fwd", "bound": "hbm", "achieved": gbs,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
-                         "traffic": None, "bytes_per_launch": b_pre,
+                         "traffic": profiled_traffic("short_conv_fwd"), "bytes_per_launch": b_pre,
                          "peak_source": peaks["source"]}}
 
 
