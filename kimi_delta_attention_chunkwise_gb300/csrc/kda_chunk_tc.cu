@@ -1195,6 +1195,8 @@ struct OutSmem {
     uint8_t qz[OUT_IMG_BYTES];   // [filler ; Q'] panels and [filler ; Z]
     uint8_t sS[NT][kStateImg];   // S_c, one MN-major image per value tile
     uint8_t bv[NT][C * 128];     // beta V, per value tile
+    uint8_t vin[NT][C * 128];    // the chunk's value tiles (TMA, 128-byte swizzle)
+    float beta[C];
     uint64_t bar_in, bar_mma;
     uint32_t tmem;
 };
@@ -1202,7 +1204,7 @@ constexpr int kOutThreads = 128;
 
 template <typename TOut>
 __global__ void __launch_bounds__(kOutThreads)
-chunk_out_kernel(const __grid_constant__ CUtensorMap out_map, const __nv_bfloat16 *__restrict__ v,
+chunk_out_kernel(const __grid_constant__ CUtensorMap out_map, const __grid_constant__ CUtensorMap v_map,
                  const int32_t *__restrict__ cu, TOut *__restrict__ out, int32_t N, int32_t T,
                  int32_t H, Scratch sc, int32_t streamed, int64_t sc_items, int *status) {
     extern __shared__ uint8_t smem_raw[];
@@ -1233,35 +1235,39 @@ chunk_out_kernel(const __grid_constant__ CUtensorMap out_map, const __nv_bfloat1
         mbar_init(&sm.bar_in, 1);
         mbar_init(&sm.bar_mma, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(&sm.bar_in, OUT_IMG_BYTES + NT * kStateImg);
+        // Q'/Z, both S_c tiles, both value tiles and beta, all on one barrier
+        mbar_arrive_expect_tx(&sm.bar_in, OUT_IMG_BYTES + NT * kStateImg + NT * C * 128 +
+                                              C * (uint32_t)sizeof(float));
         bulk_g2s(sm.qz, img + OUT_IMG_OFF, OUT_IMG_BYTES, &sm.bar_in);
         bulk_g2s(sm.sS, sc.sst + ((size_t)c * H + h) * NT * kStateImg, NT * kStateImg,
                  &sm.bar_in);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) tma_load_3d(sm.vin[t], &v_map, t * BV, h, t0, &sm.bar_in);
+        bulk_g2s(sm.beta, img + IMG_GB + D * sizeof(float), C * sizeof(float), &sm.bar_in);
     }
-    if (streamed) __syncthreads();  // beta below comes from the image too
     if (warp == 0) {
         tmem_alloc(&sm.tmem, 128);
         tmem_relinquish();
     }
-    // beta V: thread -> token tid / 2, value half tid % 2 (= value tile)
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem;
+    bool ok = mbar_wait_bounded(&sm.bar_in, 0, kWaitCycles);
+    // beta V: thread -> token tid / 2, value tile tid % 2 (rows past the
+    // sequence, another sequence's tokens or zeros past T, get beta 0)
     {
         const int i = tid >> 1, half = tid & 1;
-        uint4 x[2][4];
-        float b = 0.f;
-        if (i < L) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(
-                v + ((size_t)(t0 + i) * H + h) * D + half * BV);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) x[j >> 2][j & 3] = __ldg(src + j);
-            b = __ldcg(reinterpret_cast<const float *>(img + IMG_GB) + 128 + i);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) x[j >> 2][j & 3] = make_uint4(0, 0, 0, 0);
-        }
+        const float b = i < L ? sm.beta[i] : 0.f;
 #pragma unroll
         for (int q4 = 0; q4 < 2; ++q4) {
+            uint4 x[4];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4)
+                x[c4] = *reinterpret_cast<const uint4 *>(sm.vin[half] +
+                                                         sw128_chunk(i, q4 * 4 + c4));
             float f[32];
-            scale_row32(x[q4], b, f);
+            scale_row32(x, b, f);
             store_row32_f16(sm.bv[half], i, q4 * 4, f);
         }
     }
@@ -1269,8 +1275,6 @@ chunk_out_kernel(const __grid_constant__ CUtensorMap out_map, const __nv_bfloat1
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = sm.tmem;
-    bool ok = mbar_wait_bounded(&sm.bar_in, 0, kWaitCycles);
     if (tid == 0 && ok) {
         constexpr uint32_t IDESC = idesc_f16_f32(128, BV) | (1u << 16);  // B MN-major
         tc_fence_after();
@@ -1562,14 +1566,13 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
         // a programmatic dependent of the scan (sequential) or of the prep
         // (streamed: its CTAs fill the SMs that the prep's last CTAs leave)
         const cudaLaunchConfig_t cfg = config(dim3((unsigned)n_items), kOutThreads, kOutSmem, true);
-        const __nv_bfloat16 *vb = static_cast<const __nv_bfloat16 *>(a.v);
         const int32_t *cu = static_cast<const int32_t *>(a.cu_seqlens);
         if (a.out_f32) {
-            e = cudaLaunchKernelEx(&cfg, out_kernel_f32, out_map, vb, cu,
+            e = cudaLaunchKernelEx(&cfg, out_kernel_f32, out_map, v_map, cu,
                                    static_cast<float *>(a.out), a.N, a.T, a.H, sc,
                                    (int32_t)streamed, (int64_t)n_items, a.status);
         } else {
-            e = cudaLaunchKernelEx(&cfg, out_kernel_bf16, out_map, vb, cu,
+            e = cudaLaunchKernelEx(&cfg, out_kernel_bf16, out_map, v_map, cu,
                                    static_cast<__nv_bfloat16 *>(a.out), a.N, a.T, a.H, sc,
                                    (int32_t)streamed, (int64_t)n_items, a.status);
         }
