@@ -451,8 +451,49 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
     float G[HALF];
     {
         const float *gs = reinterpret_cast<const float *>(sm.a1);
-        const unsigned short *ks = reinterpret_cast<const unsigned short *>(sm.b1);
-        const unsigned short *qs = ks + C * D;
+        unsigned short *ks = reinterpret_cast<unsigned short *>(sm.b1);
+        unsigned short *qs = ks + C * D;
+        // The L2 prologue, on the tiles in shared memory: warp w finds 1/|k_i| and
+        // 1/|q_i| of tokens 8w .. 8w + 7 and rescales their rows in place as fp16
+        // (11-bit significand: the tf32 and fp16 operands built from them keep
+        // their precision; bf16 here cost a visible share of the error budget).
+        // The stored inverse norms serve the CUDA-core path, which reads the
+        // raw rows from global memory.
+        if (l2) {
+#pragma unroll 1
+            for (int i = warp * 8; i < warp * 8 + 8; ++i) {
+                uint2 *kr = reinterpret_cast<uint2 *>(ks + i * D + lane * 4);
+                uint2 *qr = reinterpret_cast<uint2 *>(qs + i * D + lane * 4);
+                const uint2 kw = *kr, qw = *qr;
+                const uint32_t kv4[2] = {kw.x, kw.y}, qv4[2] = {qw.x, qw.y};
+                float kf[4], qf[4], kk = 0.f, qq = 0.f;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    kf[2 * e] = __uint_as_float(kv4[e] << 16);
+                    kf[2 * e + 1] = __uint_as_float(kv4[e] & 0xFFFF0000u);
+                    qf[2 * e] = __uint_as_float(qv4[e] << 16);
+                    qf[2 * e + 1] = __uint_as_float(qv4[e] & 0xFFFF0000u);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    kk = fmaf(kf[e], kf[e], kk);
+                    qq = fmaf(qf[e], qf[e], qq);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    kk += __shfl_xor_sync(0xffffffffu, kk, o);
+                    qq += __shfl_xor_sync(0xffffffffu, qq, o);
+                }
+                const float rk = rsqrtf(kk + kL2Eps), rq = rsqrtf(qq + kL2Eps);
+                *kr = make_uint2(pack_f16x2(kf[0] * rk, kf[1] * rk), pack_f16x2(kf[2] * rk, kf[3] * rk));
+                *qr = make_uint2(pack_f16x2(qf[0] * rq, qf[1] * rq), pack_f16x2(qf[2] * rq, qf[3] * rq));
+                if (lane == 0) {
+                    sm.knorm[i] = rk;
+                    sm.qnorm[i] = rq;
+                }
+            }
+            __syncthreads();
+        }
 #pragma unroll
         for (int jj = 0; jj < HALF / 2; ++jj) {
             const int ia = i0 + 2 * jj, ib = ia + 1;
@@ -468,32 +509,6 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
             if (gate && i0 + ii < L) lg = pro_gate(lg, sens, gbias_d);
             acc += lg;
             G[ii] = acc;
-        }
-        // the L2 prologue: warp w finds 1/|k_i| and 1/|q_i| of tokens 8w .. 8w + 7
-        if (l2) {
-#pragma unroll 1
-            for (int i = warp * 8; i < warp * 8 + 8; ++i) {
-                const uint2 kw = *reinterpret_cast<const uint2 *>(ks + i * D + lane * 4);
-                const uint2 qw = *reinterpret_cast<const uint2 *>(qs + i * D + lane * 4);
-                const uint32_t kv4[2] = {kw.x, kw.y}, qv4[2] = {qw.x, qw.y};
-                float kk = 0.f, qq = 0.f;
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float k0 = __uint_as_float(kv4[e] << 16), k1 = __uint_as_float(kv4[e] & 0xFFFF0000u);
-                    const float q0 = __uint_as_float(qv4[e] << 16), q1 = __uint_as_float(qv4[e] & 0xFFFF0000u);
-                    kk += k0 * k0 + k1 * k1;
-                    qq += q0 * q0 + q1 * q1;
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    kk += __shfl_xor_sync(0xffffffffu, kk, o);
-                    qq += __shfl_xor_sync(0xffffffffu, qq, o);
-                }
-                if (lane == 0) {
-                    sm.knorm[i] = rsqrtf(kk + kL2Eps);
-                    sm.qnorm[i] = rsqrtf(qq + kL2Eps);
-                }
-            }
         }
     }
     if (hf == 0) sm.gcarry[d] = G[HALF - 1];
@@ -511,16 +526,15 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
 #pragma unroll
     for (int ii = 0; ii < HALF; ++ii) span = fmaxf(span, fabsf(G[ii] - Gm));
     const int slow = __syncthreads_or(!(span <= kSpanLimit));
-    auto kval = [&](int ii) {
-        const float x =
-            __uint_as_float((ii & 1) ? (kp[ii >> 1] & 0xFFFF0000u) : (kp[ii >> 1] << 16));
-        return l2 ? x * sm.knorm[i0 + ii] : x;
+    // k and q of this thread's tokens: bf16 inputs, or fp16 once the L2
+    // prologue has normalised them
+    auto unpack = [&](uint32_t w, int hi) {
+        if (l2)
+            return __half2float(__ushort_as_half((unsigned short)(hi ? (w >> 16) : (w & 0xFFFFu))));
+        return __uint_as_float(hi ? (w & 0xFFFF0000u) : (w << 16));
     };
-    auto qval = [&](int ii) {
-        const float x =
-            __uint_as_float((ii & 1) ? (qp[ii >> 1] & 0xFFFF0000u) : (qp[ii >> 1] << 16));
-        return l2 ? x * sm.qnorm[i0 + ii] : x;
-    };
+    auto kval = [&](int ii) { return unpack(kp[ii >> 1], ii & 1); };
+    auto qval = [&](int ii) { return unpack(qp[ii >> 1], ii & 1); };
     uint32_t mma_phase = 0;
 
     if (slow) {
