@@ -321,12 +321,23 @@ recurrent_fwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
             load_rows<ROWS>(&s_k[i][row0], rk);
             load_rows<ROWS>(&s_q[i][row0], rq);
             float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
+            {
+                // packed pairs: the same IEEE operations, half the instructions
+                float2 k01 = make_float2(0.f, 0.f), k23 = k01, q01 = k01, q23 = k01;
 #pragma unroll
-            for (int r = 0; r < ROWS; ++r) {
-                const float a = ra[r], kr = rk[r], qr = rq[r];
-                s[r].x *= a; s[r].y *= a; s[r].z *= a; s[r].w *= a;
-                pk.x += s[r].x * kr; pk.y += s[r].y * kr; pk.z += s[r].z * kr; pk.w += s[r].w * kr;
-                pq.x += s[r].x * qr; pq.y += s[r].y * qr; pq.z += s[r].z * qr; pq.w += s[r].w * qr;
+                for (int r = 0; r < ROWS; ++r) {
+                    const float2 a2 = make_float2(ra[r], ra[r]), k2 = make_float2(rk[r], rk[r]),
+                                 q2 = make_float2(rq[r], rq[r]);
+                    const float2 s01 = f2_mul(make_float2(s[r].x, s[r].y), a2);
+                    const float2 s23 = f2_mul(make_float2(s[r].z, s[r].w), a2);
+                    s[r] = make_float4(s01.x, s01.y, s23.x, s23.y);
+                    k01 = f2_fma(s01, k2, k01);
+                    k23 = f2_fma(s23, k2, k23);
+                    q01 = f2_fma(s01, q2, q01);
+                    q23 = f2_fma(s23, q2, q23);
+                }
+                pk = make_float4(k01.x, k01.y, k23.x, k23.y);
+                pq = make_float4(q01.x, q01.y, q23.x, q23.y);
             }
 #pragma unroll
             for (int o = CG; o < 32; o <<= 1) {
@@ -353,10 +364,13 @@ recurrent_fwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
             __syncthreads();
             // S_t = S_bar + k e^T
             const float4 e4 = reinterpret_cast<const float4 *>(s_e[b])[cg];
+            const float2 e01 = make_float2(e4.x, e4.y), e23 = make_float2(e4.z, e4.w);
 #pragma unroll
             for (int r = 0; r < ROWS; ++r) {
-                const float kr = rk[r];
-                s[r].x += kr * e4.x; s[r].y += kr * e4.y; s[r].z += kr * e4.z; s[r].w += kr * e4.w;
+                const float2 k2 = make_float2(rk[r], rk[r]);
+                const float2 s01 = f2_fma(k2, e01, make_float2(s[r].x, s[r].y));
+                const float2 s23 = f2_fma(k2, e23, make_float2(s[r].z, s[r].w));
+                s[r] = make_float4(s01.x, s01.y, s23.x, s23.y);
             }
         }
     }

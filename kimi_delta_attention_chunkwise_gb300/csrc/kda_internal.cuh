@@ -94,6 +94,27 @@ cudaError_t launch_recurrent_bwd(const BwdArgs &a, cudaStream_t stream);
 
 // The fused input prologue, as each kernel applies it to one element.
 constexpr float kL2Eps = 1e-6f;
+// Packed fp32 pairs (sm_100 and later): one instruction for two IEEE fp32
+// multiplies or fused multiply-adds, bit-identical to the scalar forms.
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 __device__ __forceinline__ float pro_sigmoid(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 // gate logit g of channel j of a head with sensitivity exp(A_log) = sens and
 // bias b[j] -> log retention -5 sigmoid(sens (g + b[j]))
