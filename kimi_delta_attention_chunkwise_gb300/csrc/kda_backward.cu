@@ -13,12 +13,18 @@
 //
 // where Sb = Diag(a) S_prev, p = Sb^T k, e = b (v - p).
 //
-// One CTA per (sequence, head) keeps the fp32 state (and then its gradient)
-// in registers, thread = 4 columns x ROWS consecutive rows.  A forward sweep
+// The state's value columns evolve independently (e_j needs only column j),
+// so one CTA per (sequence, head, DC-wide column tile) keeps its tile of the
+// fp32 state (and then of its gradient) in registers, thread = 4 columns x
+// ROWS consecutive rows.  The gradients that sum over columns (dq, dk,
+// dlog_alpha, dbeta) leave as per-tile partial sums that a second kernel
+// adds up; with one tile per head they are written directly.  A forward sweep
 // writes the state entering every CK-token chunk to scratch (checkpoints);
 // the reverse sweep, chunk by chunk from the end, reloads the checkpoint,
 // recomputes the chunk forward -- storing the state before each token and
-// the chunk's p and e -- and then walks its tokens backwards.
+// the chunk's p and e -- and then walks its tokens backwards.  The serial
+// walk is latency-bound, so small problems are split into 16-column tiles
+// for more CTAs with less work each.
 #include <cstdint>
 #include <cuda_bf16.h>
 
@@ -39,15 +45,16 @@ __device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16 *p) {
     return __bfloat162float(*p);
 }
 
-template <int D>
+template <int D, int DC>
 struct BwdCfg {
-    static constexpr int CG = D / 4;
+    static constexpr int NTILE = D / DC;  // column tiles per head
+    static constexpr int CG = DC / 4;     // float4 column groups of a tile
     static constexpr int THREADS = (CG * D < 256) ? CG * D : 256;
     static constexpr int RG = THREADS / CG;
     static constexpr int ROWS = D / RG;
     static constexpr int RG_PER_WARP = (CG < 32) ? 32 / CG : 1;
     static constexpr int SLOTS = RG / RG_PER_WARP;
-    static_assert(RG * ROWS == D, "row split");
+    static_assert(RG * ROWS == D && NTILE * DC == D && DC <= 128, "row and column split");
 };
 
 // sum over the CG lanes that share this thread's rows (xor within aligned groups)
@@ -58,8 +65,10 @@ __device__ __forceinline__ float row_sum(float x) {
     return x;
 }
 
-template <typename TIn, int D>
-__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
+// dq, dk, dlog_alpha ([tiles][T, H, D]) and dbeta ([tiles][T, H]) are the
+// per-tile sums over the tile's columns (the final gradients when NTILE = 1).
+template <typename TIn, int D, int DC>
+__global__ void __launch_bounds__(BwdCfg<D, DC>::THREADS, 1)
 recurrent_bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
                      const TIn *__restrict__ v, const float *__restrict__ log_alpha,
                      const float *__restrict__ beta, float scale,
@@ -69,31 +78,41 @@ recurrent_bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
                      float *__restrict__ dlog_alpha, float *__restrict__ dbeta,
                      float *__restrict__ d_initial, float *__restrict__ ckpt,
                      float *__restrict__ cstates, int32_t T, int32_t H) {
-    using Cfg = BwdCfg<D>;
+    using Cfg = BwdCfg<D, DC>;
     constexpr int CG = Cfg::CG, RG_PER_WARP = Cfg::RG_PER_WARP, SLOTS = Cfg::SLOTS;
-    constexpr int ROWS = Cfg::ROWS, THREADS = Cfg::THREADS;
-    __shared__ __align__(16) float s_k[CK][D], s_q[CK][D], s_v[CK][D], s_a[CK][D], s_do[CK][D];
-    __shared__ __align__(16) float s_p[CK][D], s_e[CK][D];
-    __shared__ __align__(16) float s_red[SLOTS][D];
-    __shared__ __align__(16) float s_dp[D];
-    __shared__ float s_prod[D];
+    constexpr int ROWS = Cfg::ROWS, THREADS = Cfg::THREADS, NTILE = Cfg::NTILE;
+    __shared__ __align__(16) float s_k[CK][D], s_q[CK][D], s_a[CK][D];   // per row
+    __shared__ __align__(16) float s_v[CK][DC], s_do[CK][DC];           // per column of the tile
+    __shared__ __align__(16) float s_p[CK][DC], s_e[CK][DC];
+    __shared__ __align__(16) float s_red[SLOTS][DC];
+    __shared__ __align__(16) float s_dp[DC];
+    __shared__ float s_prod[DC];
     __shared__ float s_b[CK];
 
     const int tid = threadIdx.x, lane = tid & 31;
     const int cg = tid % CG, rg = tid / CG, row0 = rg * ROWS;
-    const int32_t seq = blockIdx.x / H, h = blockIdx.x % H;
+    const int32_t head_item = blockIdx.x / NTILE, ct = blockIdx.x % NTILE, col0 = ct * DC;
+    const int32_t seq = head_item / H, h = head_item % H;
+    const size_t tile_out = (size_t)ct * T * H;  // partial-sum tile offset, in (t, h) rows
     int32_t ta = 0, tb = T;
     if (cu) {
         ta = min(max(cu[seq], 0), T);
         tb = min(max(cu[seq + 1], ta), T);
     }
     const int32_t L = tb - ta, nch = (L + CK - 1) / CK;
-    const size_t sdd = (size_t)D * D;
-    // checkpoint slot of chunk j: floor(ta / CK) + seq + j is unique across sequences
-    auto ck_slot = [&](int32_t j) { return ckpt + ((size_t)(ta / CK + seq + j) * H + h) * sdd; };
-    float *my_states = cstates + (size_t)blockIdx.x * CK * sdd;
-    auto tile = [&](float *base, int r) {  // this thread's float4 of row r
-        return reinterpret_cast<float4 *>(base + (size_t)(row0 + r) * D) + cg;
+    const size_t sdd = (size_t)D * D, stile = (size_t)D * DC;
+    // checkpoint slot of chunk j: floor(ta / CK) + seq + j is unique across
+    // sequences; each column tile keeps its own D x DC part
+    auto ck_slot = [&](int32_t j) {
+        return ckpt + (((size_t)(ta / CK + seq + j) * H + h) * NTILE + ct) * stile;
+    };
+    float *my_states = cstates + (size_t)blockIdx.x * CK * stile;
+    // this thread's float4 of row r: in a full D x D state, or in a tile buffer
+    auto tile = [&](float *base, int r) {
+        return reinterpret_cast<float4 *>(base + (size_t)(row0 + r) * D + col0) + cg;
+    };
+    auto tbuf = [&](float *base, int r) {
+        return reinterpret_cast<float4 *>(base + (size_t)(row0 + r) * DC) + cg;
     };
 
     // stage chunk j's per-token vectors (t0c .. t0c + nt)
@@ -102,12 +121,14 @@ recurrent_bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
             const int i = idx / D, c = idx % D;
             const size_t o = ((size_t)(t0c + i) * H + h) * D + c;
             s_k[i][c] = ldf(k + o);
-            s_v[i][c] = ldf(v + o);
             s_a[i][c] = __expf(log_alpha[o]);
-            if (with_q_do) {
-                s_q[i][c] = ldf(q + o);
-                s_do[i][c] = d_out ? ldf(d_out + o) : 0.f;
-            }
+            if (with_q_do) s_q[i][c] = ldf(q + o);
+        }
+        for (int idx = tid; idx < nt * DC; idx += THREADS) {
+            const int i = idx / DC, c = idx % DC;
+            const size_t o = ((size_t)(t0c + i) * H + h) * D + col0 + c;
+            s_v[i][c] = ldf(v + o);
+            if (with_q_do) s_do[i][c] = d_out ? ldf(d_out + o) : 0.f;
         }
         if (tid < nt) s_b[tid] = beta[(size_t)(t0c + tid) * H + h];
     };
@@ -128,7 +149,7 @@ recurrent_bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
         if ((tid % 32) < CG || CG >= 32)
             reinterpret_cast<float4 *>(s_red[rg / RG_PER_WARP])[cg] = pk;
         __syncthreads();
-        if (tid < D) {
+        if (tid < DC) {
             float p = 0.f;
 #pragma unroll
             for (int w = 0; w < SLOTS; ++w) p += s_red[w][tid];
@@ -155,7 +176,7 @@ recurrent_bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
         const int32_t t0c = ta + j * CK;
         const int nt = min(CK, tb - t0c);
 #pragma unroll
-        for (int r = 0; r < ROWS; ++r) *tile(ck_slot(j), r) = s[r];
+        for (int r = 0; r < ROWS; ++r) *tbuf(ck_slot(j), r) = s[r];
         __syncthreads();  // the previous chunk's vectors are no longer read
         stage(t0c, nt, false);
         __syncthreads();
@@ -172,14 +193,14 @@ recurrent_bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
         const int32_t t0c = ta + j * CK;
         const int nt = min(CK, tb - t0c);
 #pragma unroll
-        for (int r = 0; r < ROWS; ++r) s[r] = *tile(ck_slot(j), r);
+        for (int r = 0; r < ROWS; ++r) s[r] = *tbuf(ck_slot(j), r);
         __syncthreads();
         stage(t0c, nt, true);
         __syncthreads();
         // recompute the chunk forward, keeping the state before every token
         for (int i = 0; i < nt; ++i) {
 #pragma unroll
-            for (int r = 0; r < ROWS; ++r) *tile(my_states + (size_t)i * sdd, r) = s[r];
+            for (int r = 0; r < ROWS; ++r) *tbuf(my_states + (size_t)i * stile, r) = s[r];
             forward_token(s, i, true);
         }
         // and walk it backwards
@@ -191,7 +212,7 @@ recurrent_bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
             float dq_r[ROWS], dka_r[ROWS];
 #pragma unroll
             for (int r = 0; r < ROWS; ++r) {
-                const float4 sp = *tile(my_states + (size_t)i * sdd, r);  // S_prev
+                const float4 sp = *tbuf(my_states + (size_t)i * stile, r);  // S_prev
                 s[r] = sp;
                 const int row = row0 + r;
                 const float a = s_a[i][row], kr = s_k[i][row], qr = scale * s_q[i][row];
@@ -212,12 +233,12 @@ recurrent_bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
             if ((tid % 32) < CG || CG >= 32)
                 reinterpret_cast<float4 *>(s_red[rg / RG_PER_WARP])[cg] = de;
             __syncthreads();
-            if (tid < D) {
+            if (tid < DC) {
                 float dev = 0.f;
 #pragma unroll
                 for (int w = 0; w < SLOTS; ++w) dev += s_red[w][tid];
                 const float bt = s_b[i];
-                const size_t o = ((size_t)t * H + h) * D + tid;
+                const size_t o = ((size_t)t * H + h) * D + col0 + tid;
                 dv[o] = bt * dev;
                 s_dp[tid] = -bt * dev;
                 s_prod[tid] = dev * (s_v[i][tid] - s_p[i][tid]);
@@ -225,10 +246,10 @@ recurrent_bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
             __syncthreads();
             if (tid < 32) {
                 float acc = 0.f;
-                for (int c = tid; c < D; c += 32) acc += s_prod[c];
+                for (int c = tid; c < DC; c += 32) acc += s_prod[c];
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                if (tid == 0) dbeta[(size_t)t * H + h] = acc;
+                if (tid == 0) dbeta[tile_out + (size_t)t * H + h] = acc;
             }
             const float4 dp4 = reinterpret_cast<const float4 *>(s_dp)[cg];
 #pragma unroll
@@ -245,7 +266,7 @@ recurrent_bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
                 const float k_sum = row_sum<CG>(dka_r[r] + dkb);
                 const float a_sum = row_sum<CG>(da);
                 if (cg == 0) {
-                    const size_t o = ((size_t)t * H + h) * D + row;
+                    const size_t o = (tile_out + (size_t)t * H + h) * D + row;
                     dq[o] = scale * q_sum;
                     dk[o] = k_sum;
                     dlog_alpha[o] = a * a_sum;
@@ -261,19 +282,91 @@ recurrent_bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
     }
 }
 
-template <typename TIn, int D>
-cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
+// dq, dk, dlog_alpha and dbeta from their per-tile partial sums.  Scalar
+// accesses: the outputs need only 4-byte alignment.
+__global__ void __launch_bounds__(256) bwd_tile_sum_kernel(const float *__restrict__ part,
+                                                           float *__restrict__ dq,
+                                                           float *__restrict__ dk,
+                                                           float *__restrict__ dla,
+                                                           float *__restrict__ db, size_t n_row,
+                                                           size_t n_tok, int ntile) {
+    // part: [3][ntile][n_row] (dq, dk, dlog_alpha), then [ntile][n_tok] (dbeta)
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    float *outs[3] = {dq, dk, dla};
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_row; i += stride) {
+#pragma unroll
+        for (int g = 0; g < 3; ++g) {
+            const float *src = part + (size_t)g * ntile * n_row + i;
+            float acc = src[0];
+            for (int t = 1; t < ntile; ++t) acc += src[(size_t)t * n_row];
+            outs[g][i] = acc;
+        }
+    }
+    const float *pb = part + (size_t)3 * ntile * n_row;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_tok; i += stride) {
+        float acc = pb[i];
+        for (int t = 1; t < ntile; ++t) acc += pb[(size_t)t * n_tok + i];
+        db[i] = acc;
+    }
+}
+
+int sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return sms;
+}
+
+// Column tile width: 16 when the (sequence, head) pairs alone leave most SMs
+// idle (fewer than two CTAs per SM), else the whole state width.
+int32_t bwd_tile_cols(int32_t N, int32_t H, int32_t D) {
+    const int sms = sm_count();
+    if (D >= 32 && sms > 0 && (int64_t)N * H < 2 * (int64_t)sms) return 16;
+    return D;
+}
+
+size_t partial_bytes(int32_t N, int32_t T, int32_t H, int32_t D) {
+    const int32_t dc = bwd_tile_cols(N, H, D);
+    if (dc == D) return 0;
+    const size_t ntile = (size_t)(D / dc), rows = (size_t)T * H;
+    return (3 * ntile * rows * D + ntile * rows) * sizeof(float);
+}
+
+template <typename TIn, int D, int DC>
+cudaError_t launch_bwd_tile(const BwdArgs &a, cudaStream_t stream) {
+    using Cfg = BwdCfg<D, DC>;
     const int64_t NH = (int64_t)a.N * a.H;
-    if (NH == 0) return cudaSuccess;
     float *ckpt = static_cast<float *>(a.workspace);
     float *cstates = reinterpret_cast<float *>(static_cast<uint8_t *>(a.workspace) +
                                                ckpt_bytes(a.N, a.T, a.H, D));
-    recurrent_bwd_kernel<TIn, D><<<(unsigned)NH, BwdCfg<D>::THREADS, 0, stream>>>(
+    float *part = cstates + (size_t)a.N * a.H * CK * (size_t)D * D;
+    const size_t n_row = (size_t)a.T * a.H * D, n_tok = (size_t)a.T * a.H;
+    const bool direct = Cfg::NTILE == 1;
+    float *pq = direct ? a.dq : part;
+    float *pk = direct ? a.dk : part + (size_t)Cfg::NTILE * n_row;
+    float *pa = direct ? a.dlog_alpha : part + (size_t)2 * Cfg::NTILE * n_row;
+    float *pb = direct ? a.dbeta : part + (size_t)3 * Cfg::NTILE * n_row;
+    recurrent_bwd_kernel<TIn, D, DC><<<(unsigned)(NH * Cfg::NTILE), Cfg::THREADS, 0, stream>>>(
         static_cast<const TIn *>(a.q), static_cast<const TIn *>(a.k),
         static_cast<const TIn *>(a.v), a.log_alpha, a.beta, a.scale, a.initial_state,
-        a.cu_seqlens, static_cast<const TIn *>(a.d_out), a.d_final_state, a.dq, a.dk, a.dv,
-        a.dlog_alpha, a.dbeta, a.d_initial_state, ckpt, cstates, a.T, a.H);
+        a.cu_seqlens, static_cast<const TIn *>(a.d_out), a.d_final_state, pq, pk, a.dv, pa, pb,
+        a.d_initial_state, ckpt, cstates, a.T, a.H);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || direct || a.T == 0) return e;
+    const int sms = sm_count();
+    bwd_tile_sum_kernel<<<(unsigned)(sms > 0 ? 4 * sms : 608), 256, 0, stream>>>(
+        part, a.dq, a.dk, a.dlog_alpha, a.dbeta, n_row, n_tok, Cfg::NTILE);
     return cudaGetLastError();
+}
+
+template <typename TIn, int D>
+cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
+    if ((int64_t)a.N * a.H == 0) return cudaSuccess;
+    if constexpr (D >= 32) {
+        if (bwd_tile_cols(a.N, a.H, D) == 16) return launch_bwd_tile<TIn, D, 16>(a, stream);
+    }
+    return launch_bwd_tile<TIn, D, D>(a, stream);
 }
 
 template <typename TIn>
@@ -297,7 +390,8 @@ size_t ckpt_bytes(int32_t N, int32_t T, int32_t H, int32_t D) {
 }  // namespace
 
 size_t recurrent_bwd_workspace_bytes(int32_t N, int32_t T, int32_t H, int32_t D) {
-    return ckpt_bytes(N, T, H, D) + (size_t)N * H * CK * (size_t)D * D * sizeof(float);
+    return ckpt_bytes(N, T, H, D) + (size_t)N * H * CK * (size_t)D * D * sizeof(float) +
+           partial_bytes(N, T, H, D);
 }
 
 cudaError_t launch_recurrent_bwd(const BwdArgs &a, cudaStream_t stream) {

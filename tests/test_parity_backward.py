@@ -73,3 +73,9 @@ def test_without_states():
 
 def test_long_sequence():
     _check(_case(1200, [300], 2, 128, "bf16"), "bf16")
+
+
+def test_many_heads_whole_state_tiles():
+    """Enough (sequence, head) pairs that each CTA keeps the whole state width
+    (small problems split the columns into 16-wide tiles and sum partials)."""
+    _check(_case(1300, [3, 0, 9] * 14, 8, 128, "f32"), "f32")
