@@ -9,8 +9,8 @@
 // with inputs before the sequence's first token taken from its cache (slot
 // W - 1 the most recent) or zero.
 //
-// Memory-bound elementwise work: a thread owns VEC consecutive channels (one
-// 16-byte vector) for a block of TB tokens; it issues all of the block's rows
+// Memory-bound elementwise work: a thread owns 4 consecutive channels (one
+// 16-byte fp32 or 8-byte bf16 vector) for a block of TB tokens; it issues all of the block's rows
 // and the W - 1 before them as independent loads first, then filters from
 // registers, so every input row is read once per block (plus the halo) and
 // every output written once, fully coalesced along channels.
@@ -40,31 +40,33 @@ struct Vec<float> {
         *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
     }
 };
+// bf16: 4 channels (8 bytes) per thread, so that the block's rows, the taps
+// and the sums fit in few registers and more warps keep loads in flight
 template <>
 struct Vec<__nv_bfloat16> {
-    static constexpr int N = 8;
-    using Raw = uint4;
+    static constexpr int N = 4;
+    using Raw = uint2;
     __device__ static Raw load_raw(const __nv_bfloat16 *p) {
-        return *reinterpret_cast<const uint4 *>(p);
+        return *reinterpret_cast<const uint2 *>(p);
     }
-    __device__ static Raw zero_raw() { return make_uint4(0, 0, 0, 0); }
-    __device__ static void unpack(const Raw &x, float (&v)[8]) {
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    __device__ static Raw zero_raw() { return make_uint2(0, 0); }
+    __device__ static void unpack(const Raw &x, float (&v)[4]) {
+        const uint32_t w[2] = {x.x, x.y};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 2; ++i) {
             v[2 * i] = __uint_as_float(w[i] << 16);
             v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
         }
     }
-    __device__ static void store(__nv_bfloat16 *p, const float (&v)[8]) {
-        uint4 x;
+    __device__ static void store(__nv_bfloat16 *p, const float (&v)[4]) {
+        uint2 x;
         uint32_t *w = &x.x;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 2; ++i) {
             const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
             w[i] = *reinterpret_cast<const uint32_t *>(&h);
         }
-        *reinterpret_cast<uint4 *>(p) = x;
+        *reinterpret_cast<uint2 *>(p) = x;
     }
 };
 
