@@ -207,6 +207,7 @@ PROFILE_FILES = {
     "recurrent_step": "recurrent_step_decode_256x32_d128.md",
     "recurrent_fwd": "recurrent_fwd_decode_256x32x8_d128.md",
     "short_conv_fwd": "short_conv_fwd_prefill_C12288_T4096.md",
+    "recurrent_bwd": "recurrent_bwd_prefill_T4096_H16.md",
 }
 
 
@@ -501,7 +502,7 @@ def run_ours(args, dist: Dist):
 
     # ---------------- decode rows ----------------
     variants = run_prefill_variants(args, dist, dev, stream, w, (q, k, v, la, beta, cu))
-    backward = run_backward(args, dist, dev, stream, w, (q, k, v, la, beta, cu))
+    backward = run_backward(args, dist, peaks, dev, stream, w, (q, k, v, la, beta, cu))
     decode = recurrent = conv = None
     if not args.skip_decode:
         decode = run_decode(args, dist, peaks, dev, stream)
@@ -683,7 +684,7 @@ def run_prefill_variants(args, dist, dev, stream, w, dev_inputs):
     return res
 
 
-def run_backward(args, dist, dev, stream, w, dev_inputs):
+def run_backward(args, dist, peaks, dev, stream, w, dev_inputs):
     """Gradients of the head-group prefill workload (1 sequence x 16 heads x
     4,096 tokens): the recurrent backward with output and final-state
     gradients, timed like the headline."""
@@ -710,9 +711,19 @@ def run_backward(args, dist, dev, stream, w, dev_inputs):
     evs[1].record(stream)
     torch.cuda.synchronize()
     ms = dist.max(evs[0].elapsed_time(evs[1])) / reps
+    # compulsory bytes: q, k, v, d_out (bf16), log_alpha, beta in; dq, dk, dv,
+    # dlog_alpha (fp32), dbeta out; the final-state gradient in
+    bytes_call = (4 * 2 * d + 4 * d + 4 + 4 * 4 * d + 4) * T * H + H * d * d * 4
+    gbs = bytes_call / (ms / 1e3) / 1e9
     return {"workload": f"gradients of the headline workload (1 x {H} heads x {T} tokens, d={d}, "
                         "bf16 in, fp32 gradients), recurrent form with 8-token checkpoints",
-            "value": T * dist.world / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms}
+            "value": T * dist.world / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+            "roofline": {"kernel": "recurrent_bwd", "bound": "hbm", "achieved": gbs,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"],
+                         "traffic": profiled_traffic("recurrent_bwd"),
+                         "bytes_per_launch": bytes_call, "peak_source": peaks["source"],
+                         "note": "the per-token walk is latency-bound (barriers), not HBM-bound"}}
 
 
 def run_short_conv(args, dist, peaks, dev, stream):
