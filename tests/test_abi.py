@@ -195,3 +195,51 @@ def test_recurrent_bwd_support(lib):
     pro = kda.make_shape(1, 64, 2, 128, 128, kda.KDA_DTYPE_BF16, prologue=kda.KDA_PROLOGUE_BETA_LOGITS)
     assert bwd(pro) == kda.KDA_ERR_UNSUPPORTED
     assert bwd(kda.make_shape(2, 64, 2, 128, 128, kda.KDA_DTYPE_BF16)) == kda.KDA_ERR_INVALID_ARG
+
+
+def _align256(n):
+    return (n + 255) // 256 * 256
+
+
+def test_host_scratch_size_is_copies_plus_workspace(lib):
+    """kda_chunk_fwd_host's scratch: a device copy of every input and output
+    (each 256-byte aligned), then the engine's workspace."""
+    T, H, d, N = 4096, 16, 128, 1
+    s = _shape(T=T, H=H)
+    ws, host = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(s), ctypes.byref(ws)) == kda.KDA_SUCCESS
+    assert lib.kda_chunk_fwd_host_scratch_size(ctypes.byref(s), ctypes.byref(host)) == kda.KDA_SUCCESS
+    tok = T * H * d
+    regions = [2 * tok, 2 * tok, 2 * tok,        # q, k, v (bf16)
+               4 * tok, 4 * T * H,               # log_alpha, beta
+               4 * (N + 1),                      # cu_seqlens
+               4 * N * H * d * d,                # initial state
+               2 * tok,                          # out (bf16)
+               4 * N * H * d * d]                # final state
+    assert host.value == sum(_align256(r) for r in regions) + _align256(ws.value)
+    assert lib.kda_chunk_fwd_host_scratch_size(None, ctypes.byref(host)) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_chunk_fwd_host_scratch_size(ctypes.byref(s), None) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_host_entry_rejects_bad_arguments(lib):
+    """Every check runs on the host before any copy is enqueued."""
+    s = _shape(T=4096, H=16)
+    need = ctypes.c_size_t(0)
+    assert lib.kda_chunk_fwd_host_scratch_size(ctypes.byref(s), ctypes.byref(need)) == 0
+
+    def call(shape, scratch=FAKE, nbytes=None, **ptrs):
+        p = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, b=FAKE, out=FAKE, cu=None)
+        p.update(ptrs)
+        return lib.kda_chunk_fwd_host(
+            p["q"], p["k"], p["v"], p["g"], p["b"], ctypes.c_float(1.0), None, p["cu"],
+            p["out"], None, ctypes.byref(shape) if shape is not None else None, scratch,
+            need.value if nbytes is None else nbytes, None)
+
+    assert call(None) == kda.KDA_ERR_INVALID_ARG
+    assert call(s, scratch=None) == kda.KDA_ERR_INVALID_ARG
+    assert call(s, nbytes=need.value - 256) == kda.KDA_ERR_INVALID_ARG
+    assert call(s, scratch=FAKE + 16) == kda.KDA_ERR_INVALID_ARG    # not 256-byte aligned
+    assert call(s, q=None) == kda.KDA_ERR_INVALID_ARG
+    assert call(s, out=None) == kda.KDA_ERR_INVALID_ARG
+    assert call(_shape(N=3, T=4096, H=16)) == kda.KDA_ERR_INVALID_ARG   # N > 1 needs cu_seqlens
+    assert call(_shape(dk=96, dv=96)) == kda.KDA_ERR_UNSUPPORTED
