@@ -115,3 +115,54 @@ def test_recurrent_fwd_and_step_with_groups():
     torch.cuda.synchronize()
     assert nerr(o.cpu().numpy(), ro) <= TOL_F32
     assert nerr(st.cpu().numpy(), rst) <= TOL_F32
+
+
+@pytest.mark.parametrize("G", [1, 2])
+def test_launch_orders_agree_with_prologue_and_groups(G):
+    """With the prologue (all three parts) and value-head groups, the
+    tensor engine's concurrent and sequential launch orders (the latter forced
+    by recording per-kernel events) give bit-identical results."""
+    import torch
+    import kimi_delta_attention_chunkwise_gb300 as kda
+    r = _raw(960 + G, [700, 1, 300, 64], 2, 128, "bf16", G=G)
+    args = (_to(r["q"], torch.bfloat16), _to(r["k"], torch.bfloat16), _to(r["v"], torch.bfloat16),
+            _to(r["g"]), _to(r["beta"]), r["scale"], _to(r["s0"]), _to(r["cu"]))
+    kw = dict(engine="tensor", out_f32=True, l2norm_qk=True, beta_logits=True,
+              gate=(_to(r["bias"]), _to(r["a_log"])))
+    f1 = torch.empty(r["s0"].shape, device="cuda")
+    o1, _ = kda.kda_chunk_fwd(*args, None, f1, **kw)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    for e in ev:
+        e.record()
+    o2 = torch.empty_like(o1)
+    f2 = torch.empty_like(f1)
+    kda.kda_chunk_fwd_ws_timed(*args, o2, f2, ev, **kw)
+    torch.cuda.synchronize()
+    torch.testing.assert_close(o1, o2, rtol=0, atol=0)
+    torch.testing.assert_close(f1, f2, rtol=0, atol=0)
+    ref_o, ref_s = _oracle(r)
+    assert nerr(o1.cpu().numpy(), ref_o) <= TOL_BF16
+    assert nerr(f1.cpu().numpy(), ref_s) <= TOL_BF16
+
+
+def test_host_entry_with_prologue():
+    """kda_chunk_fwd_host with host-side gate parameters equals the device entry."""
+    import torch
+    import kimi_delta_attention_chunkwise_gb300 as kda
+    r = _raw(970, [150, 64, 1, 90], 2, 128, "bf16")
+    dev = (_to(r["q"], torch.bfloat16), _to(r["k"], torch.bfloat16), _to(r["v"], torch.bfloat16),
+           _to(r["g"]), _to(r["beta"]), r["scale"], _to(r["s0"]), _to(r["cu"]))
+    kw = dict(engine="tensor", out_f32=True, l2norm_qk=True, beta_logits=True)
+    f1 = torch.empty(r["s0"].shape, device="cuda")
+    o1, _ = kda.kda_chunk_fwd(*dev, None, f1, gate=(_to(r["bias"]), _to(r["a_log"])), **kw)
+    torch.cuda.synchronize()
+    h = lambda x, dt=None: torch.from_numpy(np.ascontiguousarray(x)).to(dt).pin_memory() \
+        if dt is not None else torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    hf = torch.empty(r["s0"].shape).pin_memory()
+    o2, _ = kda.kda_chunk_fwd_host(h(r["q"], torch.bfloat16), h(r["k"], torch.bfloat16),
+                                   h(r["v"], torch.bfloat16), h(r["g"]), h(r["beta"]), r["scale"],
+                                   h(r["s0"]), h(r["cu"]), None, hf,
+                                   gate=(h(r["bias"]), h(r["a_log"])), **kw)
+    torch.cuda.synchronize()
+    torch.testing.assert_close(o2, o1.cpu(), rtol=0, atol=0)
+    torch.testing.assert_close(hf, f1.cpu(), rtol=0, atol=0)
