@@ -16,8 +16,9 @@
  * piece of Gated DeltaNet" (key-by-value orientation, o_t = S_t^T q_t).
  *
  * Memory contract shared by every entry point:
- *   - All tensor arguments are DEVICE pointers, contiguous and row-major in
- *     the layouts given below.  q, k, v, out and the states must be 16-byte
+ *   - All tensor arguments are DEVICE pointers (HOST pointers for
+ *     kda_chunk_fwd_host), contiguous and row-major in the layouts given
+ *     below.  q, k, v, out and the states must be 16-byte
  *     aligned; log_alpha, beta and cu_seqlens 4-byte aligned.  The caller
  *     owns every buffer.
  *   - Calls are asynchronous with respect to the host; all work is enqueued
@@ -87,7 +88,9 @@ typedef struct {
  * normalization and query scaling"), applied by every kernel as it loads its
  * inputs, so the raw projections cross HBM once:
  *   KDA_PROLOGUE_L2NORM_QK   q and k are L2-normalised per head,
- *                            x / sqrt(sum x^2 + 1e-6)
+ *                            x / sqrt(sum x^2 + 1e-6) (the tensor-core
+ *                            engine rounds the normalised rows to fp16,
+ *                            the precision of its operands)
  *   KDA_PROLOGUE_BETA_LOGITS beta holds logits: beta = sigmoid(beta)
  *   KDA_PROLOGUE_GATE        log_alpha holds the gate projection g:
  *                            log_alpha = -5 sigmoid(exp(A_log[h]) (g + b[h, j]))
