@@ -160,6 +160,7 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t *cu, in
     __shared__ int32_t warp_sum[32];
     __shared__ int32_t carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_launch_dependents();  // the next kernel waits for this one's results
     for (size_t i = (size_t)blockIdx.x * 1024 + tid; i < n_ready; i += (size_t)gridDim.x * 1024)
         ready[i] = 0u;
     if (blockIdx.x != 0) return;
@@ -916,8 +917,11 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
     ScanSmem &sm = *reinterpret_cast<ScanSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // the next kernel (the output pass; streamed: the prep) may start once
-    // every scan CTA runs
+    // Streamed: a programmatic dependent of the chunk table, resident while
+    // the table runs; it waits for the table before anything reads it, and
+    // only then lets the prep (which reads it too, and must not wait on this
+    // kernel) start.  Sequential: the output pass may start setting up.
+    if (streamed) pdl_wait_primaries();
     pdl_launch_dependents();
     const int32_t seq = blockIdx.x / NT, vt = blockIdx.x % NT, h = blockIdx.y;
     int32_t ta, tb;
@@ -1456,8 +1460,9 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
     // plain.
     //
     // Streamed order, when the scan's CTAs take at most half of the SMs:
-    // table -> scan -> prep (programmatic dependent of the scan, so it starts
-    // once every scan CTA is resident) -> output (programmatic dependent of
+    // table -> scan (programmatic dependent of the table: it waits for the
+    // table, then triggers) -> prep (programmatic dependent of the scan, so it
+    // starts once every scan CTA is resident and the table is done) -> output (programmatic dependent of
     // the prep, so it starts once every prep CTA has started).  The scan
     // follows the prep chunk by chunk through the image flags, so its serial
     // chain runs under the prep's parallel work instead of after it; the
@@ -1540,7 +1545,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
                                   a.status);
     };
     if (streamed) {
-        e = launch_scan(false);
+        e = launch_scan(true);
         if (e != cudaSuccess) return e;
     }
 
