@@ -154,7 +154,12 @@ typedef enum {
  * run kernels one at a time would leave the scan waiting out its ~1 s
  * timeouts, so the engine runs its kernels in sequence when the environment
  * sets CUDA_INJECTION64_PATH (how Nsight Compute and the compute sanitizer
- * attach) or KDA_LAUNCH_ORDER=sequential.
+ * attach) or KDA_LAUNCH_ORDER=sequential.  The same applies to work that
+ * runs beside a call on other streams: calls whose scans together occupy
+ * every SM (or other kernels that do) leave the prep no SM, and the scan
+ * gives up after ~1 s with KDA_ERR_TIMEOUT in the device status word; set
+ * KDA_LAUNCH_ORDER=sequential for such workloads.  Two or three concurrent
+ * calls of the headline's size (32 scan CTAs each) are fine.
  */
 kdaStatus_t kda_chunk_fwd(const void *q, const void *k, const void *v,
                           const float *log_alpha, const float *beta, float scale,
