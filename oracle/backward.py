@@ -87,3 +87,127 @@ def recurrent_backward(q, k, v, log_alpha, beta, scale, initial_state=None, cu_s
                 dS = a[:, None] * dSb
             gS0[s, h] = dS
     return gq, gk, gv, gg, gb, gS0
+
+
+def chunk_backward(q, k, v, log_alpha, beta, scale, initial_state=None, cu_seqlens=None,
+                   d_out=None, d_final_state=None, chunk_size=64):
+    """The same gradients, through the chunkwise form ("Kimi Unveils Delta
+    Attention and K3 Architecture Updates", sec. 6): the blueprint of a
+    chunk-parallel backward.  Per chunk (tokens i, j of the chunk; G the
+    chunk-local cumulative log decay, G_l its last row; D_ij = exp(G_i - G_j)
+    per key channel), the forward of sec. 6 is
+
+        R    = tril_-1( Diag(b) [k_i . (D_ij * k_j)] )      A  = (I + R)^-1
+        Aqk  = tril_0( s [q_i . (D_ij * k_j)] )
+        W    = A Diag(b) (exp(G) * K),   U = A Diag(b) V,    E = U - W S0
+        O    = (s exp(G) * Q) S0 + Aqk E
+        S1   = Diag(exp(G_l)) S0 + K_end^T E,  K_end = exp(G_l - G) * K
+
+    and its reverse-mode derivative, with dO and dS1 given (dS1 of a chunk is
+    dS0 of the next; at the end of a sequence, the final-state gradient):
+
+        dE   = Aqk^T dO + K_end dS1
+        dS0  = (s exp(G) * Q)^T dO + Diag(exp(G_l)) dS1 - W^T dE
+        dAqk = tril_0(dO E^T),   dK_end = E dS1^T,   dU = dE,   dW = -dE S0^T
+        dA   = dU (Diag(b) V)^T + dW (Diag(b) exp(G) * K)^T
+        dR   = tril_-1(-A^T dA A^T)                       (A = (I + R)^-1)
+
+    then through the products above to q, k, v, b and G, and dlog_alpha as
+    the reverse cumulative sum of dG within the chunk.  fp64, one head of one
+    chunk at a time (no blocking beyond the chunks).  Returns the tuple of
+    ``recurrent_backward``.
+    """
+    f = lambda x: np.asarray(x, dtype=np.float64)
+    q, k, v, g, b = f(q), f(k), f(v), f(log_alpha), f(beta)
+    T, H, dk_ = q.shape
+    dv_ = v.shape[-1]
+    cu = np.array([0, T]) if cu_seqlens is None else np.asarray(cu_seqlens, dtype=np.int64)
+    N = len(cu) - 1
+    S0all = np.zeros((N, H, dk_, dv_)) if initial_state is None else f(initial_state)
+    dO = np.zeros((T, H, dv_)) if d_out is None else f(d_out)
+    dSf = np.zeros((N, H, dk_, dv_)) if d_final_state is None else f(d_final_state)
+    gq, gk, gv, gg = (np.zeros_like(x) for x in (q, k, v, g))
+    gb = np.zeros_like(b)
+    gS0 = np.zeros_like(S0all)
+    for s in range(N):
+        t0, t1 = int(cu[s]), int(cu[s + 1])
+        starts = list(range(t0, t1, chunk_size))
+        for h in range(H):
+            # forward over the chunks: the state entering each, and each
+            # chunk's intermediates
+            S = S0all[s, h].copy()
+            fwd = []
+            for c0 in starts:
+                c1 = min(c0 + chunk_size, t1)
+                K, Q, V = k[c0:c1, h], q[c0:c1, h], v[c0:c1, h]
+                B = b[c0:c1, h]
+                L = c1 - c0
+                G = np.cumsum(g[c0:c1, h], axis=0)
+                Gl = G[-1]
+                Dx = np.exp(G[:, None, :] - G[None, :, :])           # [i, j, channel]
+                low = np.tril(np.ones((L, L)), -1)
+                low0 = np.tril(np.ones((L, L)))
+                KK = np.einsum("ic,jc,ijc->ij", K, K, Dx)
+                QK = np.einsum("ic,jc,ijc->ij", Q, K, Dx)
+                R = low * (B[:, None] * KK)
+                A = np.linalg.inv(np.eye(L) + R)
+                Aqk = low0 * (scale * QK)
+                KG = np.exp(G) * K
+                W = A @ (B[:, None] * KG)
+                U = A @ (B[:, None] * V)
+                E = U - W @ S
+                QG = scale * np.exp(G) * Q
+                Kend = np.exp(Gl - G) * K
+                fwd.append(dict(c0=c0, c1=c1, K=K, Q=Q, V=V, B=B, G=G, Gl=Gl, Dx=Dx, low=low,
+                                low0=low0, KK=KK, QK=QK, A=A, Aqk=Aqk, KG=KG, W=W, E=E, QG=QG,
+                                Kend=Kend, S0=S.copy()))
+                S = np.exp(Gl)[:, None] * S + Kend.T @ E
+            # reverse over the chunks
+            dS1 = dSf[s, h].copy()
+            for ch in reversed(fwd):
+                c0, c1 = ch["c0"], ch["c1"]
+                K, Q, V, B, G, Gl, Dx = ch["K"], ch["Q"], ch["V"], ch["B"], ch["G"], ch["Gl"], ch["Dx"]
+                A, Aqk, KG, W, E, QG, Kend, S0 = (ch[x] for x in ("A", "Aqk", "KG", "W", "E",
+                                                                   "QG", "Kend", "S0"))
+                dOc = dO[c0:c1, h]
+                dE = Aqk.T @ dOc + Kend @ dS1
+                dQG = dOc @ S0.T
+                dS0 = QG.T @ dOc + np.exp(Gl)[:, None] * dS1 - W.T @ dE
+                dAqk = ch["low0"] * (dOc @ E.T)
+                dKend = E @ dS1.T
+                dGl = np.exp(Gl) * np.sum(S0 * dS1, axis=1)
+                dU, dW = dE, -dE @ S0.T
+                BV, BK = B[:, None] * V, B[:, None] * KG
+                dA = dU @ BV.T + dW @ BK.T
+                dBV, dBK = A.T @ dU, A.T @ dW
+                dV = B[:, None] * dBV
+                dB = np.sum(V * dBV, axis=1) + np.sum(KG * dBK, axis=1)
+                dKG = B[:, None] * dBK
+                dR = ch["low"] * (-(A.T @ dA @ A.T))
+                # R_ij = b_i sum_c k_ic k_jc D_ijc
+                dB += np.sum(dR * ch["KK"], axis=1)
+                wR = (B[:, None] * dR)[:, :, None] * Dx                 # [i, j, c]
+                dK = np.einsum("ijc,jc->ic", wR, K) + np.einsum("ijc,ic->jc", wR, K)
+                tR = wR * K[:, None, :] * K[None, :, :]
+                dG = tR.sum(axis=1) - tR.sum(axis=0)
+                # Aqk_ij = s sum_c q_ic k_jc D_ijc
+                wQ = (scale * dAqk)[:, :, None] * Dx
+                dQ = np.einsum("ijc,jc->ic", wQ, K)
+                dK += np.einsum("ijc,ic->jc", wQ, Q)
+                tQ = wQ * Q[:, None, :] * K[None, :, :]
+                dG += tQ.sum(axis=1) - tQ.sum(axis=0)
+                # the elementwise exp(G) factors
+                dK += np.exp(G) * dKG
+                dG += KG * dKG
+                dQ += scale * np.exp(G) * dQG
+                dG += QG * dQG
+                dK += np.exp(Gl - G) * dKend
+                dG -= Kend * dKend
+                dGl += np.sum(Kend * dKend, axis=0)
+                dG[-1] += dGl
+                # G = cumsum(log_alpha): dlog_alpha_t = sum_{i >= t} dG_i
+                gg[c0:c1, h] = np.cumsum(dG[::-1], axis=0)[::-1]
+                gq[c0:c1, h], gk[c0:c1, h], gv[c0:c1, h], gb[c0:c1, h] = dQ, dK, dV, dB
+                dS1 = dS0
+            gS0[s, h] = dS1
+    return gq, gk, gv, gg, gb, gS0

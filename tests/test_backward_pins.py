@@ -64,3 +64,42 @@ def test_read_gradient_closed_form():
     np.testing.assert_allclose(dq[:, 0], s * dO[:, 0] @ S0[0, 0].T, rtol=1e-13)
     np.testing.assert_allclose(dS0[0, 0], s * q[:, 0].T @ dO[:, 0], rtol=1e-13)
     assert not dvv.any()
+
+
+@pytest.mark.parametrize("chunk_size", [1, 3, 16, 64])
+def test_chunkwise_backward_equals_recurrent(chunk_size):
+    """The chunkwise backward (sec. 6's chunk form differentiated, the
+    blueprint of a chunk-parallel backward) gives the recurrent backward's
+    gradients to rounding, for any chunk size, across packed sequences with
+    empty and one-token ones, partial last chunks and strong decays."""
+    from oracle.backward import chunk_backward
+    P = _problem(20, [37, 0, 1, 70, 16], H=2, dk=8, dv=8)
+    P["g"][40:50] -= 6.0   # near-total forgetting inside a chunk
+    args = (P["q"], P["k"], P["v"], P["g"], P["b"], P["s"], P["S0"], P["cu"], P["R"], P["Q"])
+    ref = recurrent_backward(*args)
+    got = chunk_backward(*args, chunk_size=chunk_size)
+    for name, x, r in zip(("dq", "dk", "dv", "dlog_alpha", "dbeta", "d_initial"), got, ref):
+        np.testing.assert_allclose(x, r, rtol=0, atol=1e-11 * max(np.abs(r).max(), 1.0),
+                                   err_msg=name)
+
+
+def test_chunkwise_backward_finite_differences():
+    """An independent check of the chunk form on its own: central finite
+    differences of the C forward oracle for log_alpha and beta (the inputs
+    that reach the most factors of the chunk form)."""
+    from oracle.backward import chunk_backward
+    P = _problem(21, [6, 5], H=1, dk=3, dv=2)
+    grads = chunk_backward(P["q"], P["k"], P["v"], P["g"], P["b"], P["s"], P["S0"], P["cu"],
+                           P["R"], P["Q"], chunk_size=4)
+    for name, gi in (("g", 3), ("b", 4)):
+        x = P[name]
+        eps = 1e-6
+        fd = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            fd[idx] = (_loss(P, **{name: xp}) - _loss(P, **{name: xm})) / (2 * eps)
+        np.testing.assert_allclose(grads[gi], fd, rtol=1e-6, atol=1e-8, err_msg=name)
