@@ -7,12 +7,17 @@ seeded synthetic inputs), i.e. every prefill stage of the hot path.  The
 decode row (``kda_recurrent_step``, 256 sequences x 32 heads, 512 MiB fp32
 state, 64 steps) is measured in the same run and reported under "decode".
 
-Timing: CUDA events on the launch stream, W untimed warm-up steps, K timed
-steps with an L2 flush (256 MiB write) before each timed step (the prefill
-inputs, ~100 MB, would otherwise stay in the 129 MB L2), barrier and
-synchronize on both sides, max over ranks.  libkda itself records events
-between its kernels (kda_chunk_fwd_ws_timed), which gives the per-kernel
-device times behind the roofline figures.
+Timing: CUDA events on the launch stream, W untimed warm-up steps, about
+0.3 s of back-to-back steps (--preroll; the first call after an idle gap runs
+at half speed while the clocks come back), then K timed steps with an L2
+flush (256 MiB write) before each (the prefill inputs, ~100 MB, would
+otherwise stay in the 129 MB L2), barrier and synchronize on both sides, max
+over ranks.  libkda itself records events between its kernels
+(kda_chunk_fwd_ws_timed, which runs them one after another), which gives the
+per-kernel device times behind the roofline figures.  The end-to-end figure
+goes through kda_chunk_fwd_host (host buffers, copies inside the timed
+region).  The multi-token pass, the short convolution, the prologue and
+value-group variants and the backward are measured in the same run.
 
 ``--impl reference`` times the fp64 CPU oracle (the reference arm of this
 repository) on a bounded sample of the same workload on the host cores.
