@@ -211,3 +211,115 @@ def chunk_backward(q, k, v, log_alpha, beta, scale, initial_state=None, cu_seqle
                 dS1 = dS0
             gS0[s, h] = dS1
     return gq, gk, gv, gg, gb, gS0
+
+
+def folded_chunk_backward(q, k, v, log_alpha, beta, scale, initial_state=None,
+                          cu_seqlens=None, d_out=None, d_final_state=None, chunk_size=64):
+    """The same gradients through the folded chunk form that the forward
+    engine stores per chunk: M' = K_end^T W, P' = K_end^T A, Q' = Q_hat - Aqk W,
+    Z = Aqk A (A = (I + R)^-1, W = A Diag(b)(exp(G) * K), Q_hat = s exp(G) * Q),
+    with
+
+        S1 = Diag(exp(G_l)) S0 + P' (b V) - M' S0,      O = Q' S0 + Z (b V).
+
+    Reverse mode, chunk by chunk from the end (the serial part is the forward
+    scan transposed, on the same images):
+
+        dS0   = Q'^T dO + Diag(exp(G_l)) dS1 - M'^T dS1
+        d(bV) = Z^T dO + P'^T dS1
+        dQ'   = dO S0^T,   dZ = dO (bV)^T,   dP' = dS1 (bV)^T,   dM' = -dS1 S0^T
+        dK_end = W dM'^T + A dP'^T,          dW = K_end dM' - Aqk^T dQ'
+        dA    = K_end dP' + Aqk^T dZ + dW (b exp(G) K)^T
+        dAqk  = tril_0(-dQ' W^T + dZ A^T),   dR = tril_-1(-A^T dA A^T)
+
+    then the decayed products and exp(G) factors as in ``chunk_backward``.
+    fp64.  Returns the tuple of ``recurrent_backward``.
+    """
+    f = lambda x: np.asarray(x, dtype=np.float64)
+    q, k, v, g, b = f(q), f(k), f(v), f(log_alpha), f(beta)
+    T, H, dk_ = q.shape
+    dv_ = v.shape[-1]
+    cu = np.array([0, T]) if cu_seqlens is None else np.asarray(cu_seqlens, dtype=np.int64)
+    N = len(cu) - 1
+    S0all = np.zeros((N, H, dk_, dv_)) if initial_state is None else f(initial_state)
+    dO = np.zeros((T, H, dv_)) if d_out is None else f(d_out)
+    dSf = np.zeros((N, H, dk_, dv_)) if d_final_state is None else f(d_final_state)
+    gq, gk, gv, gg = (np.zeros_like(x) for x in (q, k, v, g))
+    gb = np.zeros_like(b)
+    gS0 = np.zeros_like(S0all)
+    for s in range(N):
+        t0, t1 = int(cu[s]), int(cu[s + 1])
+        for h in range(H):
+            S = S0all[s, h].copy()
+            fwd = []
+            for c0 in range(t0, t1, chunk_size):
+                c1 = min(c0 + chunk_size, t1)
+                K, Q, V, B = k[c0:c1, h], q[c0:c1, h], v[c0:c1, h], b[c0:c1, h]
+                L = c1 - c0
+                G = np.cumsum(g[c0:c1, h], axis=0)
+                Gl = G[-1]
+                Dx = np.exp(G[:, None, :] - G[None, :, :])
+                low, low0 = np.tril(np.ones((L, L)), -1), np.tril(np.ones((L, L)))
+                KK = np.einsum("ic,jc,ijc->ij", K, K, Dx)
+                QK = np.einsum("ic,jc,ijc->ij", Q, K, Dx)
+                A = np.linalg.inv(np.eye(L) + low * (B[:, None] * KK))
+                Aqk = low0 * (scale * QK)
+                KG = np.exp(G) * K
+                W = A @ (B[:, None] * KG)
+                Kend = np.exp(Gl - G) * K
+                QG = scale * np.exp(G) * Q
+                Mp, Pp, Qp, Zm = Kend.T @ W, Kend.T @ A, QG - Aqk @ W, Aqk @ A
+                BV = B[:, None] * V
+                fwd.append(dict(c0=c0, c1=c1, K=K, Q=Q, V=V, B=B, G=G, Gl=Gl, Dx=Dx, low=low,
+                                low0=low0, KK=KK, A=A, Aqk=Aqk, KG=KG, W=W, Kend=Kend, QG=QG,
+                                Mp=Mp, Pp=Pp, Qp=Qp, Zm=Zm, BV=BV, S0=S.copy()))
+                S = np.exp(Gl)[:, None] * S + Pp @ BV - Mp @ S
+            dS1 = dSf[s, h].copy()
+            for ch in reversed(fwd):
+                c0, c1 = ch["c0"], ch["c1"]
+                K, Q, V, B, G, Gl, Dx = (ch[x] for x in ("K", "Q", "V", "B", "G", "Gl", "Dx"))
+                A, Aqk, KG, W, Kend, QG = (ch[x] for x in ("A", "Aqk", "KG", "W", "Kend", "QG"))
+                Mp, Pp, Qp, Zm, BV, S0 = (ch[x] for x in ("Mp", "Pp", "Qp", "Zm", "BV", "S0"))
+                dOc = dO[c0:c1, h]
+                # the serial part: the forward scan, transposed
+                dS0 = Qp.T @ dOc + np.exp(Gl)[:, None] * dS1 - Mp.T @ dS1
+                dBV = Zm.T @ dOc + Pp.T @ dS1
+                dQp, dZ, dPp, dMp = dOc @ S0.T, dOc @ BV.T, dS1 @ BV.T, -dS1 @ S0.T
+                dGl = np.exp(Gl) * np.sum(S0 * dS1, axis=1)
+                # the folded factors
+                dKend = W @ dMp.T + A @ dPp.T
+                dW = Kend @ dMp - Aqk.T @ dQp
+                dA = Kend @ dPp + Aqk.T @ dZ
+                dAqk = ch["low0"] * (-dQp @ W.T + dZ @ A.T)
+                dQG = dQp
+                # W = A Diag(b) KG
+                BK = B[:, None] * KG
+                dA += dW @ BK.T
+                dBK = A.T @ dW
+                dKG = B[:, None] * dBK
+                dB = np.sum(KG * dBK, axis=1) + np.sum(V * dBV, axis=1)
+                dV = B[:, None] * dBV
+                dR = ch["low"] * (-(A.T @ dA @ A.T))
+                dB += np.sum(dR * ch["KK"], axis=1)
+                wR = (B[:, None] * dR)[:, :, None] * Dx
+                dK = np.einsum("ijc,jc->ic", wR, K) + np.einsum("ijc,ic->jc", wR, K)
+                tR = wR * K[:, None, :] * K[None, :, :]
+                dG = tR.sum(axis=1) - tR.sum(axis=0)
+                wQ = (scale * dAqk)[:, :, None] * Dx
+                dQ = np.einsum("ijc,jc->ic", wQ, K)
+                dK += np.einsum("ijc,ic->jc", wQ, Q)
+                tQ = wQ * Q[:, None, :] * K[None, :, :]
+                dG += tQ.sum(axis=1) - tQ.sum(axis=0)
+                dK += np.exp(G) * dKG
+                dG += KG * dKG
+                dQ += scale * np.exp(G) * dQG
+                dG += QG * dQG
+                dK += np.exp(Gl - G) * dKend
+                dG -= Kend * dKend
+                dGl += np.sum(Kend * dKend, axis=0)
+                dG[-1] += dGl
+                gg[c0:c1, h] = np.cumsum(dG[::-1], axis=0)[::-1]
+                gq[c0:c1, h], gk[c0:c1, h], gv[c0:c1, h], gb[c0:c1, h] = dQ, dK, dV, dB
+                dS1 = dS0
+            gS0[s, h] = dS1
+    return gq, gk, gv, gg, gb, gS0

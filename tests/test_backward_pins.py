@@ -66,18 +66,21 @@ def test_read_gradient_closed_form():
     assert not dvv.any()
 
 
+@pytest.mark.parametrize("folded", [False, True])
 @pytest.mark.parametrize("chunk_size", [1, 3, 16, 64])
-def test_chunkwise_backward_equals_recurrent(chunk_size):
+def test_chunkwise_backward_equals_recurrent(chunk_size, folded):
     """The chunkwise backward (sec. 6's chunk form differentiated, the
-    blueprint of a chunk-parallel backward) gives the recurrent backward's
-    gradients to rounding, for any chunk size, across packed sequences with
-    empty and one-token ones, partial last chunks and strong decays."""
-    from oracle.backward import chunk_backward
+    blueprint of a chunk-parallel backward), directly or through the folded
+    per-chunk factors M', P', Q', Z the forward engine stores, gives the
+    recurrent backward's gradients to rounding, for any chunk size, across
+    packed sequences with empty and one-token ones, partial last chunks and
+    strong decays."""
+    from oracle.backward import chunk_backward, folded_chunk_backward
     P = _problem(20, [37, 0, 1, 70, 16], H=2, dk=8, dv=8)
     P["g"][40:50] -= 6.0   # near-total forgetting inside a chunk
     args = (P["q"], P["k"], P["v"], P["g"], P["b"], P["s"], P["S0"], P["cu"], P["R"], P["Q"])
     ref = recurrent_backward(*args)
-    got = chunk_backward(*args, chunk_size=chunk_size)
+    got = (folded_chunk_backward if folded else chunk_backward)(*args, chunk_size=chunk_size)
     for name, x, r in zip(("dq", "dk", "dv", "dlog_alpha", "dbeta", "d_initial"), got, ref):
         np.testing.assert_allclose(x, r, rtol=0, atol=1e-11 * max(np.abs(r).max(), 1.0),
                                    err_msg=name)
