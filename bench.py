@@ -54,6 +54,9 @@ def parse_args():
     ap.add_argument("--preroll", type=float, default=0.3,
                     help="seconds of back-to-back steps before each timed loop (0: none, "
                          "for profiler runs)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the headline, time the packed 32-sequence workload and "
+                         "the 1,048,576-token sequence (one JSON line each)")
     return ap.parse_args()
 
 
@@ -793,6 +796,109 @@ def run_short_conv(args, dist, peaks, dev, stream):
                          "peak_source": peaks["source"]}}
 
 
+def run_sweep(args, dist: Dist):
+    """The two larger prefill workloads through the public call: 32 packed
+    sequences (lengths ~ U[512, 8192], H=32, initial states given) and one
+    1,048,576-token sequence (H=32).  Both hold far more than L2, so no flush.
+    Per-kernel times come from a second run with library-recorded events."""
+    import torch
+    import kimi_delta_attention_chunkwise_gb300 as kda
+    from kimi_delta_attention_chunkwise_gb300 import build, inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(dist.local_rank)
+    build.build()
+    peaks = load_peaks()
+    dev = torch.device("cuda", dist.local_rank)
+    stream = torch.cuda.current_stream()
+
+    def workloads():
+        w = inputs.varlen_prefill()
+        t = lambda a, dt=None: torch.from_numpy(a).to(dev, dt) if dt else torch.from_numpy(a).to(dev)
+        yield (w.name, dict(q=t(w.q, torch.bfloat16), k=t(w.k, torch.bfloat16),
+                            v=t(w.v, torch.bfloat16), log_alpha=t(w.log_alpha), beta=t(w.beta),
+                            cu_seqlens=t(w.cu_seqlens), initial_state=t(w.initial_state),
+                            scale=w.scale), len(w.meta["lengths"]))
+        del w
+        x = inputs.long_context_device(device=str(dev))
+        x["initial_state"] = None
+        yield ("long_context_T1048576_H32_d128", x, 1)
+
+    for name, x, n_seqs in workloads():
+        q = x["q"]
+        T, H, d = q.shape
+        out = torch.empty_like(q)
+        fin = torch.empty((n_seqs, H, d, d), dtype=torch.float32, device=dev)
+        call = lambda: kda.kda_chunk_fwd(q, x["k"], x["v"], x["log_alpha"], x["beta"],
+                                         x["scale"], x["initial_state"], x["cu_seqlens"], out,
+                                         fin, engine=args.engine)
+        for _ in range(max(3, args.warmup)):
+            call()
+        torch.cuda.synchronize()
+        steps = max(1, min(args.steps, 10))
+        sampler = ClockSampler(dist.local_rank)
+        sampler.start()
+        preroll(call)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        dist.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(steps):
+            call()
+        end.record(stream)
+        torch.cuda.synchronize()
+        dist.barrier()
+        clocks = sampler.stop()
+        ms = dist.max(start.elapsed_time(end)) / steps
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
+        for e in evs:
+            e.record(stream)
+        _, _, n_rec = kda.kda_chunk_fwd_ws_timed(q, x["k"], x["v"], x["log_alpha"], x["beta"],
+                                                 x["scale"], x["initial_state"],
+                                                 x["cu_seqlens"], out, fin, evs,
+                                                 engine=args.engine)
+        torch.cuda.synchronize()
+        names = ["chunk_table", "prep", "scan", "out"] if n_rec == 5 else \
+            [f"stage{j}" for j in range(max(0, n_rec - 1))]
+        stages = {nm: evs[j].elapsed_time(evs[j + 1]) for j, nm in enumerate(names)}
+        flops = prefill_flops_per_tok_head(d, 64) * T * H
+        path_bytes = path_bytes_per_tok_head(d) * T * H
+        line = {"sweep": name, "impl": "ours", "n_gpus": dist.world, "steps": steps,
+                "tokens": T, "heads": H, "sequences": n_seqs, "ms_per_call": ms,
+                "tokens_per_s": T * dist.world / (ms / 1e3),
+                "tflops": flops / (ms / 1e3) / 1e12,
+                "tensor_frac_of_bf16_peak": flops / (ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+                "path_gbs": path_bytes / (ms / 1e3) / 1e9,
+                "path_frac_of_hbm": path_bytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                "stages_ms": stages, "clocks": clocks, "data": "synthetic"}
+        if n_seqs > 1:
+            # the gradients of the packed workload (d_out ~ N(0, 1), no final-state gradient)
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(8)
+            do = torch.randn(q.shape, generator=gen, device=dev).to(torch.bfloat16)
+            bwd = lambda: kda.kda_recurrent_bwd(q, x["k"], x["v"], x["log_alpha"], x["beta"],
+                                                x["scale"], x["initial_state"],
+                                                x["cu_seqlens"], do, None)
+            for _ in range(2):
+                bwd()
+            torch.cuda.synchronize()
+            reps = 2
+            start.record(stream)
+            for _ in range(reps):
+                bwd()
+            end.record(stream)
+            torch.cuda.synchronize()
+            bms = dist.max(start.elapsed_time(end)) / reps
+            line["backward"] = {"ms_per_call": bms, "tokens_per_s": T * dist.world / (bms / 1e3),
+                                "form": "recurrent, 8-token checkpoints"}
+            del do
+        if dist.rank == 0:
+            print(json.dumps(line), flush=True)
+        del x, q, out, fin
+        torch.cuda.empty_cache()
+
+
 def main():
     global PREROLL_SECONDS
     args = parse_args()
@@ -801,6 +907,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, dist)
+        elif args.sweep:
+            run_sweep(args, dist)
         else:
             run_ours(args, dist)
     finally:
