@@ -149,17 +149,22 @@ typedef enum {
  * driver).  Use kda_chunk_fwd_ws to pass caller-owned scratch instead. *
  * Kernel overlap: when its serial scan needs at most half of the SMs, the
  * tensor-core engine runs the scan and the output pass beside the
- * chunk-parallel prep, handing work over through flags in its scratch (the
- * results are bit-identical to running them one after another).  Tools that
- * run kernels one at a time would leave the scan waiting out its ~1 s
- * timeouts, so the engine runs its kernels in sequence when the environment
- * sets CUDA_INJECTION64_PATH (how Nsight Compute and the compute sanitizer
- * attach) or KDA_LAUNCH_ORDER=sequential.  The same applies to work that
- * runs beside a call on other streams: calls whose scans together occupy
- * every SM (or other kernels that do) leave the prep no SM, and the scan
- * gives up after ~1 s with KDA_ERR_TIMEOUT in the device status word; set
- * KDA_LAUNCH_ORDER=sequential for such workloads.  Two or three concurrent
- * calls of the headline's size (32 scan CTAs each) are fine.
+ * chunk-parallel prep (calls of at most 65,536 (chunk, head) items), or the
+ * prep first and then the output pass beside the scan (larger calls).
+ * Either way the kernels hand work over through flags in the scratch, and
+ * the results are bit-identical to running them one after another, which is
+ * what calls with more scan CTAs do.  Tools that run kernels
+ * one at a time would leave the waits running out their ~1 s timeouts, so
+ * the engine runs its kernels in sequence when the environment sets
+ * CUDA_INJECTION64_PATH (how Nsight Compute and the compute sanitizer
+ * attach) or KDA_LAUNCH_ORDER=sequential.  In the first order the same
+ * applies to work that runs beside a call on other streams: calls whose
+ * scans together occupy every SM (or other kernels that do) leave the prep
+ * no SM, and the scan gives up after ~1 s with KDA_ERR_TIMEOUT in the device
+ * status word; set KDA_LAUNCH_ORDER=sequential for such workloads.  Two or
+ * three concurrent calls of the headline's size (32 scan CTAs each) are
+ * fine.  In the second order the output pass starts only once every scan CTA
+ * is resident, so it waits on nothing that other work can hold back.
  */
 kdaStatus_t kda_chunk_fwd(const void *q, const void *k, const void *v,
                           const float *log_alpha, const float *beta, float scale,

@@ -1468,6 +1468,17 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
     // chain runs under the prep's parallel work instead of after it; the
     // output CTAs follow the scan through the state flags and fill the SMs
     // that the prep's last CTAs leave.
+    //
+    // Tail order, when the scan's CTAs take at most half of the SMs but the
+    // prep grid is too large to run beside the scan: table -> prep (a plain
+    // launch: with flags on it does not wait on griddepcontrol, so the stream
+    // order keeps it behind the table; it publishes each image) -> scan
+    // (programmatic dependent of the prep, which it waits for, then triggers)
+    // -> output (programmatic dependent of the scan, so it starts once every
+    // scan CTA is resident).  The output CTAs follow the scan through the
+    // state flags on the SMs the scan leaves, instead of after it.  With more
+    // scan CTAs than that, output CTAs waiting on late sequences would hold
+    // SMs that finished ones could use: those calls run in sequence.
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1478,10 +1489,13 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         sms = 0;
-    const bool streamed = !timed && concurrent_order_allowed() && a.T > 0 &&
-                          n_items <= kStreamMaxItems && sms > 0 && 2 * scan_ctas <= (size_t)sms;
+    const bool overlap = !timed && concurrent_order_allowed() && a.T > 0 && sms > 0 &&
+                         2 * scan_ctas <= (size_t)sms;
+    const bool concurrent = overlap && n_items <= kStreamMaxItems;
+    // the kernels hand work over through flags (streamed or tail order)
+    const bool streamed = overlap;
     // prep CTAs resident at once (two per SM on the SMs the scan leaves)
-    const int32_t prefetch_dist = 2 * (sms - (streamed ? (int32_t)scan_ctas : 0));
+    const int32_t prefetch_dist = 2 * (sms - (concurrent ? (int32_t)scan_ctas : 0));
     auto config = [&](dim3 grid, int threads, size_t smem, bool dependent) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
@@ -1544,13 +1558,15 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
                                   a.T, a.H, sc, (int32_t)streamed, (int64_t)n_items,
                                   a.status);
     };
-    if (streamed) {
+    if (concurrent) {
         e = launch_scan(true);
         if (e != cudaSuccess) return e;
     }
 
     if (a.T > 0) {
-        const cudaLaunchConfig_t cfg = config(dim3((unsigned)n_items), kPrepThreads, kPrepSmem, true);
+        // tail order: a plain launch (see above)
+        const cudaLaunchConfig_t cfg = config(dim3((unsigned)n_items), kPrepThreads, kPrepSmem,
+                                              !streamed || concurrent);
         e = cudaLaunchKernelEx(&cfg, prep, maps, static_cast<const __nv_bfloat16 *>(a.q),
                                static_cast<const __nv_bfloat16 *>(a.k), a.beta, a.scale,
                                static_cast<const int32_t *>(a.cu_seqlens), a.N, a.T, a.H, a.G,
@@ -1560,7 +1576,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
     }
     a.clock->mark(stream);
 
-    if (!streamed) {
+    if (!concurrent) {
         e = launch_scan(a.T > 0);  // with T == 0 no prep runs ahead of it
         if (e != cudaSuccess) return e;
     }
@@ -1582,8 +1598,9 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        // a programmatic dependent of the scan (sequential) or of the prep
-        // (streamed: its CTAs fill the SMs that the prep's last CTAs leave)
+        // a programmatic dependent of the scan (sequential; tail: its CTAs
+        // follow the scan on the SMs it leaves) or of the prep (streamed: its
+        // CTAs fill the SMs that the prep's last CTAs leave)
         const cudaLaunchConfig_t cfg = config(dim3((unsigned)n_items), kOutThreads, kOutSmem, true);
         const int32_t *cu = static_cast<const int32_t *>(a.cu_seqlens);
         if (a.out_f32) {

@@ -194,13 +194,17 @@ def test_engines_agree():
     assert nerr(a[0], b[0]) < TOL_BF16 and nerr(a[1], b[1]) < TOL_BF16
 
 
-@pytest.mark.parametrize("lengths,H", [([4096], 16), ([1000, 37, 2000], 8), ([130] * 40, 2)])
+@pytest.mark.parametrize("lengths,H", [([4096], 16), ([1000, 37, 2000], 8), ([130] * 40, 2),
+                                       ([135000], 32)])
 def test_launch_orders_agree(lengths, H):
-    """The tensor engine runs the scan concurrently with the prep (image flags)
-    when the scan's CTAs fit in half the SMs, and after it otherwise; with
-    per-kernel events it always runs them in sequence.  Both orders run the
-    same arithmetic, so the results are bit-identical, and both match the
-    oracle."""
+    """When the scan's CTAs fit in half the SMs, the tensor engine runs the
+    scan concurrently with the prep (image flags) for calls of at most 65,536
+    (chunk, head) items (the first two cases), and the prep first, then the
+    output pass beside the scan (state flags) for larger ones (67,520 items
+    for 135,000 tokens x 32 heads).  With more scan CTAs (160 for 40
+    sequences x 2 heads x 2 value tiles) or with per-kernel events it runs
+    them in sequence.  All orders run the same arithmetic, so the results
+    are bit-identical, and they match the oracle."""
     import torch
     import kimi_delta_attention_chunkwise_gb300 as kda
     w = inputs.prefill(109, lengths, H=H, d=128, dtype="bf16", init_std=0.02)
