@@ -56,7 +56,8 @@ def parse_args():
                          "for profiler runs)")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the headline, time the packed 32-sequence workload and "
-                         "the 1,048,576-token sequence (one JSON line each)")
+                         "the 1,048,576-token sequence (one JSON line each); with "
+                         "--impl reference, time the oracle on every named workload")
     return ap.parse_args()
 
 
@@ -319,6 +320,51 @@ def run_reference(args, dist: Dist):
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def run_reference_sweep(args, dist: Dist):
+    """The oracle, as it stands, on each named workload (host cores): the
+    tiny fp32 one, the head-group prefill (all cores and one core), the
+    packed 32-sequence batch, the 1M-token recipe's first 8,192 tokens and
+    the 64 decode steps of 256 sequences x 32 heads.  One JSON line each."""
+    if dist.rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from kimi_delta_attention_chunkwise_gb300 import inputs
+    oracle.build()
+    thr = oracle_threads()
+
+    def decode_as_prefill():
+        dw = inputs.batched_decode()
+        steps, N, H, d = dw.q.shape
+        # sequence n's 64 steps as one 64-token sequence: [N * steps, H, d]
+        seqs = lambda a: np.ascontiguousarray(np.swapaxes(a, 0, 1)).reshape((N * steps,) + a.shape[2:])
+        cu = np.arange(0, N * steps + 1, steps, dtype=np.int32)
+        return (dw.name, seqs(dw.q), seqs(dw.k), seqs(dw.v), seqs(dw.log_alpha), seqs(dw.beta),
+                dw.scale, dw.initial_state, cu, N)
+
+    def prefill(w, name=None):
+        return (name or w.name, w.q, w.k, w.v, w.log_alpha, w.beta, w.scale, w.initial_state,
+                w.cu_seqlens, len(w.cu_seqlens) - 1)
+
+    jobs = [(lambda: prefill(inputs.tiny_f32()), thr),
+            (lambda: prefill(inputs.head_group_prefill()), thr),
+            (lambda: prefill(inputs.head_group_prefill()), 1),
+            (lambda: prefill(inputs.varlen_prefill()), thr),
+            (lambda: prefill(inputs.long_context_prefix(8192)), thr),
+            (decode_as_prefill, thr)]
+    for make, cores in jobs:
+        name, q, k, v, la, b, scale, s0, cu, n_seqs = make()
+        T, H = q.shape[0], q.shape[1]
+        t0 = time.perf_counter()
+        oracle.recurrent(q, k, v, la, b, scale, s0, cu, threads=cores)
+        sec = time.perf_counter() - t0
+        print(json.dumps({"sweep": name, "impl": "reference", "kind": "oracle",
+                          "cores": cores, "sequences": n_seqs, "tokens": T, "heads": H,
+                          "seconds": sec, "tok_heads_per_s": T * H / sec,
+                          "tokens_per_s": T / sec, "precision": "f64"}), flush=True)
+        del q, k, v, la, b, s0
 
 
 def cpu_baseline(w):
@@ -906,7 +952,10 @@ def main():
     dist = Dist()
     try:
         if args.impl == "reference":
-            run_reference(args, dist)
+            if args.sweep:
+                run_reference_sweep(args, dist)
+            else:
+                run_reference(args, dist)
         elif args.sweep:
             run_sweep(args, dist)
         else:
