@@ -97,6 +97,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                            ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32,
                                            ctypes.POINTER(ctypes.c_int32)]
     lib.kda_chunk_fwd_ws_timed.restype = ctypes.c_int
+    lib.kda_chunk_fwd_static.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, fp, ip, vp, fp,
+                                         shp, vp]
+    lib.kda_chunk_fwd_static.restype = ctypes.c_int
     lib.kda_chunk_fwd_host_scratch_size.argtypes = [shp, ctypes.POINTER(ctypes.c_size_t)]
     lib.kda_chunk_fwd_host_scratch_size.restype = ctypes.c_int
     lib.kda_chunk_fwd_host.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, fp, ip, vp, fp, shp,
@@ -329,6 +332,24 @@ def kda_chunk_fwd(q, k, v, log_alpha, beta, scale: float, initial_state=None,
         if ws is not None:
             wp = (ws.data_ptr() + 255) // 256 * 256
         _check(lib.kda_chunk_fwd_ws(*args, wp, nbytes, s), "kda_chunk_fwd_ws")
+    return out, final_state
+
+
+def kda_chunk_fwd_static(q, k, v, log_alpha, beta, scale: float, initial_state=None,
+                         cu_seqlens=None, out=None, final_state=None, *, chunk_size: int = 0,
+                         engine="auto", stream=None, out_f32: bool = False,
+                         l2norm_qk: bool = False, beta_logits: bool = False,
+                         gate=None) -> Tuple[object, object]:
+    """kda_chunk_fwd with the library's fixed scratch array (C:
+    kda_chunk_fwd_static): allocates no device memory; problems larger than
+    the array are refused (KDA_ERR_UNSUPPORTED).  Arguments as kda_chunk_fwd."""
+    shape, out = _prefill_args(q, k, v, log_alpha, beta, initial_state, cu_seqlens, out,
+                               final_state, chunk_size, engine, out_f32,
+                               (l2norm_qk, beta_logits, gate))
+    _check(load().kda_chunk_fwd_static(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), float(scale),
+        _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+        ctypes.byref(shape), _stream_handle(stream)), "kda_chunk_fwd_static")
     return out, final_state
 
 

@@ -243,3 +243,99 @@ def test_host_entry_rejects_bad_arguments(lib):
     assert call(s, out=None) == kda.KDA_ERR_INVALID_ARG
     assert call(_shape(N=3, T=4096, H=16)) == kda.KDA_ERR_INVALID_ARG   # N > 1 needs cu_seqlens
     assert call(_shape(dk=96, dv=96)) == kda.KDA_ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------------------
+# the binding against the header: prototypes and struct layouts
+# ---------------------------------------------------------------------------
+
+def _header_prototypes():
+    """{name: (return type, [parameter declarations])} for every function
+    include/kda.h declares."""
+    import os
+    import re
+    with open(os.path.join(build.INCLUDE, "kda.h")) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    protos = {}
+    for m in re.finditer(r"(kdaStatus_t|const\s+char\s*\*)\s*(kda_\w+)\s*\(([^)]*)\)\s*;", text):
+        params = [p.strip() for p in m.group(3).split(",") if p.strip() not in ("", "void")]
+        protos[m.group(2)] = (m.group(1), params)
+    return protos
+
+
+def _c_kind(decl: str) -> str:
+    if "*" in decl or "cudaStream_t" in decl:
+        return "pointer"
+    if decl.startswith("float"):
+        return "float"
+    if "size_t" in decl:
+        return "size"
+    if decl.split()[0] in ("int32_t", "int", "kdaStatus_t", "kdaDtype_t"):
+        return "int32"
+    raise AssertionError(f"unclassified parameter {decl!r}")
+
+
+def _ctypes_kind(t) -> str:
+    if t in (ctypes.c_void_p, ctypes.c_char_p) or issubclass(t, ctypes._Pointer):
+        return "pointer"
+    if t is ctypes.c_float:
+        return "float"
+    if t is ctypes.c_size_t:
+        return "size"
+    if t in (ctypes.c_int32, ctypes.c_int):
+        return "int32"
+    raise AssertionError(f"unclassified ctypes type {t!r}")
+
+
+def test_binding_prototypes_match_the_header(lib):
+    """Every declared function has a ctypes prototype with the same number
+    and kinds of parameters (pointer, float, int32, size_t) and the same
+    return kind, so no call marshals an argument into the wrong slot."""
+    protos = _header_prototypes()
+    assert set(protos) == set(binding.header_functions())
+    for name, (ret, params) in protos.items():
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, f"{name}: no ctypes prototype"
+        want = [_c_kind(p) for p in params]
+        got = [_ctypes_kind(t) for t in fn.argtypes]
+        assert got == want, f"{name}: binding {got} vs header {want}"
+        if ret == "kdaStatus_t":
+            assert fn.restype is ctypes.c_int, name
+        else:
+            assert fn.restype is ctypes.c_char_p, name
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    """kdaShape_t and kdaConvShape_t as the C compiler lays them out (a probe
+    built with gcc against include/kda.h) equal the ctypes structures: the
+    same size and the same offset and size for every field."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    cuda_inc = "/usr/local/cuda/include"
+    import os
+    if not gcc or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
+        pytest.skip("gcc or the CUDA headers are missing")
+    structs = {"kdaShape_t": binding.kdaShape_t, "kdaConvShape_t": binding.kdaConvShape_t}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "kda.h"', "int main(void) {"]
+    for sname, cls in structs.items():
+        lines.append(f'  printf("{sname} . %zu %zu\\n", (size_t)0, sizeof({sname}));')
+        for fname, _ in cls._fields_:
+            lines.append(f'  printf("{sname} {fname} %zu %zu\\n", offsetof({sname}, {fname}), '
+                         f'sizeof((({sname} *)0)->{fname}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([gcc, "-std=c99", "-I", build.INCLUDE, "-I", cuda_inc, str(src), "-o",
+                    str(exe)], check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    seen = {}
+    for line in out.splitlines():
+        sname, fname, off, size = line.split()
+        seen[(sname, fname)] = (int(off), int(size))
+    for sname, cls in structs.items():
+        assert seen[(sname, ".")][1] == ctypes.sizeof(cls), sname
+        for fname, ftype in cls._fields_:
+            assert seen[(sname, fname)] == (getattr(cls, fname).offset, ctypes.sizeof(ftype)), \
+                (sname, fname)
