@@ -32,7 +32,8 @@ L2_EPS = 1e-6
 
 def sigmoid(x):
     x = np.asarray(x, dtype=np.float64)
-    return 1.0 / (1.0 + np.exp(-x))
+    with np.errstate(over="ignore"):  # exp(-x) = inf for x < -709 gives the exact limit 0
+        return 1.0 / (1.0 + np.exp(-x))
 
 
 def l2_normalise(x):
