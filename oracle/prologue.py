@@ -22,6 +22,10 @@ ingredients.  We take log_alpha = -5 * sigmoid(exp(A_log[h]) * (g + b[h, j])):
 the sensitivity acts inside the sigmoid (outside it would leave (-5, 0)),
 and A_log is a logarithm, so exp(A_log) > 0.  The L2 norm is
 x / sqrt(sum x^2 + 1e-6) (the epsilon keeps a zero vector at zero).
+
+Parity partly unpinned: the pins fix the range, the midpoint, monotonicity
+and the closed forms; where exp(A_log) enters the gate is this reading's
+choice, which no printed value checks.
 """
 from __future__ import annotations
 

@@ -21,6 +21,10 @@ first token come from its cache (slot W-1 the most recent), or are zero
 without one; after the call the cache holds the sequence's W most recent
 inputs.  A decode step is the same filter over the cache shifted by one with
 the new token appended.
+
+Parity partly unpinned: the pins are closed forms of this reading (impulse
+and step responses, a hand-worked example, decode equal to prefill); the
+tap order itself is the reading's, since the page's formula is stripped.
 """
 from __future__ import annotations
 
