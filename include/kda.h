@@ -416,12 +416,17 @@ kdaStatus_t kda_short_conv_step(const void *x, const float *weight, const float 
  *   dq, dk [T, H, d_k];  dv [T, H, d_v];  dlog_alpha [T, H, d_k];
  *   dbeta [T, H];  d_initial_state [N, H, d_k, d_v] or NULL (not written)
  *
- * One CTA per (sequence, head) carries the state and its gradient through the
- * sequence: a forward sweep checkpoints the state every 8 tokens, and the
- * reverse sweep recomputes each 8-token chunk from its checkpoint.  Scratch
- * (checkpoints and one chunk of states per (sequence, head), about
- * (T / 8 + N) * H * d_k * d_v * 4 + N * H * 8 * d_k * d_v * 4 bytes) is taken
- * with cudaMallocAsync / cudaFreeAsync on `stream`.  Value-head groups and
+ * One CTA per (sequence, head, column tile) carries its columns of the state
+ * and of its gradient through the sequence: a forward sweep checkpoints the
+ * state every 8 tokens, and the reverse sweep recomputes each 8-token chunk
+ * from its checkpoint.  The tiles are 16 columns wide when the (sequence,
+ * head) pairs alone would leave most SMs idle (fewer than two per SM), else
+ * the whole width.  Scratch (checkpoints and one chunk of states per
+ * (sequence, head), about (T / 8 + N) * H * d_k * d_v * 4 +
+ * N * H * 8 * d_k * d_v * 4 bytes, plus, with 16-column tiles, the per-tile
+ * partial sums of dq, dk, dlog_alpha and dbeta, (d_v / 16) * T * H *
+ * (3 * d_k + 1) * 4 bytes) is taken with cudaMallocAsync / cudaFreeAsync on
+ * `stream`.  Value-head groups and
  * the input prologue are not supported here (KDA_ERR_UNSUPPORTED).
  */
 kdaStatus_t kda_recurrent_bwd(const void *q, const void *k, const void *v,
