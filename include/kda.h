@@ -57,8 +57,8 @@ typedef enum {
     KDA_ENGINE_SIMT = 2        /* fp32 CUDA-core chunk engine (any supported shape) */
 } kdaEngine_t;
 
-/* Problem description.  All fields are plain int32 so the struct has the
-   same layout from C, C++ and ctypes. */
+/* Problem description: int32 fields and, last, two pointers, so the struct
+   has the same layout from C, C++ and ctypes on 64-bit hosts. */
 typedef struct {
     int32_t num_seqs;      /* N >= 1: packed sequences (chunk_fwd) / batch (step) */
     int32_t total_tokens;  /* T >= 0: packed tokens (chunk_fwd); must equal N (step) */
@@ -116,8 +116,9 @@ typedef enum {
  * Scratch to Kimi 3", sec. 9, cu_seqlens); the last chunk of a sequence may be
  * shorter.  Results do not depend on the chunk size beyond rounding.
  *
- *   q, k          [T, H, d_k]  dtype        (q and k are used as given; the
- *                                            caller normalises them)
+ *   q, k          [T, H, d_k]  dtype        (used as given unless
+ *                                            KDA_PROLOGUE_L2NORM_QK: then
+ *                                            normalised in-kernel)
  *   v             [T, HV, d_v] dtype        HV = shape->num_v_heads, or H
  *   log_alpha     [T, HV, d_k] float32      finite and <= 0 (log retention;
  *                                            gate logits with KDA_PROLOGUE_GATE);
