@@ -21,6 +21,11 @@ value-group variants and the backward are measured in the same run.
 
 ``--impl reference`` times the fp64 CPU oracle (the reference arm of this
 repository) on a bounded sample of the same workload on the host cores.
+
+``--sweep`` prints, instead of the headline line, one JSON line for each of
+the two larger prefill workloads (32 packed sequences x 32 heads with their
+backward; one 1,048,576-token sequence x 32 heads); with ``--impl
+reference`` it times the oracle on every named workload.
 """
 from __future__ import annotations
 
