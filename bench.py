@@ -1,31 +1,34 @@
 #!/usr/bin/env python3
 """Benchmark of libkda on one GB300 (or N replicas, one per GPU).
 
-One step = one ``kda_chunk_fwd`` over the single-head-group prefill workload
-(B=1, H=16, T=4096, d_k=d_v=128, chunk 64, bf16 q/k/v, fp32 gates and state,
-seeded synthetic inputs), i.e. every prefill stage of the hot path.  The
-decode row (``kda_recurrent_step``, 256 sequences x 32 heads, 512 MiB fp32
-state, 64 steps) is measured in the same run and reported under "decode".
+One step = one ``kda_chunk_fwd`` over the long-context prefill workload: one
+sequence of 1,048,576 tokens x 32 heads, d_k = d_v = 128, chunk 64, bf16
+q/k/v, fp32 gates (log_alpha = -softplus(N(-6, 1))) and state, drawn on the
+device with a seeded generator -- every prefill stage of the hot path (chunk
+table, prep, state scan, outputs), the largest single-GPU workload named for
+this path.  Its inputs (51.7 GB) dwarf the 129 MB L2, so no flush is needed.
 
-Timing: CUDA events on the launch stream, W untimed warm-up steps, about
-0.3 s of back-to-back steps (--preroll; the first call after an idle gap runs
-at half speed while the clocks come back), then K timed steps with an L2
-flush (256 MiB write) before each (the prefill inputs, ~100 MB, would
-otherwise stay in the 129 MB L2), barrier and synchronize on both sides, max
-over ranks.  libkda itself records events between its kernels
-(kda_chunk_fwd_ws_timed, which runs them one after another), which gives the
-per-kernel device times behind the roofline figures.  The end-to-end figure
-goes through kda_chunk_fwd_host (host buffers, copies inside the timed
-region).  The multi-token pass, the short convolution, the prologue and
-value-group variants and the backward are measured in the same run.
+Timing: CUDA events on the launch stream, W untimed warm-up calls, about
+0.3 s of back-to-back calls (--preroll; the first call after an idle gap runs
+slower while the clocks come back), then K timed calls, barrier and
+synchronize on both sides, max over ranks.  libkda itself records events
+between its kernels (kda_chunk_fwd_ws_timed, which runs them one after
+another) for the per-kernel device times behind the roofline figures, which
+take the method's algorithmic bytes and flops per (token, head); the engine's
+own scratch traffic is reported apart.  The end-to-end figure goes through
+kda_chunk_fwd_host (page-locked host buffers, copies in and out inside the
+timed region).
+
+Extra rows in the same line: the single-head-group prefill (H=16, T=4096,
+L2 flushed before each step), the packed 32-sequence prefill with its
+backward, K3-range gates, the fused prologue and value-head groups, the
+backward of the head-group workload, the decode step (256 sequences x 32
+heads, 512 MiB state, 64 steps), the multi-token recurrent pass and the
+short convolution.
 
 ``--impl reference`` times the fp64 CPU oracle (the reference arm of this
-repository) on a bounded sample of the same workload on the host cores.
-
-``--sweep`` prints, instead of the headline line, one JSON line for each of
-the two larger prefill workloads (32 packed sequences x 32 heads with their
-backward; one 1,048,576-token sequence x 32 heads); with ``--impl
-reference`` it times the oracle on every named workload.
+repository) on a bounded sample of the same workload on the host cores;
+``--impl reference --sweep`` times it on every named workload.
 """
 from __future__ import annotations
 
@@ -59,10 +62,12 @@ def parse_args():
     ap.add_argument("--preroll", type=float, default=0.3,
                     help="seconds of back-to-back steps before each timed loop (0: none, "
                          "for profiler runs)")
+    ap.add_argument("--profile", action="store_true",
+                    help="run only the single-head-group prefill, --warmup + --steps plain calls "
+                         "and nothing else (for counter captures, which need a small case)")
     ap.add_argument("--sweep", action="store_true",
-                    help="instead of the headline, time the packed 32-sequence workload and "
-                         "the 1,048,576-token sequence (one JSON line each); with "
-                         "--impl reference, time the oracle on every named workload")
+                    help="with --impl reference: time the oracle on every named workload "
+                         "(one JSON line each)")
     return ap.parse_args()
 
 
@@ -186,42 +191,39 @@ class ClockSampler:
 # algorithmic work per (token, head): the figures behind the roofline
 # ---------------------------------------------------------------------------
 
+def path_bytes_per_tok_head(d: int) -> int:
+    """Whole-path minimum: q, k, v, out (bf16) and log_alpha (fp32) once, beta."""
+    return 4 * 2 * d + 4 * d + 4
+
+
 def prefill_flops_per_tok_head(d: int, C: int) -> int:
     """Dense chunk contractions: K K^T, Q K^T, A^kk (beta V), A^kk (beta Gamma K),
     A^qk E (5 x 2Cd) plus W S, K_end^T E, Q_hat S (3 x 2d^2)."""
     return 10 * C * d + 6 * d * d
 
 
-def stage_work(d: int, C: int):
-    """Per (token, head) compulsory bytes and issued tensor-core flops of each
-    kernel of the tensor-core engine (its own inputs read once, its outputs
-    written once).  The per-(chunk, head) image holds -M' (d x d), P' (d x C),
-    Q' (C x d), Z (C x C) in f16 plus Gamma_last and beta in fp32; the scan
-    reads its -M'/P' part once per value tile and writes S_c (d x d, f16) per
-    chunk; the output pass reads Q'/Z (with 8 KB of filler rows), S_c and v."""
-    nt = 2                                            # value tiles per head
-    img = (2 * d * d + 2 * d * C + 2 * C * d + 2 * C * C + 4 * d + 4 * C) / C
-    prep_bytes = 2 * 2 * d + 4 * d + 4 + img          # q, k, log_alpha, beta -> image
-    scan_bytes = (nt * (2 * d * d + 2 * d * C) / C    # -M', P' per value tile
-                  + 2 * d + 4 * d / C * nt + 4 * nt   # v, Gamma_last, beta
-                  + 2 * d * d / C)                    # S_c out (f16)
-    out_bytes = ((2 * C * d + 2 * C * C + 2 * 64 * 64 + 2 * d * d) / C  # Q', Z, filler, S_c
-                 + 2 * d + 4 + 2 * d)                 # v, beta in; out (bf16)
-    prep_flops = 10 * C * d + 2 * d * d + 2 * C * C   # [K;Q]K^T, W, M', P', A^qk W, Z
-    scan_flops = 2 * d * d + 2 * d * d * d / C        # P' (beta V), M' S_c
-    out_flops = 2 * d * d + 2 * C * d                 # Q' S_c, Z (beta V)
-    return {"prep": (prep_bytes, prep_flops), "scan": (scan_bytes, scan_flops),
-            "out": (out_bytes, out_flops)}
-
+# The method's algorithmic work per (token, head) at d = 128, C = 64 (the
+# roofline's numerators): q, k, v, out in bf16, log_alpha in fp32 and beta read
+# or written once, and the dense chunk contractions.
+PATH_BYTES = path_bytes_per_tok_head(128)
+PATH_FLOPS = prefill_flops_per_tok_head(128, 64)
+# The tensor-core engine's own scratch traffic per (token, head) of each
+# kernel, beyond the method's bytes: the prep writes one 74,496-byte image per
+# (chunk, head) (-M', P', Q', Z in f16, Gamma_last and beta); the scan reads
+# its 48 KB -M'/P' part once per 64-wide value tile and writes the chunk's
+# state (f16, 32 KB); the output pass reads Q', Z and filler (32 KB) and the
+# state (32 KB).  Per token: divide by the chunk's 64 tokens.
+SCRATCH_BYTES = {"prep": 74496 / 64, "scan": (2 * 49152 + 32768) / 64,
+                 "out": (32768 + 32768) / 64}
 
 PROFILE_FILES = {
-    "prep": "chunk_prep_prefill_T4096_H16.md",
-    "scan": "chunk_scan_prefill_T4096_H16.md",
-    "out": "chunk_out_prefill_T4096_H16.md",
-    "recurrent_step": "recurrent_step_decode_256x32_d128.md",
-    "recurrent_fwd": "recurrent_fwd_decode_256x32x8_d128.md",
-    "short_conv_fwd": "short_conv_fwd_prefill_C12288_T4096.md",
-    "recurrent_bwd": "recurrent_bwd_prefill_T4096_H16.md",
+    "prep": ("chunk_prep_prefill_T4096_H16.md", 4096 * 16),
+    "scan": ("chunk_scan_prefill_T4096_H16.md", 4096 * 16),
+    "out": ("chunk_out_prefill_T4096_H16.md", 4096 * 16),
+    "recurrent_step": ("recurrent_step_decode_256x32_d128.md", None),
+    "recurrent_fwd": ("recurrent_fwd_decode_256x32x8_d128.md", None),
+    "short_conv_fwd": ("short_conv_fwd_prefill_C12288_T4096.md", None),
+    "recurrent_bwd": ("recurrent_bwd_prefill_T4096_H16.md", None),
 }
 
 
@@ -230,7 +232,7 @@ def profiled_traffic(kernel: str):
     this workload, or None when there is none or the kernel's source has
     changed since the counters were taken (source hash recorded alongside)."""
     import hashlib
-    name = PROFILE_FILES.get(kernel)
+    name = PROFILE_FILES.get(kernel, (None, None))[0]
     if not name:
         return None
     path = os.path.join(ROOT, "profiles", name)
@@ -254,9 +256,19 @@ def profiled_traffic(kernel: str):
         return None
 
 
-def path_bytes_per_tok_head(d: int) -> int:
-    """Whole-path minimum: q, k, v, out (bf16) and log_alpha (fp32) once, beta."""
-    return 4 * 2 * d + 4 * d + 4
+def profiled_traffic_scaled(kernel: str, units: int):
+    """profiled_traffic scaled to a launch of `units` (token, head) pairs: the
+    prefill kernels' summaries come from the single-head-group workload (the
+    full-size workloads are too large for a counter capture), and their traffic
+    grows in proportion to the (chunk, head) items.  Returns (bytes, note)."""
+    t = profiled_traffic(kernel)
+    base = PROFILE_FILES.get(kernel, (None, None))[1]
+    if t is None or not base:
+        return t, None
+    if units == base:
+        return t, "ncu capture of this workload"
+    return (int(round(t * units / base)),
+            f"ncu capture at {base} (token, head) units, scaled by {units / base:g}")
 
 
 # ---------------------------------------------------------------------------
@@ -291,15 +303,21 @@ def preroll(step, seconds: float = None):
         torch.cuda.synchronize()
 
 
+REF_SAMPLE_TOKENS = 2048  # reference arm: first tokens of the long-context recipe per step
+
+
 def run_reference(args, dist: Dist):
+    """The oracle, as it stands, on the host cores: each step is the fp64 token
+    recurrence over a bounded sample of the headline workload (its first
+    REF_SAMPLE_TOKENS tokens x 32 heads, drawn on the host with the same
+    recipe), so the whole --steps/--warmup run stays within a few minutes."""
     if dist.rank != 0:
         return
     import oracle
     from kimi_delta_attention_chunkwise_gb300 import inputs
-    w = inputs.head_group_prefill()
-    Ts = 512  # bounded sample: the first 512 tokens of the workload, all 16 heads
-    sl = slice(0, Ts)
-    arrs = [w.q[sl], w.k[sl], w.v[sl], w.log_alpha[sl], w.beta[sl]]
+    Ts = REF_SAMPLE_TOKENS
+    w = inputs.long_context_prefix(Ts)
+    arrs = [w.q, w.k, w.v, w.log_alpha, w.beta]
     oracle.build()
     thr = oracle_threads()
     for _ in range(args.warmup):
@@ -311,14 +329,17 @@ def run_reference(args, dist: Dist):
         times.append(time.perf_counter() - t0)
     total = sum(times)
     value = Ts * args.steps / total
-    sample = (f"first {Ts} of {w.T} tokens x {w.H} heads of the prefill workload per step, "
-              f"fp64 token recurrence")
+    sample = (f"first {Ts} of 1048576 tokens x {w.H} heads of the long-context workload per "
+              "step (host-drawn, same recipe), fp64 token recurrence")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name + " (B=1, chunk 64, seed 1)", "sample_tokens": Ts},
+        "config": {"workload": "long_context_T1048576_H32_d128: B=1, one sequence of 1048576 "
+                               "tokens x 32 heads, d_k=d_v=128, chunk 64, bf16 q/k/v, fp32 "
+                               "log_alpha = -softplus(N(-6,1)), zero initial state, seeded",
+                   "sample_tokens": Ts},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": thr, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -372,12 +393,15 @@ def run_reference_sweep(args, dist: Dist):
         del q, k, v, la, b, s0
 
 
-def cpu_baseline(w):
-    """The oracle as it stands on the whole prefill workload, repeated to at
-    least ~10 s of wall time (bounded: at most 40 runs)."""
+def cpu_baseline():
+    """The oracle as it stands on the headline workload's 8,192-token
+    checkpoint prefix (all 32 heads, host-drawn with the same recipe),
+    repeated to about 10 s of wall time (at most 40 runs)."""
     import oracle
+    from kimi_delta_attention_chunkwise_gb300 import inputs
     oracle.build()
     thr = oracle_threads()
+    w = inputs.long_context_prefix(8192)
     runs, t_total = 0, 0.0
     while runs < 40 and (t_total < 10.0 or runs == 0):
         t0 = time.perf_counter()
@@ -386,16 +410,90 @@ def cpu_baseline(w):
         t_total += time.perf_counter() - t0
         runs += 1
     return {"value": w.T * runs / t_total, "unit": "tokens/s", "cores": thr, "kind": "oracle",
-            "sample": f"the whole workload ({w.T} tokens x {w.H} heads) x {runs} run(s), "
-                      f"fp64 token recurrence, {t_total:.1f} s"}
+            "sample": f"the headline workload's first {w.T} tokens x {w.H} heads (its parity "
+                      f"checkpoint; host-drawn, same recipe) x {runs} run(s), fp64 token "
+                      f"recurrence, {t_total:.1f} s"}
 
 
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
 
+def timed_loop(call, steps, stream, dist, flush=None):
+    """`steps` calls, each bracketed by CUDA events on the launch stream (an L2
+    flush before each when `flush` is given, outside the events); barrier and
+    synchronize on both sides.  Returns (total ms, max over ranks; per-step ms)."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    dist.barrier()
+    torch.cuda.synchronize()
+    for a, b in evs:
+        if flush is not None:
+            flush.zero_()
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    per = [a.elapsed_time(b) for a, b in evs]
+    return dist.max(sum(per)), per
+
+
+def stage_times(timed_call, reps, flush=None):
+    """Per-kernel device times (ms) of the tensor-core engine, averaged over
+    `reps` calls of kda_chunk_fwd_ws_timed (library-recorded events between
+    its kernels, which runs them one after another)."""
+    import torch
+    names = ["chunk_table", "prep", "scan", "out"]
+    acc = None
+    for _ in range(reps):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
+        for e in evs:
+            e.record()
+        if flush is not None:
+            flush.zero_()
+        n_rec = timed_call(evs)
+        torch.cuda.synchronize()
+        n = max(0, n_rec - 1)
+        t = [evs[j].elapsed_time(evs[j + 1]) for j in range(n)]
+        acc = t if acc is None else [x + y for x, y in zip(acc, t)]
+    acc = [x / reps for x in (acc or [])]
+    if len(acc) == 4:
+        return dict(zip(names, acc))
+    return {f"stage{j}": x for j, x in enumerate(acc)}
+
+
+def prefill_roofline(stages, units, call_ms, peaks, traffic=None, traffic_note=None):
+    """The roofline of one prefill launch: the dominant kernel's event time
+    against the method's algorithmic work for the units the launch processes
+    (PATH_BYTES and the dense-contraction flops per (token, head)), with the
+    whole call's figures beside it; the engine's own scratch traffic of that
+    kernel is reported apart (overhead_bytes)."""
+    dom = max(stages, key=stages.get)
+    t = stages[dom] / 1e3
+    alg_bytes = PATH_BYTES * units
+    alg_flops = PATH_FLOPS * units
+    achieved = alg_bytes / t / 1e9
+    return {
+        "kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+        "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+        "traffic_note": traffic_note, "peak_source": peaks["source"],
+        "algorithmic_bytes_per_launch": alg_bytes, "launch_ms": stages[dom],
+        "overhead_bytes": SCRATCH_BYTES.get(dom, 0) * units,
+        "overhead_note": "the engine's own scratch traffic of this kernel (images, states), "
+                         "not part of the algorithmic bytes",
+        "tensor_tflops": alg_flops / t / 1e12,
+        "tensor_frac": alg_flops / t / 1e12 / peaks["bf16_tflops"],
+        "whole_call": {"ms": call_ms, "gbs": alg_bytes / (call_ms / 1e3) / 1e9,
+                       "frac": alg_bytes / (call_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                       "tflops": alg_flops / (call_ms / 1e3) / 1e12,
+                       "tensor_frac": alg_flops / (call_ms / 1e3) / 1e12
+                       / peaks["bf16_tflops"]},
+    }
+
+
 def run_ours(args, dist: Dist):
-    import numpy as np
     import torch
     import kimi_delta_attention_chunkwise_gb300 as kda
     from kimi_delta_attention_chunkwise_gb300 import build, inputs
@@ -408,196 +506,252 @@ def run_ours(args, dist: Dist):
     dev = torch.device("cuda", dist.local_rank)
     stream = torch.cuda.current_stream()
 
-    # ---------------- prefill workload ----------------
-    w = inputs.head_group_prefill()
-    T, H, d, C = w.T, w.H, w.d_k, w.chunk_size
-    q = torch.from_numpy(w.q).to(dev, torch.bfloat16)
-    k = torch.from_numpy(w.k).to(dev, torch.bfloat16)
-    v = torch.from_numpy(w.v).to(dev, torch.bfloat16)
-    la = torch.from_numpy(w.log_alpha).to(dev)
-    beta = torch.from_numpy(w.beta).to(dev)
-    cu = torch.from_numpy(w.cu_seqlens).to(dev)
-    out = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+    # ---------------- the headline: one 1,048,576-token sequence x 32 heads ----------------
+    x = inputs.long_context_device(device=str(dev))
+    q, k, v, la, beta, cu = (x[n] for n in ("q", "k", "v", "log_alpha", "beta", "cu_seqlens"))
+    scale = x["scale"]
+    T, H, d = q.shape
+    C = 64
+    units = T * H
+    out = torch.empty_like(q)
     fin = torch.empty((1, H, d, d), dtype=torch.float32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-
-    def new_events(n):
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        for e in evs:
-            e.record(stream)  # creates the underlying CUDA event
-        return evs
-
-    MAXEV = 8
-    warm_evs = new_events(MAXEV)
-    n_rec = 0
+    call = lambda: kda.kda_chunk_fwd(q, k, v, la, beta, scale, None, cu, out, fin,
+                                     engine=args.engine)
     for _ in range(args.warmup):
-        kda.kda_chunk_fwd(q, k, v, la, beta, w.scale, None, cu, out, fin, engine=args.engine)
-        _, _, n_rec = kda.kda_chunk_fwd_ws_timed(q, k, v, la, beta, w.scale, None, cu, out, fin,
-                                                 warm_evs, engine=args.engine)
+        call()
     torch.cuda.synchronize()
-    n_stages = max(1, n_rec - 1)
-    step_evs = [new_events(MAXEV) for _ in range(args.steps)]
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    torch.cuda.synchronize()
-
-    # the headline: the public call, as a user makes it (no events between its kernels)
     sampler = ClockSampler(dist.local_rank)
     sampler.start()
-
-    def headline_step():
-        flush.zero_()
-        kda.kda_chunk_fwd(q, k, v, la, beta, w.scale, None, cu, out, fin, engine=args.engine)
-
-    preroll(headline_step)
-    dist.barrier()
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush.zero_()
-        starts[i].record(stream)
-        kda.kda_chunk_fwd(q, k, v, la, beta, w.scale, None, cu, out, fin, engine=args.engine)
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    dist.barrier()
+    preroll(call)
+    kda.kda_chunk_path_counts()  # cleared: the timed calls' paths are counted below
+    total_ms, per = timed_loop(call, args.steps, stream, dist)
     clocks = sampler.stop()
-
-    # per-kernel device times (the roofline inputs): the same call with
-    # library-recorded events between its kernels; not part of the headline
-    preroll(headline_step)
-    for i in range(args.steps):
-        flush.zero_()
-        kda.kda_chunk_fwd_ws_timed(q, k, v, la, beta, w.scale, None, cu, out, fin, step_evs[i],
-                                   engine=args.engine)
-    torch.cuda.synchronize()
-
-    step_ms = [starts[i].elapsed_time(ends[i]) for i in range(args.steps)]
-    stage_ms = [[step_evs[i][s].elapsed_time(step_evs[i][s + 1]) for s in range(n_stages)]
-                for i in range(args.steps)]
-    total_ms = dist.max(sum(step_ms))
+    paths = kda.kda_chunk_path_counts()
     ms_per_step = total_ms / args.steps
-    tokens = T * args.steps * dist.world
-    value = tokens / (total_ms / 1e3)
-    flops_step = prefill_flops_per_tok_head(d, C) * T * H
-    tflops = flops_step * args.steps * dist.world / (total_ms / 1e3) / 1e12
+    value = units // H * args.steps * dist.world / (total_ms / 1e3)
+    stages = stage_times(lambda evs: kda.kda_chunk_fwd_ws_timed(
+        q, k, v, la, beta, scale, None, cu, out, fin, evs, engine=args.engine)[2], 2)
+    traffic, tnote = profiled_traffic_scaled(max(stages, key=stages.get), units)
+    roofline = prefill_roofline(stages, units, ms_per_step, peaks, traffic, tnote)
 
-    stage_avg = [statistics.mean(s[j] for s in stage_ms) for j in range(n_stages)]
-    if n_stages == 4:
-        names = ["chunk_table", "prep", "scan", "out"]
-    else:
-        names = [f"stage{j}" for j in range(n_stages)]
-        names[-1] = "chunk_simt" if n_stages == 1 else names[-1]
-    dom = max(range(n_stages), key=lambda j: stage_avg[j])
-    work = stage_work(d, C)
-    if names[dom] in work:
-        bpt, fpt = work[names[dom]]
-    else:
-        bpt, fpt = path_bytes_per_tok_head(d), prefill_flops_per_tok_head(d, C)
-    dom_s = stage_avg[dom] / 1e3
-    achieved_gbs = bpt * T * H / dom_s / 1e9
-    roofline = {"kernel": names[dom], "bound": "hbm", "achieved": achieved_gbs,
-                "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": profiled_traffic(names[dom]),
-                "peak_source": peaks["source"],
-                "bytes_per_launch": bpt * T * H, "launch_ms": stage_avg[dom],
-                "tensor_tflops": fpt * T * H / dom_s / 1e12,
-                "tensor_frac": fpt * T * H / dom_s / 1e12 / peaks["bf16_tflops"]}
-
-    # ---------------- end to end through the public API, host buffers ----------------
-    pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
-    hq, hk, hv = (pin(a).to(torch.bfloat16).pin_memory() for a in (w.q, w.k, w.v))
-    hla, hb, hcu = pin(w.log_alpha), pin(w.beta), pin(w.cu_seqlens)
-    hout = torch.empty((T, H, d), dtype=torch.bfloat16).pin_memory()
-    hfin = torch.empty((1, H, d, d), dtype=torch.float32).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hla, hb, hcu))
+    # ---------------- end to end: the same call on host buffers ----------------
+    # Inputs go to page-locked host memory (drawn on the device above), the
+    # device copies are freed, and every step copies its inputs in and its
+    # outputs out through kda_chunk_fwd_host on one stream.
+    pinned = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+    hq, hk, hv, hla, hb, hcu = (pinned(t) for t in (q, k, v, la, beta, cu))
+    del q, k, v, la, beta, out, x, call
+    kda.binding._ws_cache.clear()
+    torch.cuda.empty_cache()
+    hout = torch.empty((T, H, d), dtype=torch.bfloat16, pin_memory=True)
+    hfin = torch.empty((1, H, d, d), dtype=torch.float32, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hla, hb, hcu))
     d2h = hout.numel() * 2 + hfin.numel() * 4
-
-    # The public host-buffer call (kda_chunk_fwd_host: copies in, prefill,
-    # copies out) on two streams with two scratch buffers and two sets of host
-    # outputs, steps alternating: one step's copies overlap the other
-    # stream's kernels.  Every step copies its inputs in and its results out.
     hshape = kda.make_shape(1, T, H, d, d, kda.KDA_DTYPE_BF16)
-    hbytes = kda.kda_chunk_fwd_host_scratch_size(hshape)
-    e2e_streams = [torch.cuda.Stream(device=dev) for _ in range(2)]
-    scratches = [torch.empty(hbytes + 256, dtype=torch.uint8, device=dev) for _ in range(2)]
-    houts = [(hout, hfin), (torch.empty_like(hout).pin_memory(),
-                            torch.empty_like(hfin).pin_memory())]
-
-    def e2e_step(i):
-        s = e2e_streams[i % 2]
-        with torch.cuda.stream(s):
-            flush.zero_()
-        kda.kda_chunk_fwd_host(hq, hk, hv, hla, hb, w.scale, None, hcu, houts[i % 2][0],
-                               houts[i % 2][1], scratch=scratches[i % 2], stream=s,
-                               engine=args.engine)
-
-    def e2e_run(n):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for s in e2e_streams:
-            s.wait_event(e0)
-        for i in range(n):
-            e2e_step(i)
-        for s in e2e_streams:
-            ev = torch.cuda.Event()
-            ev.record(s)
-            stream.wait_event(ev)
-        e1.record(stream)
-        return e0, e1
-
-    for _ in range(args.warmup):
-        e2e_run(2)
+    scratch = torch.empty(kda.kda_chunk_fwd_host_scratch_size(hshape) + 256, dtype=torch.uint8,
+                          device=dev)
+    e2e_call = lambda: kda.kda_chunk_fwd_host(hq, hk, hv, hla, hb, scale, None, hcu, hout, hfin,
+                                              scratch=scratch, stream=stream,
+                                              engine=args.engine)
+    e2e_steps = max(1, min(args.steps, 5))
+    for _ in range(min(args.warmup, 2)):
+        e2e_call()
     torch.cuda.synchronize()
-    preroll(lambda: e2e_run(2))
-    dist.barrier()
-    torch.cuda.synchronize()
-    e0, e1 = e2e_run(args.steps)
-    torch.cuda.synchronize()
-    dist.barrier()
-    e2e_ms = dist.max(e0.elapsed_time(e1))
-    e2e = {"value": T * args.steps * dist.world / (e2e_ms / 1e3), "unit": "tokens/s",
+    e2e_ms, _ = timed_loop(e2e_call, e2e_steps, stream, dist)
+    e2e = {"value": T * e2e_steps * dist.world / (e2e_ms / 1e3), "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "ms_per_step": e2e_ms / args.steps,
-           "api": "kda_chunk_fwd_host (host buffers), two streams, steps alternating"}
+           "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps,
+           "api": "kda_chunk_fwd_host (page-locked host buffers, copies in and out inside "
+                  "the timed region, one stream)"}
+    del hq, hk, hv, hla, hb, hcu, hout, hfin, scratch
+    torch.cuda.empty_cache()
 
-    # ---------------- decode rows ----------------
-    variants = run_prefill_variants(args, dist, dev, stream, w, (q, k, v, la, beta, cu))
-    backward = run_backward(args, dist, peaks, dev, stream, w, (q, k, v, la, beta, cu))
-    decode = recurrent = conv = None
+    # ---------------- the other rows ----------------
+    rows = {}
+    rows["prefill_T4096_H16"] = run_head_group(args, dist, peaks, dev, stream)
+    rows["prefill_varlen_32seq"] = run_varlen(args, dist, peaks, dev, stream)
+    rows["prefill_k3_gates"] = run_k3_gates(args, dist, dev, stream)
+    w2 = inputs.head_group_prefill()
+    t2 = lambda a, dt=None: torch.from_numpy(a).to(dev, dt)
+    dev2 = (t2(w2.q, torch.bfloat16), t2(w2.k, torch.bfloat16), t2(w2.v, torch.bfloat16),
+            t2(w2.log_alpha), t2(w2.beta), t2(w2.cu_seqlens))
+    rows["prefill_variants"] = run_prefill_variants(args, dist, dev, stream, w2, dev2)
+    rows["backward"] = run_backward(args, dist, peaks, dev, stream, w2, dev2)
     if not args.skip_decode:
-        decode = run_decode(args, dist, peaks, dev, stream)
-        recurrent = run_recurrent_fwd(args, dist, peaks, dev, stream)
-        conv = run_short_conv(args, dist, peaks, dev, stream)
+        rows["decode"] = run_decode(args, dist, peaks, dev, stream)
+        rows["recurrent_fwd"] = run_recurrent_fwd(args, dist, peaks, dev, stream)
+        rows["short_conv"] = run_short_conv(args, dist, peaks, dev, stream)
 
-    del flush
+    flops_call = PATH_FLOPS * units
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": f"{w.name}: B=1, H={H}, T={T}, d_k=d_v={d}, chunk {C}, "
-                               "bf16 q/k/v, fp32 gates/state, zero initial state, seed 1",
-                   "engine": args.engine, "l2": "flushed (256 MiB write) before each timed step",
+        "config": {"workload": f"long_context_T{T}_H{H}_d{d}: B=1, one sequence of {T} tokens "
+                               f"x {H} heads, d_k=d_v={d}, chunk {C}, bf16 q/k/v, fp32 "
+                               "log_alpha = -softplus(N(-6,1)), zero initial state, seeded",
+                   "engine": args.engine,
+                   "l2": "inputs (51.7 GB) far larger than the 129 MB L2; no flush",
                    "parallelism": "replicas" if dist.world > 1 else "single GPU"},
-        "tflops": tflops, "tensor_frac_of_bf16_peak": tflops / peaks["bf16_tflops"],
-        "path_gbs": path_bytes_per_tok_head(d) * T * H * args.steps * dist.world
-                    / (total_ms / 1e3) / 1e9,
-        "stages_ms": dict(zip(names, stage_avg)),
-        "stages_note": "per-kernel device times from a separate run with library-recorded events "
-                       "between the kernels; the headline times the plain public call",
+        "tflops": flops_call / (ms_per_step / 1e3) / 1e12,
+        "tensor_frac_of_bf16_peak": flops_call / (ms_per_step / 1e3) / 1e12
+                                    / peaks["bf16_tflops"],
+        "path_gbs": PATH_BYTES * units / (ms_per_step / 1e3) / 1e9,
+        "stages_ms": stages,
+        "stages_note": "per-kernel device times from separate calls with library-recorded "
+                       "events between the kernels (which run them one after another); the "
+                       "headline times the plain public call, whose kernels overlap",
+        "decay_paths": {"mid": paths[0], "half": paths[1], "direct": paths[2]},
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": n_stages * args.steps,
+        "gpu_launches": 4 * args.steps,
         "clocks": clocks,
-        "decode": decode,
-        "recurrent_fwd": recurrent,
-        "short_conv": conv,
-        "prefill_variants": variants,
-        "backward": backward,
     }
+    line.update(rows)
     if not args.skip_cpu_baseline and dist.rank == 0 and dist.world == 1:
-        line["cpu_baseline"] = cpu_baseline(w)
+        line["cpu_baseline"] = cpu_baseline()
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def run_head_group(args, dist, peaks, dev, stream):
+    """B=1, H=16, T=4096 (the single-head-group prefill): the public call with
+    an L2 flush (256 MiB write) before every timed step, since its ~100 MB of
+    inputs would otherwise stay in the 129 MB L2."""
+    import torch
+    import kimi_delta_attention_chunkwise_gb300 as kda
+    from kimi_delta_attention_chunkwise_gb300 import inputs
+    w = inputs.head_group_prefill()
+    T, H, d = w.T, w.H, w.d_k
+    t = lambda a, dt=None: torch.from_numpy(a).to(dev, dt)
+    q, k, v = (t(a, torch.bfloat16) for a in (w.q, w.k, w.v))
+    la, beta, cu = t(w.log_alpha), t(w.beta), t(w.cu_seqlens)
+    out = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+    fin = torch.empty((1, H, d, d), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    call = lambda: kda.kda_chunk_fwd(q, k, v, la, beta, w.scale, None, cu, out, fin,
+                                     engine=args.engine)
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    preroll(lambda: (flush.zero_(), call()))
+    total_ms, _ = timed_loop(call, args.steps, stream, dist, flush)
+    ms = total_ms / args.steps
+    stages = stage_times(lambda evs: kda.kda_chunk_fwd_ws_timed(
+        q, k, v, la, beta, w.scale, None, cu, out, fin, evs, engine=args.engine)[2],
+        max(3, min(args.steps, 10)), flush)
+    units = T * H
+    traffic, tnote = profiled_traffic_scaled(max(stages, key=stages.get), units)
+    return {"workload": f"{w.name}: B=1, H={H}, T={T}, d={d}, chunk 64, bf16, zero initial "
+                        "state, seed 1; L2 flushed before each timed step",
+            "value": T * dist.world / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+            "stages_ms": stages,
+            "roofline": prefill_roofline(stages, units, ms, peaks, traffic, tnote)}
+
+
+def run_varlen(args, dist, peaks, dev, stream):
+    """32 packed sequences, lengths ~ U[512, 8192] (136,134 tokens), H=32,
+    initial states ~ N(0, 0.02), drawn on the device; inputs far larger than
+    L2 (no flush).  Also the gradients of this workload (recurrent backward)."""
+    import torch
+    import kimi_delta_attention_chunkwise_gb300 as kda
+    from kimi_delta_attention_chunkwise_gb300 import inputs
+    x = inputs.varlen_device(device=str(dev))
+    q = x["q"]
+    T, H, d = q.shape
+    N = len(x["lengths"])
+    out = torch.empty_like(q)
+    fin = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
+    args_ = (q, x["k"], x["v"], x["log_alpha"], x["beta"], x["scale"], x["initial_state"],
+             x["cu_seqlens"])
+    call = lambda: kda.kda_chunk_fwd(*args_, out, fin, engine=args.engine)
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    preroll(call)
+    steps = max(3, min(args.steps, 10))
+    total_ms, _ = timed_loop(call, steps, stream, dist)
+    ms = total_ms / steps
+    stages = stage_times(lambda evs: kda.kda_chunk_fwd_ws_timed(
+        *args_, out, fin, evs, engine=args.engine)[2], 2)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(8)
+    do = torch.randn(q.shape, generator=gen, device=dev).to(torch.bfloat16)
+    bwd = lambda: kda.kda_recurrent_bwd(*args_, do, None)
+    bwd()
+    torch.cuda.synchronize()
+    bms, _ = timed_loop(bwd, 2, stream, dist)
+    units = T * H
+    res = {"workload": f"varlen_32seq_H{H}_d{d}: {N} packed sequences, lengths ~ U[512, 8192] "
+                       f"({T} tokens), H={H}, initial states N(0, 0.02), drawn on the device",
+           "value": T * dist.world / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+           "stages_ms": stages, "roofline": prefill_roofline(stages, units, ms, peaks),
+           "backward": {"ms_per_call": bms / 2, "tokens_per_s": T * dist.world / (bms / 2e3),
+                        "form": "recurrent, 8-token checkpoints"}}
+    del x, q, out, fin, do
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_k3_gates(args, dist, dev, stream):
+    """The single-head-group shape with K3-range gates: log alpha =
+    -5 sigmoid(g), g ~ N(0, 1) (range (-5, 0), midpoint -2.5), L2 flushed
+    before each step, and how the prep evaluated each chunk's decayed
+    products (mid-chunk reference, half-chunk references, direct)."""
+    import numpy as np
+    import torch
+    import kimi_delta_attention_chunkwise_gb300 as kda
+    from kimi_delta_attention_chunkwise_gb300 import inputs
+    w = inputs.head_group_prefill()
+    rng = np.random.default_rng(12)
+    la_np = (-5.0 / (1.0 + np.exp(-rng.standard_normal(w.log_alpha.shape)))).astype(np.float32)
+    t = lambda a, dt=None: torch.from_numpy(a).to(dev, dt)
+    q, k, v = (t(a, torch.bfloat16) for a in (w.q, w.k, w.v))
+    la, beta, cu = t(la_np), t(w.beta), t(w.cu_seqlens)
+    out = torch.empty_like(q)
+    fin = torch.empty((1, w.H, w.d_k, w.d_v), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    call = lambda: kda.kda_chunk_fwd(q, k, v, la, beta, w.scale, None, cu, out, fin,
+                                     engine=args.engine)
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    preroll(lambda: (flush.zero_(), call()))
+    kda.kda_chunk_path_counts()
+    total_ms, _ = timed_loop(call, args.steps, stream, dist, flush)
+    paths = kda.kda_chunk_path_counts()
+    ms = total_ms / args.steps
+    return {"workload": f"{w.name} with log_alpha = -5 sigmoid(N(0, 1)) (K3 gate range); "
+                        "L2 flushed before each timed step",
+            "value": w.T * dist.world / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+            "decay_paths": {"mid": paths[0], "half": paths[1], "direct": paths[2]}}
+
+
+def run_profile_case(args, dist):
+    """--profile: the single-head-group prefill (B=1, H=16, T=4096) called
+    --warmup + --steps times through the public call, no timing, no other row:
+    a small case for a profiler to capture (inputs ~100 MB, scratch ~113 MB)."""
+    import torch
+    import kimi_delta_attention_chunkwise_gb300 as kda
+    from kimi_delta_attention_chunkwise_gb300 import build, inputs
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(dist.local_rank)
+    build.build()
+    dev = torch.device("cuda", dist.local_rank)
+    w = inputs.head_group_prefill()
+    t = lambda a, dt=None: torch.from_numpy(a).to(dev, dt)
+    q, k, v = (t(a, torch.bfloat16) for a in (w.q, w.k, w.v))
+    la, beta, cu = t(w.log_alpha), t(w.beta), t(w.cu_seqlens)
+    out = torch.empty_like(q)
+    fin = torch.empty((1, w.H, w.d_k, w.d_v), dtype=torch.float32, device=dev)
+    n = args.warmup + args.steps
+    for _ in range(n):
+        kda.kda_chunk_fwd(q, k, v, la, beta, w.scale, None, cu, out, fin, engine=args.engine)
+    st = kda.kda_device_status()
+    if dist.rank == 0:
+        print(json.dumps({"profile_case": w.name, "calls": n, "device_status": st}), flush=True)
 
 
 def run_decode(args, dist, peaks, dev, stream):
@@ -774,8 +928,28 @@ def run_backward(args, dist, peaks, dev, stream, w, dev_inputs):
     # dlog_alpha (fp32), dbeta out; the final-state gradient in
     bytes_call = (4 * 2 * d + 4 * d + 4 + 4 * 4 * d + 4) * T * H + H * d * d * 4
     gbs = bytes_call / (ms / 1e3) / 1e9
-    return {"workload": f"gradients of the headline workload (1 x {H} heads x {T} tokens, d={d}, "
-                        "bf16 in, fp32 gradients), recurrent form with 8-token checkpoints",
+    # the chunkwise form on the same inputs (forward engine's factors, reverse
+    # scan on the tensor cores, the walk per 64-token chunk)
+    chunk_call = lambda: kda.kda_chunk_bwd(q, k, v, la, beta, w.scale, None, cu, do, dsf)
+    for _ in range(max(3, args.warmup)):
+        chunk_call()
+    torch.cuda.synchronize()
+    preroll(chunk_call, 0.1)
+    dist.barrier()
+    torch.cuda.synchronize()
+    evs[0].record(stream)
+    for _ in range(reps):
+        chunk_call()
+    evs[1].record(stream)
+    torch.cuda.synchronize()
+    ms_chunk = dist.max(evs[0].elapsed_time(evs[1])) / reps
+    return {"workload": f"gradients of the single-head-group workload (1 x {H} heads x {T} "
+                        "tokens, d=128, bf16 in, fp32 gradients), recurrent form with 8-token "
+                        "checkpoints",
+            "chunk_form": {"ms_per_step": ms_chunk, "value": T * dist.world / (ms_chunk / 1e3),
+                           "unit": "tokens/s",
+                           "workload": "the same gradients through kda_chunk_bwd (includes "
+                                       "its forward recompute)"},
             "value": T * dist.world / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
             "roofline": {"kernel": "recurrent_bwd", "bound": "hbm", "achieved": gbs,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -847,109 +1021,6 @@ def run_short_conv(args, dist, peaks, dev, stream):
                          "peak_source": peaks["source"]}}
 
 
-def run_sweep(args, dist: Dist):
-    """The two larger prefill workloads through the public call: 32 packed
-    sequences (lengths ~ U[512, 8192], H=32, initial states given) and one
-    1,048,576-token sequence (H=32).  Both hold far more than L2, so no flush.
-    Per-kernel times come from a second run with library-recorded events."""
-    import torch
-    import kimi_delta_attention_chunkwise_gb300 as kda
-    from kimi_delta_attention_chunkwise_gb300 import build, inputs
-
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA device")
-    torch.cuda.set_device(dist.local_rank)
-    build.build()
-    peaks = load_peaks()
-    dev = torch.device("cuda", dist.local_rank)
-    stream = torch.cuda.current_stream()
-
-    def workloads():
-        w = inputs.varlen_prefill()
-        t = lambda a, dt=None: torch.from_numpy(a).to(dev, dt) if dt else torch.from_numpy(a).to(dev)
-        yield (w.name, dict(q=t(w.q, torch.bfloat16), k=t(w.k, torch.bfloat16),
-                            v=t(w.v, torch.bfloat16), log_alpha=t(w.log_alpha), beta=t(w.beta),
-                            cu_seqlens=t(w.cu_seqlens), initial_state=t(w.initial_state),
-                            scale=w.scale), len(w.meta["lengths"]))
-        del w
-        x = inputs.long_context_device(device=str(dev))
-        x["initial_state"] = None
-        yield ("long_context_T1048576_H32_d128", x, 1)
-
-    for name, x, n_seqs in workloads():
-        q = x["q"]
-        T, H, d = q.shape
-        out = torch.empty_like(q)
-        fin = torch.empty((n_seqs, H, d, d), dtype=torch.float32, device=dev)
-        call = lambda: kda.kda_chunk_fwd(q, x["k"], x["v"], x["log_alpha"], x["beta"],
-                                         x["scale"], x["initial_state"], x["cu_seqlens"], out,
-                                         fin, engine=args.engine)
-        for _ in range(max(3, args.warmup)):
-            call()
-        torch.cuda.synchronize()
-        steps = max(1, min(args.steps, 10))
-        sampler = ClockSampler(dist.local_rank)
-        sampler.start()
-        preroll(call)
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        dist.barrier()
-        torch.cuda.synchronize()
-        start.record(stream)
-        for _ in range(steps):
-            call()
-        end.record(stream)
-        torch.cuda.synchronize()
-        dist.barrier()
-        clocks = sampler.stop()
-        ms = dist.max(start.elapsed_time(end)) / steps
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
-        for e in evs:
-            e.record(stream)
-        _, _, n_rec = kda.kda_chunk_fwd_ws_timed(q, x["k"], x["v"], x["log_alpha"], x["beta"],
-                                                 x["scale"], x["initial_state"],
-                                                 x["cu_seqlens"], out, fin, evs,
-                                                 engine=args.engine)
-        torch.cuda.synchronize()
-        names = ["chunk_table", "prep", "scan", "out"] if n_rec == 5 else \
-            [f"stage{j}" for j in range(max(0, n_rec - 1))]
-        stages = {nm: evs[j].elapsed_time(evs[j + 1]) for j, nm in enumerate(names)}
-        flops = prefill_flops_per_tok_head(d, 64) * T * H
-        path_bytes = path_bytes_per_tok_head(d) * T * H
-        line = {"sweep": name, "impl": "ours", "n_gpus": dist.world, "steps": steps,
-                "tokens": T, "heads": H, "sequences": n_seqs, "ms_per_call": ms,
-                "tokens_per_s": T * dist.world / (ms / 1e3),
-                "tflops": flops / (ms / 1e3) / 1e12,
-                "tensor_frac_of_bf16_peak": flops / (ms / 1e3) / 1e12 / peaks["bf16_tflops"],
-                "path_gbs": path_bytes / (ms / 1e3) / 1e9,
-                "path_frac_of_hbm": path_bytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
-                "stages_ms": stages, "clocks": clocks, "data": "synthetic"}
-        if n_seqs > 1:
-            # the gradients of the packed workload (d_out ~ N(0, 1), no final-state gradient)
-            gen = torch.Generator(device=dev)
-            gen.manual_seed(8)
-            do = torch.randn(q.shape, generator=gen, device=dev).to(torch.bfloat16)
-            bwd = lambda: kda.kda_recurrent_bwd(q, x["k"], x["v"], x["log_alpha"], x["beta"],
-                                                x["scale"], x["initial_state"],
-                                                x["cu_seqlens"], do, None)
-            for _ in range(2):
-                bwd()
-            torch.cuda.synchronize()
-            reps = 2
-            start.record(stream)
-            for _ in range(reps):
-                bwd()
-            end.record(stream)
-            torch.cuda.synchronize()
-            bms = dist.max(start.elapsed_time(end)) / reps
-            line["backward"] = {"ms_per_call": bms, "tokens_per_s": T * dist.world / (bms / 1e3),
-                                "form": "recurrent, 8-token checkpoints"}
-            del do
-        if dist.rank == 0:
-            print(json.dumps(line), flush=True)
-        del x, q, out, fin
-        torch.cuda.empty_cache()
-
-
 def main():
     global PREROLL_SECONDS
     args = parse_args()
@@ -961,8 +1032,8 @@ def main():
                 run_reference_sweep(args, dist)
             else:
                 run_reference(args, dist)
-        elif args.sweep:
-            run_sweep(args, dist)
+        elif args.profile:
+            run_profile_case(args, dist)
         else:
             run_ours(args, dist)
     finally:

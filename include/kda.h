@@ -147,25 +147,38 @@ typedef enum {
  * offsets give wrong results but never an out-of-bounds access.
  * Scratch: up to kda_chunk_fwd_workspace_size() bytes, taken with
  * cudaMallocAsync/cudaFreeAsync on `stream` (stream-ordered, pooled by the
- * driver).  Use kda_chunk_fwd_ws to pass caller-owned scratch instead. *
- * Kernel overlap: when its serial scan needs at most half of the SMs, the
- * tensor-core engine runs the scan and the output pass beside the
- * chunk-parallel prep (calls of at most 65,536 (chunk, head) items), or the
- * prep first and then the output pass beside the scan (larger calls).
- * Either way the kernels hand work over through flags in the scratch, and
- * the results are bit-identical to running them one after another, which is
- * what calls with more scan CTAs do.  Tools that run kernels
- * one at a time would leave the waits running out their ~1 s timeouts, so
- * the engine runs its kernels in sequence when the environment sets
- * CUDA_INJECTION64_PATH (how Nsight Compute and the compute sanitizer
- * attach) or KDA_LAUNCH_ORDER=sequential.  In the first order the same
- * applies to work that runs beside a call on other streams: calls whose
- * scans together occupy every SM (or other kernels that do) leave the prep
- * no SM, and the scan gives up after ~1 s with KDA_ERR_TIMEOUT in the device
- * status word; set KDA_LAUNCH_ORDER=sequential for such workloads.  Two or
- * three concurrent calls of the headline's size (32 scan CTAs each) are
- * fine.  In the second order the output pass starts only once every scan CTA
- * is resident, so it waits on nothing that other work can hold back.
+ * driver).  Use kda_chunk_fwd_ws to pass caller-owned scratch instead.
+ *
+ * Kernel overlap: the tensor-core engine launches, in stream order, a chunk
+ * table, the chunk-parallel prep, the serial state scan and the output pass.
+ * When the scan needs at most half of the SMs, the prep is a persistent grid
+ * whose CTAs are all running before the scan is launched; the scan follows
+ * the prep's results, and the output pass the prep's and the scan's, through
+ * flags in the scratch.  No kernel ever waits on a kernel launched after
+ * it, so the call completes under any schedule (a profiler that runs one
+ * kernel at a time, other work on other streams holding SMs): the overlap
+ * only changes how long it takes.  The results are bit-identical to the
+ * sequential order, which calls with more scan CTAs use, and which
+ * KDA_LAUNCH_ORDER=sequential forces.  Every wait inside the kernels is
+ * bounded (~1 s); a wait that gives up (a hardware fault, not a schedule)
+ * leaves KDA_ERR_TIMEOUT in the device status word (kda_device_status).
+ *
+ * Decayed products: a chunk whose cumulative log decay spans more than 80
+ * about its middle token, or about the middle of either half, is evaluated
+ * in a slower form (see kda_chunk_path_counts); any finite log_alpha <= 0
+ * is accepted.
+ *
+ * Ranges (tensor-core engine): the state entering each chunk, beta * v and
+ * the chunk's folded factors enter its MMAs as fp16 (11-bit significand,
+ * largest finite value 65504); the state itself is carried in fp32.  Entries
+ * of the state or of beta * v beyond +-65504 overflow to inf in those
+ * operands and the results are invalid; tests cover states up to 1e4 in
+ * magnitude, keys from a rank-4 subspace and repeated keys with beta = 1.
+ * The pages give beta in (0, 1] ("Kimi Unveils Delta Attention and K3
+ * Architecture Updates", sec. 2.1 and 3); the library accepts any finite
+ * beta, but with unit keys the recurrence itself only stays bounded for
+ * beta in [0, 2].  For inputs outside these ranges use KDA_ENGINE_SIMT
+ * (fp32 throughout).
  */
 kdaStatus_t kda_chunk_fwd(const void *q, const void *k, const void *v,
                           const float *log_alpha, const float *beta, float scale,
@@ -213,6 +226,41 @@ kdaStatus_t kda_chunk_fwd_ws_timed(const void *q, const void *k, const void *v,
                                    void *workspace, size_t workspace_bytes,
                                    cudaStream_t stream, cudaEvent_t *events,
                                    int32_t max_events, int32_t *n_recorded);
+
+/*
+ * kda_chunk_fwd_ws_diag -- a diagnostic form of kda_chunk_fwd_ws for tests of
+ * the failure path (no page counterpart).  It forces the tensor-core
+ * engine's overlapped order (flags between the kernels) and limits every
+ * bounded wait inside the kernels to `wait_cycles` SM clocks (<= 0: the
+ * default, ~1 s).  With withhold_prep != 0 it launches the chunk table and
+ * the state scan only: the scan's first operand flag is then never
+ * published, its waits run out after `wait_cycles`, it sets KDA_ERR_TIMEOUT
+ * in the device status word and returns without writing final_state; out is
+ * not written.  Arguments otherwise as kda_chunk_fwd_ws; KDA_ERR_UNSUPPORTED
+ * unless the problem runs on the tensor-core engine.
+ */
+kdaStatus_t kda_chunk_fwd_ws_diag(const void *q, const void *k, const void *v,
+                                  const float *log_alpha, const float *beta, float scale,
+                                  const float *initial_state, const int32_t *cu_seqlens,
+                                  void *out, float *final_state, const kdaShape_t *shape,
+                                  void *workspace, size_t workspace_bytes,
+                                  int32_t withhold_prep, int64_t wait_cycles,
+                                  cudaStream_t stream);
+
+/*
+ * kda_chunk_path_counts -- how the tensor-core engine evaluated the decayed
+ * products exp(G_i - G_j) of "Kimi Unveils Delta Attention and K3
+ * Architecture Updates", sec. 6.3 and 6.5, per (chunk, head), summed over the
+ * calls on the current device since the last read: counts[0] with one
+ * reference token in the middle of the chunk (tensor cores); counts[1] with
+ * one reference per half chunk and a third product for the block that spans
+ * both halves (tensor cores, used when the decay over half a chunk exceeds
+ * e^-80, as K3-range gates down to -5 per token reach); counts[2] with
+ * every exponential taken directly on CUDA cores (decays stronger than
+ * e^-80 within a quarter chunk).  Synchronises `stream`, then reads and
+ * clears the counters.
+ */
+kdaStatus_t kda_chunk_path_counts(uint64_t counts[3], cudaStream_t stream);
 
 /*
  * kda_chunk_fwd_host_scratch_size -- bytes of device scratch that
@@ -436,6 +484,33 @@ kdaStatus_t kda_recurrent_bwd(const void *q, const void *k, const void *v,
                               const void *d_out, const float *d_final_state, float *dq, float *dk,
                               float *dv, float *dlog_alpha, float *dbeta, float *d_initial_state,
                               const kdaShape_t *shape, cudaStream_t stream);
+
+/*
+ * kda_chunk_bwd -- the same gradients as kda_recurrent_bwd, through the
+ * chunkwise form (bf16, d_k = d_v = 128; no prologue, no value-head groups:
+ * KDA_ERR_UNSUPPORTED otherwise).
+ *
+ * Defines: the chunk form of "Kimi Unveils Delta Attention and K3
+ * Architecture Updates", sec. 6, differentiated by reverse mode.  Its one
+ * serial part is the forward scan transposed on the same per-chunk factors,
+ *     dS_c = Diag(exp(G_last)) dS_{c+1} - M'^T dS_{c+1} + Q'^T dO_c,
+ * with M' = K_end^T W and Q' = s Gamma Q - A^qk W as in kda_chunk_fwd; it
+ * runs on the tensor cores in tf32 (the gradients keep fp32 range).  With
+ * the state entering every chunk (from the forward engine) and the gradient
+ * leaving it, each 64-token chunk's gradients are computed independently
+ * (the recurrent walk of kda_recurrent_bwd, one chunk long).  Arguments,
+ * layouts and outputs as for kda_recurrent_bwd; q, k, v and log_alpha must
+ * be 16-byte aligned.  Scratch (the forward engine's, the per-chunk states,
+ * their gradients and operands: about (T / 64 + N + 1) * H * 360 KB, plus the
+ * recurrent walk's) is taken with cudaMallocAsync / cudaFreeAsync on
+ * `stream`.
+ */
+kdaStatus_t kda_chunk_bwd(const void *q, const void *k, const void *v,
+                          const float *log_alpha, const float *beta, float scale,
+                          const float *initial_state, const int32_t *cu_seqlens,
+                          const void *d_out, const float *d_final_state, float *dq, float *dk,
+                          float *dv, float *dlog_alpha, float *dbeta, float *d_initial_state,
+                          const kdaShape_t *shape, cudaStream_t stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *kda_status_string(kdaStatus_t status);

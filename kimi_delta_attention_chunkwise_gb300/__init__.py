@@ -11,7 +11,7 @@ from .binding import (  # noqa: F401
     KDA_PROLOGUE_BETA_LOGITS, KDA_PROLOGUE_GATE, KDA_PROLOGUE_L2NORM_QK,
     KdaError, kda_chunk_fwd, kda_chunk_fwd_workspace_size, kda_chunk_fwd_ws,
     kda_chunk_fwd_ws_timed, kda_chunk_fwd_host, kda_chunk_fwd_host_scratch_size,
-    kda_chunk_fwd_static,
+    kda_chunk_fwd_static, kda_chunk_fwd_ws_diag, kda_chunk_path_counts, kda_chunk_bwd,
     kda_device_status, kda_recurrent_bwd, kda_recurrent_fwd, kda_recurrent_step, kda_short_conv_fwd,
     kda_short_conv_step, kda_status_string, kdaConvShape_t, kdaShape_t, lib_path, load,
     make_shape,

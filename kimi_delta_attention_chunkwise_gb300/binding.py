@@ -15,6 +15,9 @@ The functions carry the C names:
 * ``kda_chunk_fwd_host`` / ``kda_chunk_fwd_host_scratch_size`` -- prefill on host buffers
   (copies in, prefill, copies out, all on one stream);
 * ``kda_recurrent_bwd`` -- gradients of the recurrence;
+* ``kda_chunk_fwd_ws_diag`` -- the prefill with a chosen wait limit, optionally
+  without its chunk-parallel stage (tests of the timeout path);
+* ``kda_chunk_path_counts`` -- how the decayed products were evaluated;
 * ``kda_status_string``, ``kda_device_status``.
 """
 from __future__ import annotations
@@ -97,6 +100,12 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                            ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32,
                                            ctypes.POINTER(ctypes.c_int32)]
     lib.kda_chunk_fwd_ws_timed.restype = ctypes.c_int
+    lib.kda_chunk_fwd_ws_diag.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, fp, ip, vp, fp,
+                                          shp, vp, ctypes.c_size_t, ctypes.c_int32,
+                                          ctypes.c_int64, vp]
+    lib.kda_chunk_fwd_ws_diag.restype = ctypes.c_int
+    lib.kda_chunk_path_counts.argtypes = [ctypes.POINTER(ctypes.c_uint64), vp]
+    lib.kda_chunk_path_counts.restype = ctypes.c_int
     lib.kda_chunk_fwd_static.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, fp, ip, vp, fp,
                                          shp, vp]
     lib.kda_chunk_fwd_static.restype = ctypes.c_int
@@ -120,6 +129,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.kda_recurrent_bwd.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, fp, ip, vp, fp,
                                       fp, fp, fp, fp, fp, fp, shp, vp]
     lib.kda_recurrent_bwd.restype = ctypes.c_int
+    lib.kda_chunk_bwd.argtypes = list(lib.kda_recurrent_bwd.argtypes)
+    lib.kda_chunk_bwd.restype = ctypes.c_int
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_device_status.argtypes = [vp]
@@ -377,6 +388,36 @@ def kda_chunk_fwd_ws_timed(q, k, v, log_alpha, beta, scale: float, initial_state
     return out, final_state, int(n.value)
 
 
+def kda_chunk_fwd_ws_diag(q, k, v, log_alpha, beta, scale: float, initial_state, cu_seqlens,
+                          out, final_state, *, withhold_prep: bool, wait_cycles: int = 0,
+                          chunk_size: int = 0, stream=None, out_f32: bool = False):
+    """The tensor-core prefill in its overlapped order with every bounded
+    device wait limited to ``wait_cycles`` SM clocks (C: kda_chunk_fwd_ws_diag);
+    ``withhold_prep`` launches no chunk-parallel stage, so the scan's waits run
+    out and the device status word reports KDA_ERR_TIMEOUT.  Returns
+    ``(out, final_state)``."""
+    shape, out = _prefill_args(q, k, v, log_alpha, beta, initial_state, cu_seqlens, out,
+                               final_state, chunk_size, KDA_ENGINE_TENSOR, out_f32)
+    nbytes = kda_chunk_fwd_workspace_size(shape)
+    ws = _workspace(nbytes, q.device)
+    wp = None if ws is None else (ws.data_ptr() + 255) // 256 * 256
+    _check(load().kda_chunk_fwd_ws_diag(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), float(scale),
+        _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+        ctypes.byref(shape), wp, nbytes, int(bool(withhold_prep)), int(wait_cycles),
+        _stream_handle(stream)), "kda_chunk_fwd_ws_diag")
+    return out, final_state
+
+
+def kda_chunk_path_counts(stream=None):
+    """(mid, half, direct): (chunk, head) items per evaluation path of the
+    decayed products since the last read on this device (C:
+    kda_chunk_path_counts; synchronises the stream, reads and clears)."""
+    c = (ctypes.c_uint64 * 3)()
+    _check(load().kda_chunk_path_counts(c, _stream_handle(stream)), "kda_chunk_path_counts")
+    return tuple(int(x) for x in c)
+
+
 def kda_chunk_fwd_host_scratch_size(shape: kdaShape_t) -> int:
     n = ctypes.c_size_t(0)
     _check(load().kda_chunk_fwd_host_scratch_size(ctypes.byref(shape), ctypes.byref(n)),
@@ -618,6 +659,45 @@ def kda_recurrent_bwd(q, k, v, log_alpha, beta, scale: float, initial_state=None
         _ptr(initial_state), _ptr(cu_seqlens), _ptr(d_out), _ptr(d_final_state), _ptr(dq),
         _ptr(dk), _ptr(dv), _ptr(dlog), _ptr(db), _ptr(dS0), ctypes.byref(shape),
         _stream_handle(stream)), "kda_recurrent_bwd")
+    return dq, dk, dv, dlog, db, dS0
+
+
+def kda_chunk_bwd(q, k, v, log_alpha, beta, scale: float, initial_state=None,
+                  cu_seqlens=None, d_out=None, d_final_state=None, *, stream=None,
+                  want_initial: bool = True):
+    """The same gradients through the chunkwise form (C: kda_chunk_bwd; bf16,
+    d = 128).  Returns ``(dq, dk, dv, dlog_alpha, dbeta, d_initial_state)``,
+    float32 (d_initial_state None unless ``want_initial``)."""
+    torch = _torch()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, name)
+    if q.dim() != 3:
+        raise ValueError("q must be [T, H, d_k]")
+    T, H, dk_ = q.shape
+    dv_ = v.shape[-1]
+    _require(k, "k", q.dtype, (T, H, dk_))
+    _require(v, "v", q.dtype, (T, H, dv_))
+    _require(log_alpha, "log_alpha", torch.float32, (T, H, dk_))
+    _require(beta, "beta", torch.float32, (T, H))
+    if cu_seqlens is not None:
+        _require(cu_seqlens, "cu_seqlens", torch.int32)
+        N = cu_seqlens.numel() - 1
+    else:
+        N = 1
+    _require(initial_state, "initial_state", torch.float32, (N, H, dk_, dv_))
+    _require(d_out, "d_out", q.dtype, (T, H, dv_))
+    _require(d_final_state, "d_final_state", torch.float32, (N, H, dk_, dv_))
+    f32 = dict(dtype=torch.float32, device=q.device)
+    dq, dk, dlog = (torch.empty((T, H, dk_), **f32) for _ in range(3))
+    dv = torch.empty((T, H, dv_), **f32)
+    db = torch.empty((T, H), **f32)
+    dS0 = torch.empty((N, H, dk_, dv_), **f32) if want_initial else None
+    shape = make_shape(N, T, H, dk_, dv_, _dtype_code(q))
+    _check(load().kda_chunk_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), float(scale),
+        _ptr(initial_state), _ptr(cu_seqlens), _ptr(d_out), _ptr(d_final_state), _ptr(dq),
+        _ptr(dk), _ptr(dv), _ptr(dlog), _ptr(db), _ptr(dS0), ctypes.byref(shape),
+        _stream_handle(stream)), "kda_chunk_bwd")
     return dq, dk, dv, dlog, db, dS0
 
 

@@ -134,8 +134,11 @@ kdaStatus_t cuda_status(cudaError_t e) {
     return KDA_ERR_CUDA;
 }
 
-kdaStatus_t run_plan(Plan p, void *workspace, cudaStream_t stream, StageClock *clock) {
+kdaStatus_t run_plan(Plan p, void *workspace, cudaStream_t stream, StageClock *clock,
+                     int32_t withhold_prep = 0, long long wait_cycles = 0) {
     StageClock local;
+    p.args.diag_withhold_prep = withhold_prep;
+    p.args.wait_cycles = wait_cycles;
     p.args.clock = clock ? clock : &local;
     p.args.status = device_status_ptr();
     if (!p.args.status) {
@@ -262,6 +265,34 @@ kdaStatus_t kda_chunk_fwd_ws(const void *q, const void *k, const void *v,
     return kda_chunk_fwd_ws_timed(q, k, v, log_alpha, beta, scale, initial_state, cu_seqlens,
                                   out, final_state, shape, workspace, workspace_bytes, stream,
                                   nullptr, 0, nullptr);
+}
+
+kdaStatus_t kda_chunk_fwd_ws_diag(const void *q, const void *k, const void *v,
+                                  const float *log_alpha, const float *beta, float scale,
+                                  const float *initial_state, const int32_t *cu_seqlens,
+                                  void *out, float *final_state, const kdaShape_t *shape,
+                                  void *workspace, size_t workspace_bytes,
+                                  int32_t withhold_prep, int64_t wait_cycles,
+                                  cudaStream_t stream) {
+    Plan p;
+    kdaStatus_t st = plan_chunk(q, k, v, log_alpha, beta, scale, initial_state, cu_seqlens,
+                                out, final_state, shape, &p);
+    if (st != KDA_SUCCESS) return st;
+    if (!p.use_tc) return KDA_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < p.workspace ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return KDA_ERR_INVALID_ARG;
+    return run_plan(p, workspace, stream, nullptr, withhold_prep != 0 ? 1 : 0,
+                    wait_cycles > 0 ? (long long)wait_cycles : 0);
+}
+
+kdaStatus_t kda_chunk_path_counts(uint64_t counts[3], cudaStream_t stream) {
+    if (!counts) return KDA_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    return cuda_status(chunk_path_counts(counts, true));
 }
 
 kdaStatus_t kda_chunk_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
@@ -504,6 +535,57 @@ kdaStatus_t kda_recurrent_bwd(const void *q, const void *k, const void *v,
     }
     a.workspace = ws;
     const cudaError_t e = launch_recurrent_bwd(a, stream);
+    const cudaError_t f = cudaFreeAsync(ws, stream);
+    return cuda_status(e != cudaSuccess ? e : f);
+}
+
+kdaStatus_t kda_chunk_bwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                          const float *beta, float scale, const float *initial_state,
+                          const int32_t *cu_seqlens, const void *d_out,
+                          const float *d_final_state, float *dq, float *dk, float *dv,
+                          float *dlog_alpha, float *dbeta, float *d_initial_state,
+                          const kdaShape_t *shape, cudaStream_t stream) {
+    kdaStatus_t st = check_shape(shape, false);
+    if (st != KDA_SUCCESS) return st;
+    if (group_size(shape) != 1 || shape->prologue != 0 || shape->dtype != KDA_DTYPE_BF16 ||
+        shape->d_k != 128)
+        return KDA_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale)) return KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens && shape->num_seqs != 1) return KDA_ERR_INVALID_ARG;
+    if (shape->total_tokens > 0) {
+        // the forward engine's tensor maps want 16-byte aligned q, k, v, log_alpha
+        const void *need16[] = {q, k, v, log_alpha};
+        for (const void *p : need16)
+            if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+        const void *need[] = {beta, dq, dk, dv, dlog_alpha, dbeta};
+        for (const void *p : need)
+            if (!p || !aligned4(p)) return KDA_ERR_INVALID_ARG;
+        if (d_out && !aligned4(d_out)) return KDA_ERR_INVALID_ARG;
+    }
+    const void *states[] = {initial_state, d_final_state, d_initial_state};
+    for (const void *p : states)
+        if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens && !aligned4(cu_seqlens)) return KDA_ERR_INVALID_ARG;
+    BwdArgs a;
+    a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.scale = scale;
+    a.initial_state = initial_state; a.cu_seqlens = cu_seqlens; a.d_out = d_out;
+    a.d_final_state = d_final_state; a.dq = dq; a.dk = dk; a.dv = dv; a.dlog_alpha = dlog_alpha;
+    a.dbeta = dbeta; a.d_initial_state = d_initial_state;
+    a.N = shape->num_seqs; a.T = shape->total_tokens; a.H = shape->num_heads;
+    a.D = shape->d_k; a.dtype = shape->dtype;
+    int *status = device_status_ptr();
+    if (!status) {
+        (void)cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    const size_t bytes = chunk_bwd_workspace_bytes(a.N, a.T, a.H);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes, stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    a.workspace = ws;
+    const cudaError_t e = launch_chunk_bwd(a, status, stream);
     const cudaError_t f = cudaFreeAsync(ws, stream);
     return cuda_status(e != cudaSuccess ? e : f);
 }

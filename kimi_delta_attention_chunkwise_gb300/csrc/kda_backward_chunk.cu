@@ -1,0 +1,578 @@
+// kda_backward_chunk.cu -- the chunkwise backward (training), first form.
+//
+// The pages derive no gradients ("Kimi Unveils Delta Attention and K3
+// Architecture Updates", sec. 6: the chunkwise form serves training).  The
+// chunk form of sec. 6 differentiated by reverse mode has one serial part,
+// the forward scan transposed on the same folded factors:
+//
+//   dS_c = Diag(exp(G_last)) dS_{c+1} - M'^T dS_{c+1} + Q'^T dO_c
+//
+// and, once S_c and dS_{c+1} are known at every chunk boundary, each chunk's
+// gradients are independent of the others.  This form:
+//   1. runs the forward engine (its workspace keeps every chunk's f16 M',
+//      Q', exp(G_last) and the f16 state S_c entering the chunk);
+//   2. state_rows_kernel: S_c as fp32 rows;
+//   3. chunk_bwd_aux_kernel: -M'^T as a tf32 operand image and
+//      X_c = Q'^T dO_c (one tcgen05 kind::tf32 product) per (chunk, head);
+//   4. chunk_rscan_kernel: the reverse scan, one kind::tf32 product per chunk
+//      on the chain, writing dS_{c+1} at every boundary and dS at every
+//      sequence start (the initial-state gradient);
+//   5. the recurrent backward walk per 64-token chunk (16-column tiles), from
+//      S_c and dS_{c+1}.
+// Every product that carries a gradient is tf32 (fp32 range): f16 operands
+// lose gradients of training size to underflow.
+#include <cstdint>
+
+#include <cuda_bf16.h>
+
+#include "kda_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace kda {
+namespace {
+using namespace tc;
+
+
+constexpr int AD = 128, AC = 64;
+constexpr uint32_t A_IMG_STRIDE = 74752, A_IMG_MN = 0, A_IMG_Q0 = 49152, A_IMG_Q1 = 65536,
+                   A_IMG_GB = 73728;
+constexpr long long kAWait = 2000000000LL;
+
+struct AuxSmem {
+    uint8_t mt[4 * 16384];   // -M'^T staging (tf32), then the bulk copy out
+    uint8_t qt[2 * 16384];   // A: Q'^T, 128 rows x 64 tokens, 2 panels
+    uint8_t dt[2 * 16384];   // B: dO^T, 128 rows (d_v) x 64 tokens, 2 panels
+    uint8_t mn[2 * 16384];   // -M' f16 panels (bulk copy in)
+    uint8_t q0[8192], q1[8192];  // Q' f16 panels (keys 0..63, 64..127)
+    float gl[AD];
+    uint64_t bar_in, bar_mma;
+    uint32_t tmem;
+};
+constexpr size_t kAuxSmem = sizeof(AuxSmem) + 1024;
+static_assert(kAuxSmem <= 227 * 1024, "aux shared memory");
+
+__device__ __forceinline__ float f16_at(const uint8_t *panel, uint32_t row, uint32_t col) {
+    return __half2float(*reinterpret_cast<const __half *>(panel + sw128_offset(row, col)));
+}
+
+__global__ void __launch_bounds__(256, 1)
+chunk_bwd_aux_kernel(const uint8_t *__restrict__ img_base, const int2 *__restrict__ chunk_tok,
+                     const __nv_bfloat16 *__restrict__ d_out, uint8_t *__restrict__ mt_img,
+                     float *__restrict__ x_tiles, float *__restrict__ glv, int32_t H,
+                     int *status) {
+    extern __shared__ uint8_t smem_raw[];
+    AuxSmem &sm = *reinterpret_cast<AuxSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int32_t c = (int32_t)(blockIdx.x / (unsigned)H), h = (int32_t)(blockIdx.x % (unsigned)H);
+    const int2 tok = chunk_tok[c];
+    const int32_t t0 = tok.x, L = tok.y;
+    if (L <= 0) return;
+    const size_t item = (size_t)c * H + h;
+    const uint8_t *img = img_base + item * A_IMG_STRIDE;
+
+    if (tid == 0) {
+        mbar_init(&sm.bar_in, 1);
+        mbar_init(&sm.bar_mma, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&sm.bar_in, 2 * 16384 + 2 * 8192 + AD * 4);
+        bulk_g2s(sm.mn, img + A_IMG_MN, 2 * 16384, &sm.bar_in);
+        bulk_g2s(sm.q0, img + A_IMG_Q0, 8192, &sm.bar_in);
+        bulk_g2s(sm.q1, img + A_IMG_Q1, 8192, &sm.bar_in);
+        bulk_g2s(sm.gl, img + A_IMG_GB, AD * 4, &sm.bar_in);
+    }
+    if (warp == 0) {
+        tmem_alloc(&sm.tmem, 128);
+        tmem_relinquish();
+    }
+    // dO^T (B operand): element (n, i) = dO[t0 + i][h][n], rows i >= L zero.
+    // Thread -> column n = tid % 128, tokens i = tid / 128, +2, ...
+    {
+        const int n = tid & 127;
+        for (int i = tid >> 7; i < AC; i += 2) {
+            const float x = (d_out && i < L)
+                                ? __bfloat162float(d_out[((size_t)(t0 + i) * H + h) * AD + n])
+                                : 0.f;
+            *reinterpret_cast<float *>(sm.dt + (i >> 5) * 16384u + sw128_offset_f32(n, i & 31)) = x;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem;
+    bool ok = mbar_wait_bounded(&sm.bar_in, 0, kAWait);
+    if (ok) {
+        if (tid < 128) {
+            // -M'^T row i = column i of -M': (-M')[j][i] at panel i/64, row j
+            const int i = tid;
+            const uint8_t *src = sm.mn + (i >> 6) * 16384u;
+#pragma unroll 4
+            for (int p = 0; p < 4; ++p) {
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    const int j = p * 32 + c4 * 4;
+                    float4 v;
+                    v.x = f16_at(src, j, i & 63);
+                    v.y = f16_at(src, j + 1, i & 63);
+                    v.z = f16_at(src, j + 2, i & 63);
+                    v.w = f16_at(src, j + 3, i & 63);
+                    *reinterpret_cast<float4 *>(sm.mt + p * 16384u + sw128_chunk(i, c4)) = v;
+                }
+            }
+        } else {
+            // Q'^T row d = column d of Q': Q'[i][d] at the panel of d, row i
+            const int d = tid - 128;
+            const uint8_t *src = d < 64 ? sm.q0 : sm.q1;
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    const int i = p * 32 + c4 * 4;
+                    float4 v;
+                    v.x = f16_at(src, i, d & 63);
+                    v.y = f16_at(src, i + 1, d & 63);
+                    v.z = f16_at(src, i + 2, d & 63);
+                    v.w = f16_at(src, i + 3, d & 63);
+                    *reinterpret_cast<float4 *>(sm.qt + p * 16384u + sw128_chunk(d, c4)) = v;
+                }
+            }
+        }
+    } else if (tid == 0) {
+        atomicExch(status, (int)KDA_ERR_TIMEOUT);
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        mma_panels<true>(tmem, smem_u32(sm.qt), 16384, smem_u32(sm.dt), 16384, 8,
+                         idesc_tf32_f32(128, 128), false);
+        mma_commit(&sm.bar_mma);
+        bulk_s2g(mt_img + item * (size_t)(4 * 16384), sm.mt, 4 * 16384);
+        bulk_s2g(glv + item * AD, sm.gl, AD * 4);
+        bulk_commit_group();
+    }
+    if (ok) ok = mbar_wait_bounded(&sm.bar_mma, 0, kAWait);
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    if (ok) {
+        // warp w: TMEM lanes 32 (w % 4).., columns 64 (w / 4)..: X rows, two tiles
+        const int quad = warp & 3, half = warp >> 2, d = quad * 32 + (tid & 31);
+        float v[32];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int vt = half * 2 + t;
+            tmem_ld32(tmem_addr(tmem, quad * 32, vt * 32), v);
+            float *dst = x_tiles + ((item * 4 + vt) * AD + d) * 32;
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4 *>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        }
+    } else if (tid == 0) {
+        atomicExch(status, (int)KDA_ERR_TIMEOUT);
+    }
+    if (tid == 0) bulk_wait_group_read<0>();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+// S_c in fp32 rows from the forward scan's f16 state images (one MN-major
+// SW128 image of 128 key rows x 64 value columns per value tile, 16 KB):
+// rows [item][128][128].  Thread -> (row k, 8 columns).
+__global__ void __launch_bounds__(256)
+state_rows_kernel(const uint8_t *__restrict__ sst, const int2 *__restrict__ chunk_tok,
+                  float *__restrict__ rows, size_t n_items, int32_t H) {
+    const size_t item = blockIdx.x;
+    if (item >= n_items) return;
+    if (chunk_tok[item / (size_t)H].y <= 0) {
+        for (int idx = threadIdx.x; idx < AD * AD; idx += 256) rows[item * AD * AD + idx] = 0.f;
+        return;
+    }
+    for (int idx = threadIdx.x; idx < AD * 16; idx += 256) {
+        const int k = idx >> 4, c8 = idx & 15, vt = c8 >> 3, ch = c8 & 7;
+        const uint8_t *img = sst + (item * 2 + vt) * 16384u;
+        const uint4 u = *reinterpret_cast<const uint4 *>(img + sw128_chunk(k, ch));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        float *dst = rows + (item * AD + k) * AD + vt * 64 + ch * 8;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const __half2 hv = *reinterpret_cast<const __half2 *>(&w[e]);
+            dst[2 * e] = __low2float(hv);
+            dst[2 * e + 1] = __high2float(hv);
+        }
+    }
+}
+
+
+
+
+constexpr int RD = 128, RC = 64, RBV = 32, RNT = RD / RBV, RSTAGE = 2;
+constexpr uint32_t MT_BYTES = RD * RD * 4;
+constexpr uint32_t XT_BYTES = RD * RBV * 4;
+constexpr uint32_t DS_IMG = RBV * RD * 4;
+constexpr uint32_t GL_BYTES = RD * 4;
+constexpr int kRThreads = 256;
+constexpr uint32_t kRTmemCols = 2 * RBV;  // D2 ping-pong
+constexpr long long kRWait = 2000000000LL;
+
+struct RScanSmem {
+    uint8_t mt[RSTAGE][MT_BYTES];  // 1024-aligned: offsets 0, 64 KB
+    uint8_t sb[2][DS_IMG];         // 128 KB, 144 KB
+    float xs[RSTAGE][RD * RBV];
+    float gl[RSTAGE][RD];
+    uint64_t full[RSTAGE];   // stage loaded (bulk copies -> issuer, compute)
+    uint64_t empty[RSTAGE];  // stage consumed: MMA commit + 128 compute threads
+    uint64_t ready_s;        // dS operand written (compute -> issuer)
+    uint64_t mma_s;          // product complete (commit -> compute)
+    uint64_t ready_w[2];     // dS operand written, for writer 0 / 1
+    uint32_t tmem;
+    volatile int32_t copied[2];
+    volatile int32_t issued;
+    volatile int32_t abort_flag;
+};
+constexpr size_t kRSmem = sizeof(RScanSmem) + 1024;
+static_assert(kRSmem <= 227 * 1024, "reverse scan shared memory");
+static_assert(offsetof(RScanSmem, sb) % 1024 == 0, "operand images 1024-aligned");
+
+__device__ __forceinline__ bool rbarrier_or(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, 1, 128, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+
+__global__ void __launch_bounds__(kRThreads, 1)
+chunk_rscan_kernel(const uint8_t *__restrict__ mt_img, const float *__restrict__ x_tiles,
+                   const float *__restrict__ glv, const float *__restrict__ d_final,
+                   uint8_t *__restrict__ ds_img, float *__restrict__ ds_rows,
+                   float *__restrict__ d_initial,
+                   const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_off,
+                   int32_t N, int32_t T, int32_t H, int *status) {
+    extern __shared__ uint8_t smem_raw[];
+    RScanSmem &sm = *reinterpret_cast<RScanSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t seq = blockIdx.x / RNT, vt = blockIdx.x % RNT, h = blockIdx.y;
+    if (seq >= N) return;
+    int32_t ta = 0, tb = T;
+    if (cu) {
+        ta = min(max(cu[seq], 0), T);
+        tb = min(max(cu[seq + 1], ta), T);
+    }
+    const int32_t n_chunks = (tb - ta + RC - 1) / RC;
+    const int32_t c_begin = chunk_off[seq];
+    const size_t st_off = (((size_t)seq * H + h) * RD + (tid & 127)) * RD + (size_t)vt * RBV;
+
+    float dS[RBV];
+    if (tid < 128 && d_final) {
+#pragma unroll
+        for (int j = 0; j < RBV; j += 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(d_final + st_off + j);
+            dS[j] = x.x; dS[j + 1] = x.y; dS[j + 2] = x.z; dS[j + 3] = x.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < RBV; ++j) dS[j] = 0.f;
+    }
+
+    bool ok = true;
+    if (n_chunks > 0) {
+        if (tid == 0) {
+            for (int i = 0; i < RSTAGE; ++i) {
+                mbar_init(&sm.full[i], 1);
+                mbar_init(&sm.empty[i], 1 + 128);
+            }
+            mbar_init(&sm.ready_s, 128);
+            mbar_init(&sm.mma_s, 1);
+            mbar_init(&sm.ready_w[0], 128);
+            mbar_init(&sm.ready_w[1], 128);
+            sm.copied[0] = 0;
+            sm.copied[1] = 0;
+            sm.issued = 0;
+            sm.abort_flag = 0;
+            fence_mbar_init();
+        }
+        if (warp == 0) {
+            tmem_alloc(&sm.tmem, kRTmemCols);
+            tmem_relinquish();
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        const uint32_t tmem = sm.tmem;
+        constexpr uint32_t IDESC = idesc_tf32_f32(128, RBV);  // A and B K-major
+        // step n processes chunk c = c_begin + n_chunks - 1 - n
+        auto item_of = [&](int32_t n) {
+            return (size_t)(c_begin + n_chunks - 1 - n) * H + h;
+        };
+
+        if (warp == 4) {
+            // -------- producer: -M'^T, the X tile and gl of each chunk --------
+            if (lane == 0) {
+                for (int32_t n = 0; n < n_chunks; ++n) {
+                    const int stg = n % RSTAGE;
+                    if (n >= RSTAGE) {
+                        if (!mbar_wait_bounded(&sm.empty[stg], (uint32_t)(n / RSTAGE - 1) & 1u,
+                                               kRWait) ||
+                            sm.abort_flag) {
+                            sm.abort_flag = 1;
+                            break;
+                        }
+                    }
+                    const size_t item = item_of(n);
+                    mbar_arrive_expect_tx(&sm.full[stg], MT_BYTES + XT_BYTES + GL_BYTES);
+                    bulk_g2s(sm.mt[stg], mt_img + item * MT_BYTES, MT_BYTES, &sm.full[stg]);
+                    bulk_g2s(sm.xs[stg], x_tiles + (item * RNT + vt) * (size_t)(RD * RBV),
+                             XT_BYTES, &sm.full[stg]);
+                    bulk_g2s(sm.gl[stg], glv + item * RD, GL_BYTES, &sm.full[stg]);
+                    sm.issued = n + 1;
+                }
+            }
+            __syncwarp();
+        } else if (warp == 5) {
+            // -------- MMA issuer: D2[n & 1] = (-M'^T) dS_{c+1} --------
+            if (lane == 0) {
+                int32_t done = 0;
+                for (int32_t n = 0; n < n_chunks; ++n) {
+                    const int stg = n % RSTAGE;
+                    const bool got =
+                        mbar_wait_bounded(&sm.full[stg], (uint32_t)(n / RSTAGE) & 1u, kRWait) &&
+                        mbar_wait_bounded(&sm.ready_s, (uint32_t)n & 1u, kRWait);
+                    if (!got || sm.abort_flag) {
+                        sm.abort_flag = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    mma_panels<true>(tmem + (uint32_t)(n & 1) * RBV, smem_u32(sm.mt[stg]), 16384,
+                                     smem_u32(sm.sb[n & 1]), 4096, 16, IDESC, false);
+                    mma_commit(&sm.mma_s);
+                    mma_commit(&sm.empty[stg]);
+                    done = n + 1;
+                }
+                // every product issued is complete before TMEM and the shared
+                // memory go away (they complete in order: wait for the last)
+                if (done > 0 &&
+                    !mbar_wait_bounded(&sm.mma_s, (uint32_t)(done - 1) & 1u, kRWait))
+                    sm.abort_flag = 1;
+            }
+            __syncwarp();
+        } else if (warp >= 6) {
+            // -------- writers: dS_{c+1} images out, steps b, b + 2, ... --------
+            const int b = warp - 6;
+            if (lane == 0) {
+                for (int32_t n = b; n < n_chunks; n += 2) {
+                    if (!mbar_wait_bounded(&sm.ready_w[b], (uint32_t)(n >> 1) & 1u, kRWait) ||
+                        sm.abort_flag) {
+                        sm.abort_flag = 1;
+                        break;
+                    }
+                    if (ds_img) {
+                        bulk_s2g(ds_img + (item_of(n) * RNT + vt) * (size_t)DS_IMG,
+                                 sm.sb[n & 1], DS_IMG);
+                        bulk_commit_group();
+                        bulk_wait_group_read<0>();
+                    }
+                    sm.copied[b] = (n >> 1) + 1;
+                }
+                bulk_wait_group_all();
+            }
+            __syncwarp();
+        } else {
+            // -------- compute: thread = key row k --------
+            const int k = tid;
+            auto put_state = [&](int32_t n) {
+                if (ds_rows) {
+                    float *dst = ds_rows + (item_of(n) * RD + k) * RD + (size_t)vt * RBV;
+#pragma unroll
+                    for (int j = 0; j < RBV; j += 4)
+                        *reinterpret_cast<float4 *>(dst + j) =
+                            make_float4(dS[j], dS[j + 1], dS[j + 2], dS[j + 3]);
+                }
+                uint8_t *img = sm.sb[n & 1] + (k >> 5) * 4096u;
+#pragma unroll
+                for (int j = 0; j < RBV; ++j)
+                    *reinterpret_cast<float *>(img + sw128_offset_f32(j, k & 31)) = to_tf32(dS[j]);
+                fence_proxy_async();
+            };
+            put_state(0);
+            for (int32_t n = 0; n < n_chunks; ++n) {
+                if (rbarrier_or(sm.abort_flag != 0)) break;
+                tc_fence_before();
+                mbar_arrive(&sm.ready_s);
+                mbar_arrive(&sm.ready_w[n & 1]);
+                const int stg = n % RSTAGE;
+                if (!mbar_wait_bounded(&sm.full[stg], (uint32_t)(n / RSTAGE) & 1u, kRWait))
+                    sm.abort_flag = 1;
+                const float g = sm.gl[stg][k];
+                float x[RBV];
+#pragma unroll
+                for (int j = 0; j < RBV; j += 4) {
+                    const float4 v = *reinterpret_cast<const float4 *>(&sm.xs[stg][k * RBV + j]);
+                    x[j] = v.x; x[j + 1] = v.y; x[j + 2] = v.z; x[j + 3] = v.w;
+                }
+                mbar_arrive(&sm.empty[stg]);
+                if (!mbar_wait_bounded(&sm.mma_s, (uint32_t)n & 1u, kRWait)) sm.abort_flag = 1;
+                tc_fence_after();
+                {
+                    float d2[32];
+                    tmem_ld32(tmem_addr(tmem + (uint32_t)(n & 1) * RBV, warp * 32, 0), d2);
+#pragma unroll
+                    for (int j = 0; j < RBV; ++j) dS[j] = fmaf(g, dS[j], d2[j] + x[j]);
+                }
+                if (n + 1 < n_chunks) {
+                    // sb[(n + 1) & 1] holds step n - 1's operand: wait for its copy out
+                    if (n >= 1) {
+                        const int wb = (n - 1) & 1;
+                        const int32_t need = ((n - 1) >> 1) + 1;
+                        if (sm.copied[wb] < need) {
+                            const long long t0 = clock64();
+                            while (sm.copied[wb] < need) {
+                                if (clock64() - t0 > kRWait) {
+                                    sm.abort_flag = 1;
+                                    break;
+                                }
+                            }
+                        }
+                    }
+                    put_state(n + 1);
+                }
+            }
+        }
+        __syncthreads();
+        if (sm.abort_flag) {
+            ok = false;
+            if (tid == 0) {
+                atomicExch(status, (int)KDA_ERR_TIMEOUT);
+                const int32_t iss = sm.issued;
+                for (int32_t j = max(iss - RSTAGE, 0); j < iss; ++j)
+                    (void)mbar_wait_bounded(&sm.full[j % RSTAGE], (uint32_t)(j / RSTAGE) & 1u,
+                                            kRWait);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tmem, kRTmemCols);
+        if (!ok) return;
+    }
+    if (d_initial && tid < 128) {
+#pragma unroll
+        for (int j = 0; j < RBV; j += 4)
+            *reinterpret_cast<float4 *>(d_initial + st_off + j) =
+                make_float4(dS[j], dS[j + 1], dS[j + 2], dS[j + 3]);
+    }
+}
+
+
+// seg[c] = first token of chunk c (T past the last chunk), seg[max] = T:
+// the chunks as sequences of the recurrent walk.
+__global__ void chunk_segments_kernel(const int2 *__restrict__ chunk_tok, int32_t *__restrict__ seg,
+                                      int32_t n, int32_t T) {
+    for (int32_t c = blockIdx.x * blockDim.x + threadIdx.x; c <= n; c += gridDim.x * blockDim.x)
+        seg[c] = (c < n && chunk_tok[c].y > 0) ? chunk_tok[c].x : T;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct ChunkBwdLayout {
+    size_t fwd, out, rows, mt, x, gl, dsrows, seg, bwd, total;
+};
+
+ChunkBwdLayout chunk_bwd_layout(int32_t N, int32_t T, int32_t H) {
+    const size_t maxc = (size_t)T / 64 + (size_t)N + 1, items = maxc * H;
+    ChunkBwdLayout L;
+    size_t off = 0;
+    auto take = [&](size_t n) {
+        const size_t o = off;
+        off += align256(n);
+        return o;
+    };
+    L.fwd = take(chunk_tc_workspace_bytes(N, T, H));
+    L.out = take((size_t)T * H * AD * 2);
+    L.rows = take(items * AD * AD * 4);
+    L.mt = take(items * MT_BYTES);
+    L.x = take(items * RNT * (size_t)XT_BYTES);
+    L.gl = take(items * AD * 4);
+    L.dsrows = take(items * AD * AD * 4);
+    L.seg = take((maxc + 1) * 4);
+    L.bwd = take(recurrent_bwd_tiles16_workspace_bytes((int32_t)maxc, T, H));
+    L.total = off;
+    return L;
+}
+
+}  // namespace
+
+size_t chunk_bwd_workspace_bytes(int32_t N, int32_t T, int32_t H) {
+    return chunk_bwd_layout(N, T, H).total;
+}
+
+cudaError_t launch_chunk_bwd(const BwdArgs &a, int *status, cudaStream_t stream) {
+    if (a.D != AD || a.dtype != KDA_DTYPE_BF16 || !a.workspace) return cudaErrorInvalidValue;
+    if (a.T == 0) {
+        // no tokens: the initial-state gradient is the final-state gradient
+        if (a.d_initial_state) {
+            const size_t n = (size_t)a.N * a.H * AD * AD * sizeof(float);
+            return a.d_final_state ? cudaMemcpyAsync(a.d_initial_state, a.d_final_state, n,
+                                                     cudaMemcpyDeviceToDevice, stream)
+                                   : cudaMemsetAsync(a.d_initial_state, 0, n, stream);
+        }
+        return cudaSuccess;
+    }
+    const ChunkBwdLayout L = chunk_bwd_layout(a.N, a.T, a.H);
+    uint8_t *ws = static_cast<uint8_t *>(a.workspace);
+    // 1. the forward engine, for its images (outputs into scratch)
+    StageClock clock;
+    ChunkArgs f = {};
+    f.q = a.q; f.k = a.k; f.v = a.v; f.log_alpha = a.log_alpha; f.beta = a.beta;
+    f.scale = a.scale; f.initial_state = a.initial_state; f.cu_seqlens = a.cu_seqlens;
+    f.out = ws + L.out; f.final_state = nullptr;
+    f.N = a.N; f.T = a.T; f.H = a.H; f.D = AD; f.C = 64; f.G = 1; f.pro = 0;
+    f.gbias = nullptr; f.galog = nullptr; f.dtype = KDA_DTYPE_BF16; f.out_f32 = 0;
+    f.status = status; f.clock = &clock;
+    cudaError_t e = launch_chunk_tc(f, ws + L.fwd, L.out - L.fwd, stream);
+    if (e != cudaSuccess) return e;
+    const ChunkScratchView view = chunk_tc_scratch_view(ws + L.fwd, a.N, a.T, a.H);
+    const size_t maxc = view.max_chunks, items = maxc * a.H;
+    float *rows = reinterpret_cast<float *>(ws + L.rows);
+    float *dsrows = reinterpret_cast<float *>(ws + L.dsrows);
+    int32_t *seg = reinterpret_cast<int32_t *>(ws + L.seg);
+    // 2. S_c as fp32 rows
+    state_rows_kernel<<<(unsigned)items, 256, 0, stream>>>(view.sst, view.chunk_tok, rows, items,
+                                                           a.H);
+    // 3. -M'^T, X_c and exp(G_last) per (chunk, head)
+    e = cudaFuncSetAttribute(chunk_bwd_aux_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kAuxSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(chunk_rscan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kRSmem);
+    if (e != cudaSuccess) return e;
+    chunk_bwd_aux_kernel<<<(unsigned)items, 256, kAuxSmem, stream>>>(
+        view.img, view.chunk_tok, static_cast<const __nv_bfloat16 *>(a.d_out), ws + L.mt,
+        reinterpret_cast<float *>(ws + L.x), reinterpret_cast<float *>(ws + L.gl), a.H, status);
+    // 4. the reverse scan
+    chunk_rscan_kernel<<<dim3((unsigned)(a.N * RNT), (unsigned)a.H), kRThreads, kRSmem, stream>>>(
+        ws + L.mt, reinterpret_cast<const float *>(ws + L.x),
+        reinterpret_cast<const float *>(ws + L.gl), a.d_final_state, nullptr, dsrows,
+        a.d_initial_state, a.cu_seqlens, view.chunk_off, a.N, a.T, a.H, status);
+    // 5. the recurrent walk per chunk, from S_c and dS_{c+1}
+    chunk_segments_kernel<<<(unsigned)((maxc + 256) / 256), 256, 0, stream>>>(
+        view.chunk_tok, seg, (int32_t)maxc, a.T);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    BwdArgs w = a;
+    w.N = (int32_t)maxc;
+    w.cu_seqlens = seg;
+    w.initial_state = rows;
+    w.d_final_state = dsrows;
+    w.d_initial_state = nullptr;
+    w.workspace = ws + L.bwd;
+    return launch_recurrent_bwd_tiles16(w, stream);
+}
+
+}  // namespace kda

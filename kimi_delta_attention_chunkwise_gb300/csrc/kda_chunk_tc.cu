@@ -74,8 +74,10 @@ constexpr int C = 64;         // chunk
 constexpr int BV = 64;        // value columns per scan CTA
 constexpr int NT = D / BV;    // value tiles per head
 constexpr int MID = 32;       // reference row of the factorised decay
-constexpr float kSpanLimit = 80.f;
-constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
+// A decay factor exp(G_i - G_r) of the factorised products must stay within
+// fp32 range: |G_i - G_r| <= 80, i.e. 80 log2(e) = 115.4 in the base-2 units
+// the prep keeps G in.
+constexpr float kSpanLimit2 = 115.f;
 
 // Per-(chunk, head) scratch image: the scan's operands for one chunk, already
 // in its shared-memory layout (f16, K-major, 128-byte swizzle), so the scan
@@ -151,7 +153,8 @@ __device__ __forceinline__ int32_t find_seq(const int32_t *off, int32_t N, int32
 // ---------------------------------------------------------------------------
 // 1. chunk table (CTA 0): chunk_off[s] = number of chunks before sequence s,
 //    and chunk_tok[c] = {first token, length} of chunk c ({0, 0} past the
-//    last chunk); every CTA also clears a share of the n_ready image flags.
+//    last chunk); every CTA also clears a share of the n_ready image and
+//    state flags.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t *cu, int32_t N,
                                                            int32_t T, int32_t *chunk_off,
@@ -216,10 +219,20 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t *cu, in
 
 
 // ---------------------------------------------------------------------------
-// 2. per-(chunk, head) preparation
+// 2. per-(chunk, head) preparation: a persistent kernel
 // ---------------------------------------------------------------------------
-// 256 threads: thread t owns key channel d = t % 128 for the tokens of one
-// half chunk (t / 128).  Shared memory, with regions reused once their
+// One CTA per SM it runs on, holding two independent workers of 256 threads
+// (each with its own shared memory, mbarriers, named barrier and 256 TMEM
+// columns).  Worker w of W takes items (chunk, head) w, w + W, w + 2W, ...
+// -- heads fastest, the order in which the scan consumes the images; w runs
+// over the CTAs first, so a partial last round spreads over the SMs.  A
+// kernel launched after this one starts only once every CTA of this grid is
+// running, so it may wait on any item's image: the item's worker is running.
+// A worker's image stores drain while its next item's tiles load: thread 0
+// waits for them (and publishes the flag) only after issuing those loads.
+//
+// Within a worker, thread t owns key channel d = t % 128 for the tokens of
+// one half chunk (t / 128).  Shared memory, with regions reused once their
 // first tenant is done:
 //   a1: g tile (TMA, f32 [64][128]) -> tf32 [K_tilde ; Q_tilde], 128 rows x
 //       128 K in 4 panels (64 KB) -> R, X (= A^kk) and the solve's block
@@ -227,24 +240,45 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t *cu, in
 //       beside them -> W^T (f16, at 0) -> the staging of the image's -M', P'
 //       and Q' panels, in image order;
 //   b1: k and q tiles (TMA, bf16 [64][128] each) -> tf32 K_hat, 64 rows x
-//       128 K in 4 panels (32 KB) (slow path: G f32 [64][128]) -> A^kk and
+//       128 K in 4 panels (32 KB) (direct path: G f32 [64][128]) -> A^kk and
 //       A^kk^T (f16, 8 KB each) and (beta Gamma K)^T (f16, 128 x 64, 16 KB)
 //       -> Z staging (at 0).
-constexpr int kPrepThreads = 256;
+//
+// The decayed products exp(G_i - G_j) (j <= i, so at most 1) are split as
+// exp(G_i - G_r) * exp(G_r - G_j) about a reference token r, in one of three
+// ways per item:
+//   mid   -- r = 32 for the whole chunk, when every |G_i - G_32| <= 80: one
+//            tf32 MMA [K_tilde ; Q_tilde] K_hat^T;
+//   half  -- r = 16 for the first half's rows and columns, r = 48 for the
+//            second's, when every |G_i - G_r| <= 80 within its half (log
+//            decays down to -5 per token, the K3 gate's range): the same MMA
+//            gives both diagonal half blocks; the block of second-half rows
+//            and first-half columns comes from a second MMA whose B operand
+//            is K_hat about r = 48 for the first half's tokens (exponent
+//            G_48 - G_j <= 0);
+//   direct-- every exp(G_i - G_j) on CUDA cores (decays stronger than e^-80
+//            within a quarter chunk).
+constexpr int kPrepWorkerThreads = 256;
+constexpr int kPrepWorkers = 2;
+constexpr int kPrepThreads = kPrepWorkerThreads * kPrepWorkers;
 constexpr int HALF = C / 2;
 
 struct PrepSmem {
     uint8_t a1[4 * 16384];
     uint8_t b1[4 * 8192];
     float beta[C];
-    float gcarry[D];   // G at token 31 of each channel
-    float gmid[D];     // G at the reference token MID
-    float glast[D];    // G at the chunk's last token
+    // cumulative log decays in base 2 (G log2 e) of each channel at:
+    float gcarry[D];   // token 31
+    float gmid[D];     // the reference token MID
+    float gh1[D];      // token 48 (the second half's reference)
+    float glast[D];    // the chunk's last token
     float knorm[C];    // 1 / |k_i|, 1 / |q_i| (L2 prologue; else 1)
     float qnorm[C];
     uint64_t bar_in, bar_mma;
-    uint32_t tmem;
+    uint64_t published;  // thread 0: the item whose image flag is still to go up (~0: none)
+    uint32_t n_path[3];  // items per decay path (thread 0)
 };
+constexpr size_t kPrepWorkerBytes = (sizeof(PrepSmem) + 1023) & ~size_t(1023);
 constexpr uint32_t kOffX = C * (C + 1) * 4;        // X after R inside a1
 constexpr uint32_t kOffTb = 2 * C * (C + 1) * 4;   // block products after X
 constexpr uint32_t kOffAqk = 40960;                // A^qk (f16) inside a1
@@ -255,6 +289,34 @@ static_assert(kOffTb + 32 * 33 * 4 <= kOffAqk, "solve scratch below A^qk");
 constexpr uint32_t kInBytes = 2 * C * D * 2 + C * D * 4;  // k, q bf16 + g f32 tiles
 static_assert(kOffTb + 32 * 33 * 4 <= 4 * 16384, "a1 reuse");
 static_assert(MID == HALF, "the reference token opens the second half");
+
+// Named barrier over one worker's 256 threads (ids 1 and 2; 0 is the CTA's),
+// with the id as an immediate (a warp-uniform branch picks it).
+template <int ID>
+__device__ __forceinline__ void wbar_id() {
+    asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(kPrepWorkerThreads) : "memory");
+}
+__device__ __forceinline__ void wbar(int id) {
+    if (id == 1) wbar_id<1>();
+    else wbar_id<2>();
+}
+// The same barrier, returning the OR of a predicate over the worker.
+template <int ID>
+__device__ __forceinline__ bool wbar_or_id(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "n"(ID), "n"(kPrepWorkerThreads)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ bool wbar_or(int id, bool pred) {
+    return id == 1 ? wbar_or_id<1>(pred) : wbar_or_id<2>(pred);
+}
 
 __device__ __forceinline__ void store_row_f16_image(uint8_t *img, uint32_t row,
                                                     const float (&v)[64]) {
@@ -289,9 +351,9 @@ __device__ __forceinline__ void store_quarter_f16_image(uint8_t *img, uint32_t r
 // square, L^-1 = [A^-1 0; -D^-1 B A^-1  D^-1].  Level 1 applies it inside the
 // two 32 x 32 diagonal blocks (16 x 16 halves), level 2 to the whole 64 x 64
 // (32 x 32 halves); B is the block of R below the diagonal.  The products run
-// over full K ranges: X is zero above its diagonal.  256 threads.
+// over full K ranges: X is zero above its diagonal.  One worker (256 threads).
 __device__ __forceinline__ void solve_level16(float (*R)[C + 1], float (*X)[C + 1],
-                                              float (*Tb)[33], int tid) {
+                                              float (*Tb)[33], int tid, int bid) {
     // thread -> 32 x 32 block p, one row of its lower-left 16 x 16, two columns
     const int p = tid >> 7, t = tid & 127, o = 32 * p;
     const int lr = t >> 3, lc = (t & 7) * 2;
@@ -305,7 +367,7 @@ __device__ __forceinline__ void solve_level16(float (*R)[C + 1], float (*X)[C + 
     }
     Tb[16 * p + lr][lc] = a0;
     Tb[16 * p + lr][lc + 1] = a1;
-    __syncthreads();
+    wbar(bid);
     float b0 = 0.f, b1 = 0.f;  // (D^-1 B A^-1)[r][c]
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
@@ -315,11 +377,11 @@ __device__ __forceinline__ void solve_level16(float (*R)[C + 1], float (*X)[C + 
     }
     X[r][c] = -b0;
     X[r][c + 1] = -b1;
-    __syncthreads();
+    wbar(bid);
 }
 
 __device__ __forceinline__ void solve_level32(float (*R)[C + 1], float (*X)[C + 1],
-                                              float (*Tb)[33], int tid) {
+                                              float (*Tb)[33], int tid, int bid) {
     // thread -> 2 x 2 tile of the lower-left 32 x 32: rows 32 + rr.., columns cc..
     const int rr = (tid >> 4) * 2, cc = (tid & 15) * 2, r = 32 + rr;
     float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;  // B A^-1
@@ -336,7 +398,7 @@ __device__ __forceinline__ void solve_level32(float (*R)[C + 1], float (*X)[C + 
     Tb[rr][cc + 1] = a01;
     Tb[rr + 1][cc] = a10;
     Tb[rr + 1][cc + 1] = a11;
-    __syncthreads();
+    wbar(bid);
     float b00 = 0.f, b01 = 0.f, b10 = 0.f, b11 = 0.f;  // D^-1 B A^-1
 #pragma unroll 8
     for (int m = 0; m < 32; ++m) {
@@ -351,25 +413,31 @@ __device__ __forceinline__ void solve_level32(float (*R)[C + 1], float (*X)[C + 
     X[r][cc + 1] = -b01;
     X[r + 1][cc] = -b10;
     X[r + 1][cc + 1] = -b11;
-    __syncthreads();
+    wbar(bid);
 }
 
 struct PrepMaps {
     CUtensorMap q, k, g;  // [T, H, D] viewed as {D, H, T}, box {128, 1, 64}
 };
 
+// Items of each path for the decayed products (mid, half, direct), per device;
+// kda_chunk_path_counts() reads and clears them.
+__device__ unsigned long long g_path_counts[3];
+
 // PRO: the kernel applies an input prologue (compiled out when false)
 template <bool PRO>
-__global__ void __launch_bounds__(kPrepThreads, 2)
+__global__ void __launch_bounds__(kPrepThreads, 1)
 chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__restrict__ q,
                   const __nv_bfloat16 *__restrict__ k, const float *__restrict__ beta,
-                  float scale, const int32_t *__restrict__ cu, int32_t N, int32_t T, int32_t H,
-                  int32_t grp, int32_t pro, const float *__restrict__ gbias,
-                  const float *__restrict__ galog, Scratch sc, int32_t streamed,
-                  int32_t prefetch_dist, int *status) {
+                  float scale, int32_t H, int32_t grp, int32_t pro,
+                  const float *__restrict__ gbias, const float *__restrict__ galog, Scratch sc,
+                  uint32_t n_items, int32_t flags, long long wait_cycles, int *status) {
     extern __shared__ uint8_t smem_raw[];
-    PrepSmem &sm = *reinterpret_cast<PrepSmem *>(
+    uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int wk = threadIdx.x / kPrepWorkerThreads;
+    PrepSmem &sm = *reinterpret_cast<PrepSmem *>(base + wk * kPrepWorkerBytes);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + kPrepWorkers * kPrepWorkerBytes);
     float(*R)[C + 1] = reinterpret_cast<float(*)[C + 1]>(sm.a1);
     float(*X)[C + 1] = reinterpret_cast<float(*)[C + 1]>(sm.a1 + kOffX);
     float(*Tb)[33] = reinterpret_cast<float(*)[33]>(sm.a1 + kOffTb);
@@ -381,222 +449,251 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
     uint8_t *wt = sm.a1;              // W^T, f16 panel (after the solve)
     uint8_t *zst = sm.b1;             // Z staging (after the MMAs that read A^kk)
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // After the chunk table as a programmatic dependent: wait for the table.
-    // Streamed (launched behind the scan, which waits on the image flags):
-    // the table is complete before the scan starts, and waiting here for the
-    // scan would never end.
-    if (!streamed) pdl_wait_primaries();
-    pdl_launch_dependents();   // the next kernel may start setting up once every prep CTA runs
-    // heads fastest: the images of chunk 0 of every head come first, in the
-    // order the scan consumes them
-    const int32_t c = (int32_t)(blockIdx.x / (unsigned)H), h = (int32_t)(blockIdx.x % (unsigned)H);
-    const int2 tok = sc.chunk_tok[c];
-    const int32_t t0 = tok.x, L = tok.y;
-    if (L <= 0) return;
-    const size_t ch = (size_t)c * H + h;
-    uint8_t *img = sc.img + ch * IMG_STRIDE;
-    float *gb = reinterpret_cast<float *>(img + IMG_GB);
-    const int32_t hq = h / grp;                 // the q/k head of this value head's group
-    const size_t rs = (size_t)(H / grp) * D;    // q/k token stride
-
-    // Stream the chunk's k, q and log-decay tiles in (one tensor load each).
+    const int tid = threadIdx.x % kPrepWorkerThreads, warp = tid >> 5, lane = tid & 31;
+    const int bid = 1 + wk;           // the worker's named barrier
+    // The chunk table (and the cleared flags) first; then the
+    // next kernel may start: it only waits on items of this running grid.
+    pdl_wait_primaries();
+    pdl_launch_dependents();
     if (tid == 0) {
         mbar_init(&sm.bar_in, 1);
         mbar_init(&sm.bar_mma, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(&sm.bar_in, kInBytes);
-        tma_load_3d(sm.b1, &maps.k, 0, hq, t0, &sm.bar_in);
-        tma_load_3d(sm.b1 + C * D * 2, &maps.q, 0, hq, t0, &sm.bar_in);
-        tma_load_3d(sm.a1, &maps.g, 0, h, t0, &sm.bar_in);
+        sm.n_path[0] = sm.n_path[1] = sm.n_path[2] = 0u;
+        sm.published = ~0ull;
     }
-    if (warp == 0) {
-        tmem_alloc(&sm.tmem, 256);
+    if (threadIdx.x < 32) {
+        tmem_alloc(tmem_slot, 256 * kPrepWorkers);  // both workers' columns at once
         tmem_relinquish();
-        tc_fence_before();
     }
-    // beta: loaded now, stored once the tiles are in (its latency hides under theirs)
-    float beta_i = 0.f;
-    if (tid < C && tid < L) beta_i = beta[(size_t)(t0 + tid) * H + h];
+    tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = sm.tmem;
-    if (tid == 32) {
-        // The item that will take this CTA's place about one full wave of
-        // resident CTAs later: its tiles go to L2 now (while this CTA waits
-        // for its own; off the path to the barrier above).
-        const unsigned ahead = blockIdx.x + (unsigned)prefetch_dist;
-        if (prefetch_dist > 0 && ahead < gridDim.x) {
-            const int32_t ca = (int32_t)(ahead / (unsigned)H), ha = (int32_t)(ahead % (unsigned)H);
-            const int2 ta = sc.chunk_tok[ca];
-            if (ta.y > 0) {
-                tma_prefetch_l2_3d(&maps.k, 0, ha / grp, ta.x);
-                tma_prefetch_l2_3d(&maps.q, 0, ha / grp, ta.x);
-                tma_prefetch_l2_3d(&maps.g, 0, ha, ta.x);
-            }
-        }
-    }
-    bool ok = mbar_wait_bounded(&sm.bar_in, 0, kWaitCycles);
-    if (tid < C) {
-        if (PRO && (pro & KDA_PROLOGUE_BETA_LOGITS) && tid < L) beta_i = pro_sigmoid(beta_i);
-        sm.beta[tid] = beta_i;  // read after the next block barrier
-        gb[128 + tid] = beta_i;
-    }
-
+    const uint32_t tmem = *tmem_slot + (uint32_t)wk * 256u;
+    const uint32_t stride = gridDim.x * (uint32_t)kPrepWorkers;  // items between a worker's own
     const int d = tid & (D - 1), hf = tid >> 7, i0 = hf * HALF;
     const bool l2 = PRO && (pro & KDA_PROLOGUE_L2NORM_QK);
     const bool gate = PRO && (pro & KDA_PROLOGUE_GATE);
-    const float sens = gate ? __expf(galog[h]) : 0.f;
-    const float gbias_d = gate ? gbias[(size_t)h * D + d] : 0.f;
-    uint32_t kp[HALF / 2], qp[HALF / 2];
-    float G[HALF];
-    {
-        const float *gs = reinterpret_cast<const float *>(sm.a1);
-        unsigned short *ks = reinterpret_cast<unsigned short *>(sm.b1);
-        unsigned short *qs = ks + C * D;
-        // The L2 prologue, on the tiles in shared memory: warp w finds 1/|k_i| and
-        // 1/|q_i| of tokens 8w .. 8w + 7 and rescales their rows in place as fp16
-        // (11-bit significand: the tf32 and fp16 operands built from them keep
-        // their precision; bf16 here cost a visible share of the error budget).
-        // The stored inverse norms serve the CUDA-core path, which reads the
-        // raw rows from global memory.
-        if (l2) {
-#pragma unroll 1
-            for (int i = warp * 8; i < warp * 8 + 8; ++i) {
-                uint2 *kr = reinterpret_cast<uint2 *>(ks + i * D + lane * 4);
-                uint2 *qr = reinterpret_cast<uint2 *>(qs + i * D + lane * 4);
-                const uint2 kw = *kr, qw = *qr;
-                const uint32_t kv4[2] = {kw.x, kw.y}, qv4[2] = {qw.x, qw.y};
-                float kf[4], qf[4], kk = 0.f, qq = 0.f;
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    kf[2 * e] = __uint_as_float(kv4[e] << 16);
-                    kf[2 * e + 1] = __uint_as_float(kv4[e] & 0xFFFF0000u);
-                    qf[2 * e] = __uint_as_float(qv4[e] << 16);
-                    qf[2 * e + 1] = __uint_as_float(qv4[e] & 0xFFFF0000u);
-                }
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    kk = fmaf(kf[e], kf[e], kk);
-                    qq = fmaf(qf[e], qf[e], qq);
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    kk += __shfl_xor_sync(0xffffffffu, kk, o);
-                    qq += __shfl_xor_sync(0xffffffffu, qq, o);
-                }
-                const float rk = rsqrtf(kk + kL2Eps), rq = rsqrtf(qq + kL2Eps);
-                *kr = make_uint2(pack_f16x2(kf[0] * rk, kf[1] * rk), pack_f16x2(kf[2] * rk, kf[3] * rk));
-                *qr = make_uint2(pack_f16x2(qf[0] * rq, qf[1] * rq), pack_f16x2(qf[2] * rq, qf[3] * rq));
-                if (lane == 0) {
-                    sm.knorm[i] = rk;
-                    sm.qnorm[i] = rq;
+    uint32_t in_phase = 0, mma_phase = 0;
+    bool ok = true;
+
+    for (uint32_t item = (uint32_t)wk * gridDim.x + blockIdx.x; item < n_items;
+         item += stride) {
+        const int32_t c = (int32_t)(item / (uint32_t)H), h = (int32_t)(item % (uint32_t)H);
+        const int2 tok = sc.chunk_tok[c];
+        const int32_t t0 = tok.x, L = tok.y;
+        if (L <= 0) break;  // past the last chunk: so is every later item
+        const size_t ch = (size_t)c * H + h;
+        uint8_t *img = sc.img + ch * IMG_STRIDE;
+        float *gb = reinterpret_cast<float *>(img + IMG_GB);
+        const int32_t hq = h / grp;                 // the q/k head of this value head's group
+        const size_t rs = (size_t)(H / grp) * D;    // q/k token stride
+
+        // Stream the chunk's k, q and log-decay tiles in (one tensor load each),
+        // once the previous item's first group of image stores (-M' from a1,
+        // Z from b1) has left shared memory; its second group reads the upper
+        // half of a1, which the tiles do not touch.
+        if (tid == 0) {
+            bulk_wait_group_read<1>();
+            mbar_arrive_expect_tx(&sm.bar_in, kInBytes);
+            tma_load_3d(sm.b1, &maps.k, 0, hq, t0, &sm.bar_in);
+            tma_load_3d(sm.b1 + C * D * 2, &maps.q, 0, hq, t0, &sm.bar_in);
+            tma_load_3d(sm.a1, &maps.g, 0, h, t0, &sm.bar_in);
+            // the previous image out of shared memory (its upper half is
+            // rewritten below) and, with flags, complete in global memory:
+            // publish it
+            if (flags) bulk_wait_group_all();
+            else bulk_wait_group_read<0>();
+            if (flags && sm.published != ~0ull) {
+                fence_proxy_async_global();
+                flag_release(sc.ready + sm.published, 1u);
+            }
+            sm.published = ~0ull;
+        } else if (tid == 32) {
+            // this worker's next item goes to L2 early
+            const uint32_t ahead = item + stride;
+            if (ahead < n_items) {
+                const int32_t ca = (int32_t)(ahead / (uint32_t)H),
+                              ha = (int32_t)(ahead % (uint32_t)H);
+                const int2 ta = sc.chunk_tok[ca];
+                if (ta.y > 0) {
+                    tma_prefetch_l2_3d(&maps.k, 0, ha / grp, ta.x);
+                    tma_prefetch_l2_3d(&maps.q, 0, ha / grp, ta.x);
+                    tma_prefetch_l2_3d(&maps.g, 0, ha, ta.x);
                 }
             }
-            __syncthreads();
         }
-#pragma unroll
-        for (int jj = 0; jj < HALF / 2; ++jj) {
-            const int ia = i0 + 2 * jj, ib = ia + 1;
-            const uint32_t k0 = ia < L ? ks[ia * D + d] : 0u, k1 = ib < L ? ks[ib * D + d] : 0u;
-            const uint32_t q0 = ia < L ? qs[ia * D + d] : 0u, q1 = ib < L ? qs[ib * D + d] : 0u;
-            kp[jj] = k0 | (k1 << 16);
-            qp[jj] = q0 | (q1 << 16);
+        // beta: loaded now, stored once the tiles are in (its latency hides under theirs)
+        float beta_i = 0.f;
+        if (tid < C && tid < L) beta_i = beta[(size_t)(t0 + tid) * H + h];
+        const float sens = gate ? __expf(galog[h]) : 0.f;
+        const float gbias_d = gate ? gbias[(size_t)h * D + d] : 0.f;
+        ok = mbar_wait_bounded(&sm.bar_in, in_phase, wait_cycles) && ok;
+        in_phase ^= 1u;
+        if (tid < C) {
+            if (PRO && (pro & KDA_PROLOGUE_BETA_LOGITS) && tid < L) beta_i = pro_sigmoid(beta_i);
+            sm.beta[tid] = beta_i;  // read after the next worker barrier
+            gb[128 + tid] = beta_i;
         }
-        float acc = 0.f;
-#pragma unroll
-        for (int ii = 0; ii < HALF; ++ii) {
-            float lg = (i0 + ii < L) ? gs[(i0 + ii) * D + d] : 0.f;
-            if (gate && i0 + ii < L) lg = pro_gate(lg, sens, gbias_d);
-            acc += lg;
-            G[ii] = acc;
-        }
-    }
-    if (hf == 0) sm.gcarry[d] = G[HALF - 1];
-    __syncthreads();  // staging consumed; carries published
-    if (hf == 1) {
-        const float carry = sm.gcarry[d];
-#pragma unroll
-        for (int ii = 0; ii < HALF; ++ii) G[ii] += carry;
-        sm.gmid[d] = G[0];
-        sm.glast[d] = G[HALF - 1];
-    }
-    __syncthreads();
-    const float Gm = sm.gmid[d], Gl = sm.glast[d];
-    float span = 0.f;
-#pragma unroll
-    for (int ii = 0; ii < HALF; ++ii) span = fmaxf(span, fabsf(G[ii] - Gm));
-    const int slow = __syncthreads_or(!(span <= kSpanLimit));
-    // k and q of this thread's tokens: bf16 inputs, or fp16 once the L2
-    // prologue has normalised them
-    auto unpack = [&](uint32_t w, int hi) {
-        if (l2)
-            return __half2float(__ushort_as_half((unsigned short)(hi ? (w >> 16) : (w & 0xFFFFu))));
-        return __uint_as_float(hi ? (w & 0xFFFF0000u) : (w << 16));
-    };
-    auto kval = [&](int ii) { return unpack(kp[ii >> 1], ii & 1); };
-    auto qval = [&](int ii) { return unpack(qp[ii >> 1], ii & 1); };
-    uint32_t mma_phase = 0;
 
-    if (slow) {
-        // CUDA-core path: every exp(G_i - G_j) taken directly (exponent <= 0).
-        float *Gs = reinterpret_cast<float *>(sm.b1);  // [64][128]
+        uint32_t kp[HALF / 2], qp[HALF / 2];
+        float G[HALF];  // cumulative log decay of this thread's tokens, base 2 (G log2 e)
+        {
+            const float *gs = reinterpret_cast<const float *>(sm.a1);
+            unsigned short *ks = reinterpret_cast<unsigned short *>(sm.b1);
+            unsigned short *qs = ks + C * D;
+            // The L2 prologue, on the tiles in shared memory: warp w finds 1/|k_i|
+            // and 1/|q_i| of tokens 8w .. 8w + 7 and rescales their rows in place
+            // as fp16 (11-bit significand: the tf32 and fp16 operands built from
+            // them keep their precision; bf16 here cost a visible share of the
+            // error budget).  The stored inverse norms serve the direct path,
+            // which reads the raw rows from global memory.
+            if (l2) {
+#pragma unroll 1
+                for (int i = warp * 8; i < warp * 8 + 8; ++i) {
+                    uint2 *kr = reinterpret_cast<uint2 *>(ks + i * D + lane * 4);
+                    uint2 *qr = reinterpret_cast<uint2 *>(qs + i * D + lane * 4);
+                    const uint2 kw = *kr, qw = *qr;
+                    const uint32_t kv4[2] = {kw.x, kw.y}, qv4[2] = {qw.x, qw.y};
+                    float kf[4], qf[4], kk = 0.f, qq = 0.f;
 #pragma unroll
-        for (int ii = 0; ii < HALF; ++ii) Gs[(i0 + ii) * D + d] = G[ii];
-        __syncthreads();
-        const __nv_bfloat16 *kc = k + ((size_t)t0 * (H / grp) + hq) * D;
-        const __nv_bfloat16 *qc = q + ((size_t)t0 * (H / grp) + hq) * D;
-        for (int i = warp; i < C; i += kPrepThreads / 32) {
-            for (int j = 0; j <= i; ++j) {
-                float r = 0.f, a = 0.f;
-                if (i < L) {
+                    for (int e = 0; e < 2; ++e) {
+                        kf[2 * e] = __uint_as_float(kv4[e] << 16);
+                        kf[2 * e + 1] = __uint_as_float(kv4[e] & 0xFFFF0000u);
+                        qf[2 * e] = __uint_as_float(qv4[e] << 16);
+                        qf[2 * e + 1] = __uint_as_float(qv4[e] & 0xFFFF0000u);
+                    }
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const int dd = lane + 32 * m;
-                        const float w = __expf(Gs[i * D + dd] - Gs[j * D + dd]) *
-                                        __bfloat162float(kc[j * rs + dd]);
-                        r += w * __bfloat162float(kc[i * rs + dd]);
-                        a += w * __bfloat162float(qc[i * rs + dd]);
+                    for (int e = 0; e < 4; ++e) {
+                        kk = fmaf(kf[e], kf[e], kk);
+                        qq = fmaf(qf[e], qf[e], qq);
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        kk += __shfl_xor_sync(0xffffffffu, kk, o);
+                        qq += __shfl_xor_sync(0xffffffffu, qq, o);
+                    }
+                    const float rk = rsqrtf(kk + kL2Eps), rq = rsqrtf(qq + kL2Eps);
+                    *kr = make_uint2(pack_f16x2(kf[0] * rk, kf[1] * rk),
+                                     pack_f16x2(kf[2] * rk, kf[3] * rk));
+                    *qr = make_uint2(pack_f16x2(qf[0] * rq, qf[1] * rq),
+                                     pack_f16x2(qf[2] * rq, qf[3] * rq));
+                    if (lane == 0) {
+                        sm.knorm[i] = rk;
+                        sm.qnorm[i] = rq;
                     }
                 }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    r += __shfl_xor_sync(0xffffffffu, r, o);
-                    a += __shfl_xor_sync(0xffffffffu, a, o);
-                }
-                if (lane == 0) {
-                    // the L2 prologue rescales the raw dot products
-                    const float nk = l2 ? sm.knorm[i] * sm.knorm[j] : 1.f;
-                    const float nq = l2 ? sm.qnorm[i] * sm.knorm[j] : 1.f;
-                    R[i][j] = (j < i) ? sm.beta[i] * r * nk : 0.f;
-                    X[i][j] = scale * a * nq;
-                }
+                wbar(bid);
             }
-            for (int j = i + 1 + lane; j < C; j += 32) {
-                R[i][j] = 0.f;
-                X[i][j] = 0.f;
+#pragma unroll
+            for (int jj = 0; jj < HALF / 2; ++jj) {
+                const int ia = i0 + 2 * jj, ib = ia + 1;
+                const uint32_t k0 = ia < L ? ks[ia * D + d] : 0u, k1 = ib < L ? ks[ib * D + d] : 0u;
+                const uint32_t q0 = ia < L ? qs[ia * D + d] : 0u, q1 = ib < L ? qs[ib * D + d] : 0u;
+                kp[jj] = k0 | (k1 << 16);
+                qp[jj] = q0 | (q1 << 16);
+            }
+            float acc = 0.f;
+#pragma unroll
+            for (int ii = 0; ii < HALF; ++ii) {
+                float lg = (i0 + ii < L) ? gs[(i0 + ii) * D + d] : 0.f;
+                if (gate && i0 + ii < L) lg = pro_gate(lg, sens, gbias_d);
+                acc = fmaf(lg, kLog2e, acc);
+                G[ii] = acc;
             }
         }
-        __syncthreads();
-        if (tid < C) {
-            float row[64];
+        if (hf == 0) sm.gcarry[d] = G[HALF - 1];
+        wbar(bid);  // staging consumed; carries published
+        if (hf == 1) {
+            const float carry = sm.gcarry[d];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) row[j] = X[tid][j];
-            store_row_f16_image(aqk, tid, row);
+            for (int ii = 0; ii < HALF; ++ii) G[ii] += carry;
+            sm.gmid[d] = G[0];
+            sm.gh1[d] = G[HALF / 2];
+            sm.glast[d] = G[HALF - 1];
         }
-        __syncthreads();
-    }
+        wbar(bid);
+        const float Gm = sm.gmid[d], Gl = sm.glast[d];
+        // the path: mid reference if it stays in range, else one per half, else direct
+        const float Gh = G[HALF / 2];  // this half's reference token (16 or 48)
+        float span = 0.f;
+#pragma unroll
+        for (int ii = 0; ii < HALF; ++ii) span = fmaxf(span, fabsf(G[ii] - Gm));
+        int path = wbar_or(bid, !(span <= kSpanLimit2)) ? 1 : 0;
+        if (path) {
+            span = 0.f;
+#pragma unroll
+            for (int ii = 0; ii < HALF; ++ii) span = fmaxf(span, fabsf(G[ii] - Gh));
+            path = wbar_or(bid, !(span <= kSpanLimit2)) ? 2 : 1;
+        }
+        if (tid == 0) ++sm.n_path[path];
+        const float Gr = path == 1 ? Gh : Gm;  // reference of this thread's tokens
+        // k and q of this thread's tokens: bf16 inputs, or fp16 once the L2
+        // prologue has normalised them
+        auto unpack = [&](uint32_t w, int hi) {
+            if (l2)
+                return __half2float(
+                    __ushort_as_half((unsigned short)(hi ? (w >> 16) : (w & 0xFFFFu))));
+            return __uint_as_float(hi ? (w & 0xFFFF0000u) : (w << 16));
+        };
+        auto kval = [&](int ii) { return unpack(kp[ii >> 1], ii & 1); };
+        auto qval = [&](int ii) { return unpack(qp[ii >> 1], ii & 1); };
 
-    // The decay-factorised tf32 operands, token by token.
-    {
-        const float e_m = __expf(Gm), e_lm = __expf(Gl - Gm);
-        if (!slow) {
+        if (path == 2) {
+            // Direct path: every exp(G_i - G_j) taken directly (exponent <= 0).
+            float *Gs = reinterpret_cast<float *>(sm.b1);  // [64][128]
+#pragma unroll
+            for (int ii = 0; ii < HALF; ++ii) Gs[(i0 + ii) * D + d] = G[ii];
+            wbar(bid);
+            const __nv_bfloat16 *kc = k + ((size_t)t0 * (H / grp) + hq) * D;
+            const __nv_bfloat16 *qc = q + ((size_t)t0 * (H / grp) + hq) * D;
+            for (int i = warp; i < C; i += kPrepWorkerThreads / 32) {
+                for (int j = 0; j <= i; ++j) {
+                    float r = 0.f, a = 0.f;
+                    if (i < L) {
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const int dd = lane + 32 * m;
+                            const float w = exp2_approx(Gs[i * D + dd] - Gs[j * D + dd]) *
+                                            __bfloat162float(kc[j * rs + dd]);
+                            r += w * __bfloat162float(kc[i * rs + dd]);
+                            a += w * __bfloat162float(qc[i * rs + dd]);
+                        }
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        r += __shfl_xor_sync(0xffffffffu, r, o);
+                        a += __shfl_xor_sync(0xffffffffu, a, o);
+                    }
+                    if (lane == 0) {
+                        // the L2 prologue rescales the raw dot products
+                        const float nk = l2 ? sm.knorm[i] * sm.knorm[j] : 1.f;
+                        const float nq = l2 ? sm.qnorm[i] * sm.knorm[j] : 1.f;
+                        R[i][j] = (j < i) ? sm.beta[i] * r * nk : 0.f;
+                        X[i][j] = scale * a * nq;
+                    }
+                }
+                for (int j = i + 1 + lane; j < C; j += 32) {
+                    R[i][j] = 0.f;
+                    X[i][j] = 0.f;
+                }
+            }
+            wbar(bid);
+            if (tid < C) {
+                float row[64];
+#pragma unroll
+                for (int j = 0; j < 64; ++j) row[j] = X[tid][j];
+                store_row_f16_image(aqk, tid, row);
+            }
+            wbar(bid);
+        } else {
+            // The decay-factorised tf32 operands, token by token.
             const uint32_t pa = (d >> 5) * 16384u, pb = (d >> 5) * 8192u;
 #pragma unroll
             for (int ii = 0; ii < HALF; ++ii) {
                 const int i = i0 + ii;
                 const float kv = kval(ii), qv = qval(ii);
-                const float ep = __expf(G[ii] - Gm), en = __expf(Gm - G[ii]);
+                const float ep = exp2_approx(G[ii] - Gr), en = exp2_approx(Gr - G[ii]);
                 *reinterpret_cast<float *>(sm.a1 + pa + sw128_offset_f32(i, d & 31)) =
                     to_tf32(kv * ep);
                 *reinterpret_cast<float *>(sm.a1 + pa + sw128_offset_f32(64 + i, d & 31)) =
@@ -604,210 +701,253 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
                 *reinterpret_cast<float *>(sm.b1 + pb + sw128_offset_f32(i, d & 31)) =
                     to_tf32(kv * en);
             }
-        }
-        if (hf == 0) gb[d] = slow ? __expf(Gl) : e_lm * e_m;
-    }
-
-    if (!slow) {
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();
-        // [K_tilde ; Q_tilde] K_hat^T on the tensor core (tf32): TMEM cols 0..63.
-        if (tid == 0 && ok) {
-            tc_fence_after();
-            mma_panels<true>(tmem, smem_u32(sm.a1), 16384, smem_u32(sm.b1), 8192, 16,
-                             idesc_tf32_f32(128, 64), false);
-            mma_commit(&sm.bar_mma);
-        }
-        if (ok) ok = mbar_wait_bounded(&sm.bar_mma, mma_phase, kWaitCycles);
-        ok = __all_sync(0xffffffffu, ok);  // TMEM loads below are warp-collective
-        mma_phase ^= 1;
-        tc_fence_after();
-        // warp w reads TMEM lanes 32*(w%4).., columns 32*(w/4)..
-        const int quad = warp & 3, chalf = warp >> 2, r = quad * 32 + lane;
-        float v[32];
-        if (ok) {
-            tmem_ld32(tmem_addr(tmem, quad * 32, chalf * 32), v);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = 0.f;
-        }
-        __syncthreads();  // a1 is free: the MMA consumed its operands
-        if (r < C) {
-            const int i = r;  // key-key row
-            const float b = sm.beta[i];
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int j = chalf * 32 + jj;
-                R[i][j] = (j < i && i < L) ? b * v[jj] : 0.f;
+            fence_proxy_async();
+            tc_fence_before();
+            wbar(bid);
+            // [K_tilde ; Q_tilde] K_hat^T on the tensor core (tf32): TMEM cols 0..63.
+            if (tid == 0 && ok) {
+                tc_fence_after();
+                mma_panels<true>(tmem, smem_u32(sm.a1), 16384, smem_u32(sm.b1), 8192, 16,
+                                 idesc_tf32_f32(128, 64), false);
+                mma_commit(&sm.bar_mma);
             }
-        } else {
-            const int i = r - C;  // query-key row
+            if (ok) ok = mbar_wait_bounded(&sm.bar_mma, mma_phase, wait_cycles);
+            mma_phase ^= 1u;
+            if (path == 1) {
+                // Second-half rows, first-half columns: K_hat about token 48 for
+                // tokens 0..31 over the consumed K_hat rows 0..31 (their
+                // exponents G_48 - G_j are <= 0), then A (still intact) times it
+                // into TMEM cols 64..95.
+                tc_fence_after();
+                if (hf == 0) {
+                    const float G48 = sm.gh1[d];
+#pragma unroll
+                    for (int ii = 0; ii < HALF; ++ii)
+                        *reinterpret_cast<float *>(sm.b1 + pb + sw128_offset_f32(ii, d & 31)) =
+                            to_tf32(kval(ii) * exp2_approx(G48 - G[ii]));
+                }
+                fence_proxy_async();
+                tc_fence_before();
+                wbar(bid);
+                if (tid == 0 && ok) {
+                    tc_fence_after();
+                    mma_panels<true>(tmem + 64, smem_u32(sm.a1), 16384, smem_u32(sm.b1), 8192,
+                                     16, idesc_tf32_f32(128, 32), false);
+                    mma_commit(&sm.bar_mma);
+                }
+                if (ok) ok = mbar_wait_bounded(&sm.bar_mma, mma_phase, wait_cycles);
+                mma_phase ^= 1u;
+            }
+            ok = __all_sync(0xffffffffu, ok);  // TMEM loads below are warp-collective
+            tc_fence_after();
+            // warp w reads TMEM lanes 32*(w%4).., columns 32*(w/4)..; on the half
+            // path the block of rows 32..63 (keys and queries) and columns 0..31
+            // comes from the second product
+            const int quad = warp & 3, chalf = warp >> 2, r = quad * 32 + lane;
+            const uint32_t col = (path == 1 && (quad & 1) && chalf == 0) ? 64u : chalf * 32u;
+            float v[32];
+            if (ok) {
+                tmem_ld32(tmem_addr(tmem, quad * 32, col), v);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            }
+            wbar(bid);  // a1 is free: the MMAs consumed their operands
+            if (r < C) {
+                const int i = r;  // key-key row
+                const float b = sm.beta[i];
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int j = chalf * 32 + jj;
+                    R[i][j] = (j < i && i < L) ? b * v[jj] : 0.f;
+                }
+            } else {
+                const int i = r - C;  // query-key row
+                float row[32];
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int j = chalf * 32 + jj;
+                    row[jj] = (j <= i && i < L) ? scale * v[jj] : 0.f;
+                }
+                store_quarter_f16_image(aqk, i, chalf * 4, row);
+            }
+        }
+        if (hf == 0) gb[d] = exp2_approx(Gl);
+        // The last uses of G, k and q, so that they leave the registers before
+        // the solve: -Q_hat^T (Q_hat_i = s Gamma_i q_i) into TMEM cols 192..255
+        // (lane d, token columns), where the last MMA group adds (A^qk W)^T to
+        // give -Q'^T; (beta Gamma K)^T and K_end^T (row d, this thread's half of
+        // the tokens, f16) into their operand slots, both free by now.
+        {
             float row[32];
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int j = chalf * 32 + jj;
-                row[jj] = (j <= i && i < L) ? scale * v[jj] : 0.f;
+            for (int ii = 0; ii < HALF; ++ii) row[ii] = -scale * exp2_approx(G[ii]) * qval(ii);
+            tmem_st32(tmem_addr(tmem, (warp & 3) * 32, 192 + hf * 32), row);
+#pragma unroll
+            for (int ii = 0; ii < HALF; ++ii) row[ii] = sm.beta[i0 + ii] * exp2_approx(G[ii]) * kval(ii);
+            store_quarter_f16_image(a2, d, hf * 4, row);
+#pragma unroll
+            for (int ii = 0; ii < HALF; ++ii) row[ii] = exp2_approx(Gl - G[ii]) * kval(ii);
+            store_quarter_f16_image(ket, d, hf * 4, row);
+        }
+        for (int idx = tid; idx < C * (C + 1); idx += kPrepWorkerThreads) (&X[0][0])[idx] = 0.f;
+        wbar(bid);
+
+        // sec. 6.3: A^kk = (I + R)^-1, unit lower triangular, fp32.  The 16 x 16
+        // diagonal blocks by right-looking substitution (one column per thread),
+        // then the 32 x 32 diagonal blocks and the whole from block inverses:
+        //   [A 0; B D]^-1 = [A^-1 0; -D^-1 B A^-1  D^-1]
+        if (tid < C) {
+            const int o = (tid >> 4) * 16, cc = tid & 15;
+            float x[16], acc[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) acc[r] = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                x[m] = m < cc ? 0.f : (m == cc ? 1.f : -acc[m]);
+#pragma unroll
+                for (int r = m + 1; r < 16; ++r) acc[r] = fmaf(R[o + r][o + m], x[m], acc[r]);
             }
-            store_quarter_f16_image(aqk, i, chalf * 4, row);
+#pragma unroll
+            for (int r = 0; r < 16; ++r) X[o + r][o + cc] = x[r];
         }
-    }
-    for (int idx = tid; idx < C * (C + 1); idx += kPrepThreads) (&X[0][0])[idx] = 0.f;
-    __syncthreads();
+        wbar(bid);
+        solve_level16(R, X, Tb, tid, bid);
+        solve_level32(R, X, Tb, tid, bid);
+        // A^kk (rows i) and A^kk^T (rows j), f16
+        if (tid < 2 * C) {
+            const int row = tid >> 1, q4 = tid & 1;
+            float v32[32], t32[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                v32[j] = X[row][q4 * 32 + j];
+                t32[j] = X[q4 * 32 + j][row];
+            }
+            store_quarter_f16_image(b2, row, q4 * 4, v32);
+            store_quarter_f16_image(akt, row, q4 * 4, t32);
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        wbar(bid);
 
-    // sec. 6.3: A^kk = (I + R)^-1, unit lower triangular, fp32.  The 16 x 16
-    // diagonal blocks by right-looking substitution (one column per thread),
-    // then the 32 x 32 diagonal blocks and the whole from block inverses:
-    //   [A 0; B D]^-1 = [A^-1 0; -D^-1 B A^-1  D^-1]
-    if (tid < C) {
-        const int o = (tid >> 4) * 16, cc = tid & 15;
-        float x[16], acc[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) acc[r] = 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            x[m] = m < cc ? 0.f : (m == cc ? 1.f : -acc[m]);
-#pragma unroll
-            for (int r = m + 1; r < 16; ++r) acc[r] = fmaf(R[o + r][o + m], x[m], acc[r]);
+        const int quad = warp & 3, chalf = warp >> 2;  // TMEM lanes 32*quad.., column half
+        // W^T = (beta Gamma K)^T A^kk^T (TMEM cols 64..127) and Z = A^qk A^kk (cols
+        // 0..63; rows 0..63 of a 128-row operand whose rows 64..127 are filler).
+        if (tid == 0 && ok) {
+            tc_fence_after();
+            mma_panels(tmem + 64, smem_u32(a2), 0, smem_u32(b2), 0, 4, idesc_f16_f32(128, 64),
+                       false);
+            mma_panels(tmem, smem_u32(aqk), 0, smem_u32(akt), 0, 4, idesc_f16_f32(128, 64),
+                       false);
+            mma_commit(&sm.bar_mma);
         }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) X[o + r][o + cc] = x[r];
-    }
-    __syncthreads();
-    solve_level16(R, X, Tb, tid);
-    solve_level32(R, X, Tb, tid);
-    // A^kk (rows i) and A^kk^T (rows j), f16
-    if (tid < 2 * C) {
-        const int row = tid >> 1, q4 = tid & 1;
-        float v32[32], t32[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            v32[j] = X[row][q4 * 32 + j];
-            t32[j] = X[q4 * 32 + j][row];
-        }
-        store_quarter_f16_image(b2, row, q4 * 4, v32);
-        store_quarter_f16_image(akt, row, q4 * 4, t32);
-    }
-    // (beta Gamma K)^T and K_end^T: row d, this thread's half of the tokens, f16
-    {
-        float bgk[32], kend[32];
-#pragma unroll
-        for (int ii = 0; ii < HALF; ++ii) {
-            const float kv = kval(ii);
-            bgk[ii] = sm.beta[i0 + ii] * __expf(G[ii]) * kv;
-            kend[ii] = __expf(Gl - G[ii]) * kv;
-        }
-        store_quarter_f16_image(a2, d, hf * 4, bgk);
-        store_quarter_f16_image(ket, d, hf * 4, kend);
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-
-    const int quad = warp & 3, chalf = warp >> 2;  // TMEM lanes 32*quad.., column half
-    // W^T = (beta Gamma K)^T A^kk^T (TMEM cols 64..127) and Z = A^qk A^kk (cols
-    // 0..63; rows 0..63 of a 128-row operand whose rows 64..127 are filler).
-    if (tid == 0 && ok) {
+        if (ok) ok = mbar_wait_bounded(&sm.bar_mma, mma_phase, wait_cycles);
+        ok = __all_sync(0xffffffffu, ok);  // TMEM loads below are warp-collective
+        mma_phase ^= 1u;
         tc_fence_after();
-        mma_panels(tmem + 64, smem_u32(a2), 0, smem_u32(b2), 0, 4, idesc_f16_f32(128, 64),
-                   false);
-        mma_panels(tmem, smem_u32(aqk), 0, smem_u32(akt), 0, 4, idesc_f16_f32(128, 64), false);
-        mma_commit(&sm.bar_mma);
-    }
-    if (ok) ok = mbar_wait_bounded(&sm.bar_mma, mma_phase, kWaitCycles);
-    ok = __all_sync(0xffffffffu, ok);  // TMEM loads below are warp-collective
-    mma_phase ^= 1;
-    tc_fence_after();
-    {
-        // thread = key channel d, token half chalf: W^T row d
-        float v[32];
-        if (ok) tmem_ld32(tmem_addr(tmem, quad * 32, 64 + chalf * 32), v);
-        else
+        {
+            // thread = key channel d, token half chalf: W^T row d
+            float v[32];
+            if (ok) {
+                tmem_ld32(tmem_addr(tmem, quad * 32, 64 + chalf * 32), v);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = 0.f;
-        store_quarter_f16_image(wt, d, chalf * 4, v);
-        // Z rows 0..63 -> staging in the A^kk slot (read by the MMAs just done)
-        if (quad < 2) {
-            if (ok) tmem_ld32(tmem_addr(tmem, quad * 32, chalf * 32), v);
-            store_quarter_f16_image(zst, quad * 32 + lane, chalf * 4, v);
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            }
+            store_quarter_f16_image(wt, d, chalf * 4, v);
+            // Z rows 0..63 -> staging in the A^kk slot (read by the MMAs just done)
+            if (quad < 2) {
+                if (ok) tmem_ld32(tmem_addr(tmem, quad * 32, chalf * 32), v);
+                store_quarter_f16_image(zst, quad * 32 + lane, chalf * 4, v);
+            }
         }
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
+        fence_proxy_async();
+        tc_fence_before();
+        wbar(bid);
 
-    // M' = K_end^T W (cols 0..127), P' = K_end^T A^kk (cols 128..191),
-    // (A^qk W)^T = W^T A^qk^T (cols 192..255).
-    if (tid == 0 && ok) {
-        tc_fence_after();
-        mma_panels(tmem, smem_u32(ket), 0, smem_u32(wt), 0, 4, idesc_f16_f32(128, 128), false);
-        mma_panels(tmem + 128, smem_u32(ket), 0, smem_u32(akt), 0, 4, idesc_f16_f32(128, 64),
-                   false);
-        mma_panels(tmem + 192, smem_u32(wt), 0, smem_u32(aqk), 0, 4, idesc_f16_f32(128, 64),
-                   false);
-        mma_commit(&sm.bar_mma);
-    }
-    if (ok) ok = mbar_wait_bounded(&sm.bar_mma, mma_phase, kWaitCycles);
-    ok = __all_sync(0xffffffffu, ok);  // TMEM loads below are warp-collective
-    tc_fence_after();
-    // Every operand is consumed: a1 becomes the staging of the image's first
-    // 72 KB (-M' | P' | Q' keys 0..63 | . | Q' keys 64..127), Z waits in b1.
-    if (ok) {
-        float v0[32], v1[32];
-        // -M' row d (key), columns (keys) 64*chalf.. -> image panel chalf
-        tmem_ld32x2(tmem_addr(tmem, quad * 32, chalf * 64),
-                    tmem_addr(tmem, quad * 32, chalf * 64 + 32), v0, v1);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            v0[j] = -v0[j];
-            v1[j] = -v1[j];
+        // M' = K_end^T W (cols 0..127), P' = K_end^T A^kk (cols 128..191),
+        // -Q'^T = -Q_hat^T + W^T A^qk^T (cols 192..255, onto what is there).
+        if (tid == 0 && ok) {
+            tc_fence_after();
+            mma_panels(tmem, smem_u32(ket), 0, smem_u32(wt), 0, 4, idesc_f16_f32(128, 128),
+                       false);
+            mma_panels(tmem + 128, smem_u32(ket), 0, smem_u32(akt), 0, 4,
+                       idesc_f16_f32(128, 64), false);
+            mma_panels(tmem + 192, smem_u32(wt), 0, smem_u32(aqk), 0, 4, idesc_f16_f32(128, 64),
+                       true);
+            mma_commit(&sm.bar_mma);
         }
-        store_quarter_f16_image(sm.a1 + IMG_MN + chalf * 16384, d, 0, v0);
-        store_quarter_f16_image(sm.a1 + IMG_MN + chalf * 16384, d, 4, v1);
-    }
-    // -M' (with Z, staged before) starts out while P' and Q' are staged
-    fence_proxy_async();
-    __syncthreads();
-    if (tid == 0) {
-        bulk_s2g(img, sm.a1, IMG_P - IMG_MN);
-        bulk_s2g(img + IMG_Z, zst, IMG_Q1 - IMG_Z);
-        bulk_commit_group();
-    }
-    if (ok) {
-        float v0[32];
-        // P' row d, tokens 32*chalf..
-        tmem_ld32(tmem_addr(tmem, quad * 32, 128 + chalf * 32), v0);
-        store_quarter_f16_image(sm.a1 + IMG_P, d, chalf * 4, v0);
-        // Q'[i][d] = s Gamma_i q_i[d] - (A^qk W)[i][d], tokens i = 32*chalf + jj (this
-        // thread's own tokens), as two 64-row panels
-        tmem_ld32(tmem_addr(tmem, quad * 32, 192 + chalf * 32), v0);
-        uint8_t *qs = sm.a1 + IMG_Q0 + (d >> 6) * 8192u;  // staged at IMG_Q0 and IMG_Z
+        if (ok) ok = mbar_wait_bounded(&sm.bar_mma, mma_phase, wait_cycles);
+        ok = __all_sync(0xffffffffu, ok);  // TMEM loads below are warp-collective
+        mma_phase ^= 1u;
+        tc_fence_after();
+        // Every operand is consumed: a1 becomes the staging of the image's first
+        // 72 KB (-M' | P' | Q' keys 0..63 | . | Q' keys 64..127), Z waits in b1.
+        if (ok) {
+            float v0[32], v1[32];
+            // -M' row d (key), columns (keys) 64*chalf.. -> image panel chalf
+            tmem_ld32x2(tmem_addr(tmem, quad * 32, chalf * 64),
+                        tmem_addr(tmem, quad * 32, chalf * 64 + 32), v0, v1);
 #pragma unroll
-        for (int jj = 0; jj < HALF; ++jj)
-            *reinterpret_cast<__half *>(qs + sw128_offset(chalf * 32 + jj, d & 63)) =
-                __float2half_rn(scale * __expf(G[jj]) * qval(jj) - v0[jj]);
-    } else if (tid == 0) {
-        atomicExch(status, (int)KDA_ERR_TIMEOUT);
+            for (int j = 0; j < 32; ++j) {
+                v0[j] = -v0[j];
+                v1[j] = -v1[j];
+            }
+            store_quarter_f16_image(sm.a1 + IMG_MN + chalf * 16384, d, 0, v0);
+            store_quarter_f16_image(sm.a1 + IMG_MN + chalf * 16384, d, 4, v1);
+        }
+        // -M' (with Z, staged before) starts out while P' and Q' are staged
+        fence_proxy_async();
+        wbar(bid);
+        if (tid == 0) {
+            bulk_s2g(img, sm.a1, IMG_P - IMG_MN);
+            bulk_s2g(img + IMG_Z, zst, IMG_Q1 - IMG_Z);
+            bulk_commit_group();
+        }
+        if (ok) {
+            float v0[32];
+            // P' row d, tokens 32*chalf..
+            tmem_ld32(tmem_addr(tmem, quad * 32, 128 + chalf * 32), v0);
+            store_quarter_f16_image(sm.a1 + IMG_P, d, chalf * 4, v0);
+            // Q'[i][d] = s Gamma_i q_i[d] - (A^qk W)[i][d], tokens i = 32*chalf + jj,
+            // as two 64-row panels
+            tmem_ld32(tmem_addr(tmem, quad * 32, 192 + chalf * 32), v0);
+            uint8_t *qs = sm.a1 + IMG_Q0 + (d >> 6) * 8192u;  // staged at IMG_Q0 and IMG_Z
+#pragma unroll
+            for (int jj = 0; jj < HALF; ++jj)
+                *reinterpret_cast<__half *>(qs + sw128_offset(chalf * 32 + jj, d & 63)) =
+                    __float2half_rn(-v0[jj]);
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        wbar(bid);
+        if (tid == 0) {
+            // the rest of the image: [P' | Q' 0..63] in one piece, then Q' 64..127;
+            // thread 0 waits for the stores (and publishes the image) after
+            // issuing the next item's loads, or below after the last item
+            bulk_s2g(img + IMG_P, sm.a1 + IMG_P, IMG_Z - IMG_P);
+            bulk_s2g(img + IMG_Q1, sm.a1 + IMG_Z, IMG_GB - IMG_Q1);
+            bulk_commit_group();
+            sm.published = ch;
+        }
+        // one verdict per worker: after a wait that gave up, the worker stops
+        if (wbar_or(bid, !ok)) {
+            if (tid == 0) atomicExch(status, (int)KDA_ERR_TIMEOUT);
+            break;
+        }
     }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
     if (tid == 0) {
-        // the rest of the image: [P' | Q' 0..63] in one piece, then Q' 64..127
-        bulk_s2g(img + IMG_P, sm.a1 + IMG_P, IMG_Z - IMG_P);
-        bulk_s2g(img + IMG_Q1, sm.a1 + IMG_Z, IMG_GB - IMG_Q1);
-        bulk_commit_group();
-        if (streamed) {
-            // publish the image to the scan, which is already running
-            bulk_wait_group_all();
+        bulk_wait_group_all();  // the last image in global memory (the shared memory may go)
+        if (flags && sm.published != ~0ull) {
             fence_proxy_async_global();
-            flag_release(sc.ready + ch, 1u);
-        } else {
-            bulk_wait_group_read<0>();  // the shared memory may go; the writes land on their own
+            flag_release(sc.ready + sm.published, 1u);
         }
+        for (int i = 0; i < 3; ++i)
+            if (sm.n_path[i]) atomicAdd(&g_path_counts[i], (unsigned long long)sm.n_path[i]);
     }
+    tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (threadIdx.x < 32) tmem_dealloc(*tmem_slot, 256 * kPrepWorkers);
 }
 
 // ---------------------------------------------------------------------------
@@ -911,22 +1051,22 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                   const float *__restrict__ initial_state,
                   const int32_t *__restrict__ cu, float *__restrict__ final_state, int32_t N,
-                  int32_t T, int32_t H, Scratch sc, int32_t streamed, int64_t sc_items,
-                  int *status) {
+                  int32_t T, int32_t H, Scratch sc, int32_t flags, int64_t sc_items,
+                  long long wait_cycles, int *status) {
     extern __shared__ uint8_t smem_raw[];
     ScanSmem &sm = *reinterpret_cast<ScanSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // Streamed: a programmatic dependent of the chunk table, resident while
-    // the table runs; it waits for the table before anything reads it, and
-    // only then lets the prep (which reads it too, and must not wait on this
-    // kernel) start.  Sequential: the output pass may start setting up.
-    if (streamed) pdl_wait_primaries();
+    // A programmatic dependent of the prep, which was launched before it and
+    // whose CTAs are all running: the output pass may start setting up.  With
+    // flags this kernel follows the prep item by item and never waits for its
+    // grid; without, its producer waits for the whole prep below.  The chunk
+    // table finished before the prep started, so its entries are read from L2.
     pdl_launch_dependents();
     const int32_t seq = blockIdx.x / NT, vt = blockIdx.x % NT, h = blockIdx.y;
     int32_t ta, tb;
     seq_bounds(cu, seq, T, ta, tb);
-    const int32_t c_begin = sc.chunk_off[seq];
+    const int32_t c_begin = __ldcg(sc.chunk_off + seq);
     const int32_t n_chunks = (tb - ta + C - 1) / C;
     const size_t state_off = (((size_t)seq * H + h) * D + (tid & 127)) * D + (size_t)vt * BV;
 
@@ -981,21 +1121,21 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
         if (warp == 4) {
             // -------- producer: -M' and P' of a chunk, once its stage is free --------
             if (lane == 0) {
-                pdl_wait_primaries();  // not streamed: the prep has written every image
+                if (!flags) pdl_wait_primaries();  // the prep has written every image
                 for (int32_t n = 0; n < n_chunks; ++n) {
                     const int stg = n % NSTAGE;
                     if (n >= NSTAGE) {
                         const bool got = mbar_wait_bounded(
-                            &sm.empty[stg], (uint32_t)(n / NSTAGE - 1) & 1u, kWaitCycles);
+                            &sm.empty[stg], (uint32_t)(n / NSTAGE - 1) & 1u, wait_cycles);
                         if (!got || sm.abort_flag) {
                             sm.abort_flag = 1;
                             break;
                         }
                     }
-                    if (streamed) {
-                        // the prep CTA of this chunk publishes its image
+                    if (flags) {
+                        // the prep worker of this chunk publishes its image
                         if (!flag_wait_bounded(sc.ready + (size_t)(c_begin + n) * H + h,
-                                               kWaitCycles)) {
+                                               wait_cycles)) {
                             sm.abort_flag = 1;
                             break;
                         }
@@ -1021,9 +1161,9 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                     const uint32_t d2 = tmem + (uint32_t)(n & 1) * BV;
                     // P' (beta V): needs only the chunk's own operands
                     bool got = mbar_wait_bounded(&sm.full[stg], (uint32_t)(n / NSTAGE) & 1u,
-                                                 kWaitCycles) &&
+                                                 wait_cycles) &&
                                mbar_wait_bounded(&sm.ready_bv[n & 1], (uint32_t)(n >> 1) & 1u,
-                                                 kWaitCycles);
+                                                 wait_cycles);
                     if (!got || sm.abort_flag) {
                         sm.abort_flag = 1;
                         break;
@@ -1032,7 +1172,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                     mma_kmajor_a_mn_b(d2, smem_u32(img + IMG_P), 0, smem_u32(sm.bv[n & 1]), 4,
                                       IDESC, false);
                     // (-M') S_c once the state is in
-                    got = mbar_wait_bounded(&sm.ready_s, (uint32_t)n & 1u, kWaitCycles);
+                    got = mbar_wait_bounded(&sm.ready_s, (uint32_t)n & 1u, wait_cycles);
                     if (!got || sm.abort_flag) {
                         sm.abort_flag = 1;
                         mma_commit(&sm.empty[stg]);  // keeps the drain below exact
@@ -1051,12 +1191,12 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                 // also means every MMA issued is done
                 for (int32_t j = max(done - NSTAGE, 0); j < done; ++j)
                     if (!mbar_wait_bounded(&sm.empty[j % NSTAGE], (uint32_t)(j / NSTAGE) & 1u,
-                                           kWaitCycles))
+                                           wait_cycles))
                         sm.abort_flag = 1;
             }
             __syncwarp();
         } else if (warp >= 6) {
-            // -------- state writers: the S_c images out (streamed: and their
+            // -------- state writers: the S_c images out (with flags: and their
             // flags, for the output pass), off the compute warps' chain.  Two
             // of them take the chunks in turn, so that each waits for its copy
             // to land and publishes it with no other copy of its own in flight
@@ -1066,7 +1206,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                 for (int32_t n = b; n < n_chunks; n += 2) {
                     // S_c in sb[n & 1], written and fenced by the compute warps
                     if (!mbar_wait_bounded(&sm.ready_w[b], (uint32_t)(n >> 1) & 1u,
-                                           kWaitCycles) ||
+                                           wait_cycles) ||
                         sm.abort_flag) {
                         sm.abort_flag = 1;
                         break;
@@ -1075,7 +1215,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                     bulk_commit_group();
                     bulk_wait_group_read<0>();
                     sm.copied[b] = (n >> 1) + 1;
-                    if (streamed) {
+                    if (flags) {
                         bulk_wait_group_all();
                         fence_proxy_async_global();
                         flag_release(sc.ready + (size_t)sc_items +
@@ -1109,7 +1249,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
             };
             auto wait_full = [&](int32_t n) {
                 if (!mbar_wait_bounded(&sm.full[n % NSTAGE], (uint32_t)(n / NSTAGE) & 1u,
-                                       kWaitCycles))
+                                       wait_cycles))
                     sm.abort_flag = 1;
             };
             // S_c of chunk n as the MMA's B operand (f16); the same image goes out
@@ -1139,7 +1279,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                     g_next = sm.gbs[(n + 1) % NSTAGE][tid];
                     build_bv(n + 1);
                 }
-                if (!mbar_wait_bounded(&sm.mma_s, (uint32_t)n & 1u, kWaitCycles))
+                if (!mbar_wait_bounded(&sm.mma_s, (uint32_t)n & 1u, wait_cycles))
                     sm.abort_flag = 1;
                 tc_fence_after();
                 {
@@ -1163,7 +1303,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                         if (sm.copied[wb] < need) {
                             const long long t0 = clock64();
                             while (sm.copied[wb] < need) {
-                                if (clock64() - t0 > kWaitCycles) {
+                                if (clock64() - t0 > wait_cycles) {
                                     sm.abort_flag = 1;
                                     break;
                                 }
@@ -1183,7 +1323,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                 const int32_t iss = sm.issued;
                 for (int32_t j = max(iss - NSTAGE, 0); j < iss; ++j)
                     (void)mbar_wait_bounded(&sm.full[j % NSTAGE], (uint32_t)(j / NSTAGE) & 1u,
-                                            kWaitCycles);
+                                            wait_cycles);
             }
         }
         tc_fence_before();
@@ -1224,29 +1364,31 @@ template <typename TOut>
 __global__ void __launch_bounds__(kOutThreads)
 chunk_out_kernel(const __grid_constant__ CUtensorMap out_map, const __grid_constant__ CUtensorMap v_map,
                  const int32_t *__restrict__ cu, TOut *__restrict__ out, int32_t N, int32_t T,
-                 int32_t H, Scratch sc, int32_t streamed, int64_t sc_items, int *status) {
+                 int32_t H, Scratch sc, int32_t flags, int64_t sc_items,
+                 long long wait_cycles, int *status) {
     extern __shared__ uint8_t smem_raw[];
     OutSmem &sm = *reinterpret_cast<OutSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5;
     // heads fastest: the order in which the scan finishes the chunks' states
     const int32_t c = (int32_t)(blockIdx.x / (unsigned)H), h = (int32_t)(blockIdx.x % (unsigned)H);
-    const int2 tok = sc.chunk_tok[c];
+    const int2 tok = __ldcg(sc.chunk_tok + c);  // the chunk table finished long before
     const int32_t t0 = tok.x, L = tok.y;
     if (L <= 0) return;
     const uint8_t *img = sc.img + ((size_t)c * H + h) * IMG_STRIDE;
 
-    // Sequential: the scan (and before it the prep) has finished.  Streamed
-    // (running beside the prep's last CTAs and the scan): this chunk's image
-    // and both value tiles of its S_c are up.  A wait that runs out leaves the
-    // status set and garbage outputs, never a hang.
-    if (!streamed) pdl_wait_primaries();
+    // Without flags: the scan (and before it the prep) has finished.  With
+    // flags (running beside the prep's last workers and the scan, both
+    // launched before this kernel and running): this chunk's image and both
+    // value tiles of its S_c are up.  A wait that runs out leaves the status
+    // set and garbage outputs, never a hang.
+    if (!flags) pdl_wait_primaries();
     if (tid == 0) {
-        if (streamed) {
-            bool got = flag_wait_bounded(sc.ready + (size_t)c * H + h, kWaitCycles);
+        if (flags) {
+            bool got = flag_wait_bounded(sc.ready + (size_t)c * H + h, wait_cycles);
             for (int t = 0; t < NT && got; ++t)
                 got = flag_wait_bounded(sc.ready + sc_items + ((size_t)c * H + h) * NT + t,
-                                        kWaitCycles);
+                                        wait_cycles);
             if (!got) atomicExch(status, (int)KDA_ERR_TIMEOUT);
             fence_proxy_async_global();
         }
@@ -1271,7 +1413,7 @@ chunk_out_kernel(const __grid_constant__ CUtensorMap out_map, const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem;
-    bool ok = mbar_wait_bounded(&sm.bar_in, 0, kWaitCycles);
+    bool ok = mbar_wait_bounded(&sm.bar_in, 0, wait_cycles);
     // beta V: thread -> token tid / 2, value tile tid % 2 (rows past the
     // sequence, another sequence's tokens or zeros past T, get beta 0)
     {
@@ -1305,7 +1447,7 @@ chunk_out_kernel(const __grid_constant__ CUtensorMap out_map, const __grid_const
         }
         mma_commit(&sm.bar_mma);
     }
-    if (ok) ok = mbar_wait_bounded(&sm.bar_mma, 0, kWaitCycles);
+    if (ok) ok = mbar_wait_bounded(&sm.bar_mma, 0, wait_cycles);
     tc_fence_after();
     ok = !__syncthreads_or(!ok);  // one verdict for all (warps 2-3 share a barrier below)
     if (ok && warp >= 2) {
@@ -1377,22 +1519,25 @@ chunk_out_kernel(const __grid_constant__ CUtensorMap out_map, const __grid_const
     if (!ok && tid == 0) atomicExch(status, (int)KDA_ERR_TIMEOUT);
     if (!ok && tid == 0) {
         // let the loads land before the shared memory goes away
-        (void)mbar_wait_bounded(&sm.bar_in, 0, kWaitCycles);
+        (void)mbar_wait_bounded(&sm.bar_in, 0, wait_cycles);
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
-constexpr size_t kPrepSmem = sizeof(PrepSmem) + 1024;
+constexpr size_t kPrepSmem = kPrepWorkers * kPrepWorkerBytes + 16 + 1024;
 constexpr size_t kScanSmem = sizeof(ScanSmem) + 1024;
 constexpr size_t kOutSmem = sizeof(OutSmem) + 1024;
 static_assert(kScanSmem <= 227 * 1024, "scan shared memory");
 static_assert(2 * kOutSmem <= 228 * 1024 - 2 * 1024, "two output CTAs per SM");
-static_assert(2 * kPrepSmem <= 228 * 1024 - 2 * 1024, "two prep CTAs per SM");
-// Largest prep grid run concurrently with the scan: the scan's wait for an
-// image is bounded (~1 s), and a prep of this many items ends well within it.
+static_assert(kPrepSmem <= 227 * 1024, "prep shared memory (two workers)");
+static_assert(kPrepSmem > 114 * 1024, "one prep CTA per SM: the SMs it leaves take the scan");
+// Largest prep run beside the scan on the SMs the scan leaves; longer ones
+// take every SM first, and the scan follows (the tail order).
 constexpr size_t kStreamMaxItems = 1u << 16;
+// Bounded waits give up after this many SM clocks (~1 s at 2 GHz).
+constexpr long long kWaitCycles = 2000000000LL;
 
 }  // namespace
 
@@ -1401,6 +1546,30 @@ size_t chunk_tc_workspace_bytes(int32_t N, int32_t T, int32_t H) {
     return align256(nch * IMG_STRIDE) + align256(nch * NT * (size_t)(D * 128)) +
            align256(nch * (1 + NT) * sizeof(uint32_t)) + align256(max_chunks(N, T) * sizeof(int2)) +
            align256(((size_t)N + 1) * sizeof(int32_t));
+}
+
+ChunkScratchView chunk_tc_scratch_view(void *workspace, int32_t N, int32_t T, int32_t H) {
+    static_assert(IMG_STRIDE == kChunkImgStride && NT == 2 && kStateImg == 16384,
+                  "the layout the backward reads");
+    const Scratch sc = carve(workspace, N, T, H);
+    ChunkScratchView v;
+    v.img = sc.img;
+    v.sst = sc.sst;
+    v.chunk_tok = sc.chunk_tok;
+    v.chunk_off = sc.chunk_off;
+    v.max_chunks = max_chunks(N, T);
+    return v;
+}
+
+cudaError_t chunk_path_counts(uint64_t counts[3], bool clear) {
+    unsigned long long v[3] = {0, 0, 0};
+    cudaError_t e = cudaMemcpyFromSymbol(v, g_path_counts, sizeof(v));
+    if (e == cudaSuccess && clear) {
+        const unsigned long long z[3] = {0, 0, 0};
+        e = cudaMemcpyToSymbol(g_path_counts, z, sizeof(z));
+    }
+    for (int i = 0; i < 3; ++i) counts[i] = (uint64_t)v[i];
+    return e;
 }
 
 // cuTensorMapEncodeTiled, fetched from the driver once (no libcuda link).
@@ -1433,19 +1602,14 @@ bool encode_tile_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, s
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The concurrent order needs the scan, prep and output kernels to run side by
-// side.  Tools that run kernels one at a time (Nsight Compute, the compute
-// sanitizer: both inject themselves through CUDA_INJECTION64_PATH) would make
-// the scan wait out its flag timeouts, so under them, or with
-// KDA_LAUNCH_ORDER=sequential, the sequential order is used.
-bool concurrent_order_allowed() {
-    static const bool allowed = [] {
+// KDA_LAUNCH_ORDER=sequential runs every call in the sequential order (for
+// profilers that time one kernel at a time with the whole GPU to itself).
+bool sequential_order_forced() {
+    static const bool forced = [] {
         const char *order = std::getenv("KDA_LAUNCH_ORDER");
-        if (order && std::strcmp(order, "sequential") == 0) return false;
-        const char *inj = std::getenv("CUDA_INJECTION64_PATH");
-        return !(inj && inj[0] != '\0');
+        return order && std::strcmp(order, "sequential") == 0;
     }();
-    return allowed;
+    return forced;
 }
 
 cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspace_bytes,
@@ -1453,49 +1617,44 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
     if (workspace_bytes < chunk_tc_workspace_bytes(a.N, a.T, a.H) || !workspace)
         return cudaErrorInvalidValue;
     const Scratch sc = carve(workspace, a.N, a.T, a.H);
-    // Sequential order: table -> prep -> scan -> output, each after the first
-    // a programmatic dependent (its CTAs become resident and set up while the
-    // kernel ahead drains, then wait on griddepcontrol before reading its
-    // results).  With per-kernel events between them (clock) the launches are
-    // plain.
+    // Four launches: table -> prep -> scan -> output, each after the table a
+    // programmatic dependent of the kernel before it (its CTAs may become
+    // resident while that kernel still runs).  No kernel ever waits on work
+    // of a kernel launched after it, so any schedule the GPU picks -- one
+    // kernel at a time included -- completes.
     //
-    // Streamed order, when the scan's CTAs take at most half of the SMs:
-    // table -> scan (programmatic dependent of the table: it waits for the
-    // table, then triggers) -> prep (programmatic dependent of the scan, so it
-    // starts once every scan CTA is resident and the table is done) -> output (programmatic dependent of
-    // the prep, so it starts once every prep CTA has started).  The scan
-    // follows the prep chunk by chunk through the image flags, so its serial
-    // chain runs under the prep's parallel work instead of after it; the
-    // output CTAs follow the scan through the state flags and fill the SMs
-    // that the prep's last CTAs leave.
+    // Overlapped order (the scan's CTAs fit in half of the SMs): the prep is
+    // persistent and triggers its dependents as soon as its CTAs run; with up
+    // to kStreamMaxItems items it takes only the SMs that the scan's CTAs
+    // leave, so the scan runs beside it, following each image through its
+    // flag; with more, it takes every SM and the scan starts on the SMs its
+    // workers leave when the items run out (the tail order).  The output
+    // kernel follows the images and the scan's states through flags, on SMs
+    // that prep workers leave.  The waits are on CTAs already running.
     //
-    // Tail order, when the scan's CTAs take at most half of the SMs but the
-    // prep grid is too large to run beside the scan: table -> prep (a plain
-    // launch: with flags on it does not wait on griddepcontrol, so the stream
-    // order keeps it behind the table; it publishes each image) -> scan
-    // (programmatic dependent of the prep, which it waits for, then triggers)
-    // -> output (programmatic dependent of the scan, so it starts once every
-    // scan CTA is resident).  The output CTAs follow the scan through the
-    // state flags on the SMs the scan leaves, instead of after it.  With more
-    // scan CTAs than that, output CTAs waiting on late sequences would hold
-    // SMs that finished ones could use: those calls run in sequence.
+    // Sequential order (more scan CTAs than half of the SMs, per-kernel
+    // events requested, or KDA_LAUNCH_ORDER=sequential): each kernel waits on
+    // griddepcontrol for the whole kernel ahead before it reads its results.
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     const bool timed = a.clock && a.clock->max_events > 0;
-    const size_t n_items = max_chunks(a.N, a.T) * (size_t)a.H;  // prep CTAs
+    const bool diag = a.diag_withhold_prep != 0;
+    const size_t n_items = max_chunks(a.N, a.T) * (size_t)a.H;  // prep items
     const size_t scan_ctas = (size_t)a.N * NT * (size_t)a.H;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         sms = 0;
-    const bool overlap = !timed && concurrent_order_allowed() && a.T > 0 && sms > 0 &&
-                         2 * scan_ctas <= (size_t)sms;
-    const bool concurrent = overlap && n_items <= kStreamMaxItems;
-    // the kernels hand work over through flags (streamed or tail order)
-    const bool streamed = overlap;
-    // prep CTAs resident at once (two per SM on the SMs the scan leaves)
-    const int32_t prefetch_dist = 2 * (sms - (concurrent ? (int32_t)scan_ctas : 0));
+    // the kernels hand work over through flags (overlapped order)
+    const bool flags = diag || (!timed && !sequential_order_forced() && a.T > 0 && sms > 0 &&
+                                2 * scan_ctas <= (size_t)sms);
+    const bool beside = flags && n_items <= kStreamMaxItems;
+    size_t prep_ctas = sms > 0 ? (size_t)sms : 1;
+    if (beside) prep_ctas = std::max<size_t>(1, (size_t)sms - scan_ctas);
+    prep_ctas = std::max<size_t>(
+        1, std::min(prep_ctas, (n_items + kPrepWorkers - 1) / (size_t)kPrepWorkers));
+    const long long wait_cycles = a.wait_cycles > 0 ? a.wait_cycles : kWaitCycles;
     auto config = [&](dim3 grid, int threads, size_t smem, bool dependent) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
@@ -1507,8 +1666,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
         return cfg;
     };
     // Every kernel is set up (and so loaded, under lazy module loading) before
-    // the first launch: loading the prep while the scan already waits for it
-    // would wait for the scan.
+    // the first launch, and every tensor map encoded, so that the launches
+    // follow one another without host work in between.
     auto prep = a.pro ? chunk_prep_kernel<true> : chunk_prep_kernel<false>;
     auto out_kernel_f32 = chunk_out_kernel<float>;
     auto out_kernel_bf16 = chunk_out_kernel<__nv_bfloat16>;
@@ -1526,11 +1685,11 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
                                              (int)kOutSmem);
     if (e != cudaSuccess) return e;
 
-    // the tensor maps too, so that the prep follows the scan without delay
     PrepMaps maps;
-    CUtensorMap v_map;
+    CUtensorMap v_map, out_map;
     memset(&maps, 0, sizeof(maps));
     memset(&v_map, 0, sizeof(v_map));
+    memset(&out_map, 0, sizeof(out_map));
     if (a.T > 0) {
         if (!encode_tile_map(&maps.q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H / a.G) ||
             !encode_tile_map(&maps.k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H / a.G) ||
@@ -1540,52 +1699,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
         if (!encode_tile_map(&v_map, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, BV,
                              CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
-    }
-
-    const size_t n_ready = streamed ? n_items * (1 + NT) : 0;  // image and state flags
-    const unsigned table_ctas = 1u + (unsigned)std::min<size_t>(n_ready / 16384, 63);
-    chunk_table_kernel<<<table_ctas, 1024, 0, stream>>>(a.cu_seqlens, a.N, a.T, sc.chunk_off,
-                                                        sc.chunk_tok, sc.ready, n_ready);
-    a.clock->mark(stream);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-
-    auto launch_scan = [&](bool dependent) {
-        const cudaLaunchConfig_t cfg =
-            config(dim3((unsigned)(a.N * NT), (unsigned)a.H), kScanThreads, kScanSmem, dependent);
-        return cudaLaunchKernelEx(&cfg, chunk_scan_kernel, v_map, a.initial_state,
-                                  static_cast<const int32_t *>(a.cu_seqlens), a.final_state, a.N,
-                                  a.T, a.H, sc, (int32_t)streamed, (int64_t)n_items,
-                                  a.status);
-    };
-    if (concurrent) {
-        e = launch_scan(true);
-        if (e != cudaSuccess) return e;
-    }
-
-    if (a.T > 0) {
-        // tail order: a plain launch (see above)
-        const cudaLaunchConfig_t cfg = config(dim3((unsigned)n_items), kPrepThreads, kPrepSmem,
-                                              !streamed || concurrent);
-        e = cudaLaunchKernelEx(&cfg, prep, maps, static_cast<const __nv_bfloat16 *>(a.q),
-                               static_cast<const __nv_bfloat16 *>(a.k), a.beta, a.scale,
-                               static_cast<const int32_t *>(a.cu_seqlens), a.N, a.T, a.H, a.G,
-                               a.pro, a.gbias, a.galog, sc, (int32_t)streamed, prefetch_dist,
-                               a.status);
-        if (e != cudaSuccess) return e;
-    }
-    a.clock->mark(stream);
-
-    if (!concurrent) {
-        e = launch_scan(a.T > 0);  // with T == 0 no prep runs ahead of it
-        if (e != cudaSuccess) return e;
-    }
-    a.clock->mark(stream);
-
-    if (a.T > 0) {
         // output tiles [64 tokens x 128-byte column panel] of one head
-        CUtensorMap out_map;
-        memset(&out_map, 0, sizeof(out_map));
         auto enc = tensor_map_encoder();
         const size_t es = a.out_f32 ? 4 : 2;
         const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.H, (cuuint64_t)a.T};
@@ -1598,19 +1712,53 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        // a programmatic dependent of the scan (sequential; tail: its CTAs
-        // follow the scan on the SMs it leaves) or of the prep (streamed: its
-        // CTAs fill the SMs that the prep's last CTAs leave)
+    }
+
+    const size_t n_ready = flags ? n_items * (1 + NT) : 0;  // image and state flags
+    const unsigned table_ctas = 1u + (unsigned)std::min<size_t>(n_ready / 16384, 63);
+    chunk_table_kernel<<<table_ctas, 1024, 0, stream>>>(a.cu_seqlens, a.N, a.T, sc.chunk_off,
+                                                        sc.chunk_tok, sc.ready, n_ready);
+    a.clock->mark(stream);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    // The diagnostic run withholds the prep: the scan's first flag is never
+    // published and its bounded waits run out.
+    const bool run_prep = a.T > 0 && !diag;
+    if (run_prep) {
+        const cudaLaunchConfig_t cfg =
+            config(dim3((unsigned)prep_ctas), kPrepThreads, kPrepSmem, true);
+        e = cudaLaunchKernelEx(&cfg, prep, maps, static_cast<const __nv_bfloat16 *>(a.q),
+                               static_cast<const __nv_bfloat16 *>(a.k), a.beta, a.scale, a.H,
+                               a.G, a.pro, a.gbias, a.galog, sc, (uint32_t)n_items,
+                               (int32_t)flags, wait_cycles, a.status);
+        if (e != cudaSuccess) return e;
+    }
+    a.clock->mark(stream);
+
+    {
+        // a plain launch when no prep runs ahead of it (it reads the table)
+        const cudaLaunchConfig_t cfg = config(dim3((unsigned)(a.N * NT), (unsigned)a.H),
+                                              kScanThreads, kScanSmem, run_prep);
+        e = cudaLaunchKernelEx(&cfg, chunk_scan_kernel, v_map, a.initial_state,
+                               static_cast<const int32_t *>(a.cu_seqlens), a.final_state, a.N,
+                               a.T, a.H, sc, (int32_t)flags, (int64_t)n_items, wait_cycles,
+                               a.status);
+        if (e != cudaSuccess) return e;
+    }
+    a.clock->mark(stream);
+
+    if (run_prep) {
         const cudaLaunchConfig_t cfg = config(dim3((unsigned)n_items), kOutThreads, kOutSmem, true);
         const int32_t *cu = static_cast<const int32_t *>(a.cu_seqlens);
         if (a.out_f32) {
             e = cudaLaunchKernelEx(&cfg, out_kernel_f32, out_map, v_map, cu,
                                    static_cast<float *>(a.out), a.N, a.T, a.H, sc,
-                                   (int32_t)streamed, (int64_t)n_items, a.status);
+                                   (int32_t)flags, (int64_t)n_items, wait_cycles, a.status);
         } else {
             e = cudaLaunchKernelEx(&cfg, out_kernel_bf16, out_map, v_map, cu,
                                    static_cast<__nv_bfloat16 *>(a.out), a.N, a.T, a.H, sc,
-                                   (int32_t)streamed, (int64_t)n_items, a.status);
+                                   (int32_t)flags, (int64_t)n_items, wait_cycles, a.status);
         }
         if (e != cudaSuccess) return e;
     }

@@ -40,6 +40,8 @@ struct ChunkArgs {
     int *status;                 // device status word (kernels with bounded waits
                                  // store KDA_ERR_TIMEOUT here when one gives up)
     StageClock *clock;           // never null inside the launchers
+    int32_t diag_withhold_prep = 0;  // diagnostic: launch no prep (the scan's waits run out)
+    long long wait_cycles = 0;       // limit of every bounded wait in SM clocks (0: default)
 };
 
 struct StepArgs {
@@ -91,6 +93,18 @@ struct BwdArgs {
 };
 size_t recurrent_bwd_workspace_bytes(int32_t N, int32_t T, int32_t H, int32_t D);
 cudaError_t launch_recurrent_bwd(const BwdArgs &a, cudaStream_t stream);
+// The same walk with 16-column tiles whatever the (sequence, head) count
+// (bf16 or fp32 inputs, D = 128): for many short sequences (the chunk form's
+// 64-token segments), where more CTAs with less work each pay.
+size_t recurrent_bwd_tiles16_workspace_bytes(int32_t N, int32_t T, int32_t H);
+cudaError_t launch_recurrent_bwd_tiles16(const BwdArgs &a, cudaStream_t stream);
+
+// Chunkwise backward (kda_backward_chunk.cu): the forward engine's images, a
+// reverse scan over chunks for the state gradient at every chunk boundary,
+// then the recurrent walk per 64-token chunk from its boundary values.
+// bf16, D = 128, no prologue, no value-head groups.
+size_t chunk_bwd_workspace_bytes(int32_t N, int32_t T, int32_t H);
+cudaError_t launch_chunk_bwd(const BwdArgs &a, int *status, cudaStream_t stream);
 
 // The fused input prologue, as each kernel applies it to one element.
 constexpr float kL2Eps = 1e-6f;
@@ -144,7 +158,29 @@ cudaError_t launch_recurrent_fwd(const RecurArgs &a, cudaStream_t stream);
 
 // Tensor-core chunk engine (kda_chunk_tc.cu): bf16, D = 128, C = 64.
 size_t chunk_tc_workspace_bytes(int32_t N, int32_t T, int32_t H);
+// Items per path of the decayed products since the last clear (mid, half,
+// direct), on the current device.
+cudaError_t chunk_path_counts(uint64_t counts[3], bool clear);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspace_bytes,
                             cudaStream_t stream);
+// What a finished launch_chunk_tc leaves in its workspace, for the backward:
+// per (chunk c, head h), item = c * H + h, chunks numbered sequence by
+// sequence (chunk_off[s] = first chunk of sequence s; chunk_tok[c] = {first
+// token, length}, length 0 past the last chunk; max_chunks entries):
+//   img  + item * kChunkImgStride: f16 -M' (2 K-major panels of 128 rows at
+//        0), Q' keys 0..63 / 64..127 (64 rows at 49152 / 65536), exp(G_last)
+//        [128] f32 at 73728
+//   sst  + (item * 2 + vt) * 16384: S_c entering the chunk, value columns
+//        64 vt .. 64 vt + 63, f16, one 128-byte-swizzled row of 64 values
+//        per key row
+struct ChunkScratchView {
+    const uint8_t *img;
+    const uint8_t *sst;
+    const int2 *chunk_tok;
+    const int32_t *chunk_off;
+    size_t max_chunks;
+};
+constexpr uint32_t kChunkImgStride = 74752;
+ChunkScratchView chunk_tc_scratch_view(void *workspace, int32_t N, int32_t T, int32_t H);
 
 }  // namespace kda

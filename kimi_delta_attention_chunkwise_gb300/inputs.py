@@ -201,6 +201,40 @@ def long_context_device(T: int = 1 << 20, H: int = 32, d: int = 128,
             "cu_seqlens": cu, "scale": float(d) ** -0.5}
 
 
+def varlen_device(n_seqs: int = 32, H: int = 32, d: int = 128, seed: int = 2,
+                  device: str = "cuda"):
+    """The packed 32-sequence workload's shapes and recipe, drawn on the device
+    for timing runs: the same sequence lengths as ``varlen_prefill`` (numpy
+    PCG64, seed 2), then q, k, v, beta, log_alpha and the initial states from
+    a seeded torch generator.  Returns a dict like ``long_context_device``
+    plus ``initial_state`` ([N, H, d, d] fp32, N(0, 0.02)) and ``lengths``."""
+    import torch
+    rng = np.random.default_rng(seed)
+    lengths = [int(x) for x in rng.integers(512, 8193, size=n_seqs)]
+    T = int(sum(lengths))
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+
+    def normed():
+        x = torch.randn((T, H, d), generator=gen, device=device, dtype=torch.float32)
+        x = x / x.norm(dim=-1, keepdim=True).clamp_min(1e-12)
+        return x.to(torch.bfloat16)
+
+    q = normed()
+    k = normed()
+    v = torch.randn((T, H, d), generator=gen, device=device,
+                    dtype=torch.float32).to(torch.bfloat16)
+    beta = torch.sigmoid(torch.randn((T, H), generator=gen, device=device))
+    la = -torch.nn.functional.softplus(
+        torch.randn((T, H, d), generator=gen, device=device, dtype=torch.float32) - 3.0)
+    s0 = torch.randn((n_seqs, H, d, d), generator=gen, device=device) * 0.02
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32),
+                      device=device)
+    return {"q": q, "k": k, "v": v, "log_alpha": la.contiguous(), "beta": beta,
+            "cu_seqlens": cu, "scale": float(d) ** -0.5, "initial_state": s0,
+            "lengths": lengths}
+
+
 def batched_decode(n_seqs: int = 256, H: int = 32, d: int = 128, steps: int = 64,
                    seed: int = 4) -> DecodeWorkload:
     """n_seqs independent sequences x H heads, one token per sequence per step,

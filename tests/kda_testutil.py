@@ -65,10 +65,18 @@ def run_prefill(w, engine="auto", out_f32=False, chunk_size=None, dev=None,
                                chunk_size=(w.chunk_size if chunk_size is None else chunk_size),
                                engine=engine, out_f32=out_f32,
                                use_library_scratch=use_library_scratch)
-    torch.cuda.synchronize()
+    check_device_status()
     o = out.float().cpu().numpy().astype(np.float64)
     f = final.cpu().numpy().astype(np.float64) if with_final else None
     return o, f
+
+
+def check_device_status():
+    """Synchronise and assert that no kernel's bounded wait gave up (the
+    device status word; the host call returns before the kernels run)."""
+    import kimi_delta_attention_chunkwise_gb300 as kda
+    st = kda.kda_device_status()
+    assert st == kda.KDA_SUCCESS, f"device status: {kda.kda_status_string(st)}"
 
 
 def run_oracle(w):

@@ -197,6 +197,24 @@ def test_recurrent_bwd_support(lib):
     assert bwd(kda.make_shape(2, 64, 2, 128, 128, kda.KDA_DTYPE_BF16)) == kda.KDA_ERR_INVALID_ARG
 
 
+def test_chunk_bwd_support(lib):
+    """The chunkwise backward takes bf16, d = 128 only, and checks the
+    alignment its tensor maps need before anything runs."""
+    def bwd(shape, q=FAKE):
+        return lib.kda_chunk_bwd(q, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(1.0), None, None,
+                                 None, None, FAKE, FAKE, FAKE, FAKE, FAKE, None,
+                                 ctypes.byref(shape), None)
+    assert bwd(kda.make_shape(1, 64, 2, 128, 128, kda.KDA_DTYPE_F32)) == kda.KDA_ERR_UNSUPPORTED
+    assert bwd(kda.make_shape(1, 64, 2, 64, 64, kda.KDA_DTYPE_BF16)) == kda.KDA_ERR_UNSUPPORTED
+    grouped = kda.make_shape(1, 64, 2, 128, 128, kda.KDA_DTYPE_BF16, num_v_heads=4)
+    assert bwd(grouped) == kda.KDA_ERR_UNSUPPORTED
+    pro = kda.make_shape(1, 64, 2, 128, 128, kda.KDA_DTYPE_BF16, prologue=kda.KDA_PROLOGUE_L2NORM_QK)
+    assert bwd(pro) == kda.KDA_ERR_UNSUPPORTED
+    ok = kda.make_shape(1, 64, 2, 128, 128, kda.KDA_DTYPE_BF16)
+    assert bwd(ok, q=FAKE + 4) == kda.KDA_ERR_INVALID_ARG      # q not 16-byte aligned
+    assert bwd(kda.make_shape(2, 64, 2, 128, 128, kda.KDA_DTYPE_BF16)) == kda.KDA_ERR_INVALID_ARG
+
+
 def _align256(n):
     return (n + 255) // 256 * 256
 
@@ -264,7 +282,7 @@ def _header_prototypes():
 
 
 def _c_kind(decl: str) -> str:
-    if "*" in decl or "cudaStream_t" in decl:
+    if "*" in decl or "[" in decl or "cudaStream_t" in decl:
         return "pointer"
     if decl.startswith("float"):
         return "float"
@@ -272,6 +290,8 @@ def _c_kind(decl: str) -> str:
         return "size"
     if decl.split()[0] in ("int32_t", "int", "kdaStatus_t", "kdaDtype_t"):
         return "int32"
+    if decl.split()[0] == "int64_t":
+        return "int64"
     raise AssertionError(f"unclassified parameter {decl!r}")
 
 
@@ -284,6 +304,8 @@ def _ctypes_kind(t) -> str:
         return "size"
     if t in (ctypes.c_int32, ctypes.c_int):
         return "int32"
+    if t is ctypes.c_int64:
+        return "int64"
     raise AssertionError(f"unclassified ctypes type {t!r}")
 
 

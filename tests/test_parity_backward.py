@@ -79,3 +79,28 @@ def test_many_heads_whole_state_tiles():
     """Enough (sequence, head) pairs that each CTA keeps the whole state width
     (small problems split the columns into 16-wide tiles and sum partials)."""
     _check(_case(1300, [3, 0, 9] * 14, 8, 128, "f32"), "f32")
+
+
+@pytest.mark.parametrize("lengths,H", [([130, 64, 1, 200], 2), ([1000], 4), ([0, 70, 3], 3)])
+def test_chunk_form_matches_the_oracle(lengths, H):
+    """kda_chunk_bwd (forward engine's factors, reverse scan in tf32, the walk
+    per 64-token chunk from its boundary values) against the fp64 gradients:
+    ragged packs (empty and one-token sequences), initial states and a
+    final-state gradient; bf16 bound, since the forward engine's factors and
+    states are f16."""
+    import torch
+    import kimi_delta_attention_chunkwise_gb300 as kda
+    from oracle.backward import recurrent_backward
+    from kda_testutil import TOL_BF16
+    c = _case(1300 + len(lengths), lengths, H, 128, "bf16")
+    to = lambda x, d=None: torch.from_numpy(np.ascontiguousarray(x)).to("cuda", d)
+    bf = torch.bfloat16
+    got = kda.kda_chunk_bwd(to(c["q"], bf), to(c["k"], bf), to(c["v"], bf), to(c["g"]),
+                            to(c["b"]), c["s"], to(c["S0"]), to(c["cu"]), to(c["do"], bf),
+                            to(c["dSf"]))
+    torch.cuda.synchronize()
+    assert kda.kda_device_status() == kda.KDA_SUCCESS
+    ref = recurrent_backward(c["q"], c["k"], c["v"], c["g"], c["b"], c["s"], c["S0"], c["cu"],
+                             c["do"], c["dSf"])
+    for name, x, r in zip(("dq", "dk", "dv", "dlog_alpha", "dbeta", "d_initial"), got, ref):
+        assert nerr(x.cpu().numpy(), r) <= TOL_BF16, name

@@ -64,10 +64,30 @@ def test_long_context_prefix():
     _check(inputs.long_context_prefix(8192), "tensor")
 
 
+def test_k3_range_gates_stay_on_tensor_cores():
+    """log alpha = -5 sigmoid(g), g ~ N(0, 1): the K3 gate's range (-5, 0)
+    with its midpoint -2.5 ("Linear Attention, From Scratch to Kimi 3",
+    sec. 6).  Over 32 tokens the decay passes e^-80, so the mid-chunk
+    reference cannot serve these chunks, but over 16 it cannot: every item
+    takes the half-chunk references (tensor cores), none the direct path."""
+    import kimi_delta_attention_chunkwise_gb300 as kda
+    rng = np.random.default_rng(111)
+    w = inputs.prefill(111, [2048, 700, 64, 1], H=4, d=128, dtype="bf16", init_std=0.02)
+    g = rng.standard_normal(w.log_alpha.shape)
+    w.log_alpha = (-5.0 / (1.0 + np.exp(-g))).astype(np.float32)
+    kda.kda_chunk_path_counts()  # clear
+    _check(w, "tensor")
+    mid, half, direct = kda.kda_chunk_path_counts()
+    assert direct == 0, (mid, half, direct)
+    assert half > 0 and half >= 4 * mid, (mid, half, direct)
+
+
 @pytest.mark.parametrize("engine", ENGINES)
 def test_gate_extremes(engine):
     """Gates from no decay at all (log alpha = 0) down to -80 per token (the
-    state is wiped), beta in {0, 1}, on one packed batch."""
+    state is wiped), beta in {0, 1}, on one packed batch; the tensor engine
+    takes its direct-exponent path for the chunks of the strongest decays."""
+    import kimi_delta_attention_chunkwise_gb300 as kda
     rng = np.random.default_rng(101)
     w = inputs.prefill(101, [130, 70, 64], H=2, d=128, dtype="bf16", init_std=0.5)
     T = w.T
@@ -81,7 +101,13 @@ def test_gate_extremes(engine):
     b[1::3] = 1.0
     w.beta = b
     assert T == 264
+    kda.kda_chunk_path_counts()  # clear
     _check(w, engine)
+    mid, half, direct = kda.kda_chunk_path_counts()
+    if engine == "tensor":
+        assert direct > 0 and mid > 0, (mid, half, direct)
+    else:
+        assert (mid, half, direct) == (0, 0, 0)
 
 
 @pytest.mark.parametrize("d,C", [(16, 16), (32, 32), (64, 64), (128, 32), (64, 16)])
@@ -198,13 +224,14 @@ def test_engines_agree():
                                        ([135000], 32)])
 def test_launch_orders_agree(lengths, H):
     """When the scan's CTAs fit in half the SMs, the tensor engine runs the
-    scan concurrently with the prep (image flags) for calls of at most 65,536
-    (chunk, head) items (the first two cases), and the prep first, then the
-    output pass beside the scan (state flags) for larger ones (67,520 items
-    for 135,000 tokens x 32 heads).  With more scan CTAs (160 for 40
-    sequences x 2 heads x 2 value tiles) or with per-kernel events it runs
-    them in sequence.  All orders run the same arithmetic, so the results
-    are bit-identical, and they match the oracle."""
+    scan beside the persistent prep on the SMs the prep leaves (image flags)
+    for calls of at most 65,536 (chunk, head) items (the first two cases),
+    and the prep on every SM, then the scan with the output pass beside it
+    (state flags), for larger ones (67,520 items for 135,000 tokens x 32
+    heads).  With more scan CTAs (160 for 40 sequences x 2 heads x 2 value
+    tiles) or with per-kernel events it runs them in sequence.  All orders
+    run the same arithmetic, so the results are bit-identical, and they match
+    the oracle."""
     import torch
     import kimi_delta_attention_chunkwise_gb300 as kda
     w = inputs.prefill(109, lengths, H=H, d=128, dtype="bf16", init_std=0.02)
@@ -219,7 +246,7 @@ def test_launch_orders_agree(lengths, H):
         e.record()  # the library records them again; they must exist first
     o2 = torch.empty_like(o1)
     kda.kda_chunk_fwd_ws_timed(*args, o2, fin[1], ev, engine="tensor", out_f32=True)
-    torch.cuda.synchronize()
+    assert kda.kda_device_status() == kda.KDA_SUCCESS
     torch.testing.assert_close(o1, o2, rtol=0, atol=0)
     torch.testing.assert_close(fin[0], fin[1], rtol=0, atol=0)
     if w.T <= 4096 and w.H <= 8:
