@@ -62,9 +62,10 @@ def parse_args():
     ap.add_argument("--preroll", type=float, default=0.3,
                     help="seconds of back-to-back steps before each timed loop (0: none, "
                          "for profiler runs)")
-    ap.add_argument("--profile", action="store_true",
-                    help="run only the single-head-group prefill, --warmup + --steps plain calls "
-                         "and nothing else (for counter captures, which need a small case)")
+    ap.add_argument("--profile", choices=["prefill", "backward"], default=None,
+                    help="run only the single-head-group prefill (or its chunk-form backward), "
+                         "--warmup + --steps plain calls and nothing else (for counter "
+                         "captures, which need a small case)")
     ap.add_argument("--sweep", action="store_true",
                     help="with --impl reference: time the oracle on every named workload "
                          "(one JSON line each)")
@@ -729,9 +730,11 @@ def run_k3_gates(args, dist, dev, stream):
 
 
 def run_profile_case(args, dist):
-    """--profile: the single-head-group prefill (B=1, H=16, T=4096) called
-    --warmup + --steps times through the public call, no timing, no other row:
-    a small case for a profiler to capture (inputs ~100 MB, scratch ~113 MB)."""
+    """--profile prefill: the single-head-group prefill (B=1, H=16, T=4096)
+    called --warmup + --steps times through the public call, no timing, no
+    other row: a small case for a profiler to capture (inputs ~100 MB,
+    scratch ~113 MB).  --profile backward: its chunk-form gradients
+    (kda_chunk_bwd) instead."""
     import torch
     import kimi_delta_attention_chunkwise_gb300 as kda
     from kimi_delta_attention_chunkwise_gb300 import build, inputs
@@ -747,11 +750,21 @@ def run_profile_case(args, dist):
     out = torch.empty_like(q)
     fin = torch.empty((1, w.H, w.d_k, w.d_v), dtype=torch.float32, device=dev)
     n = args.warmup + args.steps
-    for _ in range(n):
-        kda.kda_chunk_fwd(q, k, v, la, beta, w.scale, None, cu, out, fin, engine=args.engine)
+    if args.profile == "backward":
+        import numpy as np
+        rng = np.random.default_rng(8)
+        do = t(rng.standard_normal((w.T, w.H, w.d_v)).astype(np.float32), torch.bfloat16)
+        dsf = t(rng.standard_normal((1, w.H, w.d_k, w.d_v)).astype(np.float32))
+        for _ in range(n):
+            kda.kda_chunk_bwd(q, k, v, la, beta, w.scale, None, cu, do, dsf)
+    else:
+        for _ in range(n):
+            kda.kda_chunk_fwd(q, k, v, la, beta, w.scale, None, cu, out, fin,
+                              engine=args.engine)
     st = kda.kda_device_status()
     if dist.rank == 0:
-        print(json.dumps({"profile_case": w.name, "calls": n, "device_status": st}), flush=True)
+        print(json.dumps({"profile_case": w.name, "what": args.profile, "calls": n,
+                          "device_status": st}), flush=True)
 
 
 def run_decode(args, dist, peaks, dev, stream):

@@ -399,18 +399,4 @@ cudaError_t launch_recurrent_bwd(const BwdArgs &a, cudaStream_t stream) {
     return launch_bwd_dtype<float>(a, stream);
 }
 
-size_t recurrent_bwd_tiles16_workspace_bytes(int32_t N, int32_t T, int32_t H) {
-    constexpr int32_t D = 128;
-    const size_t ntile = D / 16, rows = (size_t)T * H;
-    return ckpt_bytes(N, T, H, D) + (size_t)N * H * CK * (size_t)D * D * sizeof(float) +
-           (3 * ntile * rows * D + ntile * rows) * sizeof(float);
-}
-
-cudaError_t launch_recurrent_bwd_tiles16(const BwdArgs &a, cudaStream_t stream) {
-    if (a.D != 128) return cudaErrorInvalidValue;
-    if ((int64_t)a.N * a.H == 0) return cudaSuccess;
-    if (a.dtype == KDA_DTYPE_BF16) return launch_bwd_tile<__nv_bfloat16, 128, 16>(a, stream);
-    return launch_bwd_tile<float, 128, 16>(a, stream);
-}
-
 }  // namespace kda

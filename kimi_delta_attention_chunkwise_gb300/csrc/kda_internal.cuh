@@ -93,11 +93,6 @@ struct BwdArgs {
 };
 size_t recurrent_bwd_workspace_bytes(int32_t N, int32_t T, int32_t H, int32_t D);
 cudaError_t launch_recurrent_bwd(const BwdArgs &a, cudaStream_t stream);
-// The same walk with 16-column tiles whatever the (sequence, head) count
-// (bf16 or fp32 inputs, D = 128): for many short sequences (the chunk form's
-// 64-token segments), where more CTAs with less work each pay.
-size_t recurrent_bwd_tiles16_workspace_bytes(int32_t N, int32_t T, int32_t H);
-cudaError_t launch_recurrent_bwd_tiles16(const BwdArgs &a, cudaStream_t stream);
 
 // Chunkwise backward (kda_backward_chunk.cu): the forward engine's images, a
 // reverse scan over chunks for the state gradient at every chunk boundary,
