@@ -62,10 +62,12 @@ def parse_args():
     ap.add_argument("--preroll", type=float, default=0.3,
                     help="seconds of back-to-back steps before each timed loop (0: none, "
                          "for profiler runs)")
-    ap.add_argument("--profile", choices=["prefill", "backward"], default=None,
-                    help="run only the single-head-group prefill (or its chunk-form backward), "
-                         "--warmup + --steps plain calls and nothing else (for counter "
-                         "captures, which need a small case)")
+    ap.add_argument("--profile", choices=["prefill", "backward", "decode", "recurrent", "conv"],
+                    default=None,
+                    help="run only one small case, --warmup + --steps plain calls and nothing "
+                         "else (for counter captures): the single-head-group prefill, its "
+                         "chunk-form backward, the decode step (256 x 32 heads), the 8-token "
+                         "multi-token pass, or the short convolution")
     ap.add_argument("--sweep", action="store_true",
                     help="with --impl reference: time the oracle on every named workload "
                          "(one JSON line each)")
@@ -750,6 +752,12 @@ def run_profile_case(args, dist):
     out = torch.empty_like(q)
     fin = torch.empty((1, w.H, w.d_k, w.d_v), dtype=torch.float32, device=dev)
     n = args.warmup + args.steps
+    if args.profile in ("decode", "recurrent", "conv"):
+        st = run_profile_other(args, dev)
+        if dist.rank == 0:
+            print(json.dumps({"profile_case": args.profile, "calls": n, "device_status": st}),
+                  flush=True)
+        return
     if args.profile == "backward":
         import numpy as np
         rng = np.random.default_rng(8)
@@ -765,6 +773,48 @@ def run_profile_case(args, dist):
     if dist.rank == 0:
         print(json.dumps({"profile_case": w.name, "what": args.profile, "calls": n,
                           "device_status": st}), flush=True)
+
+
+def run_profile_other(args, dev):
+    """--profile decode / recurrent / conv: the decode step of 256 sequences x
+    32 heads (512 MiB state), the 8-token multi-token pass on the same batch,
+    or the short convolution at K3 width (12,288 channels, 4,096 tokens),
+    --warmup + --steps calls each."""
+    import numpy as np
+    import torch
+    import kimi_delta_attention_chunkwise_gb300 as kda
+    from kimi_delta_attention_chunkwise_gb300 import inputs
+    n = args.warmup + args.steps
+    t = lambda a, dt=None: torch.from_numpy(a).to(dev, dt)
+    if args.profile == "decode":
+        dw = inputs.batched_decode(steps=n)
+        q, k, v = (t(a, torch.bfloat16) for a in (dw.q, dw.k, dw.v))
+        la, b, state = t(dw.log_alpha), t(dw.beta), t(dw.initial_state)
+        out = torch.empty(q.shape[1:], dtype=torch.bfloat16, device=dev)
+        for i in range(n):
+            kda.kda_recurrent_step(q[i], k[i], v[i], la[i], b[i], dw.scale, state, out)
+    elif args.profile == "recurrent":
+        N, H, d, L = 256, 32, 128, 8
+        w = inputs.prefill(5, [L] * N, H=H, d=d, dtype="bf16", init_std=0.02)
+        q, k, v = (t(a, torch.bfloat16) for a in (w.q, w.k, w.v))
+        la, b, cu, pool = t(w.log_alpha), t(w.beta), t(w.cu_seqlens), t(w.initial_state)
+        slots = torch.arange(N, dtype=torch.int32, device=dev).flip(0).contiguous()
+        for _ in range(n):
+            kda.kda_recurrent_fwd(q, k, v, la, b, w.scale, pool, cu, slots)
+    else:
+        C, W = 12288, 4
+        rng = np.random.default_rng(6)
+        lengths = [1000, 17, 2048, 1031]
+        T = sum(lengths)
+        cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32), device=dev)
+        x = t(rng.standard_normal((T, C)).astype(np.float32), torch.bfloat16)
+        wt = t((rng.standard_normal((C, W)) * 0.5).astype(np.float32))
+        bias = t(rng.standard_normal(C).astype(np.float32))
+        cin = torch.zeros((len(lengths), C, W), dtype=torch.bfloat16, device=dev)
+        cout = torch.empty_like(cin)
+        for _ in range(n):
+            kda.kda_short_conv_fwd(x, wt, bias, cu, cin, cout, silu=True)
+    return kda.kda_device_status()
 
 
 def run_decode(args, dist, peaks, dev, stream):
