@@ -62,12 +62,13 @@ def parse_args():
     ap.add_argument("--preroll", type=float, default=0.3,
                     help="seconds of back-to-back steps before each timed loop (0: none, "
                          "for profiler runs)")
-    ap.add_argument("--profile", choices=["prefill", "backward", "decode", "recurrent", "conv"],
+    ap.add_argument("--profile", choices=["prefill", "backward", "backward_recurrent", "decode",
+                                          "recurrent", "conv"],
                     default=None,
                     help="run only one small case, --warmup + --steps plain calls and nothing "
                          "else (for counter captures): the single-head-group prefill, its "
-                         "chunk-form backward, the decode step (256 x 32 heads), the 8-token "
-                         "multi-token pass, or the short convolution")
+                         "chunk-form or recurrent-form backward, the decode step (256 x 32 "
+                         "heads), the 8-token multi-token pass, or the short convolution")
     ap.add_argument("--sweep", action="store_true",
                     help="with --impl reference: time the oracle on every named workload "
                          "(one JSON line each)")
@@ -735,8 +736,8 @@ def run_profile_case(args, dist):
     """--profile prefill: the single-head-group prefill (B=1, H=16, T=4096)
     called --warmup + --steps times through the public call, no timing, no
     other row: a small case for a profiler to capture (inputs ~100 MB,
-    scratch ~113 MB).  --profile backward: its chunk-form gradients
-    (kda_chunk_bwd) instead."""
+    scratch ~113 MB).  --profile backward / backward_recurrent: its gradients
+    through kda_chunk_bwd / kda_recurrent_bwd instead."""
     import torch
     import kimi_delta_attention_chunkwise_gb300 as kda
     from kimi_delta_attention_chunkwise_gb300 import build, inputs
@@ -758,13 +759,14 @@ def run_profile_case(args, dist):
             print(json.dumps({"profile_case": args.profile, "calls": n, "device_status": st}),
                   flush=True)
         return
-    if args.profile == "backward":
+    if args.profile in ("backward", "backward_recurrent"):
         import numpy as np
         rng = np.random.default_rng(8)
         do = t(rng.standard_normal((w.T, w.H, w.d_v)).astype(np.float32), torch.bfloat16)
         dsf = t(rng.standard_normal((1, w.H, w.d_k, w.d_v)).astype(np.float32))
+        fn = kda.kda_chunk_bwd if args.profile == "backward" else kda.kda_recurrent_bwd
         for _ in range(n):
-            kda.kda_chunk_bwd(q, k, v, la, beta, w.scale, None, cu, do, dsf)
+            fn(q, k, v, la, beta, w.scale, None, cu, do, dsf)
     else:
         for _ in range(n):
             kda.kda_chunk_fwd(q, k, v, la, beta, w.scale, None, cu, out, fin,
