@@ -399,7 +399,8 @@ chunk_rscan_kernel(const uint8_t *__restrict__ mt_img, const float *__restrict__
                 uint8_t *img = sm.sb[n & 1] + (k >> 5) * 4096u;
 #pragma unroll
                 for (int j = 0; j < RBV; ++j)
-                    *reinterpret_cast<float *>(img + sw128_offset_f32(j, k & 31)) = to_tf32(dS[j]);
+                    *reinterpret_cast<float *>(img + sw128_offset_f32(j, k & 31)) =
+                        tf32_operand(dS[j]);
                 fence_proxy_async();
             };
             put_state(0);

@@ -243,6 +243,12 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t *cu, in
 //       128 K in 4 panels (32 KB) (direct path: G f32 [64][128]) -> A^kk and
 //       A^kk^T (f16, 8 KB each) and (beta Gamma K)^T (f16, 128 x 64, 16 KB)
 //       -> Z staging (at 0).
+// TMEM (fp32, lane = row): cols 0..63 the decayed products; 64..95 the half
+// path's cross block; 96..159 (beta Gamma K)^T and K_end^T as f16 pairs,
+// parked while the first products still read their operand slots; 160..191
+// the half path's K_hat about token 48, likewise; 192..255 -Q_hat^T.  Then
+// Z (0..63) and W^T (64..127); then M' (0..127), P' (128..191) and -Q'^T
+// (192..255, accumulated onto -Q_hat^T).
 //
 // The decayed products exp(G_i - G_j) (j <= i, so at most 1) are split as
 // exp(G_i - G_r) * exp(G_r - G_j) about a reference token r, in one of three
@@ -686,21 +692,78 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
                 store_row_f16_image(aqk, tid, row);
             }
             wbar(bid);
+            // The direct path's last uses of G, k and q (the tf32 paths made them
+            // while building their operands): -Q_hat^T (Q_hat_i = s Gamma_i q_i)
+            // into TMEM cols 192..255 (lane d, token columns), where the last MMA
+            // group adds (A^qk W)^T to give -Q'^T; (beta Gamma K)^T and K_end^T (row
+            // d, this thread's half of the tokens, f16) into their operand slots.
+            {
+                float row[32];
+#pragma unroll
+                for (int ii = 0; ii < HALF; ++ii)
+                    row[ii] = -scale * exp2_approx(G[ii]) * qval(ii);
+                tmem_st32(tmem_addr(tmem, (warp & 3) * 32, 192 + hf * 32), row);
+#pragma unroll
+                for (int ii = 0; ii < HALF; ++ii)
+                    row[ii] = sm.beta[i0 + ii] * exp2_approx(G[ii]) * kval(ii);
+                store_quarter_f16_image(a2, d, hf * 4, row);
+#pragma unroll
+                for (int ii = 0; ii < HALF; ++ii) row[ii] = exp2_approx(Gl - G[ii]) * kval(ii);
+                store_quarter_f16_image(ket, d, hf * 4, row);
+            }
         } else {
             // The decay-factorised tf32 operands, token by token.
+            // With them, the last uses of G, k and q, so that they leave the
+            // registers here: -Q_hat^T (Q_hat_i = s Gamma_i q_i) into TMEM cols
+            // 192..255 (lane d, token columns), where the last MMA group adds
+            // (A^qk W)^T to give -Q'^T; (beta Gamma K)^T and K_end^T as f16 pairs
+            // into TMEM cols 96..159 until the products free their operand slots
+            // (per 8 tokens: 4 columns of beta Gamma K, then 4 of K_end).
             const uint32_t pa = (d >> 5) * 16384u, pb = (d >> 5) * 8192u;
+            const uint32_t tl = tmem_addr(tmem, (warp & 3) * 32, 0);
 #pragma unroll
-            for (int ii = 0; ii < HALF; ++ii) {
-                const int i = i0 + ii;
-                const float kv = kval(ii), qv = qval(ii);
-                const float ep = exp2_approx(G[ii] - Gr), en = exp2_approx(Gr - G[ii]);
-                *reinterpret_cast<float *>(sm.a1 + pa + sw128_offset_f32(i, d & 31)) =
-                    to_tf32(kv * ep);
-                *reinterpret_cast<float *>(sm.a1 + pa + sw128_offset_f32(64 + i, d & 31)) =
-                    to_tf32(qv * ep);
-                *reinterpret_cast<float *>(sm.b1 + pb + sw128_offset_f32(i, d & 31)) =
-                    to_tf32(kv * en);
+            for (int g8 = 0; g8 < HALF / 8; ++g8) {
+                uint32_t qh[8], pk[8];
+                float bk0 = 0.f, ke0 = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int ii = g8 * 8 + e, i = i0 + ii;
+                    const float kv = kval(ii), qv = qval(ii);
+                    const float ep = exp2_approx(G[ii] - Gr), en = exp2_approx(Gr - G[ii]);
+                    *reinterpret_cast<float *>(sm.a1 + pa + sw128_offset_f32(i, d & 31)) =
+                        tf32_operand(kv * ep);
+                    *reinterpret_cast<float *>(sm.a1 + pa + sw128_offset_f32(64 + i, d & 31)) =
+                        tf32_operand(qv * ep);
+                    *reinterpret_cast<float *>(sm.b1 + pb + sw128_offset_f32(i, d & 31)) =
+                        tf32_operand(kv * en);
+                    const float gam = exp2_approx(G[ii]);
+                    const float bk = sm.beta[i] * gam * kv, ke = exp2_approx(Gl - G[ii]) * kv;
+                    qh[e] = __float_as_uint(-scale * gam * qv);
+                    if (e & 1) {
+                        pk[e >> 1] = pack_f16x2(bk0, bk);
+                        pk[4 + (e >> 1)] = pack_f16x2(ke0, ke);
+                    } else {
+                        bk0 = bk;
+                        ke0 = ke;
+                    }
+                }
+                tmem_st8_nowait(tl + 192 + hf * 32 + g8 * 8, qh);
+                tmem_st8_nowait(tl + 96 + hf * 32 + g8 * 8, pk);
+                if (path == 1 && hf == 0) {
+                    // the half path's K_hat about token 48 for tokens 0..31
+                    // (exponents G_48 - G_j <= 0), parked in cols 160..191
+                    const float G48 = sm.gh1[d];
+                    uint32_t kh[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int ii = g8 * 8 + e;
+                        kh[e] = __float_as_uint(
+                            tf32_operand(kval(ii) * exp2_approx(G48 - G[ii])));
+                    }
+                    tmem_st8_nowait(tl + 160 + g8 * 8, kh);
+                }
             }
+            tmem_wait_st();
             fence_proxy_async();
             tc_fence_before();
             wbar(bid);
@@ -715,16 +778,21 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
             mma_phase ^= 1u;
             if (path == 1) {
                 // Second-half rows, first-half columns: K_hat about token 48 for
-                // tokens 0..31 over the consumed K_hat rows 0..31 (their
-                // exponents G_48 - G_j are <= 0), then A (still intact) times it
-                // into TMEM cols 64..95.
+                // tokens 0..31 (parked in TMEM above) over the consumed K_hat rows
+                // 0..31, then A (still intact) times it into TMEM cols 64..95.
                 tc_fence_after();
                 if (hf == 0) {
-                    const float G48 = sm.gh1[d];
+                    float kh[32];
+                    if (ok) {
+                        tmem_ld32(tmem_addr(tmem, (warp & 3) * 32, 160), kh);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) kh[j] = 0.f;
+                    }
 #pragma unroll
                     for (int ii = 0; ii < HALF; ++ii)
                         *reinterpret_cast<float *>(sm.b1 + pb + sw128_offset_f32(ii, d & 31)) =
-                            to_tf32(kval(ii) * exp2_approx(G48 - G[ii]));
+                            kh[ii];
                 }
                 fence_proxy_async();
                 tc_fence_before();
@@ -740,6 +808,26 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
             }
             ok = __all_sync(0xffffffffu, ok);  // TMEM loads below are warp-collective
             tc_fence_after();
+            {
+                // the parked (beta Gamma K)^T and K_end^T into their operand
+                // slots, which the products have consumed
+                float pv[32];
+                if (ok) {
+                    tmem_ld32(tmem_addr(tmem, (warp & 3) * 32, 96 + hf * 32), pv);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) pv[j] = 0.f;
+                }
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    *reinterpret_cast<uint4 *>(a2 + sw128_chunk(d, hf * 4 + g8)) =
+                        make_uint4(__float_as_uint(pv[g8 * 8 + 0]), __float_as_uint(pv[g8 * 8 + 1]),
+                                   __float_as_uint(pv[g8 * 8 + 2]), __float_as_uint(pv[g8 * 8 + 3]));
+                    *reinterpret_cast<uint4 *>(ket + sw128_chunk(d, hf * 4 + g8)) =
+                        make_uint4(__float_as_uint(pv[g8 * 8 + 4]), __float_as_uint(pv[g8 * 8 + 5]),
+                                   __float_as_uint(pv[g8 * 8 + 6]), __float_as_uint(pv[g8 * 8 + 7]));
+                }
+            }
             // warp w reads TMEM lanes 32*(w%4).., columns 32*(w/4)..; on the half
             // path the block of rows 32..63 (keys and queries) and columns 0..31
             // comes from the second product
@@ -773,23 +861,6 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
             }
         }
         if (hf == 0) gb[d] = exp2_approx(Gl);
-        // The last uses of G, k and q, so that they leave the registers before
-        // the solve: -Q_hat^T (Q_hat_i = s Gamma_i q_i) into TMEM cols 192..255
-        // (lane d, token columns), where the last MMA group adds (A^qk W)^T to
-        // give -Q'^T; (beta Gamma K)^T and K_end^T (row d, this thread's half of
-        // the tokens, f16) into their operand slots, both free by now.
-        {
-            float row[32];
-#pragma unroll
-            for (int ii = 0; ii < HALF; ++ii) row[ii] = -scale * exp2_approx(G[ii]) * qval(ii);
-            tmem_st32(tmem_addr(tmem, (warp & 3) * 32, 192 + hf * 32), row);
-#pragma unroll
-            for (int ii = 0; ii < HALF; ++ii) row[ii] = sm.beta[i0 + ii] * exp2_approx(G[ii]) * kval(ii);
-            store_quarter_f16_image(a2, d, hf * 4, row);
-#pragma unroll
-            for (int ii = 0; ii < HALF; ++ii) row[ii] = exp2_approx(Gl - G[ii]) * kval(ii);
-            store_quarter_f16_image(ket, d, hf * 4, row);
-        }
         for (int idx = tid; idx < C * (C + 1); idx += kPrepWorkerThreads) (&X[0][0])[idx] = 0.f;
         wbar(bid);
 
@@ -960,6 +1031,7 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
 // and the state entering each chunk goes out (f16, the output kernel's B
 // operand image) for the fully parallel output pass.
 constexpr int NSTAGE = 3;                   // image ring depth
+constexpr int kScanPrefetch = 6;            // chunks ahead of the ring, into L2
 constexpr uint32_t SCAN_IMG = IMG_P + 16384;  // -M' and P': the scan's part of an image
 static_assert(SCAN_IMG == IMG_Q0, "the scan's operands lead the image");
 
@@ -972,7 +1044,8 @@ struct ScanSmem {
                                  // bulk copy out)
     uint8_t bv[2][C * 128];      // beta V: K = 64 token rows
     float gbs[NSTAGE][D + C];    // the chunk's Gamma_last [128] and beta [64]
-    uint64_t full[NSTAGE];       // stage loaded (bulk copy -> MMA issuer)
+    uint64_t full[NSTAGE];       // stage's -M' and P' loaded (bulk copy -> MMA issuer)
+    uint64_t full_v[NSTAGE];     // stage's value tile, Gamma_last and beta loaded (-> compute)
     uint64_t empty[NSTAGE];      // stage consumed (tcgen05.commit -> producer)
     uint64_t ready_s;            // S_c operand written (compute -> issuer)
     uint64_t ready_bv[2];        // beta V operand written, per buffer
@@ -1088,6 +1161,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
         if (tid == 0) {
             for (int i = 0; i < NSTAGE; ++i) {
                 mbar_init(&sm.full[i], 1);
+                mbar_init(&sm.full_v[i], 1);
                 mbar_init(&sm.empty[i], 1);
             }
             mbar_init(&sm.ready_s, 128);
@@ -1119,11 +1193,21 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
         };
 
         if (warp == 4) {
-            // -------- producer: -M' and P' of a chunk, once its stage is free --------
+            // -------- producer: a chunk's value tile, Gamma_last and beta (on
+            // full_v, for the compute warps) and its -M' and P' (on full, for
+            // the MMAs), once its stage is free --------
             if (lane == 0) {
                 if (!flags) pdl_wait_primaries();  // the prep has written every image
                 for (int32_t n = 0; n < n_chunks; ++n) {
                     const int stg = n % NSTAGE;
+                    // the image's flag first: its load latency then overlaps the
+                    // wait for the stage
+                    if (flags &&
+                        !flag_wait_bounded(sc.ready + (size_t)(c_begin + n) * H + h,
+                                           wait_cycles)) {
+                        sm.abort_flag = 1;
+                        break;
+                    }
                     if (n >= NSTAGE) {
                         const bool got = mbar_wait_bounded(
                             &sm.empty[stg], (uint32_t)(n / NSTAGE - 1) & 1u, wait_cycles);
@@ -1132,22 +1216,25 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                             break;
                         }
                     }
-                    if (flags) {
-                        // the prep worker of this chunk publishes its image
-                        if (!flag_wait_bounded(sc.ready + (size_t)(c_begin + n) * H + h,
-                                               wait_cycles)) {
-                            sm.abort_flag = 1;
-                            break;
-                        }
-                        fence_proxy_async_global();
-                    }
-                    mbar_arrive_expect_tx(&sm.full[stg],
-                                          SCAN_IMG + C * 128 + (D + C) * (uint32_t)sizeof(float));
-                    bulk_g2s(sm.st[stg], chunk_img(n), SCAN_IMG, &sm.full[stg]);
+                    if (flags) fence_proxy_async_global();
+                    // what the compute warps wait for (beta V of the chunk) ahead of
+                    // the larger -M' and P' that only the MMAs read
+                    mbar_arrive_expect_tx(&sm.full_v[stg],
+                                          C * 128 + (D + C) * (uint32_t)sizeof(float));
                     bulk_g2s(sm.gbs[stg], chunk_img(n) + IMG_GB, (D + C) * sizeof(float),
-                             &sm.full[stg]);
-                    tma_load_3d(sm.vs[stg], &v_map, vt * BV, h, ta + n * C, &sm.full[stg]);
+                             &sm.full_v[stg]);
+                    tma_load_3d(sm.vs[stg], &v_map, vt * BV, h, ta + n * C, &sm.full_v[stg]);
+                    mbar_arrive_expect_tx(&sm.full[stg], SCAN_IMG);
+                    bulk_g2s(sm.st[stg], chunk_img(n), SCAN_IMG, &sm.full[stg]);
                     sm.issued = n + 1;
+                    // a few chunks further on into L2, so that their stage loads
+                    // do not wait on HBM
+                    if (n + kScanPrefetch < n_chunks) {
+                        const uint8_t *im = chunk_img(n + kScanPrefetch);
+                        bulk_prefetch_l2(im, SCAN_IMG);
+                        bulk_prefetch_l2(im + IMG_GB, (D + C) * sizeof(float));
+                        tma_prefetch_l2_3d(&v_map, vt * BV, h, ta + (n + kScanPrefetch) * C);
+                    }
                 }
             }
             __syncwarp();
@@ -1248,7 +1335,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                 mbar_arrive(&sm.ready_bv[n & 1]);
             };
             auto wait_full = [&](int32_t n) {
-                if (!mbar_wait_bounded(&sm.full[n % NSTAGE], (uint32_t)(n / NSTAGE) & 1u,
+                if (!mbar_wait_bounded(&sm.full_v[n % NSTAGE], (uint32_t)(n / NSTAGE) & 1u,
                                        wait_cycles))
                     sm.abort_flag = 1;
             };
@@ -1321,9 +1408,12 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
                 atomicExch(status, (int)KDA_ERR_TIMEOUT);
                 // copies already in flight land before the shared memory goes away
                 const int32_t iss = sm.issued;
-                for (int32_t j = max(iss - NSTAGE, 0); j < iss; ++j)
+                for (int32_t j = max(iss - NSTAGE, 0); j < iss; ++j) {
+                    (void)mbar_wait_bounded(&sm.full_v[j % NSTAGE], (uint32_t)(j / NSTAGE) & 1u,
+                                            wait_cycles);
                     (void)mbar_wait_bounded(&sm.full[j % NSTAGE], (uint32_t)(j / NSTAGE) & 1u,
                                             wait_cycles);
+                }
             }
         }
         tc_fence_before();
@@ -1345,8 +1435,13 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap v_map,
 // Fully parallel once the scan has written every S_c.  128 threads; the
 // A operands are 128-row tiles whose first 64 rows are filler (see IMG_*),
 // so the outputs sit in TMEM lanes 64..127 (warps 2 and 3).
-constexpr uint32_t OUT_IMG_OFF = IMG_Q0 - 8192;      // filler, Q' keys 0..63, Z, Q' keys 64..
+// The output pass's A operands: [filler ; Q' keys 0..63], [Z ; Q' keys 64..127]
+// and [Q' keys 0..63 ; Z] -- 128-row panels whose upper 64 rows only produce
+// TMEM lanes that are never read.  The first 8 KB (filler) is cleared in
+// shared memory, the other 24 KB come from the image.
+constexpr uint32_t OUT_IMG_OFF = IMG_Q0 - 8192;
 constexpr uint32_t OUT_IMG_BYTES = IMG_GB - OUT_IMG_OFF;
+constexpr uint32_t OUT_FILL = 8192;
 static_assert(OUT_IMG_OFF % 1024 == 0 && OUT_IMG_BYTES == 32768, "output operand region");
 
 struct OutSmem {
@@ -1396,9 +1491,10 @@ chunk_out_kernel(const __grid_constant__ CUtensorMap out_map, const __grid_const
         mbar_init(&sm.bar_mma, 1);
         fence_mbar_init();
         // Q'/Z, both S_c tiles, both value tiles and beta, all on one barrier
-        mbar_arrive_expect_tx(&sm.bar_in, OUT_IMG_BYTES + NT * kStateImg + NT * C * 128 +
-                                              C * (uint32_t)sizeof(float));
-        bulk_g2s(sm.qz, img + OUT_IMG_OFF, OUT_IMG_BYTES, &sm.bar_in);
+        mbar_arrive_expect_tx(&sm.bar_in, OUT_IMG_BYTES - OUT_FILL + NT * kStateImg +
+                                              NT * C * 128 + C * (uint32_t)sizeof(float));
+        bulk_g2s(sm.qz + OUT_FILL, img + OUT_IMG_OFF + OUT_FILL, OUT_IMG_BYTES - OUT_FILL,
+                 &sm.bar_in);
         bulk_g2s(sm.sS, sc.sst + ((size_t)c * H + h) * NT * kStateImg, NT * kStateImg,
                  &sm.bar_in);
 #pragma unroll
@@ -1409,6 +1505,9 @@ chunk_out_kernel(const __grid_constant__ CUtensorMap out_map, const __grid_const
         tmem_alloc(&sm.tmem, 128);
         tmem_relinquish();
     }
+    // the filler rows (made visible to the MMAs by the proxy fence below)
+    for (int i = tid; i < (int)(OUT_FILL / 16); i += 128)
+        reinterpret_cast<uint4 *>(sm.qz)[i] = make_uint4(0u, 0u, 0u, 0u);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

@@ -160,6 +160,12 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int32_t x, 
                  : "memory");
 }
 
+// Bulk prefetch of a contiguous global range into L2 (no completion to wait
+// for: a hint).  Address and size multiples of 16 bytes.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Tiled tensor store (TMA) from shared memory, bulk-group completion.
 __device__ __forceinline__ void tma_store_3d(const void *tmap, const void *src, int32_t x,
                                              int32_t y, int32_t z) {
@@ -387,6 +393,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// registers -> TMEM: 8 consecutive 32-bit columns per thread, no wait (the
+// caller issues tcgen05.wait::st before anything depends on the stores).
+__device__ __forceinline__ void tmem_st8_nowait(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // TMEM address of (lane, column): lane in bits [16, 32), column in [0, 16).
 __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint32_t col) {
     return base + (lane << 16) + col;
@@ -402,15 +420,17 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// fp32 -> tf32 rounded to nearest (ties away from zero), kept in fp32 storage,
-// so the tensor core's own reduction of the operand is exact.
-// fp32 -> tf32 (10-bit significand), round to nearest with ties away from
-// zero, by integer arithmetic on the bit pattern: adding half a unit of the
-// 13 dropped bits carries into the kept ones exactly when the dropped part is
-// at least half.  Finite inputs only (the operands here are finite).  Two
-// integer operations instead of a conversion instruction.
-__device__ __forceinline__ float to_tf32(float x) {
-    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
+// An fp32 value as a tf32 MMA operand (10-bit significand), rounded to nearest
+// with ties away from zero.  A tcgen05 MMA of kind::tf32 reads only the top 19
+// bits of each 32-bit operand and drops the other 13, so adding half a unit of
+// the dropped bits (0x1000) to the bit pattern is the whole rounding: the sum
+// carries into the kept bits exactly when the dropped part is at least half,
+// and the tensor core's truncation does the rest (the outputs are bit-identical
+// to those from operands with the low bits cleared as well).  The result is an
+// MMA operand only, not an fp32 value: its low bits are left as they were.
+// Finite inputs only (the operands here are finite).
+__device__ __forceinline__ float tf32_operand(float x) {
+    return __uint_as_float(__float_as_uint(x) + 0x1000u);
 }
 
 // 2^x with the SM's special-function unit (ex2.approx.ftz.f32 of the PTX ISA:
