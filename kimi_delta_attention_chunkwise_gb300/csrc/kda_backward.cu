@@ -65,6 +65,34 @@ __device__ __forceinline__ float row_sum(float x) {
     return x;
 }
 
+// Sums of N values per lane over the 32 lanes of a warp, scattered: each
+// butterfly round keeps the half of the values that this lane's side owns
+// and adds the partner's copy of that half (N/2 shuffles instead of N), so
+// after the rounds with offsets 16, 8, 4 and 2 a lane holds N/16 complete
+// sums, those of indices base .. base + N/16 - 1 with base = N/16 times the
+// lane's bits 1-4 read as a binary number (the values of lanes 2m and 2m+1
+// after a last pairwise sum are the same).  N a multiple of 16.
+template <int N>
+__device__ __forceinline__ void warp_sum_scatter(float (&v)[N], int lane) {
+    static_assert(N % 16 == 0, "four halvings");
+#pragma unroll
+    for (int round = 0; round < 4; ++round) {
+        const int o = 16 >> round, n = N >> (round + 1);
+        const bool hi = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n; ++i) {
+            const float keep = hi ? v[i + n] : v[i], give = hi ? v[i] : v[i + n];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, give, o);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < N / 16; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], 1);
+}
+__device__ __forceinline__ int warp_sum_scatter_base(int lane, int per_lane) {
+    return per_lane * (((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 +
+                       ((lane >> 1) & 1));
+}
+
 // dq, dk, dlog_alpha ([tiles][T, H, D]) and dbeta ([tiles][T, H]) are the
 // per-tile sums over the tile's columns (the final gradients when NTILE = 1).
 template <typename TIn, int D, int DC>
@@ -252,28 +280,63 @@ recurrent_bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
                 if (tid == 0) dbeta[tile_out + (size_t)t * H + h] = acc;
             }
             const float4 dp4 = reinterpret_cast<const float4 *>(s_dp)[cg];
+            if constexpr (CG == 32) {
+                // a whole warp shares the rows: their sums over the tile's
+                // columns by one scatter-reduction (dq, dk, dlog_alpha parts)
+                float red[3 * ROWS];
 #pragma unroll
-            for (int r = 0; r < ROWS; ++r) {
-                const int row = row0 + r;
-                const float a = s_a[i][row], kr = s_k[i][row];
-                const float4 sp = s[r];
-                float4 &d = ds[r];
-                // dSb = dS + k dp^T
-                d.x += kr * dp4.x; d.y += kr * dp4.y; d.z += kr * dp4.z; d.w += kr * dp4.w;
-                const float dkb = a * (sp.x * dp4.x + sp.y * dp4.y + sp.z * dp4.z + sp.w * dp4.w);
-                const float da = d.x * sp.x + d.y * sp.y + d.z * sp.z + d.w * sp.w;
-                const float q_sum = row_sum<CG>(dq_r[r]);
-                const float k_sum = row_sum<CG>(dka_r[r] + dkb);
-                const float a_sum = row_sum<CG>(da);
-                if (cg == 0) {
-                    const size_t o = (tile_out + (size_t)t * H + h) * D + row;
-                    dq[o] = scale * q_sum;
-                    dk[o] = k_sum;
-                    dlog_alpha[o] = a * a_sum;
+                for (int r = 0; r < ROWS; ++r) {
+                    const int row = row0 + r;
+                    const float a = s_a[i][row], kr = s_k[i][row];
+                    const float4 sp = s[r];
+                    float4 &d = ds[r];
+                    // dSb = dS + k dp^T
+                    d.x += kr * dp4.x; d.y += kr * dp4.y; d.z += kr * dp4.z; d.w += kr * dp4.w;
+                    const float dkb =
+                        a * (sp.x * dp4.x + sp.y * dp4.y + sp.z * dp4.z + sp.w * dp4.w);
+                    red[r] = dq_r[r];
+                    red[ROWS + r] = dka_r[r] + dkb;
+                    red[2 * ROWS + r] = d.x * sp.x + d.y * sp.y + d.z * sp.z + d.w * sp.w;
+                    d.x *= a; d.y *= a; d.z *= a; d.w *= a;  // dS_prev = Diag(a) dSb
                 }
-                d.x *= a; d.y *= a; d.z *= a; d.w *= a;  // dS_prev = Diag(a) dSb
+                warp_sum_scatter(red, lane);
+                if ((lane & 1) == 0) {
+                    constexpr int PER = 3 * ROWS / 16;
+                    const int base = warp_sum_scatter_base(lane, PER);
+#pragma unroll
+                    for (int e = 0; e < PER; ++e) {
+                        const int idx = base + e, which = idx / ROWS, row = row0 + idx % ROWS;
+                        const size_t o = (tile_out + (size_t)t * H + h) * D + row;
+                        const float x = red[e];
+                        if (which == 0) dq[o] = scale * x;
+                        else if (which == 1) dk[o] = x;
+                        else dlog_alpha[o] = s_a[i][row] * x;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    const int row = row0 + r;
+                    const float a = s_a[i][row], kr = s_k[i][row];
+                    const float4 sp = s[r];
+                    float4 &d = ds[r];
+                    // dSb = dS + k dp^T
+                    d.x += kr * dp4.x; d.y += kr * dp4.y; d.z += kr * dp4.z; d.w += kr * dp4.w;
+                    const float dkb =
+                        a * (sp.x * dp4.x + sp.y * dp4.y + sp.z * dp4.z + sp.w * dp4.w);
+                    const float da = d.x * sp.x + d.y * sp.y + d.z * sp.z + d.w * sp.w;
+                    const float q_sum = row_sum<CG>(dq_r[r]);
+                    const float k_sum = row_sum<CG>(dka_r[r] + dkb);
+                    const float a_sum = row_sum<CG>(da);
+                    if (cg == 0) {
+                        const size_t o = (tile_out + (size_t)t * H + h) * D + row;
+                        dq[o] = scale * q_sum;
+                        dk[o] = k_sum;
+                        dlog_alpha[o] = a * a_sum;
+                    }
+                    d.x *= a; d.y *= a; d.z *= a; d.w *= a;  // dS_prev = Diag(a) dSb
+                }
             }
-            (void)lane;
         }
     }
     if (d_initial) {

@@ -285,15 +285,22 @@ struct PrepSmem {
     uint32_t n_path[3];  // items per decay path (thread 0)
 };
 constexpr size_t kPrepWorkerBytes = (sizeof(PrepSmem) + 1023) & ~size_t(1023);
-constexpr uint32_t kOffX = C * (C + 1) * 4;        // X after R inside a1
-constexpr uint32_t kOffTb = 2 * C * (C + 1) * 4;   // block products after X
+// R and X rows are kRS floats apart (a multiple of 4: rows load as float4;
+// 68 = 4 mod 32 keeps the column reads of the transposed A^kk store at most
+// two-way bank conflicted); the block products Tb rows kTS floats apart.
+constexpr int kRS = C + 4;
+constexpr int kTS = 34;
+constexpr uint32_t kOffX = C * kRS * 4;            // X after R inside a1
+constexpr uint32_t kOffTb = 2 * C * kRS * 4;       // block products after X
 constexpr uint32_t kOffAqk = 40960;                // A^qk (f16) inside a1
 constexpr uint32_t kOffKe = 49152;                 // K_end^T (f16) inside a1
 constexpr uint32_t kOffAkT = 8192;                 // A^kk^T after A^kk inside b1
 constexpr uint32_t kOffA2 = 16384;                 // (beta Gamma K)^T inside b1
-static_assert(kOffTb + 32 * 33 * 4 <= kOffAqk, "solve scratch below A^qk");
+static_assert(kOffTb + 32 * kTS * 4 <= kOffAqk, "solve scratch below A^qk");
 constexpr uint32_t kInBytes = 2 * C * D * 2 + C * D * 4;  // k, q bf16 + g f32 tiles
-static_assert(kOffTb + 32 * 33 * 4 <= 4 * 16384, "a1 reuse");
+static_assert(kOffTb + 32 * kTS * 4 <= 4 * 16384, "a1 reuse");
+static_assert(kOffX % 16 == 0 && kOffTb % 16 == 0 && kRS % 4 == 0 && kTS % 2 == 0,
+              "vector access to R, X and Tb");
 static_assert(MID == HALF, "the reference token opens the second half");
 
 // Named barrier over one worker's 256 threads (ids 1 and 2; 0 is the CTA's),
@@ -358,67 +365,80 @@ __device__ __forceinline__ void store_quarter_f16_image(uint8_t *img, uint32_t r
 // two 32 x 32 diagonal blocks (16 x 16 halves), level 2 to the whole 64 x 64
 // (32 x 32 halves); B is the block of R below the diagonal.  The products run
 // over full K ranges: X is zero above its diagonal.  One worker (256 threads).
-__device__ __forceinline__ void solve_level16(float (*R)[C + 1], float (*X)[C + 1],
-                                              float (*Tb)[33], int tid, int bid) {
+__device__ __forceinline__ void solve_level16(float (*R)[kRS], float (*X)[kRS],
+                                              float (*Tb)[kTS], int tid, int bid) {
     // thread -> 32 x 32 block p, one row of its lower-left 16 x 16, two columns
     const int p = tid >> 7, t = tid & 127, o = 32 * p;
     const int lr = t >> 3, lc = (t & 7) * 2;
     const int r = o + 16 + lr, c = o + lc;
     float a0 = 0.f, a1 = 0.f;  // (B A^-1)[r][c]
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        const float rv = R[r][o + k];
-        a0 = fmaf(rv, X[o + k][c], a0);
-        a1 = fmaf(rv, X[o + k][c + 1], a1);
+    for (int k4 = 0; k4 < 4; ++k4) {
+        const float4 rv = *reinterpret_cast<const float4 *>(&R[r][o + 4 * k4]);
+        const float rs[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 xv = *reinterpret_cast<const float2 *>(&X[o + 4 * k4 + e][c]);
+            a0 = fmaf(rs[e], xv.x, a0);
+            a1 = fmaf(rs[e], xv.y, a1);
+        }
     }
-    Tb[16 * p + lr][lc] = a0;
-    Tb[16 * p + lr][lc + 1] = a1;
+    *reinterpret_cast<float2 *>(&Tb[16 * p + lr][lc]) = make_float2(a0, a1);
     wbar(bid);
     float b0 = 0.f, b1 = 0.f;  // (D^-1 B A^-1)[r][c]
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-        const float xv = X[r][o + 16 + m];
-        b0 = fmaf(xv, Tb[16 * p + m][lc], b0);
-        b1 = fmaf(xv, Tb[16 * p + m][lc + 1], b1);
+    for (int m4 = 0; m4 < 4; ++m4) {
+        const float4 xv = *reinterpret_cast<const float4 *>(&X[r][o + 16 + 4 * m4]);
+        const float xs[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 tv = *reinterpret_cast<const float2 *>(&Tb[16 * p + 4 * m4 + e][lc]);
+            b0 = fmaf(xs[e], tv.x, b0);
+            b1 = fmaf(xs[e], tv.y, b1);
+        }
     }
-    X[r][c] = -b0;
-    X[r][c + 1] = -b1;
+    *reinterpret_cast<float2 *>(&X[r][c]) = make_float2(-b0, -b1);
     wbar(bid);
 }
-
-__device__ __forceinline__ void solve_level32(float (*R)[C + 1], float (*X)[C + 1],
-                                              float (*Tb)[33], int tid, int bid) {
+__device__ __forceinline__ void solve_level32(float (*R)[kRS], float (*X)[kRS],
+                                              float (*Tb)[kTS], int tid, int bid) {
     // thread -> 2 x 2 tile of the lower-left 32 x 32: rows 32 + rr.., columns cc..
     const int rr = (tid >> 4) * 2, cc = (tid & 15) * 2, r = 32 + rr;
     float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;  // B A^-1
-#pragma unroll 8
-    for (int k = 0; k < 32; ++k) {
-        const float ra = R[r][k], rb = R[r + 1][k];
-        const float xa = X[k][cc], xb = X[k][cc + 1];
-        a00 = fmaf(ra, xa, a00);
-        a01 = fmaf(ra, xb, a01);
-        a10 = fmaf(rb, xa, a10);
-        a11 = fmaf(rb, xb, a11);
+#pragma unroll 4
+    for (int k4 = 0; k4 < 8; ++k4) {
+        const float4 ra = *reinterpret_cast<const float4 *>(&R[r][4 * k4]);
+        const float4 rb = *reinterpret_cast<const float4 *>(&R[r + 1][4 * k4]);
+        const float as[4] = {ra.x, ra.y, ra.z, ra.w}, bs[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 xv = *reinterpret_cast<const float2 *>(&X[4 * k4 + e][cc]);
+            a00 = fmaf(as[e], xv.x, a00);
+            a01 = fmaf(as[e], xv.y, a01);
+            a10 = fmaf(bs[e], xv.x, a10);
+            a11 = fmaf(bs[e], xv.y, a11);
+        }
     }
-    Tb[rr][cc] = a00;
-    Tb[rr][cc + 1] = a01;
-    Tb[rr + 1][cc] = a10;
-    Tb[rr + 1][cc + 1] = a11;
+    *reinterpret_cast<float2 *>(&Tb[rr][cc]) = make_float2(a00, a01);
+    *reinterpret_cast<float2 *>(&Tb[rr + 1][cc]) = make_float2(a10, a11);
     wbar(bid);
     float b00 = 0.f, b01 = 0.f, b10 = 0.f, b11 = 0.f;  // D^-1 B A^-1
-#pragma unroll 8
-    for (int m = 0; m < 32; ++m) {
-        const float xa = X[r][32 + m], xb = X[r + 1][32 + m];
-        const float ta = Tb[m][cc], tb = Tb[m][cc + 1];
-        b00 = fmaf(xa, ta, b00);
-        b01 = fmaf(xa, tb, b01);
-        b10 = fmaf(xb, ta, b10);
-        b11 = fmaf(xb, tb, b11);
+#pragma unroll 4
+    for (int m4 = 0; m4 < 8; ++m4) {
+        const float4 xa = *reinterpret_cast<const float4 *>(&X[r][32 + 4 * m4]);
+        const float4 xb = *reinterpret_cast<const float4 *>(&X[r + 1][32 + 4 * m4]);
+        const float as[4] = {xa.x, xa.y, xa.z, xa.w}, bs[4] = {xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 tv = *reinterpret_cast<const float2 *>(&Tb[4 * m4 + e][cc]);
+            b00 = fmaf(as[e], tv.x, b00);
+            b01 = fmaf(as[e], tv.y, b01);
+            b10 = fmaf(bs[e], tv.x, b10);
+            b11 = fmaf(bs[e], tv.y, b11);
+        }
     }
-    X[r][cc] = -b00;
-    X[r][cc + 1] = -b01;
-    X[r + 1][cc] = -b10;
-    X[r + 1][cc + 1] = -b11;
+    *reinterpret_cast<float2 *>(&X[r][cc]) = make_float2(-b00, -b01);
+    *reinterpret_cast<float2 *>(&X[r + 1][cc]) = make_float2(-b10, -b11);
     wbar(bid);
 }
 
@@ -444,9 +464,9 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
     const int wk = threadIdx.x / kPrepWorkerThreads;
     PrepSmem &sm = *reinterpret_cast<PrepSmem *>(base + wk * kPrepWorkerBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + kPrepWorkers * kPrepWorkerBytes);
-    float(*R)[C + 1] = reinterpret_cast<float(*)[C + 1]>(sm.a1);
-    float(*X)[C + 1] = reinterpret_cast<float(*)[C + 1]>(sm.a1 + kOffX);
-    float(*Tb)[33] = reinterpret_cast<float(*)[33]>(sm.a1 + kOffTb);
+    float(*R)[kRS] = reinterpret_cast<float(*)[kRS]>(sm.a1);
+    float(*X)[kRS] = reinterpret_cast<float(*)[kRS]>(sm.a1 + kOffX);
+    float(*Tb)[kTS] = reinterpret_cast<float(*)[kTS]>(sm.a1 + kOffTb);
     uint8_t *b2 = sm.b1;              // A^kk, f16 panel
     uint8_t *akt = sm.b1 + kOffAkT;   // A^kk^T, f16 panel
     uint8_t *a2 = sm.b1 + kOffA2;     // (beta Gamma K)^T, f16 panel
@@ -845,9 +865,14 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
                 const int i = r;  // key-key row
                 const float b = sm.beta[i];
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
+                for (int jj = 0; jj < 32; jj += 4) {
                     const int j = chalf * 32 + jj;
-                    R[i][j] = (j < i && i < L) ? b * v[jj] : 0.f;
+                    float4 w;
+                    w.x = (j < i && i < L) ? b * v[jj] : 0.f;
+                    w.y = (j + 1 < i && i < L) ? b * v[jj + 1] : 0.f;
+                    w.z = (j + 2 < i && i < L) ? b * v[jj + 2] : 0.f;
+                    w.w = (j + 3 < i && i < L) ? b * v[jj + 3] : 0.f;
+                    *reinterpret_cast<float4 *>(&R[i][j]) = w;
                 }
             } else {
                 const int i = r - C;  // query-key row
@@ -861,7 +886,8 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
             }
         }
         if (hf == 0) gb[d] = exp2_approx(Gl);
-        for (int idx = tid; idx < C * (C + 1); idx += kPrepWorkerThreads) (&X[0][0])[idx] = 0.f;
+        for (int idx = tid; idx < C * kRS / 4; idx += kPrepWorkerThreads)
+            reinterpret_cast<float4 *>(&X[0][0])[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
         wbar(bid);
 
         // sec. 6.3: A^kk = (I + R)^-1, unit lower triangular, fp32.  The 16 x 16
@@ -890,10 +916,15 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
             const int row = tid >> 1, q4 = tid & 1;
             float v32[32], t32[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                v32[j] = X[row][q4 * 32 + j];
-                t32[j] = X[q4 * 32 + j][row];
+            for (int j = 0; j < 32; j += 4) {
+                const float4 xv = *reinterpret_cast<const float4 *>(&X[row][q4 * 32 + j]);
+                v32[j] = xv.x;
+                v32[j + 1] = xv.y;
+                v32[j + 2] = xv.z;
+                v32[j + 3] = xv.w;
             }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) t32[j] = X[q4 * 32 + j][row];
             store_quarter_f16_image(b2, row, q4 * 4, v32);
             store_quarter_f16_image(akt, row, q4 * 4, t32);
         }
