@@ -215,10 +215,10 @@ PATH_FLOPS = prefill_flops_per_tok_head(128, 64)
 # kernel, beyond the method's bytes: the prep writes one 74,496-byte image per
 # (chunk, head) (-M', P', Q', Z in f16, Gamma_last and beta); the scan reads
 # its 48 KB -M'/P' part once per 64-wide value tile and writes the chunk's
-# state (f16, 32 KB); the output pass reads Q', Z and filler (32 KB) and the
+# state (f16, 32 KB); the output pass reads Q' and Z (24 KB) and the
 # state (32 KB).  Per token: divide by the chunk's 64 tokens.
 SCRATCH_BYTES = {"prep": 74496 / 64, "scan": (2 * 49152 + 32768) / 64,
-                 "out": (32768 + 32768) / 64}
+                 "out": (24576 + 32768) / 64}
 
 PROFILE_FILES = {
     "prep": ("chunk_prep_prefill_T4096_H16.md", 4096 * 16),
