@@ -497,13 +497,14 @@ kdaStatus_t kda_recurrent_bwd(const void *q, const void *k, const void *v,
  * with M' = K_end^T W and Q' = s Gamma Q - A^qk W as in kda_chunk_fwd; it
  * runs on the tensor cores in tf32 (the gradients keep fp32 range).  With
  * the state entering every chunk (from the forward engine) and the gradient
- * leaving it, each 64-token chunk's gradients are computed independently
- * (the recurrent walk of kda_recurrent_bwd, one chunk long).  Arguments,
- * layouts and outputs as for kda_recurrent_bwd; q, k, v and log_alpha must
- * be 16-byte aligned.  Scratch (the forward engine's, the per-chunk states,
- * their gradients and operands: about (T / 64 + N + 1) * H * 360 KB, plus the
- * recurrent walk's) is taken with cudaMallocAsync / cudaFreeAsync on
- * `stream`.
+ * leaving it, each 64-token chunk's gradients are computed independently, as
+ * tensor-core products of the chunk form's factors (tf32 wherever a gradient
+ * is an operand) and, where the decay across half a chunk exceeds e^-80,
+ * direct exponents for the decayed products.  Arguments, layouts and outputs
+ * as for kda_recurrent_bwd; q, k, v and log_alpha must be 16-byte aligned.
+ * Scratch (the forward engine's images and states, the per-chunk factors,
+ * state gradients and intermediate gradients: about (T / 64 + N + 1) * H *
+ * 490 KB) is taken with cudaMallocAsync / cudaFreeAsync on `stream`.
  */
 kdaStatus_t kda_chunk_bwd(const void *q, const void *k, const void *v,
                           const float *log_alpha, const float *beta, float scale,

@@ -1,4 +1,4 @@
-// kda_backward_chunk.cu -- the chunkwise backward (training), first form.
+// kda_backward_chunk.cu -- the chunkwise backward (training).
 //
 // The pages derive no gradients ("Kimi Unveils Delta Attention and K3
 // Architecture Updates", sec. 6: the chunkwise form serves training).  The
@@ -9,17 +9,16 @@
 //
 // and, once S_c and dS_{c+1} are known at every chunk boundary, each chunk's
 // gradients are independent of the others.  This form:
-//   1. runs the forward engine (its workspace keeps every chunk's f16 M',
-//      Q', exp(G_last) and the f16 state S_c entering the chunk);
-//   2. state_rows_kernel: S_c as fp32 rows;
-//   3. chunk_bwd_aux_kernel: -M'^T as a tf32 operand image and
+//   1. runs the forward engine without its output pass; its workspace keeps
+//      every chunk's f16 M', Q', exp(G_last) and the f16 state S_c entering
+//      the chunk, and its prep also stores every chunk's A^kk and A^qk;
+//   2. chunk_bwd_aux_kernel: -M'^T as a tf32 operand image and
 //      X_c = Q'^T dO_c (one tcgen05 kind::tf32 product) per (chunk, head);
-//   4. chunk_rscan_kernel: the reverse scan, one kind::tf32 product per chunk
-//      on the chain, writing dS_{c+1} at every boundary and dS at every
-//      sequence start (the initial-state gradient);
-//   5. the recurrent backward walk per 64-token chunk, from S_c and dS_{c+1}
-//      (whole-width tiles once there are enough (chunk, head) pairs: 2.9 ms
-//      against 4.5 ms with 16-column tiles on 4,096 tokens x 16 heads).
+//   3. chunk_rscan_kernel: the reverse scan, one kind::tf32 product per chunk
+//      on the chain, writing dS_{c+1} at every boundary (as the transposed
+//      operand tiles it multiplies and as value-contiguous panels) and dS at
+//      every sequence start (the initial-state gradient);
+//   4. the per-chunk gradient pass on the tensor cores (kda_backward_grad.cu).
 // Every product that carries a gradient is tf32 (fp32 range): f16 operands
 // lose gradients of training size to underflow.
 #include <cstdint>
@@ -178,36 +177,6 @@ chunk_bwd_aux_kernel(const uint8_t *__restrict__ img_base, const int2 *__restric
     if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
-// S_c in fp32 rows from the forward scan's f16 state images (one MN-major
-// SW128 image of 128 key rows x 64 value columns per value tile, 16 KB):
-// rows [item][128][128].  Thread -> (row k, 8 columns).
-__global__ void __launch_bounds__(256)
-state_rows_kernel(const uint8_t *__restrict__ sst, const int2 *__restrict__ chunk_tok,
-                  float *__restrict__ rows, size_t n_items, int32_t H) {
-    const size_t item = blockIdx.x;
-    if (item >= n_items) return;
-    if (chunk_tok[item / (size_t)H].y <= 0) {
-        for (int idx = threadIdx.x; idx < AD * AD; idx += 256) rows[item * AD * AD + idx] = 0.f;
-        return;
-    }
-    for (int idx = threadIdx.x; idx < AD * 16; idx += 256) {
-        const int k = idx >> 4, c8 = idx & 15, vt = c8 >> 3, ch = c8 & 7;
-        const uint8_t *img = sst + (item * 2 + vt) * 16384u;
-        const uint4 u = *reinterpret_cast<const uint4 *>(img + sw128_chunk(k, ch));
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-        float *dst = rows + (item * AD + k) * AD + vt * 64 + ch * 8;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const __half2 hv = *reinterpret_cast<const __half2 *>(&w[e]);
-            dst[2 * e] = __low2float(hv);
-            dst[2 * e + 1] = __high2float(hv);
-        }
-    }
-}
-
-
-
-
 constexpr int RD = 128, RC = 64, RBV = 32, RNT = RD / RBV, RSTAGE = 2;
 constexpr uint32_t MT_BYTES = RD * RD * 4;
 constexpr uint32_t XT_BYTES = RD * RBV * 4;
@@ -252,7 +221,7 @@ __device__ __forceinline__ bool rbarrier_or(bool pred) {
 __global__ void __launch_bounds__(kRThreads, 1)
 chunk_rscan_kernel(const uint8_t *__restrict__ mt_img, const float *__restrict__ x_tiles,
                    const float *__restrict__ glv, const float *__restrict__ d_final,
-                   uint8_t *__restrict__ ds_img, float *__restrict__ ds_rows,
+                   uint8_t *__restrict__ ds_img, uint8_t *__restrict__ ds_nat,
                    float *__restrict__ d_initial,
                    const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_off,
                    int32_t N, int32_t T, int32_t H, int *status) {
@@ -389,11 +358,14 @@ chunk_rscan_kernel(const uint8_t *__restrict__ mt_img, const float *__restrict__
             // -------- compute: thread = key row k --------
             const int k = tid;
             auto put_state = [&](int32_t n) {
-                if (ds_rows) {
-                    float *dst = ds_rows + (item_of(n) * RD + k) * RD + (size_t)vt * RBV;
+                if (ds_nat) {
+                    // row k of panel vt of the K-major (value-contiguous) image:
+                    // the exact fp32 values, 128-byte swizzled
+                    uint8_t *dst = ds_nat + item_of(n) * (size_t)(RD * RD * 4) +
+                                   (size_t)vt * (RD * 128);
 #pragma unroll
                     for (int j = 0; j < RBV; j += 4)
-                        *reinterpret_cast<float4 *>(dst + j) =
+                        *reinterpret_cast<float4 *>(dst + sw128_chunk(k, j >> 2)) =
                             make_float4(dS[j], dS[j + 1], dS[j + 2], dS[j + 3]);
                 }
                 uint8_t *img = sm.sb[n & 1] + (k >> 5) * 4096u;
@@ -472,18 +444,10 @@ chunk_rscan_kernel(const uint8_t *__restrict__ mt_img, const float *__restrict__
 }
 
 
-// seg[c] = first token of chunk c (T past the last chunk), seg[max] = T:
-// the chunks as sequences of the recurrent walk.
-__global__ void chunk_segments_kernel(const int2 *__restrict__ chunk_tok, int32_t *__restrict__ seg,
-                                      int32_t n, int32_t T) {
-    for (int32_t c = blockIdx.x * blockDim.x + threadIdx.x; c <= n; c += gridDim.x * blockDim.x)
-        seg[c] = (c < n && chunk_tok[c].y > 0) ? chunk_tok[c].x : T;
-}
-
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct ChunkBwdLayout {
-    size_t fwd, out, rows, mt, x, gl, dsrows, seg, bwd, total;
+    size_t fwd, aux, mt, x, gl, ds_t, ds_n, de, dw, dg, daqk, total;
 };
 
 ChunkBwdLayout chunk_bwd_layout(int32_t N, int32_t T, int32_t H) {
@@ -496,14 +460,16 @@ ChunkBwdLayout chunk_bwd_layout(int32_t N, int32_t T, int32_t H) {
         return o;
     };
     L.fwd = take(chunk_tc_workspace_bytes(N, T, H));
-    L.out = take((size_t)T * H * AD * 2);
-    L.rows = take(items * AD * AD * 4);
+    L.aux = take(items * kBwdAuxBytes);
     L.mt = take(items * MT_BYTES);
     L.x = take(items * RNT * (size_t)XT_BYTES);
     L.gl = take(items * AD * 4);
-    L.dsrows = take(items * AD * AD * 4);
-    L.seg = take((maxc + 1) * 4);
-    L.bwd = take(recurrent_bwd_workspace_bytes((int32_t)maxc, T, H, AD));
+    L.ds_t = take(items * RNT * (size_t)DS_IMG);
+    L.ds_n = take(items * AD * AD * 4);
+    L.de = take(items * AC * AD * 4);
+    L.dw = take(items * AC * AD * 4);
+    L.dg = take(items * AC * AD * 4);
+    L.daqk = take(items * AC * AC * 4);
     L.total = off;
     return L;
 }
@@ -528,26 +494,22 @@ cudaError_t launch_chunk_bwd(const BwdArgs &a, int *status, cudaStream_t stream)
     }
     const ChunkBwdLayout L = chunk_bwd_layout(a.N, a.T, a.H);
     uint8_t *ws = static_cast<uint8_t *>(a.workspace);
-    // 1. the forward engine, for its images (outputs into scratch)
+    // 1. the forward engine, for its images (no outputs), keeping A^kk, A^qk
     StageClock clock;
     ChunkArgs f = {};
     f.q = a.q; f.k = a.k; f.v = a.v; f.log_alpha = a.log_alpha; f.beta = a.beta;
     f.scale = a.scale; f.initial_state = a.initial_state; f.cu_seqlens = a.cu_seqlens;
-    f.out = ws + L.out; f.final_state = nullptr;
+    f.out = nullptr; f.final_state = nullptr;
     f.N = a.N; f.T = a.T; f.H = a.H; f.D = AD; f.C = 64; f.G = 1; f.pro = 0;
     f.gbias = nullptr; f.galog = nullptr; f.dtype = KDA_DTYPE_BF16; f.out_f32 = 0;
     f.status = status; f.clock = &clock;
-    cudaError_t e = launch_chunk_tc(f, ws + L.fwd, L.out - L.fwd, stream);
+    f.bwd_aux = ws + L.aux;
+    f.skip_out = 1;
+    cudaError_t e = launch_chunk_tc(f, ws + L.fwd, L.aux - L.fwd, stream);
     if (e != cudaSuccess) return e;
     const ChunkScratchView view = chunk_tc_scratch_view(ws + L.fwd, a.N, a.T, a.H);
     const size_t maxc = view.max_chunks, items = maxc * a.H;
-    float *rows = reinterpret_cast<float *>(ws + L.rows);
-    float *dsrows = reinterpret_cast<float *>(ws + L.dsrows);
-    int32_t *seg = reinterpret_cast<int32_t *>(ws + L.seg);
-    // 2. S_c as fp32 rows
-    state_rows_kernel<<<(unsigned)items, 256, 0, stream>>>(view.sst, view.chunk_tok, rows, items,
-                                                           a.H);
-    // 3. -M'^T, X_c and exp(G_last) per (chunk, head)
+    // 2. -M'^T, X_c and exp(G_last) per (chunk, head)
     e = cudaFuncSetAttribute(chunk_bwd_aux_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kAuxSmem);
     if (e == cudaSuccess)
@@ -557,24 +519,32 @@ cudaError_t launch_chunk_bwd(const BwdArgs &a, int *status, cudaStream_t stream)
     chunk_bwd_aux_kernel<<<(unsigned)items, 256, kAuxSmem, stream>>>(
         view.img, view.chunk_tok, static_cast<const __nv_bfloat16 *>(a.d_out), ws + L.mt,
         reinterpret_cast<float *>(ws + L.x), reinterpret_cast<float *>(ws + L.gl), a.H, status);
-    // 4. the reverse scan
+    // 3. the reverse scan
     chunk_rscan_kernel<<<dim3((unsigned)(a.N * RNT), (unsigned)a.H), kRThreads, kRSmem, stream>>>(
         ws + L.mt, reinterpret_cast<const float *>(ws + L.x),
-        reinterpret_cast<const float *>(ws + L.gl), a.d_final_state, nullptr, dsrows,
+        reinterpret_cast<const float *>(ws + L.gl), a.d_final_state, ws + L.ds_t, ws + L.ds_n,
         a.d_initial_state, a.cu_seqlens, view.chunk_off, a.N, a.T, a.H, status);
-    // 5. the recurrent walk per chunk, from S_c and dS_{c+1}
-    chunk_segments_kernel<<<(unsigned)((maxc + 256) / 256), 256, 0, stream>>>(
-        view.chunk_tok, seg, (int32_t)maxc, a.T);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    BwdArgs w = a;
-    w.N = (int32_t)maxc;
-    w.cu_seqlens = seg;
-    w.initial_state = rows;
-    w.d_final_state = dsrows;
-    w.d_initial_state = nullptr;
-    w.workspace = ws + L.bwd;
-    return launch_recurrent_bwd(w, stream);
+    // 4. every chunk's gradients from S_c and dS_{c+1}
+    ChunkGradArgs g;
+    g.chunk_tok = view.chunk_tok;
+    g.n_items = items;
+    g.H = a.H;
+    g.scale = a.scale;
+    g.aux = ws + L.aux;
+    g.sst = view.sst;
+    g.ds_t = ws + L.ds_t;
+    g.ds_n = ws + L.ds_n;
+    g.q = a.q; g.k = a.k; g.v = a.v; g.d_out = a.d_out;
+    g.log_alpha = a.log_alpha; g.beta = a.beta;
+    g.dq = a.dq; g.dk = a.dk; g.dv = a.dv; g.dlog_alpha = a.dlog_alpha; g.dbeta = a.dbeta;
+    g.dE = reinterpret_cast<float *>(ws + L.de);
+    g.dW = reinterpret_cast<float *>(ws + L.dw);
+    g.dG = reinterpret_cast<float *>(ws + L.dg);
+    g.dAqk = reinterpret_cast<float *>(ws + L.daqk);
+    g.status = status;
+    return launch_chunk_grad(g, stream);
 }
 
 }  // namespace kda

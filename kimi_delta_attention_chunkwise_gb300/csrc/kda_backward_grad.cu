@@ -1,0 +1,946 @@
+// kda_backward_grad.cu -- the per-chunk gradient pass of the chunkwise
+// backward, on the tensor cores.
+//
+// The pages derive no gradients ("Kimi Unveils Delta Attention and K3
+// Architecture Updates", sec. 6 and 6.6: the chunkwise form serves training);
+// these are the chunk form of sec. 6 differentiated by reverse mode.  For one
+// chunk of one head (tokens i, j; channels a, v; G the chunk-local cumulative
+// log decay, G_l its last row; A = A^kk = (I + R)^-1 and A^qk as the forward
+// engine made them; B1 = Diag(beta) V, B2 = Diag(beta)(exp(G) * K),
+// K_end = exp(G_l - G) * K, Q_hat = s exp(G) * Q), with S = S_c the state
+// entering the chunk and dS = dS_{c+1} the gradient of the state leaving it:
+//
+//   U = A B1,  W = A B2,  E = U - W S                      (forward values)
+//   dE   = A^qk^T dO + K_end dS
+//   dQ_hat = dO S^T,   dW = -dE S^T,   dA^qk = tril_0(dO E^T),   dK_end = E dS^T
+//   dA   = dE B1^T + dW B2^T,   dB1 = A^T dE,   dB2 = A^T dW
+//   dR   = tril_-1(-A^T dA A^T)
+//
+// and through the decayed products R_ij = beta_i <k_i, exp(G_i - G_j) k_j>,
+// A^qk_ij = s <q_i, exp(G_i - G_j) k_j> to q, k and G, as
+//   XR_i = sum_j dR_ij exp(G_i - G_j) k_j       XQ_i = sum_j s dA^qk_ij exp(G_i - G_j) k_j
+//   YY_j = sum_i (beta_i dR_ij k_i + s dA^qk_ij q_i) exp(G_i - G_j)
+// (per channel), each one tensor-core product with the forward's mid-chunk
+// split exp(G_i - G_j) = exp(G_i - G_32) exp(G_32 - G_j) when every
+// |G_i - G_32| <= 80, else evaluated directly on the CUDA cores.  Then
+//   dq = s exp(G) dQ_hat + XQ
+//   dk = exp(G_l - G) dK_end + beta exp(G) dB2 + beta XR + YY
+//   dv = beta dB1,  dbeta = sum_v V dB1 + sum_a exp(G) K dB2 + sum_a K XR
+//   dG = Q_hat dQ_hat - K_end dK_end + B2 dB2 + beta K XR + Q XQ - K YY,
+//        plus, on the chunk's last token, sum_i K_end dK_end + exp(G_l) sum_v S dS
+//   dlog_alpha = the reverse cumulative sum of dG over the chunk's tokens.
+//
+// Two launches over the (chunk, head) items, 256 threads each, one CTA per
+// SM (shared memory), all 512 TMEM columns:
+//   chunk_grad_g1 -- the products with the d x d matrices S and dS: E, dE,
+//                    dQ_hat, dW, dA^qk, dK_end; writes the partial dq, dk and
+//                    dG and the scratch dE, dW, dA^qk.
+//   chunk_grad_g2 -- the C x C products: dA, dB1, dB2, A^T dA, dR, then the
+//                    decayed products' gradients and every output.
+// Operands are K-major 128-byte-swizzled shared-memory panels, staged by the
+// threads from global memory, the forward's images or TMEM readouts.  Every
+// product with a gradient operand is kind::tf32 (gradients need fp32 range);
+// the two whose operands are both forward values (U, W and W S) are
+// kind::f16 on the forward's own f16 factors, as the forward computed them.
+// A 64-row operand of a 128-row MMA is read with the 8 KB that follow it
+// (rows 64..127 give accumulator rows that are never read).
+#include <cstdint>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kda_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace kda {
+namespace {
+using namespace tc;
+
+constexpr int GD = 128, GC = 64, kGThreads = 256;
+constexpr uint32_t U16 = 16384;             // a 128-row tf32 panel (two 64-row ones)
+constexpr uint32_t P8 = 8192;               // a 64-row panel
+constexpr long long kGradWait = 2000000000LL;
+constexpr float kGradSpan2 = 115.f;         // |G_i - G_32| <= 80, in base 2
+constexpr uint32_t kIdF16MnB = idesc_f16_f32(128, 64) | (1u << 16);  // B MN-major
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+// element ii of 32 bf16 values packed in pairs
+__device__ __forceinline__ float bfv(const uint32_t (&p)[16], int ii) {
+    return (ii & 1) ? bf_hi(p[ii >> 1]) : bf_lo(p[ii >> 1]);
+}
+__device__ __forceinline__ float f16_at(const uint8_t *panel, int row, int col) {
+    return __half2float(*reinterpret_cast<const __half *>(panel + sw128_offset(row, col)));
+}
+// fp32 element (row, col) of a K-major panel, col < 32
+__device__ __forceinline__ float &f32_at(uint8_t *panel, int row, int col) {
+    return *reinterpret_cast<float *>(panel + sw128_offset_f32(row, col));
+}
+// 32 consecutive K values of one row of a K-major tf32 panel
+__device__ __forceinline__ void row32_tf32(uint8_t *panel, int row, const float (&v)[32]) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4 *>(panel + sw128_chunk(row, c)) =
+            make_float4(tf32_operand(v[4 * c]), tf32_operand(v[4 * c + 1]),
+                        tf32_operand(v[4 * c + 2]), tf32_operand(v[4 * c + 3]));
+}
+// 64 consecutive K values (two arrays of 32) of one row of a K-major f16 panel
+__device__ __forceinline__ void row64_f16(uint8_t *panel, int row, const float (&v0)[32],
+                                          const float (&v1)[32]) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const float *v = (c < 4 ? v0 : v1) + (c & 3) * 8;
+        uint4 u;
+        u.x = pack_f16x2(v[0], v[1]);
+        u.y = pack_f16x2(v[2], v[3]);
+        u.z = pack_f16x2(v[4], v[5]);
+        u.w = pack_f16x2(v[6], v[7]);
+        *reinterpret_cast<uint4 *>(panel + sw128_chunk(row, c)) = u;
+    }
+}
+__device__ __forceinline__ void zero32(float (&v)[32]) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = 0.f;
+}
+
+// The channel-ch, token-half inputs of one thread: G (base 2, cumulative from
+// the chunk's first token, carried across the halves through shared memory),
+// and k, v, q, dO as packed bf16 pairs; rows past the chunk's L tokens zero.
+struct TokenInputs {
+    float G[32];
+    uint32_t kp[16], vp[16], qp[16], dp[16];
+};
+
+__device__ __forceinline__ void load_inputs(const ChunkGradArgs &a, size_t base, size_t rs,
+                                            int i0, int L, bool want_q, bool want_do,
+                                            TokenInputs &in) {
+    const unsigned short *k16 = static_cast<const unsigned short *>(a.k);
+    const unsigned short *v16 = static_cast<const unsigned short *>(a.v);
+    const unsigned short *q16 = static_cast<const unsigned short *>(a.q);
+    const unsigned short *d16 = static_cast<const unsigned short *>(a.d_out);
+    float acc = 0.f;
+#pragma unroll
+    for (int ii = 0; ii < 32; ++ii) {
+        const int i = i0 + ii;
+        const float lg = i < L ? a.log_alpha[base + (size_t)i * rs] : 0.f;
+        acc = fmaf(lg, kLog2e, acc);
+        in.G[ii] = acc;
+    }
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) {
+        const int ia = i0 + 2 * jj, ib = ia + 1;
+        const size_t ra = base + (size_t)ia * rs, rb = base + (size_t)ib * rs;
+        const bool va = ia < L, vb = ib < L;
+        in.kp[jj] = (va ? k16[ra] : 0u) | ((vb ? (uint32_t)k16[rb] : 0u) << 16);
+        in.vp[jj] = (va ? v16[ra] : 0u) | ((vb ? (uint32_t)v16[rb] : 0u) << 16);
+        in.qp[jj] = want_q ? ((va ? q16[ra] : 0u) | ((vb ? (uint32_t)q16[rb] : 0u) << 16)) : 0u;
+        in.dp[jj] = (want_do && d16)
+                        ? ((va ? d16[ra] : 0u) | ((vb ? (uint32_t)d16[rb] : 0u) << 16))
+                        : 0u;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// G1: the products with S and dS
+// ---------------------------------------------------------------------------
+// Shared arena, in 16 KB units u0..u11 (regions reused once their MMAs have
+// completed):
+//   step 1: dO^T (rows v, K = i) u0-1 | A^kk, A^qk f16 u2 | A^qk^T-rows tf32
+//           (rows j, K = i) u3 | K_end (rows j, K = a) u4-5 | [B1 | B2] f16
+//           MN-major u6-7 | dS^T (rows v, K = a) u8-11
+//   step 2: -W f16 (rows i, K = a) u2 | S_c f16 image u6-7 | S (rows a, K = v)
+//           tf32 panels u0, u1, u4, u5 | [dO ; dE] (rows i, K = v) u8-11
+//   step 3: dS (rows a, K = v) u0-3 | E (rows j, K = v) u4-6 | dO in u8-11
+// TMEM columns: U / E 0..127, W 128..255, dE^T 256..319 -> [dQ_hat^T | -dW^T]
+// 256..383, dA^qk^T 384..447, dK_end^T 448..511.
+struct G1Smem {
+    uint8_t ar[12 * U16];
+    float beta[GC];
+    float gcarry[GD], glast[GD];
+    float sterm[2][GD];   // sum over a value half of dS[a][v] S[a][v]
+    float kterm[2][GD];   // sum over a token half of K_end dK_end
+    uint64_t bar_ld, bar_sf, bar_dsn, bar_m[4];
+    uint32_t tmem;
+};
+constexpr uint32_t G1_DOT = 0, G1_AQ = 2 * U16, G1_AQT = 3 * U16, G1_KE = 4 * U16,
+                   G1_BB = 6 * U16, G1_DST = 8 * U16;
+constexpr uint32_t G1_NW = 2 * U16, G1_SF = 6 * U16, G1_ODE = 8 * U16;
+constexpr uint32_t G1_DSN = 0, G1_E = 4 * U16;
+__device__ __forceinline__ uint32_t g1_s_panel(int p) { return (uint32_t)(p < 2 ? p : p + 2) * U16; }
+constexpr size_t kG1Smem = sizeof(G1Smem) + 1024;
+static_assert(kG1Smem <= 227 * 1024, "G1 shared memory");
+
+__global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g1_kernel(const ChunkGradArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    G1Smem &sm = *reinterpret_cast<G1Smem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *ar = sm.ar;
+    const int tid = threadIdx.x, warp = tid >> 5, quad = warp & 3;
+    const int ch = tid & 127, hf = tid >> 7, i0 = hf * 32;  // channel, token half
+    const size_t item = blockIdx.x;
+    const int32_t H = a.H;
+    const int32_t c = (int32_t)(item / (size_t)H), h = (int32_t)(item % (size_t)H);
+    const int2 tok = a.chunk_tok[c];
+    const int32_t t0 = tok.x, L = tok.y;
+    if (L <= 0) return;
+
+    if (tid == 0) {
+        mbar_init(&sm.bar_ld, 1);
+        mbar_init(&sm.bar_sf, 1);
+        mbar_init(&sm.bar_dsn, 1);
+        for (int m = 0; m < 4; ++m) mbar_init(&sm.bar_m[m], 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&sm.bar_ld, kBwdAuxBytes + 4 * U16);
+        bulk_g2s(ar + G1_AQ, a.aux + item * kBwdAuxBytes, kBwdAuxBytes, &sm.bar_ld);
+        // dS^T as four 128-row panels (K = 32 key channels each) from the
+        // reverse scan's tiles of 32 value rows
+        const uint8_t *dt = a.ds_t + item * (4 * U16);
+        for (int vt = 0; vt < 4; ++vt)
+            for (int p = 0; p < 4; ++p)
+                bulk_g2s(ar + G1_DST + p * U16 + vt * 4096, dt + vt * U16 + p * 4096, 4096,
+                         &sm.bar_ld);
+    }
+    if (warp == 0) {
+        tmem_alloc(&sm.tmem, 512);
+        tmem_relinquish();
+    }
+    const size_t rs = (size_t)H * GD;
+    const size_t base = ((size_t)t0 * H + h) * GD + ch;
+    TokenInputs in;
+    load_inputs(a, base, rs, i0, L, false, true, in);
+    if (tid < GC) sm.beta[tid] = tid < L ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
+    if (hf == 0) sm.gcarry[ch] = in.G[31];
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (hf == 1) {
+        const float cy = sm.gcarry[ch];
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) in.G[ii] += cy;
+        sm.glast[ch] = in.G[31];
+    }
+    __syncthreads();
+    const float Gl = sm.glast[ch];
+    const uint32_t tmem = sm.tmem;
+
+    // ---- step 1 operands: [B1 | B2] (f16, token rows), K_end, dO^T ----
+    {
+        uint8_t *b1 = ar + G1_BB + (ch >> 6) * P8;
+        uint8_t *b2 = ar + G1_BB + (2 + (ch >> 6)) * P8;
+        uint8_t *ke = ar + G1_KE + (ch >> 5) * P8;
+        float dov[32];
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) {
+            const int i = i0 + ii;
+            const float kv = bfv(in.kp, ii), b = sm.beta[i];
+            *reinterpret_cast<__half *>(b1 + sw128_offset(i, ch & 63)) =
+                __float2half_rn(b * bfv(in.vp, ii));
+            *reinterpret_cast<__half *>(b2 + sw128_offset(i, ch & 63)) =
+                __float2half_rn(b * exp2_approx(in.G[ii]) * kv);
+            f32_at(ke, i, ch & 31) = tf32_operand(exp2_approx(Gl - in.G[ii]) * kv);
+            dov[ii] = bfv(in.dp, ii);
+        }
+        row32_tf32(ar + G1_DOT + hf * U16, ch, dov);
+    }
+    bool ok = mbar_wait_bounded(&sm.bar_ld, 0, kGradWait);
+    {
+        // A^qk^T-rows: row j holds A^qk[i][j] over i (f16 -> fp32 is exact)
+        const int j = tid & 63, ib = (tid >> 6) * 16;
+        const uint8_t *aqk = ar + G1_AQ + 8192;
+        uint8_t *dst = ar + G1_AQT + (ib >> 5) * P8;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) f32_at(dst, j, (ib + e) & 31) = f16_at(aqk, ib + e, j);
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        // (1) [U | W] = A^kk [B1 | B2]   (f16, B MN-major; cols 0..255)
+        for (int n = 0; n < 4; ++n)
+            mma_kmajor_a_mn_b(tmem + n * 64, smem_u32(ar + G1_AQ), 0,
+                              smem_u32(ar + G1_BB + n * P8), 4, kIdF16MnB, false);
+        mma_commit(&sm.bar_m[0]);
+        // (2) dE^T = dO^T A^qk + dS^T K_end^T   (cols 256..319)
+        mma_panels<true>(tmem + 256, smem_u32(ar + G1_DOT), U16, smem_u32(ar + G1_AQT), P8, 8,
+                         idesc_tf32_f32(128, 64), false);
+        mma_panels<true>(tmem + 256, smem_u32(ar + G1_DST), U16, smem_u32(ar + G1_KE), P8, 16,
+                         idesc_tf32_f32(128, 64), true);
+        mma_commit(&sm.bar_m[1]);
+    }
+
+    // ---- step 2: -W (f16 rows i) and the S_c image once (1) is done ----
+    ok = ok && mbar_wait_bounded(&sm.bar_m[0], 0, kGradWait);
+    if (tid == 0 && ok) {
+        mbar_arrive_expect_tx(&sm.bar_sf, 2 * U16);
+        bulk_g2s(ar + G1_SF, a.sst + item * (2 * U16), 2 * U16, &sm.bar_sf);
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    if (quad < 2) {
+        // lane = row i (0..63), key channels 64 hf ..
+        float w0[32], w1[32];
+        if (ok) {
+            tmem_ld32x2(tmem_addr(tmem, quad * 32, 128 + hf * 64),
+                        tmem_addr(tmem, quad * 32, 128 + hf * 64 + 32), w0, w1);
+        } else {
+            zero32(w0);
+            zero32(w1);
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            w0[j] = -w0[j];
+            w1[j] = -w1[j];
+        }
+        row64_f16(ar + G1_NW + hf * P8, ch, w0, w1);
+    }
+    ok = ok && mbar_wait_bounded(&sm.bar_m[1], 0, kGradWait);
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    {
+        // dE^T: lane = value channel v, tokens of this half; to scratch and
+        // into rows 64.. of [dO ; dE]; dO into rows 0..63
+        float e[32];
+        if (ok) tmem_ld32(tmem_addr(tmem, quad * 32, 256 + hf * 32), e);
+        else zero32(e);
+        float *dst = a.dE + item * (GC * GD) + ch;
+        uint8_t *ode = ar + G1_ODE + (ch >> 5) * U16;
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) {
+            const int i = i0 + ii;
+            dst[(size_t)i * GD] = e[ii];
+            f32_at(ode, 64 + i, ch & 31) = tf32_operand(e[ii]);
+            f32_at(ode, i, ch & 31) = bfv(in.dp, ii);
+        }
+    }
+    ok = ok && mbar_wait_bounded(&sm.bar_sf, 0, kGradWait);
+    {
+        // S_c rows a = ch, value tile hf: f16 image -> tf32 panels 2 hf, 2 hf + 1
+        const uint8_t *src = ar + G1_SF + hf * U16;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(src + sw128_chunk(ch, c8));
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const __half2 hv = *reinterpret_cast<const __half2 *>(&w4[e]);
+                f[2 * e] = __low2float(hv);
+                f[2 * e + 1] = __high2float(hv);
+            }
+            uint8_t *pan = ar + g1_s_panel(2 * hf + (c8 >> 2));
+            const int cc = (c8 & 3) * 2;
+            *reinterpret_cast<float4 *>(pan + sw128_chunk(ch, cc)) =
+                make_float4(f[0], f[1], f[2], f[3]);
+            *reinterpret_cast<float4 *>(pan + sw128_chunk(ch, cc + 1)) =
+                make_float4(f[4], f[5], f[6], f[7]);
+        }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        // (3) E = U - W S_c onto U (cols 0..127; f16, B = the S_c image)
+        for (int vt = 0; vt < 2; ++vt)
+            mma_kmajor_a_mn_b(tmem + vt * 64, smem_u32(ar + G1_NW), P8,
+                              smem_u32(ar + G1_SF + vt * U16), 8, kIdF16MnB, true);
+        // (4) [dQ_hat^T | -dW^T] = S_c [dO ; dE]^T   (cols 256..383)
+        mma_panels<true>(tmem + 256, smem_u32(ar + g1_s_panel(0)), U16, smem_u32(ar + G1_ODE),
+                         U16, 8, idesc_tf32_f32(128, 128), false);
+        mma_panels<true>(tmem + 256, smem_u32(ar + g1_s_panel(2)), U16,
+                         smem_u32(ar + G1_ODE + 2 * U16), U16, 8, idesc_tf32_f32(128, 128),
+                         true);
+        mma_commit(&sm.bar_m[2]);
+    }
+
+    // ---- step 3: E (rows j) and dS (rows a) ----
+    ok = ok && mbar_wait_bounded(&sm.bar_m[2], 0, kGradWait);
+    if (tid == 0 && ok) {
+        mbar_arrive_expect_tx(&sm.bar_dsn, 4 * U16);
+        bulk_g2s(ar + G1_DSN, a.ds_n + item * (4 * U16), 4 * U16, &sm.bar_dsn);
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    if (quad < 2) {
+        float e0[32], e1[32];
+        if (ok) {
+            tmem_ld32x2(tmem_addr(tmem, quad * 32, hf * 64), tmem_addr(tmem, quad * 32, hf * 64 + 32),
+                        e0, e1);
+        } else {
+            zero32(e0);
+            zero32(e1);
+        }
+        row32_tf32(ar + G1_E + (2 * hf) * P8, ch, e0);
+        row32_tf32(ar + G1_E + (2 * hf + 1) * P8, ch, e1);
+    }
+    ok = ok && mbar_wait_bounded(&sm.bar_dsn, 0, kGradWait);
+    {
+        // sum_v dS[a][v] S[a][v] over value half hf (S from the f16 image)
+        const uint8_t *sf = a.sst + item * (2 * U16) + hf * U16;
+        float acc = 0.f;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(sf + sw128_chunk(ch, c8));
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+            const uint8_t *pan = ar + G1_DSN + (2 * hf + (c8 >> 2)) * U16;
+            const int cc = (c8 & 3) * 2;
+            const float4 d0 = *reinterpret_cast<const float4 *>(pan + sw128_chunk(ch, cc));
+            const float4 d1 = *reinterpret_cast<const float4 *>(pan + sw128_chunk(ch, cc + 1));
+            const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const __half2 hv = *reinterpret_cast<const __half2 *>(&w4[e]);
+                acc = fmaf(__low2float(hv), dd[2 * e], acc);
+                acc = fmaf(__high2float(hv), dd[2 * e + 1], acc);
+            }
+        }
+        sm.sterm[hf][ch] = acc;
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        // (5) dA^qk^T = E dO^T (cols 384..447): B = rows 0..63 of [dO ; dE]
+        mma_panels<true>(tmem + 384, smem_u32(ar + G1_E), P8, smem_u32(ar + G1_ODE), U16, 16,
+                         idesc_tf32_f32(128, 64), false);
+        // (6) dK_end^T = dS E^T (cols 448..511)
+        mma_panels<true>(tmem + 448, smem_u32(ar + G1_DSN), U16, smem_u32(ar + G1_E), P8, 16,
+                         idesc_tf32_f32(128, 64), false);
+        mma_commit(&sm.bar_m[3]);
+    }
+    // q for Q_hat while the products run
+    {
+        const unsigned short *q16 = static_cast<const unsigned short *>(a.q);
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+            const int ia = i0 + 2 * jj, ib = ia + 1;
+            in.qp[jj] = (ia < L ? q16[base + (size_t)ia * rs] : 0u) |
+                        ((ib < L ? (uint32_t)q16[base + (size_t)ib * rs] : 0u) << 16);
+        }
+    }
+    ok = ok && mbar_wait_bounded(&sm.bar_m[3], 0, kGradWait);
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+
+    // ---- epilogue ----
+    if (quad < 2) {
+        // dA^qk[i][j], lane = j: masked (j <= i < L) to scratch
+        float x[32];
+        if (ok) tmem_ld32(tmem_addr(tmem, quad * 32, 384 + hf * 32), x);
+        else zero32(x);
+        float *dst = a.dAqk + item * (GC * GC) + ch;
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) {
+            const int i = i0 + ii;
+            dst[(size_t)i * GC] = (ch <= i && i < L) ? x[ii] : 0.f;
+        }
+    }
+    {
+        float w[32];
+        if (ok) tmem_ld32(tmem_addr(tmem, quad * 32, 320 + hf * 32), w);
+        else zero32(w);
+        float *dst = a.dW + item * (GC * GD) + ch;
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) dst[(size_t)(i0 + ii) * GD] = -w[ii];
+    }
+    float dqh[32], dke[32];
+    if (ok) {
+        tmem_ld32x2(tmem_addr(tmem, quad * 32, 256 + hf * 32),
+                    tmem_addr(tmem, quad * 32, 448 + hf * 32), dqh, dke);
+    } else {
+        zero32(dqh);
+        zero32(dke);
+    }
+    float kt = 0.f;
+#pragma unroll
+    for (int ii = 0; ii < 32; ++ii) {
+        const int i = i0 + ii;
+        const float gam = exp2_approx(in.G[ii]), ek = exp2_approx(Gl - in.G[ii]);
+        const float qhat = a.scale * gam * bfv(in.qp, ii);
+        const float kend = ek * bfv(in.kp, ii);
+        kt = fmaf(kend, dke[ii], kt);
+        if (i < L) {
+            const size_t r = base + (size_t)i * rs;
+            a.dq[r] = a.scale * gam * dqh[ii];
+            a.dk[r] = ek * dke[ii];
+        }
+        dqh[ii] = qhat * dqh[ii] - kend * dke[ii];  // dG without the decayed products
+    }
+    sm.kterm[hf][ch] = kt;
+    __syncthreads();
+    const float dgl =
+        sm.kterm[0][ch] + sm.kterm[1][ch] + exp2_approx(Gl) * (sm.sterm[0][ch] + sm.sterm[1][ch]);
+    {
+        float *dst = a.dG + item * (GC * GD) + ch;
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) {
+            const int i = i0 + ii;
+            dst[(size_t)i * GD] = dqh[ii] + (i == L - 1 ? dgl : 0.f);
+        }
+    }
+    const bool bad = __syncthreads_or(!ok);
+    if (bad && tid == 0) {
+        atomicExch(a.status, (int)KDA_ERR_TIMEOUT);
+        // let every copy this CTA started land before its shared memory goes
+        (void)mbar_wait_bounded(&sm.bar_ld, 0, kGradWait);
+        (void)mbar_wait_bounded(&sm.bar_sf, 0, kGradWait);
+        (void)mbar_wait_bounded(&sm.bar_dsn, 0, kGradWait);
+        (void)mbar_wait_bounded(&sm.bar_m[3], 0, kGradWait);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------------------
+// G2: the C x C products, the decayed products' gradients, the outputs
+// ---------------------------------------------------------------------------
+// Shared arena (16 KB units; 13.5 of them):
+//   step 1: dE (rows i, K = v) u0-1 | dW (rows i, K = a) u2-3 | B1 (rows j,
+//           K = v) u4-5 | B2 (rows j, K = a) u6-7 | dE^T (rows v, K = i) u8-9
+//           | dW^T (rows a, K = i) u10-11 | A^T-rows (rows j, K = i) u12 |
+//           A^kk f16 at u13 (8 KB)
+//   step 2: dA^T-rows (rows m, K = i) at 0 | A (rows n, K = m) at 24 KB |
+//           K_hat^T (rows a, K = j) u4-5 | [Q_tilde^T | K_tilde^T] u6-9
+//   step 3: T1 (rows j, K = m) at 40 KB | [s dA^qk ; dR]^T-rows (rows j,
+//           K = i) at 0 (4 x 8 KB) | [dR ; s dA^qk] (rows i, K = j) u10-11
+//   direct path: G, k, q fp32 [64][128] at u4, u6, u8; dR, s dA^qk fp32
+//           [64][64] at u10
+//   epilogue: dG fp32 [64][128] at u4, dbeta partials [64][129] at u6
+// TMEM columns: dA 0..63, dB1^T 64..127, dB2^T 128..191, T1^T 192..255,
+// -dR 256..319, [X1^T | X2^T] 320..447, Y^T 448..511 (direct path: XR, XQ,
+// YY themselves in 320.., 384.., 448..).
+struct G2Smem {
+    uint8_t ar[13 * U16 + P8];
+    float beta[GC];
+    float gcarry[GD], gmid[GD];
+    uint64_t bar_ld, bar_m[4];
+    uint32_t tmem;
+};
+constexpr uint32_t G2_DE = 0, G2_DW = 2 * U16, G2_B1 = 4 * U16, G2_B2 = 6 * U16,
+                   G2_DET = 8 * U16, G2_DWT = 10 * U16, G2_AT = 12 * U16, G2_AF = 13 * U16;
+constexpr uint32_t G2_DAT = 0, G2_AN = 24576, G2_KH = 4 * U16, G2_KQ = 6 * U16, G2_T1 = 40960,
+                   G2_DRQT = 0, G2_DRQ = 10 * U16;
+constexpr uint32_t G2_GS = 4 * U16, G2_KS = 6 * U16, G2_QS = 8 * U16, G2_DRS = 10 * U16,
+                   G2_DAS = 10 * U16 + 16384;
+constexpr uint32_t G2_DGS = 4 * U16, G2_PS = 6 * U16;
+constexpr int kPS = 129;  // row stride of the dbeta partials (conflict-free column sums)
+constexpr size_t kG2Smem = sizeof(G2Smem) + 1024;
+static_assert(kG2Smem <= 227 * 1024, "G2 shared memory");
+static_assert(G2_PS + GC * kPS * 4 <= 10 * U16, "epilogue scratch below the dR operands");
+
+__global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g2_kernel(const ChunkGradArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    G2Smem &sm = *reinterpret_cast<G2Smem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *ar = sm.ar;
+    const int tid = threadIdx.x, warp = tid >> 5, quad = warp & 3;
+    const int ch = tid & 127, hf = tid >> 7, i0 = hf * 32;
+    const size_t item = blockIdx.x;
+    const int32_t H = a.H;
+    const int32_t c = (int32_t)(item / (size_t)H), h = (int32_t)(item % (size_t)H);
+    const int2 tok = a.chunk_tok[c];
+    const int32_t t0 = tok.x, L = tok.y;
+    if (L <= 0) return;
+
+    if (tid == 0) {
+        mbar_init(&sm.bar_ld, 1);
+        for (int m = 0; m < 4; ++m) mbar_init(&sm.bar_m[m], 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&sm.bar_ld, 8192);
+        bulk_g2s(ar + G2_AF, a.aux + item * kBwdAuxBytes, 8192, &sm.bar_ld);
+    }
+    if (warp == 0) {
+        tmem_alloc(&sm.tmem, 512);
+        tmem_relinquish();
+    }
+    const size_t rs = (size_t)H * GD;
+    const size_t base = ((size_t)t0 * H + h) * GD + ch;
+    TokenInputs in;
+    load_inputs(a, base, rs, i0, L, true, false, in);
+    if (tid < GC) sm.beta[tid] = tid < L ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
+    if (hf == 0) sm.gcarry[ch] = in.G[31];
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (hf == 1) {
+        const float cy = sm.gcarry[ch];
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) in.G[ii] += cy;
+        sm.gmid[ch] = in.G[0];
+    }
+    __syncthreads();
+    const float Gm = sm.gmid[ch];
+    float span = 0.f;
+#pragma unroll
+    for (int ii = 0; ii < 32; ++ii) span = fmaxf(span, fabsf(in.G[ii] - Gm));
+    const bool direct = __syncthreads_or(!(span <= kGradSpan2));
+    const uint32_t tmem = sm.tmem;
+
+    // ---- step 1 operands ----
+    {
+        uint8_t *b1 = ar + G2_B1 + (ch >> 5) * P8, *b2 = ar + G2_B2 + (ch >> 5) * P8;
+        uint8_t *de = ar + G2_DE + (ch >> 5) * P8, *dw = ar + G2_DW + (ch >> 5) * P8;
+        const float *gE = a.dE + item * (GC * GD) + ch, *gW = a.dW + item * (GC * GD) + ch;
+        float xe[32], xw[32];
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) {
+            const int i = i0 + ii;
+            const float b = sm.beta[i];
+            f32_at(b1, i, ch & 31) = tf32_operand(b * bfv(in.vp, ii));
+            f32_at(b2, i, ch & 31) = tf32_operand(b * exp2_approx(in.G[ii]) * bfv(in.kp, ii));
+            xe[ii] = gE[(size_t)i * GD];
+            xw[ii] = gW[(size_t)i * GD];
+            f32_at(de, i, ch & 31) = tf32_operand(xe[ii]);
+            f32_at(dw, i, ch & 31) = tf32_operand(xw[ii]);
+        }
+        row32_tf32(ar + G2_DET + hf * U16, ch, xe);
+        row32_tf32(ar + G2_DWT + hf * U16, ch, xw);
+    }
+    bool ok = mbar_wait_bounded(&sm.bar_ld, 0, kGradWait);
+    {
+        // A^T-rows: row j holds A[i][j] over i
+        const int j = tid & 63, ib = (tid >> 6) * 16;
+        const uint8_t *af = ar + G2_AF;
+        uint8_t *dst = ar + G2_AT + (ib >> 5) * P8;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) f32_at(dst, j, (ib + e) & 31) = f16_at(af, ib + e, j);
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        // (1) dA = dE B1^T + dW B2^T   (cols 0..63)
+        mma_panels<true>(tmem, smem_u32(ar + G2_DE), P8, smem_u32(ar + G2_B1), P8, 16,
+                         idesc_tf32_f32(128, 64), false);
+        mma_panels<true>(tmem, smem_u32(ar + G2_DW), P8, smem_u32(ar + G2_B2), P8, 16,
+                         idesc_tf32_f32(128, 64), true);
+        // (2) dB1^T = dE^T A, dB2^T = dW^T A   (cols 64..127, 128..191)
+        mma_panels<true>(tmem + 64, smem_u32(ar + G2_DET), U16, smem_u32(ar + G2_AT), P8, 8,
+                         idesc_tf32_f32(128, 64), false);
+        mma_panels<true>(tmem + 128, smem_u32(ar + G2_DWT), U16, smem_u32(ar + G2_AT), P8, 8,
+                         idesc_tf32_f32(128, 64), false);
+        mma_commit(&sm.bar_m[0]);
+    }
+    ok = ok && mbar_wait_bounded(&sm.bar_m[0], 0, kGradWait);
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+
+    // ---- step 2: dA^T-rows, A, the decayed operands ----
+    if (quad < 2) {
+        // lane = row i of dA; columns m = 32 hf ..
+        float x[32];
+        if (ok) tmem_ld32(tmem_addr(tmem, quad * 32, hf * 32), x);
+        else zero32(x);
+        uint8_t *dst = ar + G2_DAT + (ch >> 5) * P8;
+#pragma unroll
+        for (int mm = 0; mm < 32; ++mm) f32_at(dst, i0 + mm, ch & 31) = tf32_operand(x[mm]);
+    }
+    {
+        // A natural: row n holds A[n][m] over m
+        const int n = tid >> 2, mb = (tid & 3) * 16;
+        uint8_t *dst = ar + G2_AN + (mb >> 5) * P8;
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) {
+            const int m = mb + 4 * e4;
+            *reinterpret_cast<float4 *>(dst + sw128_chunk(n, (m & 31) >> 2)) =
+                make_float4(f16_at(ar + G2_AF, n, m), f16_at(ar + G2_AF, n, m + 1),
+                            f16_at(ar + G2_AF, n, m + 2), f16_at(ar + G2_AF, n, m + 3));
+        }
+    }
+    if (!direct) {
+        // K_hat^T (rows a, K = j) and [Q_tilde^T | K_tilde^T] (rows a, K = i)
+        float kh[32], qt[32], kt[32];
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) {
+            const float kv = bfv(in.kp, ii), qv = bfv(in.qp, ii);
+            const float ep = exp2_approx(in.G[ii] - Gm), en = exp2_approx(Gm - in.G[ii]);
+            kh[ii] = kv * en;
+            qt[ii] = qv * ep;
+            kt[ii] = kv * ep;
+        }
+        row32_tf32(ar + G2_KH + hf * U16, ch, kh);
+        row32_tf32(ar + G2_KQ + hf * U16, ch, qt);
+        row32_tf32(ar + G2_KQ + (2 + hf) * U16, ch, kt);
+    } else {
+        float *gs = reinterpret_cast<float *>(ar + G2_GS), *ks = reinterpret_cast<float *>(ar + G2_KS),
+              *qs = reinterpret_cast<float *>(ar + G2_QS);
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) {
+            const int i = i0 + ii;
+            gs[i * GD + ch] = in.G[ii];
+            ks[i * GD + ch] = bfv(in.kp, ii);
+            qs[i * GD + ch] = bfv(in.qp, ii);
+        }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        // (3) T1^T = dA^T A   (T1 = A^T dA; cols 192..255)
+        mma_panels<true>(tmem + 192, smem_u32(ar + G2_DAT), P8, smem_u32(ar + G2_AT), P8, 8,
+                         idesc_tf32_f32(128, 64), false);
+        mma_commit(&sm.bar_m[1]);
+    }
+    ok = ok && mbar_wait_bounded(&sm.bar_m[1], 0, kGradWait);
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+
+    // ---- step 3: T1 (rows j), s dA^qk into the decayed operands ----
+    if (quad < 2) {
+        // lane = m; columns j = 32 hf ..
+        float x[32];
+        if (ok) tmem_ld32(tmem_addr(tmem, quad * 32, 192 + hf * 32), x);
+        else zero32(x);
+        uint8_t *dst = ar + G2_T1 + (ch >> 5) * P8;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) f32_at(dst, i0 + jj, ch & 31) = tf32_operand(x[jj]);
+    }
+    {
+        // s dA^qk[i][j]: thread -> j, 16 rows i
+        const int j = tid & 63, ib = (tid >> 6) * 16;
+        const float *src = a.dAqk + item * (GC * GC) + j;
+        if (!direct) {
+            uint8_t *drq = ar + G2_DRQ + (j >> 5) * U16;     // rows 64 + i, K = j
+            uint8_t *drqt = ar + G2_DRQT + (ib >> 5) * P8;  // rows j, K = i
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int i = ib + e;
+                const float x = tf32_operand(a.scale * src[(size_t)i * GC]);
+                f32_at(drq, 64 + i, j & 31) = x;
+                f32_at(drqt, j, i & 31) = x;
+            }
+        } else {
+            float *das = reinterpret_cast<float *>(ar + G2_DAS);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) das[(ib + e) * GC + j] = a.scale * src[(size_t)(ib + e) * GC];
+        }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        // (4) -dR = T1 A^T   (cols 256..319)
+        mma_panels<true>(tmem + 256, smem_u32(ar + G2_T1), P8, smem_u32(ar + G2_AN), P8, 8,
+                         idesc_tf32_f32(128, 64), false);
+        mma_commit(&sm.bar_m[2]);
+    }
+    ok = ok && mbar_wait_bounded(&sm.bar_m[2], 0, kGradWait);
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+
+    // ---- step 4: dR (strictly lower, rows i < L) into the decayed operands ----
+    if (quad < 2) {
+        // lane = row i of dR; columns n = 32 hf ..
+        const int i = ch;
+        float x[32];
+        if (ok) tmem_ld32(tmem_addr(tmem, quad * 32, 256 + hf * 32), x);
+        else zero32(x);
+#pragma unroll
+        for (int nn = 0; nn < 32; ++nn) {
+            const int n = i0 + nn;
+            x[nn] = (n < i && i < L) ? -x[nn] : 0.f;
+        }
+        if (!direct) {
+            row32_tf32(ar + G2_DRQ + hf * U16, i, x);
+            uint8_t *drqt = ar + G2_DRQT + (2 + (i >> 5)) * P8;  // rows n, K = 64 + i
+            const float b = sm.beta[i];
+#pragma unroll
+            for (int nn = 0; nn < 32; ++nn) f32_at(drqt, i0 + nn, i & 31) = tf32_operand(b * x[nn]);
+        } else {
+            float *drs = reinterpret_cast<float *>(ar + G2_DRS);
+#pragma unroll
+            for (int nn = 0; nn < 32; ++nn) drs[i * GC + i0 + nn] = x[nn];
+        }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (!direct) {
+        if (tid == 0 && ok) {
+            tc_fence_after();
+            // (5) [X1^T | X2^T] = K_hat^T [dR ; s dA^qk]^T   (cols 320..447)
+            mma_panels<true>(tmem + 320, smem_u32(ar + G2_KH), U16, smem_u32(ar + G2_DRQ), U16, 8,
+                             idesc_tf32_f32(128, 128), false);
+            // (6) Y^T = [Q_tilde^T | K_tilde^T] [s dA^qk ; Diag(beta) dR]   (cols 448..511)
+            mma_panels<true>(tmem + 448, smem_u32(ar + G2_KQ), U16, smem_u32(ar + G2_DRQT), P8, 16,
+                             idesc_tf32_f32(128, 64), false);
+            mma_commit(&sm.bar_m[3]);
+        }
+        ok = ok && mbar_wait_bounded(&sm.bar_m[3], 0, kGradWait);
+        ok = __all_sync(0xffffffffu, ok);
+        tc_fence_after();
+    } else {
+        // Direct evaluation (decays beyond e^-80 across half a chunk): every
+        // exp(G_i - G_j) with i >= j (at most 1), into the same TMEM columns.
+        const float *gs = reinterpret_cast<const float *>(ar + G2_GS);
+        const float *ks = reinterpret_cast<const float *>(ar + G2_KS);
+        const float *qs = reinterpret_cast<const float *>(ar + G2_QS);
+        const float *drs = reinterpret_cast<const float *>(ar + G2_DRS);
+        const float *das = reinterpret_cast<const float *>(ar + G2_DAS);
+        // per-thread results go through the dead operand area at 0 (each
+        // thread reads back only what it wrote)
+        float *xrs = reinterpret_cast<float *>(ar), *xqs = xrs + GC * GD;
+#pragma unroll 1
+        for (int ii = 0; ii < 32; ++ii) {
+            const int i = i0 + ii;
+            const float gi = gs[i * GD + ch];
+            float r = 0.f, s = 0.f;
+            for (int j = 0; j <= i; ++j) {
+                const float w = exp2_approx(gi - gs[j * GD + ch]) * ks[j * GD + ch];
+                r = fmaf(drs[i * GC + j], w, r);
+                s = fmaf(das[i * GC + j], w, s);
+            }
+            xrs[i * GD + ch] = r;
+            xqs[i * GD + ch] = s;
+        }
+        float v[32];
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) v[ii] = xrs[(i0 + ii) * GD + ch];
+        tmem_st32(tmem_addr(tmem, quad * 32, 320 + hf * 32), v);
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) v[ii] = xqs[(i0 + ii) * GD + ch];
+        tmem_st32(tmem_addr(tmem, quad * 32, 384 + hf * 32), v);
+#pragma unroll 1
+        for (int ii = 0; ii < 32; ++ii) {
+            const int j = i0 + ii;
+            const float gj = gs[j * GD + ch];
+            float y = 0.f;
+            for (int i = j; i < GC; ++i) {
+                const float e = exp2_approx(gs[i * GD + ch] - gj);
+                y = fmaf(sm.beta[i] * drs[i * GC + j] * ks[i * GD + ch] +
+                             das[i * GC + j] * qs[i * GD + ch],
+                         e, y);
+            }
+            xrs[j * GD + ch] = y;
+        }
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) v[ii] = xrs[(i0 + ii) * GD + ch];
+        tmem_st32(tmem_addr(tmem, quad * 32, 448 + hf * 32), v);
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+
+    // ---- epilogue: thread = channel ch (key, and value for dv), its tokens ----
+    float *dgs = reinterpret_cast<float *>(ar + G2_DGS);
+    float *ps = reinterpret_cast<float *>(ar + G2_PS);
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+        const int c0 = hf * 32 + g * 16;  // token / column offset of this group
+        float y[16], dkv[16], dgv[16], pv[16], ep[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int ii = g * 16 + e;
+            ep[e] = direct ? 1.f : exp2_approx(in.G[ii] - Gm);
+        }
+        const float *dgp = a.dG + item * (GC * GD) + ch;
+        // dB2: B2 = Diag(beta)(exp(G) * K)
+        if (ok) tmem_ld16(tmem_addr(tmem, quad * 32, 128 + c0), y);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int ii = g * 16 + e, i = c0 + e;
+            const float yv = ok ? y[e] : 0.f;
+            const float b = sm.beta[i], gam = exp2_approx(in.G[ii]), kv = bfv(in.kp, ii);
+            dkv[e] = b * gam * yv;
+            dgv[e] = dgp[(size_t)i * GD] + b * gam * kv * yv;
+            pv[e] = gam * kv * yv;
+        }
+        // dB1: B1 = Diag(beta) V (lane = value channel)
+        if (ok) tmem_ld16(tmem_addr(tmem, quad * 32, 64 + c0), y);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int ii = g * 16 + e, i = c0 + e;
+            const float yv = ok ? y[e] : 0.f;
+            pv[e] = fmaf(bfv(in.vp, ii), yv, pv[e]);
+            if (i < L) a.dv[base + (size_t)i * rs] = sm.beta[i] * yv;
+        }
+        // XR (rows of R)
+        if (ok) tmem_ld16(tmem_addr(tmem, quad * 32, 320 + c0), y);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int ii = g * 16 + e, i = c0 + e;
+            const float xr = ok ? ep[e] * y[e] : 0.f, kv = bfv(in.kp, ii), b = sm.beta[i];
+            dkv[e] = fmaf(b, xr, dkv[e]);
+            dgv[e] = fmaf(b * kv, xr, dgv[e]);
+            pv[e] = fmaf(kv, xr, pv[e]);
+        }
+        // XQ (rows of A^qk)
+        if (ok) tmem_ld16(tmem_addr(tmem, quad * 32, 384 + c0), y);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int ii = g * 16 + e, i = c0 + e;
+            const float xq = ok ? ep[e] * y[e] : 0.f;
+            dgv[e] = fmaf(bfv(in.qp, ii), xq, dgv[e]);
+            if (i < L) {
+                float *dq = a.dq + base + (size_t)i * rs;
+                *dq = *dq + xq;
+            }
+        }
+        // YY (columns of R and A^qk)
+        if (ok) tmem_ld16(tmem_addr(tmem, quad * 32, 448 + c0), y);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int ii = g * 16 + e, i = c0 + e;
+            const float en = direct ? 1.f : exp2_approx(Gm - in.G[ii]);
+            const float yy = ok ? en * y[e] : 0.f, kv = bfv(in.kp, ii);
+            dkv[e] += yy;
+            dgv[e] = fmaf(-kv, yy, dgv[e]);
+            if (i < L) {
+                float *dk = a.dk + base + (size_t)i * rs;
+                *dk = *dk + dkv[e];
+            }
+            dgs[i * GD + ch] = dgv[e];
+            ps[i * kPS + ch] = pv[e];
+        }
+    }
+    __syncthreads();
+    if (tid < GD) {
+        // dlog_alpha: reverse cumulative sum of dG over the chunk's tokens
+        float acc = 0.f;
+        for (int i = GC - 1; i >= 0; --i) {
+            acc += dgs[i * GD + tid];
+            if (i < L) a.dlog_alpha[((size_t)(t0 + i) * H + h) * GD + tid] = acc;
+        }
+    } else if (tid < GD + GC) {
+        const int i = tid - GD;
+        float acc = 0.f;
+        for (int cc = 0; cc < GD; ++cc) acc += ps[i * kPS + cc];
+        if (i < L) a.dbeta[(size_t)(t0 + i) * H + h] = acc;
+    }
+    const bool bad = __syncthreads_or(!ok);
+    if (bad && tid == 0) {
+        atomicExch(a.status, (int)KDA_ERR_TIMEOUT);
+        (void)mbar_wait_bounded(&sm.bar_ld, 0, kGradWait);
+        (void)mbar_wait_bounded(&sm.bar_m[2], 0, kGradWait);
+        if (!direct) (void)mbar_wait_bounded(&sm.bar_m[3], 0, kGradWait);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_grad(const ChunkGradArgs &a, cudaStream_t stream) {
+    if (a.n_items == 0) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(chunk_grad_g1_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kG1Smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(chunk_grad_g2_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kG2Smem);
+    if (e != cudaSuccess) return e;
+    chunk_grad_g1_kernel<<<(unsigned)a.n_items, kGThreads, kG1Smem, stream>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    chunk_grad_g2_kernel<<<(unsigned)a.n_items, kGThreads, kG2Smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

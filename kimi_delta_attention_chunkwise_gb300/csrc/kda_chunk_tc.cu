@@ -457,7 +457,8 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
                   const __nv_bfloat16 *__restrict__ k, const float *__restrict__ beta,
                   float scale, int32_t H, int32_t grp, int32_t pro,
                   const float *__restrict__ gbias, const float *__restrict__ galog, Scratch sc,
-                  uint32_t n_items, int32_t flags, long long wait_cycles, int *status) {
+                  uint32_t n_items, int32_t flags, long long wait_cycles, int *status,
+                  uint8_t *__restrict__ bwd_aux) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -931,6 +932,13 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
         fence_proxy_async();
         tc_fence_before();
         wbar(bid);
+        // for the backward: A^kk and A^qk of this item out (read before Z is
+        // staged over A^kk, below)
+        if (bwd_aux && tid == 0) {
+            bulk_s2g(bwd_aux + ch * kBwdAuxBytes, b2, 8192);
+            bulk_s2g(bwd_aux + ch * kBwdAuxBytes + 8192, aqk, 8192);
+            bulk_commit_group();
+        }
 
         const int quad = warp & 3, chalf = warp >> 2;  // TMEM lanes 32*quad.., column half
         // W^T = (beta Gamma K)^T A^kk^T (TMEM cols 64..127) and Z = A^qk A^kk (cols
@@ -947,6 +955,11 @@ chunk_prep_kernel(const __grid_constant__ PrepMaps maps, const __nv_bfloat16 *__
         ok = __all_sync(0xffffffffu, ok);  // TMEM loads below are warp-collective
         mma_phase ^= 1u;
         tc_fence_after();
+        if (bwd_aux) {
+            // the copies of A^kk and A^qk have left shared memory
+            if (tid == 0) bulk_wait_group_read<0>();
+            wbar(bid);
+        }
         {
             // thread = key channel d, token half chalf: W^T row d
             float v[32];
@@ -1106,20 +1119,6 @@ __device__ __forceinline__ bool compute_barrier_or(bool pred) {
         : "r"((uint32_t)pred)
         : "memory");
     return r != 0;
-}
-
-// A K-major (panels of 128-byte rows), B MN-major (N = 64, SW128): K walks
-// 32 bytes of A and 16 rows = 2048 bytes of B per step.
-__device__ __forceinline__ void mma_kmajor_a_mn_b(uint32_t d_tmem, uint32_t a_base,
-                                                  uint32_t a_panel, uint32_t b_base, int ksteps,
-                                                  uint32_t idesc, bool accumulate_first) {
-#pragma unroll
-    for (int ks = 0; ks < ksteps; ++ks) {
-        const uint32_t a = a_base + (ks >> 2) * a_panel + (ks & 3) * 32;
-        const uint32_t b = b_base + ks * 2048;
-        mma_half(d_tmem, sdesc_sw128(a), sdesc_sw128(b), idesc,
-                 (ks > 0 || accumulate_first) ? 1u : 0u);
-    }
 }
 
 // 32 consecutive f16 values as 4 swizzled 16-byte chunks of one MN-major row.
@@ -1829,6 +1828,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
         if (!encode_tile_map(&v_map, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, BV,
                              CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
+    }
+    if (a.T > 0 && !a.skip_out) {
         // output tiles [64 tokens x 128-byte column panel] of one head
         auto enc = tensor_map_encoder();
         const size_t es = a.out_f32 ? 4 : 2;
@@ -1861,7 +1862,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
         e = cudaLaunchKernelEx(&cfg, prep, maps, static_cast<const __nv_bfloat16 *>(a.q),
                                static_cast<const __nv_bfloat16 *>(a.k), a.beta, a.scale, a.H,
                                a.G, a.pro, a.gbias, a.galog, sc, (uint32_t)n_items,
-                               (int32_t)flags, wait_cycles, a.status);
+                               (int32_t)flags, wait_cycles, a.status, a.bwd_aux);
         if (e != cudaSuccess) return e;
     }
     a.clock->mark(stream);
@@ -1878,7 +1879,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, void *workspace, size_t workspac
     }
     a.clock->mark(stream);
 
-    if (run_prep) {
+    if (run_prep && !a.skip_out) {
         const cudaLaunchConfig_t cfg = config(dim3((unsigned)n_items), kOutThreads, kOutSmem, true);
         const int32_t *cu = static_cast<const int32_t *>(a.cu_seqlens);
         if (a.out_f32) {

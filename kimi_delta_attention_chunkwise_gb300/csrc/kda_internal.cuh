@@ -42,7 +42,14 @@ struct ChunkArgs {
     StageClock *clock;           // never null inside the launchers
     int32_t diag_withhold_prep = 0;  // diagnostic: launch no prep (the scan's waits run out)
     long long wait_cycles = 0;       // limit of every bounded wait in SM clocks (0: default)
+    // For the chunkwise backward (tensor-core engine only): when set, the prep
+    // also stores every item's A^kk and A^qk (f16 K-major SW128 panels, 8 KB
+    // each, kBwdAuxBytes per item at item * kBwdAuxBytes), and skip_out
+    // leaves the output pass out (out may then be null).
+    uint8_t *bwd_aux = nullptr;
+    int32_t skip_out = 0;
 };
+constexpr uint32_t kBwdAuxBytes = 16384;
 
 struct StepArgs {
     const void *q, *k, *v;
@@ -100,6 +107,28 @@ cudaError_t launch_recurrent_bwd(const BwdArgs &a, cudaStream_t stream);
 // bf16, D = 128, no prologue, no value-head groups.
 size_t chunk_bwd_workspace_bytes(int32_t N, int32_t T, int32_t H);
 cudaError_t launch_chunk_bwd(const BwdArgs &a, int *status, cudaStream_t stream);
+
+// The per-chunk gradient pass of the chunkwise backward
+// (kda_backward_grad.cu), from what the forward engine, its A^kk / A^qk
+// store and the reverse scan leave: two launches over the (chunk, head)
+// items, bf16 q/k/v/dO, D = 128, C = 64.
+struct ChunkGradArgs {
+    const int2 *chunk_tok;        // [max chunks] first token, length
+    size_t n_items;               // max chunks x H
+    int32_t H;
+    float scale;
+    const uint8_t *aux;           // per item kBwdAuxBytes: A^kk, A^qk (f16 panels)
+    const uint8_t *sst;           // per item 2 x 16 KB: S_c (f16, value tiles of 64)
+    const uint8_t *ds_t;          // per item 4 x 16 KB: dS_{c+1}^T tf32 tiles of 32 rows
+    const uint8_t *ds_n;          // per item 64 KB: dS_{c+1} fp32, K-major SW128 panels
+    const void *q, *k, *v, *d_out;  // bf16 [T, H, 128] (d_out may be null)
+    const float *log_alpha, *beta;
+    float *dq, *dk, *dv, *dlog_alpha, *dbeta;
+    float *dE, *dW, *dG;          // scratch [items][64][128]
+    float *dAqk;                  // scratch [items][64][64]
+    int *status;
+};
+cudaError_t launch_chunk_grad(const ChunkGradArgs &a, cudaStream_t stream);
 
 // The fused input prologue, as each kernel applies it to one element.
 constexpr float kL2Eps = 1e-6f;

@@ -316,6 +316,21 @@ __device__ __forceinline__ void mma_panels(uint32_t d_tmem, uint32_t a_base, uin
     }
 }
 
+// Half-precision A K-major (panels of 128-byte rows), B MN-major (N = 64,
+// SW128: one 128-byte row of 64 values per K index): K walks 32 bytes of A
+// and 16 rows = 2048 bytes of B per step.
+__device__ __forceinline__ void mma_kmajor_a_mn_b(uint32_t d_tmem, uint32_t a_base,
+                                                  uint32_t a_panel, uint32_t b_base, int ksteps,
+                                                  uint32_t idesc, bool accumulate_first) {
+#pragma unroll
+    for (int ks = 0; ks < ksteps; ++ks) {
+        const uint32_t a = a_base + (ks >> 2) * a_panel + (ks & 3) * 32;
+        const uint32_t b = b_base + ks * 2048;
+        mma_half(d_tmem, sdesc_sw128(a), sdesc_sw128(b), idesc,
+                 (ks > 0 || accumulate_first) ? 1u : 0u);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // TMEM -> registers: 32 lanes x 32-bit, N consecutive columns per thread
 // ---------------------------------------------------------------------------
