@@ -504,7 +504,7 @@ kdaStatus_t kda_recurrent_bwd(const void *q, const void *k, const void *v,
  * as for kda_recurrent_bwd; q, k, v and log_alpha must be 16-byte aligned.
  * Scratch (the forward engine's images and states, the per-chunk factors,
  * state gradients and intermediate gradients: about (T / 64 + N + 1) * H *
- * 490 KB) is taken with cudaMallocAsync / cudaFreeAsync on `stream`.
+ * 540 KB) is taken with cudaMallocAsync / cudaFreeAsync on `stream`.
  */
 kdaStatus_t kda_chunk_bwd(const void *q, const void *k, const void *v,
                           const float *log_alpha, const float *beta, float scale,

@@ -447,7 +447,7 @@ chunk_rscan_kernel(const uint8_t *__restrict__ mt_img, const float *__restrict__
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct ChunkBwdLayout {
-    size_t fwd, aux, mt, x, gl, ds_t, ds_n, de, dw, dg, daqk, total;
+    size_t fwd, aux, mt, x, gl, ds_t, ds_n, img, total;
 };
 
 ChunkBwdLayout chunk_bwd_layout(int32_t N, int32_t T, int32_t H) {
@@ -466,10 +466,7 @@ ChunkBwdLayout chunk_bwd_layout(int32_t N, int32_t T, int32_t H) {
     L.gl = take(items * AD * 4);
     L.ds_t = take(items * RNT * (size_t)DS_IMG);
     L.ds_n = take(items * AD * AD * 4);
-    L.de = take(items * AC * AD * 4);
-    L.dw = take(items * AC * AD * 4);
-    L.dg = take(items * AC * AD * 4);
-    L.daqk = take(items * AC * AC * 4);
+    L.img = take(items * (size_t)kGradImgBytes);
     L.total = off;
     return L;
 }
@@ -530,6 +527,7 @@ cudaError_t launch_chunk_bwd(const BwdArgs &a, int *status, cudaStream_t stream)
     ChunkGradArgs g;
     g.chunk_tok = view.chunk_tok;
     g.n_items = items;
+    g.T = a.T;
     g.H = a.H;
     g.scale = a.scale;
     g.aux = ws + L.aux;
@@ -539,10 +537,7 @@ cudaError_t launch_chunk_bwd(const BwdArgs &a, int *status, cudaStream_t stream)
     g.q = a.q; g.k = a.k; g.v = a.v; g.d_out = a.d_out;
     g.log_alpha = a.log_alpha; g.beta = a.beta;
     g.dq = a.dq; g.dk = a.dk; g.dv = a.dv; g.dlog_alpha = a.dlog_alpha; g.dbeta = a.dbeta;
-    g.dE = reinterpret_cast<float *>(ws + L.de);
-    g.dW = reinterpret_cast<float *>(ws + L.dw);
-    g.dG = reinterpret_cast<float *>(ws + L.dg);
-    g.dAqk = reinterpret_cast<float *>(ws + L.daqk);
+    g.img = ws + L.img;
     g.status = status;
     return launch_chunk_grad(g, stream);
 }

@@ -33,18 +33,23 @@
 // Two launches over the (chunk, head) items, 256 threads each, one CTA per
 // SM (shared memory), all 512 TMEM columns:
 //   chunk_grad_g1 -- the products with the d x d matrices S and dS: E, dE,
-//                    dQ_hat, dW, dA^qk, dK_end; writes the partial dq, dk and
-//                    dG and the scratch dE, dW, dA^qk.
+//                    dQ_hat, dW, dA^qk, dK_end; stores dq, dk and dlog_alpha
+//                    without the second kernel's terms, and dE, dW, dA^qk as
+//                    that kernel's operand images (both orientations each).
 //   chunk_grad_g2 -- the C x C products: dA, dB1, dB2, A^T dA, dR, then the
-//                    decayed products' gradients and every output.
-// Operands are K-major 128-byte-swizzled shared-memory panels, staged by the
-// threads from global memory, the forward's images or TMEM readouts.  Every
+//                    decayed products' gradients; stores dv and dbeta and adds
+//                    its terms to dq, dk and dlog_alpha (reductions that return
+//                    nothing, one per element: the sums are deterministic).
+// Inputs arrive as TMA tiles (one head's 64 tokens x 128 channels), images as
+// bulk copies; operands are K-major 128-byte-swizzled shared-memory panels,
+// staged by the threads from those tiles or from TMEM readouts.  Every
 // product with a gradient operand is kind::tf32 (gradients need fp32 range);
 // the two whose operands are both forward values (U, W and W S) are
 // kind::f16 on the forward's own f16 factors, as the forward computed them.
 // A 64-row operand of a 128-row MMA is read with the 8 KB that follow it
 // (rows 64..127 give accumulator rows that are never read).
 #include <cstdint>
+#include <cstring>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -103,54 +108,67 @@ __device__ __forceinline__ void zero32(float (&v)[32]) {
     for (int j = 0; j < 32; ++j) v[j] = 0.f;
 }
 
-// The channel-ch, token-half inputs of one thread: G (base 2, cumulative from
-// the chunk's first token, carried across the halves through shared memory),
-// and k, v, q, dO as packed bf16 pairs; rows past the chunk's L tokens zero.
+// One thread's inputs: channel ch, tokens i0 .. i0 + 31 of the chunk, read
+// from the TMA tiles ([64 tokens][128 channels]; rows past the chunk's L
+// tokens read as zero): G (base 2, cumulative from the chunk's first token;
+// the caller adds the first half's carry), k, v, and q or dO as bf16 pairs.
 struct TokenInputs {
     float G[32];
-    uint32_t kp[16], vp[16], qp[16], dp[16];
+    uint32_t kp[16], vp[16], xp[16];
 };
 
-__device__ __forceinline__ void load_inputs(const ChunkGradArgs &a, size_t base, size_t rs,
-                                            int i0, int L, bool want_q, bool want_do,
-                                            TokenInputs &in) {
-    const unsigned short *k16 = static_cast<const unsigned short *>(a.k);
-    const unsigned short *v16 = static_cast<const unsigned short *>(a.v);
-    const unsigned short *q16 = static_cast<const unsigned short *>(a.q);
-    const unsigned short *d16 = static_cast<const unsigned short *>(a.d_out);
+__device__ __forceinline__ void read_tiles(const float *gt, const unsigned short *kt,
+                                           const unsigned short *vt, const unsigned short *xt,
+                                           int ch, int i0, int L, TokenInputs &in) {
     float acc = 0.f;
 #pragma unroll
     for (int ii = 0; ii < 32; ++ii) {
         const int i = i0 + ii;
-        const float lg = i < L ? a.log_alpha[base + (size_t)i * rs] : 0.f;
-        acc = fmaf(lg, kLog2e, acc);
+        acc = fmaf(i < L ? gt[i * GD + ch] : 0.f, kLog2e, acc);
         in.G[ii] = acc;
     }
+    auto pair = [&](const unsigned short *t, int jj) -> uint32_t {
+        if (!t) return 0u;
+        const int ia = i0 + 2 * jj, ib = ia + 1;
+        return (ia < L ? (uint32_t)t[ia * GD + ch] : 0u) |
+               ((ib < L ? (uint32_t)t[ib * GD + ch] : 0u) << 16);
+    };
 #pragma unroll
     for (int jj = 0; jj < 16; ++jj) {
-        const int ia = i0 + 2 * jj, ib = ia + 1;
-        const size_t ra = base + (size_t)ia * rs, rb = base + (size_t)ib * rs;
-        const bool va = ia < L, vb = ib < L;
-        in.kp[jj] = (va ? k16[ra] : 0u) | ((vb ? (uint32_t)k16[rb] : 0u) << 16);
-        in.vp[jj] = (va ? v16[ra] : 0u) | ((vb ? (uint32_t)v16[rb] : 0u) << 16);
-        in.qp[jj] = want_q ? ((va ? q16[ra] : 0u) | ((vb ? (uint32_t)q16[rb] : 0u) << 16)) : 0u;
-        in.dp[jj] = (want_do && d16)
-                        ? ((va ? d16[ra] : 0u) | ((vb ? (uint32_t)d16[rb] : 0u) << 16))
-                        : 0u;
+        in.kp[jj] = pair(kt, jj);
+        in.vp[jj] = pair(vt, jj);
+        in.xp[jj] = pair(xt, jj);
     }
 }
+
+struct GradMaps {
+    CUtensorMap q, k, v, d, g;  // {128, H, T}, box {128, 1, 64}
+};
+
+// Per-item image block that G1 writes and G2 bulk-copies (tf32 operands,
+// rounded): dE (rows i, K = v; 4 x 8 KB), dE^T (rows v, K = i; 2 x 16 KB),
+// dW and dW^T likewise, s dA^qk (rows i, K = j; 2 x 8 KB) and its transpose
+// (rows j, K = i; 2 x 8 KB); then s dA^qk as exact fp32 rows [64][64] for the
+// direct-exponent path (its column sums telescope in dlog_alpha, which
+// magnifies any rounding of it).
+constexpr uint32_t IM_DE = 0, IM_DET = 32768, IM_DW = 65536, IM_DWT = 98304, IM_AQ = 131072,
+                   IM_AQT = 147456, IM_AQX = 163840;
+static_assert(IM_AQX + 16384 == kGradImgBytes, "image block");
 
 // ---------------------------------------------------------------------------
 // G1: the products with S and dS
 // ---------------------------------------------------------------------------
-// Shared arena, in 16 KB units u0..u11 (regions reused once their MMAs have
-// completed):
+// Shared arena, in 16 KB units u0..u11 (regions reused once their readers
+// are done):
+//   step 0: the g tile u0-1, k tile u3, v and dO tiles u4-5 (read into
+//           registers), A^kk / A^qk f16 u2, dS^T u8-11 (bulk)
 //   step 1: dO^T (rows v, K = i) u0-1 | A^kk, A^qk f16 u2 | A^qk^T-rows tf32
 //           (rows j, K = i) u3 | K_end (rows j, K = a) u4-5 | [B1 | B2] f16
 //           MN-major u6-7 | dS^T (rows v, K = a) u8-11
 //   step 2: -W f16 (rows i, K = a) u2 | S_c f16 image u6-7 | S (rows a, K = v)
 //           tf32 panels u0, u1, u4, u5 | [dO ; dE] (rows i, K = v) u8-11
-//   step 3: dS (rows a, K = v) u0-3 | E (rows j, K = v) u4-6 | dO in u8-11
+//   step 3: dS (rows a, K = v) u0-3 | E (rows j, K = v) u4-6 | S_c image u6-7
+//           (read by the dG_last term) | dO in u8-11
 // TMEM columns: U / E 0..127, W 128..255, dE^T 256..319 -> [dQ_hat^T | -dW^T]
 // 256..383, dA^qk^T 384..447, dK_end^T 448..511.
 struct G1Smem {
@@ -159,18 +177,21 @@ struct G1Smem {
     float gcarry[GD], glast[GD];
     float sterm[2][GD];   // sum over a value half of dS[a][v] S[a][v]
     float kterm[2][GD];   // sum over a token half of K_end dK_end
-    uint64_t bar_ld, bar_sf, bar_dsn, bar_m[4];
+    float tail[GD];       // sum of the second token half's dG (for dlog_alpha)
+    uint64_t bar_in, bar_ld, bar_sf, bar_dsn, bar_m[4];
     uint32_t tmem;
 };
 constexpr uint32_t G1_DOT = 0, G1_AQ = 2 * U16, G1_AQT = 3 * U16, G1_KE = 4 * U16,
                    G1_BB = 6 * U16, G1_DST = 8 * U16;
+constexpr uint32_t G1_TG = 0, G1_TK = 3 * U16, G1_TV = 4 * U16, G1_TD = 5 * U16;
 constexpr uint32_t G1_NW = 2 * U16, G1_SF = 6 * U16, G1_ODE = 8 * U16;
 constexpr uint32_t G1_DSN = 0, G1_E = 4 * U16;
 __device__ __forceinline__ uint32_t g1_s_panel(int p) { return (uint32_t)(p < 2 ? p : p + 2) * U16; }
 constexpr size_t kG1Smem = sizeof(G1Smem) + 1024;
 static_assert(kG1Smem <= 227 * 1024, "G1 shared memory");
 
-__global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g1_kernel(const ChunkGradArgs a) {
+__global__ void __launch_bounds__(kGThreads, 1)
+chunk_grad_g1_kernel(const __grid_constant__ GradMaps maps, const ChunkGradArgs a) {
     extern __shared__ uint8_t smem_raw[];
     G1Smem &sm = *reinterpret_cast<G1Smem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -183,13 +204,21 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g1_kernel(const Chunk
     const int2 tok = a.chunk_tok[c];
     const int32_t t0 = tok.x, L = tok.y;
     if (L <= 0) return;
+    const bool has_do = a.d_out != nullptr;
+    uint8_t *img = a.img + item * (size_t)kGradImgBytes;
 
     if (tid == 0) {
+        mbar_init(&sm.bar_in, 1);
         mbar_init(&sm.bar_ld, 1);
         mbar_init(&sm.bar_sf, 1);
         mbar_init(&sm.bar_dsn, 1);
         for (int m = 0; m < 4; ++m) mbar_init(&sm.bar_m[m], 1);
         fence_mbar_init();
+        mbar_arrive_expect_tx(&sm.bar_in, (has_do ? 3u : 2u) * 16384u + 32768u);
+        tma_load_3d(ar + G1_TG, &maps.g, 0, h, t0, &sm.bar_in);
+        tma_load_3d(ar + G1_TK, &maps.k, 0, h, t0, &sm.bar_in);
+        tma_load_3d(ar + G1_TV, &maps.v, 0, h, t0, &sm.bar_in);
+        if (has_do) tma_load_3d(ar + G1_TD, &maps.d, 0, h, t0, &sm.bar_in);
         mbar_arrive_expect_tx(&sm.bar_ld, kBwdAuxBytes + 4 * U16);
         bulk_g2s(ar + G1_AQ, a.aux + item * kBwdAuxBytes, kBwdAuxBytes, &sm.bar_ld);
         // dS^T as four 128-row panels (K = 32 key channels each) from the
@@ -199,20 +228,29 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g1_kernel(const Chunk
             for (int p = 0; p < 4; ++p)
                 bulk_g2s(ar + G1_DST + p * U16 + vt * 4096, dt + vt * U16 + p * 4096, 4096,
                          &sm.bar_ld);
+        // the later loads to L2 now
+        bulk_prefetch_l2(a.sst + item * (2 * U16), 2 * U16);
+        bulk_prefetch_l2(a.ds_n + item * (4 * U16), 4 * U16);
     }
     if (warp == 0) {
         tmem_alloc(&sm.tmem, 512);
         tmem_relinquish();
     }
+    if (tid < GC) sm.beta[tid] = tid < L ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
     const size_t rs = (size_t)H * GD;
     const size_t base = ((size_t)t0 * H + h) * GD + ch;
-    TokenInputs in;
-    load_inputs(a, base, rs, i0, L, false, true, in);
-    if (tid < GC) sm.beta[tid] = tid < L ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
-    if (hf == 0) sm.gcarry[ch] = in.G[31];
     tc_fence_before();
-    __syncthreads();
+    __syncthreads();  // barrier init, TMEM address, beta
     tc_fence_after();
+    bool ok = mbar_wait_bounded(&sm.bar_in, 0, kGradWait);
+    TokenInputs in;
+    read_tiles(reinterpret_cast<const float *>(ar + G1_TG),
+               reinterpret_cast<const unsigned short *>(ar + G1_TK),
+               reinterpret_cast<const unsigned short *>(ar + G1_TV),
+               has_do ? reinterpret_cast<const unsigned short *>(ar + G1_TD) : nullptr, ch, i0, L,
+               in);
+    if (hf == 0) sm.gcarry[ch] = in.G[31];
+    __syncthreads();  // the tiles are consumed; carries published
     if (hf == 1) {
         const float cy = sm.gcarry[ch];
 #pragma unroll
@@ -238,11 +276,11 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g1_kernel(const Chunk
             *reinterpret_cast<__half *>(b2 + sw128_offset(i, ch & 63)) =
                 __float2half_rn(b * exp2_approx(in.G[ii]) * kv);
             f32_at(ke, i, ch & 31) = tf32_operand(exp2_approx(Gl - in.G[ii]) * kv);
-            dov[ii] = bfv(in.dp, ii);
+            dov[ii] = bfv(in.xp, ii);
         }
         row32_tf32(ar + G1_DOT + hf * U16, ch, dov);
     }
-    bool ok = mbar_wait_bounded(&sm.bar_ld, 0, kGradWait);
+    ok = mbar_wait_bounded(&sm.bar_ld, 0, kGradWait) && ok;
     {
         // A^qk^T-rows: row j holds A^qk[i][j] over i (f16 -> fp32 is exact)
         const int j = tid & 63, ib = (tid >> 6) * 16;
@@ -298,20 +336,22 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g1_kernel(const Chunk
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
     {
-        // dE^T: lane = value channel v, tokens of this half; to scratch and
-        // into rows 64.. of [dO ; dE]; dO into rows 0..63
+        // dE^T: lane = value channel v, tokens of this half.  Into rows 64..
+        // of [dO ; dE] (dO into rows 0..63), and out as G2's dE and dE^T images
         float e[32];
         if (ok) tmem_ld32(tmem_addr(tmem, quad * 32, 256 + hf * 32), e);
         else zero32(e);
-        float *dst = a.dE + item * (GC * GD) + ch;
         uint8_t *ode = ar + G1_ODE + (ch >> 5) * U16;
+        uint8_t *gde = img + IM_DE + (ch >> 5) * P8;
 #pragma unroll
         for (int ii = 0; ii < 32; ++ii) {
             const int i = i0 + ii;
-            dst[(size_t)i * GD] = e[ii];
-            f32_at(ode, 64 + i, ch & 31) = tf32_operand(e[ii]);
-            f32_at(ode, i, ch & 31) = bfv(in.dp, ii);
+            const float x = tf32_operand(e[ii]);
+            f32_at(ode, 64 + i, ch & 31) = x;
+            f32_at(gde, i, ch & 31) = x;
+            f32_at(ode, i, ch & 31) = bfv(in.xp, ii);
         }
+        row32_tf32(img + IM_DET + hf * U16, ch, e);
     }
     ok = ok && mbar_wait_bounded(&sm.bar_sf, 0, kGradWait);
     {
@@ -377,7 +417,7 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g1_kernel(const Chunk
     ok = ok && mbar_wait_bounded(&sm.bar_dsn, 0, kGradWait);
     {
         // sum_v dS[a][v] S[a][v] over value half hf (S from the f16 image)
-        const uint8_t *sf = a.sst + item * (2 * U16) + hf * U16;
+        const uint8_t *sf = ar + G1_SF + hf * U16;
         float acc = 0.f;
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
@@ -416,7 +456,7 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g1_kernel(const Chunk
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
             const int ia = i0 + 2 * jj, ib = ia + 1;
-            in.qp[jj] = (ia < L ? q16[base + (size_t)ia * rs] : 0u) |
+            in.xp[jj] = (ia < L ? q16[base + (size_t)ia * rs] : 0u) |
                         ((ib < L ? (uint32_t)q16[base + (size_t)ib * rs] : 0u) << 16);
         }
     }
@@ -426,24 +466,33 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g1_kernel(const Chunk
 
     // ---- epilogue ----
     if (quad < 2) {
-        // dA^qk[i][j], lane = j: masked (j <= i < L) to scratch
+        // s dA^qk[i][j] (lane = j), masked (j <= i < L): G2's two images
         float x[32];
         if (ok) tmem_ld32(tmem_addr(tmem, quad * 32, 384 + hf * 32), x);
         else zero32(x);
-        float *dst = a.dAqk + item * (GC * GC) + ch;
+        uint8_t *gaq = img + IM_AQ + (ch >> 5) * P8;
+        float *gax = reinterpret_cast<float *>(img + IM_AQX) + ch;
 #pragma unroll
         for (int ii = 0; ii < 32; ++ii) {
             const int i = i0 + ii;
-            dst[(size_t)i * GC] = (ch <= i && i < L) ? x[ii] : 0.f;
+            x[ii] = (ch <= i && i < L) ? a.scale * x[ii] : 0.f;
+            f32_at(gaq, i, ch & 31) = tf32_operand(x[ii]);
+            gax[i * GC] = x[ii];
         }
+        row32_tf32(img + IM_AQT + hf * P8, ch, x);
     }
     {
+        // dW = -(-dW^T)^T: G2's dW and dW^T images
         float w[32];
         if (ok) tmem_ld32(tmem_addr(tmem, quad * 32, 320 + hf * 32), w);
         else zero32(w);
-        float *dst = a.dW + item * (GC * GD) + ch;
+        uint8_t *gdw = img + IM_DW + (ch >> 5) * P8;
 #pragma unroll
-        for (int ii = 0; ii < 32; ++ii) dst[(size_t)(i0 + ii) * GD] = -w[ii];
+        for (int ii = 0; ii < 32; ++ii) {
+            w[ii] = -w[ii];
+            f32_at(gdw, i0 + ii, ch & 31) = tf32_operand(w[ii]);
+        }
+        row32_tf32(img + IM_DWT + hf * U16, ch, w);
     }
     float dqh[32], dke[32];
     if (ok) {
@@ -458,7 +507,7 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g1_kernel(const Chunk
     for (int ii = 0; ii < 32; ++ii) {
         const int i = i0 + ii;
         const float gam = exp2_approx(in.G[ii]), ek = exp2_approx(Gl - in.G[ii]);
-        const float qhat = a.scale * gam * bfv(in.qp, ii);
+        const float qhat = a.scale * gam * bfv(in.xp, ii);
         const float kend = ek * bfv(in.kp, ii);
         kt = fmaf(kend, dke[ii], kt);
         if (i < L) {
@@ -466,24 +515,32 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g1_kernel(const Chunk
             a.dq[r] = a.scale * gam * dqh[ii];
             a.dk[r] = ek * dke[ii];
         }
-        dqh[ii] = qhat * dqh[ii] - kend * dke[ii];  // dG without the decayed products
+        dqh[ii] = qhat * dqh[ii] - kend * dke[ii];  // dG without the second kernel's terms
     }
     sm.kterm[hf][ch] = kt;
     __syncthreads();
-    const float dgl =
-        sm.kterm[0][ch] + sm.kterm[1][ch] + exp2_approx(Gl) * (sm.sterm[0][ch] + sm.sterm[1][ch]);
     {
-        float *dst = a.dG + item * (GC * GD) + ch;
+        // dG_last onto the chunk's last token, then the reverse cumulative sum
+        const float dgl = sm.kterm[0][ch] + sm.kterm[1][ch] +
+                          exp2_approx(Gl) * (sm.sterm[0][ch] + sm.sterm[1][ch]);
+        float acc = 0.f;
 #pragma unroll
-        for (int ii = 0; ii < 32; ++ii) {
-            const int i = i0 + ii;
-            dst[(size_t)i * GD] = dqh[ii] + (i == L - 1 ? dgl : 0.f);
+        for (int ii = 31; ii >= 0; --ii) {
+            acc += dqh[ii] + (i0 + ii == L - 1 ? dgl : 0.f);
+            dqh[ii] = acc;
         }
+        if (hf == 1) sm.tail[ch] = acc;
+        __syncthreads();
+        const float add = hf == 0 ? sm.tail[ch] : 0.f;
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii)
+            if (i0 + ii < L) a.dlog_alpha[base + (size_t)(i0 + ii) * rs] = dqh[ii] + add;
     }
     const bool bad = __syncthreads_or(!ok);
     if (bad && tid == 0) {
         atomicExch(a.status, (int)KDA_ERR_TIMEOUT);
         // let every copy this CTA started land before its shared memory goes
+        (void)mbar_wait_bounded(&sm.bar_in, 0, kGradWait);
         (void)mbar_wait_bounded(&sm.bar_ld, 0, kGradWait);
         (void)mbar_wait_bounded(&sm.bar_sf, 0, kGradWait);
         (void)mbar_wait_bounded(&sm.bar_dsn, 0, kGradWait);
@@ -498,17 +555,21 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g1_kernel(const Chunk
 // G2: the C x C products, the decayed products' gradients, the outputs
 // ---------------------------------------------------------------------------
 // Shared arena (16 KB units; 13.5 of them):
-//   step 1: dE (rows i, K = v) u0-1 | dW (rows i, K = a) u2-3 | B1 (rows j,
-//           K = v) u4-5 | B2 (rows j, K = a) u6-7 | dE^T (rows v, K = i) u8-9
-//           | dW^T (rows a, K = i) u10-11 | A^T-rows (rows j, K = i) u12 |
+//   step 0: dE (rows i, K = v) u0-1, dW (rows i, K = a) u2-3, dE^T (rows v,
+//           K = i) u8-9, dW^T (rows a, K = i) u10-11 (bulk, from G1); the g
+//           tile u4-5, k and v tiles u6-7, q tile u12 (read into registers);
 //           A^kk f16 at u13 (8 KB)
-//   step 2: dA^T-rows (rows m, K = i) at 0 | A (rows n, K = m) at 24 KB |
-//           K_hat^T (rows a, K = j) u4-5 | [Q_tilde^T | K_tilde^T] u6-9
-//   step 3: T1 (rows j, K = m) at 40 KB | [s dA^qk ; dR]^T-rows (rows j,
-//           K = i) at 0 (4 x 8 KB) | [dR ; s dA^qk] (rows i, K = j) u10-11
-//   direct path: G, k, q fp32 [64][128] at u4, u6, u8; dR, s dA^qk fp32
-//           [64][64] at u10
-//   epilogue: dG fp32 [64][128] at u4, dbeta partials [64][129] at u6
+//   step 1: + B1 (rows j, K = v) u4-5 | B2 (rows j, K = a) u6-7 | A^T-rows
+//           (rows j, K = i) u12
+//   step 2: K_hat^T (rows a, K = j) u0-1 | [Q_tilde^T | K_tilde^T] u2-5 |
+//           dA^T-rows (rows m, K = i) at 96 KB | A (rows n, K = m) at 120 KB |
+//           s dA^qk^T-rows (rows j, K = i) at 136 KB | s dA^qk in rows 64..127
+//           of [dR ; s dA^qk] (rows i, K = j) u10-11
+//   step 3: T1 (rows j, K = m) at 96 KB
+//   step 4: dR into rows 0..63 of u10-11 and, as beta dR^T-rows, at u12
+//   direct path: G, k, q fp32 [64][128] at u0, u2, u4; dR fp32 [64][64] at
+//           u12, s dA^qk fp32 [64][64] at u10; results at 96 KB
+//   epilogue: dG fp32 [64][128] at 0, dbeta partials [64][129] at 32 KB
 // TMEM columns: dA 0..63, dB1^T 64..127, dB2^T 128..191, T1^T 192..255,
 // -dR 256..319, [X1^T | X2^T] 320..447, Y^T 448..511 (direct path: XR, XQ,
 // YY themselves in 320.., 384.., 448..).
@@ -516,22 +577,24 @@ struct G2Smem {
     uint8_t ar[13 * U16 + P8];
     float beta[GC];
     float gcarry[GD], gmid[GD];
-    uint64_t bar_ld, bar_m[4];
+    uint64_t bar_in, bar_ld, bar_aq, bar_m[4];
     uint32_t tmem;
 };
 constexpr uint32_t G2_DE = 0, G2_DW = 2 * U16, G2_B1 = 4 * U16, G2_B2 = 6 * U16,
                    G2_DET = 8 * U16, G2_DWT = 10 * U16, G2_AT = 12 * U16, G2_AF = 13 * U16;
-constexpr uint32_t G2_DAT = 0, G2_AN = 24576, G2_KH = 4 * U16, G2_KQ = 6 * U16, G2_T1 = 40960,
-                   G2_DRQT = 0, G2_DRQ = 10 * U16;
-constexpr uint32_t G2_GS = 4 * U16, G2_KS = 6 * U16, G2_QS = 8 * U16, G2_DRS = 10 * U16,
-                   G2_DAS = 10 * U16 + 16384;
-constexpr uint32_t G2_DGS = 4 * U16, G2_PS = 6 * U16;
+constexpr uint32_t G2_TG = 4 * U16, G2_TK = 6 * U16, G2_TV = 7 * U16, G2_TQ = 12 * U16;
+constexpr uint32_t G2_KH = 0, G2_KQ = 2 * U16, G2_DAT = 98304, G2_AN = 122880, G2_T1 = 98304,
+                   G2_AQT = 139264, G2_DRQ = 10 * U16, G2_DRT = 12 * U16;
+constexpr uint32_t G2_GS = 0, G2_KS = 2 * U16, G2_QS = 4 * U16, G2_XS = 98304;
+constexpr uint32_t G2_DGS = 0, G2_PS = 2 * U16;
 constexpr int kPS = 129;  // row stride of the dbeta partials (conflict-free column sums)
 constexpr size_t kG2Smem = sizeof(G2Smem) + 1024;
 static_assert(kG2Smem <= 227 * 1024, "G2 shared memory");
-static_assert(G2_PS + GC * kPS * 4 <= 10 * U16, "epilogue scratch below the dR operands");
+static_assert(G2_AN + 16384 <= G2_AQT && G2_AQT + 16384 <= G2_DRQ, "step 2 regions");
+static_assert(G2_XS + 2 * GC * GD * 4 <= G2_DRQ, "direct-path results below [dR ; dA^qk]");
 
-__global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g2_kernel(const ChunkGradArgs a) {
+__global__ void __launch_bounds__(kGThreads, 1)
+chunk_grad_g2_kernel(const __grid_constant__ GradMaps maps, const ChunkGradArgs a) {
     extern __shared__ uint8_t smem_raw[];
     G2Smem &sm = *reinterpret_cast<G2Smem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -544,27 +607,45 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g2_kernel(const Chunk
     const int2 tok = a.chunk_tok[c];
     const int32_t t0 = tok.x, L = tok.y;
     if (L <= 0) return;
+    const uint8_t *img = a.img + item * (size_t)kGradImgBytes;
 
     if (tid == 0) {
+        mbar_init(&sm.bar_in, 1);
         mbar_init(&sm.bar_ld, 1);
+        mbar_init(&sm.bar_aq, 1);
         for (int m = 0; m < 4; ++m) mbar_init(&sm.bar_m[m], 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(&sm.bar_ld, 8192);
+        mbar_arrive_expect_tx(&sm.bar_in, 3 * 16384 + 32768);
+        tma_load_3d(ar + G2_TG, &maps.g, 0, h, t0, &sm.bar_in);
+        tma_load_3d(ar + G2_TK, &maps.k, 0, h, t0, &sm.bar_in);
+        tma_load_3d(ar + G2_TV, &maps.v, 0, h, t0, &sm.bar_in);
+        tma_load_3d(ar + G2_TQ, &maps.q, 0, h, t0, &sm.bar_in);
+        mbar_arrive_expect_tx(&sm.bar_ld, 4 * 32768 + 8192);
+        bulk_g2s(ar + G2_DE, img + IM_DE, 32768, &sm.bar_ld);
+        bulk_g2s(ar + G2_DW, img + IM_DW, 32768, &sm.bar_ld);
+        bulk_g2s(ar + G2_DET, img + IM_DET, 32768, &sm.bar_ld);
+        bulk_g2s(ar + G2_DWT, img + IM_DWT, 32768, &sm.bar_ld);
         bulk_g2s(ar + G2_AF, a.aux + item * kBwdAuxBytes, 8192, &sm.bar_ld);
+        bulk_prefetch_l2(img + IM_AQ, 32768);
     }
     if (warp == 0) {
         tmem_alloc(&sm.tmem, 512);
         tmem_relinquish();
     }
+    if (tid < GC) sm.beta[tid] = tid < L ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
     const size_t rs = (size_t)H * GD;
     const size_t base = ((size_t)t0 * H + h) * GD + ch;
-    TokenInputs in;
-    load_inputs(a, base, rs, i0, L, true, false, in);
-    if (tid < GC) sm.beta[tid] = tid < L ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
-    if (hf == 0) sm.gcarry[ch] = in.G[31];
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    bool ok = mbar_wait_bounded(&sm.bar_in, 0, kGradWait);
+    TokenInputs in;
+    read_tiles(reinterpret_cast<const float *>(ar + G2_TG),
+               reinterpret_cast<const unsigned short *>(ar + G2_TK),
+               reinterpret_cast<const unsigned short *>(ar + G2_TV),
+               reinterpret_cast<const unsigned short *>(ar + G2_TQ), ch, i0, L, in);
+    if (hf == 0) sm.gcarry[ch] = in.G[31];
+    __syncthreads();  // tiles consumed; carries published
     if (hf == 1) {
         const float cy = sm.gcarry[ch];
 #pragma unroll
@@ -579,27 +660,18 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g2_kernel(const Chunk
     const bool direct = __syncthreads_or(!(span <= kGradSpan2));
     const uint32_t tmem = sm.tmem;
 
-    // ---- step 1 operands ----
+    // ---- step 1 operands: B1, B2 (token rows), A^T-rows ----
     {
         uint8_t *b1 = ar + G2_B1 + (ch >> 5) * P8, *b2 = ar + G2_B2 + (ch >> 5) * P8;
-        uint8_t *de = ar + G2_DE + (ch >> 5) * P8, *dw = ar + G2_DW + (ch >> 5) * P8;
-        const float *gE = a.dE + item * (GC * GD) + ch, *gW = a.dW + item * (GC * GD) + ch;
-        float xe[32], xw[32];
 #pragma unroll
         for (int ii = 0; ii < 32; ++ii) {
             const int i = i0 + ii;
             const float b = sm.beta[i];
             f32_at(b1, i, ch & 31) = tf32_operand(b * bfv(in.vp, ii));
             f32_at(b2, i, ch & 31) = tf32_operand(b * exp2_approx(in.G[ii]) * bfv(in.kp, ii));
-            xe[ii] = gE[(size_t)i * GD];
-            xw[ii] = gW[(size_t)i * GD];
-            f32_at(de, i, ch & 31) = tf32_operand(xe[ii]);
-            f32_at(dw, i, ch & 31) = tf32_operand(xw[ii]);
         }
-        row32_tf32(ar + G2_DET + hf * U16, ch, xe);
-        row32_tf32(ar + G2_DWT + hf * U16, ch, xw);
     }
-    bool ok = mbar_wait_bounded(&sm.bar_ld, 0, kGradWait);
+    ok = mbar_wait_bounded(&sm.bar_ld, 0, kGradWait) && ok;
     {
         // A^T-rows: row j holds A[i][j] over i
         const int j = tid & 63, ib = (tid >> 6) * 16;
@@ -626,6 +698,19 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g2_kernel(const Chunk
         mma_commit(&sm.bar_m[0]);
     }
     ok = ok && mbar_wait_bounded(&sm.bar_m[0], 0, kGradWait);
+    if (tid == 0 && ok) {
+        if (!direct) {
+            // s dA^qk in rows 64..127 of [dR ; s dA^qk] and as its transposed rows
+            mbar_arrive_expect_tx(&sm.bar_aq, 32768);
+            bulk_g2s(ar + G2_DRQ + 8192, img + IM_AQ, 8192, &sm.bar_aq);
+            bulk_g2s(ar + G2_DRQ + U16 + 8192, img + IM_AQ + 8192, 8192, &sm.bar_aq);
+            bulk_g2s(ar + G2_AQT, img + IM_AQT, 16384, &sm.bar_aq);
+        } else {
+            // the exact fp32 rows, where [dR ; s dA^qk] would be
+            mbar_arrive_expect_tx(&sm.bar_aq, 16384);
+            bulk_g2s(ar + G2_DRQ, img + IM_AQX, 16384, &sm.bar_aq);
+        }
+    }
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
 
@@ -656,7 +741,7 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g2_kernel(const Chunk
         float kh[32], qt[32], kt[32];
 #pragma unroll
         for (int ii = 0; ii < 32; ++ii) {
-            const float kv = bfv(in.kp, ii), qv = bfv(in.qp, ii);
+            const float kv = bfv(in.kp, ii), qv = bfv(in.xp, ii);
             const float ep = exp2_approx(in.G[ii] - Gm), en = exp2_approx(Gm - in.G[ii]);
             kh[ii] = kv * en;
             qt[ii] = qv * ep;
@@ -673,7 +758,7 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g2_kernel(const Chunk
             const int i = i0 + ii;
             gs[i * GD + ch] = in.G[ii];
             ks[i * GD + ch] = bfv(in.kp, ii);
-            qs[i * GD + ch] = bfv(in.qp, ii);
+            qs[i * GD + ch] = bfv(in.xp, ii);
         }
     }
     fence_proxy_async();
@@ -690,7 +775,7 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g2_kernel(const Chunk
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
 
-    // ---- step 3: T1 (rows j), s dA^qk into the decayed operands ----
+    // ---- step 3: T1 (rows j) ----
     if (quad < 2) {
         // lane = m; columns j = 32 hf ..
         float x[32];
@@ -699,26 +784,6 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g2_kernel(const Chunk
         uint8_t *dst = ar + G2_T1 + (ch >> 5) * P8;
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) f32_at(dst, i0 + jj, ch & 31) = tf32_operand(x[jj]);
-    }
-    {
-        // s dA^qk[i][j]: thread -> j, 16 rows i
-        const int j = tid & 63, ib = (tid >> 6) * 16;
-        const float *src = a.dAqk + item * (GC * GC) + j;
-        if (!direct) {
-            uint8_t *drq = ar + G2_DRQ + (j >> 5) * U16;     // rows 64 + i, K = j
-            uint8_t *drqt = ar + G2_DRQT + (ib >> 5) * P8;  // rows j, K = i
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int i = ib + e;
-                const float x = tf32_operand(a.scale * src[(size_t)i * GC]);
-                f32_at(drq, 64 + i, j & 31) = x;
-                f32_at(drqt, j, i & 31) = x;
-            }
-        } else {
-            float *das = reinterpret_cast<float *>(ar + G2_DAS);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) das[(ib + e) * GC + j] = a.scale * src[(size_t)(ib + e) * GC];
-        }
     }
     fence_proxy_async();
     tc_fence_before();
@@ -748,16 +813,18 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g2_kernel(const Chunk
         }
         if (!direct) {
             row32_tf32(ar + G2_DRQ + hf * U16, i, x);
-            uint8_t *drqt = ar + G2_DRQT + (2 + (i >> 5)) * P8;  // rows n, K = 64 + i
+            uint8_t *drt = ar + G2_DRT + (i >> 5) * P8;  // rows n, K = i
             const float b = sm.beta[i];
 #pragma unroll
-            for (int nn = 0; nn < 32; ++nn) f32_at(drqt, i0 + nn, i & 31) = tf32_operand(b * x[nn]);
+            for (int nn = 0; nn < 32; ++nn) f32_at(drt, i0 + nn, i & 31) = tf32_operand(b * x[nn]);
         } else {
-            float *drs = reinterpret_cast<float *>(ar + G2_DRS);
+            // the direct path reads dR as plain fp32 rows
+            float *drs = reinterpret_cast<float *>(ar + G2_DRT);
 #pragma unroll
             for (int nn = 0; nn < 32; ++nn) drs[i * GC + i0 + nn] = x[nn];
         }
     }
+    ok = ok && mbar_wait_bounded(&sm.bar_aq, 0, kGradWait);
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
@@ -767,9 +834,11 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g2_kernel(const Chunk
             // (5) [X1^T | X2^T] = K_hat^T [dR ; s dA^qk]^T   (cols 320..447)
             mma_panels<true>(tmem + 320, smem_u32(ar + G2_KH), U16, smem_u32(ar + G2_DRQ), U16, 8,
                              idesc_tf32_f32(128, 128), false);
-            // (6) Y^T = [Q_tilde^T | K_tilde^T] [s dA^qk ; Diag(beta) dR]   (cols 448..511)
-            mma_panels<true>(tmem + 448, smem_u32(ar + G2_KQ), U16, smem_u32(ar + G2_DRQT), P8, 16,
+            // (6) Y^T = Q_tilde^T (s dA^qk) + K_tilde^T Diag(beta) dR   (cols 448..511)
+            mma_panels<true>(tmem + 448, smem_u32(ar + G2_KQ), U16, smem_u32(ar + G2_AQT), P8, 8,
                              idesc_tf32_f32(128, 64), false);
+            mma_panels<true>(tmem + 448, smem_u32(ar + G2_KQ + 2 * U16), U16,
+                             smem_u32(ar + G2_DRT), P8, 8, idesc_tf32_f32(128, 64), true);
             mma_commit(&sm.bar_m[3]);
         }
         ok = ok && mbar_wait_bounded(&sm.bar_m[3], 0, kGradWait);
@@ -777,15 +846,18 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g2_kernel(const Chunk
         tc_fence_after();
     } else {
         // Direct evaluation (decays beyond e^-80 across half a chunk): every
-        // exp(G_i - G_j) with i >= j (at most 1), into the same TMEM columns.
+        // exp(G_i - G_j) with i >= j (at most 1), into the same TMEM columns,
+        // from dR and s dA^qk as fp32 rows.
         const float *gs = reinterpret_cast<const float *>(ar + G2_GS);
         const float *ks = reinterpret_cast<const float *>(ar + G2_KS);
         const float *qs = reinterpret_cast<const float *>(ar + G2_QS);
-        const float *drs = reinterpret_cast<const float *>(ar + G2_DRS);
-        const float *das = reinterpret_cast<const float *>(ar + G2_DAS);
-        // per-thread results go through the dead operand area at 0 (each
-        // thread reads back only what it wrote)
-        float *xrs = reinterpret_cast<float *>(ar), *xqs = xrs + GC * GD;
+        const float *drs = reinterpret_cast<const float *>(ar + G2_DRT);
+        const float *das = reinterpret_cast<const float *>(ar + G2_DRQ);
+        auto dr = [&](int i, int j) { return drs[i * GC + j]; };
+        auto da = [&](int i, int j) { return das[i * GC + j]; };
+        // per-thread results go through a dead operand area (each thread
+        // reads back only what it wrote)
+        float *xrs = reinterpret_cast<float *>(ar + G2_XS), *xqs = xrs + GC * GD;
 #pragma unroll 1
         for (int ii = 0; ii < 32; ++ii) {
             const int i = i0 + ii;
@@ -793,8 +865,8 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g2_kernel(const Chunk
             float r = 0.f, s = 0.f;
             for (int j = 0; j <= i; ++j) {
                 const float w = exp2_approx(gi - gs[j * GD + ch]) * ks[j * GD + ch];
-                r = fmaf(drs[i * GC + j], w, r);
-                s = fmaf(das[i * GC + j], w, s);
+                r = fmaf(dr(i, j), w, r);
+                s = fmaf(da(i, j), w, s);
             }
             xrs[i * GD + ch] = r;
             xqs[i * GD + ch] = s;
@@ -813,9 +885,8 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g2_kernel(const Chunk
             float y = 0.f;
             for (int i = j; i < GC; ++i) {
                 const float e = exp2_approx(gs[i * GD + ch] - gj);
-                y = fmaf(sm.beta[i] * drs[i * GC + j] * ks[i * GD + ch] +
-                             das[i * GC + j] * qs[i * GD + ch],
-                         e, y);
+                y = fmaf(sm.beta[i] * dr(i, j) * ks[i * GD + ch] + da(i, j) * qs[i * GD + ch], e,
+                         y);
             }
             xrs[j * GD + ch] = y;
         }
@@ -839,7 +910,6 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g2_kernel(const Chunk
             const int ii = g * 16 + e;
             ep[e] = direct ? 1.f : exp2_approx(in.G[ii] - Gm);
         }
-        const float *dgp = a.dG + item * (GC * GD) + ch;
         // dB2: B2 = Diag(beta)(exp(G) * K)
         if (ok) tmem_ld16(tmem_addr(tmem, quad * 32, 128 + c0), y);
 #pragma unroll
@@ -848,7 +918,7 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g2_kernel(const Chunk
             const float yv = ok ? y[e] : 0.f;
             const float b = sm.beta[i], gam = exp2_approx(in.G[ii]), kv = bfv(in.kp, ii);
             dkv[e] = b * gam * yv;
-            dgv[e] = dgp[(size_t)i * GD] + b * gam * kv * yv;
+            dgv[e] = b * gam * kv * yv;
             pv[e] = gam * kv * yv;
         }
         // dB1: B1 = Diag(beta) V (lane = value channel)
@@ -876,11 +946,8 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g2_kernel(const Chunk
         for (int e = 0; e < 16; ++e) {
             const int ii = g * 16 + e, i = c0 + e;
             const float xq = ok ? ep[e] * y[e] : 0.f;
-            dgv[e] = fmaf(bfv(in.qp, ii), xq, dgv[e]);
-            if (i < L) {
-                float *dq = a.dq + base + (size_t)i * rs;
-                *dq = *dq + xq;
-            }
+            dgv[e] = fmaf(bfv(in.xp, ii), xq, dgv[e]);
+            if (i < L) atomicAdd(a.dq + base + (size_t)i * rs, xq);
         }
         // YY (columns of R and A^qk)
         if (ok) tmem_ld16(tmem_addr(tmem, quad * 32, 448 + c0), y);
@@ -891,21 +958,18 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g2_kernel(const Chunk
             const float yy = ok ? en * y[e] : 0.f, kv = bfv(in.kp, ii);
             dkv[e] += yy;
             dgv[e] = fmaf(-kv, yy, dgv[e]);
-            if (i < L) {
-                float *dk = a.dk + base + (size_t)i * rs;
-                *dk = *dk + dkv[e];
-            }
+            if (i < L) atomicAdd(a.dk + base + (size_t)i * rs, dkv[e]);
             dgs[i * GD + ch] = dgv[e];
             ps[i * kPS + ch] = pv[e];
         }
     }
     __syncthreads();
     if (tid < GD) {
-        // dlog_alpha: reverse cumulative sum of dG over the chunk's tokens
+        // this kernel's share of dlog_alpha: the reverse cumulative sum of its dG
         float acc = 0.f;
         for (int i = GC - 1; i >= 0; --i) {
             acc += dgs[i * GD + tid];
-            if (i < L) a.dlog_alpha[((size_t)(t0 + i) * H + h) * GD + tid] = acc;
+            if (i < L) atomicAdd(a.dlog_alpha + ((size_t)(t0 + i) * H + h) * GD + tid, acc);
         }
     } else if (tid < GD + GC) {
         const int i = tid - GD;
@@ -916,7 +980,9 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g2_kernel(const Chunk
     const bool bad = __syncthreads_or(!ok);
     if (bad && tid == 0) {
         atomicExch(a.status, (int)KDA_ERR_TIMEOUT);
+        (void)mbar_wait_bounded(&sm.bar_in, 0, kGradWait);
         (void)mbar_wait_bounded(&sm.bar_ld, 0, kGradWait);
+        (void)mbar_wait_bounded(&sm.bar_aq, 0, kGradWait);
         (void)mbar_wait_bounded(&sm.bar_m[2], 0, kGradWait);
         if (!direct) (void)mbar_wait_bounded(&sm.bar_m[3], 0, kGradWait);
     }
@@ -928,7 +994,16 @@ __global__ void __launch_bounds__(kGThreads, 1) chunk_grad_g2_kernel(const Chunk
 }  // namespace
 
 cudaError_t launch_chunk_grad(const ChunkGradArgs &a, cudaStream_t stream) {
-    if (a.n_items == 0) return cudaSuccess;
+    if (a.n_items == 0 || a.T == 0) return cudaSuccess;
+    GradMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    if (!encode_tile_map(&maps.q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H) ||
+        !encode_tile_map(&maps.k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H) ||
+        !encode_tile_map(&maps.v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H) ||
+        !encode_tile_map(&maps.g, a.log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.T, a.H) ||
+        (a.d_out &&
+         !encode_tile_map(&maps.d, a.d_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H)))
+        return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(chunk_grad_g1_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kG1Smem);
@@ -936,10 +1011,10 @@ cudaError_t launch_chunk_grad(const ChunkGradArgs &a, cudaStream_t stream) {
         e = cudaFuncSetAttribute(chunk_grad_g2_kernel,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kG2Smem);
     if (e != cudaSuccess) return e;
-    chunk_grad_g1_kernel<<<(unsigned)a.n_items, kGThreads, kG1Smem, stream>>>(a);
+    chunk_grad_g1_kernel<<<(unsigned)a.n_items, kGThreads, kG1Smem, stream>>>(maps, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    chunk_grad_g2_kernel<<<(unsigned)a.n_items, kGThreads, kG2Smem, stream>>>(a);
+    chunk_grad_g2_kernel<<<(unsigned)a.n_items, kGThreads, kG2Smem, stream>>>(maps, a);
     return cudaGetLastError();
 }
 

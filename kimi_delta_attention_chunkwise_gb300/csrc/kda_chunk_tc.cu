@@ -1718,8 +1718,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // [T, H, D] row-major tensor as a 3-D map {D, H, T}; box = one head's
 // [64 tokens x 128 channels] tile.  Rows past T read as zero.
 bool encode_tile_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, size_t esize,
-                     int32_t T, int32_t H, uint32_t box_x = D,
-                     CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
+                     int32_t T, int32_t H, uint32_t box_x, CUtensorMapSwizzle swz) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};

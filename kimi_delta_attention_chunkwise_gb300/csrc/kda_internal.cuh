@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "kda.h"
@@ -115,7 +116,7 @@ cudaError_t launch_chunk_bwd(const BwdArgs &a, int *status, cudaStream_t stream)
 struct ChunkGradArgs {
     const int2 *chunk_tok;        // [max chunks] first token, length
     size_t n_items;               // max chunks x H
-    int32_t H;
+    int32_t T, H;
     float scale;
     const uint8_t *aux;           // per item kBwdAuxBytes: A^kk, A^qk (f16 panels)
     const uint8_t *sst;           // per item 2 x 16 KB: S_c (f16, value tiles of 64)
@@ -124,10 +125,11 @@ struct ChunkGradArgs {
     const void *q, *k, *v, *d_out;  // bf16 [T, H, 128] (d_out may be null)
     const float *log_alpha, *beta;
     float *dq, *dk, *dv, *dlog_alpha, *dbeta;
-    float *dE, *dW, *dG;          // scratch [items][64][128]
-    float *dAqk;                  // scratch [items][64][64]
+    uint8_t *img;                 // scratch, kGradImgBytes per item (the first kernel's
+                                  // gradients as the second's operand images)
     int *status;
 };
+constexpr uint32_t kGradImgBytes = 176 * 1024;
 cudaError_t launch_chunk_grad(const ChunkGradArgs &a, cudaStream_t stream);
 
 // The fused input prologue, as each kernel applies it to one element.
@@ -179,6 +181,13 @@ cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t stream);
 // Decode step and the multi-token recurrent pass (kda_decode.cu).
 cudaError_t launch_recurrent_step(const StepArgs &a, cudaStream_t stream);
 cudaError_t launch_recurrent_fwd(const RecurArgs &a, cudaStream_t stream);
+
+// A [T, H, 128] row-major tensor as a 3-D tensor map {128, H, T} whose box
+// is one head's [64 tokens x box_x channels] tile (rows past T read as zero),
+// for tiled TMA loads (kda_chunk_tc.cu).
+bool encode_tile_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, size_t esize,
+                     int32_t T, int32_t H, uint32_t box_x = 128,
+                     CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE);
 
 // Tensor-core chunk engine (kda_chunk_tc.cu): bf16, D = 128, C = 64.
 size_t chunk_tc_workspace_bytes(int32_t N, int32_t T, int32_t H);
