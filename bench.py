@@ -657,7 +657,7 @@ def run_head_group(args, dist, peaks, dev, stream):
 def run_varlen(args, dist, peaks, dev, stream):
     """32 packed sequences, lengths ~ U[512, 8192] (136,134 tokens), H=32,
     initial states ~ N(0, 0.02), drawn on the device; inputs far larger than
-    L2 (no flush).  Also the gradients of this workload (recurrent backward)."""
+    L2 (no flush).  Also the gradients of this workload (chunk-form backward)."""
     import torch
     import kimi_delta_attention_chunkwise_gb300 as kda
     from kimi_delta_attention_chunkwise_gb300 import inputs
@@ -682,7 +682,7 @@ def run_varlen(args, dist, peaks, dev, stream):
     gen = torch.Generator(device=dev)
     gen.manual_seed(8)
     do = torch.randn(q.shape, generator=gen, device=dev).to(torch.bfloat16)
-    bwd = lambda: kda.kda_recurrent_bwd(*args_, do, None)
+    bwd = lambda: kda.kda_chunk_bwd(*args_, do, None)
     bwd()
     torch.cuda.synchronize()
     bms, _ = timed_loop(bwd, 2, stream, dist)
@@ -692,7 +692,7 @@ def run_varlen(args, dist, peaks, dev, stream):
            "value": T * dist.world / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
            "stages_ms": stages, "roofline": prefill_roofline(stages, units, ms, peaks),
            "backward": {"ms_per_call": bms / 2, "tokens_per_s": T * dist.world / (bms / 2e3),
-                        "form": "recurrent, 8-token checkpoints"}}
+                        "form": "chunk (kda_chunk_bwd, forward recompute included)"}}
     del x, q, out, fin, do
     torch.cuda.empty_cache()
     return res
@@ -962,10 +962,26 @@ def run_prefill_variants(args, dist, dev, stream, w, dev_inputs):
     return res
 
 
+# Dense products of the chunk-form backward per (token, head), d = 128, C = 64,
+# from the kernels' valid rows (per chunk, divided by its C tokens):
+#   forward recompute without the output pass   8Cd + 4d^2
+#   X_c = Q'^T dO_c and the reverse scan's -M'^T dS  2d^2 + 2d^3 / C
+#   G1: [U | W], dE^T, W S_c, S_c [dO ; dE]^T, E dO^T, dS E^T   8Cd + 10d^2
+#   G2: dA, A^T [dE | dW], A^T dA, dR, [X1 | X2], Y               16Cd + 4C^2
+_C, _D = 64, 128
+BWD_FLOPS_PER_UNIT = ((8 * _C * _D + 4 * _D * _D) + (2 * _D * _D + 2 * _D ** 3 // _C)
+                      + (8 * _C * _D + 10 * _D * _D) + (16 * _C * _D + 4 * _C * _C))
+# Compulsory bytes per (token, head): q, k, v, d_out (bf16) and log_alpha,
+# beta in; dq, dk, dv, dlog_alpha (fp32) and dbeta out.
+BWD_BYTES_PER_UNIT = 4 * 2 * 128 + 4 * 128 + 4 + 4 * 4 * 128 + 4
+
+
 def run_backward(args, dist, peaks, dev, stream, w, dev_inputs):
     """Gradients of the head-group prefill workload (1 sequence x 16 heads x
-    4,096 tokens): the recurrent backward with output and final-state
-    gradients, timed like the headline."""
+    4,096 tokens) with output and final-state gradients, timed like the
+    headline: the chunk form (kda_chunk_bwd: forward recompute, reverse scan
+    and the per-chunk gradient products on the tensor cores) and the
+    token-recurrence form (kda_recurrent_bwd)."""
     import numpy as np
     import torch
     import kimi_delta_attention_chunkwise_gb300 as kda
@@ -974,54 +990,56 @@ def run_backward(args, dist, peaks, dev, stream, w, dev_inputs):
     rng = np.random.default_rng(8)
     do = torch.from_numpy(rng.standard_normal((T, H, d)).astype(np.float32)).to(dev, torch.bfloat16)
     dsf = torch.from_numpy(rng.standard_normal((1, H, d, d)).astype(np.float32)).to(dev)
-    call = lambda: kda.kda_recurrent_bwd(q, k, v, la, beta, w.scale, None, cu, do, dsf)
-    for _ in range(max(3, args.warmup)):
-        call()
-    torch.cuda.synchronize()
     reps = max(3, min(args.steps, 5))
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    preroll(call, 0.1)
-    dist.barrier()
-    torch.cuda.synchronize()
-    evs[0].record(stream)
-    for _ in range(reps):
-        call()
-    evs[1].record(stream)
-    torch.cuda.synchronize()
-    ms = dist.max(evs[0].elapsed_time(evs[1])) / reps
-    # compulsory bytes: q, k, v, d_out (bf16), log_alpha, beta in; dq, dk, dv,
-    # dlog_alpha (fp32), dbeta out; the final-state gradient in
-    bytes_call = (4 * 2 * d + 4 * d + 4 + 4 * 4 * d + 4) * T * H + H * d * d * 4
-    gbs = bytes_call / (ms / 1e3) / 1e9
-    # the chunkwise form on the same inputs (forward engine's factors, reverse
-    # scan on the tensor cores, the walk per 64-token chunk)
-    chunk_call = lambda: kda.kda_chunk_bwd(q, k, v, la, beta, w.scale, None, cu, do, dsf)
-    for _ in range(max(3, args.warmup)):
-        chunk_call()
-    torch.cuda.synchronize()
-    preroll(chunk_call, 0.1)
-    dist.barrier()
-    torch.cuda.synchronize()
-    evs[0].record(stream)
-    for _ in range(reps):
-        chunk_call()
-    evs[1].record(stream)
-    torch.cuda.synchronize()
-    ms_chunk = dist.max(evs[0].elapsed_time(evs[1])) / reps
+
+    def timed(call):
+        for _ in range(max(3, args.warmup)):
+            call()
+        torch.cuda.synchronize()
+        preroll(call, 0.1)
+        dist.barrier()
+        torch.cuda.synchronize()
+        evs[0].record(stream)
+        for _ in range(reps):
+            call()
+        evs[1].record(stream)
+        torch.cuda.synchronize()
+        return dist.max(evs[0].elapsed_time(evs[1])) / reps
+
+    ms_chunk = timed(lambda: kda.kda_chunk_bwd(q, k, v, la, beta, w.scale, None, cu, do, dsf))
+    ms_rec = timed(lambda: kda.kda_recurrent_bwd(q, k, v, la, beta, w.scale, None, cu, do, dsf))
+    units = T * H
+    bytes_call = BWD_BYTES_PER_UNIT * units + H * d * d * 4
+    gbs = bytes_call / (ms_chunk / 1e3) / 1e9
+    tfl = BWD_FLOPS_PER_UNIT * units / (ms_chunk / 1e3) / 1e12
+    gbs_rec = bytes_call / (ms_rec / 1e3) / 1e9
     return {"workload": f"gradients of the single-head-group workload (1 x {H} heads x {T} "
-                        "tokens, d=128, bf16 in, fp32 gradients), recurrent form with 8-token "
-                        "checkpoints",
-            "chunk_form": {"ms_per_step": ms_chunk, "value": T * dist.world / (ms_chunk / 1e3),
-                           "unit": "tokens/s",
-                           "workload": "the same gradients through kda_chunk_bwd (includes "
-                                       "its forward recompute)"},
-            "value": T * dist.world / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
-            "roofline": {"kernel": "recurrent_bwd", "bound": "hbm", "achieved": gbs,
-                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / peaks["hbm_gbs"],
-                         "traffic": profiled_traffic("recurrent_bwd"),
-                         "bytes_per_launch": bytes_call, "peak_source": peaks["source"],
-                         "note": "the per-token walk is latency-bound (barriers), not HBM-bound"}}
+                        "tokens, d=128, bf16 in, fp32 gradients) through the chunk form "
+                        "(kda_chunk_bwd, its forward recompute included)",
+            "value": T * dist.world / (ms_chunk / 1e3), "unit": "tokens/s",
+            "ms_per_step": ms_chunk,
+            "roofline": {"kernel": "chunk_bwd (whole call)", "bound": "latency",
+                         "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "tensor_tflops": tfl,
+                         "tensor_frac": tfl / peaks["bf16_tflops"],
+                         "bytes_per_launch": bytes_call,
+                         "flops_per_unit": BWD_FLOPS_PER_UNIT, "peak_source": peaks["source"],
+                         "traffic": None,
+                         "note": "eight launches (forward recompute, X_c, reverse scan, two "
+                                 "gradient kernels); per-kernel shares in profiles/"},
+            "recurrent_form": {"ms_per_step": ms_rec, "value": T * dist.world / (ms_rec / 1e3),
+                               "unit": "tokens/s",
+                               "workload": "the same gradients through kda_recurrent_bwd "
+                                           "(token recurrence with 8-token checkpoints)",
+                               "roofline": {"kernel": "recurrent_bwd", "bound": "hbm",
+                                            "achieved": gbs_rec, "peak": peaks["hbm_gbs"],
+                                            "unit": "GB/s", "frac": gbs_rec / peaks["hbm_gbs"],
+                                            "traffic": profiled_traffic("recurrent_bwd"),
+                                            "bytes_per_launch": bytes_call,
+                                            "peak_source": peaks["source"],
+                                            "note": "the per-token walk is latency-bound "
+                                                    "(barriers), not HBM-bound"}}}
 
 
 def run_short_conv(args, dist, peaks, dev, stream):

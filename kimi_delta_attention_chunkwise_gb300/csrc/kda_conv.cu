@@ -9,11 +9,14 @@
 // with inputs before the sequence's first token taken from its cache (slot
 // W - 1 the most recent) or zero.
 //
-// Memory-bound elementwise work: a thread owns 4 consecutive channels (one
-// 16-byte fp32 or 8-byte bf16 vector) for a block of TB tokens; it issues all of the block's rows
-// and the W - 1 before them as independent loads first, then filters from
-// registers, so every input row is read once per block (plus the halo) and
-// every output written once, fully coalesced along channels.
+// Memory-bound elementwise work: a thread owns one 16-byte vector of
+// consecutive channels (8 bf16 or 4 fp32) for a block of TB tokens; it issues
+// all of the block's rows and the W - 1 before them as independent loads
+// first, then filters from registers, so every input row is read once per
+// block (plus the halo) and every output written once, fully coalesced along
+// channels.  Each row is unpacked once, into a window of the W most recent
+// rows; a block with no sequence start inside its window (nearly all of them)
+// takes a path with no per-tap boundary test.
 #include <cstdint>
 #include <cuda_bf16.h>
 
@@ -24,6 +27,7 @@ namespace {
 
 constexpr int kConvThreads = 128;
 constexpr int kConvTB = 8;   // tokens per thread
+constexpr int kConvMinBlocks = 4;  // resident CTAs per SM (fewer registers spill)
 
 template <typename T>
 struct Vec;
@@ -40,33 +44,32 @@ struct Vec<float> {
         *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
     }
 };
-// bf16: 4 channels (8 bytes) per thread, so that the block's rows, the taps
-// and the sums fit in few registers and more warps keep loads in flight
+// bf16: 8 channels (16 bytes) per thread
 template <>
 struct Vec<__nv_bfloat16> {
-    static constexpr int N = 4;
-    using Raw = uint2;
+    static constexpr int N = 8;
+    using Raw = uint4;
     __device__ static Raw load_raw(const __nv_bfloat16 *p) {
-        return *reinterpret_cast<const uint2 *>(p);
+        return *reinterpret_cast<const uint4 *>(p);
     }
-    __device__ static Raw zero_raw() { return make_uint2(0, 0); }
-    __device__ static void unpack(const Raw &x, float (&v)[4]) {
-        const uint32_t w[2] = {x.x, x.y};
+    __device__ static Raw zero_raw() { return make_uint4(0, 0, 0, 0); }
+    __device__ static void unpack(const Raw &x, float (&v)[8]) {
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 4; ++i) {
             v[2 * i] = __uint_as_float(w[i] << 16);
             v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
         }
     }
-    __device__ static void store(__nv_bfloat16 *p, const float (&v)[4]) {
-        uint2 x;
+    __device__ static void store(__nv_bfloat16 *p, const float (&v)[8]) {
+        uint4 x;
         uint32_t *w = &x.x;
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 4; ++i) {
             const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
             w[i] = *reinterpret_cast<const uint32_t *>(&h);
         }
-        *reinterpret_cast<uint2 *>(p) = x;
+        *reinterpret_cast<uint4 *>(p) = x;
     }
 };
 
@@ -88,7 +91,7 @@ __device__ __forceinline__ int32_t seq_of(const int32_t *cu, int32_t N, int32_t 
 }
 
 template <typename T, int W>
-__global__ void __launch_bounds__(kConvThreads)
+__global__ void __launch_bounds__(kConvThreads, kConvMinBlocks)
 short_conv_fwd_kernel(const T *__restrict__ x, const float *__restrict__ weight,
                       const float *__restrict__ bias, const int32_t *__restrict__ cu,
                       const T *__restrict__ cache_in, T *__restrict__ y, int32_t N, int32_t T_,
@@ -138,6 +141,27 @@ short_conv_fwd_kernel(const T *__restrict__ x, const float *__restrict__ weight,
     int32_t s = seq_of(cu, N, t_begin);
     int32_t start = cu ? min(max(cu[s], 0), T_) : 0;
     int32_t next = cu ? min(max(cu[s + 1], start), T_) : T_;
+    if (start <= t_begin - (W - 1) && next >= t_begin + kConvTB && t_begin + kConvTB <= T_) {
+        // one sequence covers the block and its halo: a sliding window of
+        // unpacked rows, no boundary tests
+        float win[W][V];
+#pragma unroll
+        for (int r = 0; r < W - 1; ++r) Vec<T>::unpack(raw[r], win[r]);
+#pragma unroll
+        for (int jt = 0; jt < kConvTB; ++jt) {
+            Vec<T>::unpack(raw[jt + W - 1], win[(jt + W - 1) % W]);
+            float z[V];
+#pragma unroll
+            for (int j = 0; j < V; ++j) {
+                float acc = bsum[j];
+#pragma unroll
+                for (int i = 0; i < W; ++i) acc = fmaf(w[j][i], win[(jt + i) % W][j], acc);
+                z[j] = act(acc, activation);
+            }
+            Vec<T>::store(y + (size_t)(t_begin + jt) * C + c0, z);
+        }
+        return;
+    }
 #pragma unroll
     for (int jt = 0; jt < kConvTB; ++jt) {
         const int32_t t = t_begin + jt;

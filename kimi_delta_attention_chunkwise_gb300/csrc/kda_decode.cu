@@ -14,10 +14,13 @@
 // strided by RG, so a warp's load of one row is fully coalesced (D = 128:
 // 32 lanes x 16 B = one 512 B row).  Column sums over rows go through warp
 // registers, then one shared-memory exchange across row groups.
+#include <algorithm>
+#include <climits>
 #include <cstdint>
 #include <cuda_bf16.h>
 
 #include "kda_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace kda {
 namespace {
@@ -191,8 +194,10 @@ cudaError_t launch_step_dtype(const StepArgs &a, cudaStream_t stream) {
 // Updates", sec. 5): one CTA per (sequence, head) holds the state in
 // registers across all of the sequence's tokens, so the state crosses HBM
 // once in each direction however many tokens the sequence has.  Each token
-// is the step above; its vectors are double-buffered in shared memory (three
-// barriers a token) and the next token's are loaded while this one runs.
+// is the step above, with one block barrier: the row groups' partial column
+// sums go through shared memory (double-buffered by token parity) and every
+// thread finishes the sums of its own columns.  Blocks of 8 tokens' vectors
+// are staged in shared memory, with k.q and the norms taken once per block.
 // The state lives in a pool of slots; state_indices picks each sequence's
 // slot (negative: the sequence is skipped).
 // ---------------------------------------------------------------------------
@@ -226,80 +231,144 @@ __device__ __forceinline__ void load_rows(const float *src, float (&dst)[ROWS]) 
     }
 }
 
+// Shared memory of the multi-token pass: the next item's state (bulk copy)
+// and a block of TB tokens' vectors, fp32 (alpha = exp(log_alpha) already
+// taken).
+template <int D>
+struct FwdSmem {
+    using Cfg = FwdCfg<D, kFwdThreads>;
+    float4 state[D * D / 4];
+    float k[Cfg::TB][D], q[Cfg::TB][D], v[Cfg::TB][D], alpha[Cfg::TB][D];
+    float red[2][2][Cfg::SLOTS][D];
+    float beta[Cfg::TB];
+    float kq[Cfg::TB], rk[Cfg::TB], rq[Cfg::TB];
+    uint64_t bar;
+    int32_t next;
+};
+constexpr long long kFwdWait = 2000000000LL;  // bounded wait on a state copy (SM clocks)
+
+// Persistent: CTA b takes the (sequence, head) items b, b + grid, ... that
+// have work, and while it runs one item's tokens the next item's state
+// streams into shared memory (one bulk copy), so the state load of one item
+// hides under the tokens of the one before.
 template <typename TIn, typename TOut, int D, bool PRO>
 __global__ void __launch_bounds__(FwdCfg<D, kFwdThreads>::THREADS)
 recurrent_fwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
                      const TIn *__restrict__ v, const float *__restrict__ log_alpha,
                      const float *__restrict__ beta, float scale, const int32_t *__restrict__ cu,
                      const int32_t *__restrict__ slots, int32_t num_slots, float *pool,
-                     TOut *__restrict__ out, int32_t T, int32_t H, int32_t G, int32_t pro,
-                     const float *__restrict__ gbias, const float *__restrict__ galog,
-                     int *status) {
+                     TOut *__restrict__ out, int32_t T, int32_t H, int32_t G, int32_t n_items,
+                     int32_t pro, const float *__restrict__ gbias,
+                     const float *__restrict__ galog, int *status) {
     using Cfg = FwdCfg<D, kFwdThreads>;
     constexpr int CG = Cfg::CG, ROWS = Cfg::ROWS, THREADS = Cfg::THREADS;
     constexpr int RG_PER_WARP = Cfg::RG_PER_WARP, SLOTS = Cfg::SLOTS, TB = Cfg::TB;
-    // a block of TB tokens' vectors, fp32 (alpha = exp(log_alpha) already taken)
-    __shared__ __align__(16) float s_k[TB][D];
-    __shared__ __align__(16) float s_q[TB][D];
-    __shared__ __align__(16) float s_v[TB][D];
-    __shared__ __align__(16) float s_alpha[TB][D];
-    __shared__ float s_beta[TB];
-    __shared__ __align__(16) float s_e[2][D];
-    __shared__ __align__(16) float s_red[2][2][SLOTS][D];
-    __shared__ float s_kq[2], s_rk[2], s_rq[2];
+    extern __shared__ __align__(128) uint8_t fwd_smem_raw[];
+    FwdSmem<D> &sm = *reinterpret_cast<FwdSmem<D> *>(fwd_smem_raw);
 
     const int tid = threadIdx.x;
     const int cg = tid % CG, rg = tid / CG, row0 = rg * ROWS;
-    const int32_t seq = blockIdx.x / H, h = blockIdx.x % H;
-    int32_t ta = 0, tb = T;
-    if (cu) {
-        ta = min(max(cu[seq], 0), T);
-        tb = min(max(cu[seq + 1], ta), T);
+    auto bounds = [&](int32_t seq, int32_t &ta, int32_t &tb) {
+        ta = 0;
+        tb = T;
+        if (cu) {
+            ta = min(max(cu[seq], 0), T);
+            tb = min(max(cu[seq + 1], ta), T);
+        }
+    };
+    // thread 0: the first item at or after `from` (in this CTA's stride) with
+    // work; skipped sequences (negative slot) and empty ones leave their
+    // state untouched, an out-of-range slot sets the status word
+    auto find = [&](int32_t from) -> int32_t {
+        for (int32_t it = from; it < n_items; it += (int32_t)gridDim.x) {
+            int32_t ta, tb;
+            bounds(it / H, ta, tb);
+            const int32_t slot = slots ? slots[it / H] : it / H;
+            if (slot < 0 || ta >= tb) continue;
+            if (slot >= num_slots) {
+                atomicExch(status, (int)KDA_ERR_INVALID_ARG);
+                continue;
+            }
+            return it;
+        }
+        return -1;
+    };
+    auto state_of = [&](int32_t it) {
+        const int32_t slot = slots ? slots[it / H] : it / H;
+        return reinterpret_cast<float4 *>(pool + ((size_t)slot * H + it % H) * D * D);
+    };
+    if (tid == 0) {
+        tc::mbar_init(&sm.bar, 1);
+        tc::fence_mbar_init();
+        const int32_t first = find((int32_t)blockIdx.x);
+        sm.next = first;
+        if (first >= 0) {
+            tc::mbar_arrive_expect_tx(&sm.bar, D * D * 4);
+            tc::bulk_g2s(sm.state, state_of(first), D * D * 4, &sm.bar);
+        }
     }
-    const int32_t slot = slots ? slots[seq] : seq;
-    if (slot < 0 || ta >= tb) return;  // skipped, or nothing to do: state untouched
-    if (slot >= num_slots) {
-        if (tid == 0) atomicExch(status, (int)KDA_ERR_INVALID_ARG);
-        return;
-    }
-    float4 *S = reinterpret_cast<float4 *>(pool + ((size_t)slot * H + h) * D * D);
-    float4 s[ROWS];
-#pragma unroll
-    for (int r = 0; r < ROWS; ++r) s[r] = __ldcs(S + (size_t)(row0 + r) * CG + cg);
-
+    __syncthreads();
+    int32_t item = sm.next;
+    uint32_t phase = 0;
     if (!PRO) pro = 0;
-    const float sens = (pro & KDA_PROLOGUE_GATE) ? __expf(galog[h]) : 0.f;
     const bool l2 = pro & KDA_PROLOGUE_L2NORM_QK;
-    int32_t n = 0;  // tokens done
-    for (int32_t t0 = ta; t0 < tb; t0 += TB) {
-        const int nt = min(TB, tb - t0);
-        __syncthreads();  // the previous block's vectors are no longer read
-        for (int idx = tid; idx < nt * D; idx += THREADS) {
-            const int i = idx / D, c = idx % D;
-            const size_t o = ((size_t)(t0 + i) * H + h) * D + c;
-            const size_t oq = ((size_t)(t0 + i) * (H / G) + h / G) * D + c;  // the group's q/k
-            s_k[i][c] = to_f32(k[oq]);
-            s_q[i][c] = to_f32(q[oq]);
-            s_v[i][c] = to_f32(v[o]);
-            float lg = log_alpha[o];
-            if (pro & KDA_PROLOGUE_GATE) lg = pro_gate(lg, sens, gbias[(size_t)h * D + c]);
-            s_alpha[i][c] = __expf(lg);
+    while (item >= 0) {
+        const int32_t seq = item / H, h = item % H;
+        int32_t ta, tb;
+        bounds(seq, ta, tb);
+        float4 *S = state_of(item);
+        const bool ok = tc::mbar_wait_bounded(&sm.bar, phase, kFwdWait);
+        phase ^= 1u;
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                atomicExch(status, (int)KDA_ERR_TIMEOUT);
+                (void)tc::mbar_wait_bounded(&sm.bar, phase ^ 1u, kFwdWait);
+            }
+            return;
         }
-        if (tid < nt) {
-            const float bt = beta[(size_t)(t0 + tid) * H + h];
-            s_beta[tid] = (pro & KDA_PROLOGUE_BETA_LOGITS) ? pro_sigmoid(bt) : bt;
+        float4 s[ROWS];
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) s[r] = sm.state[(row0 + r) * CG + cg];
+        __syncthreads();  // the state buffer is free: the next item's copy goes out
+        if (tid == 0) {
+            const int32_t nx = find(item + (int32_t)gridDim.x);
+            sm.next = nx;
+            if (nx >= 0) {
+                tc::mbar_arrive_expect_tx(&sm.bar, D * D * 4);
+                tc::bulk_g2s(sm.state, state_of(nx), D * D * 4, &sm.bar);
+            }
         }
-        __syncthreads();
-        for (int i = 0; i < nt; ++i, ++n) {
-            const int b = n & 1;
-            // k.q and, with the L2 prologue, the inverse norms (the row pass
-            // uses raw k and q; its sums are rescaled below)
-            if (tid < 32) {
+        const float sens = (pro & KDA_PROLOGUE_GATE) ? __expf(galog[h]) : 0.f;
+        int32_t n = 0;  // tokens done
+        for (int32_t t0 = ta; t0 < tb; t0 += TB) {
+            const int nt = min(TB, tb - t0);
+            __syncthreads();  // the previous block's vectors are no longer read
+            for (int idx = tid; idx < nt * D; idx += THREADS) {
+                const int i = idx / D, c = idx % D;
+                const size_t o = ((size_t)(t0 + i) * H + h) * D + c;
+                const size_t oq = ((size_t)(t0 + i) * (H / G) + h / G) * D + c;  // the group's q/k
+                sm.k[i][c] = to_f32(k[oq]);
+                sm.q[i][c] = to_f32(q[oq]);
+                sm.v[i][c] = to_f32(v[o]);
+                float lg = log_alpha[o];
+                if (pro & KDA_PROLOGUE_GATE) lg = pro_gate(lg, sens, gbias[(size_t)h * D + c]);
+                sm.alpha[i][c] = __expf(lg);
+            }
+            if (tid < nt) {
+                const float bt = beta[(size_t)(t0 + tid) * H + h];
+                sm.beta[tid] = (pro & KDA_PROLOGUE_BETA_LOGITS) ? pro_sigmoid(bt) : bt;
+            }
+            __syncthreads();
+            // per token of the block, one warp each: k.q and, with the L2
+            // prologue, the inverse norms (the row pass uses raw k and q; its
+            // sums are rescaled below)
+            for (int i = tid / 32; i < nt; i += THREADS / 32) {
+                const int lane = tid % 32;
                 float acc = 0.f, kk = 0.f, qq = 0.f;
-                for (int j = tid; j < D; j += 32) {
-                    acc += s_k[i][j] * s_q[i][j];
-                    kk += s_k[i][j] * s_k[i][j];
-                    qq += s_q[i][j] * s_q[i][j];
+                for (int j = lane; j < D; j += 32) {
+                    acc += sm.k[i][j] * sm.q[i][j];
+                    kk += sm.k[i][j] * sm.k[i][j];
+                    qq += sm.q[i][j] * sm.q[i][j];
                 }
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) {
@@ -307,88 +376,123 @@ recurrent_fwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
                     kk += __shfl_xor_sync(0xffffffffu, kk, o);
                     qq += __shfl_xor_sync(0xffffffffu, qq, o);
                 }
-                if (tid == 0) {
-                    const float rk = l2 ? rsqrtf(kk + kL2Eps) : 1.f;
-                    const float rq = l2 ? rsqrtf(qq + kL2Eps) : 1.f;
-                    s_rk[b] = rk;
-                    s_rq[b] = rq;
-                    s_kq[b] = acc * rk * rq;
+                if (lane == 0) {
+                    const float rki = l2 ? rsqrtf(kk + kL2Eps) : 1.f;
+                    const float rqi = l2 ? rsqrtf(qq + kL2Eps) : 1.f;
+                    sm.rk[i] = rki;
+                    sm.rq[i] = rqi;
+                    sm.kq[i] = acc * rki * rqi;
                 }
             }
-            // decay the rows; both column reductions in one pass
-            float ra[ROWS], rk[ROWS], rq[ROWS];
-            load_rows<ROWS>(&s_alpha[i][row0], ra);
-            load_rows<ROWS>(&s_k[i][row0], rk);
-            load_rows<ROWS>(&s_q[i][row0], rq);
-            float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
-            {
-                // packed pairs: the same IEEE operations, half the instructions
-                float2 k01 = make_float2(0.f, 0.f), k23 = k01, q01 = k01, q23 = k01;
+            __syncthreads();
+            for (int i = 0; i < nt; ++i, ++n) {
+                const int b = n & 1;
+                // decay the rows; both column reductions in one pass
+                float ra[ROWS], rk[ROWS], rq[ROWS];
+                load_rows<ROWS>(&sm.alpha[i][row0], ra);
+                load_rows<ROWS>(&sm.k[i][row0], rk);
+                load_rows<ROWS>(&sm.q[i][row0], rq);
+                float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
+                {
+                    // packed pairs: the same IEEE operations, half the instructions
+                    float2 k01 = make_float2(0.f, 0.f), k23 = k01, q01 = k01, q23 = k01;
+#pragma unroll
+                    for (int r = 0; r < ROWS; ++r) {
+                        const float2 a2 = make_float2(ra[r], ra[r]), k2 = make_float2(rk[r], rk[r]),
+                                     q2 = make_float2(rq[r], rq[r]);
+                        const float2 s01 = f2_mul(make_float2(s[r].x, s[r].y), a2);
+                        const float2 s23 = f2_mul(make_float2(s[r].z, s[r].w), a2);
+                        s[r] = make_float4(s01.x, s01.y, s23.x, s23.y);
+                        k01 = f2_fma(s01, k2, k01);
+                        k23 = f2_fma(s23, k2, k23);
+                        q01 = f2_fma(s01, q2, q01);
+                        q23 = f2_fma(s23, q2, q23);
+                    }
+                    pk = make_float4(k01.x, k01.y, k23.x, k23.y);
+                    pq = make_float4(q01.x, q01.y, q23.x, q23.y);
+                }
+#pragma unroll
+                for (int o = CG; o < 32; o <<= 1) {
+                    pk.x += __shfl_xor_sync(0xffffffffu, pk.x, o); pk.y += __shfl_xor_sync(0xffffffffu, pk.y, o);
+                    pk.z += __shfl_xor_sync(0xffffffffu, pk.z, o); pk.w += __shfl_xor_sync(0xffffffffu, pk.w, o);
+                    pq.x += __shfl_xor_sync(0xffffffffu, pq.x, o); pq.y += __shfl_xor_sync(0xffffffffu, pq.y, o);
+                    pq.z += __shfl_xor_sync(0xffffffffu, pq.z, o); pq.w += __shfl_xor_sync(0xffffffffu, pq.w, o);
+                }
+                if ((tid % 32) < CG || CG >= 32) {
+                    const int sl = rg / RG_PER_WARP;
+                    reinterpret_cast<float4 *>(sm.red[b][0][sl])[cg] = pk;
+                    reinterpret_cast<float4 *>(sm.red[b][1][sl])[cg] = pq;
+                }
+                __syncthreads();
+                // every thread finishes the column sums of its own 4 columns
+                // (the same sums in the same order in each row group), so no
+                // second barrier hands e around; row group 0 writes the output
+                float4 p4 = make_float4(0.f, 0.f, 0.f, 0.f), r4 = p4;
+#pragma unroll
+                for (int w = 0; w < SLOTS; ++w) {
+                    const float4 a4 = reinterpret_cast<const float4 *>(sm.red[b][0][w])[cg];
+                    const float4 c4 = reinterpret_cast<const float4 *>(sm.red[b][1][w])[cg];
+                    p4.x += a4.x; p4.y += a4.y; p4.z += a4.z; p4.w += a4.w;
+                    r4.x += c4.x; r4.y += c4.y; r4.z += c4.z; r4.w += c4.w;
+                }
+                const float4 v4 = reinterpret_cast<const float4 *>(sm.v[i])[cg];
+                const float bi = sm.beta[i], rki = sm.rk[i];
+                float4 e4;  // e = beta (v - S_bar^T k_hat), then the write k_hat e^T
+                e4.x = bi * (v4.x - rki * p4.x);
+                e4.y = bi * (v4.y - rki * p4.y);
+                e4.z = bi * (v4.z - rki * p4.z);
+                e4.w = bi * (v4.w - rki * p4.w);
+                if (rg == 0) {
+                    const float rqi = sm.rq[i], kqi = sm.kq[i];
+                    const float o4[4] = {scale * (rqi * r4.x + kqi * e4.x), scale * (rqi * r4.y + kqi * e4.y),
+                                         scale * (rqi * r4.z + kqi * e4.z), scale * (rqi * r4.w + kqi * e4.w)};
+                    TOut *dst = out + ((size_t)(t0 + i) * H + h) * D + cg * 4;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) dst[j] = from_f32<TOut>(o4[j]);
+                }
+                e4.x *= rki; e4.y *= rki; e4.z *= rki; e4.w *= rki;
+                // S_t = S_bar + k e^T
+                const float2 e01 = make_float2(e4.x, e4.y), e23 = make_float2(e4.z, e4.w);
 #pragma unroll
                 for (int r = 0; r < ROWS; ++r) {
-                    const float2 a2 = make_float2(ra[r], ra[r]), k2 = make_float2(rk[r], rk[r]),
-                                 q2 = make_float2(rq[r], rq[r]);
-                    const float2 s01 = f2_mul(make_float2(s[r].x, s[r].y), a2);
-                    const float2 s23 = f2_mul(make_float2(s[r].z, s[r].w), a2);
+                    const float2 k2 = make_float2(rk[r], rk[r]);
+                    const float2 s01 = f2_fma(k2, e01, make_float2(s[r].x, s[r].y));
+                    const float2 s23 = f2_fma(k2, e23, make_float2(s[r].z, s[r].w));
                     s[r] = make_float4(s01.x, s01.y, s23.x, s23.y);
-                    k01 = f2_fma(s01, k2, k01);
-                    k23 = f2_fma(s23, k2, k23);
-                    q01 = f2_fma(s01, q2, q01);
-                    q23 = f2_fma(s23, q2, q23);
                 }
-                pk = make_float4(k01.x, k01.y, k23.x, k23.y);
-                pq = make_float4(q01.x, q01.y, q23.x, q23.y);
-            }
-#pragma unroll
-            for (int o = CG; o < 32; o <<= 1) {
-                pk.x += __shfl_xor_sync(0xffffffffu, pk.x, o); pk.y += __shfl_xor_sync(0xffffffffu, pk.y, o);
-                pk.z += __shfl_xor_sync(0xffffffffu, pk.z, o); pk.w += __shfl_xor_sync(0xffffffffu, pk.w, o);
-                pq.x += __shfl_xor_sync(0xffffffffu, pq.x, o); pq.y += __shfl_xor_sync(0xffffffffu, pq.y, o);
-                pq.z += __shfl_xor_sync(0xffffffffu, pq.z, o); pq.w += __shfl_xor_sync(0xffffffffu, pq.w, o);
-            }
-            if ((tid % 32) < CG || CG >= 32) {
-                const int sl = rg / RG_PER_WARP;
-                reinterpret_cast<float4 *>(s_red[b][0][sl])[cg] = pk;
-                reinterpret_cast<float4 *>(s_red[b][1][sl])[cg] = pq;
-            }
-            __syncthreads();
-            if (tid < D) {
-                float p = 0.f, rqs = 0.f;
-#pragma unroll
-                for (int w = 0; w < SLOTS; ++w) { p += s_red[b][0][w][tid]; rqs += s_red[b][1][w][tid]; }
-                const float e = s_beta[i] * (s_v[i][tid] - s_rk[b] * p);
-                s_e[b][tid] = s_rk[b] * e;  // the write k_hat e^T, k_hat = k / |k|
-                out[((size_t)(t0 + i) * H + h) * D + tid] =
-                    from_f32<TOut>(scale * (s_rq[b] * rqs + s_kq[b] * e));
-            }
-            __syncthreads();
-            // S_t = S_bar + k e^T
-            const float4 e4 = reinterpret_cast<const float4 *>(s_e[b])[cg];
-            const float2 e01 = make_float2(e4.x, e4.y), e23 = make_float2(e4.z, e4.w);
-#pragma unroll
-            for (int r = 0; r < ROWS; ++r) {
-                const float2 k2 = make_float2(rk[r], rk[r]);
-                const float2 s01 = f2_fma(k2, e01, make_float2(s[r].x, s[r].y));
-                const float2 s23 = f2_fma(k2, e23, make_float2(s[r].z, s[r].w));
-                s[r] = make_float4(s01.x, s01.y, s23.x, s23.y);
             }
         }
-    }
 #pragma unroll
-    for (int r = 0; r < ROWS; ++r) __stcs(S + (size_t)(row0 + r) * CG + cg, s[r]);
+        for (int r = 0; r < ROWS; ++r) __stcs(S + (size_t)(row0 + r) * CG + cg, s[r]);
+        __syncthreads();  // every thread has read sm.next's update (written above)
+        item = sm.next;
+    }
 }
 
 template <typename TIn, typename TOut, int D>
 cudaError_t launch_fwd_t(const RecurArgs &a, cudaStream_t stream) {
     const int64_t NH = (int64_t)a.N * a.H;
     if (NH == 0 || a.T == 0) return cudaSuccess;
+    if (NH > INT32_MAX) return cudaErrorInvalidValue;
     auto kern = a.pro ? recurrent_fwd_kernel<TIn, TOut, D, true>
                       : recurrent_fwd_kernel<TIn, TOut, D, false>;
-    kern<<<(unsigned)NH, FwdCfg<D, kFwdThreads>::THREADS, 0, stream>>>(
+    constexpr int threads = FwdCfg<D, kFwdThreads>::THREADS;
+    const size_t smem = sizeof(FwdSmem<D>);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) !=
+            cudaSuccess)
+        return cudaErrorInvalidValue;
+    const int64_t grid = std::min<int64_t>(NH, (int64_t)std::max(1, sms * std::max(1, per_sm)));
+    kern<<<(unsigned)grid, threads, smem, stream>>>(
         static_cast<const TIn *>(a.q), static_cast<const TIn *>(a.k),
         static_cast<const TIn *>(a.v), a.log_alpha, a.beta, a.scale, a.cu_seqlens,
-        a.state_indices, a.num_slots, a.pool, static_cast<TOut *>(a.out), a.T, a.H, a.G, a.pro,
-        a.gbias, a.galog, a.status);
+        a.state_indices, a.num_slots, a.pool, static_cast<TOut *>(a.out), a.T, a.H, a.G,
+        (int32_t)NH, a.pro, a.gbias, a.galog, a.status);
     return cudaGetLastError();
 }
 
