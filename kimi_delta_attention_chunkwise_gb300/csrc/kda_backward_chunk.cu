@@ -22,6 +22,7 @@
 // Every product that carries a gradient is tf32 (fp32 range): f16 operands
 // lose gradients of training size to underflow.
 #include <cstdint>
+#include <cstring>
 
 #include <cuda_bf16.h>
 
@@ -55,11 +56,16 @@ __device__ __forceinline__ float f16_at(const uint8_t *panel, uint32_t row, uint
     return __half2float(*reinterpret_cast<const __half *>(panel + sw128_offset(row, col)));
 }
 
+// dO as TMA tiles of one head's [64 tokens x 128 channels] (bf16)
+struct AuxMaps {
+    CUtensorMap d;
+};
+
 __global__ void __launch_bounds__(256, 1)
-chunk_bwd_aux_kernel(const uint8_t *__restrict__ img_base, const int2 *__restrict__ chunk_tok,
-                     const __nv_bfloat16 *__restrict__ d_out, uint8_t *__restrict__ mt_img,
-                     float *__restrict__ x_tiles, float *__restrict__ glv, int32_t H,
-                     int *status) {
+chunk_bwd_aux_kernel(const __grid_constant__ AuxMaps maps, const uint8_t *__restrict__ img_base,
+                     const int2 *__restrict__ chunk_tok, int32_t has_d_out,
+                     uint8_t *__restrict__ mt_img, float *__restrict__ x_tiles,
+                     float *__restrict__ glv, int32_t H, int *status) {
     extern __shared__ uint8_t smem_raw[];
     AuxSmem &sm = *reinterpret_cast<AuxSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -71,36 +77,43 @@ chunk_bwd_aux_kernel(const uint8_t *__restrict__ img_base, const int2 *__restric
     const size_t item = (size_t)c * H + h;
     const uint8_t *img = img_base + item * A_IMG_STRIDE;
 
+    // the dO tile lands in the upper half of the Q'^T staging, which is
+    // written only after the tile has been read
+    uint8_t *dtile = sm.qt + 16384;
     if (tid == 0) {
         mbar_init(&sm.bar_in, 1);
         mbar_init(&sm.bar_mma, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(&sm.bar_in, 2 * 16384 + 2 * 8192 + AD * 4);
+        mbar_arrive_expect_tx(&sm.bar_in,
+                              2 * 16384 + 2 * 8192 + AD * 4 + (has_d_out ? AC * AD * 2 : 0));
         bulk_g2s(sm.mn, img + A_IMG_MN, 2 * 16384, &sm.bar_in);
         bulk_g2s(sm.q0, img + A_IMG_Q0, 8192, &sm.bar_in);
         bulk_g2s(sm.q1, img + A_IMG_Q1, 8192, &sm.bar_in);
         bulk_g2s(sm.gl, img + A_IMG_GB, AD * 4, &sm.bar_in);
+        if (has_d_out) tma_load_3d(dtile, &maps.d, 0, h, t0, &sm.bar_in);
     }
     if (warp == 0) {
         tmem_alloc(&sm.tmem, 128);
         tmem_relinquish();
-    }
-    // dO^T (B operand): element (n, i) = dO[t0 + i][h][n], rows i >= L zero.
-    // Thread -> column n = tid % 128, tokens i = tid / 128, +2, ...
-    {
-        const int n = tid & 127;
-        for (int i = tid >> 7; i < AC; i += 2) {
-            const float x = (d_out && i < L)
-                                ? __bfloat162float(d_out[((size_t)(t0 + i) * H + h) * AD + n])
-                                : 0.f;
-            *reinterpret_cast<float *>(sm.dt + (i >> 5) * 16384u + sw128_offset_f32(n, i & 31)) = x;
-        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem;
     bool ok = mbar_wait_bounded(&sm.bar_in, 0, kAWait);
+    // dO^T (B operand): element (n, i) = dO[t0 + i][h][n], rows i >= L zero.
+    // Thread -> column n = tid % 128, tokens i = tid / 128, +2, ...
+    {
+        const int n = tid & 127;
+        const unsigned short *tile = reinterpret_cast<const unsigned short *>(dtile);
+#pragma unroll 8
+        for (int i = tid >> 7; i < AC; i += 2) {
+            const float x =
+                (has_d_out && i < L) ? __uint_as_float((uint32_t)tile[i * AD + n] << 16) : 0.f;
+            *reinterpret_cast<float *>(sm.dt + (i >> 5) * 16384u + sw128_offset_f32(n, i & 31)) = x;
+        }
+    }
+    __syncthreads();  // the tile is read: Q'^T may overwrite it
     if (ok) {
         if (tid < 128) {
             // -M'^T row i = column i of -M': (-M')[j][i] at panel i/64, row j
@@ -344,8 +357,12 @@ chunk_rscan_kernel(const uint8_t *__restrict__ mt_img, const float *__restrict__
                         break;
                     }
                     if (ds_img) {
-                        bulk_s2g(ds_img + (item_of(n) * RNT + vt) * (size_t)DS_IMG,
-                                 sm.sb[n & 1], DS_IMG);
+                        // as rows 32 vt .. of the item's four 128-row panels
+                        uint8_t *dst = ds_img + item_of(n) * (size_t)(RNT * DS_IMG) +
+                                       (size_t)vt * (DS_IMG / 4);
+                        for (int p = 0; p < 4; ++p)
+                            bulk_s2g(dst + (size_t)p * (RNT * DS_IMG / 4),
+                                     sm.sb[n & 1] + p * (DS_IMG / 4), DS_IMG / 4);
                         bulk_commit_group();
                         bulk_wait_group_read<0>();
                     }
@@ -357,17 +374,19 @@ chunk_rscan_kernel(const uint8_t *__restrict__ mt_img, const float *__restrict__
         } else {
             // -------- compute: thread = key row k --------
             const int k = tid;
-            auto put_state = [&](int32_t n) {
-                if (ds_nat) {
-                    // row k of panel vt of the K-major (value-contiguous) image:
-                    // the exact fp32 values, 128-byte swizzled
-                    uint8_t *dst = ds_nat + item_of(n) * (size_t)(RD * RD * 4) +
-                                   (size_t)vt * (RD * 128);
+            // dS_{c+1} of step n out as row k of panel vt of the K-major
+            // (value-contiguous) image: the exact fp32 values, 128-byte
+            // swizzled.  Issued while the step's product runs: before the
+            // operand's proxy fence these stores would hold the fence up.
+            auto put_global = [&](int32_t n) {
+                if (!ds_nat) return;
+                uint8_t *dst = ds_nat + item_of(n) * (size_t)(RD * RD * 4) + (size_t)vt * (RD * 128);
 #pragma unroll
-                    for (int j = 0; j < RBV; j += 4)
-                        *reinterpret_cast<float4 *>(dst + sw128_chunk(k, j >> 2)) =
-                            make_float4(dS[j], dS[j + 1], dS[j + 2], dS[j + 3]);
-                }
+                for (int j = 0; j < RBV; j += 4)
+                    *reinterpret_cast<float4 *>(dst + sw128_chunk(k, j >> 2)) =
+                        make_float4(dS[j], dS[j + 1], dS[j + 2], dS[j + 3]);
+            };
+            auto put_state = [&](int32_t n) {
                 uint8_t *img = sm.sb[n & 1] + (k >> 5) * 4096u;
 #pragma unroll
                 for (int j = 0; j < RBV; ++j)
@@ -381,6 +400,7 @@ chunk_rscan_kernel(const uint8_t *__restrict__ mt_img, const float *__restrict__
                 tc_fence_before();
                 mbar_arrive(&sm.ready_s);
                 mbar_arrive(&sm.ready_w[n & 1]);
+                put_global(n);
                 const int stg = n % RSTAGE;
                 if (!mbar_wait_bounded(&sm.full[stg], (uint32_t)(n / RSTAGE) & 1u, kRWait))
                     sm.abort_flag = 1;
@@ -513,8 +533,13 @@ cudaError_t launch_chunk_bwd(const BwdArgs &a, int *status, cudaStream_t stream)
         e = cudaFuncSetAttribute(chunk_rscan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kRSmem);
     if (e != cudaSuccess) return e;
+    AuxMaps amaps;
+    memset(&amaps, 0, sizeof(amaps));
+    if (a.d_out &&
+        !encode_tile_map(&amaps.d, a.d_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H))
+        return cudaErrorInvalidValue;
     chunk_bwd_aux_kernel<<<(unsigned)items, 256, kAuxSmem, stream>>>(
-        view.img, view.chunk_tok, static_cast<const __nv_bfloat16 *>(a.d_out), ws + L.mt,
+        amaps, view.img, view.chunk_tok, a.d_out != nullptr ? 1 : 0, ws + L.mt,
         reinterpret_cast<float *>(ws + L.x), reinterpret_cast<float *>(ws + L.gl), a.H, status);
     // 3. the reverse scan
     chunk_rscan_kernel<<<dim3((unsigned)(a.N * RNT), (unsigned)a.H), kRThreads, kRSmem, stream>>>(

@@ -89,6 +89,13 @@ __device__ __forceinline__ void row32_tf32(uint8_t *panel, int row, const float 
             make_float4(tf32_operand(v[4 * c]), tf32_operand(v[4 * c + 1]),
                         tf32_operand(v[4 * c + 2]), tf32_operand(v[4 * c + 3]));
 }
+// The same without the rounding (values that are tf32 operands already)
+__device__ __forceinline__ void row32_raw(uint8_t *panel, int row, const float (&v)[32]) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4 *>(panel + sw128_chunk(row, c)) =
+            make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+}
 // 64 consecutive K values (two arrays of 32) of one row of a K-major f16 panel
 __device__ __forceinline__ void row64_f16(uint8_t *panel, int row, const float (&v0)[32],
                                           const float (&v1)[32]) {
@@ -146,13 +153,13 @@ struct GradMaps {
 };
 
 // Per-item image block that G1 writes and G2 bulk-copies (tf32 operands,
-// rounded): dE (rows i, K = v; 4 x 8 KB), dE^T (rows v, K = i; 2 x 16 KB),
-// dW and dW^T likewise, s dA^qk (rows i, K = j; 2 x 8 KB) and its transpose
-// (rows j, K = i; 2 x 8 KB); then s dA^qk as exact fp32 rows [64][64] for the
-// direct-exponent path (its column sums telescope in dlog_alpha, which
-// magnifies any rounding of it).
-constexpr uint32_t IM_DE = 0, IM_DET = 32768, IM_DW = 65536, IM_DWT = 98304, IM_AQ = 131072,
-                   IM_AQT = 147456, IM_AQX = 163840;
+// rounded), in the orientation whose rows a warp writes whole (128 bytes per
+// store instruction): dE (rows i, K = v; 4 x 8 KB), dW (rows i, K = a),
+// s dA^qk (rows i, K = j; 2 x 8 KB); then s dA^qk as exact fp32 rows
+// [64][64] for the direct-exponent path (its column sums telescope in
+// dlog_alpha, which magnifies any rounding of it).  G2 transposes in shared
+// memory what it needs the other way round.
+constexpr uint32_t IM_DE = 0, IM_DW = 32768, IM_AQ = 65536, IM_AQX = 81920;
 static_assert(IM_AQX + 16384 == kGradImgBytes, "image block");
 
 // ---------------------------------------------------------------------------
@@ -221,13 +228,10 @@ chunk_grad_g1_kernel(const __grid_constant__ GradMaps maps, const ChunkGradArgs 
         if (has_do) tma_load_3d(ar + G1_TD, &maps.d, 0, h, t0, &sm.bar_in);
         mbar_arrive_expect_tx(&sm.bar_ld, kBwdAuxBytes + 4 * U16);
         bulk_g2s(ar + G1_AQ, a.aux + item * kBwdAuxBytes, kBwdAuxBytes, &sm.bar_ld);
-        // dS^T as four 128-row panels (K = 32 key channels each) from the
-        // reverse scan's tiles of 32 value rows
+        // dS^T: four 128-row panels (K = 32 key channels each), which the
+        // reverse scan writes in this layout
         const uint8_t *dt = a.ds_t + item * (4 * U16);
-        for (int vt = 0; vt < 4; ++vt)
-            for (int p = 0; p < 4; ++p)
-                bulk_g2s(ar + G1_DST + p * U16 + vt * 4096, dt + vt * U16 + p * 4096, 4096,
-                         &sm.bar_ld);
+        for (int p = 0; p < 4; ++p) bulk_g2s(ar + G1_DST + p * U16, dt + p * U16, U16, &sm.bar_ld);
         // the later loads to L2 now
         bulk_prefetch_l2(a.sst + item * (2 * U16), 2 * U16);
         bulk_prefetch_l2(a.ds_n + item * (4 * U16), 4 * U16);
@@ -351,7 +355,6 @@ chunk_grad_g1_kernel(const __grid_constant__ GradMaps maps, const ChunkGradArgs 
             f32_at(gde, i, ch & 31) = x;
             f32_at(ode, i, ch & 31) = bfv(in.xp, ii);
         }
-        row32_tf32(img + IM_DET + hf * U16, ch, e);
     }
     ok = ok && mbar_wait_bounded(&sm.bar_sf, 0, kGradWait);
     {
@@ -479,7 +482,6 @@ chunk_grad_g1_kernel(const __grid_constant__ GradMaps maps, const ChunkGradArgs 
             f32_at(gaq, i, ch & 31) = tf32_operand(x[ii]);
             gax[i * GC] = x[ii];
         }
-        row32_tf32(img + IM_AQT + hf * P8, ch, x);
     }
     {
         // dW = -(-dW^T)^T: G2's dW and dW^T images
@@ -492,7 +494,6 @@ chunk_grad_g1_kernel(const __grid_constant__ GradMaps maps, const ChunkGradArgs 
             w[ii] = -w[ii];
             f32_at(gdw, i0 + ii, ch & 31) = tf32_operand(w[ii]);
         }
-        row32_tf32(img + IM_DWT + hf * U16, ch, w);
     }
     float dqh[32], dke[32];
     if (ok) {
@@ -555,12 +556,12 @@ chunk_grad_g1_kernel(const __grid_constant__ GradMaps maps, const ChunkGradArgs 
 // G2: the C x C products, the decayed products' gradients, the outputs
 // ---------------------------------------------------------------------------
 // Shared arena (16 KB units; 13.5 of them):
-//   step 0: dE (rows i, K = v) u0-1, dW (rows i, K = a) u2-3, dE^T (rows v,
-//           K = i) u8-9, dW^T (rows a, K = i) u10-11 (bulk, from G1); the g
-//           tile u4-5, k and v tiles u6-7, q tile u12 (read into registers);
-//           A^kk f16 at u13 (8 KB)
-//   step 1: + B1 (rows j, K = v) u4-5 | B2 (rows j, K = a) u6-7 | A^T-rows
-//           (rows j, K = i) u12
+//   step 0: dE (rows i, K = v) u0-1, dW (rows i, K = a) u2-3 (bulk, from
+//           G1); the g tile u4-5, k and v tiles u6-7, q tile u12 (read into
+//           registers); A^kk f16 at u13 (8 KB)
+//   step 1: + B1 (rows j, K = v) u4-5 | B2 (rows j, K = a) u6-7 | dE^T
+//           (rows v, K = i) u8-9 | dW^T (rows a, K = i) u10-11 | A^T-rows
+//           (rows j, K = i) u12 (the transposed ones copied in shared memory)
 //   step 2: K_hat^T (rows a, K = j) u0-1 | [Q_tilde^T | K_tilde^T] u2-5 |
 //           dA^T-rows (rows m, K = i) at 96 KB | A (rows n, K = m) at 120 KB |
 //           s dA^qk^T-rows (rows j, K = i) at 136 KB | s dA^qk in rows 64..127
@@ -620,11 +621,9 @@ chunk_grad_g2_kernel(const __grid_constant__ GradMaps maps, const ChunkGradArgs 
         tma_load_3d(ar + G2_TK, &maps.k, 0, h, t0, &sm.bar_in);
         tma_load_3d(ar + G2_TV, &maps.v, 0, h, t0, &sm.bar_in);
         tma_load_3d(ar + G2_TQ, &maps.q, 0, h, t0, &sm.bar_in);
-        mbar_arrive_expect_tx(&sm.bar_ld, 4 * 32768 + 8192);
+        mbar_arrive_expect_tx(&sm.bar_ld, 2 * 32768 + 8192);
         bulk_g2s(ar + G2_DE, img + IM_DE, 32768, &sm.bar_ld);
         bulk_g2s(ar + G2_DW, img + IM_DW, 32768, &sm.bar_ld);
-        bulk_g2s(ar + G2_DET, img + IM_DET, 32768, &sm.bar_ld);
-        bulk_g2s(ar + G2_DWT, img + IM_DWT, 32768, &sm.bar_ld);
         bulk_g2s(ar + G2_AF, a.aux + item * kBwdAuxBytes, 8192, &sm.bar_ld);
         bulk_prefetch_l2(img + IM_AQ, 32768);
     }
@@ -673,6 +672,18 @@ chunk_grad_g2_kernel(const __grid_constant__ GradMaps maps, const ChunkGradArgs 
     }
     ok = mbar_wait_bounded(&sm.bar_ld, 0, kGradWait) && ok;
     {
+        // dE^T and dW^T (rows v / a, K = i) from dE and dW (rows i)
+        float xe[32], xw[32];
+        uint8_t *de = ar + G2_DE + (ch >> 5) * P8, *dw = ar + G2_DW + (ch >> 5) * P8;
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) {
+            xe[ii] = f32_at(de, i0 + ii, ch & 31);
+            xw[ii] = f32_at(dw, i0 + ii, ch & 31);
+        }
+        row32_raw(ar + G2_DET + hf * U16, ch, xe);
+        row32_raw(ar + G2_DWT + hf * U16, ch, xw);
+    }
+    {
         // A^T-rows: row j holds A[i][j] over i
         const int j = tid & 63, ib = (tid >> 6) * 16;
         const uint8_t *af = ar + G2_AF;
@@ -701,10 +712,9 @@ chunk_grad_g2_kernel(const __grid_constant__ GradMaps maps, const ChunkGradArgs 
     if (tid == 0 && ok) {
         if (!direct) {
             // s dA^qk in rows 64..127 of [dR ; s dA^qk] and as its transposed rows
-            mbar_arrive_expect_tx(&sm.bar_aq, 32768);
+            mbar_arrive_expect_tx(&sm.bar_aq, 16384);
             bulk_g2s(ar + G2_DRQ + 8192, img + IM_AQ, 8192, &sm.bar_aq);
             bulk_g2s(ar + G2_DRQ + U16 + 8192, img + IM_AQ + 8192, 8192, &sm.bar_aq);
-            bulk_g2s(ar + G2_AQT, img + IM_AQT, 16384, &sm.bar_aq);
         } else {
             // the exact fp32 rows, where [dR ; s dA^qk] would be
             mbar_arrive_expect_tx(&sm.bar_aq, 16384);
@@ -825,6 +835,14 @@ chunk_grad_g2_kernel(const __grid_constant__ GradMaps maps, const ChunkGradArgs 
         }
     }
     ok = ok && mbar_wait_bounded(&sm.bar_aq, 0, kGradWait);
+    if (!direct) {
+        // s dA^qk^T-rows (rows j, K = i) from rows 64.. of [dR ; s dA^qk]
+        const int j = tid & 63, ib = (tid >> 6) * 16;
+        uint8_t *src = ar + G2_DRQ + (j >> 5) * U16;
+        uint8_t *dst = ar + G2_AQT + (ib >> 5) * P8;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) f32_at(dst, j, (ib + e) & 31) = f32_at(src, 64 + ib + e, j & 31);
+    }
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();

@@ -129,7 +129,7 @@ struct ChunkGradArgs {
                                   // gradients as the second's operand images)
     int *status;
 };
-constexpr uint32_t kGradImgBytes = 176 * 1024;
+constexpr uint32_t kGradImgBytes = 96 * 1024;
 cudaError_t launch_chunk_grad(const ChunkGradArgs &a, cudaStream_t stream);
 
 // The fused input prologue, as each kernel applies it to one element.
