@@ -339,20 +339,20 @@ chunk_grad_g1_kernel(const __grid_constant__ GradMaps maps, const ChunkGradArgs 
     ok = ok && mbar_wait_bounded(&sm.bar_m[1], 0, kGradWait);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
+    // dE^T: lane = value channel v, tokens of this half.  Into rows 64.. of
+    // [dO ; dE] (dO into rows 0..63), and out as G2's dE image once the next
+    // products are issued (plain global stores ahead of the operands' proxy
+    // fence would hold the fence up)
+    float e[32];
     {
-        // dE^T: lane = value channel v, tokens of this half.  Into rows 64..
-        // of [dO ; dE] (dO into rows 0..63), and out as G2's dE and dE^T images
-        float e[32];
         if (ok) tmem_ld32(tmem_addr(tmem, quad * 32, 256 + hf * 32), e);
         else zero32(e);
         uint8_t *ode = ar + G1_ODE + (ch >> 5) * U16;
-        uint8_t *gde = img + IM_DE + (ch >> 5) * P8;
 #pragma unroll
         for (int ii = 0; ii < 32; ++ii) {
             const int i = i0 + ii;
-            const float x = tf32_operand(e[ii]);
-            f32_at(ode, 64 + i, ch & 31) = x;
-            f32_at(gde, i, ch & 31) = x;
+            e[ii] = tf32_operand(e[ii]);
+            f32_at(ode, 64 + i, ch & 31) = e[ii];
             f32_at(ode, i, ch & 31) = bfv(in.xp, ii);
         }
     }
@@ -395,6 +395,11 @@ chunk_grad_g1_kernel(const __grid_constant__ GradMaps maps, const ChunkGradArgs 
                          smem_u32(ar + G1_ODE + 2 * U16), U16, 8, idesc_tf32_f32(128, 128),
                          true);
         mma_commit(&sm.bar_m[2]);
+    }
+    {
+        uint8_t *gde = img + IM_DE + (ch >> 5) * P8;
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) f32_at(gde, i0 + ii, ch & 31) = e[ii];
     }
 
     // ---- step 3: E (rows j) and dS (rows a) ----
