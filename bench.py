@@ -228,6 +228,11 @@ PROFILE_FILES = {
     "recurrent_fwd": ("recurrent_fwd_decode_256x32x8_d128.md", None),
     "short_conv_fwd": ("short_conv_fwd_prefill_C12288_T4096.md", None),
     "recurrent_bwd": ("recurrent_bwd_prefill_T4096_H16.md", None),
+    # the chunk-form backward's own kernels, captured on its benchmark workload
+    "chunk_bwd_aux": ("chunk_bwd_aux_T4096_H16.md", None),
+    "chunk_rscan": ("chunk_rscan_T4096_H16.md", None),
+    "chunk_grad_g1": ("chunk_grad_g1_T4096_H16.md", None),
+    "chunk_grad_g2": ("chunk_grad_g2_T4096_H16.md", None),
 }
 
 
@@ -1008,6 +1013,11 @@ def run_backward(args, dist, peaks, dev, stream, w, dev_inputs):
         return dist.max(evs[0].elapsed_time(evs[1])) / reps
 
     ms_chunk = timed(lambda: kda.kda_chunk_bwd(q, k, v, la, beta, w.scale, None, cu, do, dsf))
+    # DRAM bytes of one call: its kernels' ncu captures on this workload (the
+    # forward recompute's prep and scan from the prefill capture)
+    parts = [profiled_traffic(k_) for k_ in ("prep", "scan", "chunk_bwd_aux", "chunk_rscan",
+                                            "chunk_grad_g1", "chunk_grad_g2")]
+    traffic = sum(parts) if all(p_ is not None for p_ in parts) else None
     ms_rec = timed(lambda: kda.kda_recurrent_bwd(q, k, v, la, beta, w.scale, None, cu, do, dsf))
     units = T * H
     bytes_call = BWD_BYTES_PER_UNIT * units + H * d * d * 4
@@ -1025,7 +1035,8 @@ def run_backward(args, dist, peaks, dev, stream, w, dev_inputs):
                          "tensor_frac": tfl / peaks["bf16_tflops"],
                          "bytes_per_launch": bytes_call,
                          "flops_per_unit": BWD_FLOPS_PER_UNIT, "peak_source": peaks["source"],
-                         "traffic": None,
+                         "traffic": traffic,
+                         "traffic_note": "sum of the DRAM bytes of its kernels' ncu captures",
                          "note": "eight launches (forward recompute, X_c, reverse scan, two "
                                  "gradient kernels); per-kernel shares in profiles/"},
             "recurrent_form": {"ms_per_step": ms_rec, "value": T * dist.world / (ms_rec / 1e3),
