@@ -503,8 +503,9 @@ kdaStatus_t kda_recurrent_bwd(const void *q, const void *k, const void *v,
  * direct exponents for the decayed products.  Arguments, layouts and outputs
  * as for kda_recurrent_bwd; q, k, v and log_alpha must be 16-byte aligned.
  * Scratch (the forward engine's images and states, the per-chunk factors,
- * state gradients and intermediate gradients: about (T / 64 + N + 1) * H *
- * 540 KB) is taken with cudaMallocAsync / cudaFreeAsync on `stream`.
+ * the state gradients at every chunk boundary and the first gradient
+ * kernel's operand images for the second: about (T / 64 + N + 1) * H *
+ * 480 KB) is taken with cudaMallocAsync / cudaFreeAsync on `stream`.
  */
 kdaStatus_t kda_chunk_bwd(const void *q, const void *k, const void *v,
                           const float *log_alpha, const float *beta, float scale,
