@@ -922,83 +922,104 @@ chunk_grad_g2_kernel(const __grid_constant__ GradMaps maps, const ChunkGradArgs 
     }
 
     // ---- epilogue: thread = channel ch (key, and value for dv), its tokens ----
+    // dG per (token, channel) in shared memory for dlog_alpha's reverse sums;
+    // dbeta's channel sums reduced across each warp's 32 channels first
     float *dgs = reinterpret_cast<float *>(ar + G2_DGS);
-    float *ps = reinterpret_cast<float *>(ar + G2_PS);
+    float *pbs = reinterpret_cast<float *>(ar + G2_PS);  // [4 warp quadrants][64 tokens]
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
-        const int c0 = hf * 32 + g * 16;  // token / column offset of this group
-        float y[16], dkv[16], dgv[16], pv[16], ep[16];
+    for (int g = 0; g < 4; ++g) {
+        const int c0 = hf * 32 + g * 8;  // token / column offset of this group
+        // dB2^T, dB1^T, XR, XQ, YY for the group's 8 tokens: one wait
+        float y[5][8];
+        const uint32_t tl = tmem_addr(tmem, quad * 32, c0);
+        const uint32_t cols[5] = {tl + 128, tl + 64, tl + 320, tl + 384, tl + 448};
+        if (ok) {
+            tmem_ld8x5(cols, y);
+        } else {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const int ii = g * 16 + e;
-            ep[e] = direct ? 1.f : exp2_approx(in.G[ii] - Gm);
+            for (int k = 0; k < 5; ++k)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[k][e] = 0.f;
         }
-        // dB2: B2 = Diag(beta)(exp(G) * K)
-        if (ok) tmem_ld16(tmem_addr(tmem, quad * 32, 128 + c0), y);
+        float pv[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const int ii = g * 16 + e, i = c0 + e;
-            const float yv = ok ? y[e] : 0.f;
-            const float b = sm.beta[i], gam = exp2_approx(in.G[ii]), kv = bfv(in.kp, ii);
-            dkv[e] = b * gam * yv;
-            dgv[e] = b * gam * kv * yv;
-            pv[e] = gam * kv * yv;
-        }
-        // dB1: B1 = Diag(beta) V (lane = value channel)
-        if (ok) tmem_ld16(tmem_addr(tmem, quad * 32, 64 + c0), y);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const int ii = g * 16 + e, i = c0 + e;
-            const float yv = ok ? y[e] : 0.f;
-            pv[e] = fmaf(bfv(in.vp, ii), yv, pv[e]);
-            if (i < L) a.dv[base + (size_t)i * rs] = sm.beta[i] * yv;
-        }
-        // XR (rows of R)
-        if (ok) tmem_ld16(tmem_addr(tmem, quad * 32, 320 + c0), y);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const int ii = g * 16 + e, i = c0 + e;
-            const float xr = ok ? ep[e] * y[e] : 0.f, kv = bfv(in.kp, ii), b = sm.beta[i];
-            dkv[e] = fmaf(b, xr, dkv[e]);
-            dgv[e] = fmaf(b * kv, xr, dgv[e]);
-            pv[e] = fmaf(kv, xr, pv[e]);
-        }
-        // XQ (rows of A^qk)
-        if (ok) tmem_ld16(tmem_addr(tmem, quad * 32, 384 + c0), y);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const int ii = g * 16 + e, i = c0 + e;
-            const float xq = ok ? ep[e] * y[e] : 0.f;
-            dgv[e] = fmaf(bfv(in.xp, ii), xq, dgv[e]);
-            if (i < L) atomicAdd(a.dq + base + (size_t)i * rs, xq);
-        }
-        // YY (columns of R and A^qk)
-        if (ok) tmem_ld16(tmem_addr(tmem, quad * 32, 448 + c0), y);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const int ii = g * 16 + e, i = c0 + e;
+        for (int e = 0; e < 8; ++e) {
+            const int ii = g * 8 + e, i = c0 + e;
+            const float b = sm.beta[i], gam = exp2_approx(in.G[ii]);
+            const float kv = bfv(in.kp, ii);
+            const float ep = direct ? 1.f : exp2_approx(in.G[ii] - Gm);
             const float en = direct ? 1.f : exp2_approx(Gm - in.G[ii]);
-            const float yy = ok ? en * y[e] : 0.f, kv = bfv(in.kp, ii);
-            dkv[e] += yy;
-            dgv[e] = fmaf(-kv, yy, dgv[e]);
-            if (i < L) atomicAdd(a.dk + base + (size_t)i * rs, dkv[e]);
-            dgs[i * GD + ch] = dgv[e];
-            ps[i * kPS + ch] = pv[e];
+            // dB2 (B2 = Diag(beta)(exp(G) * K)), dB1 (B1 = Diag(beta) V, lane =
+            // value channel), XR (rows of R), XQ (rows of A^qk), YY (columns of
+            // R and A^qk)
+            const float d2 = y[0][e], d1 = y[1][e], xr = ep * y[2][e], xq = ep * y[3][e],
+                        yy = en * y[4][e];
+            const float dkv = b * gam * d2 + b * xr + yy;
+            float dgv = b * gam * kv * d2;
+            dgv = fmaf(b * kv, xr, dgv);
+            dgv = fmaf(bfv(in.xp, ii), xq, dgv);
+            dgv = fmaf(-kv, yy, dgv);
+            pv[e] = gam * kv * d2 + bfv(in.vp, ii) * d1 + kv * xr;
+            if (i < L) {
+                const size_t r = base + (size_t)i * rs;
+                a.dv[r] = b * d1;
+                atomicAdd(a.dq + r, xq);
+                atomicAdd(a.dk + r, dkv);
+            }
+            dgs[i * GD + ch] = dgv;
         }
+        // sum pv over the warp's 32 channels: halve the token set at each
+        // exchange, then finish on one value; lane l ends with token
+        // 4 (l>>4 & 1) + 2 (l>>3 & 1) + (l>>2 & 1) of the group
+        const int lane = tid & 31;
+        float w4[4], w2[2];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const bool up = lane & 16;
+            const float send = up ? pv[k] : pv[k + 4];
+            w4[k] = (up ? pv[k + 4] : pv[k]) + __shfl_xor_sync(0xffffffffu, send, 16);
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const bool up = lane & 8;
+            const float send = up ? w4[k] : w4[k + 2];
+            w2[k] = (up ? w4[k + 2] : w4[k]) + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+        float z;
+        {
+            const bool up = lane & 4;
+            z = (up ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, up ? w2[0] : w2[1], 4);
+        }
+        z += __shfl_xor_sync(0xffffffffu, z, 2);
+        z += __shfl_xor_sync(0xffffffffu, z, 1);
+        if ((lane & 3) == 0)
+            pbs[quad * GC + c0 + ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 +
+                ((lane >> 2) & 1)] = z;
     }
     __syncthreads();
-    if (tid < GD) {
-        // this kernel's share of dlog_alpha: the reverse cumulative sum of its dG
+    {
+        // this kernel's share of dlog_alpha: the reverse cumulative sum of its
+        // dG, over each token half, then the second half's total onto the first
+        float dg[32];
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) dg[ii] = dgs[(i0 + ii) * GD + ch];
         float acc = 0.f;
-        for (int i = GC - 1; i >= 0; --i) {
-            acc += dgs[i * GD + tid];
-            if (i < L) atomicAdd(a.dlog_alpha + ((size_t)(t0 + i) * H + h) * GD + tid, acc);
+#pragma unroll
+        for (int ii = 31; ii >= 0; --ii) {
+            acc += dg[ii];
+            dg[ii] = acc;
         }
-    } else if (tid < GD + GC) {
-        const int i = tid - GD;
-        float acc = 0.f;
-        for (int cc = 0; cc < GD; ++cc) acc += ps[i * kPS + cc];
-        if (i < L) a.dbeta[(size_t)(t0 + i) * H + h] = acc;
+        if (hf == 1) sm.gcarry[ch] = acc;  // the carries are read out: reuse
+        if (tid >= GD && tid < GD + GC) {
+            const int i = tid - GD;
+            const float db = pbs[i] + pbs[GC + i] + pbs[2 * GC + i] + pbs[3 * GC + i];
+            if (i < L) a.dbeta[(size_t)(t0 + i) * H + h] = db;
+        }
+        __syncthreads();
+        const float add = hf == 0 ? sm.gcarry[ch] : 0.f;
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii)
+            if (i0 + ii < L) atomicAdd(a.dlog_alpha + base + (size_t)(i0 + ii) * rs, dg[ii] + add);
     }
     const bool bad = __syncthreads_or(!ok);
     if (bad && tid == 0) {

@@ -392,6 +392,22 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Five loads of 8 consecutive columns each (any addresses), one wait.
+__device__ __forceinline__ void tmem_ld8x5(const uint32_t (&ta)[5], float (&v)[5][8]) {
+    uint32_t r[5][8];
+#pragma unroll
+    for (int k = 0; k < 5; ++k)
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(r[k][0]), "=r"(r[k][1]), "=r"(r[k][2]), "=r"(r[k][3]),
+                       "=r"(r[k][4]), "=r"(r[k][5]), "=r"(r[k][6]), "=r"(r[k][7])
+                     : "r"(ta[k]));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int k = 0; k < 5; ++k)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[k][i] = __uint_as_float(r[k][i]);
+}
+
 // registers -> TMEM: 32 lanes x 32-bit, 32 consecutive columns per thread
 // (each warp writes its own 32-lane quadrant), then wait for the store.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
