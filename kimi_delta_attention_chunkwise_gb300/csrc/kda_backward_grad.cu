@@ -155,9 +155,9 @@ struct GradMaps {
 // Per-item image block that G1 writes and G2 bulk-copies (tf32 operands,
 // rounded), in the orientation whose rows a warp writes whole (128 bytes per
 // store instruction): dE (rows i, K = v; 4 x 8 KB), dW (rows i, K = a),
-// s dA^qk (rows i, K = j; 2 x 8 KB); then s dA^qk as exact fp32 rows
-// [64][64] for the direct-exponent path (its column sums telescope in
-// dlog_alpha, which magnifies any rounding of it).  G2 transposes in shared
+// s dA^qk (rows i, K = j; 2 x 8 KB) or, for items on the direct-exponent
+// path, s dA^qk as exact fp32 rows [64][64] instead (its column sums
+// telescope in dlog_alpha, which magnifies any rounding of it).  G2 transposes in shared
 // memory what it needs the other way round.
 constexpr uint32_t IM_DE = 0, IM_DW = 32768, IM_AQ = 65536, IM_AQX = 81920;
 static_assert(IM_AQX + 16384 == kGradImgBytes, "image block");
@@ -165,10 +165,11 @@ static_assert(IM_AQX + 16384 == kGradImgBytes, "image block");
 // ---------------------------------------------------------------------------
 // G1: the products with S and dS
 // ---------------------------------------------------------------------------
-// Shared arena, in 16 KB units u0..u11 (regions reused once their readers
+// Shared arena, in 16 KB units u0..u12 (regions reused once their readers
 // are done):
 //   step 0: the g tile u0-1, k tile u3, v and dO tiles u4-5 (read into
-//           registers), A^kk / A^qk f16 u2, dS^T u8-11 (bulk)
+//           registers), A^kk / A^qk f16 u2, dS^T u8-11 (bulk); the q tile
+//           u12 (read by the epilogue)
 //   step 1: dO^T (rows v, K = i) u0-1 | A^kk, A^qk f16 u2 | A^qk^T-rows tf32
 //           (rows j, K = i) u3 | K_end (rows j, K = a) u4-5 | [B1 | B2] f16
 //           MN-major u6-7 | dS^T (rows v, K = a) u8-11
@@ -179,9 +180,9 @@ static_assert(IM_AQX + 16384 == kGradImgBytes, "image block");
 // TMEM columns: U / E 0..127, W 128..255, dE^T 256..319 -> [dQ_hat^T | -dW^T]
 // 256..383, dA^qk^T 384..447, dK_end^T 448..511.
 struct G1Smem {
-    uint8_t ar[12 * U16];
+    uint8_t ar[13 * U16];
     float beta[GC];
-    float gcarry[GD], glast[GD];
+    float gcarry[GD], glast[GD], gmid[GD];
     float sterm[2][GD];   // sum over a value half of dS[a][v] S[a][v]
     float kterm[2][GD];   // sum over a token half of K_end dK_end
     float tail[GD];       // sum of the second token half's dG (for dlog_alpha)
@@ -190,7 +191,8 @@ struct G1Smem {
 };
 constexpr uint32_t G1_DOT = 0, G1_AQ = 2 * U16, G1_AQT = 3 * U16, G1_KE = 4 * U16,
                    G1_BB = 6 * U16, G1_DST = 8 * U16;
-constexpr uint32_t G1_TG = 0, G1_TK = 3 * U16, G1_TV = 4 * U16, G1_TD = 5 * U16;
+constexpr uint32_t G1_TG = 0, G1_TK = 3 * U16, G1_TV = 4 * U16, G1_TD = 5 * U16,
+                   G1_TQ = 12 * U16;
 constexpr uint32_t G1_NW = 2 * U16, G1_SF = 6 * U16, G1_ODE = 8 * U16;
 constexpr uint32_t G1_DSN = 0, G1_E = 4 * U16;
 __device__ __forceinline__ uint32_t g1_s_panel(int p) { return (uint32_t)(p < 2 ? p : p + 2) * U16; }
@@ -221,11 +223,13 @@ chunk_grad_g1_kernel(const __grid_constant__ GradMaps maps, const ChunkGradArgs 
         mbar_init(&sm.bar_dsn, 1);
         for (int m = 0; m < 4; ++m) mbar_init(&sm.bar_m[m], 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(&sm.bar_in, (has_do ? 3u : 2u) * 16384u + 32768u);
+        mbar_arrive_expect_tx(&sm.bar_in, (has_do ? 4u : 3u) * 16384u + 32768u);
         tma_load_3d(ar + G1_TG, &maps.g, 0, h, t0, &sm.bar_in);
         tma_load_3d(ar + G1_TK, &maps.k, 0, h, t0, &sm.bar_in);
         tma_load_3d(ar + G1_TV, &maps.v, 0, h, t0, &sm.bar_in);
         if (has_do) tma_load_3d(ar + G1_TD, &maps.d, 0, h, t0, &sm.bar_in);
+        // q, read only by the epilogue (a region nothing else uses)
+        tma_load_3d(ar + G1_TQ, &maps.q, 0, h, t0, &sm.bar_in);
         mbar_arrive_expect_tx(&sm.bar_ld, kBwdAuxBytes + 4 * U16);
         bulk_g2s(ar + G1_AQ, a.aux + item * kBwdAuxBytes, kBwdAuxBytes, &sm.bar_ld);
         // dS^T: four 128-row panels (K = 32 key channels each), which the
@@ -260,9 +264,20 @@ chunk_grad_g1_kernel(const __grid_constant__ GradMaps maps, const ChunkGradArgs 
 #pragma unroll
         for (int ii = 0; ii < 32; ++ii) in.G[ii] += cy;
         sm.glast[ch] = in.G[31];
+        sm.gmid[ch] = in.G[0];
     }
     __syncthreads();
     const float Gl = sm.glast[ch];
+    // the second kernel's choice of path, made the same way here: only the
+    // dA^qk image that path reads is written
+    bool direct;
+    {
+        const float Gm = sm.gmid[ch];
+        float span = 0.f;
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) span = fmaxf(span, fabsf(in.G[ii] - Gm));
+        direct = __syncthreads_or(!(span <= kGradSpan2));
+    }
     const uint32_t tmem = sm.tmem;
 
     // ---- step 1 operands: [B1 | B2] (f16, token rows), K_end, dO^T ----
@@ -458,14 +473,14 @@ chunk_grad_g1_kernel(const __grid_constant__ GradMaps maps, const ChunkGradArgs 
                          idesc_tf32_f32(128, 64), false);
         mma_commit(&sm.bar_m[3]);
     }
-    // q for Q_hat while the products run
+    // q for Q_hat (its tile) while the products run
     {
-        const unsigned short *q16 = static_cast<const unsigned short *>(a.q);
+        const unsigned short *qt = reinterpret_cast<const unsigned short *>(ar + G1_TQ);
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
             const int ia = i0 + 2 * jj, ib = ia + 1;
-            in.xp[jj] = (ia < L ? q16[base + (size_t)ia * rs] : 0u) |
-                        ((ib < L ? (uint32_t)q16[base + (size_t)ib * rs] : 0u) << 16);
+            in.xp[jj] = (ia < L ? (uint32_t)qt[ia * GD + ch] : 0u) |
+                        ((ib < L ? (uint32_t)qt[ib * GD + ch] : 0u) << 16);
         }
     }
     ok = ok && mbar_wait_bounded(&sm.bar_m[3], 0, kGradWait);
@@ -484,8 +499,13 @@ chunk_grad_g1_kernel(const __grid_constant__ GradMaps maps, const ChunkGradArgs 
         for (int ii = 0; ii < 32; ++ii) {
             const int i = i0 + ii;
             x[ii] = (ch <= i && i < L) ? a.scale * x[ii] : 0.f;
-            f32_at(gaq, i, ch & 31) = tf32_operand(x[ii]);
-            gax[i * GC] = x[ii];
+        }
+        if (!direct) {
+#pragma unroll
+            for (int ii = 0; ii < 32; ++ii) f32_at(gaq, i0 + ii, ch & 31) = tf32_operand(x[ii]);
+        } else {
+#pragma unroll
+            for (int ii = 0; ii < 32; ++ii) gax[(i0 + ii) * GC] = x[ii];
         }
     }
     {
