@@ -21,6 +21,7 @@
 //   4. the per-chunk gradient pass on the tensor cores (kda_backward_grad.cu).
 // Every product that carries a gradient is tf32 (fp32 range): f16 operands
 // lose gradients of training size to underflow.
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 
@@ -61,22 +62,24 @@ struct AuxMaps {
     CUtensorMap d;
 };
 
+// Persistent: CTA b takes items b, b + grid, ... in the order the reverse
+// scan consumes them (chunks from the last, heads fastest).  With flags,
+// each item's outputs are published once they are in global memory (thread
+// 0 waits for its bulk stores and releases the item's flag after issuing the
+// next item's loads), so the reverse scan, launched as a programmatic
+// dependent once every CTA of this grid runs, follows item by item.
 __global__ void __launch_bounds__(256, 1)
 chunk_bwd_aux_kernel(const __grid_constant__ AuxMaps maps, const uint8_t *__restrict__ img_base,
                      const int2 *__restrict__ chunk_tok, int32_t has_d_out,
                      uint8_t *__restrict__ mt_img, float *__restrict__ x_tiles,
-                     float *__restrict__ glv, int32_t H, int *status) {
+                     float *__restrict__ glv, int32_t H, int32_t max_chunks,
+                     uint32_t *__restrict__ ready, int *status) {
     extern __shared__ uint8_t smem_raw[];
     AuxSmem &sm = *reinterpret_cast<AuxSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int32_t c = (int32_t)(blockIdx.x / (unsigned)H), h = (int32_t)(blockIdx.x % (unsigned)H);
-    const int2 tok = chunk_tok[c];
-    const int32_t t0 = tok.x, L = tok.y;
-    if (L <= 0) return;
-    const size_t item = (size_t)c * H + h;
-    const uint8_t *img = img_base + item * A_IMG_STRIDE;
-
+    // the reverse scan may start: it waits on items of this running grid
+    pdl_launch_dependents();
     // the dO tile lands in the upper half of the Q'^T staging, which is
     // written only after the tile has been read
     uint8_t *dtile = sm.qt + 16384;
@@ -84,13 +87,6 @@ chunk_bwd_aux_kernel(const __grid_constant__ AuxMaps maps, const uint8_t *__rest
         mbar_init(&sm.bar_in, 1);
         mbar_init(&sm.bar_mma, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(&sm.bar_in,
-                              2 * 16384 + 2 * 8192 + AD * 4 + (has_d_out ? AC * AD * 2 : 0));
-        bulk_g2s(sm.mn, img + A_IMG_MN, 2 * 16384, &sm.bar_in);
-        bulk_g2s(sm.q0, img + A_IMG_Q0, 8192, &sm.bar_in);
-        bulk_g2s(sm.q1, img + A_IMG_Q1, 8192, &sm.bar_in);
-        bulk_g2s(sm.gl, img + A_IMG_GB, AD * 4, &sm.bar_in);
-        if (has_d_out) tma_load_3d(dtile, &maps.d, 0, h, t0, &sm.bar_in);
     }
     if (warp == 0) {
         tmem_alloc(&sm.tmem, 128);
@@ -100,91 +96,136 @@ chunk_bwd_aux_kernel(const __grid_constant__ AuxMaps maps, const uint8_t *__rest
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem;
-    bool ok = mbar_wait_bounded(&sm.bar_in, 0, kAWait);
-    // dO^T (B operand): element (n, i) = dO[t0 + i][h][n], rows i >= L zero.
-    // Thread -> column n = tid % 128, tokens i = tid / 128, +2, ...
-    {
-        const int n = tid & 127;
-        const unsigned short *tile = reinterpret_cast<const unsigned short *>(dtile);
+    const size_t n_items = (size_t)max_chunks * H;
+    size_t published = ~size_t(0);  // thread 0: the item whose flag is still to go up
+    uint32_t phase = 0;
+    bool ok = true;
+    for (size_t k = blockIdx.x; k < n_items; k += gridDim.x) {
+        const int32_t c = max_chunks - 1 - (int32_t)(k / (size_t)H), h = (int32_t)(k % (size_t)H);
+        const int2 tok = chunk_tok[c];
+        const int32_t t0 = tok.x, L = tok.y;
+        if (L <= 0) continue;  // no such chunk: the reverse scan never asks for it
+        const size_t item = (size_t)c * H + h;
+        const uint8_t *img = img_base + item * A_IMG_STRIDE;
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&sm.bar_in,
+                                  2 * 16384 + 2 * 8192 + AD * 4 + (has_d_out ? AC * AD * 2 : 0));
+            bulk_g2s(sm.mn, img + A_IMG_MN, 2 * 16384, &sm.bar_in);
+            bulk_g2s(sm.q0, img + A_IMG_Q0, 8192, &sm.bar_in);
+            bulk_g2s(sm.q1, img + A_IMG_Q1, 8192, &sm.bar_in);
+            bulk_g2s(sm.gl, img + A_IMG_GB, AD * 4, &sm.bar_in);
+            if (has_d_out) tma_load_3d(dtile, &maps.d, 0, h, t0, &sm.bar_in);
+            // the previous item's outputs are in global memory: publish it
+            if (ready && published != ~size_t(0)) {
+                bulk_wait_group<0>();
+                __threadfence();
+                fence_proxy_async_global();
+                flag_release(ready + published, 1u);
+                published = ~size_t(0);
+            }
+        }
+        ok = mbar_wait_bounded(&sm.bar_in, phase, kAWait) && ok;
+        // dO^T (B operand): element (n, i) = dO[t0 + i][h][n], rows i >= L zero.
+        // Thread -> column n = tid % 128, tokens i = tid / 128, +2, ...
+        {
+            const int n = tid & 127;
+            const unsigned short *tile = reinterpret_cast<const unsigned short *>(dtile);
 #pragma unroll 8
-        for (int i = tid >> 7; i < AC; i += 2) {
-            const float x =
-                (has_d_out && i < L) ? __uint_as_float((uint32_t)tile[i * AD + n] << 16) : 0.f;
-            *reinterpret_cast<float *>(sm.dt + (i >> 5) * 16384u + sw128_offset_f32(n, i & 31)) = x;
+            for (int i = tid >> 7; i < AC; i += 2) {
+                const float x = (has_d_out && i < L)
+                                    ? __uint_as_float((uint32_t)tile[i * AD + n] << 16)
+                                    : 0.f;
+                *reinterpret_cast<float *>(sm.dt + (i >> 5) * 16384u +
+                                           sw128_offset_f32(n, i & 31)) = x;
+            }
         }
-    }
-    __syncthreads();  // the tile is read: Q'^T may overwrite it
-    if (ok) {
-        if (tid < 128) {
-            // -M'^T row i = column i of -M': (-M')[j][i] at panel i/64, row j
-            const int i = tid;
-            const uint8_t *src = sm.mn + (i >> 6) * 16384u;
+        __syncthreads();  // the tile is read: Q'^T may overwrite it
+        if (ok) {
+            if (tid < 128) {
+                // -M'^T row i = column i of -M': (-M')[j][i] at panel i/64, row j
+                const int i = tid;
+                const uint8_t *src = sm.mn + (i >> 6) * 16384u;
 #pragma unroll 4
-            for (int p = 0; p < 4; ++p) {
+                for (int p = 0; p < 4; ++p) {
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4) {
-                    const int j = p * 32 + c4 * 4;
-                    float4 v;
-                    v.x = f16_at(src, j, i & 63);
-                    v.y = f16_at(src, j + 1, i & 63);
-                    v.z = f16_at(src, j + 2, i & 63);
-                    v.w = f16_at(src, j + 3, i & 63);
-                    *reinterpret_cast<float4 *>(sm.mt + p * 16384u + sw128_chunk(i, c4)) = v;
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const int j = p * 32 + c4 * 4;
+                        float4 v;
+                        v.x = f16_at(src, j, i & 63);
+                        v.y = f16_at(src, j + 1, i & 63);
+                        v.z = f16_at(src, j + 2, i & 63);
+                        v.w = f16_at(src, j + 3, i & 63);
+                        *reinterpret_cast<float4 *>(sm.mt + p * 16384u + sw128_chunk(i, c4)) = v;
+                    }
                 }
-            }
-        } else {
-            // Q'^T row d = column d of Q': Q'[i][d] at the panel of d, row i
-            const int d = tid - 128;
-            const uint8_t *src = d < 64 ? sm.q0 : sm.q1;
+            } else {
+                // Q'^T row d = column d of Q': Q'[i][d] at the panel of d, row i
+                const int d = tid - 128;
+                const uint8_t *src = d < 64 ? sm.q0 : sm.q1;
 #pragma unroll
-            for (int p = 0; p < 2; ++p) {
+                for (int p = 0; p < 2; ++p) {
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4) {
-                    const int i = p * 32 + c4 * 4;
-                    float4 v;
-                    v.x = f16_at(src, i, d & 63);
-                    v.y = f16_at(src, i + 1, d & 63);
-                    v.z = f16_at(src, i + 2, d & 63);
-                    v.w = f16_at(src, i + 3, d & 63);
-                    *reinterpret_cast<float4 *>(sm.qt + p * 16384u + sw128_chunk(d, c4)) = v;
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const int i = p * 32 + c4 * 4;
+                        float4 v;
+                        v.x = f16_at(src, i, d & 63);
+                        v.y = f16_at(src, i + 1, d & 63);
+                        v.z = f16_at(src, i + 2, d & 63);
+                        v.w = f16_at(src, i + 3, d & 63);
+                        *reinterpret_cast<float4 *>(sm.qt + p * 16384u + sw128_chunk(d, c4)) = v;
+                    }
                 }
             }
         }
-    } else if (tid == 0) {
-        atomicExch(status, (int)KDA_ERR_TIMEOUT);
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0 && ok) {
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0 && ok) {
+            tc_fence_after();
+            mma_panels<true>(tmem, smem_u32(sm.qt), 16384, smem_u32(sm.dt), 16384, 8,
+                             idesc_tf32_f32(128, 128), false);
+            mma_commit(&sm.bar_mma);
+            bulk_s2g(mt_img + item * (size_t)(4 * 16384), sm.mt, 4 * 16384);
+            bulk_s2g(glv + item * AD, sm.gl, AD * 4);
+            bulk_commit_group();
+        }
+        if (ok) ok = mbar_wait_bounded(&sm.bar_mma, phase, kAWait);
+        ok = __all_sync(0xffffffffu, ok);
+        phase ^= 1u;
         tc_fence_after();
-        mma_panels<true>(tmem, smem_u32(sm.qt), 16384, smem_u32(sm.dt), 16384, 8,
-                         idesc_tf32_f32(128, 128), false);
-        mma_commit(&sm.bar_mma);
-        bulk_s2g(mt_img + item * (size_t)(4 * 16384), sm.mt, 4 * 16384);
-        bulk_s2g(glv + item * AD, sm.gl, AD * 4);
-        bulk_commit_group();
-    }
-    if (ok) ok = mbar_wait_bounded(&sm.bar_mma, 0, kAWait);
-    ok = __all_sync(0xffffffffu, ok);
-    tc_fence_after();
-    if (ok) {
-        // warp w: TMEM lanes 32 (w % 4).., columns 64 (w / 4)..: X rows, two tiles
-        const int quad = warp & 3, half = warp >> 2, d = quad * 32 + (tid & 31);
-        float v[32];
+        if (ok) {
+            // warp w: TMEM lanes 32 (w % 4).., columns 64 (w / 4)..: X rows, two tiles
+            const int quad = warp & 3, half = warp >> 2, d = quad * 32 + (tid & 31);
+            float v[32];
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            const int vt = half * 2 + t;
-            tmem_ld32(tmem_addr(tmem, quad * 32, vt * 32), v);
-            float *dst = x_tiles + ((item * 4 + vt) * AD + d) * 32;
+            for (int t = 0; t < 2; ++t) {
+                const int vt = half * 2 + t;
+                tmem_ld32(tmem_addr(tmem, quad * 32, vt * 32), v);
+                float *dst = x_tiles + ((item * 4 + vt) * AD + d) * 32;
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4 *>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4 *>(dst + j) =
+                        make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            }
         }
-    } else if (tid == 0) {
-        atomicExch(status, (int)KDA_ERR_TIMEOUT);
+        // the copies out have read the staging before the next item rewrites it
+        if (tid == 0) {
+            bulk_wait_group_read<0>();
+            published = item;
+        }
+        tc_fence_before();
+        // one verdict per CTA: after a wait that gave up, it stops
+        if (__syncthreads_or(!ok)) break;
     }
-    if (tid == 0) bulk_wait_group_read<0>();
+    if (tid == 0) {
+        if (!ok) atomicExch(status, (int)KDA_ERR_TIMEOUT);
+        bulk_wait_group<0>();
+        if (ok && ready && published != ~size_t(0)) {
+            __threadfence();
+            fence_proxy_async_global();
+            flag_release(ready + published, 1u);
+        }
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 128);
@@ -237,7 +278,8 @@ chunk_rscan_kernel(const uint8_t *__restrict__ mt_img, const float *__restrict__
                    uint8_t *__restrict__ ds_img, uint8_t *__restrict__ ds_nat,
                    float *__restrict__ d_initial,
                    const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_off,
-                   int32_t N, int32_t T, int32_t H, int *status) {
+                   int32_t N, int32_t T, int32_t H, const uint32_t *__restrict__ ready,
+                   int *status) {
     extern __shared__ uint8_t smem_raw[];
     RScanSmem &sm = *reinterpret_cast<RScanSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -310,6 +352,15 @@ chunk_rscan_kernel(const uint8_t *__restrict__ mt_img, const float *__restrict__
                         }
                     }
                     const size_t item = item_of(n);
+                    // with flags: the item's inputs are published by the running
+                    // producer kernel
+                    if (ready) {
+                        if (!flag_wait_bounded(ready + item, kRWait)) {
+                            sm.abort_flag = 1;
+                            break;
+                        }
+                        fence_proxy_async_global();
+                    }
                     mbar_arrive_expect_tx(&sm.full[stg], MT_BYTES + XT_BYTES + GL_BYTES);
                     bulk_g2s(sm.mt[stg], mt_img + item * MT_BYTES, MT_BYTES, &sm.full[stg]);
                     bulk_g2s(sm.xs[stg], x_tiles + (item * RNT + vt) * (size_t)(RD * RBV),
@@ -461,13 +512,16 @@ chunk_rscan_kernel(const uint8_t *__restrict__ mt_img, const float *__restrict__
             *reinterpret_cast<float4 *>(d_initial + st_off + j) =
                 make_float4(dS[j], dS[j + 1], dS[j + 2], dS[j + 3]);
     }
+    // launched beside its producer: this grid completes only after it, so
+    // that later work in the stream sees everything both wrote
+    if (tid == 0) pdl_wait_primaries();
 }
 
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct ChunkBwdLayout {
-    size_t fwd, aux, mt, x, gl, ds_t, ds_n, img, total;
+    size_t fwd, aux, mt, x, gl, ds_t, ds_n, img, ready, total;
 };
 
 ChunkBwdLayout chunk_bwd_layout(int32_t N, int32_t T, int32_t H) {
@@ -487,6 +541,7 @@ ChunkBwdLayout chunk_bwd_layout(int32_t N, int32_t T, int32_t H) {
     L.ds_t = take(items * RNT * (size_t)DS_IMG);
     L.ds_n = take(items * AD * AD * 4);
     L.img = take(items * (size_t)kGradImgBytes);
+    L.ready = take(items * sizeof(uint32_t));
     L.total = off;
     return L;
 }
@@ -538,15 +593,47 @@ cudaError_t launch_chunk_bwd(const BwdArgs &a, int *status, cudaStream_t stream)
     if (a.d_out &&
         !encode_tile_map(&amaps.d, a.d_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H))
         return cudaErrorInvalidValue;
-    chunk_bwd_aux_kernel<<<(unsigned)items, 256, kAuxSmem, stream>>>(
+    // Beside each other when the reverse scan's CTAs fit in half of the SMs:
+    // the persistent aux grid takes the others, publishes every item with a
+    // flag, and the reverse scan (a programmatic dependent, so it starts only
+    // once every aux CTA runs) follows the flags.  Otherwise one after the
+    // other.
+    const size_t rscan_ctas = (size_t)a.N * RNT * (size_t)a.H;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 0;
+    const bool beside = sms > 0 && 2 * rscan_ctas <= (size_t)sms && !sequential_order_forced();
+    const size_t aux_ctas = std::max<size_t>(
+        1, std::min<size_t>(items, beside ? (size_t)sms - rscan_ctas
+                                          : (size_t)std::max(sms, 1)));
+    uint32_t *ready = beside ? reinterpret_cast<uint32_t *>(ws + L.ready) : nullptr;
+    if (ready) {
+        e = cudaMemsetAsync(ready, 0, items * sizeof(uint32_t), stream);
+        if (e != cudaSuccess) return e;
+    }
+    chunk_bwd_aux_kernel<<<(unsigned)aux_ctas, 256, kAuxSmem, stream>>>(
         amaps, view.img, view.chunk_tok, a.d_out != nullptr ? 1 : 0, ws + L.mt,
-        reinterpret_cast<float *>(ws + L.x), reinterpret_cast<float *>(ws + L.gl), a.H, status);
-    // 3. the reverse scan
-    chunk_rscan_kernel<<<dim3((unsigned)(a.N * RNT), (unsigned)a.H), kRThreads, kRSmem, stream>>>(
-        ws + L.mt, reinterpret_cast<const float *>(ws + L.x),
-        reinterpret_cast<const float *>(ws + L.gl), a.d_final_state, ws + L.ds_t, ws + L.ds_n,
-        a.d_initial_state, a.cu_seqlens, view.chunk_off, a.N, a.T, a.H, status);
+        reinterpret_cast<float *>(ws + L.x), reinterpret_cast<float *>(ws + L.gl), a.H,
+        (int32_t)maxc, ready, status);
     e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // 3. the reverse scan
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.N * RNT), (unsigned)a.H);
+    cfg.blockDim = dim3((unsigned)kRThreads);
+    cfg.dynamicSmemBytes = kRSmem;
+    cfg.stream = stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = beside ? 1u : 0u;
+    e = cudaLaunchKernelEx(&cfg, chunk_rscan_kernel, (const uint8_t *)(ws + L.mt),
+                           reinterpret_cast<const float *>(ws + L.x),
+                           reinterpret_cast<const float *>(ws + L.gl), a.d_final_state,
+                           ws + L.ds_t, ws + L.ds_n, a.d_initial_state, a.cu_seqlens,
+                           view.chunk_off, a.N, a.T, a.H, (const uint32_t *)ready, status);
     if (e != cudaSuccess) return e;
     // 4. every chunk's gradients from S_c and dS_{c+1}
     ChunkGradArgs g;

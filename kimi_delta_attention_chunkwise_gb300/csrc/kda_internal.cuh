@@ -188,6 +188,9 @@ cudaError_t launch_recurrent_fwd(const RecurArgs &a, cudaStream_t stream);
 bool encode_tile_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, size_t esize,
                      int32_t T, int32_t H, uint32_t box_x = 128,
                      CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE);
+// KDA_LAUNCH_ORDER=sequential in the environment: every multi-kernel path
+// runs its kernels one after another (kda_chunk_tc.cu).
+bool sequential_order_forced();
 
 // Tensor-core chunk engine (kda_chunk_tc.cu): bf16, D = 128, C = 64.
 size_t chunk_tc_workspace_bytes(int32_t N, int32_t T, int32_t H);
