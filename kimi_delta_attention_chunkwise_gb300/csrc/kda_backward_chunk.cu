@@ -46,7 +46,8 @@ struct AuxSmem {
     uint8_t dt[2 * 16384];   // B: dO^T, 128 rows (d_v) x 64 tokens, 2 panels
     uint8_t mn[2 * 16384];   // -M' f16 panels (bulk copy in)
     uint8_t q0[8192], q1[8192];  // Q' f16 panels (keys 0..63, 64..127)
-    float gl[AD];
+    uint8_t dtile[AC * AD * 2];  // the dO tile, bf16 [64 tokens][128]
+    float gl[2][AD];             // exp(G_last), by item parity (in while the last goes out)
     uint64_t bar_in, bar_mma;
     uint32_t tmem;
 };
@@ -80,9 +81,7 @@ chunk_bwd_aux_kernel(const __grid_constant__ AuxMaps maps, const uint8_t *__rest
     const int tid = threadIdx.x, warp = tid >> 5;
     // the reverse scan may start: it waits on items of this running grid
     pdl_launch_dependents();
-    // the dO tile lands in the upper half of the Q'^T staging, which is
-    // written only after the tile has been read
-    uint8_t *dtile = sm.qt + 16384;
+    uint8_t *dtile = sm.dtile;
     if (tid == 0) {
         mbar_init(&sm.bar_in, 1);
         mbar_init(&sm.bar_mma, 1);
@@ -97,33 +96,34 @@ chunk_bwd_aux_kernel(const __grid_constant__ AuxMaps maps, const uint8_t *__rest
     tc_fence_after();
     const uint32_t tmem = sm.tmem;
     const size_t n_items = (size_t)max_chunks * H;
+    // this CTA's items in order, skipping chunks that do not exist
+    auto chunk_of = [&](size_t k) { return max_chunks - 1 - (int32_t)(k / (size_t)H); };
+    auto next_valid = [&](size_t k) {
+        while (k < n_items && chunk_tok[chunk_of(k)].y <= 0) k += gridDim.x;
+        return k;
+    };
+    // one item's inputs: -M', Q', exp(G_last) (into the parity's slot) and dO
+    auto issue = [&](size_t k, uint32_t par) {
+        const int32_t c = chunk_of(k), h = (int32_t)(k % (size_t)H);
+        const uint8_t *img = img_base + ((size_t)c * H + h) * A_IMG_STRIDE;
+        mbar_arrive_expect_tx(&sm.bar_in,
+                              2 * 16384 + 2 * 8192 + AD * 4 + (has_d_out ? AC * AD * 2 : 0));
+        bulk_g2s(sm.mn, img + A_IMG_MN, 2 * 16384, &sm.bar_in);
+        bulk_g2s(sm.q0, img + A_IMG_Q0, 8192, &sm.bar_in);
+        bulk_g2s(sm.q1, img + A_IMG_Q1, 8192, &sm.bar_in);
+        bulk_g2s(sm.gl[par], img + A_IMG_GB, AD * 4, &sm.bar_in);
+        if (has_d_out) tma_load_3d(dtile, &maps.d, 0, h, chunk_tok[c].x, &sm.bar_in);
+    };
     size_t published = ~size_t(0);  // thread 0: the item whose flag is still to go up
     uint32_t phase = 0;
     bool ok = true;
-    for (size_t k = blockIdx.x; k < n_items; k += gridDim.x) {
-        const int32_t c = max_chunks - 1 - (int32_t)(k / (size_t)H), h = (int32_t)(k % (size_t)H);
-        const int2 tok = chunk_tok[c];
-        const int32_t t0 = tok.x, L = tok.y;
-        if (L <= 0) continue;  // no such chunk: the reverse scan never asks for it
+    size_t k = next_valid(blockIdx.x);
+    if (tid == 0 && k < n_items) issue(k, 0);
+    while (k < n_items) {
+        const int32_t c = chunk_of(k), h = (int32_t)(k % (size_t)H);
+        const int32_t L = chunk_tok[c].y;
         const size_t item = (size_t)c * H + h;
-        const uint8_t *img = img_base + item * A_IMG_STRIDE;
-        if (tid == 0) {
-            mbar_arrive_expect_tx(&sm.bar_in,
-                                  2 * 16384 + 2 * 8192 + AD * 4 + (has_d_out ? AC * AD * 2 : 0));
-            bulk_g2s(sm.mn, img + A_IMG_MN, 2 * 16384, &sm.bar_in);
-            bulk_g2s(sm.q0, img + A_IMG_Q0, 8192, &sm.bar_in);
-            bulk_g2s(sm.q1, img + A_IMG_Q1, 8192, &sm.bar_in);
-            bulk_g2s(sm.gl, img + A_IMG_GB, AD * 4, &sm.bar_in);
-            if (has_d_out) tma_load_3d(dtile, &maps.d, 0, h, t0, &sm.bar_in);
-            // the previous item's outputs are in global memory: publish it
-            if (ready && published != ~size_t(0)) {
-                bulk_wait_group<0>();
-                __threadfence();
-                fence_proxy_async_global();
-                flag_release(ready + published, 1u);
-                published = ~size_t(0);
-            }
-        }
+        const size_t k_next = next_valid(k + gridDim.x);
         ok = mbar_wait_bounded(&sm.bar_in, phase, kAWait) && ok;
         // dO^T (B operand): element (n, i) = dO[t0 + i][h][n], rows i >= L zero.
         // Thread -> column n = tid % 128, tokens i = tid / 128, +2, ...
@@ -139,7 +139,6 @@ chunk_bwd_aux_kernel(const __grid_constant__ AuxMaps maps, const uint8_t *__rest
                                            sw128_offset_f32(n, i & 31)) = x;
             }
         }
-        __syncthreads();  // the tile is read: Q'^T may overwrite it
         if (ok) {
             if (tid < 128) {
                 // -M'^T row i = column i of -M': (-M')[j][i] at panel i/64, row j
@@ -179,14 +178,25 @@ chunk_bwd_aux_kernel(const __grid_constant__ AuxMaps maps, const uint8_t *__rest
         }
         fence_proxy_async();
         tc_fence_before();
-        __syncthreads();
+        __syncthreads();  // -M', Q' and the dO tile are read: the next item's may land
+        if (tid == 0) {
+            if (ok && k_next < n_items) issue(k_next, phase ^ 1u);
+            // the previous item's outputs are in global memory: publish it
+            if (ready && published != ~size_t(0)) {
+                bulk_wait_group<0>();
+                __threadfence();
+                fence_proxy_async_global();
+                flag_release(ready + published, 1u);
+                published = ~size_t(0);
+            }
+        }
         if (tid == 0 && ok) {
             tc_fence_after();
             mma_panels<true>(tmem, smem_u32(sm.qt), 16384, smem_u32(sm.dt), 16384, 8,
                              idesc_tf32_f32(128, 128), false);
             mma_commit(&sm.bar_mma);
             bulk_s2g(mt_img + item * (size_t)(4 * 16384), sm.mt, 4 * 16384);
-            bulk_s2g(glv + item * AD, sm.gl, AD * 4);
+            bulk_s2g(glv + item * AD, sm.gl[phase], AD * 4);
             bulk_commit_group();
         }
         if (ok) ok = mbar_wait_bounded(&sm.bar_mma, phase, kAWait);
@@ -216,9 +226,14 @@ chunk_bwd_aux_kernel(const __grid_constant__ AuxMaps maps, const uint8_t *__rest
         tc_fence_before();
         // one verdict per CTA: after a wait that gave up, it stops
         if (__syncthreads_or(!ok)) break;
+        k = k_next;
     }
     if (tid == 0) {
-        if (!ok) atomicExch(status, (int)KDA_ERR_TIMEOUT);
+        if (!ok) {
+            atomicExch(status, (int)KDA_ERR_TIMEOUT);
+            // inputs requested for an item that will not run land first
+            (void)mbar_wait_bounded(&sm.bar_in, phase, kAWait);
+        }
         bulk_wait_group<0>();
         if (ok && ready && published != ~size_t(0)) {
             __threadfence();
