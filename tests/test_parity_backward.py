@@ -132,6 +132,13 @@ def test_chunk_form_matches_the_oracle(lengths, H):
     _chunk_check(_case(1300 + len(lengths), lengths, H, 128, "bf16", dsf_scale=DSF_SCALE))
 
 
+def test_chunk_form_many_heads_one_after_the_other():
+    """More reverse-scan CTAs (1 sequence x 4 value tiles x 20 heads = 80)
+    than half of the SMs: the X_c kernel runs to completion before the
+    reverse scan starts (no flags), instead of beside it."""
+    _chunk_check(_case(1310, [200], 20, 128, "bf16", dsf_scale=DSF_SCALE))
+
+
 def test_chunk_form_heavy_tailed_final_state_gradient():
     """A final-state gradient of N(0, 1) per element over a 1000-token
     sequence: RMS error bound (see HEAVY_RMS)."""
