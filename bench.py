@@ -1037,8 +1037,9 @@ def run_backward(args, dist, peaks, dev, stream, w, dev_inputs):
                          "flops_per_unit": BWD_FLOPS_PER_UNIT, "peak_source": peaks["source"],
                          "traffic": traffic,
                          "traffic_note": "sum of the DRAM bytes of its kernels' ncu captures",
-                         "note": "eight launches (forward recompute, X_c, reverse scan, two "
-                                 "gradient kernels); per-kernel shares in profiles/"},
+                         "note": "seven kernels and one flag memset per call (forward "
+                                 "recompute: chunk table, prep, scan; X_c beside the reverse "
+                                 "scan; two gradient kernels); per-kernel shares in profiles/"},
             "recurrent_form": {"ms_per_step": ms_rec, "value": T * dist.world / (ms_rec / 1e3),
                                "unit": "tokens/s",
                                "workload": "the same gradients through kda_recurrent_bwd "
