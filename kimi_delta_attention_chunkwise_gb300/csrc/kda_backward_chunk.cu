@@ -12,15 +12,19 @@
 //   1. runs the forward engine without its output pass; its workspace keeps
 //      every chunk's f16 M', Q', exp(G_last) and the f16 state S_c entering
 //      the chunk, and its prep also stores every chunk's A^kk and A^qk;
-//   2. chunk_bwd_aux_kernel: -M'^T as a tf32 operand image and
+//   2. chunk_bwd_aux_kernel: -M'^T as a bf16 operand image and
 //      X_c = Q'^T dO_c (one tcgen05 kind::tf32 product) per (chunk, head);
-//   3. chunk_rscan_kernel: the reverse scan, one kind::tf32 product per chunk
-//      on the chain, writing dS_{c+1} at every boundary (as the transposed
-//      operand tiles it multiplies and as value-contiguous panels) and dS at
-//      every sequence start (the initial-state gradient);
+//   3. chunk_rscan_kernel: the reverse scan, one kind::f16 product on bf16
+//      operands per chunk on the chain, writing dS_{c+1} at every boundary
+//      (as the gradient pass's transposed tf32 operand tiles and as
+//      value-contiguous fp32 panels) and dS at every sequence start (the
+//      initial-state gradient);
 //   4. the per-chunk gradient pass on the tensor cores (kda_backward_grad.cu).
-// Every product that carries a gradient is tf32 (fp32 range): f16 operands
-// lose gradients of training size to underflow.
+// Every product that carries a gradient keeps fp32 range (tf32 or bf16
+// operands): f16 operands lose gradients of training size to underflow.  The
+// reverse scan's state operand is bf16 (its fp32 state stays in registers):
+// the rounding of that one product's operands moves the gradients by far less
+// than the gradient pass's own tf32 roundings.
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
@@ -41,7 +45,7 @@ constexpr uint32_t A_IMG_STRIDE = 74752, A_IMG_MN = 0, A_IMG_Q0 = 49152, A_IMG_Q
 constexpr long long kAWait = 2000000000LL;
 
 struct AuxSmem {
-    uint8_t mt[4 * 16384];   // -M'^T staging (tf32), then the bulk copy out
+    uint8_t mt[2 * 16384];   // -M'^T staging (bf16), then the bulk copy out
     uint8_t qt[2 * 16384];   // A: Q'^T, 128 rows x 64 tokens, 2 panels
     uint8_t dt[2 * 16384];   // B: dO^T, 128 rows (d_v) x 64 tokens, 2 panels
     uint8_t mn[2 * 16384];   // -M' f16 panels (bulk copy in)
@@ -141,20 +145,25 @@ chunk_bwd_aux_kernel(const __grid_constant__ AuxMaps maps, const uint8_t *__rest
         }
         if (ok) {
             if (tid < 128) {
-                // -M'^T row i = column i of -M': (-M')[j][i] at panel i/64, row j
+                // -M'^T row i = column i of -M': (-M')[j][i] at panel i/64, row j;
+                // bf16 (the reverse scan's product is kind::f16 on bf16 operands:
+                // the gradient keeps fp32 range)
                 const int i = tid;
                 const uint8_t *src = sm.mn + (i >> 6) * 16384u;
-#pragma unroll 4
-                for (int p = 0; p < 4; ++p) {
+#pragma unroll 2
+                for (int p = 0; p < 2; ++p) {
 #pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4) {
-                        const int j = p * 32 + c4 * 4;
-                        float4 v;
-                        v.x = f16_at(src, j, i & 63);
-                        v.y = f16_at(src, j + 1, i & 63);
-                        v.z = f16_at(src, j + 2, i & 63);
-                        v.w = f16_at(src, j + 3, i & 63);
-                        *reinterpret_cast<float4 *>(sm.mt + p * 16384u + sw128_chunk(i, c4)) = v;
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        const int j = p * 64 + c8 * 8;
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(
+                                f16_at(src, j + 2 * e, i & 63), f16_at(src, j + 2 * e + 1, i & 63));
+                            w[e] = *reinterpret_cast<const uint32_t *>(&b2);
+                        }
+                        *reinterpret_cast<uint4 *>(sm.mt + p * 16384u + sw128_chunk(i, c8)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
             } else {
@@ -195,7 +204,7 @@ chunk_bwd_aux_kernel(const __grid_constant__ AuxMaps maps, const uint8_t *__rest
             mma_panels<true>(tmem, smem_u32(sm.qt), 16384, smem_u32(sm.dt), 16384, 8,
                              idesc_tf32_f32(128, 128), false);
             mma_commit(&sm.bar_mma);
-            bulk_s2g(mt_img + item * (size_t)(4 * 16384), sm.mt, 4 * 16384);
+            bulk_s2g(mt_img + item * (size_t)(2 * 16384), sm.mt, 2 * 16384);
             bulk_s2g(glv + item * AD, sm.gl[phase], AD * 4);
             bulk_commit_group();
         }
@@ -247,7 +256,8 @@ chunk_bwd_aux_kernel(const __grid_constant__ AuxMaps maps, const uint8_t *__rest
 }
 
 constexpr int RD = 128, RC = 64, RBV = 32, RNT = RD / RBV, RSTAGE = 2;
-constexpr uint32_t MT_BYTES = RD * RD * 4;
+constexpr uint32_t MT_BYTES = RD * RD * 2;   // -M'^T, bf16, 2 K-major panels
+constexpr uint32_t SB_BYTES = RBV * RD * 2;   // dS_{c+1} operand, bf16, 2 K-major panels
 constexpr uint32_t XT_BYTES = RD * RBV * 4;
 constexpr uint32_t DS_IMG = RBV * RD * 4;
 constexpr uint32_t GL_BYTES = RD * 4;
@@ -256,17 +266,15 @@ constexpr uint32_t kRTmemCols = 2 * RBV;  // D2 ping-pong
 constexpr long long kRWait = 2000000000LL;
 
 struct RScanSmem {
-    uint8_t mt[RSTAGE][MT_BYTES];  // 1024-aligned: offsets 0, 64 KB
-    uint8_t sb[2][DS_IMG];         // 128 KB, 144 KB
+    uint8_t mt[RSTAGE][MT_BYTES];  // 1024-aligned: offsets 0, 32 KB
+    uint8_t sb[2][SB_BYTES];       // 64 KB, 72 KB
     float xs[RSTAGE][RD * RBV];
     float gl[RSTAGE][RD];
     uint64_t full[RSTAGE];   // stage loaded (bulk copies -> issuer, compute)
     uint64_t empty[RSTAGE];  // stage consumed: MMA commit + 128 compute threads
     uint64_t ready_s;        // dS operand written (compute -> issuer)
     uint64_t mma_s;          // product complete (commit -> compute)
-    uint64_t ready_w[2];     // dS operand written, for writer 0 / 1
     uint32_t tmem;
-    volatile int32_t copied[2];
     volatile int32_t issued;
     volatile int32_t abort_flag;
 };
@@ -331,10 +339,6 @@ chunk_rscan_kernel(const uint8_t *__restrict__ mt_img, const float *__restrict__
             }
             mbar_init(&sm.ready_s, 128);
             mbar_init(&sm.mma_s, 1);
-            mbar_init(&sm.ready_w[0], 128);
-            mbar_init(&sm.ready_w[1], 128);
-            sm.copied[0] = 0;
-            sm.copied[1] = 0;
             sm.issued = 0;
             sm.abort_flag = 0;
             fence_mbar_init();
@@ -347,7 +351,7 @@ chunk_rscan_kernel(const uint8_t *__restrict__ mt_img, const float *__restrict__
         __syncthreads();
         tc_fence_after();
         const uint32_t tmem = sm.tmem;
-        constexpr uint32_t IDESC = idesc_tf32_f32(128, RBV);  // A and B K-major
+        constexpr uint32_t IDESC = idesc_bf16_f32(128, RBV);  // A and B K-major
         // step n processes chunk c = c_begin + n_chunks - 1 - n
         auto item_of = [&](int32_t n) {
             return (size_t)(c_begin + n_chunks - 1 - n) * H + h;
@@ -399,8 +403,8 @@ chunk_rscan_kernel(const uint8_t *__restrict__ mt_img, const float *__restrict__
                         break;
                     }
                     tc_fence_after();
-                    mma_panels<true>(tmem + (uint32_t)(n & 1) * RBV, smem_u32(sm.mt[stg]), 16384,
-                                     smem_u32(sm.sb[n & 1]), 4096, 16, IDESC, false);
+                    mma_panels<false>(tmem + (uint32_t)(n & 1) * RBV, smem_u32(sm.mt[stg]), 16384,
+                                      smem_u32(sm.sb[n & 1]), 4096, 8, IDESC, false);
                     mma_commit(&sm.mma_s);
                     mma_commit(&sm.empty[stg]);
                     done = n + 1;
@@ -413,30 +417,7 @@ chunk_rscan_kernel(const uint8_t *__restrict__ mt_img, const float *__restrict__
             }
             __syncwarp();
         } else if (warp >= 6) {
-            // -------- writers: dS_{c+1} images out, steps b, b + 2, ... --------
-            const int b = warp - 6;
-            if (lane == 0) {
-                for (int32_t n = b; n < n_chunks; n += 2) {
-                    if (!mbar_wait_bounded(&sm.ready_w[b], (uint32_t)(n >> 1) & 1u, kRWait) ||
-                        sm.abort_flag) {
-                        sm.abort_flag = 1;
-                        break;
-                    }
-                    if (ds_img) {
-                        // as rows 32 vt .. of the item's four 128-row panels
-                        uint8_t *dst = ds_img + item_of(n) * (size_t)(RNT * DS_IMG) +
-                                       (size_t)vt * (DS_IMG / 4);
-                        for (int p = 0; p < 4; ++p)
-                            bulk_s2g(dst + (size_t)p * (RNT * DS_IMG / 4),
-                                     sm.sb[n & 1] + p * (DS_IMG / 4), DS_IMG / 4);
-                        bulk_commit_group();
-                        bulk_wait_group_read<0>();
-                    }
-                    sm.copied[b] = (n >> 1) + 1;
-                }
-                bulk_wait_group_all();
-            }
-            __syncwarp();
+            // (no role: the dS images leave from the compute threads' registers)
         } else {
             // -------- compute: thread = key row k --------
             const int k = tid;
@@ -452,12 +433,26 @@ chunk_rscan_kernel(const uint8_t *__restrict__ mt_img, const float *__restrict__
                     *reinterpret_cast<float4 *>(dst + sw128_chunk(k, j >> 2)) =
                         make_float4(dS[j], dS[j + 1], dS[j + 2], dS[j + 3]);
             };
-            auto put_state = [&](int32_t n) {
-                uint8_t *img = sm.sb[n & 1] + (k >> 5) * 4096u;
+            // ... and as rows 32 vt .. of the item's four 128-row panels of
+            // dS^T (rows v, K = 32 keys each), tf32-rounded: the gradient
+            // pass's operand image
+            auto put_global_t = [&](int32_t n) {
+                if (!ds_img) return;
+                uint8_t *dst = ds_img + item_of(n) * (size_t)(RNT * DS_IMG) +
+                               (size_t)(k >> 5) * (RNT * DS_IMG / 4);
 #pragma unroll
                 for (int j = 0; j < RBV; ++j)
-                    *reinterpret_cast<float *>(img + sw128_offset_f32(j, k & 31)) =
+                    *reinterpret_cast<float *>(dst + sw128_offset_f32(vt * RBV + j, k & 31)) =
                         tf32_operand(dS[j]);
+            };
+            // the product's B operand: dS_{c+1} as bf16 (fp32 range), rows v,
+            // K = keys, two 64-key panels
+            auto put_state = [&](int32_t n) {
+                uint8_t *img = sm.sb[n & 1] + (k >> 6) * 4096u;
+#pragma unroll
+                for (int j = 0; j < RBV; ++j)
+                    *reinterpret_cast<__nv_bfloat16 *>(img + sw128_offset(j, k & 63)) =
+                        __float2bfloat16_rn(dS[j]);
                 fence_proxy_async();
             };
             put_state(0);
@@ -465,8 +460,8 @@ chunk_rscan_kernel(const uint8_t *__restrict__ mt_img, const float *__restrict__
                 if (rbarrier_or(sm.abort_flag != 0)) break;
                 tc_fence_before();
                 mbar_arrive(&sm.ready_s);
-                mbar_arrive(&sm.ready_w[n & 1]);
                 put_global(n);
+                put_global_t(n);
                 const int stg = n % RSTAGE;
                 if (!mbar_wait_bounded(&sm.full[stg], (uint32_t)(n / RSTAGE) & 1u, kRWait))
                     sm.abort_flag = 1;
@@ -486,23 +481,8 @@ chunk_rscan_kernel(const uint8_t *__restrict__ mt_img, const float *__restrict__
 #pragma unroll
                     for (int j = 0; j < RBV; ++j) dS[j] = fmaf(g, dS[j], d2[j] + x[j]);
                 }
-                if (n + 1 < n_chunks) {
-                    // sb[(n + 1) & 1] holds step n - 1's operand: wait for its copy out
-                    if (n >= 1) {
-                        const int wb = (n - 1) & 1;
-                        const int32_t need = ((n - 1) >> 1) + 1;
-                        if (sm.copied[wb] < need) {
-                            const long long t0 = clock64();
-                            while (sm.copied[wb] < need) {
-                                if (clock64() - t0 > kRWait) {
-                                    sm.abort_flag = 1;
-                                    break;
-                                }
-                            }
-                        }
-                    }
-                    put_state(n + 1);
-                }
+                // sb[(n + 1) & 1] held step n - 1's operand, whose product is done
+                if (n + 1 < n_chunks) put_state(n + 1);
             }
         }
         __syncthreads();
