@@ -682,6 +682,11 @@ chunk_grad_g2_kernel(const __grid_constant__ GradMaps maps, const ChunkGradArgs 
 #pragma unroll
     for (int ii = 0; ii < 32; ++ii) span = fmaxf(span, fabsf(in.G[ii] - Gm));
     const bool direct = __syncthreads_or(!(span <= kGradSpan2));
+    // direct exponents factorised about each 16-token block's first token
+    // when every block spans at most 115 (base 2: no factor leaves fp32)
+    const bool blocks =
+        direct && !__syncthreads_or(!(in.G[0] - in.G[15] <= kGradSpan2 &&
+                                      in.G[16] - in.G[31] <= kGradSpan2));
     const uint32_t tmem = sm.tmem;
 
     // ---- step 1 operands: B1, B2 (token rows), A^T-rows ----
@@ -786,14 +791,17 @@ chunk_grad_g2_kernel(const __grid_constant__ GradMaps maps, const ChunkGradArgs 
         row32_tf32(ar + G2_KQ + hf * U16, ch, qt);
         row32_tf32(ar + G2_KQ + (2 + hf) * U16, ch, kt);
     } else {
+        // G, and k and q -- or, with block references, exp(G_r - G_i) k_i and
+        // exp(G_i - G_r) q_i (r = the first token of i's 16-token block)
         float *gs = reinterpret_cast<float *>(ar + G2_GS), *ks = reinterpret_cast<float *>(ar + G2_KS),
               *qs = reinterpret_cast<float *>(ar + G2_QS);
 #pragma unroll
         for (int ii = 0; ii < 32; ++ii) {
             const int i = i0 + ii;
+            const float gr = ii < 16 ? in.G[0] : in.G[16];
             gs[i * GD + ch] = in.G[ii];
-            ks[i * GD + ch] = bfv(in.kp, ii);
-            qs[i * GD + ch] = bfv(in.xp, ii);
+            ks[i * GD + ch] = blocks ? exp2_approx(gr - in.G[ii]) * bfv(in.kp, ii) : bfv(in.kp, ii);
+            qs[i * GD + ch] = blocks ? exp2_approx(in.G[ii] - gr) * bfv(in.xp, ii) : bfv(in.xp, ii);
         }
     }
     fence_proxy_async();
@@ -886,6 +894,99 @@ chunk_grad_g2_kernel(const __grid_constant__ GradMaps maps, const ChunkGradArgs 
         }
         ok = ok && mbar_wait_bounded(&sm.bar_m[3], 0, kGradWait);
         ok = __all_sync(0xffffffffu, ok);
+        tc_fence_after();
+    } else if (blocks) {
+        // Direct evaluation with 16-token block references (decays beyond
+        // e^-80 across half a chunk, within 115 base 2 across each block):
+        //   XR_i = sum_b exp(G_i - G_rb) sum_{j in b, j <= i} dR_ij [exp(G_rb - G_j) k_j]
+        //   YY_j = sum_b exp(G_rb - G_j) sum_{i in b, i >= j}
+        //              (beta_i dR_ij k_i + s dA^qk_ij q_i) exp(G_i - G_rb)
+        // (r_b the first token of block b), so one 2^x per (row, block)
+        // instead of one per (row, column); results straight into the same
+        // TMEM columns as the split's products.
+        const float *gs = reinterpret_cast<const float *>(ar + G2_GS);
+        const float *kek = reinterpret_cast<const float *>(ar + G2_KS);
+        const float *qp = reinterpret_cast<const float *>(ar + G2_QS);
+        const float *drs = reinterpret_cast<const float *>(ar + G2_DRT);
+        const float *das = reinterpret_cast<const float *>(ar + G2_DRQ);
+        auto dr = [&](int i, int j) { return drs[i * GC + j]; };
+        auto da = [&](int i, int j) { return das[i * GC + j]; };
+        // beta_i exp(G_i - G_r) k_i into a dead operand area
+        float *kp = reinterpret_cast<float *>(ar + G2_XS);
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) {
+            const int i = i0 + ii;
+            const float gr = ii < 16 ? in.G[0] : in.G[16];
+            kp[i * GD + ch] = sm.beta[i] * exp2_approx(in.G[ii] - gr) * bfv(in.kp, ii);
+        }
+        __syncthreads();
+        const uint32_t tl = tmem_addr(tmem, quad * 32, 0);
+        // 4 rows (then 4 columns) of this thread's half at a time, inside one
+        // block; dR and s dA^qk are zero outside their triangles, so whole
+        // blocks are summed and rows of 4 columns load as float4
+#pragma unroll 1
+        for (int t4 = 0; t4 < 8; ++t4) {
+            const int ib = i0 + 4 * t4, blk = ib >> 4;
+            float gi[4], r[4] = {0.f, 0.f, 0.f, 0.f}, sq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) gi[e] = gs[(ib + e) * GD + ch];
+            for (int b = 0; b <= blk; ++b) {
+                const float gr = gs[(16 * b) * GD + ch];
+                float rb[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+                for (int j = 16 * b; j < 16 * b + 16; j += 4) {
+                    float w[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) w[c] = kek[(j + c) * GD + ch];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float4 x = *reinterpret_cast<const float4 *>(drs + (ib + e) * GC + j);
+                        const float4 z = *reinterpret_cast<const float4 *>(das + (ib + e) * GC + j);
+                        rb[e] = fmaf(x.x, w[0], fmaf(x.y, w[1], fmaf(x.z, w[2], fmaf(x.w, w[3], rb[e]))));
+                        sb[e] = fmaf(z.x, w[0], fmaf(z.y, w[1], fmaf(z.z, w[2], fmaf(z.w, w[3], sb[e]))));
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float fb = exp2_approx(gi[e] - gr);
+                    r[e] = fmaf(fb, rb[e], r[e]);
+                    sq[e] = fmaf(fb, sb[e], sq[e]);
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                tmem_st1_nowait(tl + 320 + hf * 32 + 4 * t4 + e, r[e]);
+                tmem_st1_nowait(tl + 384 + hf * 32 + 4 * t4 + e, sq[e]);
+            }
+        }
+#pragma unroll 1
+        for (int t4 = 0; t4 < 8; ++t4) {
+            const int jb = i0 + 4 * t4, blk = jb >> 4;
+            float gj[4], y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) gj[e] = gs[(jb + e) * GD + ch];
+            for (int b = blk; b < 4; ++b) {
+                const float gr = gs[(16 * b) * GD + ch];
+                float yb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+                for (int i = 16 * b; i < 16 * b + 16; ++i) {
+                    const float kv = kp[i * GD + ch], qv = qp[i * GD + ch];
+                    const float4 x = *reinterpret_cast<const float4 *>(drs + i * GC + jb);
+                    const float4 z = *reinterpret_cast<const float4 *>(das + i * GC + jb);
+                    yb[0] = fmaf(x.x, kv, fmaf(z.x, qv, yb[0]));
+                    yb[1] = fmaf(x.y, kv, fmaf(z.y, qv, yb[1]));
+                    yb[2] = fmaf(x.z, kv, fmaf(z.z, qv, yb[2]));
+                    yb[3] = fmaf(x.w, kv, fmaf(z.w, qv, yb[3]));
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) y[e] = fmaf(exp2_approx(gr - gj[e]), yb[e], y[e]);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) tmem_st1_nowait(tl + 448 + hf * 32 + 4 * t4 + e, y[e]);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncthreads();
         tc_fence_after();
     } else {
         // Direct evaluation (decays beyond e^-80 across half a chunk): every

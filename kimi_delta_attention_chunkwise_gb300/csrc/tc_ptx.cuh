@@ -424,6 +424,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// registers -> TMEM: one 32-bit column per thread (its lane), no wait (the
+// caller issues tcgen05.wait::st before anything depends on the store).
+__device__ __forceinline__ void tmem_st1_nowait(uint32_t taddr, float v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "f"(v)
+                 : "memory");
+}
 // registers -> TMEM: 8 consecutive 32-bit columns per thread, no wait (the
 // caller issues tcgen05.wait::st before anything depends on the stores).
 __device__ __forceinline__ void tmem_st8_nowait(uint32_t taddr, const uint32_t (&v)[8]) {
