@@ -495,7 +495,8 @@ kdaStatus_t kda_recurrent_bwd(const void *q, const void *k, const void *v,
  * serial part is the forward scan transposed on the same per-chunk factors,
  *     dS_c = Diag(exp(G_last)) dS_{c+1} - M'^T dS_{c+1} + Q'^T dO_c,
  * with M' = K_end^T W and Q' = s Gamma Q - A^qk W as in kda_chunk_fwd; it
- * runs on the tensor cores in tf32 (the gradients keep fp32 range).  With
+ * runs on the tensor cores with bf16 operands and an fp32 state (the
+ * gradients keep fp32 range).  With
  * the state entering every chunk (from the forward engine) and the gradient
  * leaving it, each 64-token chunk's gradients are computed independently, as
  * tensor-core products of the chunk form's factors (tf32 wherever a gradient
@@ -505,7 +506,8 @@ kdaStatus_t kda_recurrent_bwd(const void *q, const void *k, const void *v,
  * Scratch (the forward engine's images and states, the per-chunk factors,
  * the state gradients at every chunk boundary and the first gradient
  * kernel's operand images for the second: about (T / 64 + N + 1) * H *
- * 480 KB) is taken with cudaMallocAsync / cudaFreeAsync on `stream`.
+ * 450 KB) is taken with cudaMallocAsync / cudaFreeAsync on `stream`; use
+ * kda_chunk_bwd_ws to pass caller-owned scratch instead.
  */
 kdaStatus_t kda_chunk_bwd(const void *q, const void *k, const void *v,
                           const float *log_alpha, const float *beta, float scale,
@@ -513,6 +515,27 @@ kdaStatus_t kda_chunk_bwd(const void *q, const void *k, const void *v,
                           const void *d_out, const float *d_final_state, float *dq, float *dk,
                           float *dv, float *dlog_alpha, float *dbeta, float *d_initial_state,
                           const kdaShape_t *shape, cudaStream_t stream);
+
+/*
+ * kda_chunk_bwd_workspace_size -- bytes of device scratch kda_chunk_bwd_ws
+ * needs for `shape` (the shape kda_chunk_bwd accepts).  *bytes is written on
+ * success; unsupported shapes return KDA_ERR_UNSUPPORTED.
+ */
+kdaStatus_t kda_chunk_bwd_workspace_size(const kdaShape_t *shape, size_t *bytes);
+
+/*
+ * kda_chunk_bwd_ws -- kda_chunk_bwd with caller-owned scratch: `workspace` is
+ * a device buffer of at least kda_chunk_bwd_workspace_size() bytes, 256-byte
+ * aligned, not used by anything else until the work on `stream` is done
+ * (KDA_ERR_INVALID_ARG otherwise).  Allocates nothing.
+ */
+kdaStatus_t kda_chunk_bwd_ws(const void *q, const void *k, const void *v,
+                             const float *log_alpha, const float *beta, float scale,
+                             const float *initial_state, const int32_t *cu_seqlens,
+                             const void *d_out, const float *d_final_state, float *dq,
+                             float *dk, float *dv, float *dlog_alpha, float *dbeta,
+                             float *d_initial_state, const kdaShape_t *shape, void *workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *kda_status_string(kdaStatus_t status);

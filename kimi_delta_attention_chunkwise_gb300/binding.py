@@ -131,6 +131,11 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.kda_recurrent_bwd.restype = ctypes.c_int
     lib.kda_chunk_bwd.argtypes = list(lib.kda_recurrent_bwd.argtypes)
     lib.kda_chunk_bwd.restype = ctypes.c_int
+    lib.kda_chunk_bwd_ws.argtypes = (list(lib.kda_recurrent_bwd.argtypes[:-1]) +
+                                     [vp, ctypes.c_size_t, vp])
+    lib.kda_chunk_bwd_ws.restype = ctypes.c_int
+    lib.kda_chunk_bwd_workspace_size.argtypes = [shp, ctypes.POINTER(ctypes.c_size_t)]
+    lib.kda_chunk_bwd_workspace_size.restype = ctypes.c_int
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_device_status.argtypes = [vp]
@@ -257,11 +262,14 @@ def kda_chunk_fwd_workspace_size(shape: kdaShape_t) -> int:
     return int(n.value)
 
 
-def _workspace(nbytes: int, device):
+def _workspace(nbytes: int, device, stream=None):
+    """A cached scratch buffer of at least nbytes (+256 for alignment), one per
+    (device, stream): calls on one stream run in order, so they may share it."""
     torch = _torch()
     if nbytes == 0:
         return None
-    key = (device.index if device.index is not None else torch.cuda.current_device())
+    key = (device.index if device.index is not None else torch.cuda.current_device(),
+           _stream_handle(stream))
     buf = _ws_cache.get(key)
     if buf is None or buf.numel() < nbytes:
         buf = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
@@ -338,7 +346,7 @@ def kda_chunk_fwd(q, k, v, log_alpha, beta, scale: float, initial_state=None,
         _check(lib.kda_chunk_fwd(*args, s), "kda_chunk_fwd")
     else:
         nbytes = kda_chunk_fwd_workspace_size(shape)
-        ws = _workspace(nbytes, q.device)
+        ws = _workspace(nbytes, q.device, stream)
         wp = None
         if ws is not None:
             wp = (ws.data_ptr() + 255) // 256 * 256
@@ -376,7 +384,7 @@ def kda_chunk_fwd_ws_timed(q, k, v, log_alpha, beta, scale: float, initial_state
                                final_state, chunk_size, engine, out_f32,
                                (l2norm_qk, beta_logits, gate))
     nbytes = kda_chunk_fwd_workspace_size(shape)
-    ws = _workspace(nbytes, q.device)
+    ws = _workspace(nbytes, q.device, stream)
     wp = None if ws is None else (ws.data_ptr() + 255) // 256 * 256
     handles = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     n = ctypes.c_int32(0)
@@ -399,7 +407,7 @@ def kda_chunk_fwd_ws_diag(q, k, v, log_alpha, beta, scale: float, initial_state,
     shape, out = _prefill_args(q, k, v, log_alpha, beta, initial_state, cu_seqlens, out,
                                final_state, chunk_size, KDA_ENGINE_TENSOR, out_f32)
     nbytes = kda_chunk_fwd_workspace_size(shape)
-    ws = _workspace(nbytes, q.device)
+    ws = _workspace(nbytes, q.device, stream)
     wp = None if ws is None else (ws.data_ptr() + 255) // 256 * 256
     _check(load().kda_chunk_fwd_ws_diag(
         _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), float(scale),
@@ -437,14 +445,14 @@ def kda_chunk_fwd_host(q, k, v, log_alpha, beta, scale: float, initial_state=Non
     ``scratch``: a uint8 CUDA tensor of at least
     kda_chunk_fwd_host_scratch_size() bytes (plus 256 for alignment), owned
     by the call until its work is done; one per stream for overlapping calls.
-    Without it, a cached per-device buffer serves (calls on one stream)."""
+    Without it, a cached buffer per (device, stream) serves."""
     shape, out = _prefill_args(q, k, v, log_alpha, beta, initial_state, cu_seqlens, out,
                                final_state, chunk_size, engine, out_f32,
                                (l2norm_qk, beta_logits, gate), on_host=True)
     torch = _torch()
     nbytes = kda_chunk_fwd_host_scratch_size(shape)
     if scratch is None:
-        scratch = _workspace(nbytes, torch.device("cuda", torch.cuda.current_device()))
+        scratch = _workspace(nbytes, torch.device("cuda", torch.cuda.current_device()), stream)
     if not scratch.is_cuda or scratch.numel() * scratch.element_size() < nbytes + 255:
         raise ValueError(f"scratch must be a CUDA buffer of at least {nbytes + 256} bytes")
     sp = (scratch.data_ptr() + 255) // 256 * 256
@@ -693,11 +701,17 @@ def kda_chunk_bwd(q, k, v, log_alpha, beta, scale: float, initial_state=None,
     db = torch.empty((T, H), **f32)
     dS0 = torch.empty((N, H, dk_, dv_), **f32) if want_initial else None
     shape = make_shape(N, T, H, dk_, dv_, _dtype_code(q))
-    _check(load().kda_chunk_bwd(
+    # scratch from the binding's per-device cache (no allocation per call)
+    n = ctypes.c_size_t(0)
+    _check(load().kda_chunk_bwd_workspace_size(ctypes.byref(shape), ctypes.byref(n)),
+           "kda_chunk_bwd_workspace_size")
+    ws = _workspace(int(n.value), q.device, stream)
+    wp = None if ws is None else (ws.data_ptr() + 255) // 256 * 256
+    _check(load().kda_chunk_bwd_ws(
         _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), float(scale),
         _ptr(initial_state), _ptr(cu_seqlens), _ptr(d_out), _ptr(d_final_state), _ptr(dq),
-        _ptr(dk), _ptr(dv), _ptr(dlog), _ptr(db), _ptr(dS0), ctypes.byref(shape),
-        _stream_handle(stream)), "kda_chunk_bwd")
+        _ptr(dk), _ptr(dv), _ptr(dlog), _ptr(db), _ptr(dS0), ctypes.byref(shape), wp,
+        int(n.value), _stream_handle(stream)), "kda_chunk_bwd_ws")
     return dq, dk, dv, dlog, db, dS0
 
 

@@ -539,12 +539,14 @@ kdaStatus_t kda_recurrent_bwd(const void *q, const void *k, const void *v,
     return cuda_status(e != cudaSuccess ? e : f);
 }
 
-kdaStatus_t kda_chunk_bwd(const void *q, const void *k, const void *v, const float *log_alpha,
-                          const float *beta, float scale, const float *initial_state,
-                          const int32_t *cu_seqlens, const void *d_out,
-                          const float *d_final_state, float *dq, float *dk, float *dv,
-                          float *dlog_alpha, float *dbeta, float *d_initial_state,
-                          const kdaShape_t *shape, cudaStream_t stream) {
+namespace {
+// Arguments of kda_chunk_bwd / kda_chunk_bwd_ws, checked before anything runs.
+kdaStatus_t plan_chunk_bwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                           const float *beta, float scale, const float *initial_state,
+                           const int32_t *cu_seqlens, const void *d_out,
+                           const float *d_final_state, float *dq, float *dk, float *dv,
+                           float *dlog_alpha, float *dbeta, float *d_initial_state,
+                           const kdaShape_t *shape, BwdArgs &a) {
     kdaStatus_t st = check_shape(shape, false);
     if (st != KDA_SUCCESS) return st;
     if (group_size(shape) != 1 || shape->prologue != 0 || shape->dtype != KDA_DTYPE_BF16 ||
@@ -566,13 +568,27 @@ kdaStatus_t kda_chunk_bwd(const void *q, const void *k, const void *v, const flo
     for (const void *p : states)
         if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
     if (cu_seqlens && !aligned4(cu_seqlens)) return KDA_ERR_INVALID_ARG;
-    BwdArgs a;
     a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.scale = scale;
     a.initial_state = initial_state; a.cu_seqlens = cu_seqlens; a.d_out = d_out;
     a.d_final_state = d_final_state; a.dq = dq; a.dk = dk; a.dv = dv; a.dlog_alpha = dlog_alpha;
     a.dbeta = dbeta; a.d_initial_state = d_initial_state;
     a.N = shape->num_seqs; a.T = shape->total_tokens; a.H = shape->num_heads;
     a.D = shape->d_k; a.dtype = shape->dtype;
+    return KDA_SUCCESS;
+}
+}  // namespace
+
+kdaStatus_t kda_chunk_bwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                          const float *beta, float scale, const float *initial_state,
+                          const int32_t *cu_seqlens, const void *d_out,
+                          const float *d_final_state, float *dq, float *dk, float *dv,
+                          float *dlog_alpha, float *dbeta, float *d_initial_state,
+                          const kdaShape_t *shape, cudaStream_t stream) {
+    BwdArgs a;
+    const kdaStatus_t st = plan_chunk_bwd(q, k, v, log_alpha, beta, scale, initial_state,
+                                          cu_seqlens, d_out, d_final_state, dq, dk, dv,
+                                          dlog_alpha, dbeta, d_initial_state, shape, a);
+    if (st != KDA_SUCCESS) return st;
     int *status = device_status_ptr();
     if (!status) {
         (void)cudaGetLastError();
@@ -588,6 +604,41 @@ kdaStatus_t kda_chunk_bwd(const void *q, const void *k, const void *v, const flo
     const cudaError_t e = launch_chunk_bwd(a, status, stream);
     const cudaError_t f = cudaFreeAsync(ws, stream);
     return cuda_status(e != cudaSuccess ? e : f);
+}
+
+kdaStatus_t kda_chunk_bwd_workspace_size(const kdaShape_t *shape, size_t *bytes) {
+    if (!bytes) return KDA_ERR_INVALID_ARG;
+    kdaStatus_t st = check_shape(shape, false);
+    if (st != KDA_SUCCESS) return st;
+    if (group_size(shape) != 1 || shape->prologue != 0 || shape->dtype != KDA_DTYPE_BF16 ||
+        shape->d_k != 128)
+        return KDA_ERR_UNSUPPORTED;
+    *bytes = chunk_bwd_workspace_bytes(shape->num_seqs, shape->total_tokens, shape->num_heads);
+    return KDA_SUCCESS;
+}
+
+kdaStatus_t kda_chunk_bwd_ws(const void *q, const void *k, const void *v, const float *log_alpha,
+                             const float *beta, float scale, const float *initial_state,
+                             const int32_t *cu_seqlens, const void *d_out,
+                             const float *d_final_state, float *dq, float *dk, float *dv,
+                             float *dlog_alpha, float *dbeta, float *d_initial_state,
+                             const kdaShape_t *shape, void *workspace, size_t workspace_bytes,
+                             cudaStream_t stream) {
+    BwdArgs a;
+    const kdaStatus_t st = plan_chunk_bwd(q, k, v, log_alpha, beta, scale, initial_state,
+                                          cu_seqlens, d_out, d_final_state, dq, dk, dv,
+                                          dlog_alpha, dbeta, d_initial_state, shape, a);
+    if (st != KDA_SUCCESS) return st;
+    if (!workspace || workspace_bytes < chunk_bwd_workspace_bytes(a.N, a.T, a.H) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return KDA_ERR_INVALID_ARG;
+    int *status = device_status_ptr();
+    if (!status) {
+        (void)cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    a.workspace = workspace;
+    return cuda_status(launch_chunk_bwd(a, status, stream));
 }
 
 kdaStatus_t kda_device_status(cudaStream_t stream) {

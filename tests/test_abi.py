@@ -197,6 +197,29 @@ def test_recurrent_bwd_support(lib):
     assert bwd(kda.make_shape(2, 64, 2, 128, 128, kda.KDA_DTYPE_BF16)) == kda.KDA_ERR_INVALID_ARG
 
 
+def test_chunk_backward_workspace_variant_checks_its_scratch(lib):
+    """kda_chunk_bwd_ws: the size query answers for the shapes the chunk form
+    accepts, and missing, short or misaligned scratch is rejected before
+    anything runs."""
+    ok = kda.make_shape(1, 4096, 16, 128, 128, kda.KDA_DTYPE_BF16)
+    n = ctypes.c_size_t(0)
+    assert lib.kda_chunk_bwd_workspace_size(ctypes.byref(ok), ctypes.byref(n)) == kda.KDA_SUCCESS
+    assert n.value > 0
+    f32 = kda.make_shape(1, 4096, 16, 128, 128, kda.KDA_DTYPE_F32)
+    assert lib.kda_chunk_bwd_workspace_size(ctypes.byref(f32), ctypes.byref(n)) == \
+        kda.KDA_ERR_UNSUPPORTED
+    need = ctypes.c_size_t(0)
+    lib.kda_chunk_bwd_workspace_size(ctypes.byref(ok), ctypes.byref(need))
+
+    def bwd_ws(ws, nbytes):
+        return lib.kda_chunk_bwd_ws(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(1.0), None, None,
+                                    None, None, FAKE, FAKE, FAKE, FAKE, FAKE, None,
+                                    ctypes.byref(ok), ws, ctypes.c_size_t(nbytes), None)
+    assert bwd_ws(None, need.value) == kda.KDA_ERR_INVALID_ARG
+    assert bwd_ws(FAKE, need.value - 1) == kda.KDA_ERR_INVALID_ARG
+    assert bwd_ws(FAKE + 16, need.value) == kda.KDA_ERR_INVALID_ARG   # not 256-byte aligned
+
+
 def test_chunk_bwd_support(lib):
     """The chunkwise backward takes bf16, d = 128 only, and checks the
     alignment its tensor maps need before anything runs."""
@@ -213,6 +236,29 @@ def test_chunk_bwd_support(lib):
     ok = kda.make_shape(1, 64, 2, 128, 128, kda.KDA_DTYPE_BF16)
     assert bwd(ok, q=FAKE + 4) == kda.KDA_ERR_INVALID_ARG      # q not 16-byte aligned
     assert bwd(kda.make_shape(2, 64, 2, 128, 128, kda.KDA_DTYPE_BF16)) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_chunk_backward_workspace_variant_checks_its_scratch(lib):
+    """kda_chunk_bwd_ws: the size query answers for the shapes the chunk form
+    accepts, and missing, short or misaligned scratch is rejected before
+    anything runs."""
+    ok = kda.make_shape(1, 4096, 16, 128, 128, kda.KDA_DTYPE_BF16)
+    n = ctypes.c_size_t(0)
+    assert lib.kda_chunk_bwd_workspace_size(ctypes.byref(ok), ctypes.byref(n)) == kda.KDA_SUCCESS
+    assert n.value > 0
+    f32 = kda.make_shape(1, 4096, 16, 128, 128, kda.KDA_DTYPE_F32)
+    assert lib.kda_chunk_bwd_workspace_size(ctypes.byref(f32), ctypes.byref(n)) == \
+        kda.KDA_ERR_UNSUPPORTED
+    need = ctypes.c_size_t(0)
+    lib.kda_chunk_bwd_workspace_size(ctypes.byref(ok), ctypes.byref(need))
+
+    def bwd_ws(ws, nbytes):
+        return lib.kda_chunk_bwd_ws(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(1.0), None, None,
+                                    None, None, FAKE, FAKE, FAKE, FAKE, FAKE, None,
+                                    ctypes.byref(ok), ws, ctypes.c_size_t(nbytes), None)
+    assert bwd_ws(None, need.value) == kda.KDA_ERR_INVALID_ARG
+    assert bwd_ws(FAKE, need.value - 1) == kda.KDA_ERR_INVALID_ARG
+    assert bwd_ws(FAKE + 16, need.value) == kda.KDA_ERR_INVALID_ARG   # not 256-byte aligned
 
 
 def _align256(n):
